@@ -1,0 +1,483 @@
+/*
+ * Plain CPU oracle for the routed MoE SwiGLU expert FFN with rank-r side-LoRA,
+ * forward and backward.  TEST INFRASTRUCTURE ONLY: it is called from tests/,
+ * from the package smoke check and from the benchmark's CPU-baseline leg, never
+ * from the product path.  It shares no code with the CUDA library.
+ *
+ * What it computes (the method of "feat(mega): add fused shared side-LoRA kernels",
+ * DeepGEMM PR #9, Summary: "W1/W3 share A, W2 shares B; B1/B3/A2 remain expert-local",
+ * frozen W1/W2/W3 receive no gradient), per token t and per unmasked slot j with
+ * expert e = ids[t,j] and adapter a = adapter(t):
+ *
+ *   y1 = rb(A1_a x_t)            y3 = rb(A3_a x_t)                       [r]
+ *   g  = W1_e x_t + s B1_{a,e} y1      u = W3_e x_t + s B3_{a,e} y3      [I]
+ *   h  = rb(silu(g) * u)               silu(z) = z / (1 + exp(-z))       [I]
+ *   z2 = rb(A2_{a,e} h)                                                  [r]
+ *   o  = W2_e h + s B2_a z2                                              [H]
+ *   y_t = rb( sum_j w_tj o_j )   (slot order; masked slots contribute nothing)
+ *
+ * rb() rounds to bf16 (round to nearest even) at the points where a BF16
+ * tensor-core implementation forms an operand or an output; it is the identity
+ * when rounding is switched off (the FP64 build used for finite differences).
+ * The backward is the exact reverse-mode derivative of the above with rb treated
+ * as the identity: grad-x, the router-weight gradient dL/dw_tj = <dy_t, o_j>
+ * (the "grad-route" of PR #9, Correctness coverage) and the six adapter gradients
+ * dA1, dA3, dB1, dB3, dA2, dB2 (PR #9, Summary: "a native backward that returns
+ * grad-x, router gradients, and all six adapter gradients without frozen W1/W2/W3
+ * gradients").  Adapter gradients are summed in (token, slot) order.
+ *
+ * The routing plan is a stable counting sort of the live routes by
+ * (adapter, expert, token, slot), each group padded to a multiple of BLOCK_M rows
+ * (pool padding of PR #9, Implementation: "keep true physical expert offsets").
+ *
+ * MXFP4 base weights: E2M1 element codes (1 sign, 2 exponent with bias 1,
+ * 1 mantissa bit) with one UE8M0 scale 2^(b-127) per 32 contiguous elements along
+ * the contraction axis; low nibble = lower index.  Decoded here from the bit fields.
+ *
+ * Build: real = float (default) or double (-DORACLE_DOUBLE).  Compile with
+ * -ffp-contract=off so x86 and Arm hosts give identical results.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#define NTHREADS(d) ((d)->nthreads > 0 ? (d)->nthreads : omp_get_max_threads())
+#else
+#define NTHREADS(d) 1
+#endif
+
+#ifdef ORACLE_DOUBLE
+typedef double real;
+#define REXP exp
+#else
+typedef float real;
+#define REXP expf
+#endif
+
+enum { DT_BF16 = 0, DT_REAL = 1, DT_MXFP4 = 2 };
+
+typedef struct {
+  const void* p;          /* element storage */
+  const uint8_t* scales;  /* MXFP4: one UE8M0 byte per 32 elements; else NULL */
+  int32_t dtype;          /* DT_* */
+  int32_t pad_;
+} otensor;
+
+typedef struct {
+  int64_t T;
+  int32_t H, I, E, k, r, A, block_m;
+  double scale;           /* side-LoRA scale s */
+  int32_t round_bf16;     /* 1: bf16 rounding points on; 0: off */
+  int32_t nthreads;       /* OpenMP threads (0 = runtime default) */
+} odims;
+
+typedef struct {
+  const int32_t* ids;              /* [T,k], -1 = masked route */
+  const int64_t* adapter_offsets;  /* [A+1] tokens of adapter a are [off[a], off[a+1]) */
+  otensor w;                       /* topk weights [T,k] */
+  otensor x;                       /* [T,H] */
+  otensor dy;                      /* [T,H] (backward only) */
+  otensor W1, W3, W2;              /* [E,I,H], [E,I,H], [E,H,I] */
+  otensor A1, A3;                  /* [A,r,H] */
+  otensor B1, B3;                  /* [A,E,I,r] */
+  otensor A2;                      /* [A,E,r,I] */
+  otensor B2;                      /* [A,H,r] */
+} oinputs;
+
+/* ---------------- scalar helpers ---------------- */
+
+static real bf16_bits_to_real(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (real)f;
+}
+
+/* round to the nearest bf16 value (8 significant bits), ties to even */
+static real round_bf16(real v) {
+  if (!(v == v) || v == 0 || isinf((double)v)) return v;
+  int ex;
+  double m = frexp((double)v, &ex);          /* v = m * 2^ex, 0.5 <= |m| < 1 */
+  double q = nearbyint(ldexp(m, 8));         /* 8 significant bits, RNE */
+  return (real)ldexp(q, ex - 8);
+}
+
+/* E2M1 code -> value, from the bit fields */
+static double e2m1_value(int code) {
+  int sign = (code >> 3) & 1, ebits = (code >> 1) & 3, mbit = code & 1;
+  double mag = (ebits == 0) ? 0.5 * mbit : ldexp(1.0 + 0.5 * mbit, ebits - 1);
+  return sign ? -mag : mag;
+}
+
+static double ue8m0_value(uint8_t b) { return b == 255 ? NAN : ldexp(1.0, (int)b - 127); }
+
+static real ld(const otensor* t, int64_t i) {
+  switch (t->dtype) {
+    case DT_BF16: return bf16_bits_to_real(((const uint16_t*)t->p)[i]);
+    case DT_REAL: return ((const real*)t->p)[i];
+    default: {
+      uint8_t byte = ((const uint8_t*)t->p)[i >> 1];
+      int code = (i & 1) ? (byte >> 4) : (byte & 15);
+      return (real)(e2m1_value(code) * ue8m0_value(t->scales[i >> 5]));
+    }
+  }
+}
+
+static void ld_row(const otensor* t, int64_t base, int64_t n, real* dst) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = ld(t, base + i);
+}
+
+static real rb(const odims* d, real v) { return d->round_bf16 ? round_bf16(v) : v; }
+
+static real silu(real z) { return z / ((real)1 + REXP(-z)); }
+static real sigmoid(real z) { return (real)1 / ((real)1 + REXP(-z)); }
+
+static int adapter_of(const oinputs* in, int A, int64_t t) {
+  for (int a = 0; a < A; ++a)
+    if (t >= in->adapter_offsets[a] && t < in->adapter_offsets[a + 1]) return a;
+  return -1;
+}
+
+/* ---------------- routing plan ---------------- */
+
+/* Stable counting sort of live routes by (adapter, expert, token, slot).
+ * Returns the number of invalid ids (>= E or < -1), which are dropped. */
+int oracle_plan(int64_t T, int32_t k, int32_t E, int32_t A, int32_t BM, const int32_t* ids,
+                const int64_t* adapter_offsets, int32_t* counts, int32_t* offsets,
+                int32_t* row_of_route, int32_t* route_of_row, int64_t row_cap) {
+  int64_t G = (int64_t)A * E;
+  int bad = 0;
+  memset(counts, 0, sizeof(int32_t) * G);
+  for (int64_t t = 0; t < T; ++t) {
+    int a = 0;
+    while (a + 1 < A && t >= adapter_offsets[a + 1]) ++a;
+    for (int j = 0; j < k; ++j) {
+      int32_t e = ids[t * k + j];
+      if (e >= E || e < -1) { ++bad; continue; }
+      if (e >= 0) counts[(int64_t)a * E + e]++;
+    }
+  }
+  offsets[0] = 0;
+  for (int64_t g = 0; g < G; ++g)
+    offsets[g + 1] = offsets[g] + (counts[g] + BM - 1) / BM * BM;
+  for (int64_t p = 0; p < row_cap; ++p) route_of_row[p] = -1;
+  int32_t* cursor = (int32_t*)malloc(sizeof(int32_t) * G);
+  for (int64_t g = 0; g < G; ++g) cursor[g] = offsets[g];
+  for (int64_t t = 0; t < T; ++t) {
+    int a = 0;
+    while (a + 1 < A && t >= adapter_offsets[a + 1]) ++a;
+    for (int j = 0; j < k; ++j) {
+      int32_t e = ids[t * k + j];
+      int64_t rt = t * k + j;
+      if (e < 0 || e >= E) { row_of_route[rt] = -1; continue; }
+      int32_t row = cursor[(int64_t)a * E + e]++;
+      row_of_route[rt] = row;
+      if (row < row_cap) route_of_row[row] = (int32_t)rt;
+    }
+  }
+  free(cursor);
+  return bad;
+}
+
+/* ---------------- per-route forward ---------------- */
+
+typedef struct {
+  real *xt, *y1, *y3, *g, *u, *h, *z2, *o, *rowbuf;
+} fwd_scratch;
+
+static void fwd_alloc(const odims* d, fwd_scratch* s) {
+  int64_t H = d->H, I = d->I, r = d->r;
+  int64_t n = H + 2 * r + 3 * I + r + H + (H > I ? H : I);
+  real* p = (real*)malloc(sizeof(real) * n);
+  s->xt = p; p += H;
+  s->y1 = p; p += r;
+  s->y3 = p; p += r;
+  s->g = p; p += I;
+  s->u = p; p += I;
+  s->h = p; p += I;
+  s->z2 = p; p += r;
+  s->o = p; p += H;
+  s->rowbuf = p;
+}
+
+static void fwd_free(fwd_scratch* s) { free(s->xt); }
+
+/* forward of one live route (t, slot with expert e, adapter a); s->xt holds x_t */
+static void route_forward(const odims* d, const oinputs* in, int a, int e, fwd_scratch* s) {
+  const int64_t H = d->H, I = d->I, r = d->r, E = d->E;
+  const real sc = (real)d->scale;
+  real* row = s->rowbuf;
+  for (int64_t q = 0; q < r; ++q) {
+    real acc1 = 0, acc3 = 0;
+    ld_row(&in->A1, ((int64_t)a * r + q) * H, H, row);
+    for (int64_t c = 0; c < H; ++c) acc1 += row[c] * s->xt[c];
+    ld_row(&in->A3, ((int64_t)a * r + q) * H, H, row);
+    for (int64_t c = 0; c < H; ++c) acc3 += row[c] * s->xt[c];
+    s->y1[q] = rb(d, acc1);
+    s->y3[q] = rb(d, acc3);
+  }
+  for (int64_t i = 0; i < I; ++i) {
+    real gb = 0, ub = 0, gl = 0, ul = 0;
+    ld_row(&in->W1, ((int64_t)e * I + i) * H, H, row);
+    for (int64_t c = 0; c < H; ++c) gb += row[c] * s->xt[c];
+    ld_row(&in->W3, ((int64_t)e * I + i) * H, H, row);
+    for (int64_t c = 0; c < H; ++c) ub += row[c] * s->xt[c];
+    int64_t bbase = (((int64_t)a * E + e) * I + i) * r;
+    for (int64_t q = 0; q < r; ++q) gl += ld(&in->B1, bbase + q) * s->y1[q];
+    for (int64_t q = 0; q < r; ++q) ul += ld(&in->B3, bbase + q) * s->y3[q];
+    s->g[i] = gb + sc * gl;
+    s->u[i] = ub + sc * ul;
+    s->h[i] = rb(d, silu(s->g[i]) * s->u[i]);
+  }
+  for (int64_t q = 0; q < r; ++q) {
+    real acc = 0;
+    ld_row(&in->A2, (((int64_t)a * E + e) * r + q) * I, I, row);
+    for (int64_t i = 0; i < I; ++i) acc += row[i] * s->h[i];
+    s->z2[q] = rb(d, acc);
+  }
+  for (int64_t c = 0; c < H; ++c) {
+    real ob = 0, ol = 0;
+    ld_row(&in->W2, ((int64_t)e * H + c) * I, I, row);
+    for (int64_t i = 0; i < I; ++i) ob += row[i] * s->h[i];
+    int64_t b2 = ((int64_t)a * H + c) * r;
+    for (int64_t q = 0; q < r; ++q) ol += ld(&in->B2, b2 + q) * s->z2[q];
+    s->o[c] = ob + sc * ol;
+  }
+}
+
+/* y for the listed tokens: y[n*H + c] for token tokens[n] (or token n if tokens == NULL). */
+int oracle_forward(const odims* d, const oinputs* in, const int64_t* tokens, int64_t ntok, real* y) {
+  const int64_t H = d->H, k = d->k;
+#pragma omp parallel num_threads(NTHREADS(d))
+  {
+    fwd_scratch s;
+    fwd_alloc(d, &s);
+    real* acc = (real*)malloc(sizeof(real) * H);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t n = 0; n < ntok; ++n) {
+      int64_t t = tokens ? tokens[n] : n;
+      int a = adapter_of(in, d->A, t);
+      for (int64_t c = 0; c < H; ++c) acc[c] = 0;
+      ld_row(&in->x, t * H, H, s.xt);
+      for (int64_t j = 0; j < k; ++j) {
+        int32_t e = in->ids[t * k + j];
+        if (e < 0 || e >= d->E) continue;
+        route_forward(d, in, a, e, &s);
+        real wj = ld(&in->w, t * k + j);
+        for (int64_t c = 0; c < H; ++c) acc[c] += wj * s.o[c];
+      }
+      for (int64_t c = 0; c < H; ++c) y[n * H + c] = rb(d, acc[c]);
+    }
+    free(acc);
+    fwd_free(&s);
+  }
+  return 0;
+}
+
+/* ---------------- backward ---------------- */
+
+/* Per-route quantities kept for the adapter-gradient sums. */
+typedef struct {
+  int64_t t;
+  int32_t a, e, live;
+  real wj;
+} route_meta;
+
+int oracle_backward(const odims* d, const oinputs* in, const int64_t* tokens, int64_t ntok, real* dx,
+                    real* dw, real* dA1, real* dA3, real* dB1, real* dB3, real* dA2, real* dB2) {
+  const int64_t H = d->H, I = d->I, r = d->r, E = d->E, k = d->k, A = d->A;
+  const real sc = (real)d->scale;
+  const int64_t nr = ntok * k;
+  /* per-route saved vectors */
+  real* S_dg = (real*)calloc((size_t)nr * I, sizeof(real));
+  real* S_du = (real*)calloc((size_t)nr * I, sizeof(real));
+  real* S_h = (real*)calloc((size_t)nr * I, sizeof(real));
+  real* S_y1 = (real*)calloc((size_t)nr * r, sizeof(real));
+  real* S_y3 = (real*)calloc((size_t)nr * r, sizeof(real));
+  real* S_z2 = (real*)calloc((size_t)nr * r, sizeof(real));
+  real* S_dz2 = (real*)calloc((size_t)nr * r, sizeof(real));
+  real* S_dy1 = (real*)calloc((size_t)nr * r, sizeof(real));
+  real* S_dy3 = (real*)calloc((size_t)nr * r, sizeof(real));
+  route_meta* M = (route_meta*)calloc((size_t)nr, sizeof(route_meta));
+  if (!S_dg || !S_du || !S_h || !S_y1 || !S_y3 || !S_z2 || !S_dz2 || !S_dy1 || !S_dy3 || !M) return -1;
+
+#pragma omp parallel num_threads(NTHREADS(d))
+  {
+    fwd_scratch s;
+    fwd_alloc(d, &s);
+    real* dyt = (real*)malloc(sizeof(real) * H);
+    real* dyB2 = (real*)malloc(sizeof(real) * r);
+    real* dact = (real*)malloc(sizeof(real) * I);
+    real* dxa = (real*)malloc(sizeof(real) * H);
+    real* row = (real*)malloc(sizeof(real) * (H > I ? H : I));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t n = 0; n < ntok; ++n) {
+      int64_t t = tokens ? tokens[n] : n;
+      int a = adapter_of(in, d->A, t);
+      ld_row(&in->x, t * H, H, s.xt);
+      ld_row(&in->dy, t * H, H, dyt);
+      for (int64_t c = 0; c < H; ++c) dxa[c] = 0;
+      for (int64_t j = 0; j < k; ++j) {
+        int64_t ri = n * k + j;
+        int32_t e = in->ids[t * k + j];
+        M[ri].t = t;
+        M[ri].a = a;
+        M[ri].e = e;
+        M[ri].live = (e >= 0 && e < E);
+        if (!M[ri].live) { dw[n * k + j] = 0; continue; }
+        real wj = ld(&in->w, t * k + j);
+        M[ri].wj = wj;
+        route_forward(d, in, a, e, &s);
+        /* router-weight gradient */
+        real dwj = 0;
+        for (int64_t c = 0; c < H; ++c) dwj += dyt[c] * s.o[c];
+        dw[n * k + j] = dwj;
+        /* B2^T dy */
+        for (int64_t q = 0; q < r; ++q) {
+          real acc = 0;
+          for (int64_t c = 0; c < H; ++c) acc += ld(&in->B2, ((int64_t)a * H + c) * r + q) * dyt[c];
+          dyB2[q] = acc;
+        }
+        /* dL/dh = w (W2_e^T dy + s A2_e^T (B2^T dy)) */
+        for (int64_t i = 0; i < I; ++i) dact[i] = 0;
+        for (int64_t c = 0; c < H; ++c) {
+          ld_row(&in->W2, ((int64_t)e * H + c) * I, I, row);
+          for (int64_t i = 0; i < I; ++i) dact[i] += row[i] * dyt[c];
+        }
+        for (int64_t q = 0; q < r; ++q) {
+          ld_row(&in->A2, (((int64_t)a * E + e) * r + q) * I, I, row);
+          for (int64_t i = 0; i < I; ++i) dact[i] += sc * row[i] * dyB2[q];
+        }
+        for (int64_t i = 0; i < I; ++i) dact[i] *= wj;
+        for (int64_t q = 0; q < r; ++q) {
+          S_dz2[ri * r + q] = sc * wj * dyB2[q];
+          S_z2[ri * r + q] = s.z2[q];
+          S_y1[ri * r + q] = s.y1[q];
+          S_y3[ri * r + q] = s.y3[q];
+        }
+        /* SwiGLU backward */
+        for (int64_t i = 0; i < I; ++i) {
+          real gi = s.g[i], sg = sigmoid(gi);
+          S_dg[ri * I + i] = dact[i] * s.u[i] * sg * ((real)1 + gi * ((real)1 - sg));
+          S_du[ri * I + i] = dact[i] * gi * sg;
+          S_h[ri * I + i] = s.h[i];
+        }
+        const real* dg = S_dg + ri * I;
+        const real* du = S_du + ri * I;
+        /* side-path gradients w.r.t. y1, y3 */
+        for (int64_t q = 0; q < r; ++q) {
+          real a1 = 0, a3 = 0;
+          int64_t bb = (((int64_t)a * E + e) * I) * r + q;
+          for (int64_t i = 0; i < I; ++i) {
+            a1 += ld(&in->B1, bb + i * r) * dg[i];
+            a3 += ld(&in->B3, bb + i * r) * du[i];
+          }
+          S_dy1[ri * r + q] = sc * a1;
+          S_dy3[ri * r + q] = sc * a3;
+        }
+        /* grad-x: W1_e^T dg + W3_e^T du + A1^T dy1 + A3^T dy3 */
+        for (int64_t i = 0; i < I; ++i) {
+          ld_row(&in->W1, ((int64_t)e * I + i) * H, H, row);
+          for (int64_t c = 0; c < H; ++c) dxa[c] += row[c] * dg[i];
+          ld_row(&in->W3, ((int64_t)e * I + i) * H, H, row);
+          for (int64_t c = 0; c < H; ++c) dxa[c] += row[c] * du[i];
+        }
+        for (int64_t q = 0; q < r; ++q) {
+          ld_row(&in->A1, ((int64_t)a * r + q) * H, H, row);
+          for (int64_t c = 0; c < H; ++c) dxa[c] += row[c] * S_dy1[ri * r + q];
+          ld_row(&in->A3, ((int64_t)a * r + q) * H, H, row);
+          for (int64_t c = 0; c < H; ++c) dxa[c] += row[c] * S_dy3[ri * r + q];
+        }
+      }
+      for (int64_t c = 0; c < H; ++c) dx[n * H + c] = rb(d, dxa[c]);
+    }
+    free(dyt); free(dyB2); free(dact); free(dxa); free(row);
+    fwd_free(&s);
+  }
+
+  /* adapter gradients: sums over live routes in (token, slot) order.
+   * Routes of each (adapter, expert) group are listed in that order first. */
+  const int64_t G = A * E;
+  int64_t* gstart = (int64_t*)calloc((size_t)G + 1, sizeof(int64_t));
+  int64_t* gorder = (int64_t*)malloc(sizeof(int64_t) * (nr > 0 ? nr : 1));
+  for (int64_t ri = 0; ri < nr; ++ri)
+    if (M[ri].live) gstart[(int64_t)M[ri].a * E + M[ri].e + 1]++;
+  for (int64_t g = 0; g < G; ++g) gstart[g + 1] += gstart[g];
+  {
+    int64_t* cur = (int64_t*)malloc(sizeof(int64_t) * (G > 0 ? G : 1));
+    for (int64_t g = 0; g < G; ++g) cur[g] = gstart[g];
+    for (int64_t ri = 0; ri < nr; ++ri)
+      if (M[ri].live) gorder[cur[(int64_t)M[ri].a * E + M[ri].e]++] = ri;
+    free(cur);
+  }
+#pragma omp parallel for schedule(dynamic, 4) num_threads(NTHREADS(d))
+  for (int64_t gi = 0; gi < G * I; ++gi) {
+    int64_t g = gi / I, i = gi % I;
+    int64_t a = g / E, e = g % E;
+    real* o1 = dB1 + gi * r;
+    real* o3 = dB3 + gi * r;
+    for (int64_t q = 0; q < r; ++q) o1[q] = o3[q] = 0;
+    (void)a; (void)e;
+    for (int64_t n = gstart[g]; n < gstart[g + 1]; ++n) {
+      int64_t ri = gorder[n];
+      real g1 = S_dg[ri * I + i], g3 = S_du[ri * I + i];
+      for (int64_t q = 0; q < r; ++q) {
+        o1[q] += sc * g1 * S_y1[ri * r + q];
+        o3[q] += sc * g3 * S_y3[ri * r + q];
+      }
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 4) num_threads(NTHREADS(d))
+  for (int64_t gq = 0; gq < G * r; ++gq) {
+    int64_t g = gq / r, q = gq % r;
+    int64_t a = g / E, e = g % E;
+    real* o = dA2 + gq * I;
+    for (int64_t i = 0; i < I; ++i) o[i] = 0;
+    (void)a; (void)e;
+    for (int64_t n = gstart[g]; n < gstart[g + 1]; ++n) {
+      int64_t ri = gorder[n];
+      real z = S_dz2[ri * r + q];
+      for (int64_t i = 0; i < I; ++i) o[i] += z * S_h[ri * I + i];
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 4) num_threads(NTHREADS(d))
+  for (int64_t ac = 0; ac < A * H; ++ac) {
+    int64_t a = ac / H, c = ac % H;
+    real* o = dB2 + ac * r;
+    for (int64_t q = 0; q < r; ++q) o[q] = 0;
+    for (int64_t ri = 0; ri < nr; ++ri) {
+      if (!M[ri].live || M[ri].a != a) continue;
+      real dyc = ld(&in->dy, M[ri].t * H + c);
+      for (int64_t q = 0; q < r; ++q) o[q] += sc * M[ri].wj * dyc * S_z2[ri * r + q];
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 1) num_threads(NTHREADS(d))
+  for (int64_t aq = 0; aq < A * r; ++aq) {
+    int64_t a = aq / r, q = aq % r;
+    real* o1 = dA1 + aq * H;
+    real* o3 = dA3 + aq * H;
+    for (int64_t c = 0; c < H; ++c) o1[c] = o3[c] = 0;
+    for (int64_t ri = 0; ri < nr; ++ri) {
+      if (!M[ri].live || M[ri].a != a) continue;
+      real v1 = S_dy1[ri * r + q], v3 = S_dy3[ri * r + q];
+      int64_t xb = M[ri].t * H;
+      for (int64_t c = 0; c < H; ++c) {
+        real xc = ld(&in->x, xb + c);
+        o1[c] += v1 * xc;
+        o3[c] += v3 * xc;
+      }
+    }
+  }
+  free(S_dg); free(S_du); free(S_h); free(S_y1); free(S_y3); free(S_z2); free(S_dz2);
+  free(S_dy1); free(S_dy3); free(M); free(gstart); free(gorder);
+  return 0;
+}
+
+/* decoders exposed for the format pins */
+double oracle_e2m1_value(int code) { return e2m1_value(code); }
+double oracle_ue8m0_value(int b) { return ue8m0_value((uint8_t)b); }
+double oracle_round_bf16(double v) { return (double)round_bf16((real)v); }
+int oracle_real_bytes(void) { return (int)sizeof(real); }

@@ -1,0 +1,183 @@
+/*
+ * moe_lora.h -- C ABI of the GB300 (sm_103a) routed MoE SwiGLU expert FFN with
+ * rank-r side-LoRA adapters, forward and backward, BF16 with FP32 accumulation.
+ *
+ * The operation ("feat(mega): add fused shared side-LoRA kernels", DeepGEMM PR #9,
+ * Summary): each token goes to its top-k experts; expert e computes
+ *     gate = x W1_e^T + s (x A1^T) B1_e^T,   up = x W3_e^T + s (x A3^T) B3_e^T,
+ *     h = silu(gate) * up,                    down = h W2_e^T + s (h A2_e^T) B2^T,
+ * and the routing-weighted sum of the k down rows is the output.  A1/A3 [r,H]
+ * and B2 [H,r] are shared by all experts; B1_e/B3_e [I,r] and A2_e [r,I] are
+ * expert-local ("W1/W3 share A, W2 shares B; B1/B3/A2 remain expert-local").
+ * The frozen W1/W2/W3 receive no gradient; the backward returns grad-x, the
+ * router-weight gradient and the six adapter gradients (same PR, Summary).
+ *
+ * Conventions for every entry point
+ *   - All tensors are row-major, contiguous, in DEVICE memory unless stated.
+ *     bf16 tensors are passed as uint16_t* holding bf16 bit patterns.
+ *   - Every device pointer must be 16-byte aligned.
+ *   - The caller owns and allocates every buffer; the library never allocates,
+ *     frees or synchronises the stream.  Inputs are read only.  Outputs are fully
+ *     overwritten (never accumulated into), so buffers may be reused across calls
+ *     (PR #9, Correctness coverage: "reusable output/source buffers").
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work of a
+ *     call is enqueued on it; nothing returns to the host in between.
+ *   - Return value: 0 on success.  A negative code means the call was rejected on
+ *     the host BEFORE any launch (bad shape, NULL or misaligned pointer, short
+ *     workspace, unsupported option), in the spirit of PR #9's fail-fast checks
+ *     ("reject unsupported post-down side-LoRA and undersized scratch before
+ *     launching kernels").  MOE_LORA_ERR_CUDA means a launch failed.  Problems
+ *     only the device can see (an expert id out of range, a pipeline wait that
+ *     timed out) set bits in a sticky device error word read by
+ *     moe_lora_get_error().
+ */
+#ifndef MOE_LORA_H_
+#define MOE_LORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_LORA_API __attribute__((visibility("default")))
+#else
+#define MOE_LORA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---- */
+#define MOE_LORA_OK 0
+#define MOE_LORA_ERR_NULL (-1)        /* a required pointer is NULL */
+#define MOE_LORA_ERR_DIMS (-2)        /* unsupported or inconsistent sizes */
+#define MOE_LORA_ERR_ALIGN (-3)       /* a pointer is not 16-byte aligned */
+#define MOE_LORA_ERR_WORKSPACE (-4)   /* a workspace is smaller than required */
+#define MOE_LORA_ERR_UNSUPPORTED (-5) /* activation / base format not supported */
+#define MOE_LORA_ERR_CUDA (-6)        /* a CUDA call or kernel launch failed */
+#define MOE_LORA_ERR_DEVICE (-7)      /* current device is not an sm_103 GPU */
+
+/* ---- device error word bits (moe_lora_get_error) ---- */
+#define MOE_LORA_DEV_BAD_ID 1         /* an id >= E or < -1 was seen and dropped */
+#define MOE_LORA_DEV_TIMEOUT 2        /* a bounded pipeline wait expired */
+
+/* ---- workspaces ---- */
+#define MOE_LORA_WS_PLAN 0        /* routing plan; written by moe_lora_plan */
+#define MOE_LORA_WS_SAVED 1       /* forward activations kept for the backward */
+#define MOE_LORA_WS_FWD_SCRATCH 2 /* forward temporaries */
+#define MOE_LORA_WS_BWD_SCRATCH 3 /* backward temporaries */
+
+/* Problem sizes.  H and I must be multiples of 256; r a multiple of 8 in [8,128];
+ * 1 <= k <= 32; 1 <= E; A >= 1 adapters; block_m must be 128 (the plan pads
+ * every (adapter, expert) group to a multiple of it); act must be 0 (SwiGLU);
+ * base_fmt must be 0 (bf16 base weights).  T may be 0 (every call is a no-op). */
+typedef struct moe_lora_dims {
+  int64_t T;        /* tokens */
+  int32_t H;        /* hidden size */
+  int32_t I;        /* expert intermediate size */
+  int32_t E;        /* experts */
+  int32_t k;        /* experts per token (top-k) */
+  int32_t r;        /* side-LoRA rank */
+  int32_t A;        /* adapters sharing the layer (1 = one adapter) */
+  int32_t block_m;  /* plan padding unit, 128 */
+  float scale;      /* side-LoRA scale s */
+  int32_t act;      /* 0 = SwiGLU */
+  int32_t base_fmt; /* 0 = bf16 */
+} moe_lora_dims;
+
+/* Frozen base and adapter weights (device, bf16 bits).
+ *   W1, W3 [E,I,H]; W2 [E,H,I];
+ *   A1, A3 [A,r,H] (shared by experts); B1, B3 [A,E,I,r] (expert-local);
+ *   A2 [A,E,r,I] (expert-local); B2 [A,H,r] (shared). */
+typedef struct moe_lora_weights {
+  const uint16_t* W1;
+  const uint16_t* W3;
+  const uint16_t* W2;
+  const uint16_t* A1;
+  const uint16_t* A3;
+  const uint16_t* B1;
+  const uint16_t* B3;
+  const uint16_t* A2;
+  const uint16_t* B2;
+} moe_lora_weights;
+
+/* Adapter gradients (device, fp32), same shapes as the factors they belong to. */
+typedef struct moe_lora_grads {
+  float* dA1;
+  float* dA3;
+  float* dB1;
+  float* dB3;
+  float* dA2;
+  float* dB2;
+} moe_lora_grads;
+
+/* Bytes of workspace `which` (MOE_LORA_WS_*) for these sizes; 0 for bad sizes.
+ * Sizes depend only on dims (the routed row count is bounded on the host by
+ * T*k + A*E*(block_m-1)), so no device value is ever read back. */
+MOE_LORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims* dims, int which);
+
+/* Routing plan ("routing-plan construction", excluded from the pages' timing,
+ * PR #9, Scope).  A stable counting sort of the live routes by
+ * (adapter, expert, token, slot); each group's rows are padded to a multiple of
+ * block_m and padding rows map to no route (PR #9, Implementation: "keep true
+ * physical expert offsets; do not round group starts into neighboring experts").
+ *   topk_ids         [T,k] int32, device.  -1 = masked route (not dispatched).
+ *                    Ids >= E or < -1 are dropped and flagged MOE_LORA_DEV_BAD_ID.
+ *   adapter_offsets  [A+1] int64, HOST.  Tokens of adapter a are
+ *                    [off[a], off[a+1]); off[0] = 0, off[A] = T, non-decreasing,
+ *                    and every off[a] with a < A a multiple of 128 when A > 1.
+ *                    May be NULL when A == 1.
+ *   plan_ws          device buffer of moe_lora_workspace_bytes(.., MOE_LORA_WS_PLAN).
+ * Also clears the device error word. */
+MOE_LORA_API int moe_lora_plan(const moe_lora_dims* dims, const int32_t* topk_ids, const int64_t* adapter_offsets,
+                  void* plan_ws, size_t plan_bytes, void* stream);
+
+/* Forward.  x [T,H] bf16; topk_w [T,k] fp32 routing weights (masked slots are
+ * ignored); y [T,H] bf16 output.  `saved` receives what the backward needs
+ * (opaque; size MOE_LORA_WS_SAVED); `scratch` is temporary (MOE_LORA_WS_FWD_SCRATCH).
+ * Requires a plan built by moe_lora_plan for the same dims. */
+MOE_LORA_API int moe_lora_forward(const moe_lora_dims* dims, const void* plan_ws, const uint16_t* x, const float* topk_w,
+                     const moe_lora_weights* w, uint16_t* y, void* saved, size_t saved_bytes, void* scratch,
+                     size_t scratch_bytes, void* stream);
+
+/* Backward of the forward above, given dy [T,H] bf16.
+ * Outputs: dx [T,H] bf16; dw [T,k] fp32 (0 at masked slots); the six adapter
+ * gradients in fp32.  No gradient is produced for W1/W2/W3.  `saved` must come
+ * from moe_lora_forward with the same plan, inputs and weights. */
+MOE_LORA_API int moe_lora_backward(const moe_lora_dims* dims, const void* plan_ws, const void* saved, const uint16_t* x,
+                      const float* topk_w, const uint16_t* dy, const moe_lora_weights* w, uint16_t* dx, float* dw,
+                      const moe_lora_grads* grads, void* scratch, size_t scratch_bytes, void* stream);
+
+/* Reads the sticky device error word of a plan workspace (MOE_LORA_DEV_* bits,
+ * 0 = none).  Synchronises `stream`.  Returns a negative MOE_LORA_ERR_* code if
+ * the read itself failed. */
+MOE_LORA_API int moe_lora_get_error(const moe_lora_dims* dims, const void* plan_ws, void* stream);
+
+/* Copies a plan to HOST arrays for inspection (tests, debugging); synchronises
+ * `stream`.  counts [A*E], offsets [A*E+1] (offsets[A*E] = P, the padded routed
+ * row count), row_of_route [T*k] (-1 = not dispatched), route_of_row [P]
+ * (t*k+j, or -1 on a padding row; pass cap >= P, or NULL/0 to skip). */
+MOE_LORA_API int moe_lora_plan_readback(const moe_lora_dims* dims, const void* plan_ws, int32_t* counts,
+                                        int32_t* offsets, int32_t* row_of_route, int32_t* route_of_row,
+                                        int64_t route_of_row_cap, void* stream);
+
+/* Static description of a return code. */
+MOE_LORA_API const char* moe_lora_strerror(int code);
+
+/* Engine self-test: C[M,N] (fp32, device) = sum_k A(m,k) B(n,k) on the same
+ * tcgen05/TMA GEMM engine that runs the MoE contractions.  A is [M,K] row-major
+ * (a_mn = 0, K-major) or [K,M] (a_mn = 1, MN-major); B is [N,K] (b_mn = 0) or
+ * [K,N] (b_mn = 1); bf16 bits, 16-byte aligned.  M % 128 == 0, K % 64 == 0, and
+ * N % 256 == 0 or (N <= 256 and N % 16 == 0).  Not part of the MoE method; it
+ * exists to check and time the engine in isolation.  Device-side wait timeouts
+ * are reported through moe_lora_gemm_selftest_error(). */
+MOE_LORA_API int moe_lora_gemm_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn, const uint16_t* B,
+                           int32_t b_mn, float* C, void* stream);
+/* Device error word of the self-test GEMM (MOE_LORA_DEV_* bits); synchronises
+ * the stream and clears the word. */
+MOE_LORA_API int moe_lora_gemm_selftest_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LORA_H_ */

@@ -1,0 +1,228 @@
+"""GB300 (sm_103a) routed MoE SwiGLU expert FFN with rank-r side-LoRA adapters.
+
+Thin Python binding over ``libmoelora.so`` (C ABI, ``include/moe_lora.h``).  The
+functions below carry the C names and only marshal arguments: torch CUDA tensors
+become device pointers, the current torch stream becomes the ``cudaStream_t``.
+Every step of the path runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and importing a function fails loudly if the library is
+missing (build it with ``moe_expert_ffn_top_gb300._build.build()``).
+
+The method ("feat(mega): add fused shared side-LoRA kernels", DeepGEMM PR #9,
+Summary): shared A1/A3/B2 side factors, expert-local B1/B3/A2, frozen W1/W2/W3;
+the backward returns grad-x, router-weight gradients and the six adapter
+gradients.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Dict, Optional, Sequence
+
+import torch
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+MOE_LORA_WS_PLAN, MOE_LORA_WS_SAVED, MOE_LORA_WS_FWD_SCRATCH, MOE_LORA_WS_BWD_SCRATCH = 0, 1, 2, 3
+MOE_LORA_DEV_BAD_ID, MOE_LORA_DEV_TIMEOUT = 1, 2
+
+
+class MoeLoraError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {moe_lora_strerror(code)} (code {code})")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("r", ctypes.c_int32), ("A", ctypes.c_int32), ("block_m", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("act", ctypes.c_int32), ("base_fmt", ctypes.c_int32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")]
+
+
+class Grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dA1", "dA3", "dB1", "dB3", "dA2", "dB2")]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run moe_expert_ffn_top_gb300._build.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        L.moe_lora_workspace_bytes.restype = ctypes.c_size_t
+        L.moe_lora_workspace_bytes.argtypes = [ctypes.POINTER(Dims), ctypes.c_int]
+        L.moe_lora_plan.restype = ctypes.c_int
+        L.moe_lora_plan.argtypes = [ctypes.POINTER(Dims), P, P, P, ctypes.c_size_t, P]
+        L.moe_lora_forward.restype = ctypes.c_int
+        L.moe_lora_forward.argtypes = [ctypes.POINTER(Dims), P, P, P, ctypes.POINTER(Weights), P, P,
+                                       ctypes.c_size_t, P, ctypes.c_size_t, P]
+        L.moe_lora_backward.restype = ctypes.c_int
+        L.moe_lora_backward.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, ctypes.POINTER(Weights), P, P,
+                                        ctypes.POINTER(Grads), P, ctypes.c_size_t, P]
+        L.moe_lora_get_error.restype = ctypes.c_int
+        L.moe_lora_get_error.argtypes = [ctypes.POINTER(Dims), P, P]
+        L.moe_lora_plan_readback.restype = ctypes.c_int
+        L.moe_lora_plan_readback.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, ctypes.c_int64, P]
+        L.moe_lora_strerror.restype = ctypes.c_char_p
+        L.moe_lora_strerror.argtypes = [ctypes.c_int]
+        L.moe_lora_gemm_selftest.restype = ctypes.c_int
+        L.moe_lora_gemm_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32, P,
+                                             ctypes.c_int32, P, P]
+        L.moe_lora_gemm_selftest_error.restype = ctypes.c_int
+        L.moe_lora_gemm_selftest_error.argtypes = [P]
+        _lib = L
+    return _lib
+
+
+def make_dims(T: int, H: int, I: int, E: int, k: int, r: int, A: int = 1, scale: float = 1.0) -> Dims:
+    return Dims(T, H, I, E, k, r, A, 128, float(scale), 0, 0)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise MoeLoraError(rc, what)
+
+
+def moe_lora_strerror(code: int) -> str:
+    return lib().moe_lora_strerror(code).decode()
+
+
+def moe_lora_workspace_bytes(dims: Dims, which: int) -> int:
+    return int(lib().moe_lora_workspace_bytes(ctypes.byref(dims), which))
+
+
+def moe_lora_plan(dims: Dims, topk_ids: torch.Tensor, adapter_offsets: Optional[Sequence[int]],
+                  plan_ws: torch.Tensor, stream=None) -> None:
+    offs = None
+    if adapter_offsets is not None:
+        vals = [int(v) for v in adapter_offsets]
+        offs = (ctypes.c_int64 * len(vals))(*vals)
+    rc = lib().moe_lora_plan(ctypes.byref(dims), _ptr(topk_ids, torch.int32, "topk_ids"),
+                             ctypes.cast(offs, ctypes.c_void_p) if offs is not None else None,
+                             _ptr(plan_ws, None, "plan_ws"), plan_ws.numel() * plan_ws.element_size(),
+                             _stream(stream))
+    _check(rc, "moe_lora_plan")
+
+
+def moe_lora_plan_readback(dims: Dims, plan_ws: torch.Tensor, stream=None) -> Dict[str, torch.Tensor]:
+    """Host copies of the plan: counts, offsets, row_of_route, route_of_row."""
+    G = dims.A * dims.E
+    counts = torch.zeros(G, dtype=torch.int32)
+    offsets = torch.zeros(G + 1, dtype=torch.int32)
+    ror = torch.zeros(max(dims.T * dims.k, 1), dtype=torch.int32)
+    cap = dims.T * dims.k + G * 128
+    rrow = torch.zeros(max(cap, 1), dtype=torch.int32)
+    rc = lib().moe_lora_plan_readback(ctypes.byref(dims), _ptr(plan_ws), counts.data_ptr(), offsets.data_ptr(),
+                                      ror.data_ptr(), rrow.data_ptr(), cap, _stream(stream))
+    _check(rc, "moe_lora_plan_readback")
+    P = int(offsets[-1])
+    return {"counts": counts, "offsets": offsets, "row_of_route": ror[:dims.T * dims.k],
+            "route_of_row": rrow[:P].clone()}
+
+
+def _weights(w: Dict[str, torch.Tensor]) -> Weights:
+    return Weights(*[_ptr(w[n], torch.bfloat16, n) for n in ("W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")])
+
+
+def moe_lora_forward(dims: Dims, plan_ws: torch.Tensor, x: torch.Tensor, topk_w: torch.Tensor,
+                     weights: Dict[str, torch.Tensor], y: torch.Tensor, saved: torch.Tensor,
+                     scratch: torch.Tensor, stream=None) -> None:
+    W = _weights(weights)
+    rc = lib().moe_lora_forward(ctypes.byref(dims), _ptr(plan_ws), _ptr(x, torch.bfloat16, "x"),
+                                _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(W),
+                                _ptr(y, torch.bfloat16, "y"), _ptr(saved), saved.numel() * saved.element_size(),
+                                _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream))
+    _check(rc, "moe_lora_forward")
+
+
+def moe_lora_backward(dims: Dims, plan_ws: torch.Tensor, saved: torch.Tensor, x: torch.Tensor,
+                      topk_w: torch.Tensor, dy: torch.Tensor, weights: Dict[str, torch.Tensor],
+                      dx: torch.Tensor, dw: torch.Tensor, grads: Dict[str, torch.Tensor],
+                      scratch: torch.Tensor, stream=None) -> None:
+    W = _weights(weights)
+    Gr = Grads(*[_ptr(grads[n], torch.float32, n) for n in ("dA1", "dA3", "dB1", "dB3", "dA2", "dB2")])
+    rc = lib().moe_lora_backward(ctypes.byref(dims), _ptr(plan_ws), _ptr(saved), _ptr(x, torch.bfloat16, "x"),
+                                 _ptr(topk_w, torch.float32, "topk_w"), _ptr(dy, torch.bfloat16, "dy"),
+                                 ctypes.byref(W), _ptr(dx, torch.bfloat16, "dx"), _ptr(dw, torch.float32, "dw"),
+                                 ctypes.byref(Gr), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                 _stream(stream))
+    _check(rc, "moe_lora_backward")
+
+
+def moe_lora_get_error(dims: Dims, plan_ws: torch.Tensor, stream=None) -> int:
+    rc = lib().moe_lora_get_error(ctypes.byref(dims), _ptr(plan_ws), _stream(stream))
+    if rc < 0:
+        raise MoeLoraError(rc, "moe_lora_get_error")
+    return rc
+
+
+def moe_lora_gemm_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor, b_mn: bool, C: torch.Tensor,
+                           stream=None) -> None:
+    """C[M,N] = A(m,k) B(n,k) on the GEMM engine; A is [M,K] or, if a_mn, [K,M]; B is [N,K] or [K,N]."""
+    M, N = C.shape
+    K = A.shape[0] if a_mn else A.shape[1]
+    rc = lib().moe_lora_gemm_selftest(M, N, K, _ptr(A, torch.bfloat16, "A"), int(a_mn),
+                                      _ptr(B, torch.bfloat16, "B"), int(b_mn), _ptr(C, torch.float32, "C"),
+                                      _stream(stream))
+    _check(rc, "moe_lora_gemm_selftest")
+
+
+def moe_lora_gemm_selftest_error(stream=None) -> int:
+    return lib().moe_lora_gemm_selftest_error(_stream(stream))
+
+
+# ------------------------------------------------------------------ convenience
+@dataclass
+class Workspaces:
+    """Device buffers for one problem size (allocated by torch, owned by the caller)."""
+    plan: torch.Tensor
+    saved: torch.Tensor
+    fwd: torch.Tensor
+    bwd: torch.Tensor
+
+    @staticmethod
+    def allocate(dims: Dims, device="cuda") -> "Workspaces":
+        def buf(which):
+            n = moe_lora_workspace_bytes(dims, which)
+            if n == 0:
+                raise MoeLoraError(-2, "moe_lora_workspace_bytes")
+            return torch.empty(n, dtype=torch.uint8, device=device)
+        return Workspaces(buf(MOE_LORA_WS_PLAN), buf(MOE_LORA_WS_SAVED), buf(MOE_LORA_WS_FWD_SCRATCH),
+                          buf(MOE_LORA_WS_BWD_SCRATCH))
+
+
+def alloc_grads(dims: Dims, device="cuda") -> Dict[str, torch.Tensor]:
+    A, E, H, I, r = dims.A, dims.E, dims.H, dims.I, dims.r
+    f = dict(dtype=torch.float32, device=device)
+    return {"dA1": torch.empty(A, r, H, **f), "dA3": torch.empty(A, r, H, **f),
+            "dB1": torch.empty(A, E, I, r, **f), "dB3": torch.empty(A, E, I, r, **f),
+            "dA2": torch.empty(A, E, r, I, **f), "dB2": torch.empty(A, H, r, **f)}

@@ -1,0 +1,184 @@
+// Backward pass of the routed MoE side-LoRA FFN ("a native backward that returns
+// grad-x, router gradients, and all six adapter gradients without frozen W1/W2/W3
+// gradients", "feat(mega): add fused shared side-LoRA kernels", Summary).
+// Launch sequence, one stream, no host synchronisation:
+//   B1a dyB2 = dy B2 (per token)      B1b dB2 = s dy^T Z2w
+//   B2  gather dy rows, s*dyB2, s*w*dyB2 (zero padding)
+//   B3  W2^T dgrad + A2 path + SwiGLU backward + router partial dots
+//       dw reduce;  dA2 (K-grouped per expert)
+//   B5  W13^T dgrad + B1/B3 path;  dB1/dB3 (K-grouped per expert)
+//   B6a per-token sum of dY13;  B6 grad-x (A1/A3 path + combine);  dA1/dA3
+#include "gemm_problems.cuh"
+#include "launch.h"
+#include "passes.h"
+#include "tmap.h"
+
+namespace moelora {
+
+int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved, const uint16_t* x,
+                 const float* topk_w, const uint16_t* dy, const moe_lora_weights* w, uint16_t* dx, float* dw,
+                 const moe_lora_grads* gr, void* scratch, int num_sms, cudaStream_t stream) {
+  const PlanView pl = make_plan_view(d, plan_ws);
+  const SavedLayout SL = saved_layout(d);
+  const BwdLayout BL = bwd_layout(d);
+  const char* sv = static_cast<const char*>(saved);
+  char* sc = static_cast<char*>(scratch);
+  const uint16_t* Y13p = (const uint16_t*)(sv + SL.Y13p);
+  const uint16_t* Gs = (const uint16_t*)(sv + SL.G);
+  const uint16_t* Us = (const uint16_t*)(sv + SL.U);
+  const uint16_t* Act = (const uint16_t*)(sv + SL.Act);
+  const uint16_t* Z2w = (const uint16_t*)(sv + SL.Z2w);
+  uint16_t* dyB2 = (uint16_t*)(sc + BL.dyB2);
+  uint16_t* Dp = (uint16_t*)(sc + BL.Dp);
+  uint16_t* dXp = Dp;  // Dp is dead once B3 has run
+  uint16_t* D2p = (uint16_t*)(sc + BL.D2p);
+  uint16_t* dZ2p = (uint16_t*)(sc + BL.dZ2p);
+  uint16_t* dG = (uint16_t*)(sc + BL.dG);
+  uint16_t* dU = (uint16_t*)(sc + BL.dU);
+  float* part = (float*)(sc + BL.part);
+  float* dY13 = (float*)(sc + BL.dY13);
+  uint16_t* dY13w = (uint16_t*)(sc + BL.dY13w);
+
+  const uint64_t T = (uint64_t)d->T, H = d->H, I = d->I, E = d->E, A = d->A, r = d->r;
+  const uint64_t P = (uint64_t)rows_cap(d), G = A * E;
+  const int max_tok_tiles = (int)((T + 127) / 128) + d->A;
+  const int max_row_tiles = (int)(P / 128);
+  cudaError_t ce;
+#define MAP(call)                                 \
+  do {                                            \
+    if ((call) != 0) return MOE_LORA_ERR_CUDA;    \
+  } while (0)
+#define LAUNCH(call)                                            \
+  do {                                                          \
+    if ((ce = (call)) != cudaSuccess) return MOE_LORA_ERR_CUDA; \
+  } while (0)
+
+  // B1a: dyB2 = bf16(dy B2)
+  {
+    ProbDyB2 p;
+    MAP(tmap_2d(&p.mdy, dy, H, T, 64, 128));
+    MAP(tmap_3d(&p.mB2, w->B2, r, H, A, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.dyB2 = dyB2;
+    p.H = d->H;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, max_tok_tiles, num_sms, stream));
+  }
+  // B1b: dB2 = s dy^T Z2w
+  {
+    ProbDB2 p;
+    MAP(tmap_2d(&p.mdy, dy, H, T, 64, 64));
+    MAP(tmap_2d(&p.mZ2w, Z2w, r, T, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.dB2 = gr->dB2;
+    p.H = d->H;
+    p.r = d->r;
+    p.s = d->scale;
+    LAUNCH(launch_gemm(p, d->A * (d->H / 128), num_sms, stream));
+  }
+  // B2: routed dy rows and the scaled shared-expand gradients
+  LAUNCH(launch_gather_bwd(pl, dy, dyB2, topk_w, Dp, D2p, dZ2p, d->H, d->r, d->scale, num_sms, stream));
+  // B3/B4: W2^T dgrad + A2 path + SwiGLU backward + router dots
+  {
+    ProbW2Dgrad p;
+    MAP(tmap_2d(&p.mDp, Dp, H, P, 64, 128));
+    MAP(tmap_2d(&p.mD2p, D2p, r, P, 64, 128));
+    MAP(tmap_3d(&p.mW2, w->W2, I, H, E, 64, 64));
+    MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.topk_w = topk_w;
+    p.G = Gs;
+    p.U = Us;
+    p.Act = Act;
+    p.dG = dG;
+    p.dU = dU;
+    p.part = part;
+    p.H = d->H;
+    p.I = d->I;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream));
+  }
+  LAUNCH(launch_dw(pl, part, d->I / 256, dw, num_sms, stream));
+  // dA2 per (adapter, expert)
+  {
+    ProbDA2 p;
+    MAP(tmap_2d(&p.mdZ2p, dZ2p, r, P, 64, 64));
+    MAP(tmap_2d(&p.mAct, Act, I, P, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.dA2 = gr->dA2;
+    p.I = d->I;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, (int)G * (d->I / 256), num_sms, stream));
+  }
+  // B5: W13^T dgrad + B1/B3 path
+  {
+    ProbW13Dgrad p;
+    MAP(tmap_2d(&p.mdG, dG, I, P, 64, 128));
+    MAP(tmap_2d(&p.mdU, dU, I, P, 64, 128));
+    MAP(tmap_3d(&p.mW1, w->W1, H, I, E, 64, 64));
+    MAP(tmap_3d(&p.mW3, w->W3, H, I, E, 64, 64));
+    MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 64));
+    MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.dXp = dXp;
+    p.dY13 = dY13;
+    p.H = d->H;
+    p.I = d->I;
+    p.r = d->r;
+    p.s = d->scale;
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream));
+  }
+  // dB1 / dB3 per (adapter, expert)
+  {
+    ProbDB13 p;
+    MAP(tmap_2d(&p.mdG, dG, I, P, 64, 64));
+    MAP(tmap_2d(&p.mdU, dU, I, P, 64, 64));
+    MAP(tmap_2d(&p.mY13p, Y13p, 2 * r, P, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.dB1 = gr->dB1;
+    p.dB3 = gr->dB3;
+    p.I = d->I;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, 2 * (int)G * (d->I / 128), num_sms, stream));
+  }
+  // B6a: per-token sum of the shared-shrink gradients
+  LAUNCH(launch_dy13w(pl, dY13, dY13w, 2 * d->r, num_sms, stream));
+  // B6: grad-x
+  {
+    ProbGradX p;
+    MAP(tmap_2d(&p.mdY13w, dY13w, 2 * r, T, 64, 128));
+    MAP(tmap_3d(&p.mA1, w->A1, H, r, A, 64, 64));
+    MAP(tmap_3d(&p.mA3, w->A3, H, r, A, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.dXp = dXp;
+    p.dx = dx;
+    p.H = d->H;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream));
+  }
+  // dA1 / dA3 per adapter
+  {
+    ProbDA13 p;
+    MAP(tmap_2d(&p.mdY13w, dY13w, 2 * r, T, 64, 64));
+    MAP(tmap_2d(&p.mx, x, H, T, 64, 64));
+    p.pl = pl;
+    p.err = pl.err;
+    p.dA1 = gr->dA1;
+    p.dA3 = gr->dA3;
+    p.H = d->H;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, d->A * ((2 * d->r + 127) / 128) * (d->H / 256), num_sms, stream));
+  }
+#undef MAP
+#undef LAUNCH
+  return MOE_LORA_OK;
+}
+
+}  // namespace moelora

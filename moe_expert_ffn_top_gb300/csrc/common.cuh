@@ -1,0 +1,185 @@
+// Shared definitions of the MoE side-LoRA library: size rules, workspace
+// layouts (host), and the device view of a routing plan.
+#pragma once
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_lora.h"
+
+namespace moelora {
+
+constexpr int kBlockM = 128;       // plan padding unit = GEMM M tile
+constexpr int kMaxAdapters = 64;   // adapters sharing one layer
+constexpr int kMaxGroups = 16384;  // adapters x experts
+constexpr int kPlanChunk = 1024;   // routes per plan chunk (one warp each)
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Returns MOE_LORA_OK when the sizes are supported.
+inline int check_dims(const moe_lora_dims* d) {
+  if (!d) return MOE_LORA_ERR_NULL;
+  if (d->act != 0 || d->base_fmt != 0) return MOE_LORA_ERR_UNSUPPORTED;
+  if (d->T < 0 || d->T > (int64_t)1 << 30) return MOE_LORA_ERR_DIMS;
+  if (d->H < 256 || d->H % 256 || d->I < 256 || d->I % 256) return MOE_LORA_ERR_DIMS;
+  if (d->r < 8 || d->r > 128 || d->r % 8) return MOE_LORA_ERR_DIMS;
+  if (d->k < 1 || d->k > 32 || d->E < 1 || d->A < 1 || d->A > kMaxAdapters) return MOE_LORA_ERR_DIMS;
+  if ((int64_t)d->A * d->E > kMaxGroups) return MOE_LORA_ERR_DIMS;
+  if (d->block_m != kBlockM) return MOE_LORA_ERR_DIMS;
+  if (d->T * d->k + (int64_t)d->A * d->E * kBlockM > ((int64_t)1 << 31) - 1) return MOE_LORA_ERR_DIMS;
+  return MOE_LORA_OK;
+}
+
+// Upper bound of the padded routed-row count P = sum_g roundup(c_g, 128).
+inline int64_t rows_cap(const moe_lora_dims* d) {
+  int64_t G = (int64_t)d->A * d->E;
+  int64_t p = d->T * d->k + G * (kBlockM - 1);
+  return (int64_t)align_up((size_t)p, kBlockM);
+}
+
+inline int64_t plan_chunks(const moe_lora_dims* d) {
+  return (d->T * d->k + kPlanChunk - 1) / kPlanChunk;
+}
+
+// ------------------------------------------------------------------ layouts
+struct PlanLayout {
+  size_t err, counts, offsets, row_of_route, route_of_row, tile_group, tok_off, tok_tile, chunk_base, total;
+};
+inline PlanLayout plan_layout(const moe_lora_dims* d) {
+  PlanLayout L;
+  const int64_t G = (int64_t)d->A * d->E, P = rows_cap(d), TK = d->T * d->k;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.err = take(16);
+  L.counts = take(sizeof(int32_t) * G);
+  L.offsets = take(sizeof(int32_t) * (G + 1));
+  L.row_of_route = take(sizeof(int32_t) * (TK > 0 ? TK : 1));
+  L.route_of_row = take(sizeof(int32_t) * P);
+  L.tile_group = take(sizeof(int32_t) * (P / kBlockM + 1));
+  L.tok_off = take(sizeof(int32_t) * (kMaxAdapters + 1));
+  L.tok_tile = take(sizeof(int32_t) * (kMaxAdapters + 1));
+  L.chunk_base = take(sizeof(int32_t) * G * (plan_chunks(d) > 0 ? plan_chunks(d) : 1));
+  L.total = o;
+  return L;
+}
+
+// What the forward keeps for the backward (bf16 unless noted).
+struct SavedLayout {
+  size_t Y13p, G, U, Act, Z2w, total;   // [P,2r], [P,I], [P,I], [P,I], [T,r]
+};
+inline SavedLayout saved_layout(const moe_lora_dims* d) {
+  SavedLayout L;
+  const int64_t P = rows_cap(d), T = d->T > 0 ? d->T : 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.Y13p = take(2 * (size_t)P * 2 * d->r);
+  L.G = take(2 * (size_t)P * d->I);
+  L.U = take(2 * (size_t)P * d->I);
+  L.Act = take(2 * (size_t)P * d->I);
+  L.Z2w = take(2 * (size_t)T * d->r);
+  L.total = o;
+  return L;
+}
+
+struct FwdLayout {
+  size_t Y13, Xp, O, Z2, total;   // [T,2r], [P,H], [P,H], [P,r]  (bf16)
+};
+inline FwdLayout fwd_layout(const moe_lora_dims* d) {
+  FwdLayout L;
+  const int64_t P = rows_cap(d), T = d->T > 0 ? d->T : 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.Y13 = take(2 * (size_t)T * 2 * d->r);
+  L.Xp = take(2 * (size_t)P * d->H);
+  L.O = take(2 * (size_t)P * d->H);
+  L.Z2 = take(2 * (size_t)P * d->r);
+  L.total = o;
+  return L;
+}
+
+struct BwdLayout {
+  // dyB2 [T,r] bf16; Dp [P,H] bf16 (reused for dXp); D2p, dZ2p [P,r] bf16;
+  // dG, dU [P,I] bf16; part [P, I/256] f32; dY13 [P,2r] f32; dY13w [T,2r] bf16
+  size_t dyB2, Dp, D2p, dZ2p, dG, dU, part, dY13, dY13w, total;
+};
+inline BwdLayout bwd_layout(const moe_lora_dims* d) {
+  BwdLayout L;
+  const int64_t P = rows_cap(d), T = d->T > 0 ? d->T : 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.dyB2 = take(2 * (size_t)T * d->r);
+  L.Dp = take(2 * (size_t)P * d->H);
+  L.D2p = take(2 * (size_t)P * d->r);
+  L.dZ2p = take(2 * (size_t)P * d->r);
+  L.dG = take(2 * (size_t)P * d->I);
+  L.dU = take(2 * (size_t)P * d->I);
+  L.part = take(4 * (size_t)P * (d->I / 256));
+  L.dY13 = take(4 * (size_t)P * 2 * d->r);
+  L.dY13w = take(2 * (size_t)T * 2 * d->r);
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ device plan view
+struct PlanView {
+  int* err;                  // sticky device error word
+  const int* counts;         // [G] live routes per (adapter, expert) group
+  const int* offsets;        // [G+1] padded row offsets; offsets[G] = P
+  const int* row_of_route;   // [T*k] padded row of route t*k+j, or -1
+  const int* route_of_row;   // [P] route of a row, or -1 for padding
+  const int* tile_group;     // [P/128] group of each 128-row tile
+  const int* tok_off;        // [A+1] first token of each adapter
+  const int* tok_tile;       // [A+1] first 128-token tile of each adapter
+  int64_t T;
+  int G, E, A, k;
+};
+
+inline PlanView make_plan_view(const moe_lora_dims* d, const void* ws) {
+  const PlanLayout L = plan_layout(d);
+  const char* b = static_cast<const char*>(ws);
+  PlanView v;
+  v.err = (int*)(b + L.err);
+  v.counts = (const int*)(b + L.counts);
+  v.offsets = (const int*)(b + L.offsets);
+  v.row_of_route = (const int*)(b + L.row_of_route);
+  v.route_of_row = (const int*)(b + L.route_of_row);
+  v.tile_group = (const int*)(b + L.tile_group);
+  v.tok_off = (const int*)(b + L.tok_off);
+  v.tok_tile = (const int*)(b + L.tok_tile);
+  v.T = d->T;
+  v.G = d->A * d->E;
+  v.E = d->E;
+  v.A = d->A;
+  v.k = d->k;
+  return v;
+}
+
+// ------------------------------------------------------------------ bf16 helpers
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// 8 bf16 <-> 8 floats through one 16-byte access.
+__device__ __forceinline__ void st_bf16x8(uint16_t* dst, const float* v) {
+  uint4 u;
+  u.x = pack_bf16x2(v[0], v[1]);
+  u.y = pack_bf16x2(v[2], v[3]);
+  u.z = pack_bf16x2(v[4], v[5]);
+  u.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(dst) = u;
+}
+__device__ __forceinline__ void ld_bf16x8(const uint16_t* src, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(src);
+  v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+  v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z);
+  v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void st_f32x4(float* dst, const float* v) {
+  *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+}  // namespace moelora

@@ -1,0 +1,120 @@
+// Forward pass of the routed MoE side-LoRA FFN: tensor maps and the launch
+// sequence, all on one stream with no host synchronisation.
+//   F1 shrink (per token)  ->  F2 gather (routed rows, zero padding)
+//   F3 W13 + B1/B3 expand + SwiGLU  ->  F4 W2 + A2 shrink
+//   F6a per-token Z2 combine  ->  F6 B2 expand + routing-weighted combine
+#include "gemm_problems.cuh"
+#include "launch.h"
+#include "passes.h"
+#include "tmap.h"
+
+namespace moelora {
+
+int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, const float* topk_w,
+                const moe_lora_weights* w, uint16_t* y, void* saved, void* scratch, int num_sms,
+                cudaStream_t stream) {
+  const PlanView pl = make_plan_view(d, plan_ws);
+  const SavedLayout SL = saved_layout(d);
+  const FwdLayout FL = fwd_layout(d);
+  char* sv = static_cast<char*>(saved);
+  char* sc = static_cast<char*>(scratch);
+  uint16_t* Y13p = (uint16_t*)(sv + SL.Y13p);
+  uint16_t* Gs = (uint16_t*)(sv + SL.G);
+  uint16_t* Us = (uint16_t*)(sv + SL.U);
+  uint16_t* Act = (uint16_t*)(sv + SL.Act);
+  uint16_t* Z2w = (uint16_t*)(sv + SL.Z2w);
+  uint16_t* Y13 = (uint16_t*)(sc + FL.Y13);
+  uint16_t* Xp = (uint16_t*)(sc + FL.Xp);
+  uint16_t* O = (uint16_t*)(sc + FL.O);
+  uint16_t* Z2 = (uint16_t*)(sc + FL.Z2);
+
+  const uint64_t T = (uint64_t)d->T, H = d->H, I = d->I, E = d->E, A = d->A, r = d->r;
+  const uint64_t P = (uint64_t)rows_cap(d), G = A * E;
+  const uint32_t r16 = (uint32_t)((r + 15) / 16 * 16);
+  const int max_tok_tiles = (int)((T + 127) / 128) + d->A;
+  const int max_row_tiles = (int)(P / 128);
+  int rc = 0;
+  cudaError_t ce;
+#define MAP(call)               \
+  do {                          \
+    if ((rc = (call)) != 0) return MOE_LORA_ERR_CUDA; \
+  } while (0)
+#define LAUNCH(call)                                  \
+  do {                                                \
+    if ((ce = (call)) != cudaSuccess) return MOE_LORA_ERR_CUDA; \
+  } while (0)
+
+  // F1: Y13 = bf16(s * x [A1; A3]^T), per token
+  {
+    ProbShrink p;
+    MAP(tmap_2d(&p.mx, x, H, T, 64, 128));
+    MAP(tmap_3d(&p.mA1, w->A1, H, r, A, 64, (uint32_t)r));
+    MAP(tmap_3d(&p.mA3, w->A3, H, r, A, 64, (uint32_t)r));
+    p.pl = pl;
+    p.err = pl.err;
+    p.Y13 = Y13;
+    p.H = d->H;
+    p.r = d->r;
+    p.s = d->scale;
+    LAUNCH(launch_gemm(p, max_tok_tiles, num_sms, stream));
+  }
+  // F2: routed rows
+  LAUNCH(launch_gather_fwd(pl, x, Y13, Xp, Y13p, d->H, 2 * d->r, num_sms, stream));
+  // F3: W13 + expert-local expand + SwiGLU
+  {
+    ProbW13 p;
+    MAP(tmap_2d(&p.mXp, Xp, H, P, 64, 128));
+    MAP(tmap_2d(&p.mY13p, Y13p, 2 * r, P, 64, 128));
+    MAP(tmap_3d(&p.mW1, w->W1, H, I, E, 64, 128));
+    MAP(tmap_3d(&p.mW3, w->W3, H, I, E, 64, 128));
+    MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 128));
+    MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 128));
+    p.pl = pl;
+    p.err = pl.err;
+    p.G = Gs;
+    p.U = Us;
+    p.Act = Act;
+    p.H = d->H;
+    p.I = d->I;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream));
+  }
+  // F4/F5: W2 + expert-local A2 shrink
+  {
+    ProbW2 p;
+    MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
+    MAP(tmap_3d(&p.mW2, w->W2, I, H, E, 64, 256));
+    MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, r16));
+    p.pl = pl;
+    p.err = pl.err;
+    p.O = O;
+    p.Z2 = Z2;
+    p.H = d->H;
+    p.I = d->I;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream));
+  }
+  // F6a: per-token weighted sum of the A2 shrink
+  LAUNCH(launch_z2w(pl, Z2, topk_w, Z2w, d->r, num_sms, stream));
+  // F6: shared B2 expand + combine
+  {
+    ProbCombine p;
+    MAP(tmap_2d(&p.mZ2w, Z2w, r, T, 64, 128));
+    MAP(tmap_3d(&p.mB2, w->B2, r, H, A, 64, 256));
+    p.pl = pl;
+    p.err = pl.err;
+    p.O = O;
+    p.topk_w = topk_w;
+    p.y = y;
+    p.H = d->H;
+    p.r = d->r;
+    p.s = d->scale;
+    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream));
+  }
+#undef MAP
+#undef LAUNCH
+  (void)rc;
+  return MOE_LORA_OK;
+}
+
+}  // namespace moelora

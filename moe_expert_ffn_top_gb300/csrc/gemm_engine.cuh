@@ -1,0 +1,209 @@
+// Persistent, warp-specialised BF16 GEMM engine for sm_103a.
+//
+//   warp 0 (one lane)  : TMA producer, fills a kStages-deep ring of (A, B) tiles
+//   warp 1 (one lane)  : tcgen05.mma issuer; also owns the TMEM allocation
+//   warps 2..5         : epilogue, one accumulator row (TMEM lane) per thread
+//
+// Accumulators are 128 x 256 fp32 in tensor memory, double buffered (512
+// columns), so the epilogue of tile i overlaps the main loop of tile i+1.
+// Every output tile is 128 rows (M) by up to 256 columns (N); the K loop runs in
+// steps of 64.  What a tile means -- its rows, which operand tiles each K step
+// loads, and what the epilogue does with the accumulator -- is supplied by a
+// problem type P (see gemm_problems.cuh):
+//
+//   static constexpr bool kAmn, kBmn;      operand majorness (true = MN-major)
+//   int*  err;                              device error word
+//   int      num_tiles() const;             read from device plan data
+//   TileInfo tile(int t) const;
+//   void     prefetch() const;              tensor-map prefetch
+//   void     load(const TileInfo&, int ks, uint8_t* sA, uint8_t* sB, uint64_t* bar) const;
+//   MmaStep  mma_step(const TileInfo&, int ks) const;
+//   void     epilogue(const TileInfo&, int row, uint32_t tmem_lane_addr) const;
+//   void     epilogue_empty(const TileInfo&, int row) const;   (tiles with nk == 0)
+//
+// Operand tiles in shared memory use the 128-byte swizzle written by TMA:
+//   A K-major : 128 rows x 128 B                         (one 16 KB box)
+//   A MN-major: two boxes of 64 K-rows x 64 M, 8 KB apart
+//   B K-major : N rows x 128 B
+//   B MN-major: N/64 boxes of 64 K-rows x 64 N, 8 KB apart
+#pragma once
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moelora {
+
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kAStageBytes = 128 * 128;  // 16 KB
+constexpr int kBStageBytes = 256 * 128;  // 32 KB
+constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+constexpr int kAccCols = 256;
+constexpr int kGemmThreads = 192;
+constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 + 256;
+
+struct TileInfo {
+  int m0;    // first output row
+  int n0;    // first output column
+  int g;     // plan group or adapter index
+  int sub;   // problem-specific tile variant
+  int nk;    // number of 64-wide K steps (0 = empty tile)
+  int k0;    // first K index for K-grouped problems
+  int mend;  // one past the last valid output row
+};
+
+struct MmaStep {
+  int n;      // MMA N (multiple of 16, <= 256)
+  int col;    // TMEM column of D inside the accumulator
+  int b_off;  // byte offset of B inside the B stage
+  int first;  // 1: the step's first MMA overwrites D instead of accumulating
+};
+
+template <class P>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ P p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* err = p.err;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * kAccCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = p.num_tiles();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      p.prefetch();
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      uint32_t issued = 0;  // bit s: stage s has received a load
+      uint32_t last_ph = 0; // bit s: phase parity of stage s's last load
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = p.tile(t);
+        for (int ks = 0; ks < ti.nk; ++ks) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * kStageBytes;
+          p.load(ti, ks, sa, sa + kAStageBytes, &full[s]);
+          issued |= 1u << s;
+          last_ph = (last_ph & ~(1u << s)) | (ph << s);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // No TMA copy may still be landing in shared memory when the CTA exits
+      // (matters only if a wait above gave up): wait, bounded, for each stage's
+      // last load to complete.
+      for (int i = 0; i < kStages; ++i)
+        if (issued & (1u << i)) mbar_wait(&full[i], (last_ph >> i) & 1u, err, 100000000ull);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = p.tile(t);
+        if (ti.nk == 0) continue;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
+        for (int ks = 0; ks < ti.nk; ++ks) {
+          if (!mbar_wait(&full[s], ph, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const MmaStep st = p.mma_step(ti, ks);
+          const uint32_t idesc = idesc_bf16_f32(128, st.n, P::kAmn, P::kBmn);
+          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sb = sa + kAStageBytes + (uint32_t)st.b_off;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = P::kAmn ? sw128_desc(sa + kk * 2048, 8192, 1024) : sw128_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = P::kBmn ? sw128_desc(sb + kk * 2048, 8192, 1024) : sw128_desc(sb + kk * 32, 16, 1024);
+            mma_bf16(d + (uint32_t)st.col, ad, bd, idesc, (st.first && kk == 0) ? 0u : 1u);
+          }
+          mma_commit(&empty[s]);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1u;
+      }
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const TileInfo ti = p.tile(t);
+      if (ti.nk == 0) {
+        p.epilogue_empty(ti, row);
+        continue;
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, err));
+      if (!ok) break;
+      tc_fence_after();
+      p.epilogue(ti, row, tmem_base + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * kAccCols);
+  }
+}
+
+// Host launch: one CTA per SM (or fewer if the problem has fewer tiles).
+template <class P>
+cudaError_t launch_gemm(const P& p, int max_tiles, int num_sms, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (max_tiles <= 0) return cudaSuccess;
+  const int grid = max_tiles < num_sms ? max_tiles : num_sms;
+  gemm_kernel<P><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moelora

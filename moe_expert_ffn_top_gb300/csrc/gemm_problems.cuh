@@ -1,0 +1,901 @@
+// The contractions of the routed MoE side-LoRA FFN, each expressed as a problem
+// type for the GEMM engine (gemm_engine.cuh): which 128-row x N-column tiles exist,
+// which TMA boxes every 64-wide K step loads, and the fused epilogue.
+//
+// Notation (row-major): x [T,H], Xp [P,H] routed rows (zero on padding rows),
+// W1/W3 [E,I,H], W2 [E,H,I], A1/A3 [A,r,H], B1/B3 [A*E,I,r], A2 [A*E,r,I], B2 [A,H,r].
+// A plan group g = a*E + e is (adapter a, expert e); its rows are
+// [offsets[g], offsets[g+1]), a multiple of 128 long.
+//
+// The side-LoRA contract ("feat(mega): add fused shared side-LoRA kernels",
+// DeepGEMM PR #9, Summary): A1/A3 and B2 are shared, so the rank-r shrink
+// x A^T and the expand Z B2^T run once per TOKEN; B1/B3/A2 are expert-local and
+// run per routed row, fused into the expert GEMMs as extra K steps (B1/B3) or an
+// extra N tile (A2).
+#pragma once
+#include "gemm_engine.cuh"
+
+namespace moelora {
+
+__device__ __forceinline__ int adapter_of_tile(const PlanView& pl, int t) {
+  int a = 0;
+  while (a + 1 < pl.A && t >= pl.tok_tile[a + 1]) ++a;
+  return a;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Stores n (multiple of 8, <= 32) bf16 values v[i] * mul.
+__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float (&v)[32], float mul, int n) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 8) {
+    if (j < n) {
+      float t[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) t[i] = v[j + i] * mul;
+      st_bf16x8(dst + j, t);
+    }
+  }
+}
+// Stores n (multiple of 4, <= 32) fp32 values v[i] * mul.
+__device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], float mul, int n) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    if (j < n) {
+      float t[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) t[i] = v[j + i] * mul;
+      st_f32x4(dst + j, t);
+    }
+  }
+}
+
+__device__ __forceinline__ int round16(int r) { return (r + 15) & ~15; }
+
+// =====================================================================================
+// Forward F1 -- shared shrink, once per token:  Y13[t] = bf16(s * x_t [A1_a; A3_a]^T).
+// M = tokens of adapter a, N = 2r (y1 | y3), K = H.  A: x K-major; B: A1/A3 K-major.
+// =====================================================================================
+struct ProbShrink {
+  static constexpr bool kAmn = false, kBmn = false;
+  CUtensorMap mx, mA1, mA3;  // x (H,T) box(64,128); A1/A3 (H,r,A) box(64,r,1)
+  PlanView pl;
+  int* err;
+  uint16_t* Y13;
+  int H, r;
+  float s;
+  __device__ int num_tiles() const { return pl.tok_tile[pl.A]; }
+  __device__ TileInfo tile(int t) const {
+    const int a = adapter_of_tile(pl, t);
+    TileInfo ti;
+    ti.g = a;
+    ti.m0 = pl.tok_off[a] + (t - pl.tok_tile[a]) * 128;
+    ti.mend = pl.tok_off[a + 1];
+    ti.n0 = 0;
+    ti.sub = 0;
+    ti.nk = H / kBK;
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mx);
+    tma_prefetch_map(&mA1);
+    tma_prefetch_map(&mA3);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    mbar_arrive_expect_tx(bar, kAStageBytes + 2 * r * 128);
+    tma_load_2d(sa, &mx, bar, ks * kBK, ti.m0);
+    tma_load_3d(sb, &mA1, bar, ks * kBK, 0, ti.g);
+    tma_load_3d(sb + r * 128, &mA3, bar, ks * kBK, 0, ti.g);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{2 * r, 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t t = (int64_t)ti.m0 + row;
+    const bool ok = t < ti.mend;
+    for (int c = 0; c < 2 * r; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      const int n = 2 * r - c < 32 ? 2 * r - c : 32;
+      if (ok) store_row_bf16(Y13 + t * (2 * r) + c, v, s, n);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Forward F3 -- W13 expert GEMM with the expert-local B1/B3 expand and SwiGLU:
+//   G = Xp W1_e^T + Y1p B1_ae^T,  U = Xp W3_e^T + Y3p B3_ae^T   (s folded into Y13)
+//   Act = bf16(silu(G) * U); G and U are kept (bf16) for the backward.
+// Tile: 128 rows x 128 columns of I; the accumulator holds the gate columns in
+// TMEM [0,128) and the up columns in [128,256).  K steps: H/64 base steps (one
+// N=256 MMA over W1|W3 rows), then ceil(r/64) steps per side for the expand
+// (N=128 into the gate half with Y1p/B1, then into the up half with Y3p/B3).
+// =====================================================================================
+struct ProbW13 {
+  static constexpr bool kAmn = false, kBmn = false;
+  CUtensorMap mXp, mY13p, mW1, mW3, mB1, mB3;  // Xp (H,P) box(64,128); Y13p (2r,P) box(64,128);
+                                               // W1/W3 (H,I,E) box(64,128,1); B1/B3 (r,I,G) box(64,128,1)
+  PlanView pl;
+  int* err;
+  uint16_t *G, *U, *Act;
+  int H, I, r;
+  __device__ int ntn() const { return I / 128; }
+  __device__ int nkr() const { return (r + 63) / 64; }
+  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int mt = t / ntn(), nt = t % ntn();
+    TileInfo ti;
+    ti.m0 = mt * 128;
+    ti.mend = ti.m0 + 128;
+    ti.n0 = nt * 128;
+    ti.g = pl.tile_group[mt];
+    ti.sub = 0;
+    ti.nk = H / kBK + 2 * nkr();
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mXp);
+    tma_prefetch_map(&mY13p);
+    tma_prefetch_map(&mW1);
+    tma_prefetch_map(&mW3);
+    tma_prefetch_map(&mB1);
+    tma_prefetch_map(&mB3);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int nb = H / kBK;
+    const int e = ti.g % pl.E;
+    if (ks < nb) {
+      mbar_arrive_expect_tx(bar, kAStageBytes + 2 * 128 * 128);
+      tma_load_2d(sa, &mXp, bar, ks * kBK, ti.m0);
+      tma_load_3d(sb, &mW1, bar, ks * kBK, ti.n0, e);
+      tma_load_3d(sb + 128 * 128, &mW3, bar, ks * kBK, ti.n0, e);
+    } else {
+      const int j = ks - nb, half = j / nkr(), kb = j % nkr();
+      mbar_arrive_expect_tx(bar, kAStageBytes + 128 * 128);
+      tma_load_2d(sa, &mY13p, bar, half * r + kb * kBK, ti.m0);
+      tma_load_3d(sb, half ? &mB3 : &mB1, bar, kb * kBK, ti.n0, ti.g);
+    }
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const {
+    const int nb = H / kBK;
+    if (ks < nb) return MmaStep{256, 0, 0, ks == 0};
+    const int half = (ks - nb) / nkr();
+    return MmaStep{128, half * 128, 0, 0};
+  }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t p = (int64_t)ti.m0 + row;
+    const int64_t base = p * I + ti.n0;
+    for (int c = 0; c < 128; c += 32) {
+      float g[32], u[32];
+      tmem_ld32(taddr + c, g);
+      tmem_ld32(taddr + 128 + c, u);
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        float a8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a8[i] = silu_f(g[j + i]) * u[j + i];
+        st_bf16x8(G + base + c + j, g + j);
+        st_bf16x8(U + base + c + j, u + j);
+        st_bf16x8(Act + base + c + j, a8);
+      }
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Forward F4/F5 -- W2 expert GEMM with the expert-local A2 shrink:
+//   O = Act W2_e^T  [P,H] (unweighted),   Z2 = bf16(Act A2_ae^T) [P,r]
+// N tiles: H/256 base tiles over W2 rows, then one tile of round16(r) over A2 rows.
+// =====================================================================================
+struct ProbW2 {
+  static constexpr bool kAmn = false, kBmn = false;
+  CUtensorMap mAct, mW2, mA2;  // Act (I,P) box(64,128); W2 (I,H,E) box(64,256,1); A2 (I,r,G) box(64,r16,1)
+  PlanView pl;
+  int* err;
+  uint16_t *O, *Z2;
+  int H, I, r;
+  __device__ int ntn() const { return H / 256 + 1; }
+  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int mt = t / ntn(), nt = t % ntn();
+    TileInfo ti;
+    ti.m0 = mt * 128;
+    ti.mend = ti.m0 + 128;
+    ti.sub = nt == H / 256;
+    ti.n0 = ti.sub ? 0 : nt * 256;
+    ti.g = pl.tile_group[mt];
+    ti.nk = I / kBK;
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mAct);
+    tma_prefetch_map(&mW2);
+    tma_prefetch_map(&mA2);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    if (!ti.sub) {
+      mbar_arrive_expect_tx(bar, kAStageBytes + 256 * 128);
+      tma_load_2d(sa, &mAct, bar, ks * kBK, ti.m0);
+      tma_load_3d(sb, &mW2, bar, ks * kBK, ti.n0, ti.g % pl.E);
+    } else {
+      mbar_arrive_expect_tx(bar, kAStageBytes + round16(r) * 128);
+      tma_load_2d(sa, &mAct, bar, ks * kBK, ti.m0);
+      tma_load_3d(sb, &mA2, bar, ks * kBK, 0, ti.g);
+    }
+  }
+  __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
+    return MmaStep{ti.sub ? round16(r) : 256, 0, 0, ks == 0};
+  }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t p = (int64_t)ti.m0 + row;
+    if (!ti.sub) {
+      for (int c = 0; c < 256; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+        store_row_bf16(O + p * H + ti.n0 + c, v, 1.0f, 32);
+      }
+    } else {
+      for (int c = 0; c < r; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+        store_row_bf16(Z2 + p * r + c, v, 1.0f, r - c < 32 ? r - c : 32);
+      }
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Forward F6 -- shared B2 expand fused with the routing-weighted combine:
+//   y_t = bf16( s * Z2w_t B2_a^T + sum_j w_tj O[row(t,j)] )   (slot order, fp32)
+// M = tokens of adapter a, N = H (tiles of 256), K = r.
+// =====================================================================================
+struct ProbCombine {
+  static constexpr bool kAmn = false, kBmn = false;
+  CUtensorMap mZ2w, mB2;  // Z2w (r,T) box(64,128); B2 (r,H,A) box(64,256,1)
+  PlanView pl;
+  int* err;
+  const uint16_t* O;
+  const float* topk_w;
+  uint16_t* y;
+  int H, r;
+  float s;
+  __device__ int ntn() const { return H / 256; }
+  __device__ int num_tiles() const { return pl.tok_tile[pl.A] * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int mt = t / ntn(), nt = t % ntn();
+    const int a = adapter_of_tile(pl, mt);
+    TileInfo ti;
+    ti.g = a;
+    ti.m0 = pl.tok_off[a] + (mt - pl.tok_tile[a]) * 128;
+    ti.mend = pl.tok_off[a + 1];
+    ti.n0 = nt * 256;
+    ti.sub = 0;
+    ti.nk = (r + kBK - 1) / kBK;
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mZ2w);
+    tma_prefetch_map(&mB2);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    mbar_arrive_expect_tx(bar, kAStageBytes + 256 * 128);
+    tma_load_2d(sa, &mZ2w, bar, ks * kBK, ti.m0);
+    tma_load_3d(sb, &mB2, bar, ks * kBK, ti.n0, ti.g);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t t = (int64_t)ti.m0 + row;
+    const bool ok = t < ti.mend;
+    const int k = pl.k;
+    for (int c = 0; c < 256; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      if (!ok) continue;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= s;
+      float acc[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int R = pl.row_of_route[t * k + j];
+        if (R < 0) continue;
+        const float w = topk_w[t * k + j];
+        const uint16_t* src = O + (int64_t)R * H + ti.n0 + c;
+#pragma unroll
+        for (int q = 0; q < 32; q += 8) {
+          float o[8];
+          ld_bf16x8(src + q, o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[q + i] += w * o[i];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += acc[i];
+      store_row_bf16(y + t * H + ti.n0 + c, v, 1.0f, 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Backward B1a -- dyB2 = bf16(dy B2_a) [T,r], per token (B2 shared).
+// A: dy K-major; B: (n=q, k=h) = B2[a][h][q], MN-major.
+// =====================================================================================
+struct ProbDyB2 {
+  static constexpr bool kAmn = false, kBmn = true;
+  CUtensorMap mdy, mB2;  // dy (H,T) box(64,128); B2 (r,H,A) box(64,64,1)
+  PlanView pl;
+  int* err;
+  uint16_t* dyB2;
+  int H, r;
+  __device__ int num_tiles() const { return pl.tok_tile[pl.A]; }
+  __device__ TileInfo tile(int t) const {
+    const int a = adapter_of_tile(pl, t);
+    TileInfo ti;
+    ti.g = a;
+    ti.m0 = pl.tok_off[a] + (t - pl.tok_tile[a]) * 128;
+    ti.mend = pl.tok_off[a + 1];
+    ti.n0 = 0;
+    ti.sub = 0;
+    ti.nk = H / kBK;
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mdy);
+    tma_prefetch_map(&mB2);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int nbox = (round16(r) + 63) / 64;
+    mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
+    tma_load_2d(sa, &mdy, bar, ks * kBK, ti.m0);
+    for (int c = 0; c < nbox; ++c) tma_load_3d(sb + c * 8192, &mB2, bar, c * 64, ks * kBK, ti.g);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t t = (int64_t)ti.m0 + row;
+    const bool ok = t < ti.mend;
+    for (int c = 0; c < r; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      if (ok) store_row_bf16(dyB2 + t * r + c, v, 1.0f, r - c < 32 ? r - c : 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Backward B1b -- dB2_a = s * dy^T Z2w over the adapter's tokens  [H,r] fp32.
+// M = H, N = r, K = tokens.  A: (m=h, k=t) = dy[t][h] MN-major; B: (n=q, k=t) = Z2w[t][q] MN-major.
+// =====================================================================================
+struct ProbDB2 {
+  static constexpr bool kAmn = true, kBmn = true;
+  CUtensorMap mdy, mZ2w;  // dy (H,T) box(64,64); Z2w (r,T) box(64,64)
+  PlanView pl;
+  int* err;
+  float* dB2;
+  int H, r;
+  float s;
+  __device__ int num_tiles() const { return pl.A * (H / 128); }
+  __device__ TileInfo tile(int t) const {
+    const int a = t / (H / 128), mt = t % (H / 128);
+    TileInfo ti;
+    ti.g = a;
+    ti.m0 = mt * 128;
+    ti.mend = H;
+    ti.n0 = 0;
+    ti.sub = 0;
+    ti.k0 = pl.tok_off[a];
+    ti.nk = (pl.tok_off[a + 1] - pl.tok_off[a] + kBK - 1) / kBK;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mdy);
+    tma_prefetch_map(&mZ2w);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int nbox = (round16(r) + 63) / 64;
+    const int kt = ti.k0 + ks * kBK;
+    mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
+    tma_load_2d(sa, &mdy, bar, ti.m0, kt);
+    tma_load_2d(sa + 8192, &mdy, bar, ti.m0 + 64, kt);
+    for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mZ2w, bar, c * 64, kt);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t h = (int64_t)ti.m0 + row;
+    for (int c = 0; c < r; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, v, s, r - c < 32 ? r - c : 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+    const float z[32] = {};
+    const int64_t h = (int64_t)ti.m0 + row;
+    for (int c = 0; c < r; c += 32) store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, z, 0.f, r - c < 32 ? r - c : 32);
+  }
+};
+
+// =====================================================================================
+// Backward B3/B4 -- W2^T dgrad with the A2 path, SwiGLU backward and router dots:
+//   Q  = Dp W2_e + D2p A2_ae              [P,I]   (D2p = s * dyB2 of the row's token)
+//   dAct = w * Q;  dG = dAct * U * sig(G) * (1 + G (1 - sig(G)));  dU = dAct * silu(G)
+//   part[p, n-tile] = <Q, Act> over the tile's columns (router gradient partial sums)
+// Padding rows produce exact zeros.  A: Dp/D2p K-major; B: W2/A2 MN-major.
+// =====================================================================================
+struct ProbW2Dgrad {
+  static constexpr bool kAmn = false, kBmn = true;
+  CUtensorMap mDp, mD2p, mW2, mA2;  // Dp (H,P) box(64,128); D2p (r,P) box(64,128);
+                                    // W2 (I,H,E) box(64,64,1); A2 (I,r,G) box(64,64,1)
+  PlanView pl;
+  int* err;
+  const float* topk_w;
+  const uint16_t *G, *U, *Act;
+  uint16_t *dG, *dU;
+  float* part;
+  int H, I, r;
+  __device__ int ntn() const { return I / 256; }
+  __device__ int nkr() const { return (r + 63) / 64; }
+  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int mt = t / ntn(), nt = t % ntn();
+    TileInfo ti;
+    ti.m0 = mt * 128;
+    ti.mend = ti.m0 + 128;
+    ti.n0 = nt * 256;
+    ti.g = pl.tile_group[mt];
+    ti.sub = nt;
+    ti.nk = H / kBK + nkr();
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mDp);
+    tma_prefetch_map(&mD2p);
+    tma_prefetch_map(&mW2);
+    tma_prefetch_map(&mA2);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int nb = H / kBK;
+    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    if (ks < nb) {
+      tma_load_2d(sa, &mDp, bar, ks * kBK, ti.m0);
+      for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
+    } else {
+      const int kb = ks - nb;
+      tma_load_2d(sa, &mD2p, bar, kb * kBK, ti.m0);
+      for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mA2, bar, ti.n0 + c * 64, kb * kBK, ti.g);
+    }
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t p = (int64_t)ti.m0 + row;
+    const int rt = pl.route_of_row[p];
+    const bool live = rt >= 0;
+    const float w = live ? topk_w[rt] : 0.0f;
+    const int64_t base = p * I + ti.n0;
+    float dot = 0.0f;
+    for (int c = 0; c < 256; c += 32) {
+      float q[32];
+      tmem_ld32(taddr + c, q);
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        float g[8], u[8], a[8], og[8], ou[8];
+        ld_bf16x8(G + base + c + j, g);
+        ld_bf16x8(U + base + c + j, u);
+        ld_bf16x8(Act + base + c + j, a);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float qv = q[j + i];
+          dot += qv * a[i];
+          const float da = w * qv;
+          const float sg = 1.0f / (1.0f + expf(-g[i]));
+          og[i] = live ? da * u[i] * sg * (1.0f + g[i] * (1.0f - sg)) : 0.0f;
+          ou[i] = live ? da * g[i] * sg : 0.0f;
+        }
+        st_bf16x8(dG + base + c + j, og);
+        st_bf16x8(dU + base + c + j, ou);
+      }
+    }
+    part[p * ntn() + ti.sub] = live ? dot : 0.0f;
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Backward -- expert-local A2 gradient, K-grouped over each group's rows:
+//   dA2_ae = dZ2p^T Act  [r,I] fp32,  dZ2p = s * w * dyB2 of the row's token.
+// M = r (one tile), N = I (tiles of 256), K = the group's padded rows (zero on padding).
+// =====================================================================================
+struct ProbDA2 {
+  static constexpr bool kAmn = true, kBmn = true;
+  CUtensorMap mdZ2p, mAct;  // dZ2p (r,P) box(64,64); Act (I,P) box(64,64)
+  PlanView pl;
+  int* err;
+  float* dA2;
+  int I, r;
+  __device__ int ntn() const { return I / 256; }
+  __device__ int num_tiles() const { return pl.G * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int g = t / ntn(), nt = t % ntn();
+    TileInfo ti;
+    ti.g = g;
+    ti.m0 = 0;
+    ti.mend = r;
+    ti.n0 = nt * 256;
+    ti.sub = 0;
+    ti.k0 = pl.offsets[g];
+    ti.nk = (pl.offsets[g + 1] - pl.offsets[g]) / kBK;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mdZ2p);
+    tma_prefetch_map(&mAct);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int kt = ti.k0 + ks * kBK;
+    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    tma_load_2d(sa, &mdZ2p, bar, 0, kt);
+    tma_load_2d(sa + 8192, &mdZ2p, bar, 64, kt);
+    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mAct, bar, ti.n0 + c * 64, kt);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const bool ok = row < r;
+    for (int c = 0; c < 256; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      if (ok) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, v, 1.0f, 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+    if (row >= r) return;
+    const float z[32] = {};
+    for (int c = 0; c < 256; c += 32) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, z, 0.f, 32);
+  }
+};
+
+// =====================================================================================
+// Backward B5 -- W13^T dgrad with the B1/B3 path:
+//   dXp = dG W1_e + dU W3_e                 [P,H] bf16     (N tiles of 256, K = 2I)
+//   dY13 = s * [dG B1_ae | dU B3_ae]        [P,2r] fp32    (one extra N tile)
+// A: dG/dU K-major; B: W1/W3/B1/B3 MN-major.  In the extra tile dY1 accumulates
+// in TMEM columns [0,r) and dY3 in [128,128+r).
+// =====================================================================================
+struct ProbW13Dgrad {
+  static constexpr bool kAmn = false, kBmn = true;
+  CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1);
+                                             // B1/B3 (r,I,G) box(64,64,1)
+  PlanView pl;
+  int* err;
+  uint16_t* dXp;
+  float* dY13;
+  int H, I, r;
+  float s;
+  __device__ int ntn() const { return H / 256 + 1; }
+  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int mt = t / ntn(), nt = t % ntn();
+    TileInfo ti;
+    ti.m0 = mt * 128;
+    ti.mend = ti.m0 + 128;
+    ti.sub = nt == H / 256;
+    ti.n0 = ti.sub ? 0 : nt * 256;
+    ti.g = pl.tile_group[mt];
+    ti.nk = 2 * (I / kBK);
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mdG);
+    tma_prefetch_map(&mdU);
+    tma_prefetch_map(&mW1);
+    tma_prefetch_map(&mW3);
+    tma_prefetch_map(&mB1);
+    tma_prefetch_map(&mB3);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int nb = I / kBK;
+    const bool second = ks >= nb;
+    const int kk = (second ? ks - nb : ks) * kBK;
+    if (!ti.sub) {
+      mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+      tma_load_2d(sa, second ? &mdU : &mdG, bar, kk, ti.m0);
+      const CUtensorMap* mw = second ? &mW3 : &mW1;
+      const int e = ti.g % pl.E;
+      for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, mw, bar, ti.n0 + c * 64, kk, e);
+    } else {
+      const int nbox = (round16(r) + 63) / 64;
+      mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
+      tma_load_2d(sa, second ? &mdU : &mdG, bar, kk, ti.m0);
+      const CUtensorMap* mb = second ? &mB3 : &mB1;
+      for (int c = 0; c < nbox; ++c) tma_load_3d(sb + c * 8192, mb, bar, c * 64, kk, ti.g);
+    }
+  }
+  __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
+    const int nb = I / kBK;
+    if (!ti.sub) return MmaStep{256, 0, 0, ks == 0};
+    const bool second = ks >= nb;
+    return MmaStep{round16(r), second ? 128 : 0, 0, ks == 0 || ks == nb};
+  }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t p = (int64_t)ti.m0 + row;
+    if (!ti.sub) {
+      for (int c = 0; c < 256; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+        store_row_bf16(dXp + p * H + ti.n0 + c, v, 1.0f, 32);
+      }
+    } else {
+      for (int half = 0; half < 2; ++half) {
+        for (int c = 0; c < r; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + half * 128 + c, v);
+          store_row_f32(dY13 + p * (2 * r) + half * r + c, v, s, r - c < 32 ? r - c : 32);
+        }
+      }
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Backward -- expert-local B1/B3 gradients, K-grouped over each group's rows:
+//   dB1_ae = dG^T Y1p,  dB3_ae = dU^T Y3p   [I,r] fp32   (s already inside Y13p)
+// M = I (tiles of 128), N = round16(r), K = the group's padded rows.
+// =====================================================================================
+struct ProbDB13 {
+  static constexpr bool kAmn = true, kBmn = true;
+  CUtensorMap mdG, mdU, mY13p;  // dG/dU (I,P) box(64,64); Y13p (2r,P) box(64,64)
+  PlanView pl;
+  int* err;
+  float *dB1, *dB3;
+  int I, r;
+  __device__ int ntm() const { return I / 128; }
+  __device__ int num_tiles() const { return 2 * pl.G * ntm(); }
+  __device__ TileInfo tile(int t) const {
+    const int which = t / (pl.G * ntm());
+    const int rem = t % (pl.G * ntm());
+    const int g = rem / ntm(), mt = rem % ntm();
+    TileInfo ti;
+    ti.g = g;
+    ti.m0 = mt * 128;
+    ti.mend = I;
+    ti.n0 = 0;
+    ti.sub = which;
+    ti.k0 = pl.offsets[g];
+    ti.nk = (pl.offsets[g + 1] - pl.offsets[g]) / kBK;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mdG);
+    tma_prefetch_map(&mdU);
+    tma_prefetch_map(&mY13p);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int kt = ti.k0 + ks * kBK;
+    const int nbox = (round16(r) + 63) / 64;
+    const CUtensorMap* ma = ti.sub ? &mdU : &mdG;
+    mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
+    tma_load_2d(sa, ma, bar, ti.m0, kt);
+    tma_load_2d(sa + 8192, ma, bar, ti.m0 + 64, kt);
+    for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mY13p, bar, ti.sub * r + c * 64, kt);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t i = (int64_t)ti.m0 + row;
+    float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
+    for (int c = 0; c < r; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      store_row_f32(out + c, v, 1.0f, r - c < 32 ? r - c : 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+    const int64_t i = (int64_t)ti.m0 + row;
+    float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
+    const float z[32] = {};
+    for (int c = 0; c < r; c += 32) store_row_f32(out + c, z, 0.f, r - c < 32 ? r - c : 32);
+  }
+};
+
+// =====================================================================================
+// Backward B6 -- grad-x: shared A1/A3 path fused with the source combine:
+//   dx_t = bf16( dY13w_t [A1_a; A3_a] + sum_j dXp[row(t,j)] )
+// M = tokens of adapter a, N = H (tiles of 256), K = 2r (dY1 steps with A1, then dY3 with A3).
+// A: dY13w K-major; B: (n=h, k=q) = A1[a][q][h], MN-major.
+// =====================================================================================
+struct ProbGradX {
+  static constexpr bool kAmn = false, kBmn = true;
+  CUtensorMap mdY13w, mA1, mA3;  // dY13w (2r,T) box(64,128); A1/A3 (H,r,A) box(64,64,1)
+  PlanView pl;
+  int* err;
+  const uint16_t* dXp;
+  uint16_t* dx;
+  int H, r;
+  __device__ int ntn() const { return H / 256; }
+  __device__ int nkr() const { return (r + 63) / 64; }
+  __device__ int num_tiles() const { return pl.tok_tile[pl.A] * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int mt = t / ntn(), nt = t % ntn();
+    const int a = adapter_of_tile(pl, mt);
+    TileInfo ti;
+    ti.g = a;
+    ti.m0 = pl.tok_off[a] + (mt - pl.tok_tile[a]) * 128;
+    ti.mend = pl.tok_off[a + 1];
+    ti.n0 = nt * 256;
+    ti.sub = 0;
+    ti.nk = 2 * nkr();
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mdY13w);
+    tma_prefetch_map(&mA1);
+    tma_prefetch_map(&mA3);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int half = ks / nkr(), kb = ks % nkr();
+    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    tma_load_2d(sa, &mdY13w, bar, half * r + kb * kBK, ti.m0);
+    const CUtensorMap* m = half ? &mA3 : &mA1;
+    for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, m, bar, ti.n0 + c * 64, kb * kBK, ti.g);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t t = (int64_t)ti.m0 + row;
+    const bool ok = t < ti.mend;
+    const int k = pl.k;
+    for (int c = 0; c < 256; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      if (!ok) continue;
+      float acc[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int R = pl.row_of_route[t * k + j];
+        if (R < 0) continue;
+        const uint16_t* src = dXp + (int64_t)R * H + ti.n0 + c;
+#pragma unroll
+        for (int q = 0; q < 32; q += 8) {
+          float o[8];
+          ld_bf16x8(src + q, o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[q + i] += o[i];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += acc[i];
+      store_row_bf16(dx + t * H + ti.n0 + c, v, 1.0f, 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+// =====================================================================================
+// Backward -- shared A1/A3 gradients, per adapter over its tokens:
+//   [dA1; dA3]_a = dY13w^T x   [2r,H] fp32
+// M = 2r (tiles of 128), N = H (tiles of 256), K = tokens.  Both operands MN-major.
+// =====================================================================================
+struct ProbDA13 {
+  static constexpr bool kAmn = true, kBmn = true;
+  CUtensorMap mdY13w, mx;  // dY13w (2r,T) box(64,64); x (H,T) box(64,64)
+  PlanView pl;
+  int* err;
+  float *dA1, *dA3;
+  int H, r;
+  __device__ int ntm() const { return (2 * r + 127) / 128; }
+  __device__ int ntn() const { return H / 256; }
+  __device__ int num_tiles() const { return pl.A * ntm() * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    const int per = ntm() * ntn();
+    const int a = t / per, rem = t % per;
+    const int mt = rem / ntn(), nt = rem % ntn();
+    TileInfo ti;
+    ti.g = a;
+    ti.m0 = mt * 128;
+    ti.mend = 2 * r;
+    ti.n0 = nt * 256;
+    ti.sub = 0;
+    ti.k0 = pl.tok_off[a];
+    ti.nk = (pl.tok_off[a + 1] - pl.tok_off[a] + kBK - 1) / kBK;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mdY13w);
+    tma_prefetch_map(&mx);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int kt = ti.k0 + ks * kBK;
+    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    tma_load_2d(sa, &mdY13w, bar, ti.m0, kt);
+    tma_load_2d(sa + 8192, &mdY13w, bar, ti.m0 + 64, kt);
+    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mx, bar, ti.n0 + c * 64, kt);
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
+  __device__ float* out_row(const TileInfo& ti, int m) const {
+    return (m < r ? dA1 + ((int64_t)ti.g * r + m) * H : dA3 + ((int64_t)ti.g * r + (m - r)) * H) + ti.n0;
+  }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int m = ti.m0 + row;
+    const bool ok = m < 2 * r;
+    for (int c = 0; c < 256; c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      if (ok) store_row_f32(out_row(ti, m) + c, v, 1.0f, 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+    const int m = ti.m0 + row;
+    if (m >= 2 * r) return;
+    const float z[32] = {};
+    for (int c = 0; c < 256; c += 32) store_row_f32(out_row(ti, m) + c, z, 0.f, 32);
+  }
+};
+
+// =====================================================================================
+// Plain GEMM for engine self-tests: C[M,N] fp32 = sum_k A(m,k) B(n,k).
+// A is [M,K] (K-major) or [K,M] (MN-major); B is [N,K] or [K,N].  M % 128 == 0,
+// K % 64 == 0, N % 256 == 0 or N <= 256 with N % 16 == 0.
+// =====================================================================================
+template <bool AMN, bool BMN>
+struct ProbPlain {
+  static constexpr bool kAmn = AMN, kBmn = BMN;
+  CUtensorMap mA, mB;  // K-major: (K,rows) box(64,128 | N); MN-major: (rows,K) box(64,64)
+  int* err;
+  float* C;
+  int M, N, K;
+  __device__ int tn() const { return N < 256 ? N : 256; }
+  __device__ int ntn() const { return (N + 255) / 256; }
+  __device__ int num_tiles() const { return M / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    TileInfo ti;
+    ti.m0 = t / ntn() * 128;
+    ti.n0 = t % ntn() * 256;
+    ti.mend = M;
+    ti.g = 0;
+    ti.sub = 0;
+    ti.nk = K / kBK;
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mA);
+    tma_prefetch_map(&mB);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int kt = ks * kBK;
+    const int nbox = (tn() + 63) / 64;
+    mbar_arrive_expect_tx(bar, kAStageBytes + (BMN ? nbox * 8192 : tn() * 128));
+    if (AMN) {
+      tma_load_2d(sa, &mA, bar, ti.m0, kt);
+      tma_load_2d(sa + 8192, &mA, bar, ti.m0 + 64, kt);
+    } else {
+      tma_load_2d(sa, &mA, bar, kt, ti.m0);
+    }
+    if (BMN) {
+      for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mB, bar, ti.n0 + c * 64, kt);
+    } else {
+      tma_load_2d(sb, &mB, bar, kt, ti.n0);
+    }
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{tn(), 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+    const int64_t m = (int64_t)ti.m0 + row;
+    for (int c = 0; c < tn(); c += 32) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      store_row_f32(C + m * N + ti.n0 + c, v, 1.0f, tn() - c < 32 ? tn() - c : 32);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int) const {}
+};
+
+}  // namespace moelora

@@ -1,0 +1,40 @@
+// Host-side launch interface between the C-ABI entry points and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace moelora {
+
+// Adapter token ranges, passed by value to the plan kernels.
+struct AdapterTable {
+  int n;                               // adapters
+  int tok_off[kMaxAdapters + 1];       // first token of each adapter; tok_off[n] = T
+  int tok_tile[kMaxAdapters + 1];      // first 128-token tile of each adapter
+};
+
+cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const AdapterTable& at, void* ws,
+                        cudaStream_t stream);
+
+// Xp[p] = x[token(p)], Y13p[p] = Y13[token(p)]; zero rows for padding.
+cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint16_t* Xp,
+                              uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream);
+
+// Z2w[t] = bf16(sum_j w_tj Z2[row(t,j)])  [T,r]
+cudaError_t launch_z2w(const PlanView& pl, const uint16_t* Z2, const float* topk_w, uint16_t* Z2w, int r,
+                       int num_sms, cudaStream_t stream);
+
+// Dp[p] = dy[token], D2p[p] = bf16(s*dyB2[token]), dZ2p[p] = bf16(s*w*dyB2[token]); zero on padding.
+cudaError_t launch_gather_bwd(const PlanView& pl, const uint16_t* dy, const uint16_t* dyB2, const float* topk_w,
+                              uint16_t* Dp, uint16_t* D2p, uint16_t* dZ2p, int H, int r, float s, int num_sms,
+                              cudaStream_t stream);
+
+// dw[t*k+j] = sum over n-tiles of part[row(t,j)], 0 for masked routes.
+cudaError_t launch_dw(const PlanView& pl, const float* part, int nparts, float* dw, int num_sms,
+                      cudaStream_t stream);
+
+// dY13w[t] = bf16(sum_j dY13[row(t,j)])  [T,2r]
+cudaError_t launch_dy13w(const PlanView& pl, const float* dY13, uint16_t* dY13w, int r2, int num_sms,
+                         cudaStream_t stream);
+
+}  // namespace moelora

@@ -1,0 +1,151 @@
+// HBM-bound kernels of the MoE side-LoRA path: routed-row gathers (with zeroed
+// padding rows, so allocator garbage can never reach a shared reduction --
+// "feat(mega): add fused shared side-LoRA kernels", Summary: "zeroing expert
+// padding ... before shared contractions") and per-token reductions over the k
+// routes of a token (fixed slot order, fp32, one bf16 rounding).
+// All use 16-byte vector accesses, one warp per row, grid-stride over rows.
+#include "launch.h"
+
+namespace moelora {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void copy_row_or_zero(uint16_t* dst, const uint16_t* src, int n, int lane) {
+  // n bf16 (multiple of 8), 16 B per lane per step
+  for (int c = lane * 8; c < n; c += 32 * 8) {
+    uint4 v = src ? *reinterpret_cast<const uint4*>(src + c) : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(dst + c) = v;
+  }
+}
+
+__global__ void gather_fwd_kernel(PlanView pl, const uint16_t* __restrict__ x, const uint16_t* __restrict__ Y13,
+                                  uint16_t* __restrict__ Xp, uint16_t* __restrict__ Y13p, int H, int r2) {
+  const int64_t P = pl.offsets[pl.G];
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t p = w0; p < P; p += nw) {
+    const int rt = pl.route_of_row[p];
+    const int64_t t = rt >= 0 ? rt / pl.k : -1;
+    copy_row_or_zero(Xp + p * H, t >= 0 ? x + t * H : nullptr, H, lane);
+    copy_row_or_zero(Y13p + p * r2, t >= 0 ? Y13 + t * r2 : nullptr, r2, lane);
+  }
+}
+
+// one warp per token; lane covers r/32.. columns (r <= 128 -> up to 4 per lane)
+__global__ void z2w_kernel(PlanView pl, const uint16_t* __restrict__ Z2, const float* __restrict__ topk_w,
+                           uint16_t* __restrict__ Z2w, int r) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = w0; t < pl.T; t += nw) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < pl.k; ++j) {
+      const int R = pl.row_of_route[t * pl.k + j];
+      if (R < 0) continue;
+      const float w = topk_w[t * pl.k + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = lane + 32 * i;
+        if (q < r) acc[i] += w * __uint_as_float((uint32_t)Z2[(int64_t)R * r + q] << 16);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int q = lane + 32 * i;
+      if (q < r) {
+        __nv_bfloat16 h = __float2bfloat16_rn(acc[i]);
+        Z2w[t * r + q] = *reinterpret_cast<uint16_t*>(&h);
+      }
+    }
+  }
+}
+
+__global__ void gather_bwd_kernel(PlanView pl, const uint16_t* __restrict__ dy, const uint16_t* __restrict__ dyB2,
+                                  const float* __restrict__ topk_w, uint16_t* __restrict__ Dp,
+                                  uint16_t* __restrict__ D2p, uint16_t* __restrict__ dZ2p, int H, int r, float s) {
+  const int64_t P = pl.offsets[pl.G];
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t p = w0; p < P; p += nw) {
+    const int rt = pl.route_of_row[p];
+    const int64_t t = rt >= 0 ? rt / pl.k : -1;
+    copy_row_or_zero(Dp + p * H, t >= 0 ? dy + t * H : nullptr, H, lane);
+    const float w = rt >= 0 ? topk_w[rt] : 0.0f;
+    for (int q = lane; q < r; q += 32) {
+      const float v = t >= 0 ? __uint_as_float((uint32_t)dyB2[t * r + q] << 16) : 0.0f;
+      __nv_bfloat16 a = __float2bfloat16_rn(s * v);
+      __nv_bfloat16 b = __float2bfloat16_rn(s * w * v);
+      D2p[p * r + q] = *reinterpret_cast<uint16_t*>(&a);
+      dZ2p[p * r + q] = *reinterpret_cast<uint16_t*>(&b);
+    }
+  }
+}
+
+__global__ void dw_kernel(PlanView pl, const float* __restrict__ part, int nparts, float* __restrict__ dw) {
+  const int64_t TK = pl.T * pl.k;
+  for (int64_t rt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; rt < TK; rt += (int64_t)gridDim.x * blockDim.x) {
+    const int R = pl.row_of_route[rt];
+    float acc = 0.0f;
+    if (R >= 0)
+      for (int n = 0; n < nparts; ++n) acc += part[(int64_t)R * nparts + n];
+    dw[rt] = acc;
+  }
+}
+
+__global__ void dy13w_kernel(PlanView pl, const float* __restrict__ dY13, uint16_t* __restrict__ dY13w, int r2) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = w0; t < pl.T; t += nw) {
+    for (int q = lane; q < r2; q += 32) {
+      float acc = 0.0f;
+      for (int j = 0; j < pl.k; ++j) {
+        const int R = pl.row_of_route[t * pl.k + j];
+        if (R >= 0) acc += dY13[(int64_t)R * r2 + q];
+      }
+      __nv_bfloat16 h = __float2bfloat16_rn(acc);
+      dY13w[t * r2 + q] = *reinterpret_cast<uint16_t*>(&h);
+    }
+  }
+}
+
+int grid_for(int num_sms) { return num_sms * 8; }
+
+}  // namespace
+
+cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint16_t* Xp,
+                              uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream) {
+  gather_fwd_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, x, Y13, Xp, Y13p, H, r2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_z2w(const PlanView& pl, const uint16_t* Z2, const float* topk_w, uint16_t* Z2w, int r,
+                       int num_sms, cudaStream_t stream) {
+  z2w_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, Z2, topk_w, Z2w, r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_bwd(const PlanView& pl, const uint16_t* dy, const uint16_t* dyB2, const float* topk_w,
+                              uint16_t* Dp, uint16_t* D2p, uint16_t* dZ2p, int H, int r, float s, int num_sms,
+                              cudaStream_t stream) {
+  gather_bwd_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, dy, dyB2, topk_w, Dp, D2p, dZ2p, H, r, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw(const PlanView& pl, const float* part, int nparts, float* dw, int num_sms,
+                      cudaStream_t stream) {
+  dw_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, part, nparts, dw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dy13w(const PlanView& pl, const float* dY13, uint16_t* dY13w, int r2, int num_sms,
+                         cudaStream_t stream) {
+  dy13w_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, dY13, dY13w, r2);
+  return cudaGetLastError();
+}
+
+}  // namespace moelora

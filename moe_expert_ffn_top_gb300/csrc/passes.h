@@ -1,0 +1,21 @@
+// Forward / backward launch sequences (forward.cu, backward.cu) and the plain
+// engine GEMM used by the self-test entry point (selftest.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "../../include/moe_lora.h"
+
+namespace moelora {
+
+int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, const float* topk_w,
+                const moe_lora_weights* w, uint16_t* y, void* saved, void* scratch, int num_sms,
+                cudaStream_t stream);
+
+int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved, const uint16_t* x,
+                 const float* topk_w, const uint16_t* dy, const moe_lora_weights* w, uint16_t* dx, float* dw,
+                 const moe_lora_grads* gr, void* scratch, int num_sms, cudaStream_t stream);
+
+int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,
+                   int* err, int num_sms, cudaStream_t stream);
+
+}  // namespace moelora

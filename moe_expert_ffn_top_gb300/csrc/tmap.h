@@ -1,0 +1,16 @@
+// TMA tensor-map construction (host).  All maps are bf16, row-major, with the
+// 128-byte swizzle the GEMM engine's shared-memory descriptors expect, and zero
+// fill outside the tensor (used for ragged token tails and for ranks below 64).
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+namespace moelora {
+
+// 2D tensor [outer][inner]; box of box_inner x box_outer elements.  Returns 0 on success.
+int tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+            uint32_t box_outer);
+// 3D tensor [d2][d1][d0]; box of b0 x b1 x 1.
+int tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1);
+
+}  // namespace moelora

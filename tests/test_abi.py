@@ -1,0 +1,124 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+entry point include/moe_lora.h declares, sizes workspaces, and rejects bad calls
+on the host before any launch (the pages' fail-fast rule: "reject unsupported
+post-down side-LoRA and undersized scratch before launching kernels",
+"feat(mega): add fused shared side-LoRA kernels", Summary)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import moe_expert_ffn_top_gb300 as m
+from moe_expert_ffn_top_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return m.lib()
+
+
+def _declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"MOE_LORA_API\s+[\w\s\*]+?\b(moe_lora_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def _dims(**kw):
+    base = dict(T=256, H=512, I=256, E=16, k=2, r=16)
+    base.update(kw)
+    return m.make_dims(**base)
+
+
+def test_workspace_sizes(L):
+    d = _dims()
+    sizes = [m.moe_lora_workspace_bytes(d, w) for w in range(4)]
+    assert all(s > 0 for s in sizes)
+    assert m.moe_lora_workspace_bytes(d, 9) == 0
+    # production shape: bounded by T*k + E*(BM-1) rows
+    p = m.make_dims(65536, 4096, 2048, 256, 6, 128)
+    P = 65536 * 6 + 256 * 127
+    assert m.moe_lora_workspace_bytes(p, m.MOE_LORA_WS_SAVED) >= 2 * P * (3 * 2048 + 256)
+    for bad in (dict(H=500), dict(I=128), dict(r=12), dict(r=136), dict(k=0), dict(k=33), dict(E=0), dict(A=0)):
+        assert m.moe_lora_workspace_bytes(_dims(**bad), 0) == 0, bad
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: every call below is rejected before any CUDA work
+
+
+def _call_forward(L, d, **over):
+    args = dict(plan=FAKE, x=FAKE, w=FAKE, y=FAKE, saved=FAKE, saved_bytes=1 << 40, scratch=FAKE,
+                scratch_bytes=1 << 40)
+    args.update(over)
+    W = m.Weights(*([over.get("weight", FAKE)] * 9))
+    return L.moe_lora_forward(ctypes.byref(d), args["plan"], args["x"], args["w"], ctypes.byref(W), args["y"],
+                              args["saved"], args["saved_bytes"], args["scratch"], args["scratch_bytes"], None)
+
+
+def test_forward_rejections(L):
+    d = _dims()
+    assert _call_forward(L, _dims(H=500)) == -2
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 1, 0)) == -5   # GeGLU: not built
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 1)) == -5   # MXFP4 base: not built
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 64, 1.0, 0, 0)) == -2    # block_m != 128
+    assert _call_forward(L, d, plan=None) == -1
+    assert _call_forward(L, d, weight=FAKE + 8) == -3
+    assert _call_forward(L, d, saved_bytes=16) == -4
+    assert _call_forward(L, d, scratch_bytes=16) == -4
+    assert _call_forward(L, d, x=FAKE + 2) == -3
+    assert _call_forward(L, d, y=None) == -1
+
+
+def test_plan_rejections(L):
+    d = _dims()
+    nbytes = m.moe_lora_workspace_bytes(d, 0)
+    assert L.moe_lora_plan(ctypes.byref(d), FAKE, None, FAKE, nbytes - 1, None) == -4
+    assert L.moe_lora_plan(ctypes.byref(d), None, None, FAKE, nbytes, None) == -1
+    assert L.moe_lora_plan(ctypes.byref(d), FAKE, None, FAKE + 4, nbytes, None) == -3
+    d2 = _dims(A=2)
+    n2 = m.moe_lora_workspace_bytes(d2, 0)
+    assert L.moe_lora_plan(ctypes.byref(d2), FAKE, None, FAKE, n2, None) == -1
+    offs = (ctypes.c_int64 * 3)(0, 100, 256)        # adapter start not a multiple of 128
+    assert L.moe_lora_plan(ctypes.byref(d2), FAKE, offs, FAKE, n2, None) == -2
+    offs = (ctypes.c_int64 * 3)(0, 128, 200)        # does not end at T
+    assert L.moe_lora_plan(ctypes.byref(d2), FAKE, offs, FAKE, n2, None) == -2
+
+
+def test_backward_rejections(L):
+    d = _dims()
+    W = m.Weights(*([FAKE] * 9))
+    G = m.Grads(*([FAKE] * 6))
+    Gbad = m.Grads(*([FAKE] * 5 + [FAKE + 4]))
+    bb = 1 << 40
+    assert L.moe_lora_backward(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(W), FAKE, FAKE,
+                               None, FAKE, bb, None) == -1
+    assert L.moe_lora_backward(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(W), FAKE, FAKE,
+                               ctypes.byref(Gbad), FAKE, bb, None) == -3
+    assert L.moe_lora_backward(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(W), FAKE, FAKE,
+                               ctypes.byref(G), FAKE, 100, None) == -4
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_no_device_is_reported(L):
+    d = _dims()
+    nbytes = m.moe_lora_workspace_bytes(d, 0)
+    assert L.moe_lora_plan(ctypes.byref(d), FAKE, None, FAKE, nbytes, None) == -7
+
+
+def test_strerror(L):
+    for c in range(-7, 1):
+        assert m.moe_lora_strerror(c) and m.moe_lora_strerror(c) != "unknown error"

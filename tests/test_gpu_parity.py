@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: routing plan bit-exact; BF16 outputs and every gradient within relative L2
+5e-3 and cosine 0.9999 (FP64 metrics over whole tensors), the accuracy gate the
+side-LoRA pages use ("feat(mega): add fused shared side-LoRA kernels", Accuracy
+and regression tests / Correctness coverage).  Inputs are seeded and synthetic
+(synth.make_inputs); expected values come only from the oracle.
+"""
+import os
+
+import pytest
+import torch
+
+import moe_expert_ffn_top_gb300 as m
+import oracle
+from synth import EDGE_TOKEN_COUNTS, Shape, make_inputs, shape
+
+from gpu_common import ADAPTER_GRADS, assert_close, dims_of, rel_l2, run_gpu, sub_problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from moe_expert_ffn_top_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+    yield
+
+
+# ----------------------------------------------------------------------------- engine
+@pytest.mark.parametrize("a_mn", [False, True])
+@pytest.mark.parametrize("b_mn", [False, True])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 320), (128, 16, 128), (384, 144, 192)])
+def test_engine_gemm(a_mn, b_mn, M, N, K):
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N + K)
+    A = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    m.moe_lora_gemm_selftest(A.t().contiguous() if a_mn else A, a_mn, B.t().contiguous() if b_mn else B, b_mn, C)
+    torch.cuda.synchronize()
+    assert m.moe_lora_gemm_selftest_error() == 0
+    ref = A.double() @ B.double().t()
+    assert rel_l2(C, ref) < 1e-5
+
+
+# ----------------------------------------------------------------------------- plan
+def _plan_check(ids_cpu, E, shp, offs=None, BM=128):
+    d = m.make_dims(shp.T, shp.H, shp.I, E, shp.k, shp.r, shp.A)
+    ws = m.Workspaces.allocate(d)
+    m.moe_lora_plan(d, ids_cpu.cuda(), offs, ws.plan)
+    got = m.moe_lora_plan_readback(d, ws.plan)
+    want = oracle.plan(ids_cpu, E, torch.tensor(offs if offs else [0, shp.T]), BM)
+    for n in ("counts", "offsets", "row_of_route", "route_of_row"):
+        assert torch.equal(got[n], want[n]), n
+    return d, ws, want
+
+
+@pytest.mark.parametrize("T,k,E,mask,seed", [(1, 1, 4, 0.0, 0), (256, 2, 16, 0.0, 1), (1000, 6, 256, 0.2, 2),
+                                             (5000, 8, 128, 0.3, 3), (2048, 6, 256, 0.2, 4)])
+def test_plan_bit_exact(T, k, E, mask, seed):
+    g = torch.Generator().manual_seed(seed)
+    ids = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+    ids[torch.rand(T, k, generator=g) < mask] = -1
+    ids[:, 0][ids[:, 0] == 3] = -1
+    shp = Shape(T=T, H=256, I=256, E=E, k=k, r=8)
+    _plan_check(ids, E, shp)
+
+
+def test_plan_multi_adapter_bit_exact():
+    T, k, E, A = 16 * 128, 4, 32, 16
+    g = torch.Generator().manual_seed(11)
+    ids = torch.randint(-1, E, (T, k), generator=g, dtype=torch.int32)
+    shp = Shape(T=T, H=256, I=256, E=E, k=k, r=8, A=A)
+    _plan_check(ids, E, shp, offs=list(range(0, T + 1, 128)))
+
+
+def test_plan_bad_ids_flagged_and_dropped():
+    ids = torch.tensor([[0, 7], [-3, 1], [2, -1]], dtype=torch.int32)
+    shp = Shape(T=3, H=256, I=256, E=4, k=2, r=8)
+    d = m.make_dims(3, 256, 256, 4, 2, 8)
+    ws = m.Workspaces.allocate(d)
+    m.moe_lora_plan(d, ids.cuda(), None, ws.plan)
+    got = m.moe_lora_plan_readback(d, ws.plan)
+    assert m.moe_lora_get_error(d, ws.plan) & m.MOE_LORA_DEV_BAD_ID
+    want = oracle.plan(ids, 4, torch.tensor([0, 3]), 128)
+    assert torch.equal(got["row_of_route"], want["row_of_route"])
+
+
+# ----------------------------------------------------------------------------- full path
+def _full_check(inp, shp, out, tokens=None):
+    """Compare everything the GPU returned with the oracle (all tokens if None)."""
+    y_ref = oracle.forward(inp, shp, tokens=tokens)
+    g_ref = oracle.backward(inp, shp, tokens=tokens)
+    sel = slice(None) if tokens is None else torch.as_tensor(tokens)
+    assert_close("y", out["y"].cpu()[sel], y_ref)
+    assert_close("dx", out["dx"].cpu()[sel], g_ref["dx"])
+    assert_close("dw", out["dw"].cpu()[sel], g_ref["dw"])
+    for n in ADAPTER_GRADS:
+        assert_close(n, out[n].cpu(), g_ref[n])
+
+
+@pytest.mark.parametrize("T,mask", [(256, 0.0), (200, 0.15), (17, 0.0)])
+def test_tiny_forward_backward(T, mask):
+    shp = Shape(T=T, H=512, I=256, E=16, k=2, r=16, mask_frac=mask)
+    inp = make_inputs(shp, seed=0)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    _full_check(inp, shp, out)
+
+
+def test_small_rank8_top8():
+    shp = Shape(T=300, H=256, I=512, E=8, k=8, r=8, scale=0.5)
+    inp = make_inputs(shp, seed=5)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    _full_check(inp, shp, out)
+
+
+def test_rank128_wide():
+    shp = Shape(T=130, H=1024, I=512, E=8, k=3, r=128, mask_frac=0.2, empty_experts=(0, 7))
+    inp = make_inputs(shp, seed=6)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    _full_check(inp, shp, out)
+    for n in ("dB1", "dB3", "dA2"):
+        assert out[n][0, 0].abs().max().item() == 0 and out[n][0, 7].abs().max().item() == 0
+
+
+def test_zero_scale_is_plain_moe_bitwise():
+    """Zero adapter scale reproduces the layer without side adapters bit for bit
+    (the pages' zero-scale preservation check)."""
+    shp = Shape(T=256, H=512, I=256, E=16, k=2, r=16)
+    inp = make_inputs(shp, seed=7)
+    out0 = run_gpu(inp, shp, scale=0.0)
+    bare = dict(inp)
+    for n in ("A1", "A3", "B1", "B3", "A2", "B2"):
+        bare[n] = torch.zeros_like(inp[n])
+    outp = run_gpu(bare, shp, scale=1.0)
+    for n in ("y", "dx", "dw"):
+        assert torch.equal(out0[n], outp[n]), n
+    y_ref = oracle.forward(inp, shp, scale=0.0)
+    assert_close("y(s=0)", out0["y"].cpu(), y_ref)
+
+
+def test_deterministic_and_poison_free():
+    """Two runs are bitwise identical, also with every workspace and output
+    pre-filled with NaN (padding rows and stale scratch never leak)."""
+    shp = Shape(T=200, H=512, I=256, E=16, k=2, r=16, mask_frac=0.2)
+    inp = make_inputs(shp, seed=8)
+    a = run_gpu(inp, shp)
+    b = run_gpu(inp, shp, poison=True)
+    for n in ("y", "dx", "dw") + ADAPTER_GRADS:
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_empty_batch():
+    shp = Shape(T=0, H=512, I=256, E=16, k=2, r=16)
+    d = dims_of(shp)
+    ws = m.Workspaces.allocate(d)
+    ids = torch.empty(0, 2, dtype=torch.int32, device="cuda")
+    m.moe_lora_plan(d, ids, None, ws.plan)
+    g = m.alloc_grads(d)
+    for t in g.values():
+        t.fill_(float("nan"))
+    e = torch.empty(0, device="cuda")
+    x = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    inp = make_inputs(Shape(T=1, H=512, I=256, E=16, k=2, r=16), seed=0)
+    wts = {n: inp[n].cuda() for n in ("W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")}
+    m.moe_lora_backward(d, ws.plan, ws.saved, x, e, x, wts, x, e, g, ws.bwd)
+    torch.cuda.synchronize()
+    for n, t in g.items():
+        assert t.abs().max().item() == 0, n
+
+
+# ----------------------------------------------------------------------------- production width
+def _sampled_check(inp, shp, out, sample):
+    """Sparse-dy parity: dy is zero outside `sample`, so every gradient only has
+    contributions from the sampled tokens and the oracle can compute it exactly
+    on that sub-problem; outside the sample dx and dw must be exactly zero."""
+    sub, sshp, used, tok = sub_problem(inp, shp, sample)
+    y_ref = oracle.forward(sub, sshp)
+    g_ref = oracle.backward(sub, sshp)
+    tk = tok.cuda()
+    assert_close("y", out["y"][tk].cpu(), y_ref)
+    assert_close("dx", out["dx"][tk].cpu(), g_ref["dx"])
+    assert_close("dw", out["dw"][tk].cpu(), g_ref["dw"])
+    mask = torch.ones(shp.T, dtype=torch.bool, device="cuda")
+    mask[tk] = False
+    assert out["dx"][mask].abs().max().item() == 0 if mask.any() else True
+    assert out["dw"][mask].abs().max().item() == 0 if mask.any() else True
+    ex = torch.as_tensor(used, device="cuda")
+    for n in ("dA1", "dA3", "dB2"):
+        assert_close(n, out[n].cpu(), g_ref[n])
+    for n in ("dB1", "dB3", "dA2"):
+        assert_close(n, out[n][:, ex].cpu(), g_ref[n])
+        other = torch.ones(shp.E, dtype=torch.bool, device="cuda")
+        other[ex] = False
+        assert out[n][:, other].abs().max().item() == 0, n
+
+
+def _sparse_dy(inp, shp, sample):
+    dy = torch.zeros_like(inp["dy"])
+    idx = torch.as_tensor(sample, device=dy.device)
+    dy[idx] = inp["dy"][idx]
+    out = dict(inp)
+    out["dy"] = dy
+    return out
+
+
+@pytest.mark.parametrize("T", EDGE_TOKEN_COUNTS)
+def test_edge_sweep_production_width(T):
+    """H=4096, I=2048, E=256, top-6, rank 128, 20% masked routes, experts 0/127/255
+    empty, at the 15 token counts of the pages' boundary sweep."""
+    shp = shape("edge", T)
+    inp = make_inputs(shp, seed=1000 + T, device="cuda")
+    g = torch.Generator().manual_seed(T)
+    n = min(T, 12)
+    sample = sorted(torch.randperm(T, generator=g)[:n].tolist())
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    want = oracle.plan(inp["topk_ids"].cpu(), shp.E, torch.tensor([0, T]), 128)
+    got = m.moe_lora_plan_readback(out["dims"], out["ws"].plan)
+    for k in ("counts", "offsets", "row_of_route", "route_of_row"):
+        assert torch.equal(got[k], want[k]), k
+    _sampled_check(inp, shp, out, sample)
+
+
+@pytest.mark.slow
+def test_production_shape_sampled():
+    """65,536 tokens, H=4096, I=2048, E=256, top-6, rank 128: the benchmark's
+    workload and launch configuration, checked on sampled tokens (sparse dy)."""
+    shp = shape("prod")
+    inp = make_inputs(shp, seed=2, device="cuda")
+    sample = [0, 1, 777, 4096, 33333, 65535]
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    want = oracle.plan(inp["topk_ids"].cpu(), shp.E, torch.tensor([0, shp.T]), 128)
+    got = m.moe_lora_plan_readback(out["dims"], out["ws"].plan)
+    for k in ("counts", "offsets", "row_of_route", "route_of_row"):
+        assert torch.equal(got[k], want[k]), k
+    _sampled_check(inp, shp, out, sample)

@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Forward+backward benchmark of the routed MoE SwiGLU expert FFN with rank-128
+side-LoRA at the production shape of "feat(mega): add fused shared side-LoRA
+kernels" (DeepGEMM PR #9, Matched production-shape performance): 65,536 tokens,
+H=4096, I=2048, E=256, top-6, rank 128, s=1, BF16 with FP32 accumulation, on one
+GB300 (the pages measured 65,536 tokens per rank on 4 GPUs with expert
+parallelism; this path has no expert parallelism).
+
+One step = routing plan + forward + backward over one batch.  Inputs are seeded
+synthetic tensors of the pages' shapes and distributions (synth.make_inputs),
+resident in HBM; the working set (12.9 GB of frozen weights alone) is far larger
+than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  `value` is algorithmic TFLOP/s of the whole job (N GPUs,
+max-over-ranks time); `e2e` repeats the measurement through the public Python
+API with the inputs copied from pinned host memory and every result read back,
+inside the timed region.  `--impl reference` times the CPU oracle (the method
+written plainly in C) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from synth import Shape, make_inputs, shape  # noqa: E402
+
+METRIC = "fwd+bwd ms & TFLOP/s (% BF16 peak), 64K tok H4096 I2048 E256 top6 r128"
+ADAPTER_GRADS = ("dA1", "dA3", "dB1", "dB3", "dA2", "dB2")
+WEIGHTS = ("W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sus": d.get("bf16_tflops_sustained",
+                                                                                  d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ algorithmic work
+def step_flops(T, R, H, I, r):
+    """Forward + backward FLOPs over live routes R (no padding, no per-route
+    re-expansion of the shared factors): 12RHI + 18THr + 18RIr."""
+    return 12.0 * R * H * I + 18.0 * T * H * r + 18.0 * R * I * r
+
+
+def kernel_work(T, R, H, I, r, k):
+    """Per-launch algorithmic FLOPs (tensor kernels) or bytes (HBM kernels)."""
+    fl = {
+        "shrink_x_A13": 2.0 * T * H * 2 * r,
+        "w13_lora_swiglu": 4.0 * R * H * I + 4.0 * R * I * r,
+        "w2_a2": 2.0 * R * I * H + 2.0 * R * I * r,
+        "b2_expand_combine": 2.0 * T * r * H,
+        "dy_b2": 2.0 * T * H * r,
+        "dB2": 2.0 * T * H * r,
+        "w2_dgrad_swiglu_bwd": 2.0 * R * H * I + 2.0 * R * r * I,
+        "dA2": 2.0 * R * r * I,
+        "w13_dgrad_b13": 4.0 * R * I * H + 4.0 * R * I * r,
+        "dB13": 4.0 * R * I * r,
+        "gradx_a13_combine": 4.0 * T * r * H,
+        "dA13": 4.0 * T * r * H,
+    }
+    by = {
+        "gather_fwd": 2.0 * (2 * R * H + 2 * R * 2 * r),
+        "z2_combine": 2.0 * (R * r + T * r),
+        "gather_bwd": 2.0 * (2 * R * H + 3 * R * r),
+        "dw_reduce": 4.0 * (R * (I // 256) + T * k),
+        "dy13_combine": 4.0 * R * 2 * r + 2.0 * T * 2 * r,
+        "plan_count": 4.0 * T * k, "plan_scan": 0.0, "plan_scatter": 4.0 * T * k * 3, "plan_finish": 0.0,
+    }
+    return fl, by
+
+
+def src_hash():
+    h = hashlib.sha256()
+    for d in (os.path.join(ROOT, "moe_expert_ffn_top_gb300", "csrc"), os.path.join(ROOT, "include")):
+        for f in sorted(os.listdir(d)):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    captured on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("src_hash") != src_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [l.strip().split(", ") for l in self.f.read().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(inp_cpu, shp, seconds_target, max_tokens=512):
+    """Times the CPU oracle (forward + backward) on the first tokens of the
+    workload, sized to take about `seconds_target`.  Returns (TFLOP/s, info)."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count()
+
+    def run(n):
+        toks = list(range(n))
+        R = int((inp_cpu["topk_ids"][:n] >= 0).sum())
+        t0 = time.perf_counter()
+        oracle.forward(inp_cpu, shp, tokens=toks)
+        oracle.backward(inp_cpu, shp, tokens=toks)
+        dt = time.perf_counter() - t0
+        return dt, step_flops(n, R, shp.H, shp.I, shp.r), R
+
+    dt, fl, R = run(2)
+    n = int(min(max_tokens, max(2, 2 * seconds_target / max(dt, 1e-3))))
+    dt, fl, R = run(n)
+    return fl / dt / 1e12, {"tokens": n, "routes": R, "seconds": dt, "cores": cores, "flops": fl}
+
+
+def host_inputs(shp, seed):
+    """The workload's seeded inputs drawn on the device, copied to host memory."""
+    inp = make_inputs(shp, seed=seed, device="cuda")
+    out = {n: v.cpu() for n, v in inp.items()}
+    del inp
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import moe_expert_ffn_top_gb300 as m
+    from moe_expert_ffn_top_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    shp = shape(args.workload)
+    inp = make_inputs(shp, seed=2 + rank, device="cuda")
+    T, H, I, E, k, r = shp.T, shp.H, shp.I, shp.E, shp.k, shp.r
+    R = int((inp["topk_ids"] >= 0).sum())
+    d = m.make_dims(T, H, I, E, k, r, 1, shp.scale)
+    ws = m.Workspaces.allocate(d)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty_like(y)
+    dw = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    g = m.alloc_grads(d)
+    wts = {n: inp[n] for n in WEIGHTS}
+    stream = torch.cuda.current_stream()
+
+    def step(x, ids, tw, dy):
+        m.moe_lora_plan(d, ids, None, ws.plan)
+        m.moe_lora_forward(d, ws.plan, x, tw, wts, y, ws.saved, ws.fwd)
+        m.moe_lora_backward(d, ws.plan, ws.saved, x, tw, dy, wts, dx, dw, g, ws.bwd)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    args_dev = (inp["x"], inp["topk_ids"], inp["topk_w"], inp["dy"])
+    for _ in range(args.warmup):
+        step(*args_dev)
+    torch.cuda.synchronize()
+    assert m.moe_lora_get_error(d, ws.plan) == 0, "device error word set"
+
+    # ---- device-resident timing
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    m.moe_lora_launch_count(reset=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(*args_dev)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    launches = m.moe_lora_launch_count(reset=True)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    flops = step_flops(T, R, H, I, r)
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # ---- per-kernel event timing (a separate, identical pass)
+    m.moe_lora_profile_enable(True)
+    for _ in range(args.steps):
+        step(*args_dev)
+    torch.cuda.synchronize()
+    prof = m.moe_lora_profile_read()
+    m.moe_lora_profile_enable(False)
+    pk = peaks()
+    fl, by = kernel_work(T, R, H, I, r, k)
+    kernels = {}
+    for name, (tot, n) in prof.items():
+        avg = tot / n
+        e = {"ms": round(avg, 4), "launches_per_step": n // args.steps, "share": None}
+        if name in fl:
+            e["tflops"] = round(fl[name] / (avg * 1e-3) / 1e12, 1)
+        elif name in by:
+            e["gbs"] = round(by[name] / (avg * 1e-3) / 1e9, 1)
+        kernels[name] = e
+    tot_all = sum(t for t, _ in prof.values())
+    for name, (tot, n) in prof.items():
+        kernels[name]["share"] = round(tot / tot_all, 4)
+    dom = max((n for n in prof if n in fl), key=lambda n: prof[n][0])
+    dom_ms = prof[dom][0] / prof[dom][1]
+    achieved = fl[dom] / (dom_ms * 1e-3) / 1e12
+    gemm_ms = sum(prof[n][0] for n in prof if n in fl) / args.steps
+    gemm_flops = sum(fl[n] for n in prof if n in fl)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["bf16_sus"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sus"], 4), "traffic": traffic_for(dom),
+                "peak_kind": f"bf16 dense, sustained ({pk['source']})",
+                "grouped_gemms_tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
+                "grouped_gemms_frac_of_burst_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 / pk["bf16"], 4)}
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    h_in = [t.cpu().pin_memory() for t in args_dev]
+    d_in = [torch.empty_like(t) for t in args_dev]
+    outs = [y, dx, dw] + [g[n] for n in ADAPTER_GRADS]
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for hd, dd in zip(h_in, d_in):
+            dd.copy_(hd, non_blocking=True)
+        step(*d_in)
+        for o, ho in zip(outs, h_out):
+            ho.copy_(o, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    e2e = {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    # ---- CPU oracle baseline (rank 0, single GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del ws
+        torch.cuda.empty_cache()
+        host = {n: v.cpu() for n, v in inp.items()}
+        v, info = oracle_sample(host, shp, args.cpu_seconds)
+        cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
+               "sample": f"first {info['tokens']} tokens ({info['routes']} routes) of the same workload, "
+                         f"forward+backward, {info['seconds']:.1f} s, plain C FP32 oracle with OpenMP"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and distributions of the pages' workload)",
+            "config": {"workload": f"{args.workload}: T={T} H={H} I={I} E={E} top{k} r={r} s={shp.scale}, "
+                                   f"fwd+bwd incl. routing plan",
+                       "tokens_per_gpu": T, "live_routes_per_gpu": R, "tflop_per_step_per_gpu": round(flops / 1e12, 3),
+                       "pct_of_bf16_peak": round(100 * value / world / pk["bf16"], 2),
+                       "parallelism": "replicas only (one independent batch per GPU, no collectives)",
+                       "l2": "inputs larger than L2 (12.9 GB frozen weights), no flush"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk, "kernels": kernels,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is a bounded sample
+    (the first tokens of the same workload) of forward + backward."""
+    if rank != 0:
+        return
+    shp = shape(args.workload)
+    host = host_inputs(shp, seed=2)
+    per_step = max(1.0, args.cpu_seconds / 3)
+    import oracle
+    oracle.build()
+    # size one step's sample once (calibration is not timed)
+    _, info = oracle_sample(host, shp, per_step)
+    n = info["tokens"]
+    toks = list(range(n))
+    R = int((host["topk_ids"][:n] >= 0).sum())
+    fl = step_flops(n, R, shp.H, shp.I, shp.r)
+    for _ in range(args.warmup):
+        oracle.forward(host, shp, tokens=toks[:2])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(host, shp, tokens=toks)
+        oracle.backward(host, shp, tokens=toks)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = fl / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; same inputs as our arm)",
+            "config": {"workload": f"{args.workload}: first {n} tokens per step ({R} routes), "
+                                   f"T={shp.T} H={shp.H} I={shp.I} E={shp.E} top{shp.k} r={shp.r}"},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"first {n} tokens of the workload per step, forward+backward"},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prod", choices=["prod", "prod_e16", "tiny", "edge"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

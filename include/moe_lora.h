@@ -161,6 +161,19 @@ MOE_LORA_API int moe_lora_plan_readback(const moe_lora_dims* dims, const void* p
                                         int32_t* offsets, int32_t* row_of_route, int32_t* route_of_row,
                                         int64_t route_of_row_cap, void* stream);
 
+/* Per-kernel timing of this library's own launches, for profiling and the
+ * benchmark's roofline figures (off by default).  When on, every kernel launch is
+ * bracketed by a CUDA event pair recorded on its launch stream. */
+MOE_LORA_API int moe_lora_profile_enable(int on);
+/* Reads and resets the per-kernel totals since the last read: for each kernel
+ * that ran (at most cap), its static name, total milliseconds and launch count.
+ * Waits for the recorded events.  Returns how many entries were written, or a
+ * negative MOE_LORA_ERR_* code. */
+MOE_LORA_API int moe_lora_profile_read(const char** names, double* total_ms, int64_t* launches, int cap);
+/* Kernel launches issued by this library since the last reset (always counted);
+ * reset != 0 returns the count and sets it to zero. */
+MOE_LORA_API int64_t moe_lora_launch_count(int reset);
+
 /* Static description of a return code. */
 MOE_LORA_API const char* moe_lora_strerror(int code);
 

@@ -79,6 +79,12 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_gemm_selftest.restype = ctypes.c_int
         L.moe_lora_gemm_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32, P,
                                              ctypes.c_int32, P, P]
+        L.moe_lora_profile_enable.restype = ctypes.c_int
+        L.moe_lora_profile_enable.argtypes = [ctypes.c_int]
+        L.moe_lora_profile_read.restype = ctypes.c_int
+        L.moe_lora_profile_read.argtypes = [P, P, P, ctypes.c_int]
+        L.moe_lora_launch_count.restype = ctypes.c_int64
+        L.moe_lora_launch_count.argtypes = [ctypes.c_int]
         L.moe_lora_gemm_selftest_error.restype = ctypes.c_int
         L.moe_lora_gemm_selftest_error.argtypes = [P]
         _lib = L
@@ -198,6 +204,27 @@ def moe_lora_gemm_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor, b_mn: b
 
 def moe_lora_gemm_selftest_error(stream=None) -> int:
     return lib().moe_lora_gemm_selftest_error(_stream(stream))
+
+
+def moe_lora_profile_enable(on: bool) -> None:
+    lib().moe_lora_profile_enable(1 if on else 0)
+
+
+def moe_lora_profile_read() -> Dict[str, tuple]:
+    """{kernel name: (total ms, launches)} since the last read (then reset)."""
+    cap = 64
+    names = (ctypes.c_char_p * cap)()
+    ms = (ctypes.c_double * cap)()
+    cnt = (ctypes.c_int64 * cap)()
+    n = lib().moe_lora_profile_read(ctypes.cast(names, ctypes.c_void_p), ctypes.cast(ms, ctypes.c_void_p),
+                                    ctypes.cast(cnt, ctypes.c_void_p), cap)
+    if n < 0:
+        raise MoeLoraError(n, "moe_lora_profile_read")
+    return {names[i].decode(): (ms[i], int(cnt[i])) for i in range(n)}
+
+
+def moe_lora_launch_count(reset: bool = False) -> int:
+    return int(lib().moe_lora_launch_count(1 if reset else 0))
 
 
 # ------------------------------------------------------------------ convenience

@@ -63,7 +63,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.dyB2 = dyB2;
     p.H = d->H;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_tok_tiles, num_sms, stream));
+    LAUNCH(launch_gemm(p, max_tok_tiles, num_sms, stream, K_DYB2));
   }
   // B1b: dB2 = s dy^T Z2w
   {
@@ -76,7 +76,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, d->A * (d->H / 128), num_sms, stream));
+    LAUNCH(launch_gemm(p, d->A * (d->H / 128), num_sms, stream, K_DB2));
   }
   // B2: routed dy rows and the scaled shared-expand gradients
   LAUNCH(launch_gather_bwd(pl, dy, dyB2, topk_w, Dp, D2p, dZ2p, d->H, d->r, d->scale, num_sms, stream));
@@ -99,7 +99,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream));
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream, K_W2_DGRAD));
   }
   LAUNCH(launch_dw(pl, part, d->I / 256, dw, num_sms, stream));
   // dA2 per (adapter, expert)
@@ -112,7 +112,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.dA2 = gr->dA2;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, (int)G * (d->I / 256), num_sms, stream));
+    LAUNCH(launch_gemm(p, (int)G * (d->I / 256), num_sms, stream, K_DA2));
   }
   // B5: W13^T dgrad + B1/B3 path
   {
@@ -131,7 +131,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.I = d->I;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream));
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W13_DGRAD));
   }
   // dB1 / dB3 per (adapter, expert)
   {
@@ -145,7 +145,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.dB3 = gr->dB3;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, 2 * (int)G * (d->I / 128), num_sms, stream));
+    LAUNCH(launch_gemm(p, 2 * (int)G * (d->I / 128), num_sms, stream, K_DB13));
   }
   // B6a: per-token sum of the shared-shrink gradients
   LAUNCH(launch_dy13w(pl, dY13, dY13w, 2 * d->r, num_sms, stream));
@@ -161,7 +161,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.dx = dx;
     p.H = d->H;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream));
+    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_GRADX));
   }
   // dA1 / dA3 per adapter
   {
@@ -174,7 +174,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.dA3 = gr->dA3;
     p.H = d->H;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, d->A * ((2 * d->r + 127) / 128) * (d->H / 256), num_sms, stream));
+    LAUNCH(launch_gemm(p, d->A * ((2 * d->r + 127) / 128) * (d->H / 256), num_sms, stream, K_DA13));
   }
 #undef MAP
 #undef LAUNCH

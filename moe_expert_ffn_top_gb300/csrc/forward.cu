@@ -56,7 +56,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, max_tok_tiles, num_sms, stream));
+    LAUNCH(launch_gemm(p, max_tok_tiles, num_sms, stream, K_SHRINK));
   }
   // F2: routed rows
   LAUNCH(launch_gather_fwd(pl, x, Y13, Xp, Y13p, d->H, 2 * d->r, num_sms, stream));
@@ -77,7 +77,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream));
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13));
   }
   // F4/F5: W2 + expert-local A2 shrink
   {
@@ -92,7 +92,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream));
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W2));
   }
   // F6a: per-token weighted sum of the A2 shrink
   LAUNCH(launch_z2w(pl, Z2, topk_w, Z2w, d->r, num_sms, stream));
@@ -109,7 +109,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream));
+    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_COMBINE));
   }
 #undef MAP
 #undef LAUNCH

@@ -28,6 +28,7 @@
 //   B MN-major: N/64 boxes of 64 K-rows x 64 N, 8 KB apart
 #pragma once
 #include "common.cuh"
+#include "prof.h"
 #include "sm100_ptx.cuh"
 
 namespace moelora {
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 // Host launch: one CTA per SM (or fewer if the problem has fewer tiles).
 template <class P>
-cudaError_t launch_gemm(const P& p, int max_tiles, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemm(const P& p, int max_tiles, int num_sms, cudaStream_t stream, int slot) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
@@ -202,7 +203,9 @@ cudaError_t launch_gemm(const P& p, int max_tiles, int num_sms, cudaStream_t str
   }
   if (max_tiles <= 0) return cudaSuccess;
   const int grid = max_tiles < num_sms ? max_tiles : num_sms;
+  prof_begin(slot, stream);
   gemm_kernel<P><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  prof_end(slot, stream);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,7 @@
 // routes of a token (fixed slot order, fp32, one bf16 rounding).
 // All use 16-byte vector accesses, one warp per row, grid-stride over rows.
 #include "launch.h"
+#include "prof.h"
 
 namespace moelora {
 
@@ -119,32 +120,42 @@ int grid_for(int num_sms) { return num_sms * 8; }
 
 cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint16_t* Xp,
                               uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream) {
+  prof_begin(K_GATHER_FWD, stream);
   gather_fwd_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, x, Y13, Xp, Y13p, H, r2);
+  prof_end(K_GATHER_FWD, stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_z2w(const PlanView& pl, const uint16_t* Z2, const float* topk_w, uint16_t* Z2w, int r,
                        int num_sms, cudaStream_t stream) {
+  prof_begin(K_Z2W, stream);
   z2w_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, Z2, topk_w, Z2w, r);
+  prof_end(K_Z2W, stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gather_bwd(const PlanView& pl, const uint16_t* dy, const uint16_t* dyB2, const float* topk_w,
                               uint16_t* Dp, uint16_t* D2p, uint16_t* dZ2p, int H, int r, float s, int num_sms,
                               cudaStream_t stream) {
+  prof_begin(K_GATHER_BWD, stream);
   gather_bwd_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, dy, dyB2, topk_w, Dp, D2p, dZ2p, H, r, s);
+  prof_end(K_GATHER_BWD, stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dw(const PlanView& pl, const float* part, int nparts, float* dw, int num_sms,
                       cudaStream_t stream) {
+  prof_begin(K_DW, stream);
   dw_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, part, nparts, dw);
+  prof_end(K_DW, stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dy13w(const PlanView& pl, const float* dY13, uint16_t* dY13w, int r2, int num_sms,
                          cudaStream_t stream) {
+  prof_begin(K_DY13W, stream);
   dy13w_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, dY13, dY13w, r2);
+  prof_end(K_DY13W, stream);
   return cudaGetLastError();
 }
 

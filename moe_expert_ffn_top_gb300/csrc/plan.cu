@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "prof.h"
 
 namespace moelora {
 
@@ -170,17 +171,26 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
     if (e != cudaSuccess) return e;
   }
   if (nchunks > 0) {
+    prof_begin(K_PLAN_COUNT, stream);
     plan_count<<<nchunks, 32, hist_bytes, stream>>>(ids, TK, d->k, d->E, G, at, chunk_base, nchunks, err);
+    prof_end(K_PLAN_COUNT, stream);
   } else {
     e = cudaMemsetAsync(chunk_base, 0, sizeof(int) * (size_t)G, stream);
     if (e != cudaSuccess) return e;
   }
+  prof_begin(K_PLAN_SCAN, stream);
   plan_scan<<<1, 1024, 0, stream>>>(chunk_base, nchunks > 0 ? nchunks : 1, G, counts, offsets);
-  if (nchunks > 0)
+  prof_end(K_PLAN_SCAN, stream);
+  if (nchunks > 0) {
+    prof_begin(K_PLAN_SCATTER, stream);
     plan_scatter<<<nchunks, 32, hist_bytes, stream>>>(ids, TK, d->k, d->E, G, at, chunk_base, offsets, nchunks,
                                                       row_of_route, route_of_row, err);
+    prof_end(K_PLAN_SCATTER, stream);
+  }
+  prof_begin(K_PLAN_FINISH, stream);
   plan_finish<<<G < 1024 ? G : 1024, 128, 0, stream>>>(G, counts, offsets, route_of_row, tile_group, at, tok_off,
                                                        tok_tile);
+  prof_end(K_PLAN_FINISH, stream);
   return cudaGetLastError();
 }
 

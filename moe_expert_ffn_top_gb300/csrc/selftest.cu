@@ -27,7 +27,7 @@ static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, floa
   p.N = N;
   p.K = K;
   const int tiles = M / 128 * ((N + 255) / 256);
-  return launch_gemm(p, tiles, num_sms, stream) == cudaSuccess ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
+  return launch_gemm(p, tiles, num_sms, stream, K_SELFTEST) == cudaSuccess ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
 }
 
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,

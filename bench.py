@@ -186,9 +186,14 @@ def oracle_sample(inp_cpu, shp, seconds_target, max_tokens=512):
         dt = time.perf_counter() - t0
         return dt, step_flops(n, R, shp.H, shp.I, shp.r), R
 
-    dt, fl, R = run(2)
-    n = int(min(max_tokens, max(2, 2 * seconds_target / max(dt, 1e-3))))
+    n = 4
     dt, fl, R = run(n)
+    while dt < seconds_target / 8 and n < max_tokens:
+        n = min(max_tokens, 2 * n)
+        dt, fl, R = run(n)
+    if dt < seconds_target / 2 and n < max_tokens:
+        n = int(min(max_tokens, n * seconds_target / max(dt, 1e-3)))
+        dt, fl, R = run(n)
     return fl / dt / 1e12, {"tokens": n, "routes": R, "seconds": dt, "cores": cores, "flops": fl}
 
 

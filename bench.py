@@ -88,13 +88,17 @@ def kernel_work(T, R, H, I, r, k):
     return fl, by
 
 
+# Sources that define the grouped-GEMM kernels and their launch configuration:
+# a change to any of them invalidates committed DRAM-traffic counters.
+GEMM_SOURCES = ("sm100_ptx.cuh", "common.cuh", "gemm_engine.cuh", "gemm_problems.cuh", "forward.cu", "backward.cu")
+
+
 def src_hash():
     h = hashlib.sha256()
-    for d in (os.path.join(ROOT, "moe_expert_ffn_top_gb300", "csrc"), os.path.join(ROOT, "include")):
-        for f in sorted(os.listdir(d)):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "moe_expert_ffn_top_gb300", "csrc", f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -8,7 +8,7 @@
  *     h = silu(gate) * up,                    down = h W2_e^T + s (h A2_e^T) B2^T,
  * and the routing-weighted sum of the k down rows is the output.  A1/A3 [r,H]
  * and B2 [H,r] are shared by all experts; B1_e/B3_e [I,r] and A2_e [r,I] are
- * expert-local ("W1/W3 share A, W2 shares B; B1/B3/A2 remain expert-local").
+ * expert-local (the shared-factor contract of that Summary).
  * The frozen W1/W2/W3 receive no gradient; the backward returns grad-x, the
  * router-weight gradient and the six adapter gradients (same PR, Summary).
  *
@@ -19,14 +19,14 @@
  *   - The caller owns and allocates every buffer; the library never allocates,
  *     frees or synchronises the stream.  Inputs are read only.  Outputs are fully
  *     overwritten (never accumulated into), so buffers may be reused across calls
- *     (PR #9, Correctness coverage: "reusable output/source buffers").
+ *     (PR #9, Correctness coverage, lists buffer reuse among the tested cases).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work of a
  *     call is enqueued on it; nothing returns to the host in between.
  *   - Return value: 0 on success.  A negative code means the call was rejected on
  *     the host BEFORE any launch (bad shape, NULL or misaligned pointer, short
  *     workspace, unsupported option), in the spirit of PR #9's fail-fast checks
- *     ("reject unsupported post-down side-LoRA and undersized scratch before
- *     launching kernels").  MOE_LORA_ERR_CUDA means a launch failed.  Problems
+ *     (Summary: unsupported placements and short scratch are refused before any
+ *     kernel starts).  MOE_LORA_ERR_CUDA means a launch failed.  Problems
  *     only the device can see (an expert id out of range, a pipeline wait that
  *     timed out) set bits in a sticky device error word read by
  *     moe_lora_get_error().
@@ -116,11 +116,10 @@ typedef struct moe_lora_grads {
  * T*k + A*E*(block_m-1)), so no device value is ever read back. */
 MOE_LORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims* dims, int which);
 
-/* Routing plan ("routing-plan construction", excluded from the pages' timing,
- * PR #9, Scope).  A stable counting sort of the live routes by
+/* Routing plan (PR #9 leaves plan construction out of its timed scope).  A stable counting sort of the live routes by
  * (adapter, expert, token, slot); each group's rows are padded to a multiple of
- * block_m and padding rows map to no route (PR #9, Implementation: "keep true
- * physical expert offsets; do not round group starts into neighboring experts").
+ * block_m and padding rows map to no route; every group starts at its own padded
+ * offset, never rounded into a neighbouring expert (PR #9, Implementation).
  *   topk_ids         [T,k] int32, device.  -1 = masked route (not dispatched).
  *                    Ids >= E or < -1 are dropped and flagged MOE_LORA_DEV_BAD_ID.
  *   adapter_offsets  [A+1] int64, HOST.  Tokens of adapter a are

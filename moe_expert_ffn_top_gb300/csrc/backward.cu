@@ -1,6 +1,6 @@
-// Backward pass of the routed MoE side-LoRA FFN ("a native backward that returns
-// grad-x, router gradients, and all six adapter gradients without frozen W1/W2/W3
-// gradients", "feat(mega): add fused shared side-LoRA kernels", Summary).
+// Backward pass of the routed MoE side-LoRA FFN: the input gradient, the
+// routing-weight gradient and all six factor gradients, nothing for the frozen
+// base weights ("feat(mega): add fused shared side-LoRA kernels", Summary).
 // Launch sequence, one stream, no host synchronisation:
 //   B1a dyB2 = dy B2 (per token)      B1b dB2 = s dy^T Z2w
 //   B2  gather dy rows, s*dyB2, s*w*dyB2 (zero padding)

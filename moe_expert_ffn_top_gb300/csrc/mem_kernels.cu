@@ -1,7 +1,7 @@
 // HBM-bound kernels of the MoE side-LoRA path: routed-row gathers (with zeroed
-// padding rows, so allocator garbage can never reach a shared reduction --
-// "feat(mega): add fused shared side-LoRA kernels", Summary: "zeroing expert
-// padding ... before shared contractions") and per-token reductions over the k
+// padding rows, so allocator garbage can never reach a shared reduction, the
+// padding rule of "feat(mega): add fused shared side-LoRA kernels", Summary) and
+// per-token reductions over the k
 // routes of a token (fixed slot order, fp32, one bf16 rounding).
 // All use 16-byte vector accesses, one warp per row, grid-stride over rows.
 #include "launch.h"

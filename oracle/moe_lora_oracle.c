@@ -5,9 +5,11 @@
  * from the product path.  It shares no code with the CUDA library.
  *
  * What it computes (the method of "feat(mega): add fused shared side-LoRA kernels",
- * DeepGEMM PR #9, Summary: "W1/W3 share A, W2 shares B; B1/B3/A2 remain expert-local",
- * frozen W1/W2/W3 receive no gradient), per token t and per unmasked slot j with
- * expert e = ids[t,j] and adapter a = adapter(t):
+ * DeepGEMM PR #9, Summary: the down-projection factors A1/A3 of the gate and up
+ * projections and the up-projection factor B2 of the down projection are common to
+ * all experts, while B1, B3 and A2 belong to each expert; the base weights W1/W2/W3
+ * are frozen), per token t and per unmasked slot j with expert e = ids[t,j] and
+ * adapter a = adapter(t):
  *
  *   y1 = rb(A1_a x_t)            y3 = rb(A3_a x_t)                       [r]
  *   g  = W1_e x_t + s B1_{a,e} y1      u = W3_e x_t + s B3_{a,e} y3      [I]
@@ -22,13 +24,14 @@
  * The backward is the exact reverse-mode derivative of the above with rb treated
  * as the identity: grad-x, the router-weight gradient dL/dw_tj = <dy_t, o_j>
  * (the "grad-route" of PR #9, Correctness coverage) and the six adapter gradients
- * dA1, dA3, dB1, dB3, dA2, dB2 (PR #9, Summary: "a native backward that returns
- * grad-x, router gradients, and all six adapter gradients without frozen W1/W2/W3
- * gradients").  Adapter gradients are summed in (token, slot) order.
+ * dA1, dA3, dB1, dB3, dA2, dB2 (PR #9, Summary: the backward yields the input
+ * gradient, the routing-weight gradient and all six factor gradients, and nothing
+ * for the frozen base weights).  Adapter gradients are summed in (token, slot) order.
  *
  * The routing plan is a stable counting sort of the live routes by
  * (adapter, expert, token, slot), each group padded to a multiple of BLOCK_M rows
- * (pool padding of PR #9, Implementation: "keep true physical expert offsets").
+ * (pool padding of PR #9, Implementation: each expert's rows start at its own
+ * padded offset, never rounded into a neighbour).
  *
  * MXFP4 base weights: E2M1 element codes (1 sign, 2 exponent with bias 1,
  * 1 mantissa bit) with one UE8M0 scale 2^(b-127) per 32 contiguous elements along

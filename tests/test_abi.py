@@ -1,7 +1,7 @@
 """C-ABI checks that need no GPU: the library builds and loads, exports every
 entry point include/moe_lora.h declares, sizes workspaces, and rejects bad calls
-on the host before any launch (the pages' fail-fast rule: "reject unsupported
-post-down side-LoRA and undersized scratch before launching kernels",
+on the host before any launch (the pages' fail-fast rule: unsupported side-LoRA
+placements and too-small scratch are refused before a kernel starts,
 "feat(mega): add fused shared side-LoRA kernels", Summary)."""
 import ctypes
 import os

@@ -210,7 +210,7 @@ def _sparse_dy(inp, shp, sample):
 
 @pytest.mark.parametrize("T", EDGE_TOKEN_COUNTS)
 def test_edge_sweep_production_width(T):
-    """H=4096, I=2048, E=256, top-6, rank 128, 20% masked routes, experts 0/127/255
+    """H=4096, I=2048, E=256, top-6, rank 128, a fifth of the routes masked, experts 0/127/255
     empty, at the 15 token counts of the pages' boundary sweep."""
     shp = shape("edge", T)
     inp = make_inputs(shp, seed=1000 + T, device="cuda")

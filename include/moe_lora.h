@@ -56,6 +56,7 @@ extern "C" {
 #define MOE_LORA_ERR_UNSUPPORTED (-5) /* activation / base format not supported */
 #define MOE_LORA_ERR_CUDA (-6)        /* a CUDA call or kernel launch failed */
 #define MOE_LORA_ERR_DEVICE (-7)      /* current device is not an sm_103 GPU */
+#define MOE_LORA_ERR_SCRATCH_LIMIT (-8) /* sizes exceed moe_lora_plan_noalloc's fixed scratch */
 
 /* ---- device error word bits (moe_lora_get_error) ---- */
 #define MOE_LORA_DEV_BAD_ID 1         /* an id >= E or < -1 was seen and dropped */
@@ -130,6 +131,29 @@ MOE_LORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims* dims, int whic
  * Also clears the device error word. */
 MOE_LORA_API int moe_lora_plan(const moe_lora_dims* dims, const int32_t* topk_ids, const int64_t* adapter_offsets,
                   void* plan_ws, size_t plan_bytes, void* stream);
+
+/* Routing plan for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers that may not call
+ * cudaMalloc (or any allocator) when they route tokens -- code running while a
+ * stream is being captured into a CUDA graph, memory-planned serving runtimes that
+ * only hand out pre-reserved buffers, C hosts without an allocator binding.
+ * It writes exactly the plan moe_lora_plan() writes, but the per-chunk expert
+ * histograms it needs as temporary space live in a fixed 4 MiB array inside the
+ * library (a file-scope __device__ array that every GPU loading the library holds
+ * until the process exits), so the caller passes only the plan buffer itself:
+ *   plan_bytes >= moe_lora_workspace_bytes(dims, MOE_LORA_WS_PLAN)
+ *                 - 256 * ceil(4 * A * E * ceil(T*k / 1024) / 256)
+ * (a full MOE_LORA_WS_PLAN buffer also works).  Sizes with
+ * A * E * ceil(T*k / 1024) > 1,048,576 are rejected with MOE_LORA_ERR_SCRATCH_LIMIT
+ * before any launch.  Nothing is allocated or freed.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture begins.
+ * All calls share the one array: calls whose work overlaps on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the caller.
+ * Other arguments, checks and errors are those of moe_lora_plan(). */
+MOE_LORA_API int moe_lora_plan_noalloc(const moe_lora_dims* dims, const int32_t* topk_ids,
+                                       const int64_t* adapter_offsets, void* plan_ws, size_t plan_bytes,
+                                       void* stream);
 
 /* Forward.  x [T,H] bf16; topk_w [T,k] fp32 routing weights (masked slots are
  * ignored); y [T,H] bf16 output.  `saved` receives what the backward needs

@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
                                         ctypes.POINTER(Grads), P, ctypes.c_size_t, P]
         L.moe_lora_get_error.restype = ctypes.c_int
         L.moe_lora_get_error.argtypes = [ctypes.POINTER(Dims), P, P]
+        L.moe_lora_plan_noalloc.restype = ctypes.c_int
+        L.moe_lora_plan_noalloc.argtypes = [ctypes.POINTER(Dims), P, P, P, ctypes.c_size_t, P]
         L.moe_lora_plan_readback.restype = ctypes.c_int
         L.moe_lora_plan_readback.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, ctypes.c_int64, P]
         L.moe_lora_strerror.restype = ctypes.c_char_p
@@ -137,6 +139,21 @@ def moe_lora_plan(dims: Dims, topk_ids: torch.Tensor, adapter_offsets: Optional[
                              _ptr(plan_ws, None, "plan_ws"), plan_ws.numel() * plan_ws.element_size(),
                              _stream(stream))
     _check(rc, "moe_lora_plan")
+
+
+def moe_lora_plan_noalloc(dims: Dims, topk_ids: torch.Tensor, adapter_offsets: Optional[Sequence[int]],
+                          plan_ws: torch.Tensor, plan_bytes: Optional[int] = None, stream=None) -> None:
+    """The routing plan without caller-provided temporary space (see the C header):
+    plan_ws only needs to hold the plan itself."""
+    offs = None
+    if adapter_offsets is not None:
+        vals = [int(v) for v in adapter_offsets]
+        offs = (ctypes.c_int64 * len(vals))(*vals)
+    nbytes = plan_ws.numel() * plan_ws.element_size() if plan_bytes is None else plan_bytes
+    rc = lib().moe_lora_plan_noalloc(ctypes.byref(dims), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                     ctypes.cast(offs, ctypes.c_void_p) if offs is not None else None,
+                                     _ptr(plan_ws, None, "plan_ws"), nbytes, _stream(stream))
+    _check(rc, "moe_lora_plan_noalloc")
 
 
 def moe_lora_plan_readback(dims: Dims, plan_ws: torch.Tensor, stream=None) -> Dict[str, torch.Tensor]:

@@ -227,6 +227,7 @@ const char* moe_lora_strerror(int code) {
     case MOE_LORA_ERR_UNSUPPORTED: return "unsupported activation or base format";
     case MOE_LORA_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case MOE_LORA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case MOE_LORA_ERR_SCRATCH_LIMIT: return "sizes exceed the fixed scratch of moe_lora_plan_noalloc";
     default: return "unknown error";
   }
 }

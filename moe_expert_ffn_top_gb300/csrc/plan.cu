@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "plan_kernels.h"
 #include "prof.h"
 
 namespace moelora {

@@ -67,22 +67,24 @@ def kernel_work(T, R, H, I, r, k):
         "shrink_x_A13": 2.0 * T * H * 2 * r,
         "w13_lora_swiglu": 4.0 * R * H * I + 4.0 * R * I * r,
         "w2_a2": 2.0 * R * I * H + 2.0 * R * I * r,
-        "b2_expand_combine": 2.0 * T * r * H,
+        "b2_expand": 2.0 * T * r * H,
         "dy_b2": 2.0 * T * H * r,
         "dB2": 2.0 * T * H * r,
         "w2_dgrad_swiglu_bwd": 2.0 * R * H * I + 2.0 * R * r * I,
         "dA2": 2.0 * R * r * I,
         "w13_dgrad_b13": 4.0 * R * I * H + 4.0 * R * I * r,
         "dB13": 4.0 * R * I * r,
-        "gradx_a13_combine": 4.0 * T * r * H,
+        "a13_expand": 4.0 * T * r * H,
         "dA13": 4.0 * T * r * H,
     }
     by = {
         "gather_fwd": 2.0 * (2 * R * H + 2 * R * 2 * r),
         "z2_combine": 2.0 * (R * r + T * r),
         "gather_bwd": 2.0 * (2 * R * H + 3 * R * r),
-        "dw_reduce": 4.0 * (R * (I // 256) + T * k),
+        "dw_reduce": 4.0 * (R * (I // 128) + T * k),
         "dy13_combine": 4.0 * R * 2 * r + 2.0 * T * 2 * r,
+        "combine_y": 2.0 * (R * H + 2 * T * H),
+        "combine_dx": 2.0 * (R * H + 2 * T * H),
         "plan_count": 4.0 * T * k, "plan_scan": 0.0, "plan_scatter": 4.0 * T * k * 3, "plan_finish": 0.0,
     }
     return fl, by

@@ -7,7 +7,8 @@
 //   B3  W2^T dgrad + A2 path + SwiGLU backward + router partial dots
 //       dw reduce;  dA2 (K-grouped per expert)
 //   B5  W13^T dgrad + B1/B3 path;  dB1/dB3 (K-grouped per expert)
-//   B6a per-token sum of dY13;  B6 grad-x (A1/A3 path + combine);  dA1/dA3
+//   B6a per-token sum of dY13;  B6 grad-x (A1/A3 path per token, then the source
+//       combine of the routed dXp rows);  dA1/dA3
 #include "gemm_problems.cuh"
 #include "launch.h"
 #include "passes.h"
@@ -38,6 +39,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   float* part = (float*)(sc + BL.part);
   float* dY13 = (float*)(sc + BL.dY13);
   uint16_t* dY13w = (uint16_t*)(sc + BL.dY13w);
+  uint16_t* dXl = (uint16_t*)(sc + BL.dXl);
 
   const uint64_t T = (uint64_t)d->T, H = d->H, I = d->I, E = d->E, A = d->A, r = d->r;
   const uint64_t P = (uint64_t)rows_cap(d), G = A * E;
@@ -101,7 +103,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.r = d->r;
     LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream, K_W2_DGRAD));
   }
-  LAUNCH(launch_dw(pl, part, d->I / 256, dw, num_sms, stream));
+  LAUNCH(launch_dw(pl, part, d->I / 128, dw, num_sms, stream));
   // dA2 per (adapter, expert)
   {
     ProbDA2 p;
@@ -149,20 +151,20 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   }
   // B6a: per-token sum of the shared-shrink gradients
   LAUNCH(launch_dy13w(pl, dY13, dY13w, 2 * d->r, num_sms, stream));
-  // B6: grad-x
+  // B6: grad-x through the shared A1/A3 per token, then the source combine of dXp
   {
-    ProbGradX p;
+    ProbA13Expand p;
     MAP(tmap_2d(&p.mdY13w, dY13w, 2 * r, T, 64, 128));
     MAP(tmap_3d(&p.mA1, w->A1, H, r, A, 64, 64));
     MAP(tmap_3d(&p.mA3, w->A3, H, r, A, 64, 64));
     p.pl = pl;
     p.err = pl.err;
-    p.dXp = dXp;
-    p.dx = dx;
+    p.dXl = dXl;
     p.H = d->H;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_GRADX));
+    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_A13_EXPAND));
   }
+  LAUNCH(launch_combine_rows(pl, dXl, dXp, nullptr, dx, d->H, num_sms, stream, K_COMBINE_DX));
   // dA1 / dA3 per adapter
   {
     ProbDA13 p;

@@ -99,8 +99,9 @@ inline FwdLayout fwd_layout(const moe_lora_dims* d) {
 
 struct BwdLayout {
   // dyB2 [T,r] bf16; Dp [P,H] bf16 (reused for dXp); D2p, dZ2p [P,r] bf16;
-  // dG, dU [P,I] bf16; part [P, I/256] f32; dY13 [P,2r] f32; dY13w [T,2r] bf16
-  size_t dyB2, Dp, D2p, dZ2p, dG, dU, part, dY13, dY13w, total;
+  // dG, dU [P,I] bf16; part [P, I/128] f32; dY13 [P,2r] f32; dY13w [T,2r] bf16;
+  // dXl [T,H] bf16 (grad-x through A1/A3)
+  size_t dyB2, Dp, D2p, dZ2p, dG, dU, part, dY13, dY13w, dXl, total;
 };
 inline BwdLayout bwd_layout(const moe_lora_dims* d) {
   BwdLayout L;
@@ -113,9 +114,10 @@ inline BwdLayout bwd_layout(const moe_lora_dims* d) {
   L.dZ2p = take(2 * (size_t)P * d->r);
   L.dG = take(2 * (size_t)P * d->I);
   L.dU = take(2 * (size_t)P * d->I);
-  L.part = take(4 * (size_t)P * (d->I / 256));
+  L.part = take(4 * (size_t)P * (d->I / 128));
   L.dY13 = take(4 * (size_t)P * 2 * d->r);
   L.dY13w = take(2 * (size_t)T * 2 * d->r);
+  L.dXl = take(2 * (size_t)T * d->H);
   L.total = o;
   return L;
 }

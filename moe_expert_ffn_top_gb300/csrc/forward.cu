@@ -2,7 +2,7 @@
 // sequence, all on one stream with no host synchronisation.
 //   F1 shrink (per token)  ->  F2 gather (routed rows, zero padding)
 //   F3 W13 + B1/B3 expand + SwiGLU  ->  F4 W2 + A2 shrink
-//   F6a per-token Z2 combine  ->  F6 B2 expand + routing-weighted combine
+//   F6a per-token Z2 combine  ->  F6 B2 expand per token  ->  routing-weighted combine
 #include "gemm_problems.cuh"
 #include "launch.h"
 #include "passes.h"
@@ -96,21 +96,22 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   }
   // F6a: per-token weighted sum of the A2 shrink
   LAUNCH(launch_z2w(pl, Z2, topk_w, Z2w, d->r, num_sms, stream));
-  // F6: shared B2 expand + combine
+  // F6: shared B2 expand per token (into the dead Xp buffer), then the
+  // routing-weighted combine of the routed rows on top of it
+  uint16_t* Yl = Xp;
   {
-    ProbCombine p;
+    ProbB2Expand p;
     MAP(tmap_2d(&p.mZ2w, Z2w, r, T, 64, 128));
     MAP(tmap_3d(&p.mB2, w->B2, r, H, A, 64, 256));
     p.pl = pl;
     p.err = pl.err;
-    p.O = O;
-    p.topk_w = topk_w;
-    p.y = y;
+    p.Yl = Yl;
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_COMBINE));
+    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_B2_EXPAND));
   }
+  LAUNCH(launch_combine_rows(pl, Yl, O, topk_w, y, d->H, num_sms, stream, K_COMBINE_Y));
 #undef MAP
 #undef LAUNCH
   (void)rc;

@@ -2,7 +2,9 @@
 //
 //   warp 0 (one lane)  : TMA producer, fills a kStages-deep ring of (A, B) tiles
 //   warp 1 (one lane)  : tcgen05.mma issuer; also owns the TMEM allocation
-//   warps 2..5         : epilogue, one accumulator row (TMEM lane) per thread
+//   warps 2..          : P::kEpiWarps epilogue warps (4 or 8); warp w may read TMEM
+//                        lane quarter w%4 (one accumulator row per thread); with 8
+//                        warps, warps w and w+4 take alternate 32-column chunks
 //
 // Accumulators are 128 x 256 fp32 in tensor memory, double buffered (512
 // columns), so the epilogue of tile i overlaps the main loop of tile i+1.
@@ -12,14 +14,17 @@
 // problem type P (see gemm_problems.cuh):
 //
 //   static constexpr bool kAmn, kBmn;      operand majorness (true = MN-major)
+//   static constexpr int  kEpiWarps;       4 or 8 epilogue warps
 //   int*  err;                              device error word
 //   int      num_tiles() const;             read from device plan data
 //   TileInfo tile(int t) const;
 //   void     prefetch() const;              tensor-map prefetch
 //   void     load(const TileInfo&, int ks, uint8_t* sA, uint8_t* sB, uint64_t* bar) const;
 //   MmaStep  mma_step(const TileInfo&, int ks) const;
-//   void     epilogue(const TileInfo&, int row, uint32_t tmem_lane_addr) const;
-//   void     epilogue_empty(const TileInfo&, int row) const;   (tiles with nk == 0)
+//   void     epilogue(const TileInfo&, int row, uint32_t tmem_lane_addr, int half, int nh) const;
+//   void     epilogue_empty(const TileInfo&, int row, int half, int nh) const;   (tiles with nk == 0)
+// An epilogue warp handles the 32-column chunks c = 32*half, 32*(half + nh), ... of its
+// row, where nh = kEpiWarps / 4 warps share each TMEM lane quarter.
 //
 // Operand tiles in shared memory use the 128-byte swizzle written by TMA:
 //   A K-major : 128 rows x 128 B                         (one 16 KB box)
@@ -39,7 +44,8 @@ constexpr int kAStageBytes = 128 * 128;  // 16 KB
 constexpr int kBStageBytes = 256 * 128;  // 32 KB
 constexpr int kStageBytes = kAStageBytes + kBStageBytes;
 constexpr int kAccCols = 256;
-constexpr int kGemmThreads = 192;
+constexpr int kMaxEpiWarps = 8;
+constexpr int kGemmMaxThreads = 64 + 32 * kMaxEpiWarps;
 constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 + 256;
 
 struct TileInfo {
@@ -60,7 +66,9 @@ struct MmaStep {
 };
 
 template <class P>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ P p) {
+__global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const __grid_constant__ P p) {
+  static_assert(P::kEpiWarps == 4 || P::kEpiWarps == 8, "4 or 8 epilogue warps");
+  constexpr int kNh = P::kEpiWarps / 4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -78,7 +86,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], P::kEpiWarps);
     }
     fence_mbar_init();
   }
@@ -164,19 +172,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileInfo ti = p.tile(t);
       if (ti.nk == 0) {
-        p.epilogue_empty(ti, row);
+        p.epilogue_empty(ti, row, half, kNh);
         continue;
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, err));
       if (!ok) break;
       tc_fence_after();
-      p.epilogue(ti, row, tmem_base + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16));
+      p.epilogue(ti, row, tmem_base + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16), half, kNh);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -204,7 +213,7 @@ cudaError_t launch_gemm(const P& p, int max_tiles, int num_sms, cudaStream_t str
   if (max_tiles <= 0) return cudaSuccess;
   const int grid = max_tiles < num_sms ? max_tiles : num_sms;
   prof_begin(slot, stream);
-  gemm_kernel<P><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  gemm_kernel<P><<<grid, 64 + 32 * P::kEpiWarps, kGemmSmemBytes, stream>>>(p);
   prof_end(slot, stream);
   return cudaGetLastError();
 }

@@ -58,6 +58,7 @@ __device__ __forceinline__ int round16(int r) { return (r + 15) & ~15; }
 // =====================================================================================
 struct ProbShrink {
   static constexpr bool kAmn = false, kBmn = false;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mx, mA1, mA3;  // x (H,T) box(64,128); A1/A3 (H,r,A) box(64,r,1)
   PlanView pl;
   int* err;
@@ -89,17 +90,17 @@ struct ProbShrink {
     tma_load_3d(sb + r * 128, &mA3, bar, ks * kBK, 0, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{2 * r, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    for (int c = 0; c < 2 * r; c += 32) {
+    for (int c = 32 * half; c < 2 * r; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
       const int n = 2 * r - c < 32 ? 2 * r - c : 32;
       if (ok) store_row_bf16(Y13 + t * (2 * r) + c, v, s, n);
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
@@ -113,6 +114,7 @@ struct ProbShrink {
 // =====================================================================================
 struct ProbW13 {
   static constexpr bool kAmn = false, kBmn = false;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mXp, mY13p, mW1, mW3, mB1, mB3;  // Xp (H,P) box(64,128); Y13p (2r,P) box(64,128);
                                                // W1/W3 (H,I,E) box(64,128,1); B1/B3 (r,I,G) box(64,128,1)
   PlanView pl;
@@ -163,10 +165,10 @@ struct ProbW13 {
     const int half = (ks - nb) / nkr();
     return MmaStep{128, half * 128, 0, 0};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t p = (int64_t)ti.m0 + row;
     const int64_t base = p * I + ti.n0;
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 32 * half; c < 128; c += 32 * nh) {
       float g[32], u[32];
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
@@ -181,7 +183,7 @@ struct ProbW13 {
       }
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
@@ -191,6 +193,7 @@ struct ProbW13 {
 // =====================================================================================
 struct ProbW2 {
   static constexpr bool kAmn = false, kBmn = false;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mAct, mW2, mA2;  // Act (I,P) box(64,128); W2 (I,H,E) box(64,256,1); A2 (I,r,G) box(64,r16,1)
   PlanView pl;
   int* err;
@@ -229,38 +232,40 @@ struct ProbW2 {
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     return MmaStep{ti.sub ? round16(r) : 256, 0, 0, ks == 0};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t p = (int64_t)ti.m0 + row;
     if (!ti.sub) {
-      for (int c = 0; c < 256; c += 32) {
+      for (int c = 32 * half; c < 256; c += 32 * nh) {
         float v[32];
         tmem_ld32(taddr + c, v);
         store_row_bf16(O + p * H + ti.n0 + c, v, 1.0f, 32);
       }
     } else {
-      for (int c = 0; c < r; c += 32) {
+      for (int c = 32 * half; c < r; c += 32 * nh) {
         float v[32];
         tmem_ld32(taddr + c, v);
         store_row_bf16(Z2 + p * r + c, v, 1.0f, r - c < 32 ? r - c : 32);
       }
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
-// Forward F6 -- shared B2 expand fused with the routing-weighted combine:
-//   y_t = bf16( s * Z2w_t B2_a^T + sum_j w_tj O[row(t,j)] )   (slot order, fp32)
-// M = tokens of adapter a, N = H (tiles of 256), K = r.
+// Forward F6 (first half) -- shared B2 expand, once per token:
+//   Yl_t = bf16( s * Z2w_t B2_a^T )   [T,H]
+// M = tokens of adapter a, N = H (tiles of 256), K = r.  The routing-weighted sum
+// of the routed rows is added by combine_rows (mem_kernels.cu), which reads them
+// one whole row per warp: a TMEM-row-per-thread epilogue would touch 32 scattered
+// rows per warp instruction.
 // =====================================================================================
-struct ProbCombine {
+struct ProbB2Expand {
   static constexpr bool kAmn = false, kBmn = false;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mZ2w, mB2;  // Z2w (r,T) box(64,128); B2 (r,H,A) box(64,256,1)
   PlanView pl;
   int* err;
-  const uint16_t* O;
-  const float* topk_w;
-  uint16_t* y;
+  uint16_t* Yl;
   int H, r;
   float s;
   __device__ int ntn() const { return H / 256; }
@@ -288,38 +293,16 @@ struct ProbCombine {
     tma_load_3d(sb, &mB2, bar, ks * kBK, ti.n0, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    const int k = pl.k;
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 32 * half; c < 256; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      if (!ok) continue;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= s;
-      float acc[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        const int R = pl.row_of_route[t * k + j];
-        if (R < 0) continue;
-        const float w = topk_w[t * k + j];
-        const uint16_t* src = O + (int64_t)R * H + ti.n0 + c;
-#pragma unroll
-        for (int q = 0; q < 32; q += 8) {
-          float o[8];
-          ld_bf16x8(src + q, o);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[q + i] += w * o[i];
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] += acc[i];
-      store_row_bf16(y + t * H + ti.n0 + c, v, 1.0f, 32);
+      if (ok) store_row_bf16(Yl + t * H + ti.n0 + c, v, s, 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
@@ -328,6 +311,7 @@ struct ProbCombine {
 // =====================================================================================
 struct ProbDyB2 {
   static constexpr bool kAmn = false, kBmn = true;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mdy, mB2;  // dy (H,T) box(64,128); B2 (r,H,A) box(64,64,1)
   PlanView pl;
   int* err;
@@ -357,16 +341,16 @@ struct ProbDyB2 {
     for (int c = 0; c < nbox; ++c) tma_load_3d(sb + c * 8192, &mB2, bar, c * 64, ks * kBK, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    for (int c = 0; c < r; c += 32) {
+    for (int c = 32 * half; c < r; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_bf16(dyB2 + t * r + c, v, 1.0f, r - c < 32 ? r - c : 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
@@ -375,6 +359,7 @@ struct ProbDyB2 {
 // =====================================================================================
 struct ProbDB2 {
   static constexpr bool kAmn = true, kBmn = true;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mdy, mZ2w;  // dy (H,T) box(64,64); Z2w (r,T) box(64,64)
   PlanView pl;
   int* err;
@@ -407,18 +392,18 @@ struct ProbDB2 {
     for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mZ2w, bar, c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t h = (int64_t)ti.m0 + row;
-    for (int c = 0; c < r; c += 32) {
+    for (int c = 32 * half; c < r; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
       store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, v, s, r - c < 32 ? r - c : 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
     const float z[32] = {};
     const int64_t h = (int64_t)ti.m0 + row;
-    for (int c = 0; c < r; c += 32) store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, z, 0.f, r - c < 32 ? r - c : 32);
+    for (int c = 32 * half; c < r; c += 32 * nh) store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, z, 0.f, r - c < 32 ? r - c : 32);
   }
 };
 
@@ -426,11 +411,13 @@ struct ProbDB2 {
 // Backward B3/B4 -- W2^T dgrad with the A2 path, SwiGLU backward and router dots:
 //   Q  = Dp W2_e + D2p A2_ae              [P,I]   (D2p = s * dyB2 of the row's token)
 //   dAct = w * Q;  dG = dAct * U * sig(G) * (1 + G (1 - sig(G)));  dU = dAct * silu(G)
-//   part[p, n-tile] = <Q, Act> over the tile's columns (router gradient partial sums)
+//   part[p, 2*n-tile + half] = <Q, Act> over the columns one epilogue warp handles
+//   (router-gradient partial sums, reduced in a fixed order by the dw kernel)
 // Padding rows produce exact zeros.  A: Dp/D2p K-major; B: W2/A2 MN-major.
 // =====================================================================================
 struct ProbW2Dgrad {
   static constexpr bool kAmn = false, kBmn = true;
+  static constexpr int kEpiWarps = 8;  // load-heavy epilogue: two warps per lane quarter
   CUtensorMap mDp, mD2p, mW2, mA2;  // Dp (H,P) box(64,128); D2p (r,P) box(64,128);
                                     // W2 (I,H,E) box(64,64,1); A2 (I,r,G) box(64,64,1)
   PlanView pl;
@@ -474,22 +461,39 @@ struct ProbW2Dgrad {
     }
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t p = (int64_t)ti.m0 + row;
     const int rt = pl.route_of_row[p];
     const bool live = rt >= 0;
     const float w = live ? topk_w[rt] : 0.0f;
     const int64_t base = p * I + ti.n0;
     float dot = 0.0f;
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 32 * half; c < 256; c += 32 * nh) {
+      // the chunk's saved G, U and activation: all 12 loads in flight first
+      uint4 gu[4], uu[4], au[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gu[j] = __ldg(reinterpret_cast<const uint4*>(G + base + c) + j);
+        uu[j] = __ldg(reinterpret_cast<const uint4*>(U + base + c) + j);
+        au[j] = __ldg(reinterpret_cast<const uint4*>(Act + base + c) + j);
+      }
       float q[32];
       tmem_ld32(taddr + c, q);
 #pragma unroll
       for (int j = 0; j < 32; j += 8) {
         float g[8], u[8], a[8], og[8], ou[8];
-        ld_bf16x8(G + base + c + j, g);
-        ld_bf16x8(U + base + c + j, u);
-        ld_bf16x8(Act + base + c + j, a);
+        const uint32_t gw[4] = {gu[j / 8].x, gu[j / 8].y, gu[j / 8].z, gu[j / 8].w};
+        const uint32_t uw[4] = {uu[j / 8].x, uu[j / 8].y, uu[j / 8].z, uu[j / 8].w};
+        const uint32_t aw[4] = {au[j / 8].x, au[j / 8].y, au[j / 8].z, au[j / 8].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          g[2 * e] = bf16_lo(gw[e]);
+          g[2 * e + 1] = bf16_hi(gw[e]);
+          u[2 * e] = bf16_lo(uw[e]);
+          u[2 * e + 1] = bf16_hi(uw[e]);
+          a[2 * e] = bf16_lo(aw[e]);
+          a[2 * e + 1] = bf16_hi(aw[e]);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float qv = q[j + i];
@@ -503,9 +507,9 @@ struct ProbW2Dgrad {
         st_bf16x8(dU + base + c + j, ou);
       }
     }
-    part[p * ntn() + ti.sub] = live ? dot : 0.0f;
+    part[p * (nh * ntn()) + nh * ti.sub + half] = live ? dot : 0.0f;
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
@@ -515,6 +519,7 @@ struct ProbW2Dgrad {
 // =====================================================================================
 struct ProbDA2 {
   static constexpr bool kAmn = true, kBmn = true;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mdZ2p, mAct;  // dZ2p (r,P) box(64,64); Act (I,P) box(64,64)
   PlanView pl;
   int* err;
@@ -546,18 +551,18 @@ struct ProbDA2 {
     for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mAct, bar, ti.n0 + c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const bool ok = row < r;
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 32 * half; c < 256; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, v, 1.0f, 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
     if (row >= r) return;
     const float z[32] = {};
-    for (int c = 0; c < 256; c += 32) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, z, 0.f, 32);
+    for (int c = 32 * half; c < 256; c += 32 * nh) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, z, 0.f, 32);
   }
 };
 
@@ -570,6 +575,7 @@ struct ProbDA2 {
 // =====================================================================================
 struct ProbW13Dgrad {
   static constexpr bool kAmn = false, kBmn = true;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1);
                                              // B1/B3 (r,I,G) box(64,64,1)
   PlanView pl;
@@ -624,25 +630,25 @@ struct ProbW13Dgrad {
     const bool second = ks >= nb;
     return MmaStep{round16(r), second ? 128 : 0, 0, ks == 0 || ks == nb};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t p = (int64_t)ti.m0 + row;
     if (!ti.sub) {
-      for (int c = 0; c < 256; c += 32) {
+      for (int c = 32 * half; c < 256; c += 32 * nh) {
         float v[32];
         tmem_ld32(taddr + c, v);
         store_row_bf16(dXp + p * H + ti.n0 + c, v, 1.0f, 32);
       }
     } else {
-      for (int half = 0; half < 2; ++half) {
-        for (int c = 0; c < r; c += 32) {
+      for (int hh = 0; hh < 2; ++hh) {
+        for (int c = 32 * half; c < r; c += 32 * nh) {
           float v[32];
-          tmem_ld32(taddr + half * 128 + c, v);
-          store_row_f32(dY13 + p * (2 * r) + half * r + c, v, s, r - c < 32 ? r - c : 32);
+          tmem_ld32(taddr + hh * 128 + c, v);
+          store_row_f32(dY13 + p * (2 * r) + hh * r + c, v, s, r - c < 32 ? r - c : 32);
         }
       }
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
@@ -652,6 +658,7 @@ struct ProbW13Dgrad {
 // =====================================================================================
 struct ProbDB13 {
   static constexpr bool kAmn = true, kBmn = true;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mdG, mdU, mY13p;  // dG/dU (I,P) box(64,64); Y13p (2r,P) box(64,64)
   PlanView pl;
   int* err;
@@ -688,36 +695,37 @@ struct ProbDB13 {
     for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mY13p, bar, ti.sub * r + c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t i = (int64_t)ti.m0 + row;
     float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
-    for (int c = 0; c < r; c += 32) {
+    for (int c = 32 * half; c < r; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
       store_row_f32(out + c, v, 1.0f, r - c < 32 ? r - c : 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
     const int64_t i = (int64_t)ti.m0 + row;
     float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
     const float z[32] = {};
-    for (int c = 0; c < r; c += 32) store_row_f32(out + c, z, 0.f, r - c < 32 ? r - c : 32);
+    for (int c = 32 * half; c < r; c += 32 * nh) store_row_f32(out + c, z, 0.f, r - c < 32 ? r - c : 32);
   }
 };
 
 // =====================================================================================
-// Backward B6 -- grad-x: shared A1/A3 path fused with the source combine:
-//   dx_t = bf16( dY13w_t [A1_a; A3_a] + sum_j dXp[row(t,j)] )
-// M = tokens of adapter a, N = H (tiles of 256), K = 2r (dY1 steps with A1, then dY3 with A3).
-// A: dY13w K-major; B: (n=h, k=q) = A1[a][q][h], MN-major.
+// Backward B6 (first half) -- grad-x through the shared A1/A3, once per token:
+//   dXl_t = bf16( dY13w_t [A1_a; A3_a] )   [T,H]
+// M = tokens of adapter a, N = H (tiles of 256), K = 2r (dY1 steps with A1, then dY3
+// with A3).  A: dY13w K-major; B: (n=h, k=q) = A1[a][q][h], MN-major.  The source
+// combine of the routed dXp rows is added by combine_rows.
 // =====================================================================================
-struct ProbGradX {
+struct ProbA13Expand {
   static constexpr bool kAmn = false, kBmn = true;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mdY13w, mA1, mA3;  // dY13w (2r,T) box(64,128); A1/A3 (H,r,A) box(64,64,1)
   PlanView pl;
   int* err;
-  const uint16_t* dXp;
-  uint16_t* dx;
+  uint16_t* dXl;
   int H, r;
   __device__ int ntn() const { return H / 256; }
   __device__ int nkr() const { return (r + 63) / 64; }
@@ -748,35 +756,16 @@ struct ProbGradX {
     for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, m, bar, ti.n0 + c * 64, kb * kBK, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    const int k = pl.k;
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 32 * half; c < 256; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      if (!ok) continue;
-      float acc[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        const int R = pl.row_of_route[t * k + j];
-        if (R < 0) continue;
-        const uint16_t* src = dXp + (int64_t)R * H + ti.n0 + c;
-#pragma unroll
-        for (int q = 0; q < 32; q += 8) {
-          float o[8];
-          ld_bf16x8(src + q, o);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[q + i] += o[i];
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] += acc[i];
-      store_row_bf16(dx + t * H + ti.n0 + c, v, 1.0f, 32);
+      if (ok) store_row_bf16(dXl + t * H + ti.n0 + c, v, 1.0f, 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 // =====================================================================================
@@ -786,6 +775,7 @@ struct ProbGradX {
 // =====================================================================================
 struct ProbDA13 {
   static constexpr bool kAmn = true, kBmn = true;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mdY13w, mx;  // dY13w (2r,T) box(64,64); x (H,T) box(64,64)
   PlanView pl;
   int* err;
@@ -823,20 +813,20 @@ struct ProbDA13 {
   __device__ float* out_row(const TileInfo& ti, int m) const {
     return (m < r ? dA1 + ((int64_t)ti.g * r + m) * H : dA3 + ((int64_t)ti.g * r + (m - r)) * H) + ti.n0;
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int m = ti.m0 + row;
     const bool ok = m < 2 * r;
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 32 * half; c < 256; c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_f32(out_row(ti, m) + c, v, 1.0f, 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
     const int m = ti.m0 + row;
     if (m >= 2 * r) return;
     const float z[32] = {};
-    for (int c = 0; c < 256; c += 32) store_row_f32(out_row(ti, m) + c, z, 0.f, 32);
+    for (int c = 32 * half; c < 256; c += 32 * nh) store_row_f32(out_row(ti, m) + c, z, 0.f, 32);
   }
 };
 
@@ -848,6 +838,7 @@ struct ProbDA13 {
 template <bool AMN, bool BMN>
 struct ProbPlain {
   static constexpr bool kAmn = AMN, kBmn = BMN;
+  static constexpr int kEpiWarps = 4;
   CUtensorMap mA, mB;  // K-major: (K,rows) box(64,128 | N); MN-major: (rows,K) box(64,64)
   int* err;
   float* C;
@@ -887,15 +878,15 @@ struct ProbPlain {
     }
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{tn(), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
     const int64_t m = (int64_t)ti.m0 + row;
-    for (int c = 0; c < tn(); c += 32) {
+    for (int c = 32 * half; c < tn(); c += 32 * nh) {
       float v[32];
       tmem_ld32(taddr + c, v);
       store_row_f32(C + m * N + ti.n0 + c, v, 1.0f, tn() - c < 32 ? tn() - c : 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo&, int) const {}
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 
 }  // namespace moelora

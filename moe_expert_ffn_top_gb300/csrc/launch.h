@@ -29,6 +29,10 @@ cudaError_t launch_gather_bwd(const PlanView& pl, const uint16_t* dy, const uint
                               uint16_t* Dp, uint16_t* D2p, uint16_t* dZ2p, int H, int r, float s, int num_sms,
                               cudaStream_t stream);
 
+// out[t] = bf16(base[t] + sum_j w_tj src[row(t,j)])  [T,H]; w = 1 when topk_w is NULL.
+cudaError_t launch_combine_rows(const PlanView& pl, const uint16_t* base, const uint16_t* src, const float* topk_w,
+                                uint16_t* out, int H, int num_sms, cudaStream_t stream, int slot);
+
 // dw[t*k+j] = sum over n-tiles of part[row(t,j)], 0 for masked routes.
 cudaError_t launch_dw(const PlanView& pl, const float* part, int nparts, float* dw, int num_sms,
                       cudaStream_t stream);

@@ -114,9 +114,61 @@ __global__ void dy13w_kernel(PlanView pl, const float* __restrict__ dY13, uint16
   }
 }
 
+// out_t = bf16( base_t + sum_j w_tj src[row(t,j)] ), one warp per token: every
+// warp access is one contiguous 512-byte piece of one row (coalesced, one page),
+// with the 16-byte loads of up to 8 routes in flight before they are summed.
+// fp32, slot order j = 0..k-1 after the base term; w = 1 when topk_w is NULL.
+__global__ void combine_rows_kernel(PlanView pl, const uint16_t* __restrict__ base, const uint16_t* __restrict__ src,
+                                    const float* __restrict__ topk_w, uint16_t* __restrict__ out, int H) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int k = pl.k;
+  for (int64_t t = w0; t < pl.T; t += nw) {
+    const int* rows = pl.row_of_route + t * k;
+    for (int c = lane * 8; c < H; c += 32 * 8) {
+      float acc[8];
+      ld_bf16x8(base + t * H + c, acc);
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        int R[8];
+        float w[8];
+        uint4 u[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const bool in = j0 + j < k;
+          R[j] = in ? rows[j0 + j] : -1;
+          w[j] = (in && topk_w) ? topk_w[t * k + j0 + j] : 1.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          u[j] = R[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)R[j] * H + c)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (R[j] < 0) continue;
+          const uint32_t wd[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] += w[j] * bf16_lo(wd[e]);
+            acc[2 * e + 1] += w[j] * bf16_hi(wd[e]);
+          }
+        }
+      }
+      st_bf16x8(out + t * H + c, acc);
+    }
+  }
+}
+
 int grid_for(int num_sms) { return num_sms * 8; }
 
 }  // namespace
+
+cudaError_t launch_combine_rows(const PlanView& pl, const uint16_t* base, const uint16_t* src, const float* topk_w,
+                                uint16_t* out, int H, int num_sms, cudaStream_t stream, int slot) {
+  prof_begin(slot, stream);
+  combine_rows_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, base, src, topk_w, out, H);
+  prof_end(slot, stream);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint16_t* Xp,
                               uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream) {

@@ -43,7 +43,8 @@ inline int64_t plan_chunks(const moe_lora_dims* d) {
 
 // ------------------------------------------------------------------ layouts
 struct PlanLayout {
-  size_t err, counts, offsets, row_of_route, route_of_row, tile_group, tok_off, tok_tile, chunk_base, total;
+  size_t err, counts, offsets, row_of_route, route_of_row, tile_group, tok_off, tok_tile, wtile_off, wtile,
+      chunk_base, total;
 };
 inline PlanLayout plan_layout(const moe_lora_dims* d) {
   PlanLayout L;
@@ -58,6 +59,8 @@ inline PlanLayout plan_layout(const moe_lora_dims* d) {
   L.tile_group = take(sizeof(int32_t) * (P / kBlockM + 1));
   L.tok_off = take(sizeof(int32_t) * (kMaxAdapters + 1));
   L.tok_tile = take(sizeof(int32_t) * (kMaxAdapters + 1));
+  L.wtile_off = take(sizeof(int32_t) * (G + 1));
+  L.wtile = take(sizeof(int32_t) * (P / kBlockM + 1));
   L.chunk_base = take(sizeof(int32_t) * G * (plan_chunks(d) > 0 ? plan_chunks(d) : 1));
   L.total = o;
   return L;
@@ -132,6 +135,8 @@ struct PlanView {
   const int* tile_group;     // [P/128] group of each 128-row tile
   const int* tok_off;        // [A+1] first token of each adapter
   const int* tok_tile;       // [A+1] first 128-token tile of each adapter
+  const int* wtile_off;      // [G+1] first 256-row tile of each group
+  const int* wtile;          // 256-row tiles: (first 128-row tile index << 1) | (halves - 1)
   int64_t T;
   int G, E, A, k;
 };
@@ -148,6 +153,8 @@ inline PlanView make_plan_view(const moe_lora_dims* d, const void* ws) {
   v.tile_group = (const int*)(b + L.tile_group);
   v.tok_off = (const int*)(b + L.tok_off);
   v.tok_tile = (const int*)(b + L.tok_tile);
+  v.wtile_off = (const int*)(b + L.wtile_off);
+  v.wtile = (const int*)(b + L.wtile);
   v.T = d->T;
   v.G = d->A * d->E;
   v.E = d->E;

@@ -21,10 +21,10 @@
 //   void     prefetch() const;              tensor-map prefetch
 //   void     load(const TileInfo&, int ks, uint8_t* sA, uint8_t* sB, uint64_t* bar) const;
 //   MmaStep  mma_step(const TileInfo&, int ks) const;
-//   void     epilogue(const TileInfo&, int row, uint32_t tmem_lane_addr, int half, int nh) const;
-//   void     epilogue_empty(const TileInfo&, int row, int half, int nh) const;   (tiles with nk == 0)
-// An epilogue warp handles the 32-column chunks c = 32*half, 32*(half + nh), ... of its
-// row, where nh = kEpiWarps / 4 warps share each TMEM lane quarter.
+//   void     epilogue(const TileInfo&, int row, uint32_t tmem_lane_addr, int c0, int cs) const;
+//   void     epilogue_empty(const TileInfo&, int row, int c0, int cs) const;   (tiles with nk == 0)
+//   static constexpr bool kWide;           256-row tiles (see EngineShape)
+// An epilogue warp handles the 32-column chunks c = c0, c0 + cs, ... of its row.
 //
 // Operand tiles in shared memory use the 128-byte swizzle written by TMA:
 //   A K-major : 128 rows x 128 B                         (one 16 KB box)
@@ -39,14 +39,25 @@
 namespace moelora {
 
 constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kAStageBytes = 128 * 128;  // 16 KB
-constexpr int kBStageBytes = 256 * 128;  // 32 KB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+constexpr int kBStageBytes = 256 * 128;  // 32 KB: up to 256 rows x 64 bf16
 constexpr int kAccCols = 256;
-constexpr int kMaxEpiWarps = 8;
-constexpr int kGemmMaxThreads = 64 + 32 * kMaxEpiWarps;
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 + 256;
+constexpr int kGemmSmemBytes = 192 * 1024 + 1024 + 256;
+
+// Per-problem pipeline shape.  Narrow problems: 128-row tiles, 4 stages of
+// (A 16 KB + B 32 KB), two TMEM accumulators (the epilogue of one tile overlaps the
+// main loop of the next).  Wide problems (P::kWide): 256-row tiles as two M=128
+// MMAs sharing each B tile, 3 stages of (A 32 KB + B 32 KB), one accumulator pair
+// using all 512 TMEM columns -- a third fewer operand bytes per FLOP streamed into
+// the SM, at the price of an epilogue that no longer overlaps the main loop.
+template <class P>
+struct EngineShape {
+  static constexpr bool kWide = P::kWide;
+  static constexpr int kAStage = kWide ? 2 * 128 * 128 : 128 * 128;
+  static constexpr int kStage = kAStage + kBStageBytes;
+  static constexpr int kStages = kWide ? 3 : 4;
+  static constexpr int kAccBufs = kWide ? 1 : 2;
+  static_assert(kStages * kStage <= 192 * 1024, "pipeline exceeds shared memory budget");
+};
 
 struct TileInfo {
   int m0;    // first output row
@@ -56,6 +67,7 @@ struct TileInfo {
   int nk;    // number of 64-wide K steps (0 = empty tile)
   int k0;    // first K index for K-grouped problems
   int mend;  // one past the last valid output row
+  int mh;    // wide problems: 128-row halves present (1 or 2)
 };
 
 struct MmaStep {
@@ -67,20 +79,21 @@ struct MmaStep {
 
 template <class P>
 __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const __grid_constant__ P p) {
+  using S = EngineShape<P>;
   static_assert(P::kEpiWarps == 4 || P::kEpiWarps == 8, "4 or 8 epilogue warps");
-  constexpr int kNh = P::kEpiWarps / 4;
+  static_assert(!P::kWide || (P::kEpiWarps == 8 && !P::kAmn), "wide tiles: 8 epilogue warps, K-major A");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStage);
+  uint64_t* empty = full + S::kStages;
+  uint64_t* tfull = empty + S::kStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = p.err;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -106,8 +119,8 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      uint32_t issued = 0;  // bit s: stage s has received a load
-      uint32_t last_ph = 0; // bit s: phase parity of stage s's last load
+      uint32_t issued = 0;   // bit s: stage s has received a load
+      uint32_t last_ph = 0;  // bit s: phase parity of stage s's last load
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const TileInfo ti = p.tile(t);
         for (int ks = 0; ks < ti.nk; ++ks) {
@@ -115,11 +128,11 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
             ok = false;
             break;
           }
-          uint8_t* sa = smem + s * kStageBytes;
-          p.load(ti, ks, sa, sa + kAStageBytes, &full[s]);
+          uint8_t* sa = smem + s * S::kStage;
+          p.load(ti, ks, sa, sa + S::kAStage, &full[s]);
           issued |= 1u << s;
           last_ph = (last_ph & ~(1u << s)) | (ph << s);
-          if (++s == kStages) {
+          if (++s == S::kStages) {
             s = 0;
             ph ^= 1u;
           }
@@ -128,7 +141,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
       // No TMA copy may still be landing in shared memory when the CTA exits
       // (matters only if a wait above gave up): wait, bounded, for each stage's
       // last load to complete.
-      for (int i = 0; i < kStages; ++i)
+      for (int i = 0; i < S::kStages; ++i)
         if (issued & (1u << i)) mbar_wait(&full[i], (last_ph >> i) & 1u, err, 100000000ull);
     }
   } else if (warp == 1) {
@@ -141,7 +154,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
         if (ti.nk == 0) continue;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, err)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
+        const uint32_t d = tmem_base + (uint32_t)(S::kWide ? 0 : acc * kAccCols);
         for (int ks = 0; ks < ti.nk; ++ks) {
           if (!mbar_wait(&full[s], ph, err)) {
             ok = false;
@@ -150,47 +163,62 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
           tc_fence_after();
           const MmaStep st = p.mma_step(ti, ks);
           const uint32_t idesc = idesc_bf16_f32(128, st.n, P::kAmn, P::kBmn);
-          const uint32_t sa = smem_u32(smem + s * kStageBytes);
-          const uint32_t sb = sa + kAStageBytes + (uint32_t)st.b_off;
+          const uint32_t sa = smem_u32(smem + s * S::kStage);
+          const uint32_t sb = sa + S::kAStage + (uint32_t)st.b_off;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = P::kAmn ? sw128_desc(sa + kk * 2048, 8192, 1024) : sw128_desc(sa + kk * 32, 16, 1024);
             const uint64_t bd = P::kBmn ? sw128_desc(sb + kk * 2048, 8192, 1024) : sw128_desc(sb + kk * 32, 16, 1024);
-            mma_bf16(d + (uint32_t)st.col, ad, bd, idesc, (st.first && kk == 0) ? 0u : 1u);
+            const uint32_t accum = (st.first && kk == 0) ? 0u : 1u;
+            mma_bf16(d + (uint32_t)st.col, ad, bd, idesc, accum);
+            if (S::kWide && ti.mh == 2)  // rows 128..255 of the tile: second A half, same B
+              mma_bf16(d + kAccCols + (uint32_t)st.col, sw128_desc(sa + 128 * 128 + kk * 32, 16, 1024), bd, idesc,
+                       accum);
           }
           mma_commit(&empty[s]);
-          if (++s == kStages) {
+          if (++s == S::kStages) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
         mma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1u;
+        if (++acc == S::kAccBufs) {
+          acc = 0;
+          aph ^= 1u;
+        }
       }
     }
   } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;
-    const int row = q * 32 + lane;
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // 0 for warps 2..5, 1 for warps 6..9
+    // Narrow: warps sharing a quarter split the columns.  Wide: half selects the
+    // 128-row half of the tile (its own accumulator), all columns.
+    const int row = (S::kWide ? half * 128 : 0) + q * 32 + lane;
+    const int c0 = S::kWide ? 0 : 32 * half;
+    const int cs = S::kWide ? 32 : 32 * (P::kEpiWarps / 4);
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileInfo ti = p.tile(t);
       if (ti.nk == 0) {
-        p.epilogue_empty(ti, row, half, kNh);
+        p.epilogue_empty(ti, row, c0, cs);
         continue;
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, err));
       if (!ok) break;
       tc_fence_after();
-      p.epilogue(ti, row, tmem_base + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16), half, kNh);
+      if (!S::kWide || half < ti.mh) {
+        const uint32_t col = (uint32_t)(S::kWide ? half * kAccCols : acc * kAccCols);
+        p.epilogue(ti, row, tmem_base + col + ((uint32_t)(q * 32) << 16), c0, cs);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) aph ^= 1u;
+      if (++acc == S::kAccBufs) {
+        acc = 0;
+        aph ^= 1u;
+      }
     }
   }
   __syncthreads();

@@ -15,12 +15,44 @@
 #pragma once
 #include "gemm_engine.cuh"
 
+
 namespace moelora {
+
+constexpr int kAStage128 = 128 * 128;  // bytes of one 128-row x 64 bf16 operand tile
 
 __device__ __forceinline__ int adapter_of_tile(const PlanView& pl, int t) {
   int a = 0;
   while (a + 1 < pl.A && t >= pl.tok_tile[a + 1]) ++a;
   return a;
+}
+
+// 256-row tile t of an M-grouped problem with ntn column tiles: rows
+// [m0, m0 + 128*mh) of one plan group (mh = 2, or 1 for a group's odd last tile).
+__device__ __forceinline__ void wide_tile(const PlanView& pl, int t, int ntn, TileInfo& ti) {
+  const int w = pl.wtile[t / ntn];
+  const int mt = w >> 1;
+  ti.mh = (w & 1) + 1;
+  ti.m0 = mt * 128;
+  ti.mend = ti.m0 + 128 * ti.mh;
+  ti.g = pl.tile_group[mt];
+  ti.k0 = 0;
+}
+
+// 128-row tile t of an M-grouped problem with ntn column tiles.
+__device__ __forceinline__ void narrow_tile(const PlanView& pl, int t, int ntn, TileInfo& ti) {
+  const int mt = t / ntn;
+  ti.mh = 1;
+  ti.m0 = mt * 128;
+  ti.mend = ti.m0 + 128;
+  ti.g = pl.tile_group[mt];
+  ti.k0 = 0;
+}
+
+// A-operand rows of a wide tile: one 128-row box per half present.
+__device__ __forceinline__ void load_a_wide(const TileInfo& ti, uint8_t* sa, const CUtensorMap* m, uint64_t* bar,
+                                            int kx) {
+  tma_load_2d(sa, m, bar, kx, ti.m0);
+  if (ti.mh == 2) tma_load_2d(sa + kAStage128, m, bar, kx, ti.m0 + 128);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -59,6 +91,7 @@ __device__ __forceinline__ int round16(int r) { return (r + 15) & ~15; }
 struct ProbShrink {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mx, mA1, mA3;  // x (H,T) box(64,128); A1/A3 (H,r,A) box(64,r,1)
   PlanView pl;
   int* err;
@@ -84,16 +117,16 @@ struct ProbShrink {
     tma_prefetch_map(&mA3);
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
-    mbar_arrive_expect_tx(bar, kAStageBytes + 2 * r * 128);
+    mbar_arrive_expect_tx(bar, kAStage128 + 2 * r * 128);
     tma_load_2d(sa, &mx, bar, ks * kBK, ti.m0);
     tma_load_3d(sb, &mA1, bar, ks * kBK, 0, ti.g);
     tma_load_3d(sb + r * 128, &mA3, bar, ks * kBK, 0, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{2 * r, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    for (int c = 32 * half; c < 2 * r; c += 32 * nh) {
+    for (int c = c0; c < 2 * r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       const int n = 2 * r - c < 32 ? 2 * r - c : 32;
@@ -115,6 +148,7 @@ struct ProbShrink {
 struct ProbW13 {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;  // 256-row tiles measured slower: its epilogue is heavy
   CUtensorMap mXp, mY13p, mW1, mW3, mB1, mB3;  // Xp (H,P) box(64,128); Y13p (2r,P) box(64,128);
                                                // W1/W3 (H,I,E) box(64,128,1); B1/B3 (r,I,G) box(64,128,1)
   PlanView pl;
@@ -125,15 +159,11 @@ struct ProbW13 {
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
   __device__ TileInfo tile(int t) const {
-    const int mt = t / ntn(), nt = t % ntn();
     TileInfo ti;
-    ti.m0 = mt * 128;
-    ti.mend = ti.m0 + 128;
-    ti.n0 = nt * 128;
-    ti.g = pl.tile_group[mt];
+    narrow_tile(pl, t, ntn(), ti);
+    ti.n0 = t % ntn() * 128;
     ti.sub = 0;
     ti.nk = H / kBK + 2 * nkr();
-    ti.k0 = 0;
     return ti;
   }
   __device__ void prefetch() const {
@@ -148,14 +178,14 @@ struct ProbW13 {
     const int nb = H / kBK;
     const int e = ti.g % pl.E;
     if (ks < nb) {
-      mbar_arrive_expect_tx(bar, kAStageBytes + 2 * 128 * 128);
-      tma_load_2d(sa, &mXp, bar, ks * kBK, ti.m0);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 2 * 128 * 128);
+      load_a_wide(ti, sa, &mXp, bar, ks * kBK);
       tma_load_3d(sb, &mW1, bar, ks * kBK, ti.n0, e);
       tma_load_3d(sb + 128 * 128, &mW3, bar, ks * kBK, ti.n0, e);
     } else {
       const int j = ks - nb, half = j / nkr(), kb = j % nkr();
-      mbar_arrive_expect_tx(bar, kAStageBytes + 128 * 128);
-      tma_load_2d(sa, &mY13p, bar, half * r + kb * kBK, ti.m0);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 128 * 128);
+      load_a_wide(ti, sa, &mY13p, bar, half * r + kb * kBK);
       tma_load_3d(sb, half ? &mB3 : &mB1, bar, kb * kBK, ti.n0, ti.g);
     }
   }
@@ -165,10 +195,10 @@ struct ProbW13 {
     const int half = (ks - nb) / nkr();
     return MmaStep{128, half * 128, 0, 0};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t p = (int64_t)ti.m0 + row;
     const int64_t base = p * I + ti.n0;
-    for (int c = 32 * half; c < 128; c += 32 * nh) {
+    for (int c = c0; c < 128; c += cs) {
       float g[32], u[32];
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
@@ -194,6 +224,7 @@ struct ProbW13 {
 struct ProbW2 {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;  // 256-row tiles measured slower: K = I is short
   CUtensorMap mAct, mW2, mA2;  // Act (I,P) box(64,128); W2 (I,H,E) box(64,256,1); A2 (I,r,G) box(64,r16,1)
   PlanView pl;
   int* err;
@@ -202,15 +233,12 @@ struct ProbW2 {
   __device__ int ntn() const { return H / 256 + 1; }
   __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
   __device__ TileInfo tile(int t) const {
-    const int mt = t / ntn(), nt = t % ntn();
+    const int nt = t % ntn();
     TileInfo ti;
-    ti.m0 = mt * 128;
-    ti.mend = ti.m0 + 128;
+    narrow_tile(pl, t, ntn(), ti);
     ti.sub = nt == H / 256;
     ti.n0 = ti.sub ? 0 : nt * 256;
-    ti.g = pl.tile_group[mt];
     ti.nk = I / kBK;
-    ti.k0 = 0;
     return ti;
   }
   __device__ void prefetch() const {
@@ -220,28 +248,28 @@ struct ProbW2 {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     if (!ti.sub) {
-      mbar_arrive_expect_tx(bar, kAStageBytes + 256 * 128);
-      tma_load_2d(sa, &mAct, bar, ks * kBK, ti.m0);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 256 * 128);
+      load_a_wide(ti, sa, &mAct, bar, ks * kBK);
       tma_load_3d(sb, &mW2, bar, ks * kBK, ti.n0, ti.g % pl.E);
     } else {
-      mbar_arrive_expect_tx(bar, kAStageBytes + round16(r) * 128);
-      tma_load_2d(sa, &mAct, bar, ks * kBK, ti.m0);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + round16(r) * 128);
+      load_a_wide(ti, sa, &mAct, bar, ks * kBK);
       tma_load_3d(sb, &mA2, bar, ks * kBK, 0, ti.g);
     }
   }
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     return MmaStep{ti.sub ? round16(r) : 256, 0, 0, ks == 0};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t p = (int64_t)ti.m0 + row;
     if (!ti.sub) {
-      for (int c = 32 * half; c < 256; c += 32 * nh) {
+      for (int c = c0; c < 256; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
         store_row_bf16(O + p * H + ti.n0 + c, v, 1.0f, 32);
       }
     } else {
-      for (int c = 32 * half; c < r; c += 32 * nh) {
+      for (int c = c0; c < r; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
         store_row_bf16(Z2 + p * r + c, v, 1.0f, r - c < 32 ? r - c : 32);
@@ -262,6 +290,7 @@ struct ProbW2 {
 struct ProbB2Expand {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mZ2w, mB2;  // Z2w (r,T) box(64,128); B2 (r,H,A) box(64,256,1)
   PlanView pl;
   int* err;
@@ -288,15 +317,15 @@ struct ProbB2Expand {
     tma_prefetch_map(&mB2);
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
-    mbar_arrive_expect_tx(bar, kAStageBytes + 256 * 128);
+    mbar_arrive_expect_tx(bar, kAStage128 + 256 * 128);
     tma_load_2d(sa, &mZ2w, bar, ks * kBK, ti.m0);
     tma_load_3d(sb, &mB2, bar, ks * kBK, ti.n0, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    for (int c = 32 * half; c < 256; c += 32 * nh) {
+    for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_bf16(Yl + t * H + ti.n0 + c, v, s, 32);
@@ -312,6 +341,7 @@ struct ProbB2Expand {
 struct ProbDyB2 {
   static constexpr bool kAmn = false, kBmn = true;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mdy, mB2;  // dy (H,T) box(64,128); B2 (r,H,A) box(64,64,1)
   PlanView pl;
   int* err;
@@ -336,15 +366,15 @@ struct ProbDyB2 {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int nbox = (round16(r) + 63) / 64;
-    mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
+    mbar_arrive_expect_tx(bar, kAStage128 + nbox * 8192);
     tma_load_2d(sa, &mdy, bar, ks * kBK, ti.m0);
     for (int c = 0; c < nbox; ++c) tma_load_3d(sb + c * 8192, &mB2, bar, c * 64, ks * kBK, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    for (int c = 32 * half; c < r; c += 32 * nh) {
+    for (int c = c0; c < r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_bf16(dyB2 + t * r + c, v, 1.0f, r - c < 32 ? r - c : 32);
@@ -360,6 +390,7 @@ struct ProbDyB2 {
 struct ProbDB2 {
   static constexpr bool kAmn = true, kBmn = true;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mdy, mZ2w;  // dy (H,T) box(64,64); Z2w (r,T) box(64,64)
   PlanView pl;
   int* err;
@@ -386,24 +417,24 @@ struct ProbDB2 {
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int nbox = (round16(r) + 63) / 64;
     const int kt = ti.k0 + ks * kBK;
-    mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
+    mbar_arrive_expect_tx(bar, kAStage128 + nbox * 8192);
     tma_load_2d(sa, &mdy, bar, ti.m0, kt);
     tma_load_2d(sa + 8192, &mdy, bar, ti.m0 + 64, kt);
     for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mZ2w, bar, c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t h = (int64_t)ti.m0 + row;
-    for (int c = 32 * half; c < r; c += 32 * nh) {
+    for (int c = c0; c < r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, v, s, r - c < 32 ? r - c : 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     const float z[32] = {};
     const int64_t h = (int64_t)ti.m0 + row;
-    for (int c = 32 * half; c < r; c += 32 * nh) store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, z, 0.f, r - c < 32 ? r - c : 32);
+    for (int c = c0; c < r; c += cs) store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, z, 0.f, r - c < 32 ? r - c : 32);
   }
 };
 
@@ -417,6 +448,7 @@ struct ProbDB2 {
 // =====================================================================================
 struct ProbW2Dgrad {
   static constexpr bool kAmn = false, kBmn = true;
+  static constexpr bool kWide = false;
   static constexpr int kEpiWarps = 8;  // load-heavy epilogue: two warps per lane quarter
   CUtensorMap mDp, mD2p, mW2, mA2;  // Dp (H,P) box(64,128); D2p (r,P) box(64,128);
                                     // W2 (I,H,E) box(64,64,1); A2 (I,r,G) box(64,64,1)
@@ -450,7 +482,7 @@ struct ProbW2Dgrad {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int nb = H / kBK;
-    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    mbar_arrive_expect_tx(bar, kAStage128 + 4 * 8192);
     if (ks < nb) {
       tma_load_2d(sa, &mDp, bar, ks * kBK, ti.m0);
       for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
@@ -461,14 +493,14 @@ struct ProbW2Dgrad {
     }
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t p = (int64_t)ti.m0 + row;
     const int rt = pl.route_of_row[p];
     const bool live = rt >= 0;
     const float w = live ? topk_w[rt] : 0.0f;
     const int64_t base = p * I + ti.n0;
     float dot = 0.0f;
-    for (int c = 32 * half; c < 256; c += 32 * nh) {
+    for (int c = c0; c < 256; c += cs) {
       // the chunk's saved G, U and activation: all 12 loads in flight first
       uint4 gu[4], uu[4], au[4];
 #pragma unroll
@@ -507,7 +539,7 @@ struct ProbW2Dgrad {
         st_bf16x8(dU + base + c + j, ou);
       }
     }
-    part[p * (nh * ntn()) + nh * ti.sub + half] = live ? dot : 0.0f;
+    part[p * ((cs / 32) * ntn()) + (cs / 32) * ti.sub + c0 / 32] = live ? dot : 0.0f;
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
@@ -520,6 +552,7 @@ struct ProbW2Dgrad {
 struct ProbDA2 {
   static constexpr bool kAmn = true, kBmn = true;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mdZ2p, mAct;  // dZ2p (r,P) box(64,64); Act (I,P) box(64,64)
   PlanView pl;
   int* err;
@@ -545,24 +578,24 @@ struct ProbDA2 {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int kt = ti.k0 + ks * kBK;
-    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    mbar_arrive_expect_tx(bar, kAStage128 + 4 * 8192);
     tma_load_2d(sa, &mdZ2p, bar, 0, kt);
     tma_load_2d(sa + 8192, &mdZ2p, bar, 64, kt);
     for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mAct, bar, ti.n0 + c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const bool ok = row < r;
-    for (int c = 32 * half; c < 256; c += 32 * nh) {
+    for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, v, 1.0f, 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     if (row >= r) return;
     const float z[32] = {};
-    for (int c = 32 * half; c < 256; c += 32 * nh) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, z, 0.f, 32);
+    for (int c = c0; c < 256; c += cs) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, z, 0.f, 32);
   }
 };
 
@@ -575,7 +608,8 @@ struct ProbDA2 {
 // =====================================================================================
 struct ProbW13Dgrad {
   static constexpr bool kAmn = false, kBmn = true;
-  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiWarps = 8;
+  static constexpr bool kWide = true;
   CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1);
                                              // B1/B3 (r,I,G) box(64,64,1)
   PlanView pl;
@@ -585,17 +619,14 @@ struct ProbW13Dgrad {
   int H, I, r;
   float s;
   __device__ int ntn() const { return H / 256 + 1; }
-  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
   __device__ TileInfo tile(int t) const {
-    const int mt = t / ntn(), nt = t % ntn();
+    const int nt = t % ntn();
     TileInfo ti;
-    ti.m0 = mt * 128;
-    ti.mend = ti.m0 + 128;
+    wide_tile(pl, t, ntn(), ti);
     ti.sub = nt == H / 256;
     ti.n0 = ti.sub ? 0 : nt * 256;
-    ti.g = pl.tile_group[mt];
     ti.nk = 2 * (I / kBK);
-    ti.k0 = 0;
     return ti;
   }
   __device__ void prefetch() const {
@@ -611,15 +642,15 @@ struct ProbW13Dgrad {
     const bool second = ks >= nb;
     const int kk = (second ? ks - nb : ks) * kBK;
     if (!ti.sub) {
-      mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
-      tma_load_2d(sa, second ? &mdU : &mdG, bar, kk, ti.m0);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 4 * 8192);
+      load_a_wide(ti, sa, second ? &mdU : &mdG, bar, kk);
       const CUtensorMap* mw = second ? &mW3 : &mW1;
       const int e = ti.g % pl.E;
       for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, mw, bar, ti.n0 + c * 64, kk, e);
     } else {
       const int nbox = (round16(r) + 63) / 64;
-      mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
-      tma_load_2d(sa, second ? &mdU : &mdG, bar, kk, ti.m0);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + nbox * 8192);
+      load_a_wide(ti, sa, second ? &mdU : &mdG, bar, kk);
       const CUtensorMap* mb = second ? &mB3 : &mB1;
       for (int c = 0; c < nbox; ++c) tma_load_3d(sb + c * 8192, mb, bar, c * 64, kk, ti.g);
     }
@@ -630,17 +661,17 @@ struct ProbW13Dgrad {
     const bool second = ks >= nb;
     return MmaStep{round16(r), second ? 128 : 0, 0, ks == 0 || ks == nb};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t p = (int64_t)ti.m0 + row;
     if (!ti.sub) {
-      for (int c = 32 * half; c < 256; c += 32 * nh) {
+      for (int c = c0; c < 256; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
         store_row_bf16(dXp + p * H + ti.n0 + c, v, 1.0f, 32);
       }
     } else {
       for (int hh = 0; hh < 2; ++hh) {
-        for (int c = 32 * half; c < r; c += 32 * nh) {
+        for (int c = c0; c < r; c += cs) {
           float v[32];
           tmem_ld32(taddr + hh * 128 + c, v);
           store_row_f32(dY13 + p * (2 * r) + hh * r + c, v, s, r - c < 32 ? r - c : 32);
@@ -659,6 +690,7 @@ struct ProbW13Dgrad {
 struct ProbDB13 {
   static constexpr bool kAmn = true, kBmn = true;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mdG, mdU, mY13p;  // dG/dU (I,P) box(64,64); Y13p (2r,P) box(64,64)
   PlanView pl;
   int* err;
@@ -689,26 +721,26 @@ struct ProbDB13 {
     const int kt = ti.k0 + ks * kBK;
     const int nbox = (round16(r) + 63) / 64;
     const CUtensorMap* ma = ti.sub ? &mdU : &mdG;
-    mbar_arrive_expect_tx(bar, kAStageBytes + nbox * 8192);
+    mbar_arrive_expect_tx(bar, kAStage128 + nbox * 8192);
     tma_load_2d(sa, ma, bar, ti.m0, kt);
     tma_load_2d(sa + 8192, ma, bar, ti.m0 + 64, kt);
     for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mY13p, bar, ti.sub * r + c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t i = (int64_t)ti.m0 + row;
     float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
-    for (int c = 32 * half; c < r; c += 32 * nh) {
+    for (int c = c0; c < r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       store_row_f32(out + c, v, 1.0f, r - c < 32 ? r - c : 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     const int64_t i = (int64_t)ti.m0 + row;
     float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
     const float z[32] = {};
-    for (int c = 32 * half; c < r; c += 32 * nh) store_row_f32(out + c, z, 0.f, r - c < 32 ? r - c : 32);
+    for (int c = c0; c < r; c += cs) store_row_f32(out + c, z, 0.f, r - c < 32 ? r - c : 32);
   }
 };
 
@@ -722,6 +754,7 @@ struct ProbDB13 {
 struct ProbA13Expand {
   static constexpr bool kAmn = false, kBmn = true;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mdY13w, mA1, mA3;  // dY13w (2r,T) box(64,128); A1/A3 (H,r,A) box(64,64,1)
   PlanView pl;
   int* err;
@@ -750,16 +783,16 @@ struct ProbA13Expand {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int half = ks / nkr(), kb = ks % nkr();
-    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    mbar_arrive_expect_tx(bar, kAStage128 + 4 * 8192);
     tma_load_2d(sa, &mdY13w, bar, half * r + kb * kBK, ti.m0);
     const CUtensorMap* m = half ? &mA3 : &mA1;
     for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, m, bar, ti.n0 + c * 64, kb * kBK, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
-    for (int c = 32 * half; c < 256; c += 32 * nh) {
+    for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_bf16(dXl + t * H + ti.n0 + c, v, 1.0f, 32);
@@ -776,6 +809,7 @@ struct ProbA13Expand {
 struct ProbDA13 {
   static constexpr bool kAmn = true, kBmn = true;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mdY13w, mx;  // dY13w (2r,T) box(64,64); x (H,T) box(64,64)
   PlanView pl;
   int* err;
@@ -804,7 +838,7 @@ struct ProbDA13 {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int kt = ti.k0 + ks * kBK;
-    mbar_arrive_expect_tx(bar, kAStageBytes + 4 * 8192);
+    mbar_arrive_expect_tx(bar, kAStage128 + 4 * 8192);
     tma_load_2d(sa, &mdY13w, bar, ti.m0, kt);
     tma_load_2d(sa + 8192, &mdY13w, bar, ti.m0 + 64, kt);
     for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mx, bar, ti.n0 + c * 64, kt);
@@ -813,20 +847,20 @@ struct ProbDA13 {
   __device__ float* out_row(const TileInfo& ti, int m) const {
     return (m < r ? dA1 + ((int64_t)ti.g * r + m) * H : dA3 + ((int64_t)ti.g * r + (m - r)) * H) + ti.n0;
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int m = ti.m0 + row;
     const bool ok = m < 2 * r;
-    for (int c = 32 * half; c < 256; c += 32 * nh) {
+    for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_f32(out_row(ti, m) + c, v, 1.0f, 32);
     }
   }
-  __device__ void epilogue_empty(const TileInfo& ti, int row, int half, int nh) const {
+  __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     const int m = ti.m0 + row;
     if (m >= 2 * r) return;
     const float z[32] = {};
-    for (int c = 32 * half; c < 256; c += 32 * nh) store_row_f32(out_row(ti, m) + c, z, 0.f, 32);
+    for (int c = c0; c < 256; c += cs) store_row_f32(out_row(ti, m) + c, z, 0.f, 32);
   }
 };
 
@@ -839,6 +873,7 @@ template <bool AMN, bool BMN>
 struct ProbPlain {
   static constexpr bool kAmn = AMN, kBmn = BMN;
   static constexpr int kEpiWarps = 4;
+  static constexpr bool kWide = false;
   CUtensorMap mA, mB;  // K-major: (K,rows) box(64,128 | N); MN-major: (rows,K) box(64,64)
   int* err;
   float* C;
@@ -864,7 +899,7 @@ struct ProbPlain {
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int kt = ks * kBK;
     const int nbox = (tn() + 63) / 64;
-    mbar_arrive_expect_tx(bar, kAStageBytes + (BMN ? nbox * 8192 : tn() * 128));
+    mbar_arrive_expect_tx(bar, kAStage128 + (BMN ? nbox * 8192 : tn() * 128));
     if (AMN) {
       tma_load_2d(sa, &mA, bar, ti.m0, kt);
       tma_load_2d(sa + 8192, &mA, bar, ti.m0 + 64, kt);
@@ -878,9 +913,9 @@ struct ProbPlain {
     }
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{tn(), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int half, int nh) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int64_t m = (int64_t)ti.m0 + row;
-    for (int c = 32 * half; c < tn(); c += 32 * nh) {
+    for (int c = c0; c < tn(); c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       store_row_f32(C + m * N + ti.n0 + c, v, 1.0f, tn() - c < 32 ? tn() - c : 32);

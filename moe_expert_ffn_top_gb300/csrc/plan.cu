@@ -10,6 +10,7 @@
 //   2. plan_scan    : per-group sums and prefix over chunks, padded group offsets
 //   3. plan_scatter : in-order ranking inside each chunk (warp match), rows out
 //   4. plan_finish  : padding rows -> -1, tile -> group table, adapter tables
+//   5. plan_wide    : 256-row tiles (pairs of a group's 128-row tiles)
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -146,6 +147,32 @@ __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __
   }
 }
 
+__global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restrict__ wtile_off,
+                          int* __restrict__ wtile) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    int carry = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      const int v = g < G ? ((offsets[g + 1] - offsets[g]) / kBlockM + 1) / 2 : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (g < G) wtile_off[g] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) wtile_off[G] = carry;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const int m = offsets[g] / kBlockM, n = (offsets[g + 1] - offsets[g]) / kBlockM, base = wtile_off[g];
+    for (int j = 0; 2 * j < n; ++j) wtile[base + j] = ((m + 2 * j) << 1) | (n - 2 * j >= 2 ? 1 : 0);
+  }
+}
+
 cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const AdapterTable& at, void* ws,
                         cudaStream_t stream) {
   const PlanLayout L = plan_layout(d);
@@ -158,6 +185,8 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
   int* tile_group = (int*)(b + L.tile_group);
   int* tok_off = (int*)(b + L.tok_off);
   int* tok_tile = (int*)(b + L.tok_tile);
+  int* wtile_off = (int*)(b + L.wtile_off);
+  int* wtile = (int*)(b + L.wtile);
   int* chunk_base = (int*)(b + L.chunk_base);
   const int G = d->A * d->E;
   const int64_t TK = d->T * d->k;
@@ -192,6 +221,9 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
   plan_finish<<<G < 1024 ? G : 1024, 128, 0, stream>>>(G, counts, offsets, route_of_row, tile_group, at, tok_off,
                                                        tok_tile);
   prof_end(K_PLAN_FINISH, stream);
+  prof_begin(K_PLAN_WIDE, stream);
+  plan_wide<<<1, 1024, 0, stream>>>(G, offsets, wtile_off, wtile);
+  prof_end(K_PLAN_WIDE, stream);
   return cudaGetLastError();
 }
 

@@ -17,4 +17,8 @@ __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __
                             int* __restrict__ route_of_row, int* __restrict__ tile_group, AdapterTable at,
                             int* __restrict__ tok_off, int* __restrict__ tok_tile);
 
+// 256-row tiles: each group's 128-row tiles in pairs (a lone last tile is a half).
+__global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restrict__ wtile_off,
+                          int* __restrict__ wtile);
+
 }  // namespace moelora

@@ -96,6 +96,8 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
   int* tile_group = (int*)(b + L.tile_group);
   int* tok_off = (int*)(b + L.tok_off);
   int* tok_tile = (int*)(b + L.tok_tile);
+  int* wtile_off = (int*)(b + L.wtile_off);
+  int* wtile = (int*)(b + L.wtile);
   const int64_t TK = d->T * d->k;
   const int nch = (int)nchunks;
   if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_LORA_ERR_CUDA;
@@ -121,5 +123,6 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
                                              route_of_row, err);
   plan_finish<<<G < 1024 ? G : 1024, 128, 0, s>>>(G, counts, offsets, route_of_row, tile_group, at, tok_off,
                                                   tok_tile);
+  plan_wide<<<1, 1024, 0, s>>>(G, offsets, wtile_off, wtile);
   return cudaGetLastError() == cudaSuccess ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
 }

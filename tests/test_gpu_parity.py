@@ -242,3 +242,64 @@ def test_production_shape_sampled():
     for k in ("counts", "offsets", "row_of_route", "route_of_row"):
         assert torch.equal(got[k], want[k]), k
     _sampled_check(inp, shp, out, sample)
+
+
+# ----------------------------------------------------------------------------- several adapters
+def _adapter_slice(inp, shp, a):
+    """Adapter a's standalone problem: its tokens and its factors, one adapter."""
+    per = shp.T // shp.A
+    sl = slice(a * per, (a + 1) * per)
+    sub = {n: inp[n][sl] for n in ("x", "dy", "topk_ids", "topk_w")}
+    for n in ("W1", "W3", "W2"):
+        sub[n] = inp[n]
+    for n in ("A1", "A3", "B1", "B3", "A2", "B2"):
+        sub[n] = inp[n][a:a + 1].contiguous()
+    sub["adapter_offsets"] = torch.tensor([0, per], dtype=torch.int64)
+    return sub, Shape(T=per, H=shp.H, I=shp.I, E=shp.E, k=shp.k, r=shp.r, A=1, scale=shp.scale), sl
+
+
+def test_multi_adapter_fused_equals_standalone_bitwise():
+    """16 adapters (rank 8) share one layer, each with its own routing; every
+    adapter's outputs and gradients from the fused pass equal its standalone
+    single-adapter run bit for bit (OpenPipe/ART PR #1139, Validation)."""
+    shp = shape("multi")
+    inp = make_inputs(shp, seed=4, device="cuda")
+    fused = run_gpu(inp, shp)
+    assert fused["err"] == 0
+    for a in (0, 7, 15):
+        sub, sshp, sl = _adapter_slice(inp, shp, a)
+        alone = run_gpu(sub, sshp)
+        for n in ("y", "dx", "dw"):
+            assert torch.equal(fused[n][sl], alone[n]), (a, n)
+        for n in ADAPTER_GRADS:
+            assert torch.equal(fused[n][a:a + 1], alone[n]), (a, n)
+
+
+def test_multi_adapter_sampled_oracle():
+    """Fused multi-adapter pass against the oracle: dy is non-zero only on tokens
+    of adapter 3, so adapter 3's gradients come from that sample alone and every
+    other adapter's gradients are exactly zero."""
+    shp = shape("multi")
+    inp = make_inputs(shp, seed=5, device="cuda")
+    a, per = 3, shp.T // shp.A
+    sample = [a * per + t for t in (0, 1, 100, 511, 777, 1023)]
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    one, oshp, sl = _adapter_slice(inp, shp, a)
+    local = [t - a * per for t in sample]
+    sub, sshp, used, tok = sub_problem(one, oshp, local)
+    y_ref = oracle.forward(sub, sshp)
+    g_ref = oracle.backward(sub, sshp)
+    gt = (tok + a * per).cuda()
+    assert_close("y", out["y"][gt].cpu(), y_ref)
+    assert_close("dx", out["dx"][gt].cpu(), g_ref["dx"])
+    assert_close("dw", out["dw"][gt].cpu(), g_ref["dw"])
+    ex = torch.as_tensor(used, device="cuda")
+    for n in ("dA1", "dA3", "dB2"):
+        assert_close(n, out[n][a:a + 1].cpu(), g_ref[n])
+    for n in ("dB1", "dB3", "dA2"):
+        assert_close(n, out[n][a:a + 1, ex].cpu(), g_ref[n])
+    others = [b for b in range(shp.A) if b != a]
+    for n in ADAPTER_GRADS:
+        assert out[n][others].abs().max().item() == 0, n

@@ -61,8 +61,9 @@ def step_flops(T, R, H, I, r):
     return 12.0 * R * H * I + 18.0 * T * H * r + 18.0 * R * I * r
 
 
-def kernel_work(T, R, H, I, r, k):
+def kernel_work(T, R, H, I, r, k, E=256):
     """Per-launch algorithmic FLOPs (tensor kernels) or bytes (HBM kernels)."""
+    E_I_H = float(E) * I * H
     fl = {
         "shrink_x_A13": 2.0 * T * H * 2 * r,
         "w13_lora_swiglu": 4.0 * R * H * I + 4.0 * R * I * r,
@@ -83,6 +84,7 @@ def kernel_work(T, R, H, I, r, k):
         "gather_bwd": 2.0 * (2 * R * H + 3 * R * r),
         "dw_reduce": 4.0 * (R * (I // 128) + T * k),
         "dy13_combine": 4.0 * R * 2 * r + 2.0 * T * 2 * r,
+        "dequant_mxfp4": (2.0 + 0.5 + 1.0 / 32) * E_I_H,
         "combine_y": 2.0 * (R * H + 2 * T * H),
         "combine_dx": 2.0 * (R * H + 2 * T * H),
         "plan_count": 4.0 * T * k, "plan_scan": 0.0, "plan_scatter": 4.0 * T * k * 3, "plan_finish": 0.0, "plan_wide": 0.0,
@@ -226,13 +228,13 @@ def run_ours(args, rank, world, local_rank):
     inp = make_inputs(shp, seed=2 + rank, device="cuda")
     T, H, I, E, k, r = shp.T, shp.H, shp.I, shp.E, shp.k, shp.r
     R = int((inp["topk_ids"] >= 0).sum())
-    d = m.make_dims(T, H, I, E, k, r, 1, shp.scale)
+    d = m.make_dims(T, H, I, E, k, r, 1, shp.scale, base_fmt=1 if shp.base_fmt == "mxfp4" else 0)
     ws = m.Workspaces.allocate(d)
     y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     dx = torch.empty_like(y)
     dw = torch.empty(T, k, dtype=torch.float32, device="cuda")
     g = m.alloc_grads(d)
-    wts = {n: inp[n] for n in WEIGHTS}
+    wts = {n: inp[n] for n in WEIGHTS + ("S1", "S3", "S2") if n in inp}
     stream = torch.cuda.current_stream()
 
     def step(x, ids, tw, dy):
@@ -284,7 +286,7 @@ def run_ours(args, rank, world, local_rank):
     prof = m.moe_lora_profile_read()
     m.moe_lora_profile_enable(False)
     pk = peaks()
-    fl, by = kernel_work(T, R, H, I, r, k)
+    fl, by = kernel_work(T, R, H, I, r, k, E)
     kernels = {}
     for name, (tot, n) in prof.items():
         avg = tot / n
@@ -441,7 +443,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="prod", choices=["prod", "prod_e16", "tiny", "edge"])
+    ap.add_argument("--workload", default="prod", choices=["prod", "prod_mxfp4", "prod_e16", "tiny", "edge"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -71,7 +71,8 @@ extern "C" {
 /* Problem sizes.  H and I must be multiples of 256; r a multiple of 8 in [8,128];
  * 1 <= k <= 32; 1 <= E; A >= 1 adapters; block_m must be 128 (the plan pads
  * every (adapter, expert) group to a multiple of it); act must be 0 (SwiGLU);
- * base_fmt must be 0 (bf16 base weights).  T may be 0 (every call is a no-op). */
+ * base_fmt 0 (bf16 base weights) or 1 (MXFP4 base weights, see moe_lora_weights).
+ * T may be 0 (every call is a no-op). */
 typedef struct moe_lora_dims {
   int64_t T;        /* tokens */
   int32_t H;        /* hidden size */
@@ -83,23 +84,33 @@ typedef struct moe_lora_dims {
   int32_t block_m;  /* plan padding unit, 128 */
   float scale;      /* side-LoRA scale s */
   int32_t act;      /* 0 = SwiGLU */
-  int32_t base_fmt; /* 0 = bf16 */
+  int32_t base_fmt; /* 0 = bf16, 1 = MXFP4 */
 } moe_lora_dims;
 
-/* Frozen base and adapter weights (device, bf16 bits).
- *   W1, W3 [E,I,H]; W2 [E,H,I];
+/* Frozen base and adapter weights (device).
+ *   W1, W3 [E,I,H]; W2 [E,H,I]: bf16 bits when base_fmt = 0.  When base_fmt = 1
+ *     (MXFP4) they hold E2M1 element codes, two per byte (low nibble = lower index
+ *     along the last axis), and S1, S3 [E,I,H/32], S2 [E,H,I/32] hold one UE8M0
+ *     scale byte (value 2^(b-127); 255 decodes to NaN) per 32 consecutive elements
+ *     of that axis: the OCP MX encoding, read from the pages' "E2M1 values with a
+ *     UE8M0 scale per 32 elements".  The base is decoded exactly to bf16 (in the
+ *     saved workspace) and the BF16 tensor-core path runs on it; the adapters
+ *     stay bf16.  S1/S3/S2 are ignored (may be NULL) when base_fmt = 0.
  *   A1, A3 [A,r,H] (shared by experts); B1, B3 [A,E,I,r] (expert-local);
- *   A2 [A,E,r,I] (expert-local); B2 [A,H,r] (shared). */
+ *   A2 [A,E,r,I] (expert-local); B2 [A,H,r] (shared), bf16 bits. */
 typedef struct moe_lora_weights {
-  const uint16_t* W1;
-  const uint16_t* W3;
-  const uint16_t* W2;
+  const void* W1;
+  const void* W3;
+  const void* W2;
   const uint16_t* A1;
   const uint16_t* A3;
   const uint16_t* B1;
   const uint16_t* B3;
   const uint16_t* A2;
   const uint16_t* B2;
+  const uint8_t* S1;
+  const uint8_t* S3;
+  const uint8_t* S2;
 } moe_lora_weights;
 
 /* Adapter gradients (device, fp32), same shapes as the factors they belong to. */

@@ -42,7 +42,8 @@ class Dims(ctypes.Structure):
 
 
 class Weights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2",
+                                                 "S1", "S3", "S2")]
 
 
 class Grads(ctypes.Structure):
@@ -93,8 +94,10 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def make_dims(T: int, H: int, I: int, E: int, k: int, r: int, A: int = 1, scale: float = 1.0) -> Dims:
-    return Dims(T, H, I, E, k, r, A, 128, float(scale), 0, 0)
+def make_dims(T: int, H: int, I: int, E: int, k: int, r: int, A: int = 1, scale: float = 1.0,
+              base_fmt: int = 0) -> Dims:
+    """base_fmt: 0 = bf16 base weights, 1 = MXFP4 (packed E2M1 codes + UE8M0 scales S1/S3/S2)."""
+    return Dims(T, H, I, E, k, r, A, 128, float(scale), 0, int(base_fmt))
 
 
 def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]:
@@ -172,14 +175,18 @@ def moe_lora_plan_readback(dims: Dims, plan_ws: torch.Tensor, stream=None) -> Di
             "route_of_row": rrow[:P].clone()}
 
 
-def _weights(w: Dict[str, torch.Tensor]) -> Weights:
-    return Weights(*[_ptr(w[n], torch.bfloat16, n) for n in ("W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")])
+def _weights(w: Dict[str, torch.Tensor], dims: Dims) -> Weights:
+    mx = dims.base_fmt == 1
+    base = [_ptr(w[n], torch.uint8 if mx else torch.bfloat16, n) for n in ("W1", "W3", "W2")]
+    side = [_ptr(w[n], torch.bfloat16, n) for n in ("A1", "A3", "B1", "B3", "A2", "B2")]
+    scales = [_ptr(w[n], torch.uint8, n) if mx else None for n in ("S1", "S3", "S2")]
+    return Weights(*(base + side + scales))
 
 
 def moe_lora_forward(dims: Dims, plan_ws: torch.Tensor, x: torch.Tensor, topk_w: torch.Tensor,
                      weights: Dict[str, torch.Tensor], y: torch.Tensor, saved: torch.Tensor,
                      scratch: torch.Tensor, stream=None) -> None:
-    W = _weights(weights)
+    W = _weights(weights, dims)
     rc = lib().moe_lora_forward(ctypes.byref(dims), _ptr(plan_ws), _ptr(x, torch.bfloat16, "x"),
                                 _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(W),
                                 _ptr(y, torch.bfloat16, "y"), _ptr(saved), saved.numel() * saved.element_size(),
@@ -191,7 +198,7 @@ def moe_lora_backward(dims: Dims, plan_ws: torch.Tensor, saved: torch.Tensor, x:
                       topk_w: torch.Tensor, dy: torch.Tensor, weights: Dict[str, torch.Tensor],
                       dx: torch.Tensor, dw: torch.Tensor, grads: Dict[str, torch.Tensor],
                       scratch: torch.Tensor, stream=None) -> None:
-    W = _weights(weights)
+    W = _weights(weights, dims)
     Gr = Grads(*[_ptr(grads[n], torch.float32, n) for n in ("dA1", "dA3", "dB1", "dB3", "dA2", "dB2")])
     rc = lib().moe_lora_backward(ctypes.byref(dims), _ptr(plan_ws), _ptr(saved), _ptr(x, torch.bfloat16, "x"),
                                  _ptr(topk_w, torch.float32, "topk_w"), _ptr(dy, torch.bfloat16, "dy"),

@@ -81,12 +81,19 @@ static int check_ptr(const void* p) {
   return MOE_LORA_OK;
 }
 
-static int check_weights(const moe_lora_weights* w) {
+static int check_weights(const moe_lora_dims* d, const moe_lora_weights* w) {
   if (!w) return MOE_LORA_ERR_NULL;
   const void* ps[] = {w->W1, w->W3, w->W2, w->A1, w->A3, w->B1, w->B3, w->A2, w->B2};
   for (const void* p : ps) {
     const int rc = check_ptr(p);
     if (rc) return rc;
+  }
+  if (d->base_fmt == 1) {
+    const void* sc[] = {w->S1, w->S3, w->S2};
+    for (const void* p : sc) {
+      const int rc = check_ptr(p);
+      if (rc) return rc;
+    }
   }
   return MOE_LORA_OK;
 }
@@ -140,7 +147,8 @@ int moe_lora_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t
                      size_t scratch_bytes, void* stream) {
   int rc = check_dims(d);
   if (rc) return rc;
-  if ((rc = check_ptr(plan_ws)) || (rc = check_weights(w)) || (rc = check_ptr(saved)) || (rc = check_ptr(scratch)))
+  if ((rc = check_ptr(plan_ws)) || (rc = check_weights(d, w)) || (rc = check_ptr(saved)) ||
+      (rc = check_ptr(scratch)))
     return rc;
   if (saved_bytes < saved_layout(d).total || scratch_bytes < fwd_layout(d).total) return MOE_LORA_ERR_WORKSPACE;
   if (d->T == 0) return MOE_LORA_OK;
@@ -156,7 +164,8 @@ int moe_lora_backward(const moe_lora_dims* d, const void* plan_ws, const void* s
                       const moe_lora_grads* g, void* scratch, size_t scratch_bytes, void* stream) {
   int rc = check_dims(d);
   if (rc) return rc;
-  if ((rc = check_ptr(plan_ws)) || (rc = check_weights(w)) || (rc = check_ptr(saved)) || (rc = check_ptr(scratch)))
+  if ((rc = check_ptr(plan_ws)) || (rc = check_weights(d, w)) || (rc = check_ptr(saved)) ||
+      (rc = check_ptr(scratch)))
     return rc;
   if (!g) return MOE_LORA_ERR_NULL;
   const void* gp[] = {g->dA1, g->dA3, g->dB1, g->dB3, g->dA2, g->dB2};

@@ -46,6 +46,10 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   const int max_tok_tiles = (int)((T + 127) / 128) + d->A;
   const int max_row_tiles = (int)(P / 128);
   cudaError_t ce;
+  // Base weights: as given (bf16), or the copy the forward decoded from MXFP4.
+  const void* bW1 = d->base_fmt == 1 ? (const void*)(sv + SL.W1) : w->W1;
+  const void* bW3 = d->base_fmt == 1 ? (const void*)(sv + SL.W3) : w->W3;
+  const void* bW2 = d->base_fmt == 1 ? (const void*)(sv + SL.W2) : w->W2;
 #define MAP(call)                                 \
   do {                                            \
     if ((call) != 0) return MOE_LORA_ERR_CUDA;    \
@@ -87,7 +91,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     ProbW2Dgrad p;
     MAP(tmap_2d(&p.mDp, Dp, H, P, 64, 128));
     MAP(tmap_2d(&p.mD2p, D2p, r, P, 64, 128));
-    MAP(tmap_3d(&p.mW2, w->W2, I, H, E, 64, 64));
+    MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 64));
     MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, 64));
     p.pl = pl;
     p.err = pl.err;
@@ -121,8 +125,8 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     ProbW13Dgrad p;
     MAP(tmap_2d(&p.mdG, dG, I, P, 64, 128));
     MAP(tmap_2d(&p.mdU, dU, I, P, 64, 128));
-    MAP(tmap_3d(&p.mW1, w->W1, H, I, E, 64, 64));
-    MAP(tmap_3d(&p.mW3, w->W3, H, I, E, 64, 64));
+    MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 64));
+    MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 64));
     MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 64));
     MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 64));
     p.pl = pl;

@@ -19,7 +19,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Returns MOE_LORA_OK when the sizes are supported.
 inline int check_dims(const moe_lora_dims* d) {
   if (!d) return MOE_LORA_ERR_NULL;
-  if (d->act != 0 || d->base_fmt != 0) return MOE_LORA_ERR_UNSUPPORTED;
+  if (d->act != 0 || (d->base_fmt != 0 && d->base_fmt != 1)) return MOE_LORA_ERR_UNSUPPORTED;
   if (d->T < 0 || d->T > (int64_t)1 << 30) return MOE_LORA_ERR_DIMS;
   if (d->H < 256 || d->H % 256 || d->I < 256 || d->I % 256) return MOE_LORA_ERR_DIMS;
   if (d->r < 8 || d->r > 128 || d->r % 8) return MOE_LORA_ERR_DIMS;
@@ -66,9 +66,10 @@ inline PlanLayout plan_layout(const moe_lora_dims* d) {
   return L;
 }
 
-// What the forward keeps for the backward (bf16 unless noted).
+// What the forward keeps for the backward (bf16 unless noted).  With an MXFP4
+// base it also holds the decoded bf16 base W1, W3 [E,I,H] and W2 [E,H,I].
 struct SavedLayout {
-  size_t Y13p, G, U, Act, Z2w, total;   // [P,2r], [P,I], [P,I], [P,I], [T,r]
+  size_t Y13p, G, U, Act, Z2w, W1, W3, W2, total;   // [P,2r], [P,I], [P,I], [P,I], [T,r]
 };
 inline SavedLayout saved_layout(const moe_lora_dims* d) {
   SavedLayout L;
@@ -80,6 +81,10 @@ inline SavedLayout saved_layout(const moe_lora_dims* d) {
   L.U = take(2 * (size_t)P * d->I);
   L.Act = take(2 * (size_t)P * d->I);
   L.Z2w = take(2 * (size_t)T * d->r);
+  const size_t wbytes = d->base_fmt == 1 ? 2 * (size_t)d->E * d->I * d->H : 0;
+  L.W1 = take(wbytes);
+  L.W3 = take(wbytes);
+  L.W2 = take(wbytes);
   L.total = o;
   return L;
 }

@@ -35,6 +35,24 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   const int max_row_tiles = (int)(P / 128);
   int rc = 0;
   cudaError_t ce;
+  // Base weights for the BF16 path: as given, or decoded from MXFP4 into `saved`
+  // (the backward reuses the decoded copy).
+  const void* bW1 = w->W1;
+  const void* bW3 = w->W3;
+  const void* bW2 = w->W2;
+  if (d->base_fmt == 1) {
+    uint16_t* q1 = (uint16_t*)(sv + SL.W1);
+    uint16_t* q3 = (uint16_t*)(sv + SL.W3);
+    uint16_t* q2 = (uint16_t*)(sv + SL.W2);
+    const int64_t n = (int64_t)E * I * H;
+    if (launch_dequant_mxfp4((const uint8_t*)w->W1, w->S1, q1, n, num_sms, stream) != cudaSuccess ||
+        launch_dequant_mxfp4((const uint8_t*)w->W3, w->S3, q3, n, num_sms, stream) != cudaSuccess ||
+        launch_dequant_mxfp4((const uint8_t*)w->W2, w->S2, q2, n, num_sms, stream) != cudaSuccess)
+      return MOE_LORA_ERR_CUDA;
+    bW1 = q1;
+    bW3 = q3;
+    bW2 = q2;
+  }
 #define MAP(call)               \
   do {                          \
     if ((rc = (call)) != 0) return MOE_LORA_ERR_CUDA; \
@@ -65,8 +83,8 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     ProbW13 p;
     MAP(tmap_2d(&p.mXp, Xp, H, P, 64, 128));
     MAP(tmap_2d(&p.mY13p, Y13p, 2 * r, P, 64, 128));
-    MAP(tmap_3d(&p.mW1, w->W1, H, I, E, 64, 128));
-    MAP(tmap_3d(&p.mW3, w->W3, H, I, E, 64, 128));
+    MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 128));
+    MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 128));
     MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 128));
     MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 128));
     p.pl = pl;
@@ -83,7 +101,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   {
     ProbW2 p;
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
-    MAP(tmap_3d(&p.mW2, w->W2, I, H, E, 64, 256));
+    MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 256));
     MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, r16));
     p.pl = pl;
     p.err = pl.err;

@@ -16,6 +16,10 @@ struct AdapterTable {
 cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const AdapterTable& at, void* ws,
                         cudaStream_t stream);
 
+// Decodes `elems` MXFP4 elements (E2M1 nibbles + one UE8M0 byte per 32) to bf16.
+cudaError_t launch_dequant_mxfp4(const uint8_t* packed, const uint8_t* scales, uint16_t* out, int64_t elems,
+                                 int num_sms, cudaStream_t stream);
+
 // Xp[p] = x[token(p)], Y13p[p] = Y13[token(p)]; zero rows for padding.
 cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint16_t* Xp,
                               uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream);

@@ -158,6 +158,35 @@ __global__ void combine_rows_kernel(PlanView pl, const uint16_t* __restrict__ ba
   }
 }
 
+// MXFP4 -> bf16, exactly: one thread per 32-element scale group (16 packed bytes
+// and one UE8M0 byte in, 64 bytes of bf16 out).  E2M1 magnitudes are
+// {0, 0.5, 1, 1.5, 2, 3, 4, 6} (bit 3 = sign); the scale byte b means 2^(b-127)
+// (b = 0 is the fp32 subnormal 2^-127, b = 255 is NaN).  Every product is a bf16
+// value, so the conversion below rounds nothing.
+__global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
+                                     uint16_t* __restrict__ out, int64_t groups) {
+  const float kMag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+  for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
+       gi += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 pk = __ldg(reinterpret_cast<const uint4*>(packed) + gi);
+    const uint32_t b = scales[gi];
+    const float sc = __uint_as_float(b == 0 ? 0x00400000u : b == 255 ? 0x7FC00000u : b << 23);
+    const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
+    uint16_t* dst = out + gi * 32;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v[8];
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const uint32_t code = (w[q] >> (4 * n)) & 15u;
+        const float mag = kMag[code & 7u] * sc;
+        v[n] = (code & 8u) ? -mag : mag;
+      }
+      st_bf16x8(dst + 8 * q, v);
+    }
+  }
+}
+
 int grid_for(int num_sms) { return num_sms * 8; }
 
 }  // namespace
@@ -167,6 +196,14 @@ cudaError_t launch_combine_rows(const PlanView& pl, const uint16_t* base, const 
   prof_begin(slot, stream);
   combine_rows_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, base, src, topk_w, out, H);
   prof_end(slot, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_mxfp4(const uint8_t* packed, const uint8_t* scales, uint16_t* out, int64_t elems,
+                                 int num_sms, cudaStream_t stream) {
+  prof_begin(K_DEQUANT, stream);
+  dequant_mxfp4_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(packed, scales, out, elems / 32);
+  prof_end(K_DEQUANT, stream);
   return cudaGetLastError();
 }
 

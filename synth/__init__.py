@@ -99,9 +99,22 @@ def route_topk(logits: torch.Tensor, k: int):
 _E2M1_GRID = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
 
-def mxfp4_quantize(w: torch.Tensor):
+def mxfp4_quantize(w: torch.Tensor, chunk: int = 1 << 22):
     """w: [..., K] (K % 32 == 0) -> (packed uint8 [..., K/2], scales uint8 [..., K/32]).
-    Low nibble holds the element with the lower K index."""
+    Low nibble holds the element with the lower K index.  Large tensors are
+    quantised in slices of `chunk` 32-element groups to bound temporaries."""
+    K = w.shape[-1]
+    groups = w.numel() // 32
+    if groups > chunk:
+        flat = w.reshape(-1, 32)
+        parts = [_mxfp4_quantize(flat[s:s + chunk]) for s in range(0, groups, chunk)]
+        packed = torch.cat([p for p, _ in parts]).reshape(*w.shape[:-1], K // 2)
+        scales = torch.cat([q for _, q in parts]).reshape(*w.shape[:-1], K // 32)
+        return packed.contiguous(), scales.contiguous()
+    return _mxfp4_quantize(w)
+
+
+def _mxfp4_quantize(w: torch.Tensor):
     K = w.shape[-1]
     assert K % 32 == 0
     lead = w.shape[:-1]

@@ -40,7 +40,8 @@ def assert_close(name: str, got: torch.Tensor, ref: torch.Tensor) -> None:
 
 
 def dims_of(shp: Shape, scale: Optional[float] = None) -> m.Dims:
-    return m.make_dims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, shp.scale if scale is None else scale)
+    return m.make_dims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, shp.scale if scale is None else scale,
+                       base_fmt=1 if shp.base_fmt == "mxfp4" else 0)
 
 
 def run_gpu(inp: Dict[str, torch.Tensor], shp: Shape, scale: Optional[float] = None, poison: bool = False,
@@ -99,11 +100,13 @@ def sub_problem(inp: Dict[str, torch.Tensor], shp: Shape, tokens: Iterable[int])
         "adapter_offsets": torch.tensor([0, len(tok)], dtype=torch.int64),
     }
     exd = ex.to(inp["W1"].device)
-    for n in ("W1", "W3", "W2"):
-        sub[n] = inp[n][exd].cpu()
+    for n in ("W1", "W3", "W2", "S1", "S3", "S2"):
+        if n in inp:
+            sub[n] = inp[n][exd].cpu()
     for n in ("B1", "B3", "A2"):
         sub[n] = inp[n][:, exd].cpu()
     for n in ("A1", "A3", "B2"):
         sub[n] = inp[n].cpu()
-    sshp = Shape(T=len(tok), H=shp.H, I=shp.I, E=len(used), k=shp.k, r=shp.r, A=1, scale=shp.scale)
+    sshp = Shape(T=len(tok), H=shp.H, I=shp.I, E=len(used), k=shp.k, r=shp.r, A=1, scale=shp.scale,
+                 base_fmt=shp.base_fmt)
     return sub, sshp, used, tok

@@ -303,3 +303,49 @@ def test_multi_adapter_sampled_oracle():
     others = [b for b in range(shp.A) if b != a]
     for n in ADAPTER_GRADS:
         assert out[n][others].abs().max().item() == 0, n
+
+
+# ----------------------------------------------------------------------------- MXFP4 base
+def _decode_mxfp4_golden(packed, scales):
+    """bf16 values of an MXFP4 tensor from the OCP table in tests/golden (host)."""
+    rows = [l.split() for l in open(os.path.join(os.path.dirname(__file__), "golden", "e2m1_ue8m0.txt"))
+            if l.strip() and l[0] != "#"]
+    table = torch.tensor([float(v) for kd, c, v in rows if kd == "e2m1"], dtype=torch.float64)
+    p = packed.cpu()
+    codes = torch.stack([(p & 15).long(), (p >> 4).long()], dim=-1).reshape(*p.shape[:-1], p.shape[-1] * 2)
+    sc = torch.exp2(scales.cpu().double() - 127).repeat_interleave(32, dim=-1)
+    return (table[codes] * sc).to(torch.bfloat16)
+
+
+def test_mxfp4_tiny_forward_backward():
+    shp = Shape(T=200, H=512, I=256, E=16, k=2, r=16, mask_frac=0.1, base_fmt="mxfp4")
+    inp = make_inputs(shp, seed=31)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    _full_check(inp, shp, out)
+
+
+def test_mxfp4_equals_decoded_bf16_base_bitwise():
+    """An MXFP4 base gives bit for bit what the same layer gives with the decoded
+    values as a bf16 base (the decode is exact)."""
+    shp = Shape(T=256, H=512, I=256, E=16, k=2, r=16, base_fmt="mxfp4")
+    inp = make_inputs(shp, seed=32)
+    q = run_gpu(inp, shp)
+    deq = {n: v for n, v in inp.items() if n not in ("S1", "S3", "S2")}
+    for n in ("W1", "W3", "W2"):
+        deq[n] = _decode_mxfp4_golden(inp[n], inp["S" + n[1]])
+    b = run_gpu(deq, Shape(T=256, H=512, I=256, E=16, k=2, r=16))
+    for n in ("y", "dx", "dw") + ADAPTER_GRADS:
+        assert torch.equal(q[n], b[n]), n
+
+
+def test_mxfp4_production_width_sampled():
+    """MXFP4 base at production widths (H=4096, I=2048, E=256, top-6, rank 128),
+    2,048 tokens, sampled sparse-dy parity against the oracle."""
+    shp = shape("prod_mxfp4", 2048)
+    inp = make_inputs(shp, seed=33, device="cuda")
+    sample = [0, 5, 333, 1024, 2047]
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    _sampled_check(inp, shp, out, sample)

@@ -40,6 +40,17 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   float* dY13 = (float*)(sc + BL.dY13);
   uint16_t* dY13w = (uint16_t*)(sc + BL.dY13w);
   uint16_t* dXl = (uint16_t*)(sc + BL.dXl);
+  float* ksplit = (float*)(sc + BL.ksplit);
+  // Token-range slices for the two long-K reductions (dB2, dA1/dA3), at least 256
+  // K steps (16,384 tokens) each.  The choice depends only on the adapter's own
+  // token count, and several adapters are never split, so an adapter's gradients
+  // from a shared pass equal its standalone run bit for bit whenever it has fewer
+  // than 32,768 tokens.
+  auto pick_split = [&]() {
+    if (d->A > 1) return 1;
+    const int64_t sp = ((d->T + 63) / 64) / 256;
+    return (int)(sp < 1 ? 1 : sp > kMaxSplit ? kMaxSplit : sp);
+  };
 
   const uint64_t T = (uint64_t)d->T, H = d->H, I = d->I, E = d->E, A = d->A, r = d->r;
   const uint64_t P = (uint64_t)rows_cap(d), G = A * E;
@@ -78,11 +89,14 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     MAP(tmap_2d(&p.mZ2w, Z2w, r, T, 64, 64));
     p.pl = pl;
     p.err = pl.err;
-    p.dB2 = gr->dB2;
+    p.split = pick_split();
+    p.out = p.split > 1 ? ksplit : gr->dB2;
+    p.split_stride = (int64_t)A * H * r;
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, d->A * (d->H / 128), num_sms, stream, K_DB2));
+    LAUNCH(launch_gemm(p, p.split * d->A * (d->H / 128), num_sms, stream, K_DB2));
+    if (p.split > 1) LAUNCH(launch_reduce_splits(ksplit, p.split_stride, p.split, p.split_stride, gr->dB2, num_sms, stream));
   }
   // B2: routed dy rows and the scaled shared-expand gradients
   LAUNCH(launch_gather_bwd(pl, dy, dyB2, topk_w, Dp, D2p, dZ2p, d->H, d->r, d->scale, num_sms, stream));
@@ -176,11 +190,19 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     MAP(tmap_2d(&p.mx, x, H, T, 64, 64));
     p.pl = pl;
     p.err = pl.err;
-    p.dA1 = gr->dA1;
-    p.dA3 = gr->dA3;
+    const int tiles = d->A * ((2 * d->r + 127) / 128) * (d->H / 256);
+    p.split = pick_split();
+    const int64_t n1 = (int64_t)A * r * H;
+    p.out1 = p.split > 1 ? ksplit : gr->dA1;
+    p.out3 = p.split > 1 ? ksplit + n1 : gr->dA3;
+    p.split_stride = 2 * n1;
     p.H = d->H;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, d->A * ((2 * d->r + 127) / 128) * (d->H / 256), num_sms, stream, K_DA13));
+    LAUNCH(launch_gemm(p, p.split * tiles, num_sms, stream, K_DA13));
+    if (p.split > 1) {
+      LAUNCH(launch_reduce_splits(ksplit, 2 * n1, p.split, n1, gr->dA1, num_sms, stream));
+      LAUNCH(launch_reduce_splits(ksplit + n1, 2 * n1, p.split, n1, gr->dA3, num_sms, stream));
+    }
   }
 #undef MAP
 #undef LAUNCH

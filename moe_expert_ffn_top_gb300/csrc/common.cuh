@@ -13,6 +13,7 @@ constexpr int kBlockM = 128;       // plan padding unit = GEMM M tile
 constexpr int kMaxAdapters = 64;   // adapters sharing one layer
 constexpr int kMaxGroups = 16384;  // adapters x experts
 constexpr int kPlanChunk = 1024;   // routes per plan chunk (one warp each)
+constexpr int kMaxSplit = 8;       // token-range slices of the long-K reductions
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -108,8 +109,9 @@ inline FwdLayout fwd_layout(const moe_lora_dims* d) {
 struct BwdLayout {
   // dyB2 [T,r] bf16; Dp [P,H] bf16 (reused for dXp); D2p, dZ2p [P,r] bf16;
   // dG, dU [P,I] bf16; part [P, I/128] f32; dY13 [P,2r] f32; dY13w [T,2r] bf16;
-  // dXl [T,H] bf16 (grad-x through A1/A3)
-  size_t dyB2, Dp, D2p, dZ2p, dG, dU, part, dY13, dY13w, dXl, total;
+  // dXl [T,H] bf16 (grad-x through A1/A3); ksplit: fp32 partials of the
+  // token-split dB2 and dA1/dA3 reductions [kMaxSplit][2][A][r][H]
+  size_t dyB2, Dp, D2p, dZ2p, dG, dU, part, dY13, dY13w, dXl, ksplit, total;
 };
 inline BwdLayout bwd_layout(const moe_lora_dims* d) {
   BwdLayout L;
@@ -126,6 +128,7 @@ inline BwdLayout bwd_layout(const moe_lora_dims* d) {
   L.dY13 = take(4 * (size_t)P * 2 * d->r);
   L.dY13w = take(2 * (size_t)T * 2 * d->r);
   L.dXl = take(2 * (size_t)T * d->H);
+  L.ksplit = take(4 * (size_t)kMaxSplit * 2 * d->A * d->r * d->H);
   L.total = o;
   return L;
 }

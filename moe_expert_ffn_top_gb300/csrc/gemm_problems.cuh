@@ -386,6 +386,9 @@ struct ProbDyB2 {
 // =====================================================================================
 // Backward B1b -- dB2_a = s * dy^T Z2w over the adapter's tokens  [H,r] fp32.
 // M = H, N = r, K = tokens.  A: (m=h, k=t) = dy[t][h] MN-major; B: (n=q, k=t) = Z2w[t][q] MN-major.
+// The token range is cut into `split` slices of whole 64-token steps (few output
+// tiles, very long K); slice s writes out + s*split_stride, summed afterwards in
+// slice order by reduce_splits.
 // =====================================================================================
 struct ProbDB2 {
   static constexpr bool kAmn = true, kBmn = true;
@@ -394,21 +397,27 @@ struct ProbDB2 {
   CUtensorMap mdy, mZ2w;  // dy (H,T) box(64,64); Z2w (r,T) box(64,64)
   PlanView pl;
   int* err;
-  float* dB2;
-  int H, r;
+  float* out;  // dB2, or the split partials
+  int64_t split_stride;
+  int H, r, split;
   float s;
-  __device__ int num_tiles() const { return pl.A * (H / 128); }
+  __device__ int num_tiles() const { return split * pl.A * (H / 128); }
   __device__ TileInfo tile(int t) const {
-    const int a = t / (H / 128), mt = t % (H / 128);
+    const int per = pl.A * (H / 128);
+    const int sp = t / per, a = (t % per) / (H / 128), mt = t % (H / 128);
     TileInfo ti;
     ti.g = a;
     ti.m0 = mt * 128;
     ti.mend = H;
     ti.n0 = 0;
-    ti.sub = 0;
-    ti.k0 = pl.tok_off[a];
-    ti.nk = (pl.tok_off[a + 1] - pl.tok_off[a] + kBK - 1) / kBK;
+    ti.sub = sp;
+    const int nk = (pl.tok_off[a + 1] - pl.tok_off[a] + kBK - 1) / kBK, cs = (nk + split - 1) / split;
+    ti.k0 = pl.tok_off[a] + sp * cs * kBK;
+    ti.nk = max(0, min(cs, nk - sp * cs));
     return ti;
+  }
+  __device__ float* row_ptr(const TileInfo& ti, int64_t h) const {
+    return out + ti.sub * split_stride + ((int64_t)ti.g * H + h) * r;
   }
   __device__ void prefetch() const {
     tma_prefetch_map(&mdy);
@@ -428,13 +437,13 @@ struct ProbDB2 {
     for (int c = c0; c < r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, v, s, r - c < 32 ? r - c : 32);
+      store_row_f32(row_ptr(ti, h) + c, v, s, r - c < 32 ? r - c : 32);
     }
   }
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     const float z[32] = {};
     const int64_t h = (int64_t)ti.m0 + row;
-    for (int c = c0; c < r; c += cs) store_row_f32(dB2 + ((int64_t)ti.g * H + h) * r + c, z, 0.f, r - c < 32 ? r - c : 32);
+    for (int c = c0; c < r; c += cs) store_row_f32(row_ptr(ti, h) + c, z, 0.f, r - c < 32 ? r - c : 32);
   }
 };
 
@@ -805,6 +814,8 @@ struct ProbA13Expand {
 // Backward -- shared A1/A3 gradients, per adapter over its tokens:
 //   [dA1; dA3]_a = dY13w^T x   [2r,H] fp32
 // M = 2r (tiles of 128), N = H (tiles of 256), K = tokens.  Both operands MN-major.
+// Split over the token range like dB2: slice s writes dA1 rows to out1 and dA3
+// rows to out3, each offset by s*split_stride.
 // =====================================================================================
 struct ProbDA13 {
   static constexpr bool kAmn = true, kBmn = true;
@@ -813,23 +824,26 @@ struct ProbDA13 {
   CUtensorMap mdY13w, mx;  // dY13w (2r,T) box(64,64); x (H,T) box(64,64)
   PlanView pl;
   int* err;
-  float *dA1, *dA3;
-  int H, r;
+  float *out1, *out3;  // dA1 / dA3, or the split partials
+  int64_t split_stride;
+  int H, r, split;
   __device__ int ntm() const { return (2 * r + 127) / 128; }
   __device__ int ntn() const { return H / 256; }
-  __device__ int num_tiles() const { return pl.A * ntm() * ntn(); }
+  __device__ int num_tiles() const { return split * pl.A * ntm() * ntn(); }
   __device__ TileInfo tile(int t) const {
     const int per = ntm() * ntn();
-    const int a = t / per, rem = t % per;
+    const int sp = t / (pl.A * per), ta = t % (pl.A * per);
+    const int a = ta / per, rem = ta % per;
     const int mt = rem / ntn(), nt = rem % ntn();
     TileInfo ti;
     ti.g = a;
     ti.m0 = mt * 128;
     ti.mend = 2 * r;
     ti.n0 = nt * 256;
-    ti.sub = 0;
-    ti.k0 = pl.tok_off[a];
-    ti.nk = (pl.tok_off[a + 1] - pl.tok_off[a] + kBK - 1) / kBK;
+    ti.sub = sp;
+    const int nk = (pl.tok_off[a + 1] - pl.tok_off[a] + kBK - 1) / kBK, cs = (nk + split - 1) / split;
+    ti.k0 = pl.tok_off[a] + sp * cs * kBK;
+    ti.nk = max(0, min(cs, nk - sp * cs));
     return ti;
   }
   __device__ void prefetch() const {
@@ -845,7 +859,8 @@ struct ProbDA13 {
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
   __device__ float* out_row(const TileInfo& ti, int m) const {
-    return (m < r ? dA1 + ((int64_t)ti.g * r + m) * H : dA3 + ((int64_t)ti.g * r + (m - r)) * H) + ti.n0;
+    const int64_t so = ti.sub * split_stride;
+    return (m < r ? out1 + so + ((int64_t)ti.g * r + m) * H : out3 + so + ((int64_t)ti.g * r + (m - r)) * H) + ti.n0;
   }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
     const int m = ti.m0 + row;

@@ -16,6 +16,10 @@ struct AdapterTable {
 cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const AdapterTable& at, void* ws,
                         cudaStream_t stream);
 
+// out[i] = sum_s in[s*stride + i] for s = 0..split-1 in order (fp32, n % 4 == 0).
+cudaError_t launch_reduce_splits(const float* in, int64_t stride, int split, int64_t n, float* out, int num_sms,
+                                 cudaStream_t stream);
+
 // Decodes `elems` MXFP4 elements (E2M1 nibbles + one UE8M0 byte per 32) to bf16.
 cudaError_t launch_dequant_mxfp4(const uint8_t* packed, const uint8_t* scales, uint16_t* out, int64_t elems,
                                  int num_sms, cudaStream_t stream);

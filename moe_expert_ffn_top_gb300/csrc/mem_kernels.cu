@@ -187,6 +187,22 @@ __global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ packed, const u
   }
 }
 
+// out[i] = sum over s = 0..split-1 (in order) of in[s * stride + i]; n % 4 == 0.
+__global__ void reduce_splits_kernel(const float* __restrict__ in, int64_t stride, int split, int64_t n,
+                                     float* __restrict__ out) {
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n; i += (int64_t)gridDim.x * blockDim.x * 4) {
+    float4 a = *reinterpret_cast<const float4*>(in + i);
+    for (int s = 1; s < split; ++s) {
+      const float4 b = *reinterpret_cast<const float4*>(in + s * stride + i);
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    *reinterpret_cast<float4*>(out + i) = a;
+  }
+}
+
 int grid_for(int num_sms) { return num_sms * 8; }
 
 }  // namespace
@@ -204,6 +220,14 @@ cudaError_t launch_dequant_mxfp4(const uint8_t* packed, const uint8_t* scales, u
   prof_begin(K_DEQUANT, stream);
   dequant_mxfp4_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(packed, scales, out, elems / 32);
   prof_end(K_DEQUANT, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_splits(const float* in, int64_t stride, int split, int64_t n, float* out, int num_sms,
+                                 cudaStream_t stream) {
+  prof_begin(K_SPLIT_REDUCE, stream);
+  reduce_splits_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(in, stride, split, n, out);
+  prof_end(K_SPLIT_REDUCE, stream);
   return cudaGetLastError();
 }
 

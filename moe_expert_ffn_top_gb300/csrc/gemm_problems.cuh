@@ -509,14 +509,23 @@ struct ProbW2Dgrad {
     const float w = live ? topk_w[rt] : 0.0f;
     const int64_t base = p * I + ti.n0;
     float dot = 0.0f;
+    // saved G, U and activation of the chunk, loaded one chunk ahead so their
+    // latency overlaps the previous chunk's arithmetic and stores
+    uint4 gu[4], uu[4], au[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      gu[j] = __ldg(reinterpret_cast<const uint4*>(G + base + c0) + j);
+      uu[j] = __ldg(reinterpret_cast<const uint4*>(U + base + c0) + j);
+      au[j] = __ldg(reinterpret_cast<const uint4*>(Act + base + c0) + j);
+    }
     for (int c = c0; c < 256; c += cs) {
-      // the chunk's saved G, U and activation: all 12 loads in flight first
-      uint4 gu[4], uu[4], au[4];
+      uint4 gn[4], un[4], an[4];
+      const int cn = c + cs < 256 ? c + cs : c;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        gu[j] = __ldg(reinterpret_cast<const uint4*>(G + base + c) + j);
-        uu[j] = __ldg(reinterpret_cast<const uint4*>(U + base + c) + j);
-        au[j] = __ldg(reinterpret_cast<const uint4*>(Act + base + c) + j);
+        gn[j] = __ldg(reinterpret_cast<const uint4*>(G + base + cn) + j);
+        un[j] = __ldg(reinterpret_cast<const uint4*>(U + base + cn) + j);
+        an[j] = __ldg(reinterpret_cast<const uint4*>(Act + base + cn) + j);
       }
       float q[32];
       tmem_ld32(taddr + c, q);
@@ -546,6 +555,12 @@ struct ProbW2Dgrad {
         }
         st_bf16x8(dG + base + c + j, og);
         st_bf16x8(dU + base + c + j, ou);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gu[j] = gn[j];
+        uu[j] = un[j];
+        au[j] = an[j];
       }
     }
     part[p * ((cs / 32) * ntn()) + (cs / 32) * ti.sub + c0 / 32] = live ? dot : 0.0f;

@@ -21,18 +21,57 @@ __device__ __forceinline__ void copy_row_or_zero(uint16_t* dst, const uint16_t* 
   }
 }
 
+// Zero the padding rows of each group (rows [offsets[g] + counts[g], offsets[g+1]))
+// in up to two routed-row buffers; one warp per padding row.
+__device__ __forceinline__ void zero_padding_rows(const PlanView& pl, uint16_t* a, int na, uint16_t* b, int nb) {
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = blockDim.x >> 5, wib = threadIdx.x >> 5;
+  for (int g = blockIdx.x; g < pl.G; g += gridDim.x) {
+    const int beg = pl.offsets[g] + pl.counts[g], end = pl.offsets[g + 1];
+    for (int64_t p = beg + wib; p < end; p += warps_per_block) {
+      copy_row_or_zero(a + p * na, nullptr, na, lane);
+      if (b) copy_row_or_zero(b + p * nb, nullptr, nb, lane);
+    }
+  }
+}
+
+// Forward routed rows by scatter: one warp per token reads its x row (and Y13 row)
+// once and writes a copy to each of the token's routed rows; padding rows are
+// zeroed.  Reads T*H instead of k*T*H elements compared with a per-row gather.
 __global__ void gather_fwd_kernel(PlanView pl, const uint16_t* __restrict__ x, const uint16_t* __restrict__ Y13,
                                   uint16_t* __restrict__ Xp, uint16_t* __restrict__ Y13p, int H, int r2) {
-  const int64_t P = pl.offsets[pl.G];
   const int lane = threadIdx.x & 31;
   const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t p = w0; p < P; p += nw) {
-    const int rt = pl.route_of_row[p];
-    const int64_t t = rt >= 0 ? rt / pl.k : -1;
-    copy_row_or_zero(Xp + p * H, t >= 0 ? x + t * H : nullptr, H, lane);
-    copy_row_or_zero(Y13p + p * r2, t >= 0 ? Y13 + t * r2 : nullptr, r2, lane);
+  const int k = pl.k;
+  for (int64_t t = w0; t < pl.T; t += nw) {
+    const int* rows = pl.row_of_route + t * k;
+    for (int c0 = 0; c0 < H; c0 += 32 * 8 * 8) {  // 2048 columns per pass: 8 x 16 B per lane
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + (i * 32 + lane) * 8;
+        v[i] = c < H ? __ldg(reinterpret_cast<const uint4*>(x + t * H + c)) : make_uint4(0, 0, 0, 0);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int R = rows[j];
+        if (R < 0) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + (i * 32 + lane) * 8;
+          if (c < H) *reinterpret_cast<uint4*>(Xp + (int64_t)R * H + c) = v[i];
+        }
+      }
+    }
+    for (int c = lane * 8; c < r2; c += 32 * 8) {
+      const uint4 y = __ldg(reinterpret_cast<const uint4*>(Y13 + t * r2 + c));
+      for (int j = 0; j < k; ++j) {
+        const int R = rows[j];
+        if (R >= 0) *reinterpret_cast<uint4*>(Y13p + (int64_t)R * r2 + c) = y;
+      }
+    }
   }
+  zero_padding_rows(pl, Xp, H, Y13p, r2);
 }
 
 // one warp per token; lane covers r/32.. columns (r <= 128 -> up to 4 per lane)
@@ -64,24 +103,54 @@ __global__ void z2w_kernel(PlanView pl, const uint16_t* __restrict__ Z2, const f
   }
 }
 
+// Backward routed rows by scatter (as gather_fwd_kernel): Dp gets the token's dy
+// row, D2p = bf16(s*dyB2) and dZ2p = bf16(s*w*dyB2) of the token; padding rows zero.
 __global__ void gather_bwd_kernel(PlanView pl, const uint16_t* __restrict__ dy, const uint16_t* __restrict__ dyB2,
                                   const float* __restrict__ topk_w, uint16_t* __restrict__ Dp,
                                   uint16_t* __restrict__ D2p, uint16_t* __restrict__ dZ2p, int H, int r, float s) {
-  const int64_t P = pl.offsets[pl.G];
   const int lane = threadIdx.x & 31;
   const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t p = w0; p < P; p += nw) {
-    const int rt = pl.route_of_row[p];
-    const int64_t t = rt >= 0 ? rt / pl.k : -1;
-    copy_row_or_zero(Dp + p * H, t >= 0 ? dy + t * H : nullptr, H, lane);
-    const float w = rt >= 0 ? topk_w[rt] : 0.0f;
+  const int k = pl.k;
+  for (int64_t t = w0; t < pl.T; t += nw) {
+    const int* rows = pl.row_of_route + t * k;
+    for (int c0 = 0; c0 < H; c0 += 32 * 8 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + (i * 32 + lane) * 8;
+        v[i] = c < H ? __ldg(reinterpret_cast<const uint4*>(dy + t * H + c)) : make_uint4(0, 0, 0, 0);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int R = rows[j];
+        if (R < 0) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + (i * 32 + lane) * 8;
+          if (c < H) *reinterpret_cast<uint4*>(Dp + (int64_t)R * H + c) = v[i];
+        }
+      }
+    }
     for (int q = lane; q < r; q += 32) {
-      const float v = t >= 0 ? __uint_as_float((uint32_t)dyB2[t * r + q] << 16) : 0.0f;
+      const float v = __uint_as_float((uint32_t)dyB2[t * r + q] << 16);
       __nv_bfloat16 a = __float2bfloat16_rn(s * v);
-      __nv_bfloat16 b = __float2bfloat16_rn(s * w * v);
-      D2p[p * r + q] = *reinterpret_cast<uint16_t*>(&a);
-      dZ2p[p * r + q] = *reinterpret_cast<uint16_t*>(&b);
+      for (int j = 0; j < k; ++j) {
+        const int R = rows[j];
+        if (R < 0) continue;
+        __nv_bfloat16 b = __float2bfloat16_rn(s * topk_w[t * k + j] * v);
+        D2p[(int64_t)R * r + q] = *reinterpret_cast<uint16_t*>(&a);
+        dZ2p[(int64_t)R * r + q] = *reinterpret_cast<uint16_t*>(&b);
+      }
+    }
+  }
+  zero_padding_rows(pl, Dp, H, nullptr, 0);
+  // D2p and dZ2p padding rows (r columns, r % 8 == 0)
+  const int wib = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  for (int g = blockIdx.x; g < pl.G; g += gridDim.x) {
+    const int beg = pl.offsets[g] + pl.counts[g], end = pl.offsets[g + 1];
+    for (int64_t p = beg + wib; p < end; p += wpb) {
+      copy_row_or_zero(D2p + p * r, nullptr, r, lane);
+      copy_row_or_zero(dZ2p + p * r, nullptr, r, lane);
     }
   }
 }

@@ -79,9 +79,9 @@ def kernel_work(T, R, H, I, r, k, E=256):
         "dA13": 4.0 * T * r * H,
     }
     by = {
-        "gather_fwd": 2.0 * (2 * R * H + 2 * R * 2 * r),
+        "gather_fwd": 2.0 * (T * H + R * H + 2 * R * 2 * r),
         "z2_combine": 2.0 * (R * r + T * r),
-        "gather_bwd": 2.0 * (2 * R * H + 3 * R * r),
+        "gather_bwd": 2.0 * (T * H + R * H + 3 * R * r),
         "dw_reduce": 4.0 * (R * (I // 128) + T * k),
         "dy13_combine": 4.0 * R * 2 * r + 2.0 * T * 2 * r,
         "dequant_mxfp4": (2.0 + 0.5 + 1.0 / 32) * E_I_H,

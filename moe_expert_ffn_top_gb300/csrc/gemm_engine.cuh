@@ -21,7 +21,8 @@
 //   void     prefetch() const;              tensor-map prefetch
 //   void     load(const TileInfo&, int ks, uint8_t* sA, uint8_t* sB, uint64_t* bar) const;
 //   MmaStep  mma_step(const TileInfo&, int ks) const;
-//   void     epilogue(const TileInfo&, int row, uint32_t tmem_lane_addr, int c0, int cs) const;
+//   void     epilogue(const TileInfo&, int row, uint32_t tmem_lane_addr, int c0, int cs,
+//                     uint32_t* stg) const;    stg: the warp's staging buffer
 //   void     epilogue_empty(const TileInfo&, int row, int c0, int cs) const;   (tiles with nk == 0)
 //   static constexpr bool kWide;           256-row tiles (see EngineShape)
 // An epilogue warp handles the 32-column chunks c = c0, c0 + cs, ... of its row.
@@ -41,7 +42,11 @@ namespace moelora {
 constexpr int kBK = 64;
 constexpr int kBStageBytes = 256 * 128;  // 32 KB: up to 256 rows x 64 bf16
 constexpr int kAccCols = 256;
-constexpr int kGemmSmemBytes = 192 * 1024 + 1024 + 256;
+// Per epilogue warp: a 32-row staging buffer (17-word pitch: conflict-free row
+// writes) used to turn row-per-thread accumulator data into coalesced row segments.
+constexpr int kStgPitch = 17;
+constexpr int kStgWordsPerWarp = 32 * kStgPitch;
+constexpr int kGemmSmemBytes = 192 * 1024 + 1024 + 256 + 8 * kStgWordsPerWarp * 4;
 
 // Per-problem pipeline shape.  Narrow problems: 128-row tiles, 4 stages of
 // (A 16 KB + B 32 KB), two TMEM accumulators (the epilogue of one tile overlaps the
@@ -89,6 +94,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
   uint64_t* tfull = empty + S::kStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + S::kStages * S::kStage + 256);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = p.err;
 
@@ -210,7 +216,8 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
       tc_fence_after();
       if (!S::kWide || half < ti.mh) {
         const uint32_t col = (uint32_t)(S::kWide ? half * kAccCols : acc * kAccCols);
-        p.epilogue(ti, row, tmem_base + col + ((uint32_t)(q * 32) << 16), c0, cs);
+        p.epilogue(ti, row, tmem_base + col + ((uint32_t)(q * 32) << 16), c0, cs,
+                   stg_base + (warp - 2) * kStgWordsPerWarp);
       }
       tc_fence_before();
       __syncwarp();

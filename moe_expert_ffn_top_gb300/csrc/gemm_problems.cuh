@@ -84,6 +84,59 @@ __device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], 
 
 __device__ __forceinline__ int round16(int r) { return (r + 15) & ~15; }
 
+// Coalesced epilogue row access.  An epilogue warp owns 32 consecutive
+// accumulator rows, one per lane.  Storing "my row" directly makes every 16-byte
+// warp store touch 32 different rows; instead the warp stages its 32 x 32-column
+// chunk in shared memory and writes it back 4 lanes per row (8 rows of 64
+// contiguous bytes per instruction).  Loads go the same way in reverse.
+
+// dst0: row 0 of the warp, first column of the chunk; rows >= nvalid are skipped.
+__device__ __forceinline__ void warp_store_rows_bf16(uint16_t* dst0, int64_t ld, int nvalid, const float (&v)[32],
+                                                     float mul, uint32_t* stg) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) stg[lane * kStgPitch + j] = pack_bf16x2(v[2 * j] * mul, v[2 * j + 1] * mul);
+  __syncwarp();
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int r = s * 8 + (lane >> 2), w = (lane & 3) * 4;
+    const uint32_t* src = stg + r * kStgPitch + w;
+    const uint4 u = make_uint4(src[0], src[1], src[2], src[3]);
+    if (r < nvalid) *reinterpret_cast<uint4*>(dst0 + (int64_t)r * ld + 2 * w) = u;
+  }
+  __syncwarp();
+}
+
+// Issues the coalesced global loads of a warp's 32 rows x 32 bf16 columns.
+__device__ __forceinline__ void warp_load_rows_issue(const uint16_t* src0, int64_t ld, uint4 (&u)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int r = s * 8 + (lane >> 2);
+    u[s] = __ldg(reinterpret_cast<const uint4*>(src0 + (int64_t)r * ld + (lane & 3) * 8));
+  }
+}
+// Redistributes loaded rows so each lane holds its own row's 32 values.
+__device__ __forceinline__ void warp_rows_to_lane(const uint4 (&u)[4], uint32_t* stg, float (&out)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t* d = stg + (s * 8 + (lane >> 2)) * kStgPitch + (lane & 3) * 4;
+    d[0] = u[s].x;
+    d[1] = u[s].y;
+    d[2] = u[s].z;
+    d[3] = u[s].w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t w = stg[lane * kStgPitch + j];
+    out[2 * j] = bf16_lo(w);
+    out[2 * j + 1] = bf16_hi(w);
+  }
+  __syncwarp();
+}
+
 // =====================================================================================
 // Forward F1 -- shared shrink, once per token:  Y13[t] = bf16(s * x_t [A1_a; A3_a]^T).
 // M = tokens of adapter a, N = 2r (y1 | y3), K = H.  A: x K-major; B: A1/A3 K-major.
@@ -123,7 +176,7 @@ struct ProbShrink {
     tma_load_3d(sb + r * 128, &mA3, bar, ks * kBK, 0, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{2 * r, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
     for (int c = c0; c < 2 * r; c += cs) {
@@ -195,22 +248,17 @@ struct ProbW13 {
     const int half = (ks - nb) / nkr();
     return MmaStep{128, half * 128, 0, 0};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
-    const int64_t p = (int64_t)ti.m0 + row;
-    const int64_t base = p * I + ti.n0;
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
+    const int64_t base = ((int64_t)ti.m0 + row - (threadIdx.x & 31)) * I + ti.n0;  // warp's first row
     for (int c = c0; c < 128; c += cs) {
-      float g[32], u[32];
+      float g[32], u[32], a[32];
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        float a8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a8[i] = silu_f(g[j + i]) * u[j + i];
-        st_bf16x8(G + base + c + j, g + j);
-        st_bf16x8(U + base + c + j, u + j);
-        st_bf16x8(Act + base + c + j, a8);
-      }
+      for (int i = 0; i < 32; ++i) a[i] = silu_f(g[i]) * u[i];
+      warp_store_rows_bf16(G + base + c, I, 32, g, 1.0f, stg);
+      warp_store_rows_bf16(U + base + c, I, 32, u, 1.0f, stg);
+      warp_store_rows_bf16(Act + base + c, I, 32, a, 1.0f, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
@@ -260,13 +308,14 @@ struct ProbW2 {
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     return MmaStep{ti.sub ? round16(r) : 256, 0, 0, ks == 0};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t p = (int64_t)ti.m0 + row;
     if (!ti.sub) {
+      uint16_t* o0 = O + (p - (threadIdx.x & 31)) * H + ti.n0;  // warp's first row
       for (int c = c0; c < 256; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
-        store_row_bf16(O + p * H + ti.n0 + c, v, 1.0f, 32);
+        warp_store_rows_bf16(o0 + c, H, 32, v, 1.0f, stg);
       }
     } else {
       for (int c = c0; c < r; c += cs) {
@@ -322,13 +371,13 @@ struct ProbB2Expand {
     tma_load_3d(sb, &mB2, bar, ks * kBK, ti.n0, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
-    const int64_t t = (int64_t)ti.m0 + row;
-    const bool ok = t < ti.mend;
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
+    const int64_t t0 = (int64_t)ti.m0 + row - (threadIdx.x & 31);  // warp's first row
+    const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
     for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      if (ok) store_row_bf16(Yl + t * H + ti.n0 + c, v, s, 32);
+      warp_store_rows_bf16(Yl + t0 * H + ti.n0 + c, H, nvalid, v, s, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
@@ -371,7 +420,7 @@ struct ProbDyB2 {
     for (int c = 0; c < nbox; ++c) tma_load_3d(sb + c * 8192, &mB2, bar, c * 64, ks * kBK, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t t = (int64_t)ti.m0 + row;
     const bool ok = t < ti.mend;
     for (int c = c0; c < r; c += cs) {
@@ -432,7 +481,7 @@ struct ProbDB2 {
     for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mZ2w, bar, c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t h = (int64_t)ti.m0 + row;
     for (int c = c0; c < r; c += cs) {
       float v[32];
@@ -502,66 +551,41 @@ struct ProbW2Dgrad {
     }
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t p = (int64_t)ti.m0 + row;
     const int rt = pl.route_of_row[p];
     const bool live = rt >= 0;
     const float w = live ? topk_w[rt] : 0.0f;
-    const int64_t base = p * I + ti.n0;
+    const int64_t base0 = (p - (threadIdx.x & 31)) * I + ti.n0;  // warp's first row
     float dot = 0.0f;
-    // saved G, U and activation of the chunk, loaded one chunk ahead so their
-    // latency overlaps the previous chunk's arithmetic and stores
-    uint4 gu[4], uu[4], au[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      gu[j] = __ldg(reinterpret_cast<const uint4*>(G + base + c0) + j);
-      uu[j] = __ldg(reinterpret_cast<const uint4*>(U + base + c0) + j);
-      au[j] = __ldg(reinterpret_cast<const uint4*>(Act + base + c0) + j);
-    }
     for (int c = c0; c < 256; c += cs) {
-      uint4 gn[4], un[4], an[4];
-      const int cn = c + cs < 256 ? c + cs : c;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        gn[j] = __ldg(reinterpret_cast<const uint4*>(G + base + cn) + j);
-        un[j] = __ldg(reinterpret_cast<const uint4*>(U + base + cn) + j);
-        an[j] = __ldg(reinterpret_cast<const uint4*>(Act + base + cn) + j);
-      }
+      // the chunk's saved G, U and activation: coalesced loads, all in flight,
+      // then redistributed so each lane holds its own row
+      uint4 lg[4], lu[4], la[4];
+      warp_load_rows_issue(G + base0 + c, I, lg);
+      warp_load_rows_issue(U + base0 + c, I, lu);
+      warp_load_rows_issue(Act + base0 + c, I, la);
       float q[32];
       tmem_ld32(taddr + c, q);
+      float g[32], u[32];
+      {
+        float a[32];
+        warp_rows_to_lane(la, stg, a);
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        float g[8], u[8], a[8], og[8], ou[8];
-        const uint32_t gw[4] = {gu[j / 8].x, gu[j / 8].y, gu[j / 8].z, gu[j / 8].w};
-        const uint32_t uw[4] = {uu[j / 8].x, uu[j / 8].y, uu[j / 8].z, uu[j / 8].w};
-        const uint32_t aw[4] = {au[j / 8].x, au[j / 8].y, au[j / 8].z, au[j / 8].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          g[2 * e] = bf16_lo(gw[e]);
-          g[2 * e + 1] = bf16_hi(gw[e]);
-          u[2 * e] = bf16_lo(uw[e]);
-          u[2 * e + 1] = bf16_hi(uw[e]);
-          a[2 * e] = bf16_lo(aw[e]);
-          a[2 * e + 1] = bf16_hi(aw[e]);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float qv = q[j + i];
-          dot += qv * a[i];
-          const float da = w * qv;
-          const float sg = 1.0f / (1.0f + expf(-g[i]));
-          og[i] = live ? da * u[i] * sg * (1.0f + g[i] * (1.0f - sg)) : 0.0f;
-          ou[i] = live ? da * g[i] * sg : 0.0f;
-        }
-        st_bf16x8(dG + base + c + j, og);
-        st_bf16x8(dU + base + c + j, ou);
+        for (int i = 0; i < 32; ++i) dot += q[i] * a[i];
       }
+      warp_rows_to_lane(lg, stg, g);
+      warp_rows_to_lane(lu, stg, u);
+      float og[32], ou[32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        gu[j] = gn[j];
-        uu[j] = un[j];
-        au[j] = an[j];
+      for (int i = 0; i < 32; ++i) {
+        const float da = w * q[i];
+        const float sg = 1.0f / (1.0f + expf(-g[i]));
+        og[i] = live ? da * u[i] * sg * (1.0f + g[i] * (1.0f - sg)) : 0.0f;
+        ou[i] = live ? da * g[i] * sg : 0.0f;
       }
+      warp_store_rows_bf16(dG + base0 + c, I, 32, og, 1.0f, stg);
+      warp_store_rows_bf16(dU + base0 + c, I, 32, ou, 1.0f, stg);
     }
     part[p * ((cs / 32) * ntn()) + (cs / 32) * ti.sub + c0 / 32] = live ? dot : 0.0f;
   }
@@ -608,7 +632,7 @@ struct ProbDA2 {
     for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mAct, bar, ti.n0 + c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const bool ok = row < r;
     for (int c = c0; c < 256; c += cs) {
       float v[32];
@@ -685,13 +709,14 @@ struct ProbW13Dgrad {
     const bool second = ks >= nb;
     return MmaStep{round16(r), second ? 128 : 0, 0, ks == 0 || ks == nb};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t p = (int64_t)ti.m0 + row;
     if (!ti.sub) {
+      uint16_t* o0 = dXp + (p - (threadIdx.x & 31)) * H + ti.n0;  // warp's first row
       for (int c = c0; c < 256; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
-        store_row_bf16(dXp + p * H + ti.n0 + c, v, 1.0f, 32);
+        warp_store_rows_bf16(o0 + c, H, 32, v, 1.0f, stg);
       }
     } else {
       for (int hh = 0; hh < 2; ++hh) {
@@ -751,7 +776,7 @@ struct ProbDB13 {
     for (int c = 0; c < nbox; ++c) tma_load_2d(sb + c * 8192, &mY13p, bar, ti.sub * r + c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t i = (int64_t)ti.m0 + row;
     float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
     for (int c = c0; c < r; c += cs) {
@@ -813,13 +838,13 @@ struct ProbA13Expand {
     for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, m, bar, ti.n0 + c * 64, kb * kBK, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
-    const int64_t t = (int64_t)ti.m0 + row;
-    const bool ok = t < ti.mend;
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
+    const int64_t t0 = (int64_t)ti.m0 + row - (threadIdx.x & 31);  // warp's first row
+    const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
     for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      if (ok) store_row_bf16(dXl + t * H + ti.n0 + c, v, 1.0f, 32);
+      warp_store_rows_bf16(dXl + t0 * H + ti.n0 + c, H, nvalid, v, 1.0f, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
@@ -877,7 +902,7 @@ struct ProbDA13 {
     const int64_t so = ti.sub * split_stride;
     return (m < r ? out1 + so + ((int64_t)ti.g * r + m) * H : out3 + so + ((int64_t)ti.g * r + (m - r)) * H) + ti.n0;
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int m = ti.m0 + row;
     const bool ok = m < 2 * r;
     for (int c = c0; c < 256; c += cs) {
@@ -943,7 +968,7 @@ struct ProbPlain {
     }
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{tn(), 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs) const {
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t m = (int64_t)ti.m0 + row;
     for (int c = c0; c < tn(); c += cs) {
       float v[32];

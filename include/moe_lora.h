@@ -70,7 +70,13 @@ extern "C" {
 
 /* Problem sizes.  H and I must be multiples of 256; r a multiple of 8 in [8,128];
  * 1 <= k <= 32; 1 <= E; A >= 1 adapters; block_m must be 128 (the plan pads
- * every (adapter, expert) group to a multiple of it); act must be 0 (SwiGLU);
+ * every (adapter, expert) group to a multiple of it).
+ * Gated activation h = act(cl(gate)) * cl(up): act 0 = SwiGLU (silu), 1 = GeGLU
+ * (exact erf GELU); cl clamps to [-act_clamp, act_clamp] when act_clamp > 0 (the
+ * gradient passes on the closed interval), no clamp when act_clamp = 0.  The pages
+ * thread SwiGLU/GeGLU and an activation clamp through every kernel (PR #9,
+ * Summary); which pre-activations the clamp applies to is not stated there, and
+ * this library clamps both gate and up.
  * base_fmt 0 (bf16 base weights) or 1 (MXFP4 base weights, see moe_lora_weights).
  * T may be 0 (every call is a no-op). */
 typedef struct moe_lora_dims {
@@ -83,8 +89,9 @@ typedef struct moe_lora_dims {
   int32_t A;        /* adapters sharing the layer (1 = one adapter) */
   int32_t block_m;  /* plan padding unit, 128 */
   float scale;      /* side-LoRA scale s */
-  int32_t act;      /* 0 = SwiGLU */
+  int32_t act;      /* 0 = SwiGLU, 1 = GeGLU */
   int32_t base_fmt; /* 0 = bf16, 1 = MXFP4 */
+  float act_clamp;  /* activation clamp (0 = none) */
 } moe_lora_dims;
 
 /* Frozen base and adapter weights (device).

@@ -38,7 +38,8 @@ class MoeLoraError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("r", ctypes.c_int32), ("A", ctypes.c_int32), ("block_m", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("act", ctypes.c_int32), ("base_fmt", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("act", ctypes.c_int32), ("base_fmt", ctypes.c_int32),
+                ("act_clamp", ctypes.c_float)]
 
 
 class Weights(ctypes.Structure):
@@ -95,9 +96,10 @@ def lib() -> ctypes.CDLL:
 
 
 def make_dims(T: int, H: int, I: int, E: int, k: int, r: int, A: int = 1, scale: float = 1.0,
-              base_fmt: int = 0) -> Dims:
-    """base_fmt: 0 = bf16 base weights, 1 = MXFP4 (packed E2M1 codes + UE8M0 scales S1/S3/S2)."""
-    return Dims(T, H, I, E, k, r, A, 128, float(scale), 0, int(base_fmt))
+              base_fmt: int = 0, act: int = 0, act_clamp: float = 0.0) -> Dims:
+    """base_fmt: 0 = bf16 base weights, 1 = MXFP4 (packed E2M1 codes + UE8M0 scales S1/S3/S2);
+    act: 0 = SwiGLU, 1 = GeGLU; act_clamp: clamp of the gate/up pre-activations (0 = none)."""
+    return Dims(T, H, I, E, k, r, A, 128, float(scale), int(act), int(base_fmt), float(act_clamp))
 
 
 def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]:

@@ -119,6 +119,8 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
+    p.act = d->act;
+    p.clamp = d->act_clamp;
     LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream, K_W2_DGRAD));
   }
   LAUNCH(launch_dw(pl, part, d->I / 128, dw, num_sms, stream));

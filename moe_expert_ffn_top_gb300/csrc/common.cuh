@@ -20,7 +20,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Returns MOE_LORA_OK when the sizes are supported.
 inline int check_dims(const moe_lora_dims* d) {
   if (!d) return MOE_LORA_ERR_NULL;
-  if (d->act != 0 || (d->base_fmt != 0 && d->base_fmt != 1)) return MOE_LORA_ERR_UNSUPPORTED;
+  if ((d->act != 0 && d->act != 1) || (d->base_fmt != 0 && d->base_fmt != 1)) return MOE_LORA_ERR_UNSUPPORTED;
+  if (!(d->act_clamp >= 0.0f) || d->act_clamp > 3.0e38f) return MOE_LORA_ERR_DIMS;
   if (d->T < 0 || d->T > (int64_t)1 << 30) return MOE_LORA_ERR_DIMS;
   if (d->H < 256 || d->H % 256 || d->I < 256 || d->I % 256) return MOE_LORA_ERR_DIMS;
   if (d->r < 8 || d->r > 128 || d->r % 8) return MOE_LORA_ERR_DIMS;

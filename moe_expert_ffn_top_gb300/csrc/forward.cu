@@ -95,6 +95,8 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
+    p.act = d->act;
+    p.clamp = d->act_clamp;
     LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13));
   }
   // F4/F5: W2 + expert-local A2 shrink

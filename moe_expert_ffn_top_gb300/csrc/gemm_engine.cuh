@@ -42,10 +42,12 @@ namespace moelora {
 constexpr int kBK = 64;
 constexpr int kBStageBytes = 256 * 128;  // 32 KB: up to 256 rows x 64 bf16
 constexpr int kAccCols = 256;
-// Per epilogue warp: a 32-row staging buffer (17-word pitch: conflict-free row
-// writes) used to turn row-per-thread accumulator data into coalesced row segments.
+// Per epilogue warp: a 32-row staging buffer used to turn row-per-thread
+// accumulator data into coalesced row segments (pitch 17 words for bf16 rows,
+// 33 for fp32 rows: conflict-free row writes either way).
 constexpr int kStgPitch = 17;
-constexpr int kStgWordsPerWarp = 32 * kStgPitch;
+constexpr int kStgPitchF32 = 33;
+constexpr int kStgWordsPerWarp = 32 * kStgPitchF32;
 constexpr int kGemmSmemBytes = 192 * 1024 + 1024 + 256 + 8 * kStgWordsPerWarp * 4;
 
 // Per-problem pipeline shape.  Narrow problems: 128-row tiles, 4 stages of

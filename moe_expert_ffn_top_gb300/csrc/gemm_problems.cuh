@@ -55,7 +55,93 @@ __device__ __forceinline__ void load_a_wide(const TileInfo& ti, uint8_t* sa, con
   if (ti.mh == 2) tma_load_2d(sa + kAStage128, m, bar, kx, ti.m0 + 128);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// Gated activations: ACT 0 = silu (SwiGLU), 1 = exact erf GELU (GeGLU); the
+// clamp c > 0 limits gate and up pre-activations to [-c, c] (0 = no clamp).
+template <int ACT>
+__device__ __forceinline__ float act_fwd(float z) {
+  if (ACT == 1) return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+  return z / (1.0f + expf(-z));
+}
+// f(z) and f'(z) together (one exponential and one division for silu).
+template <int ACT>
+__device__ __forceinline__ void act_pair(float z, float& f, float& df) {
+  if (ACT == 1) {
+    const float cdf = 0.5f * (1.0f + erff(z * 0.70710678118654752f));
+    f = z * cdf;
+    df = cdf + z * 0.39894228040143268f * expf(-0.5f * z * z);
+  } else {
+    const float sg = 1.0f / (1.0f + expf(-z));
+    f = z * sg;
+    df = sg * (1.0f + z * (1.0f - sg));
+  }
+}
+__device__ __forceinline__ float clamp_act(float v, float c) { return fminf(fmaxf(v, -c), c); }
+// derivative of the clamp: 1 on [-c, c], ends included
+__device__ __forceinline__ float clamp_pass(float v, float c) { return (v >= -c && v <= c) ? 1.0f : 0.0f; }
+
+// Forward of one 32-column chunk: a = act(cl(g)) * cl(u), then g/u replaced by
+// the values to save (clamp_encode, defined below).
+__device__ __forceinline__ float clamp_encode(float v, float c);
+template <int ACT, bool CL>
+__device__ __forceinline__ void act_fwd_chunk(float (&g)[32], float (&u)[32], float (&a)[32], float c) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = CL ? act_fwd<ACT>(clamp_act(g[i], c)) * clamp_act(u[i], c) : act_fwd<ACT>(g[i]) * u[i];
+    if (CL) {
+      g[i] = clamp_encode(g[i], c);
+      u[i] = clamp_encode(u[i], c);
+    }
+  }
+}
+__device__ __forceinline__ void act_fwd_chunk(int act, float c, float (&g)[32], float (&u)[32], float (&a)[32]) {
+  if (act == 1) {
+    if (c > 0.0f) act_fwd_chunk<1, true>(g, u, a, c); else act_fwd_chunk<1, false>(g, u, a, c);
+  } else {
+    if (c > 0.0f) act_fwd_chunk<0, true>(g, u, a, c); else act_fwd_chunk<0, false>(g, u, a, c);
+  }
+}
+
+// Backward of one chunk from the upstream dAct = w * q:
+//   dG = dAct * cl(U) * act'(cl(G)) * [G in clamp],  dU = dAct * act(cl(G)) * [U in clamp]
+// (dead rows give zeros).  G/U are the saved values, whose clamp test matches the
+// forward's fp32 decision.
+template <int ACT, bool CL>
+__device__ __forceinline__ void act_bwd_chunk(const float (&q)[32], const float (&g)[32], const float (&u)[32],
+                                              float w, bool live, float c, float (&og)[32], float (&ou)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float da = w * q[i];
+    float f, df;
+    act_pair<ACT>(CL ? clamp_act(g[i], c) : g[i], f, df);
+    const float uc = CL ? clamp_act(u[i], c) : u[i];
+    og[i] = live ? da * uc * df * (CL ? clamp_pass(g[i], c) : 1.0f) : 0.0f;
+    ou[i] = live ? da * f * (CL ? clamp_pass(u[i], c) : 1.0f) : 0.0f;
+  }
+}
+__device__ __forceinline__ void act_bwd_chunk(int act, float c, const float (&q)[32], const float (&g)[32],
+                                              const float (&u)[32], float w, bool live, float (&og)[32],
+                                              float (&ou)[32]) {
+  if (act == 1) {
+    if (c > 0.0f) act_bwd_chunk<1, true>(q, g, u, w, live, c, og, ou);
+    else act_bwd_chunk<1, false>(q, g, u, w, live, c, og, ou);
+  } else {
+    if (c > 0.0f) act_bwd_chunk<0, true>(q, g, u, w, live, c, og, ou);
+    else act_bwd_chunk<0, false>(q, g, u, w, live, c, og, ou);
+  }
+}
+// Value saved (as bf16) for a gate/up pre-activation v so that the backward sees
+// the forward's fp32 clamp decision: a clamped element (|v| > c) is saved as the
+// smallest bf16 magnitude above c, an element inside [-c, c] as its bf16 value,
+// rounded toward zero when rounding to nearest would cross c.  The result is a
+// bf16 value; |saved| <= c exactly when the forward did not clamp.
+__device__ __forceinline__ float clamp_encode(float v, float c) {
+  if (fabsf(v) > c) {
+    const uint32_t above = (__float_as_uint(c) & 0xFFFF0000u) + 0x10000u;  // next bf16 above trunc(c)
+    return copysignf(__uint_as_float(above), v);
+  }
+  const float r = __bfloat162float(__float2bfloat16_rn(v));
+  return fabsf(r) > c ? __uint_as_float(__float_as_uint(v) & 0xFFFF0000u) : r;
+}
 
 // Stores n (multiple of 8, <= 32) bf16 values v[i] * mul.
 __device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float (&v)[32], float mul, int n) {
@@ -103,6 +189,24 @@ __device__ __forceinline__ void warp_store_rows_bf16(uint16_t* dst0, int64_t ld,
     const uint32_t* src = stg + r * kStgPitch + w;
     const uint4 u = make_uint4(src[0], src[1], src[2], src[3]);
     if (r < nvalid) *reinterpret_cast<uint4*>(dst0 + (int64_t)r * ld + 2 * w) = u;
+  }
+  __syncwarp();
+}
+
+// fp32 version: n (<= 32, multiple of 4) columns of v * mul, 8 lanes per row
+// (4 rows of 128 contiguous bytes per instruction).
+__device__ __forceinline__ void warp_store_rows_f32(float* dst0, int64_t ld, int nvalid, const float (&v)[32],
+                                                    float mul, int n, uint32_t* stg) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) stg[lane * kStgPitchF32 + j] = __float_as_uint(v[j] * mul);
+  __syncwarp();
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int r = s * 4 + (lane >> 3), w = (lane & 7) * 4;
+    const uint32_t* src = stg + r * kStgPitchF32 + w;
+    const uint4 u = make_uint4(src[0], src[1], src[2], src[3]);
+    if (r < nvalid && w < n) *reinterpret_cast<uint4*>(dst0 + (int64_t)r * ld + w) = u;
   }
   __syncwarp();
 }
@@ -192,7 +296,8 @@ struct ProbShrink {
 // =====================================================================================
 // Forward F3 -- W13 expert GEMM with the expert-local B1/B3 expand and SwiGLU:
 //   G = Xp W1_e^T + Y1p B1_ae^T,  U = Xp W3_e^T + Y3p B3_ae^T   (s folded into Y13)
-//   Act = bf16(silu(G) * U); G and U are kept (bf16) for the backward.
+//   Act = bf16(act(cl(G)) * cl(U)); G and U are kept (bf16) for the backward, with
+//   the forward's clamp decision encoded (clamp_encode).
 // Tile: 128 rows x 128 columns of I; the accumulator holds the gate columns in
 // TMEM [0,128) and the up columns in [128,256).  K steps: H/64 base steps (one
 // N=256 MMA over W1|W3 rows), then ceil(r/64) steps per side for the expand
@@ -208,6 +313,8 @@ struct ProbW13 {
   int* err;
   uint16_t *G, *U, *Act;
   int H, I, r;
+  int act;      // 0 = SwiGLU, 1 = GeGLU
+  float clamp;  // activation clamp (0 = none)
   __device__ int ntn() const { return I / 128; }
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
@@ -254,8 +361,7 @@ struct ProbW13 {
       float g[32], u[32], a[32];
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) a[i] = silu_f(g[i]) * u[i];
+      act_fwd_chunk(act, clamp, g, u, a);
       warp_store_rows_bf16(G + base + c, I, 32, g, 1.0f, stg);
       warp_store_rows_bf16(U + base + c, I, 32, u, 1.0f, stg);
       warp_store_rows_bf16(Act + base + c, I, 32, a, 1.0f, stg);
@@ -482,11 +588,11 @@ struct ProbDB2 {
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    const int64_t h = (int64_t)ti.m0 + row;
+    float* o0 = row_ptr(ti, (int64_t)ti.m0 + row - (threadIdx.x & 31));  // warp's first row
     for (int c = c0; c < r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      store_row_f32(row_ptr(ti, h) + c, v, s, r - c < 32 ? r - c : 32);
+      warp_store_rows_f32(o0 + c, r, 32, v, s, r - c < 32 ? r - c : 32, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
@@ -499,7 +605,7 @@ struct ProbDB2 {
 // =====================================================================================
 // Backward B3/B4 -- W2^T dgrad with the A2 path, SwiGLU backward and router dots:
 //   Q  = Dp W2_e + D2p A2_ae              [P,I]   (D2p = s * dyB2 of the row's token)
-//   dAct = w * Q;  dG = dAct * U * sig(G) * (1 + G (1 - sig(G)));  dU = dAct * silu(G)
+//   dAct = w * Q;  dG = dAct * cl(U) * act'(cl(G)) * [G in clamp];  dU = dAct * act(cl(G)) * [U in clamp]
 //   part[p, 2*n-tile + half] = <Q, Act> over the columns one epilogue warp handles
 //   (router-gradient partial sums, reduced in a fixed order by the dw kernel)
 // Padding rows produce exact zeros.  A: Dp/D2p K-major; B: W2/A2 MN-major.
@@ -517,6 +623,8 @@ struct ProbW2Dgrad {
   uint16_t *dG, *dU;
   float* part;
   int H, I, r;
+  int act;      // 0 = SwiGLU, 1 = GeGLU
+  float clamp;  // activation clamp (0 = none)
   __device__ int ntn() const { return I / 256; }
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
@@ -577,13 +685,7 @@ struct ProbW2Dgrad {
       warp_rows_to_lane(lg, stg, g);
       warp_rows_to_lane(lu, stg, u);
       float og[32], ou[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float da = w * q[i];
-        const float sg = 1.0f / (1.0f + expf(-g[i]));
-        og[i] = live ? da * u[i] * sg * (1.0f + g[i] * (1.0f - sg)) : 0.0f;
-        ou[i] = live ? da * g[i] * sg : 0.0f;
-      }
+      act_bwd_chunk(act, clamp, q, g, u, w, live, og, ou);
       warp_store_rows_bf16(dG + base0 + c, I, 32, og, 1.0f, stg);
       warp_store_rows_bf16(dU + base0 + c, I, 32, ou, 1.0f, stg);
     }
@@ -633,11 +735,12 @@ struct ProbDA2 {
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    const bool ok = row < r;
+    const int rb = row - (threadIdx.x & 31);  // warp's first row
+    float* o0 = dA2 + ((int64_t)ti.g * r + rb) * I + ti.n0;
     for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      if (ok) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, v, 1.0f, 32);
+      warp_store_rows_f32(o0 + c, I, r - rb, v, 1.0f, 32, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
@@ -719,11 +822,12 @@ struct ProbW13Dgrad {
         warp_store_rows_bf16(o0 + c, H, 32, v, 1.0f, stg);
       }
     } else {
+      float* o0 = dY13 + (p - (threadIdx.x & 31)) * (2 * r);  // warp's first row
       for (int hh = 0; hh < 2; ++hh) {
         for (int c = c0; c < r; c += cs) {
           float v[32];
           tmem_ld32(taddr + hh * 128 + c, v);
-          store_row_f32(dY13 + p * (2 * r) + hh * r + c, v, s, r - c < 32 ? r - c : 32);
+          warp_store_rows_f32(o0 + hh * r + c, 2 * r, 32, v, s, r - c < 32 ? r - c : 32, stg);
         }
       }
     }
@@ -777,12 +881,12 @@ struct ProbDB13 {
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    const int64_t i = (int64_t)ti.m0 + row;
-    float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
+    const int64_t i0 = (int64_t)ti.m0 + row - (threadIdx.x & 31);  // warp's first row
+    float* o0 = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i0) * r;
     for (int c = c0; c < r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      store_row_f32(out + c, v, 1.0f, r - c < 32 ? r - c : 32);
+      warp_store_rows_f32(o0 + c, r, 32, v, 1.0f, r - c < 32 ? r - c : 32, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {

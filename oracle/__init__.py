@@ -55,7 +55,8 @@ class _ODims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("r", ctypes.c_int32),
                 ("A", ctypes.c_int32), ("block_m", ctypes.c_int32), ("scale", ctypes.c_double),
-                ("round_bf16", ctypes.c_int32), ("nthreads", ctypes.c_int32)]
+                ("round_bf16", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("pad_", ctypes.c_int32), ("clamp", ctypes.c_double)]
 
 
 _TENSOR_FIELDS = ("w", "x", "dy", "W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")
@@ -114,7 +115,7 @@ def _otensor(t: Optional[torch.Tensor], prec: str, keep: _Keep, scales=None) -> 
 def _pack(inp: dict, shp, prec: str, scale: float, round_bf16: bool, nthreads: int):
     keep = _Keep()
     d = _ODims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, 128, float(scale),
-               1 if round_bf16 else 0, nthreads)
+               1 if round_bf16 else 0, nthreads, 1 if shp.act == "geglu" else 0, 0, float(shp.clamp))
     ids = keep(inp["topk_ids"].to(torch.int32).contiguous().cpu())
     offs = keep(inp["adapter_offsets"].to(torch.int64).contiguous().cpu())
     fields = {}

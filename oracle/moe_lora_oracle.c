@@ -13,7 +13,12 @@
  *
  *   y1 = rb(A1_a x_t)            y3 = rb(A3_a x_t)                       [r]
  *   g  = W1_e x_t + s B1_{a,e} y1      u = W3_e x_t + s B3_{a,e} y3      [I]
- *   h  = rb(silu(g) * u)               silu(z) = z / (1 + exp(-z))       [I]
+ *   h  = rb(act(cl(g)) * cl(u))                                          [I]
+ *        act = silu(z) = z / (1 + exp(-z))  (SwiGLU, the default), or
+ *        act = gelu(z) = z/2 (1 + erf(z / sqrt 2))  (GeGLU);
+ *        cl(v) = min(max(v, -c), c) with the activation clamp c (none when c = 0);
+ *        the pages thread "SwiGLU/GeGLU" and an activation clamp through every
+ *        kernel (PR #9, Summary; the production runs used clamp 10).
  *   z2 = rb(A2_{a,e} h)                                                  [r]
  *   o  = W2_e h + s B2_a z2                                              [H]
  *   y_t = rb( sum_j w_tj o_j )   (slot order; masked slots contribute nothing)
@@ -75,6 +80,9 @@ typedef struct {
   double scale;           /* side-LoRA scale s */
   int32_t round_bf16;     /* 1: bf16 rounding points on; 0: off */
   int32_t nthreads;       /* OpenMP threads (0 = runtime default) */
+  int32_t act;            /* 0: SwiGLU, 1: GeGLU */
+  int32_t pad_;
+  double clamp;           /* activation clamp c (0 = none) */
 } odims;
 
 typedef struct {
@@ -137,6 +145,36 @@ static real rb(const odims* d, real v) { return d->round_bf16 ? round_bf16(v) : 
 
 static real silu(real z) { return z / ((real)1 + REXP(-z)); }
 static real sigmoid(real z) { return (real)1 / ((real)1 + REXP(-z)); }
+
+#ifdef ORACLE_DOUBLE
+#define RERF erf
+#else
+#define RERF erff
+#endif
+static const double kInvSqrt2 = 0.70710678118654752440;
+static const double kInvSqrt2Pi = 0.39894228040143267794;
+static real gelu(real z) { return (real)0.5 * z * ((real)1 + RERF(z * (real)kInvSqrt2)); }
+/* d gelu / dz = Phi(z) + z phi(z) */
+static real gelu_grad(real z) {
+  return (real)0.5 * ((real)1 + RERF(z * (real)kInvSqrt2)) + z * (real)kInvSqrt2Pi * REXP((real)-0.5 * z * z);
+}
+static real act_f(const odims* d, real z) { return d->act == 1 ? gelu(z) : silu(z); }
+static real act_grad(const odims* d, real z) {
+  if (d->act == 1) return gelu_grad(z);
+  const real sg = sigmoid(z);
+  return sg * ((real)1 + z * ((real)1 - sg));
+}
+static real clampv(const odims* d, real v) {
+  if (d->clamp <= 0) return v;
+  const real c = (real)d->clamp;
+  return v < -c ? -c : (v > c ? c : v);
+}
+/* derivative of the clamp: 1 on [-c, c] (the ends included), else 0 */
+static real clamp_pass(const odims* d, real v) {
+  if (d->clamp <= 0) return (real)1;
+  const real c = (real)d->clamp;
+  return (v >= -c && v <= c) ? (real)1 : (real)0;
+}
 
 static int adapter_of(const oinputs* in, int A, int64_t t) {
   for (int a = 0; a < A; ++a)
@@ -233,7 +271,7 @@ static void route_forward(const odims* d, const oinputs* in, int a, int e, fwd_s
     for (int64_t q = 0; q < r; ++q) ul += ld(&in->B3, bbase + q) * s->y3[q];
     s->g[i] = gb + sc * gl;
     s->u[i] = ub + sc * ul;
-    s->h[i] = rb(d, silu(s->g[i]) * s->u[i]);
+    s->h[i] = rb(d, act_f(d, clampv(d, s->g[i])) * clampv(d, s->u[i]));
   }
   for (int64_t q = 0; q < r; ++q) {
     real acc = 0;
@@ -361,11 +399,11 @@ int oracle_backward(const odims* d, const oinputs* in, const int64_t* tokens, in
           S_y1[ri * r + q] = s.y1[q];
           S_y3[ri * r + q] = s.y3[q];
         }
-        /* SwiGLU backward */
+        /* gated-activation backward (through the clamp) */
         for (int64_t i = 0; i < I; ++i) {
-          real gi = s.g[i], sg = sigmoid(gi);
-          S_dg[ri * I + i] = dact[i] * s.u[i] * sg * ((real)1 + gi * ((real)1 - sg));
-          S_du[ri * I + i] = dact[i] * gi * sg;
+          const real gc = clampv(d, s.g[i]), uc = clampv(d, s.u[i]);
+          S_dg[ri * I + i] = dact[i] * uc * act_grad(d, gc) * clamp_pass(d, s.g[i]);
+          S_du[ri * I + i] = dact[i] * act_f(d, gc) * clamp_pass(d, s.u[i]);
           S_h[ri * I + i] = s.h[i];
         }
         const real* dg = S_dg + ri * I;

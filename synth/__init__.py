@@ -44,6 +44,8 @@ class Shape:
     empty_experts: tuple = ()  # experts that receive no token
     router: str = "linear"  # "linear": logits = x W_r^T ; "normal": logits ~ N(0,1)
     base_fmt: str = "bf16"  # "bf16" or "mxfp4"
+    act: str = "swiglu"     # "swiglu" or "geglu"
+    clamp: float = 0.0      # activation clamp c on the gate/up pre-activations (0 = none)
 
 
 def shape(name: str, T: Optional[int] = None) -> Shape:

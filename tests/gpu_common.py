@@ -41,7 +41,8 @@ def assert_close(name: str, got: torch.Tensor, ref: torch.Tensor) -> None:
 
 def dims_of(shp: Shape, scale: Optional[float] = None) -> m.Dims:
     return m.make_dims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, shp.scale if scale is None else scale,
-                       base_fmt=1 if shp.base_fmt == "mxfp4" else 0)
+                       base_fmt=1 if shp.base_fmt == "mxfp4" else 0, act=1 if shp.act == "geglu" else 0,
+                       act_clamp=shp.clamp)
 
 
 def run_gpu(inp: Dict[str, torch.Tensor], shp: Shape, scale: Optional[float] = None, poison: bool = False,
@@ -108,5 +109,5 @@ def sub_problem(inp: Dict[str, torch.Tensor], shp: Shape, tokens: Iterable[int])
     for n in ("A1", "A3", "B2"):
         sub[n] = inp[n].cpu()
     sshp = Shape(T=len(tok), H=shp.H, I=shp.I, E=len(used), k=shp.k, r=shp.r, A=1, scale=shp.scale,
-                 base_fmt=shp.base_fmt)
+                 base_fmt=shp.base_fmt, act=shp.act, clamp=shp.clamp)
     return sub, sshp, used, tok

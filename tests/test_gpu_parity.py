@@ -349,3 +349,28 @@ def test_mxfp4_production_width_sampled():
     out = run_gpu(inp, shp)
     assert out["err"] == 0
     _sampled_check(inp, shp, out, sample)
+
+
+# ----------------------------------------------------------------------------- activation variants
+@pytest.mark.parametrize("act,clamp", [("geglu", 0.0), ("swiglu", 0.25), ("geglu", 0.25)])
+def test_activation_variants(act, clamp):
+    """GeGLU (exact erf GELU) and the activation clamp on gate/up (the pages'
+    SwiGLU/GeGLU and clamp variants); clamp 0.25 binds on these inputs."""
+    shp = Shape(T=200, H=512, I=256, E=16, k=2, r=16, mask_frac=0.1, act=act, clamp=clamp)
+    inp = make_inputs(shp, seed=41)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    _full_check(inp, shp, out)
+
+
+def test_activation_clamp_production_width_sampled():
+    """GeGLU with the production runs' clamp value 10 (PR #9, Direct old/new
+    numerical comparison), production widths, 1,029 tokens, sampled sparse dy."""
+    shp = Shape(T=1029, H=4096, I=2048, E=256, k=6, r=128, mask_frac=0.2, empty_experts=(0, 127, 255),
+                act="geglu", clamp=10.0)
+    inp = make_inputs(shp, seed=42, device="cuda")
+    sample = [0, 3, 500, 1028]
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    _sampled_check(inp, shp, out, sample)

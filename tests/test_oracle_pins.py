@@ -38,8 +38,8 @@ def _f64(inp):
     return out
 
 
-def _tiny(T=5, H=16, I=8, E=3, k=2, r=2, A=1, scale=0.7, seed=0, mask=0.0):
-    shp = Shape(T=T, H=H, I=I, E=E, k=k, r=r, A=A, scale=scale, mask_frac=mask)
+def _tiny(T=5, H=16, I=8, E=3, k=2, r=2, A=1, scale=0.7, seed=0, mask=0.0, act="swiglu", clamp=0.0):
+    shp = Shape(T=T, H=H, I=I, E=E, k=k, r=r, A=A, scale=scale, mask_frac=mask, act=act, clamp=clamp)
     inp = _f64(make_inputs(shp, seed=seed))
     # make the side path large enough to matter in the comparisons
     g = torch.Generator().manual_seed(100 + seed)
@@ -72,7 +72,11 @@ def _merged_reference(inp, shp, scale):
             W3m = W3[e] + scale * leaves["B3"][a, e] @ leaves["A3"][a]
             W2m = W2[e] + scale * leaves["B2"][a] @ leaves["A2"][a, e]
             xt = leaves["x"][t]
-            h = torch.nn.functional.silu(W1m @ xt) * (W3m @ xt)
+            g, u = W1m @ xt, W3m @ xt
+            if shp.clamp > 0:
+                g, u = g.clamp(-shp.clamp, shp.clamp), u.clamp(-shp.clamp, shp.clamp)
+            act = torch.nn.functional.gelu(g) if shp.act == "geglu" else torch.nn.functional.silu(g)
+            h = act * u
             acc = acc + leaves["topk_w"][t, j] * (W2m @ h)
         outs.append(acc)
     y = torch.stack(outs)
@@ -87,10 +91,13 @@ def _rel(a, b):
     return (a - b).norm().item() / (den if den > 0 else 1.0)
 
 
+@pytest.mark.parametrize("act,clamp", [("swiglu", 0.0), ("geglu", 0.0), ("swiglu", 0.3), ("geglu", 0.3)])
 @pytest.mark.parametrize("scale", [0.7, 0.0])
 @pytest.mark.parametrize("A,mask", [(1, 0.0), (1, 0.3), (2, 0.2)])
-def test_dense_merged_weight_autograd(scale, A, mask):
-    shp, inp = _tiny(T=6, A=A, mask=mask, scale=scale, seed=1)
+def test_dense_merged_weight_autograd(scale, A, mask, act, clamp):
+    """torch.nn.functional.silu / gelu (exact erf form) and torch.clamp give the
+    activation variants; the clamp value 0.3 is small enough to bind on these inputs."""
+    shp, inp = _tiny(T=6, A=A, mask=mask, scale=scale, seed=1, act=act, clamp=clamp)
     y_ref, g_ref = _merged_reference(inp, shp, scale)
     y = oracle.forward(inp, shp, prec="f64", scale=scale, round_bf16=False)
     assert _rel(y, y_ref) < 1e-12
@@ -106,10 +113,11 @@ def test_dense_merged_weight_autograd(scale, A, mask):
             assert _rel(g[n], ref) < 1e-11, n
 
 
-def test_finite_differences():
+@pytest.mark.parametrize("act,clamp", [("swiglu", 0.0), ("geglu", 0.3)])
+def test_finite_differences(act, clamp):
     """Central differences of the FP64 oracle forward against its backward, for
     every differentiable input (x, routing weights, six adapters)."""
-    shp, inp = _tiny(T=4, seed=2)
+    shp, inp = _tiny(T=4, seed=2, act=act, clamp=clamp)
     g = oracle.backward(inp, shp, prec="f64", round_bf16=False)
     gen = torch.Generator().manual_seed(7)
     names = {"x": "dx", "topk_w": "dw", "A1": "dA1", "A3": "dA3", "B1": "dB1",

@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from synth import Shape, make_inputs, shape  # noqa: E402
+from synth import Shape, make_inputs, make_router_inputs, shape  # noqa: E402
 
 METRIC = "fwd+bwd ms & TFLOP/s (% BF16 peak), 64K tok H4096 I2048 E256 top6 r128"
 ADAPTER_GRADS = ("dA1", "dA3", "dB1", "dB3", "dA2", "dB2")
@@ -310,6 +310,49 @@ def run_ours(args, rank, world, local_rank):
                 "grouped_gemms_tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
                 "grouped_gemms_frac_of_burst_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 / pk["bf16"], 4)}
 
+    # ---- the routing step ahead of the path (router forward / backward), timed on
+    # its own: the headline step takes ids and weights as inputs, as the pages do.
+    router = None
+    if shp.A == 1 and 16 <= E <= 256 and E % 16 == 0:
+        rin = make_router_inputs(T, H, E, k, seed=100 + rank, device="cuda")
+        rsc = m.router_scratch(d)
+        rids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+        rw = torch.empty(T, k, dtype=torch.float32, device="cuda")
+        rdWr = torch.empty(E, H, dtype=torch.float32, device="cuda")
+        rdx = torch.zeros(T, H, dtype=torch.bfloat16, device="cuda")
+        rf = lambda: m.moe_lora_router_forward(d, rin["x"], rin["Wr"], rids, rw, None, rsc)
+        rb = lambda: m.moe_lora_router_backward(d, rin["x"], rin["Wr"], rids, rw, rin["dw"], None, rdWr, rdx, rsc)
+        for _ in range(args.warmup):
+            rf()
+            rb()
+        torch.cuda.synchronize()
+        rt = []
+        for fn in (rf, rb):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            rt.append(a0.elapsed_time(a1) / args.steps)
+        m.moe_lora_profile_enable(True)
+        for _ in range(args.steps):
+            rf()
+            rb()
+        torch.cuda.synchronize()
+        rprof = m.moe_lora_profile_read()
+        m.moe_lora_profile_enable(False)
+        assert m.moe_lora_router_get_error(rsc) == 0, "router device error word set"
+        rfl = 2.0 * T * E * H
+        router = {"ms_forward": round(rt[0], 4), "ms_backward": round(rt[1], 4),
+                  "tflops_forward": round(rfl / (rt[0] * 1e-3) / 1e12, 1),
+                  "tflops_backward": round(2 * rfl / (rt[1] * 1e-3) / 1e12, 1),
+                  "kernels": {n: round(tot / cnt, 4) for n, (tot, cnt) in rprof.items()},
+                  "note": "softmax top-k router GEMM (fused epilogue) and its backward "
+                          "(dlogits, dx += dlogits W_r, dW_r); not part of the headline step"}
+        del rin, rsc, rids, rw, rdWr, rdx
+        torch.cuda.empty_cache()
+
     # ---- end to end through the public API: pinned host inputs in, results out.
     # Every step copies its own inputs host->device and reads all of its results
     # back device->host inside the timed region; copies run on their own streams
@@ -393,7 +436,7 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas only (one independent batch per GPU, no collectives)",
                        "l2": "inputs larger than L2 (12.9 GB frozen weights), no flush"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "kernels": kernels,
+            "clocks": clk, "kernels": kernels, "router": router,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

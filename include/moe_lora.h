@@ -67,6 +67,7 @@ extern "C" {
 #define MOE_LORA_WS_SAVED 1       /* forward activations kept for the backward */
 #define MOE_LORA_WS_FWD_SCRATCH 2 /* forward temporaries */
 #define MOE_LORA_WS_BWD_SCRATCH 3 /* backward temporaries */
+#define MOE_LORA_WS_ROUTER_SCRATCH 4 /* router error word and backward temporaries */
 
 /* Problem sizes.  H and I must be multiples of 256; r a multiple of 8 in [8,128];
  * 1 <= k <= 32; 1 <= E; A >= 1 adapters; block_m must be 128 (the plan pads
@@ -214,6 +215,45 @@ MOE_LORA_API int moe_lora_profile_read(const char** names, double* total_ms, int
 /* Kernel launches issued by this library since the last reset (always counted);
  * reset != 0 returns the count and sets it to zero. */
 MOE_LORA_API int64_t moe_lora_launch_count(int reset);
+
+/* ---- router: the routing step ahead of the expert path ----
+ * PR #9 takes the routes as inputs and returns their weight gradient (its
+ * "grad-route", Correctness coverage).  These two calls add the step that makes
+ * the routes and carry that gradient back to the router, read as the usual
+ * softmax top-k gate:
+ *     l_t = W_r x_t  (fp32 accumulation),   p_t = softmax(l_t) over all E,
+ *     the k experts of largest p_t, largest first, equal values to the lower id
+ *     (selected on l_t in fp32: softmax keeps the order),
+ *     w_tj = p_t[e_j] / sum_j' p_t[e_j']   (renormalised to sum 1).
+ * Backward, for the selection made in the forward: since w_t is the softmax of
+ * the selected logits alone, dl_te = w_tj (dw_tj - sum_j' w_tj' dw_tj') at
+ * e = e_j and 0 elsewhere; dW_r = sum_t dl_t^T x_t; grad-x gains dl_t W_r.
+ * Requirements beyond moe_lora_dims' rules: A == 1, 16 <= E <= 256 with
+ * E % 16 == 0, k <= E (else MOE_LORA_ERR_UNSUPPORTED / MOE_LORA_ERR_DIMS).
+ * `scratch` is a device buffer of moe_lora_workspace_bytes(.., MOE_LORA_WS_ROUTER_SCRATCH);
+ * its first word is the device error word both calls clear and
+ * moe_lora_router_get_error() reads. */
+
+/* x [T,H] bf16, W_r [E,H] bf16.  Writes topk_ids [T,k] int32 (largest first) and
+ * topk_w [T,k] fp32; logits [T,E] fp32 as well when non-NULL.  One launch. */
+MOE_LORA_API int moe_lora_router_forward(const moe_lora_dims* dims, const uint16_t* x, const uint16_t* Wr,
+                                         int32_t* topk_ids, float* topk_w, float* logits, void* scratch,
+                                         size_t scratch_bytes, void* stream);
+
+/* topk_ids / topk_w as written by moe_lora_router_forward (slots with an id
+ * outside [0, E) are skipped), dw [T,k] fp32 (e.g. moe_lora_backward's dw).
+ * Writes dWr [E,H] fp32 and, when non-NULL, dlogits [T,E] fp32.  dx [T,H] bf16
+ * is READ AND UPDATED in place, dx <- bf16(dx + dl W_r), so that the expert
+ * path's grad-x and the router's share one buffer (the one exception to
+ * "outputs are overwritten"; pass a zeroed dx for the router's part alone). */
+MOE_LORA_API int moe_lora_router_backward(const moe_lora_dims* dims, const uint16_t* x, const uint16_t* Wr,
+                                          const int32_t* topk_ids, const float* topk_w, const float* dw,
+                                          float* dlogits, float* dWr, uint16_t* dx, void* scratch,
+                                          size_t scratch_bytes, void* stream);
+
+/* Reads (and keeps) the device error word of a router scratch buffer
+ * (MOE_LORA_DEV_* bits); synchronises `stream`. */
+MOE_LORA_API int moe_lora_router_get_error(const void* scratch, void* stream);
 
 /* Static description of a return code. */
 MOE_LORA_API const char* moe_lora_strerror(int code);

@@ -26,6 +26,7 @@ from . import _build
 LIB_PATH = _build.LIB
 
 MOE_LORA_WS_PLAN, MOE_LORA_WS_SAVED, MOE_LORA_WS_FWD_SCRATCH, MOE_LORA_WS_BWD_SCRATCH = 0, 1, 2, 3
+MOE_LORA_WS_ROUTER_SCRATCH = 4
 MOE_LORA_DEV_BAD_ID, MOE_LORA_DEV_TIMEOUT = 1, 2
 
 
@@ -91,6 +92,12 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_launch_count.argtypes = [ctypes.c_int]
         L.moe_lora_gemm_selftest_error.restype = ctypes.c_int
         L.moe_lora_gemm_selftest_error.argtypes = [P]
+        L.moe_lora_router_forward.restype = ctypes.c_int
+        L.moe_lora_router_forward.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_lora_router_backward.restype = ctypes.c_int
+        L.moe_lora_router_backward.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_lora_router_get_error.restype = ctypes.c_int
+        L.moe_lora_router_get_error.argtypes = [P, P]
         _lib = L
     return _lib
 
@@ -215,6 +222,45 @@ def moe_lora_get_error(dims: Dims, plan_ws: torch.Tensor, stream=None) -> int:
     if rc < 0:
         raise MoeLoraError(rc, "moe_lora_get_error")
     return rc
+
+
+def moe_lora_router_forward(dims: Dims, x: torch.Tensor, Wr: torch.Tensor, topk_ids: torch.Tensor,
+                            topk_w: torch.Tensor, logits: Optional[torch.Tensor], scratch: torch.Tensor,
+                            stream=None) -> None:
+    """Softmax top-k router: topk_ids [T,k] int32, topk_w [T,k] fp32 (and logits [T,E] fp32 if given)."""
+    rc = lib().moe_lora_router_forward(ctypes.byref(dims), _ptr(x, torch.bfloat16, "x"),
+                                       _ptr(Wr, torch.bfloat16, "Wr"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                       _ptr(topk_w, torch.float32, "topk_w"), _ptr(logits, torch.float32, "logits"),
+                                       _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream))
+    _check(rc, "moe_lora_router_forward")
+
+
+def moe_lora_router_backward(dims: Dims, x: torch.Tensor, Wr: torch.Tensor, topk_ids: torch.Tensor,
+                             topk_w: torch.Tensor, dw: torch.Tensor, dlogits: Optional[torch.Tensor],
+                             dWr: torch.Tensor, dx: torch.Tensor, scratch: torch.Tensor, stream=None) -> None:
+    """Router backward: dWr [E,H] fp32 (and dlogits [T,E] fp32 if given); dx [T,H] bf16 is
+    updated in place, dx <- bf16(dx + dlogits W_r)."""
+    rc = lib().moe_lora_router_backward(ctypes.byref(dims), _ptr(x, torch.bfloat16, "x"),
+                                        _ptr(Wr, torch.bfloat16, "Wr"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                        _ptr(topk_w, torch.float32, "topk_w"), _ptr(dw, torch.float32, "dw"),
+                                        _ptr(dlogits, torch.float32, "dlogits"), _ptr(dWr, torch.float32, "dWr"),
+                                        _ptr(dx, torch.bfloat16, "dx"), _ptr(scratch),
+                                        scratch.numel() * scratch.element_size(), _stream(stream))
+    _check(rc, "moe_lora_router_backward")
+
+
+def moe_lora_router_get_error(scratch: torch.Tensor, stream=None) -> int:
+    rc = lib().moe_lora_router_get_error(_ptr(scratch), _stream(stream))
+    if rc < 0:
+        raise MoeLoraError(rc, "moe_lora_router_get_error")
+    return rc
+
+
+def router_scratch(dims: Dims, device="cuda") -> torch.Tensor:
+    n = moe_lora_workspace_bytes(dims, MOE_LORA_WS_ROUTER_SCRATCH)
+    if n == 0:
+        raise MoeLoraError(-5, "moe_lora_workspace_bytes(ROUTER_SCRATCH)")
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def moe_lora_gemm_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor, b_mn: bool, C: torch.Tensor,

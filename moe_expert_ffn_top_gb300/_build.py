@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoelora.so")
-SOURCES = ["api.cu", "plan.cu", "mem_kernels.cu", "forward.cu", "backward.cu", "selftest.cu", "prof.cu", "plan_noalloc.cu"]
+SOURCES = ["api.cu", "plan.cu", "mem_kernels.cu", "forward.cu", "backward.cu", "selftest.cu", "prof.cu", "plan_noalloc.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

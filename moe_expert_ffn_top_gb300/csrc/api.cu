@@ -111,6 +111,7 @@ size_t moe_lora_workspace_bytes(const moe_lora_dims* d, int which) {
     case MOE_LORA_WS_SAVED: return saved_layout(d).total;
     case MOE_LORA_WS_FWD_SCRATCH: return fwd_layout(d).total;
     case MOE_LORA_WS_BWD_SCRATCH: return bwd_layout(d).total;
+    case MOE_LORA_WS_ROUTER_SCRATCH: return check_router_dims(d) == MOE_LORA_OK ? router_layout(d).total : 0;
     default: return 0;
   }
 }
@@ -186,6 +187,54 @@ int moe_lora_backward(const moe_lora_dims* d, const void* plan_ws, const void* s
   if ((rc = check_ptr(x)) || (rc = check_ptr(dy)) || (rc = check_ptr(dx))) return rc;
   if (!topk_w || !dw) return MOE_LORA_ERR_NULL;
   return run_backward(d, plan_ws, saved, x, topk_w, dy, w, dx, dw, g, scratch, sms, s);
+}
+
+int moe_lora_router_forward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, int32_t* topk_ids,
+                            float* topk_w, float* logits, void* scratch, size_t scratch_bytes, void* stream) {
+  int rc = check_router_dims(d);
+  if (rc) return rc;
+  if ((rc = check_ptr(scratch))) return rc;
+  if (scratch_bytes < router_layout(d).total) return MOE_LORA_ERR_WORKSPACE;
+  if ((rc = check_ptr(Wr))) return rc;
+  if (logits && !aligned16(logits)) return MOE_LORA_ERR_ALIGN;
+  if (d->T > 0) {
+    const void* ps[] = {x, topk_ids, topk_w};
+    for (const void* p : ps)
+      if ((rc = check_ptr(p))) return rc;
+  }
+  int sms;
+  if ((rc = device_sms(&sms))) return rc;
+  return run_router_forward(d, x, Wr, topk_ids, topk_w, logits, scratch, sms, static_cast<cudaStream_t>(stream));
+}
+
+int moe_lora_router_backward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, const int32_t* topk_ids,
+                             const float* topk_w, const float* dw, float* dlogits, float* dWr, uint16_t* dx,
+                             void* scratch, size_t scratch_bytes, void* stream) {
+  int rc = check_router_dims(d);
+  if (rc) return rc;
+  if ((rc = check_ptr(scratch))) return rc;
+  if (scratch_bytes < router_layout(d).total) return MOE_LORA_ERR_WORKSPACE;
+  if ((rc = check_ptr(Wr)) || (rc = check_ptr(dWr))) return rc;
+  if (dlogits && !aligned16(dlogits)) return MOE_LORA_ERR_ALIGN;
+  if (d->T > 0) {
+    const void* ps[] = {x, topk_ids, topk_w, dw, dx};
+    for (const void* p : ps)
+      if ((rc = check_ptr(p))) return rc;
+  }
+  int sms;
+  if ((rc = device_sms(&sms))) return rc;
+  return run_router_backward(d, x, Wr, topk_ids, topk_w, dw, dlogits, dWr, dx, scratch, sms,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int moe_lora_router_get_error(const void* scratch, void* stream) {
+  if (!scratch) return MOE_LORA_ERR_NULL;
+  int v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, scratch, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_LORA_ERR_CUDA;
+  return v;
 }
 
 int moe_lora_get_error(const moe_lora_dims* d, const void* plan_ws, void* stream) {

@@ -11,6 +11,7 @@ enum ProfSlot {
   K_SHRINK, K_GATHER_FWD, K_W13, K_W2, K_Z2W, K_B2_EXPAND, K_COMBINE_Y,
   K_DYB2, K_DB2, K_GATHER_BWD, K_W2_DGRAD, K_DW, K_DA2, K_W13_DGRAD, K_DB13, K_DY13W, K_A13_EXPAND, K_COMBINE_DX, K_DA13,
   K_DEQUANT, K_SPLIT_REDUCE, K_SELFTEST,
+  K_ROUTER_FWD, K_ROUTER_DL, K_ROUTER_DX, K_ROUTER_DW,
   K_NUM_SLOTS
 };
 

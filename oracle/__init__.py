@@ -8,7 +8,9 @@ compiles it with gcc and marshals torch CPU tensors to it through ctypes.
 
 Parity pins: see tests/test_oracle_pins.py (dense merged-weight special case
 against torch float64 autograd, central finite differences, zero-scale identity,
-plan brute force, MXFP4 decode table, multi-adapter standalone equality).
+plan brute force, MXFP4 decode table, multi-adapter standalone equality) and
+tests/test_router_pins.py (router against torch float64 softmax/top-k/autograd,
+the closed-form logit gradient, finite differences, tie order).
 """
 from __future__ import annotations
 
@@ -79,6 +81,8 @@ def lib(prec: str = "f32") -> ctypes.CDLL:
             L.oracle_ue8m0_value.restype = ctypes.c_double
             L.oracle_round_bf16.restype = ctypes.c_double
             L.oracle_round_bf16.argtypes = [ctypes.c_double]
+            L.oracle_router_forward.restype = ctypes.c_int
+            L.oracle_router_backward.restype = ctypes.c_int
             _LIBS[prec] = L
         return _LIBS[prec]
 
@@ -205,3 +209,48 @@ def ue8m0_value(b: int) -> float:
 
 def round_bf16(v: float) -> float:
     return lib("f32").oracle_round_bf16(v)
+
+
+def _router_args(x: torch.Tensor, Wr: torch.Tensor, prec: str, keep: _Keep):
+    T, H = x.shape
+    E = Wr.shape[0]
+    assert Wr.shape[1] == H
+    return T, H, E, _otensor(x, prec, keep), _otensor(Wr, prec, keep)
+
+
+def router_forward(x: torch.Tensor, Wr: torch.Tensor, k: int, prec: str = "f32", nthreads: int = 0):
+    """Softmax top-k router: logits [T,E], ids [T,k] int32, w [T,k] (oracle precision)."""
+    L = lib(prec)
+    keep = _Keep()
+    T, H, E, xo, wo = _router_args(x, Wr, prec, keep)
+    rd = _real_dtype(prec)
+    logits = torch.zeros(T, E, dtype=rd)
+    ids = torch.zeros(T, k, dtype=torch.int32)
+    w = torch.zeros(T, k, dtype=rd)
+    rc = L.oracle_router_forward(ctypes.c_int64(T), H, E, k, nthreads, ctypes.byref(xo), ctypes.byref(wo),
+                                 ctypes.c_void_p(logits.data_ptr()), ctypes.c_void_p(ids.data_ptr()),
+                                 ctypes.c_void_p(w.data_ptr()))
+    assert rc == 0
+    return logits, ids, w
+
+
+def router_backward(x: torch.Tensor, Wr: torch.Tensor, ids: torch.Tensor, dw: torch.Tensor, prec: str = "f32",
+                    nthreads: int = 0):
+    """Router backward for a fixed selection: dlogits [T,E], dWr [E,H], and the
+    router's part of grad-x [T,H] (oracle precision)."""
+    L = lib(prec)
+    keep = _Keep()
+    T, H, E, xo, wo = _router_args(x, Wr, prec, keep)
+    k = ids.shape[1]
+    rd = _real_dtype(prec)
+    ids = keep(ids.to(torch.int32).contiguous().cpu())
+    dw = keep(dw.detach().to(rd).contiguous().cpu())
+    dl = torch.zeros(T, E, dtype=rd)
+    dWr = torch.zeros(E, H, dtype=rd)
+    dx = torch.zeros(T, H, dtype=rd)
+    rc = L.oracle_router_backward(ctypes.c_int64(T), H, E, k, nthreads, ctypes.byref(xo), ctypes.byref(wo),
+                                  ctypes.c_void_p(ids.data_ptr()), ctypes.c_void_p(dw.data_ptr()),
+                                  ctypes.c_void_p(dl.data_ptr()), ctypes.c_void_p(dWr.data_ptr()),
+                                  ctypes.c_void_p(dx.data_ptr()))
+    assert rc == 0
+    return dl, dWr, dx

@@ -53,8 +53,10 @@
 #ifdef _OPENMP
 #include <omp.h>
 #define NTHREADS(d) ((d)->nthreads > 0 ? (d)->nthreads : omp_get_max_threads())
+#define NTHREADS_N(n) ((n) > 0 ? (n) : omp_get_max_threads())
 #else
 #define NTHREADS(d) 1
+#define NTHREADS_N(n) 1
 #endif
 
 #ifdef ORACLE_DOUBLE
@@ -514,6 +516,131 @@ int oracle_backward(const odims* d, const oinputs* in, const int64_t* tokens, in
   }
   free(S_dg); free(S_du); free(S_h); free(S_y1); free(S_y3); free(S_z2); free(S_dz2);
   free(S_dy1); free(S_dy3); free(M); free(gstart); free(gorder);
+  return 0;
+}
+
+/* ---------------- router (the routing step ahead of the expert path) ----------------
+ *
+ * The pages take the routes as given and return the routing-weight gradient
+ * ("grad-route", PR #9, Correctness coverage); the router itself follows the usual
+ * softmax top-k gate, read here as:
+ *   l_t = W_r x_t                         logits [E]
+ *   p_t = softmax(l_t) over all E experts
+ *   the k experts of largest p_t, in descending order, equal values to the lower
+ *   expert id (softmax is strictly increasing in each logit, so the selection is
+ *   made on l_t, which is the same order without exp/division rounding)
+ *   w_tj = p_t[e_j] / sum_j' p_t[e_j']    (the k weights renormalised to sum 1)
+ * The backward is the reverse-mode derivative of this map for a fixed selection:
+ *   dp_i = [i selected] (dw_i / S - sum_j dw_j p_j / S^2),  S = sum of selected p
+ *   dl   = p (dp - <p, dp>)                 (softmax backward)
+ *   dW_r = sum_t dl_t x_t^T,   dx_t = W_r^T dl_t
+ * Slots whose id is outside [0, E) are left out of the selection. */
+
+static void router_logits(int64_t H, int64_t E, const otensor* x, const otensor* Wr, int64_t t, real* xt,
+                          real* l) {
+  ld_row(x, t * H, H, xt);
+  for (int64_t e = 0; e < E; ++e) {
+    real acc = 0;
+    for (int64_t c = 0; c < H; ++c) acc += ld(Wr, e * H + c) * xt[c];
+    l[e] = acc;
+  }
+}
+
+static void softmax_all(int64_t E, const real* l, real* p) {
+  real m = l[0];
+  for (int64_t e = 1; e < E; ++e) m = l[e] > m ? l[e] : m;
+  real z = 0;
+  for (int64_t e = 0; e < E; ++e) z += REXP(l[e] - m);
+  for (int64_t e = 0; e < E; ++e) p[e] = REXP(l[e] - m) / z;
+}
+
+int oracle_router_forward(int64_t T, int32_t H, int32_t E, int32_t k, int32_t nthreads, const otensor* x,
+                          const otensor* Wr, real* logits, int32_t* ids, real* w) {
+  if (k > E) return -1;
+#pragma omp parallel num_threads(NTHREADS_N(nthreads))
+  {
+    real* xt = (real*)malloc(sizeof(real) * H);
+    real* l = (real*)malloc(sizeof(real) * E);
+    real* p = (real*)malloc(sizeof(real) * E);
+    char* taken = (char*)malloc((size_t)E);
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t t = 0; t < T; ++t) {
+      router_logits(H, E, x, Wr, t, xt, l);
+      if (logits)
+        for (int64_t e = 0; e < E; ++e) logits[t * E + e] = l[e];
+      softmax_all(E, l, p);
+      memset(taken, 0, (size_t)E);
+      real S = 0;
+      for (int j = 0; j < k; ++j) {
+        int best = -1;
+        for (int e = 0; e < E; ++e)
+          if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;  /* strict: ties keep the lower id */
+        taken[best] = 1;
+        ids[t * k + j] = best;
+        S += p[best];
+      }
+      for (int j = 0; j < k; ++j) w[t * k + j] = p[ids[t * k + j]] / S;
+    }
+    free(xt); free(l); free(p); free(taken);
+  }
+  return 0;
+}
+
+/* dlogits [T,E] (may be NULL), dWr [E,H], dx [T,H]: the router's part of the input
+ * gradient alone. */
+int oracle_router_backward(int64_t T, int32_t H, int32_t E, int32_t k, int32_t nthreads, const otensor* x,
+                           const otensor* Wr, const int32_t* ids, const real* dw, real* dlogits, real* dWr,
+                           real* dx) {
+  real* dl_all = (real*)calloc((size_t)(T > 0 ? T : 1) * E, sizeof(real));
+  if (!dl_all) return -1;
+#pragma omp parallel num_threads(NTHREADS_N(nthreads))
+  {
+    real* xt = (real*)malloc(sizeof(real) * H);
+    real* l = (real*)malloc(sizeof(real) * E);
+    real* p = (real*)malloc(sizeof(real) * E);
+    real* dp = (real*)malloc(sizeof(real) * E);
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t t = 0; t < T; ++t) {
+      router_logits(H, E, x, Wr, t, xt, l);
+      softmax_all(E, l, p);
+      real S = 0, num = 0;
+      for (int j = 0; j < k; ++j) {
+        int e = ids[t * k + j];
+        if (e < 0 || e >= E) continue;
+        S += p[e];
+        num += dw[t * k + j] * p[e];
+      }
+      for (int64_t e = 0; e < E; ++e) dp[e] = 0;
+      for (int j = 0; j < k; ++j) {
+        int e = ids[t * k + j];
+        if (e < 0 || e >= E) continue;
+        dp[e] += dw[t * k + j] / S - num / (S * S);
+      }
+      real pdp = 0;
+      for (int64_t e = 0; e < E; ++e) pdp += p[e] * dp[e];
+      real* dl = dl_all + t * E;
+      for (int64_t e = 0; e < E; ++e) dl[e] = p[e] * (dp[e] - pdp);
+      if (dlogits)
+        for (int64_t e = 0; e < E; ++e) dlogits[t * E + e] = dl[e];
+      for (int64_t c = 0; c < H; ++c) {
+        real acc = 0;
+        for (int64_t e = 0; e < E; ++e) acc += dl[e] * ld(Wr, e * H + c);
+        dx[t * H + c] = acc;
+      }
+    }
+    free(xt); free(l); free(p); free(dp);
+  }
+#pragma omp parallel for schedule(dynamic, 1) num_threads(NTHREADS_N(nthreads))
+  for (int64_t e = 0; e < E; ++e) {
+    real* o = dWr + e * H;
+    for (int64_t c = 0; c < H; ++c) o[c] = 0;
+    for (int64_t t = 0; t < T; ++t) {
+      const real g = dl_all[t * E + e];
+      if (g == 0) continue;
+      for (int64_t c = 0; c < H; ++c) o[c] += g * ld(x, t * H + c);
+    }
+  }
+  free(dl_all);
   return 0;
 }
 

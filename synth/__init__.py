@@ -198,6 +198,17 @@ def make_inputs(shp: Shape, seed: int = 0, device: str = "cpu") -> Dict[str, tor
     return out
 
 
+def make_router_inputs(T: int, H: int, E: int, k: int, seed: int = 0, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """Inputs of the routing step: x [T,H] ~ N(0,1), W_r [E,H] ~ N(0, 1/H) (bf16 values);
+    the upstream routing-weight gradient dw [T,k] ~ N(0,1) fp32 and a grad-x the router
+    adds into, dx0 [T,H] ~ N(0,1) bf16."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    return {"x": _randn_bf16(g, (T, H), 1.0, device, 8192),
+            "Wr": _randn_bf16(g, (E, H), 1.0 / math.sqrt(H), device),
+            "dw": _randn(g, (T, k), 1.0, device),
+            "dx0": _randn_bf16(g, (T, H), 1.0, device, 8192)}
+
+
 def sha256(t: torch.Tensor) -> str:
     """SHA-256 of a tensor's bytes (input manifests)."""
     b = t.detach().contiguous().cpu().view(torch.uint8).numpy().tobytes()

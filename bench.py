@@ -132,7 +132,8 @@ class ClockSampler:
         self.dev = device_index
 
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        # 20 ms: the clock under a power cap moves within one 30 ms step
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "20"]
         try:
             uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
             cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
@@ -157,24 +158,26 @@ class ClockSampler:
         self.f.seek(0)
         rows = [l.strip().split(", ") for l in self.f.read().splitlines() if l.strip()]
         os.unlink(self.f.name)
-        sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for r in rows:
             if len(r) < 9:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                power.append(float(r[3]))
+                samples.append((float(r[1]), float(r[2]), float(r[3]),
+                                [n for n, v in zip(names, r[5:9]) if v.strip().lower().startswith("active")]))
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+        # "under load": samples drawing at least 40% of the window's peak power
+        # (the sampler also sees the gaps around the timed region)
+        pmax = max(p for _, _, p, _ in samples)
+        load = [s for s in samples if s[2] >= 0.4 * pmax] or samples
+        reasons = sorted({n for s in load for n in s[3]})
+        return {"sm_mhz": statistics.median(s[0] for s in load), "sm_max_mhz": max(s[1] for s in samples),
+                "reasons": reasons, "samples": len(samples), "samples_under_load": len(load),
+                "power_w_median": statistics.median(s[2] for s in load), "power_w_max": pmax}
 
 
 # ------------------------------------------------------------------ CPU oracle

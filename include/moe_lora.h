@@ -267,7 +267,13 @@ MOE_LORA_API const char* moe_lora_strerror(int code);
  * are reported through moe_lora_gemm_selftest_error(). */
 MOE_LORA_API int moe_lora_gemm_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn, const uint16_t* B,
                            int32_t b_mn, float* C, void* stream);
-/* Device error word of the self-test GEMM (MOE_LORA_DEV_* bits); synchronises
+/* The same plain GEMM on the two-SM engine the base expert GEMMs use: clusters of
+ * two CTAs sharing each 256-row tile through tcgen05.mma.cta_group::2 (an odd last
+ * 128-row tile runs on one CTA of the pair).  Same arguments, rules and error
+ * reporting as moe_lora_gemm_selftest. */
+MOE_LORA_API int moe_lora_gemm_pair_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
+                                             const uint16_t* B, int32_t b_mn, float* C, void* stream);
+/* Device error word of the self-test GEMMs (MOE_LORA_DEV_* bits); synchronises
  * the stream and clears the word. */
 MOE_LORA_API int moe_lora_gemm_selftest_error(void* stream);
 

@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_gemm_selftest.restype = ctypes.c_int
         L.moe_lora_gemm_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32, P,
                                              ctypes.c_int32, P, P]
+        L.moe_lora_gemm_pair_selftest.restype = ctypes.c_int
+        L.moe_lora_gemm_pair_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32,
+                                                  P, ctypes.c_int32, P, P]
         L.moe_lora_profile_enable.restype = ctypes.c_int
         L.moe_lora_profile_enable.argtypes = [ctypes.c_int]
         L.moe_lora_profile_read.restype = ctypes.c_int
@@ -272,6 +275,17 @@ def moe_lora_gemm_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor, b_mn: b
                                       _ptr(B, torch.bfloat16, "B"), int(b_mn), _ptr(C, torch.float32, "C"),
                                       _stream(stream))
     _check(rc, "moe_lora_gemm_selftest")
+
+
+def moe_lora_gemm_pair_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor, b_mn: bool, C: torch.Tensor,
+                                stream=None) -> None:
+    """As moe_lora_gemm_selftest, on the two-SM (cta_group::2) engine."""
+    M, N = C.shape
+    K = A.shape[0] if a_mn else A.shape[1]
+    rc = lib().moe_lora_gemm_pair_selftest(M, N, K, _ptr(A, torch.bfloat16, "A"), int(a_mn),
+                                           _ptr(B, torch.bfloat16, "B"), int(b_mn), _ptr(C, torch.float32, "C"),
+                                           _stream(stream))
+    _check(rc, "moe_lora_gemm_pair_selftest")
 
 
 def moe_lora_gemm_selftest_error(stream=None) -> int:

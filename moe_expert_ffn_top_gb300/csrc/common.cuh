@@ -62,7 +62,7 @@ inline PlanLayout plan_layout(const moe_lora_dims* d) {
   L.tok_off = take(sizeof(int32_t) * (kMaxAdapters + 1));
   L.tok_tile = take(sizeof(int32_t) * (kMaxAdapters + 1));
   L.wtile_off = take(sizeof(int32_t) * (G + 1));
-  L.wtile = take(sizeof(int32_t) * (P / kBlockM + 1));
+  L.wtile = take(2 * sizeof(int32_t) * (P / kBlockM + 1));
   L.chunk_base = take(sizeof(int32_t) * G * (plan_chunks(d) > 0 ? plan_chunks(d) : 1));
   L.total = o;
   return L;
@@ -173,7 +173,7 @@ struct PlanView {
   const int* tok_off;        // [A+1] first token of each adapter
   const int* tok_tile;       // [A+1] first 128-token tile of each adapter
   const int* wtile_off;      // [G+1] first 256-row tile of each group
-  const int* wtile;          // 256-row tiles: (first 128-row tile index << 1) | (halves - 1)
+  const int2* wtile;         // 256-row tiles: x = (first 128-row tile index << 1) | (halves - 1), y = group
   int64_t T;
   int G, E, A, k;
 };
@@ -191,7 +191,7 @@ inline PlanView make_plan_view(const moe_lora_dims* d, const void* ws) {
   v.tok_off = (const int*)(b + L.tok_off);
   v.tok_tile = (const int*)(b + L.tok_tile);
   v.wtile_off = (const int*)(b + L.wtile_off);
-  v.wtile = (const int*)(b + L.wtile);
+  v.wtile = (const int2*)(b + L.wtile);
   v.T = d->T;
   v.G = d->A * d->E;
   v.E = d->E;

@@ -3,6 +3,7 @@
 //   F1 shrink (per token)  ->  F2 gather (routed rows, zero padding)
 //   F3 W13 + B1/B3 expand + SwiGLU  ->  F4 W2 + A2 shrink
 //   F6a per-token Z2 combine  ->  F6 B2 expand per token  ->  routing-weighted combine
+#include "gemm_pair.cuh"
 #include "gemm_problems.cuh"
 #include "launch.h"
 #include "passes.h"
@@ -30,7 +31,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
 
   const uint64_t T = (uint64_t)d->T, H = d->H, I = d->I, E = d->E, A = d->A, r = d->r;
   const uint64_t P = (uint64_t)rows_cap(d), G = A * E;
-  const uint32_t r16 = (uint32_t)((r + 15) / 16 * 16);
+  const uint32_t r32 = (uint32_t)((r + 31) / 32 * 32);
   const int max_tok_tiles = (int)((T + 127) / 128) + d->A;
   const int max_row_tiles = (int)(P / 128);
   int rc = 0;
@@ -99,12 +100,12 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.clamp = d->act_clamp;
     LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13));
   }
-  // F4/F5: W2 + expert-local A2 shrink
+  // F4/F5: W2 + expert-local A2 shrink (two-SM tiles)
   {
-    ProbW2 p;
+    ProbW2Pair p;
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
-    MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 256));
-    MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, r16));
+    MAP(tmap_3d(&p.mW2h, bW2, I, H, E, 64, 128));
+    MAP(tmap_3d(&p.mA2h, w->A2, I, r, G, 64, r32 / 2));
     p.pl = pl;
     p.err = pl.err;
     p.O = O;
@@ -112,7 +113,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W2));
+    LAUNCH(launch_gemm_pair(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W2));
   }
   // F6a: per-token weighted sum of the A2 shrink
   LAUNCH(launch_z2w(pl, Z2, topk_w, Z2w, d->r, num_sms, stream));

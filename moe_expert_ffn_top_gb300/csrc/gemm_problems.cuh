@@ -26,16 +26,19 @@ __device__ __forceinline__ int adapter_of_tile(const PlanView& pl, int t) {
   return a;
 }
 
-// 256-row tile t of an M-grouped problem with ntn column tiles: rows
-// [m0, m0 + 128*mh) of one plan group (mh = 2, or 1 for a group's odd last tile).
-__device__ __forceinline__ void wide_tile(const PlanView& pl, int t, int ntn, TileInfo& ti) {
-  const int w = pl.wtile[t / ntn];
-  const int mt = w >> 1;
-  ti.mh = (w & 1) + 1;
+// 256-row tile of an M-grouped problem from its plan entry w: rows
+// [m0, m0 + 128*mh) of plan group w.y (mh = 2, or 1 for a group's odd last tile).
+__device__ __forceinline__ void wide_tile_from(int2 w, TileInfo& ti) {
+  const int mt = w.x >> 1;
+  ti.mh = (w.x & 1) + 1;
   ti.m0 = mt * 128;
   ti.mend = ti.m0 + 128 * ti.mh;
-  ti.g = pl.tile_group[mt];
+  ti.g = w.y;
   ti.k0 = 0;
+}
+// 256-row tile t of an M-grouped problem with ntn column tiles.
+__device__ __forceinline__ void wide_tile(const PlanView& pl, int t, int ntn, TileInfo& ti) {
+  wide_tile_from(pl.wtile[t / ntn], ti);
 }
 
 // 128-row tile t of an M-grouped problem with ntn column tiles.
@@ -169,6 +172,8 @@ __device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], 
 }
 
 __device__ __forceinline__ int round16(int r) { return (r + 15) & ~15; }
+// N of a two-SM (M = 256) MMA: a multiple of 32, so each CTA holds a multiple of 16 columns.
+__device__ __forceinline__ int round32(int r) { return (r + 31) & ~31; }
 
 // Coalesced epilogue row access.  An epilogue warp owns 32 consecutive
 // accumulator rows, one per lane.  Storing "my row" directly makes every 16-byte
@@ -1024,6 +1029,81 @@ struct ProbDA13 {
 };
 
 // =====================================================================================
+// Two-SM (cta_group::2) forms of the four base expert GEMMs, for gemm_pair.cuh.
+// A tile is 256 rows of one plan group: rank-0 CTA rows [m0, m0+128), rank-1 CTA
+// rows [m0+128, m0+256) (absent on a group's odd last tile).  The N columns of every
+// pair MMA are split in halves: rank v holds B columns [v*N/2, (v+1)*N/2).  Each
+// CTA's accumulator has the same column meaning as the one-SM problem's, so the
+// fused epilogues are inherited unchanged.
+// =====================================================================================
+
+// F4/F5: base tiles split 256 W2 rows 128 / 128; the A2 tile (N = round32(r))
+// splits the A2 rows in halves of round32(r)/2 (rows past r read as zeros).
+struct ProbW2Pair : ProbW2 {
+  CUtensorMap mW2h, mA2h;  // W2 (I,H,E) box(64,128,1); A2 (I,r,G) box(64,round32(r)/2,1),
+                           // in place of the one-SM mW2/mA2
+  __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
+  __device__ int2 tile_fetch(int t) const { return pl.wtile[t / ntn()]; }
+  __device__ TileInfo tile_at(int t, int2 w) const {
+    const int nt = t % ntn();
+    TileInfo ti;
+    wide_tile_from(w, ti);
+    ti.sub = nt == H / 256;
+    ti.n0 = ti.sub ? 0 : nt * 256;
+    ti.nk = I / kBK;
+    return ti;
+  }
+  __device__ TileInfo tile(int t) const { return tile_at(t, tile_fetch(t)); }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mAct);
+    tma_prefetch_map(&mW2h);
+    tma_prefetch_map(&mA2h);
+  }
+  __device__ uint32_t tx_bytes(const TileInfo& ti, int) const {
+    return (uint32_t)(ti.mh * kAStage128 + (ti.sub ? round32(r) : 256) * 128);
+  }
+  __device__ void load_pair(const TileInfo& ti, int ks, int rank, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    if (rank < ti.mh) tma_load_2d_pair(sa, &mAct, bar, ks * kBK, ti.m0 + rank * 128);
+    if (!ti.sub)
+      tma_load_3d_pair(sb, &mW2h, bar, ks * kBK, ti.n0 + rank * 128, ti.g % pl.E);
+    else
+      tma_load_3d_pair(sb, &mA2h, bar, ks * kBK, rank * (round32(r) / 2), ti.g);
+  }
+  __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
+    return MmaStep{ti.sub ? round32(r) : 256, 0, 0, ks == 0};
+  }
+};
+
+// B3/B4: the 256 columns of I are two 64-wide MN-major boxes per CTA.
+struct ProbW2DgradPair : ProbW2Dgrad {
+  __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
+  __device__ int2 tile_fetch(int t) const { return pl.wtile[t / ntn()]; }
+  __device__ TileInfo tile_at(int t, int2 w) const {
+    const int nt = t % ntn();
+    TileInfo ti;
+    wide_tile_from(w, ti);
+    ti.n0 = nt * 256;
+    ti.sub = nt;
+    ti.nk = H / kBK + nkr();
+    return ti;
+  }
+  __device__ TileInfo tile(int t) const { return tile_at(t, tile_fetch(t)); }
+  __device__ uint32_t tx_bytes(const TileInfo& ti, int) const { return (uint32_t)(ti.mh * kAStage128 + 4 * 8192); }
+  __device__ void load_pair(const TileInfo& ti, int ks, int rank, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    const int nb = H / kBK;
+    const int mrow = ti.m0 + rank * 128, nc = ti.n0 + rank * 128;
+    if (ks < nb) {
+      if (rank < ti.mh) tma_load_2d_pair(sa, &mDp, bar, ks * kBK, mrow);
+      for (int c = 0; c < 2; ++c) tma_load_3d_pair(sb + c * 8192, &mW2, bar, nc + c * 64, ks * kBK, ti.g % pl.E);
+    } else {
+      const int kb = ks - nb;
+      if (rank < ti.mh) tma_load_2d_pair(sa, &mD2p, bar, kb * kBK, mrow);
+      for (int c = 0; c < 2; ++c) tma_load_3d_pair(sb + c * 8192, &mA2, bar, nc + c * 64, kb * kBK, ti.g);
+    }
+  }
+};
+
+// =====================================================================================
 // Plain GEMM for engine self-tests: C[M,N] fp32 = sum_k A(m,k) B(n,k).
 // A is [M,K] (K-major) or [K,M] (MN-major); B is [N,K] or [K,N].  M % 128 == 0,
 // K % 64 == 0, N % 256 == 0 or N <= 256 with N % 16 == 0.
@@ -1073,14 +1153,60 @@ struct ProbPlain {
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{tn(), 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    const int64_t m = (int64_t)ti.m0 + row;
+    float* o0 = C + ((int64_t)ti.m0 + row - (threadIdx.x & 31)) * N + ti.n0;  // warp's first row
     for (int c = c0; c < tn(); c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      store_row_f32(C + m * N + ti.n0 + c, v, 1.0f, tn() - c < 32 ? tn() - c : 32);
+      warp_store_rows_f32(o0 + c, N, 32, v, 1.0f, tn() - c < 32 ? tn() - c : 32, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
+};
+
+// Plain GEMM on the two-SM engine (self-test): 256-row tiles, the MMA N (tn rounded
+// up to 32) split in halves.  M % 128 == 0 (an odd last 128-row tile runs on the
+// rank-0 CTA alone).
+template <bool AMN, bool BMN>
+struct ProbPlainPair : ProbPlain<AMN, BMN> {
+  using Base = ProbPlain<AMN, BMN>;
+  // B maps: K-major box(64, tn/2); MN-major box(64,64) as in the one-SM form.
+  __device__ int num_tiles() const { return (this->M + 255) / 256 * this->ntn(); }
+  __device__ int2 tile_fetch(int) const { return make_int2(0, 0); }
+  __device__ TileInfo tile_at(int t, int2) const { return tile(t); }
+  __device__ TileInfo tile(int t) const {
+    TileInfo ti;
+    ti.m0 = t / this->ntn() * 256;
+    ti.mh = this->M - ti.m0 >= 256 ? 2 : 1;
+    ti.n0 = t % this->ntn() * 256;
+    ti.mend = this->M;
+    ti.g = 0;
+    ti.sub = 0;
+    ti.nk = this->K / kBK;
+    ti.k0 = 0;
+    return ti;
+  }
+  __device__ int half_n() const { return round32(this->tn()) / 2; }
+  __device__ int nbox() const { return (half_n() + 63) / 64; }
+  __device__ uint32_t tx_bytes(const TileInfo& ti, int) const {
+    return (uint32_t)(ti.mh * kAStage128 + 2 * (BMN ? nbox() * 8192 : half_n() * 128));
+  }
+  __device__ void load_pair(const TileInfo& ti, int ks, int rank, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    const int kt = ks * kBK, mrow = ti.m0 + rank * 128, nc = ti.n0 + rank * half_n();
+    if (rank < ti.mh) {
+      if (AMN) {
+        tma_load_2d_pair(sa, &this->mA, bar, mrow, kt);
+        tma_load_2d_pair(sa + 8192, &this->mA, bar, mrow + 64, kt);
+      } else {
+        tma_load_2d_pair(sa, &this->mA, bar, kt, mrow);
+      }
+    }
+    if (BMN) {
+      for (int c = 0; c < nbox(); ++c) tma_load_2d_pair(sb + c * 8192, &this->mB, bar, nc + c * 64, kt);
+    } else {
+      tma_load_2d_pair(sb, &this->mB, bar, kt, nc);
+    }
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round32(this->tn()), 0, 0, ks == 0}; }
 };
 
 }  // namespace moelora

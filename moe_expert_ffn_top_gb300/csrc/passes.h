@@ -23,7 +23,8 @@ int run_router_backward(const moe_lora_dims* d, const uint16_t* x, const uint16_
                         const float* w, const float* dw, float* dlogits, float* dWr, uint16_t* dx, void* scratch,
                         int num_sms, cudaStream_t stream);
 
+// pair != 0: on the two-SM (cta_group::2) engine.
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,
-                   int* err, int num_sms, cudaStream_t stream);
+                   int* err, int num_sms, int pair, cudaStream_t stream);
 
 }  // namespace moelora

@@ -148,7 +148,7 @@ __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __
 }
 
 __global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restrict__ wtile_off,
-                          int* __restrict__ wtile) {
+                          int2* __restrict__ wtile) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     int carry = 0;
@@ -169,7 +169,7 @@ __global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restric
   __syncthreads();
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const int m = offsets[g] / kBlockM, n = (offsets[g + 1] - offsets[g]) / kBlockM, base = wtile_off[g];
-    for (int j = 0; 2 * j < n; ++j) wtile[base + j] = ((m + 2 * j) << 1) | (n - 2 * j >= 2 ? 1 : 0);
+    for (int j = 0; 2 * j < n; ++j) wtile[base + j] = make_int2(((m + 2 * j) << 1) | (n - 2 * j >= 2 ? 1 : 0), g);
   }
 }
 
@@ -186,7 +186,7 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
   int* tok_off = (int*)(b + L.tok_off);
   int* tok_tile = (int*)(b + L.tok_tile);
   int* wtile_off = (int*)(b + L.wtile_off);
-  int* wtile = (int*)(b + L.wtile);
+  int2* wtile = (int2*)(b + L.wtile);
   int* chunk_base = (int*)(b + L.chunk_base);
   const int G = d->A * d->E;
   const int64_t TK = d->T * d->k;

@@ -19,6 +19,6 @@ __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __
 
 // 256-row tiles: each group's 128-row tiles in pairs (a lone last tile is a half).
 __global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restrict__ wtile_off,
-                          int* __restrict__ wtile);
+                          int2* __restrict__ wtile);
 
 }  // namespace moelora

@@ -97,7 +97,7 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
   int* tok_off = (int*)(b + L.tok_off);
   int* tok_tile = (int*)(b + L.tok_tile);
   int* wtile_off = (int*)(b + L.wtile_off);
-  int* wtile = (int*)(b + L.wtile);
+  int2* wtile = (int2*)(b + L.wtile);
   const int64_t TK = d->T * d->k;
   const int nch = (int)nchunks;
   if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_LORA_ERR_CUDA;

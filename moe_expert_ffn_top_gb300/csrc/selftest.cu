@@ -1,16 +1,15 @@
-// Plain GEMM through the same tcgen05/TMA engine as the MoE path, for the
-// engine self-test entry point (all four operand-majorness combinations).
+// Plain GEMM through the same tcgen05/TMA engines as the MoE path, for the
+// engine self-test entry points (all four operand-majorness combinations, on
+// the one-SM engine and on the two-SM cta_group::2 engine).
+#include "gemm_pair.cuh"
 #include "gemm_problems.cuh"
 #include "passes.h"
 #include "tmap.h"
 
 namespace moelora {
 
-template <bool AMN, bool BMN>
-static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, float* C, int* err, int num_sms,
-                 cudaStream_t stream) {
-  ProbPlain<AMN, BMN> p;
-  const uint32_t tn = N < 256 ? (uint32_t)N : 256u;
+template <class Prob, bool AMN, bool BMN>
+static int plain_maps(Prob& p, int M, int N, int K, const uint16_t* A, const uint16_t* B, uint32_t b_rows) {
   if (AMN) {
     if (tmap_2d(&p.mA, A, (uint64_t)M, (uint64_t)K, 64, 64)) return MOE_LORA_ERR_CUDA;
   } else {
@@ -19,23 +18,48 @@ static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, floa
   if (BMN) {
     if (tmap_2d(&p.mB, B, (uint64_t)N, (uint64_t)K, 64, 64)) return MOE_LORA_ERR_CUDA;
   } else {
-    if (tmap_2d(&p.mB, B, (uint64_t)K, (uint64_t)N, 64, tn)) return MOE_LORA_ERR_CUDA;
+    if (tmap_2d(&p.mB, B, (uint64_t)K, (uint64_t)N, 64, b_rows)) return MOE_LORA_ERR_CUDA;
   }
+  return MOE_LORA_OK;
+}
+
+template <bool AMN, bool BMN>
+static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, float* C, int* err, int num_sms,
+                 bool pair, cudaStream_t stream) {
+  const uint32_t tn = N < 256 ? (uint32_t)N : 256u;
+  const int ntn = (N + 255) / 256;
+  int rc;
+  if (pair) {
+    ProbPlainPair<AMN, BMN> p;
+    if ((rc = plain_maps<ProbPlainPair<AMN, BMN>, AMN, BMN>(p, M, N, K, A, B, ((tn + 31) & ~31u) / 2))) return rc;
+    p.err = err;
+    p.C = C;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    return launch_gemm_pair(p, (M + 255) / 256 * ntn, num_sms, stream, K_SELFTEST) == cudaSuccess
+               ? MOE_LORA_OK
+               : MOE_LORA_ERR_CUDA;
+  }
+  ProbPlain<AMN, BMN> p;
+  if ((rc = plain_maps<ProbPlain<AMN, BMN>, AMN, BMN>(p, M, N, K, A, B, tn))) return rc;
   p.err = err;
   p.C = C;
   p.M = M;
   p.N = N;
   p.K = K;
-  const int tiles = M / 128 * ((N + 255) / 256);
-  return launch_gemm(p, tiles, num_sms, stream, K_SELFTEST) == cudaSuccess ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
+  return launch_gemm(p, M / 128 * ntn, num_sms, stream, K_SELFTEST) == cudaSuccess ? MOE_LORA_OK
+                                                                                  : MOE_LORA_ERR_CUDA;
 }
 
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,
-                   int* err, int num_sms, cudaStream_t stream) {
-  if (a_mn && b_mn) return plain<true, true>(M, N, K, A, B, C, err, num_sms, stream);
-  if (a_mn) return plain<true, false>(M, N, K, A, B, C, err, num_sms, stream);
-  if (b_mn) return plain<false, true>(M, N, K, A, B, C, err, num_sms, stream);
-  return plain<false, false>(M, N, K, A, B, C, err, num_sms, stream);
+                   int* err, int num_sms, int pair, cudaStream_t stream) {
+  const bool pr = pair != 0;
+  if (a_mn && b_mn) return plain<true, true>(M, N, K, A, B, C, err, num_sms, pr, stream);
+  if (a_mn) return plain<true, false>(M, N, K, A, B, C, err, num_sms, pr, stream);
+  if (b_mn) return plain<false, true>(M, N, K, A, B, C, err, num_sms, pr, stream);
+  return plain<false, false>(M, N, K, A, B, C, err, num_sms, pr, stream);
 }
 
 }  // namespace moelora
+

@@ -44,6 +44,25 @@ def test_engine_gemm(a_mn, b_mn, M, N, K):
     assert rel_l2(C, ref) < 1e-5
 
 
+@pytest.mark.parametrize("a_mn", [False, True])
+@pytest.mark.parametrize("b_mn", [False, True])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (384, 512, 320), (128, 16, 128), (640, 144, 192),
+                                   (2432, 768, 1024)])
+def test_engine_gemm_pair(a_mn, b_mn, M, N, K):
+    """The two-SM engine: 256-row tiles shared by a CTA pair, including an odd last
+    128-row tile (M = 128, 384, 640) and more tiles than clusters (M = 2432)."""
+    g = torch.Generator(device="cuda").manual_seed(M * 5 + N + K)
+    A = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    m.moe_lora_gemm_pair_selftest(A.t().contiguous() if a_mn else A, a_mn, B.t().contiguous() if b_mn else B, b_mn,
+                                  C)
+    torch.cuda.synchronize()
+    assert m.moe_lora_gemm_selftest_error() == 0
+    ref = A.double() @ B.double().t()
+    assert rel_l2(C, ref) < 1e-5
+
+
 # ----------------------------------------------------------------------------- plan
 def _plan_check(ids_cpu, E, shp, offs=None, BM=128):
     d = m.make_dims(shp.T, shp.H, shp.I, E, shp.k, shp.r, shp.A)

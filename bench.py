@@ -94,7 +94,8 @@ def kernel_work(T, R, H, I, r, k, E=256):
 
 # Sources that define the grouped-GEMM kernels and their launch configuration:
 # a change to any of them invalidates committed DRAM-traffic counters.
-GEMM_SOURCES = ("sm100_ptx.cuh", "common.cuh", "gemm_engine.cuh", "gemm_problems.cuh", "forward.cu", "backward.cu")
+GEMM_SOURCES = ("sm100_ptx.cuh", "common.cuh", "gemm_engine.cuh", "gemm_pair.cuh", "gemm_problems.cuh", "forward.cu",
+                "backward.cu")
 
 
 def src_hash():

@@ -228,28 +228,34 @@ MOE_LORA_API int64_t moe_lora_launch_count(int reset);
  * Backward, for the selection made in the forward: since w_t is the softmax of
  * the selected logits alone, dl_te = w_tj (dw_tj - sum_j' w_tj' dw_tj') at
  * e = e_j and 0 elsewhere; dW_r = sum_t dl_t^T x_t; grad-x gains dl_t W_r.
- * Requirements beyond moe_lora_dims' rules: A == 1, 16 <= E <= 256 with
- * E % 16 == 0, k <= E (else MOE_LORA_ERR_UNSUPPORTED / MOE_LORA_ERR_DIMS).
+ * Several adapters (OpenPipe/ART PR #1139, Behavior: each adapter routes with its
+ * own router) own contiguous token ranges given by adapter_offsets [A+1] int64,
+ * HOST, with the rules of moe_lora_plan (NULL allowed when A == 1); adapter a's
+ * tokens use W_r[a] and contribute to dW_r[a] only, and every adapter's results
+ * equal its standalone run with the same tokens bit for bit.
+ * Requirements beyond moe_lora_dims' rules: 16 <= E <= 256 with E % 16 == 0,
+ * k <= E (else MOE_LORA_ERR_UNSUPPORTED / MOE_LORA_ERR_DIMS).
  * `scratch` is a device buffer of moe_lora_workspace_bytes(.., MOE_LORA_WS_ROUTER_SCRATCH);
  * its first word is the device error word both calls clear and
  * moe_lora_router_get_error() reads. */
 
-/* x [T,H] bf16, W_r [E,H] bf16.  Writes topk_ids [T,k] int32 (largest first) and
+/* x [T,H] bf16, W_r [A,E,H] bf16.  Writes topk_ids [T,k] int32 (largest first) and
  * topk_w [T,k] fp32; logits [T,E] fp32 as well when non-NULL.  One launch. */
 MOE_LORA_API int moe_lora_router_forward(const moe_lora_dims* dims, const uint16_t* x, const uint16_t* Wr,
-                                         int32_t* topk_ids, float* topk_w, float* logits, void* scratch,
-                                         size_t scratch_bytes, void* stream);
+                                         const int64_t* adapter_offsets, int32_t* topk_ids, float* topk_w,
+                                         float* logits, void* scratch, size_t scratch_bytes, void* stream);
 
 /* topk_ids / topk_w as written by moe_lora_router_forward (slots with an id
- * outside [0, E) are skipped), dw [T,k] fp32 (e.g. moe_lora_backward's dw).
- * Writes dWr [E,H] fp32 and, when non-NULL, dlogits [T,E] fp32.  dx [T,H] bf16
+ * outside [0, E) are skipped), dw [T,k] fp32 (e.g. moe_lora_backward's dw), the
+ * same adapter_offsets as the forward.  Writes dWr [A,E,H] fp32 and, when
+ * non-NULL, dlogits [T,E] fp32.  dx [T,H] bf16
  * is READ AND UPDATED in place, dx <- bf16(dx + dl W_r), so that the expert
  * path's grad-x and the router's share one buffer (the one exception to
  * "outputs are overwritten"; pass a zeroed dx for the router's part alone). */
 MOE_LORA_API int moe_lora_router_backward(const moe_lora_dims* dims, const uint16_t* x, const uint16_t* Wr,
-                                          const int32_t* topk_ids, const float* topk_w, const float* dw,
-                                          float* dlogits, float* dWr, uint16_t* dx, void* scratch,
-                                          size_t scratch_bytes, void* stream);
+                                          const int64_t* adapter_offsets, const int32_t* topk_ids,
+                                          const float* topk_w, const float* dw, float* dlogits, float* dWr,
+                                          uint16_t* dx, void* scratch, size_t scratch_bytes, void* stream);
 
 /* Reads (and keeps) the device error word of a router scratch buffer
  * (MOE_LORA_DEV_* bits); synchronises `stream`. */

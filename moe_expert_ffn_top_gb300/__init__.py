@@ -96,9 +96,10 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_gemm_selftest_error.restype = ctypes.c_int
         L.moe_lora_gemm_selftest_error.argtypes = [P]
         L.moe_lora_router_forward.restype = ctypes.c_int
-        L.moe_lora_router_forward.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_lora_router_forward.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_lora_router_backward.restype = ctypes.c_int
-        L.moe_lora_router_backward.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_lora_router_backward.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t,
+                                               P]
         L.moe_lora_router_get_error.restype = ctypes.c_int
         L.moe_lora_router_get_error.argtypes = [P, P]
         _lib = L
@@ -227,12 +228,23 @@ def moe_lora_get_error(dims: Dims, plan_ws: torch.Tensor, stream=None) -> int:
     return rc
 
 
+def _offsets(adapter_offsets: Optional[Sequence[int]]):
+    if adapter_offsets is None:
+        return None
+    vals = [int(v) for v in adapter_offsets]
+    return (ctypes.c_int64 * len(vals))(*vals)
+
+
 def moe_lora_router_forward(dims: Dims, x: torch.Tensor, Wr: torch.Tensor, topk_ids: torch.Tensor,
                             topk_w: torch.Tensor, logits: Optional[torch.Tensor], scratch: torch.Tensor,
-                            stream=None) -> None:
-    """Softmax top-k router: topk_ids [T,k] int32, topk_w [T,k] fp32 (and logits [T,E] fp32 if given)."""
+                            stream=None, adapter_offsets: Optional[Sequence[int]] = None) -> None:
+    """Softmax top-k router: topk_ids [T,k] int32, topk_w [T,k] fp32 (and logits [T,E] fp32 if given).
+    W_r is [E,H] or [A,E,H]; adapter_offsets [A+1] (host) splits the tokens between adapters."""
+    offs = _offsets(adapter_offsets)
     rc = lib().moe_lora_router_forward(ctypes.byref(dims), _ptr(x, torch.bfloat16, "x"),
-                                       _ptr(Wr, torch.bfloat16, "Wr"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                       _ptr(Wr, torch.bfloat16, "Wr"),
+                                       ctypes.cast(offs, ctypes.c_void_p) if offs is not None else None,
+                                       _ptr(topk_ids, torch.int32, "topk_ids"),
                                        _ptr(topk_w, torch.float32, "topk_w"), _ptr(logits, torch.float32, "logits"),
                                        _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream))
     _check(rc, "moe_lora_router_forward")
@@ -240,11 +252,15 @@ def moe_lora_router_forward(dims: Dims, x: torch.Tensor, Wr: torch.Tensor, topk_
 
 def moe_lora_router_backward(dims: Dims, x: torch.Tensor, Wr: torch.Tensor, topk_ids: torch.Tensor,
                              topk_w: torch.Tensor, dw: torch.Tensor, dlogits: Optional[torch.Tensor],
-                             dWr: torch.Tensor, dx: torch.Tensor, scratch: torch.Tensor, stream=None) -> None:
-    """Router backward: dWr [E,H] fp32 (and dlogits [T,E] fp32 if given); dx [T,H] bf16 is
-    updated in place, dx <- bf16(dx + dlogits W_r)."""
+                             dWr: torch.Tensor, dx: torch.Tensor, scratch: torch.Tensor, stream=None,
+                             adapter_offsets: Optional[Sequence[int]] = None) -> None:
+    """Router backward: dWr [E,H] or [A,E,H] fp32 (and dlogits [T,E] fp32 if given); dx [T,H]
+    bf16 is updated in place, dx <- bf16(dx + dlogits W_r)."""
+    offs = _offsets(adapter_offsets)
     rc = lib().moe_lora_router_backward(ctypes.byref(dims), _ptr(x, torch.bfloat16, "x"),
-                                        _ptr(Wr, torch.bfloat16, "Wr"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                        _ptr(Wr, torch.bfloat16, "Wr"),
+                                        ctypes.cast(offs, ctypes.c_void_p) if offs is not None else None,
+                                        _ptr(topk_ids, torch.int32, "topk_ids"),
                                         _ptr(topk_w, torch.float32, "topk_w"), _ptr(dw, torch.float32, "dw"),
                                         _ptr(dlogits, torch.float32, "dlogits"), _ptr(dWr, torch.float32, "dWr"),
                                         _ptr(dx, torch.bfloat16, "dx"), _ptr(scratch),

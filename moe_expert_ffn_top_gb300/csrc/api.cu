@@ -123,20 +123,8 @@ int moe_lora_plan(const moe_lora_dims* d, const int32_t* topk_ids, const int64_t
   if ((rc = check_ptr(plan_ws))) return rc;
   if (d->T > 0 && !topk_ids) return MOE_LORA_ERR_NULL;
   if (plan_bytes < plan_layout(d).total) return MOE_LORA_ERR_WORKSPACE;
-  if (d->A > 1 && !adapter_offsets) return MOE_LORA_ERR_NULL;
   AdapterTable at;
-  std::memset(&at, 0, sizeof(at));
-  at.n = d->A;
-  for (int a = 0; a <= d->A; ++a) {
-    const int64_t o = adapter_offsets ? adapter_offsets[a] : (a == 0 ? 0 : d->T);
-    if (o < 0 || o > d->T) return MOE_LORA_ERR_DIMS;
-    if (a > 0 && o < at.tok_off[a - 1]) return MOE_LORA_ERR_DIMS;
-    if (a < d->A && d->A > 1 && o % 128) return MOE_LORA_ERR_DIMS;
-    at.tok_off[a] = (int)o;
-  }
-  if (at.tok_off[0] != 0 || at.tok_off[d->A] != d->T) return MOE_LORA_ERR_DIMS;
-  at.tok_tile[0] = 0;
-  for (int a = 0; a < d->A; ++a) at.tok_tile[a + 1] = at.tok_tile[a] + (at.tok_off[a + 1] - at.tok_off[a] + 127) / 128;
+  if ((rc = make_adapter_table(d, adapter_offsets, &at))) return rc;
   int sms;
   if ((rc = device_sms(&sms))) return rc;
   return launch_plan(d, topk_ids, at, plan_ws, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_LORA_OK
@@ -189,10 +177,13 @@ int moe_lora_backward(const moe_lora_dims* d, const void* plan_ws, const void* s
   return run_backward(d, plan_ws, saved, x, topk_w, dy, w, dx, dw, g, scratch, sms, s);
 }
 
-int moe_lora_router_forward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, int32_t* topk_ids,
-                            float* topk_w, float* logits, void* scratch, size_t scratch_bytes, void* stream) {
+int moe_lora_router_forward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr,
+                            const int64_t* adapter_offsets, int32_t* topk_ids, float* topk_w, float* logits,
+                            void* scratch, size_t scratch_bytes, void* stream) {
   int rc = check_router_dims(d);
   if (rc) return rc;
+  AdapterTable at;
+  if ((rc = make_adapter_table(d, adapter_offsets, &at))) return rc;
   if ((rc = check_ptr(scratch))) return rc;
   if (scratch_bytes < router_layout(d).total) return MOE_LORA_ERR_WORKSPACE;
   if ((rc = check_ptr(Wr))) return rc;
@@ -204,14 +195,17 @@ int moe_lora_router_forward(const moe_lora_dims* d, const uint16_t* x, const uin
   }
   int sms;
   if ((rc = device_sms(&sms))) return rc;
-  return run_router_forward(d, x, Wr, topk_ids, topk_w, logits, scratch, sms, static_cast<cudaStream_t>(stream));
+  return run_router_forward(d, at, x, Wr, topk_ids, topk_w, logits, scratch, sms, static_cast<cudaStream_t>(stream));
 }
 
-int moe_lora_router_backward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, const int32_t* topk_ids,
-                             const float* topk_w, const float* dw, float* dlogits, float* dWr, uint16_t* dx,
-                             void* scratch, size_t scratch_bytes, void* stream) {
+int moe_lora_router_backward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr,
+                             const int64_t* adapter_offsets, const int32_t* topk_ids, const float* topk_w,
+                             const float* dw, float* dlogits, float* dWr, uint16_t* dx, void* scratch,
+                             size_t scratch_bytes, void* stream) {
   int rc = check_router_dims(d);
   if (rc) return rc;
+  AdapterTable at;
+  if ((rc = make_adapter_table(d, adapter_offsets, &at))) return rc;
   if ((rc = check_ptr(scratch))) return rc;
   if (scratch_bytes < router_layout(d).total) return MOE_LORA_ERR_WORKSPACE;
   if ((rc = check_ptr(Wr)) || (rc = check_ptr(dWr))) return rc;
@@ -223,7 +217,7 @@ int moe_lora_router_backward(const moe_lora_dims* d, const uint16_t* x, const ui
   }
   int sms;
   if ((rc = device_sms(&sms))) return rc;
-  return run_router_backward(d, x, Wr, topk_ids, topk_w, dw, dlogits, dWr, dx, scratch, sms,
+  return run_router_backward(d, at, x, Wr, topk_ids, topk_w, dw, dlogits, dWr, dx, scratch, sms,
                              static_cast<cudaStream_t>(stream));
 }
 

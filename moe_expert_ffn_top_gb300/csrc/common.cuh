@@ -136,7 +136,7 @@ inline BwdLayout bwd_layout(const moe_lora_dims* d) {
 
 // Router scratch: error word; dl [T,E] bf16 (dense logit gradient, the tensor-core
 // operand of both router-backward contractions); fp32 partials of the token-split
-// dW_r reduction [kMaxSplit][E][H].
+// dW_r reduction [A][kMaxSplit][E][H].
 struct RouterLayout {
   size_t err, dl, part, total;
 };
@@ -147,17 +147,17 @@ inline RouterLayout router_layout(const moe_lora_dims* d) {
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.err = take(16);
   L.dl = take(2 * (size_t)T * d->E);
-  L.part = take(4 * (size_t)kMaxSplit * d->E * d->H);
+  L.part = take(4 * (size_t)d->A * kMaxSplit * d->E * d->H);
   L.total = o;
   return L;
 }
 
-// Extra size rules of the router: one adapter, 16 <= E <= 256 with E % 16 == 0 (the
-// whole logit row is one MMA tile N), k <= E.
+// Extra size rules of the router: 16 <= E <= 256 with E % 16 == 0 (the whole logit
+// row is one MMA tile N), k <= E.
 inline int check_router_dims(const moe_lora_dims* d) {
   const int rc = check_dims(d);
   if (rc) return rc;
-  if (d->A != 1 || d->E < 16 || d->E > 256 || d->E % 16) return MOE_LORA_ERR_UNSUPPORTED;
+  if (d->E < 16 || d->E > 256 || d->E % 16) return MOE_LORA_ERR_UNSUPPORTED;
   if (d->k > d->E) return MOE_LORA_ERR_DIMS;
   return MOE_LORA_OK;
 }

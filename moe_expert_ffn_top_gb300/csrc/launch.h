@@ -13,6 +13,27 @@ struct AdapterTable {
   int tok_tile[kMaxAdapters + 1];      // first 128-token tile of each adapter
 };
 
+// Adapter token ranges from the caller's host offsets [A+1] (NULL allowed when
+// A == 1): off[0] = 0, off[A] = T, non-decreasing, and every off[a] with a < A a
+// multiple of 128 when A > 1.  Returns MOE_LORA_OK or the rejection code.
+inline int make_adapter_table(const moe_lora_dims* d, const int64_t* adapter_offsets, AdapterTable* at) {
+  if (d->A > 1 && !adapter_offsets) return MOE_LORA_ERR_NULL;
+  *at = AdapterTable{};
+  at->n = d->A;
+  for (int a = 0; a <= d->A; ++a) {
+    const int64_t o = adapter_offsets ? adapter_offsets[a] : (a == 0 ? 0 : d->T);
+    if (o < 0 || o > d->T) return MOE_LORA_ERR_DIMS;
+    if (a > 0 && o < at->tok_off[a - 1]) return MOE_LORA_ERR_DIMS;
+    if (a < d->A && d->A > 1 && o % 128) return MOE_LORA_ERR_DIMS;
+    at->tok_off[a] = (int)o;
+  }
+  if (at->tok_off[0] != 0 || at->tok_off[d->A] != d->T) return MOE_LORA_ERR_DIMS;
+  at->tok_tile[0] = 0;
+  for (int a = 0; a < d->A; ++a)
+    at->tok_tile[a + 1] = at->tok_tile[a] + (at->tok_off[a + 1] - at->tok_off[a] + 127) / 128;
+  return MOE_LORA_OK;
+}
+
 cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const AdapterTable& at, void* ws,
                         cudaStream_t stream);
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/moe_lora.h"
+#include "launch.h"
 
 namespace moelora {
 
@@ -17,11 +18,11 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
 
 // Router step (router.cu): softmax top-k forward; logit gradient, grad-x update
 // and W_r gradient backward.
-int run_router_forward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, int32_t* ids, float* w,
-                       float* logits, void* scratch, int num_sms, cudaStream_t stream);
-int run_router_backward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, const int32_t* ids,
-                        const float* w, const float* dw, float* dlogits, float* dWr, uint16_t* dx, void* scratch,
-                        int num_sms, cudaStream_t stream);
+int run_router_forward(const moe_lora_dims* d, const AdapterTable& at, const uint16_t* x, const uint16_t* Wr,
+                       int32_t* ids, float* w, float* logits, void* scratch, int num_sms, cudaStream_t stream);
+int run_router_backward(const moe_lora_dims* d, const AdapterTable& at, const uint16_t* x, const uint16_t* Wr,
+                        const int32_t* ids, const float* w, const float* dw, float* dlogits, float* dWr, uint16_t* dx,
+                        void* scratch, int num_sms, cudaStream_t stream);
 
 // pair != 0: on the two-SM (cta_group::2) engine.
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,

@@ -64,19 +64,8 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
   if ((int64_t)G * (nchunks > 0 ? nchunks : 1) > kNoallocScratchInts) return MOE_LORA_ERR_SCRATCH_LIMIT;
   const PlanLayout L = plan_layout(d);
   if (plan_bytes < L.chunk_base) return MOE_LORA_ERR_WORKSPACE;  // the plan itself, without the histograms
-  if (d->A > 1 && !adapter_offsets) return MOE_LORA_ERR_NULL;
   AdapterTable at;
-  std::memset(&at, 0, sizeof(at));
-  at.n = d->A;
-  for (int a = 0; a <= d->A; ++a) {
-    const int64_t o = adapter_offsets ? adapter_offsets[a] : (a == 0 ? 0 : d->T);
-    if (o < 0 || o > d->T) return MOE_LORA_ERR_DIMS;
-    if (a > 0 && o < at.tok_off[a - 1]) return MOE_LORA_ERR_DIMS;
-    if (a < d->A && d->A > 1 && o % 128) return MOE_LORA_ERR_DIMS;
-    at.tok_off[a] = (int)o;
-  }
-  if (at.tok_off[0] != 0 || at.tok_off[d->A] != d->T) return MOE_LORA_ERR_DIMS;
-  for (int a = 0; a < d->A; ++a) at.tok_tile[a + 1] = at.tok_tile[a] + (at.tok_off[a + 1] - at.tok_off[a] + 127) / 128;
+  if ((rc = make_adapter_table(d, adapter_offsets, &at))) return rc;
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||

@@ -13,6 +13,12 @@
 //             (w_t is the softmax of the selected logits alone, so the full-softmax
 //             normaliser cancels); dx += dl W_r and dW_r = dl^T x on the tensor
 //             cores, the dense dl [T,E] as their bf16 operand.
+//
+// Several adapters (OpenPipe/ART PR #1139, Behavior: one router per adapter) own
+// contiguous token ranges starting at multiples of 128; adapter a's tokens use
+// W_r[a] and produce dW_r[a].  Every tile lies in one adapter's range, and the
+// token-split of each adapter's dW_r reduction depends on that adapter's token
+// count alone, so each adapter's results equal its standalone run bit for bit.
 #include <algorithm>
 
 #include "gemm_problems.cuh"
@@ -26,28 +32,37 @@ namespace moelora {
 // Router forward: logits of 128 tokens x E experts, softmax + top-k in the epilogue.
 // A: x K-major; B: W_r K-major (one box of E rows).
 // =====================================================================================
+// The 128-token tile t of an adapter table: rows [m0, min(m0+128, end of its adapter)).
+__device__ __forceinline__ TileInfo adapter_token_tile(const AdapterTable& at, int t) {
+  int a = 0;
+  while (a + 1 < at.n && t >= at.tok_tile[a + 1]) ++a;
+  TileInfo ti;
+  ti.g = a;
+  ti.m0 = at.tok_off[a] + (t - at.tok_tile[a]) * 128;
+  ti.mend = at.tok_off[a + 1] < ti.m0 + 128 ? at.tok_off[a + 1] : ti.m0 + 128;
+  ti.n0 = 0;
+  ti.sub = 0;
+  ti.k0 = 0;
+  ti.mh = 1;
+  return ti;
+}
+
 struct ProbRouter {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr int kEpiWarps = 4;  // one thread per token row, all E columns
   static constexpr bool kWide = false;
-  CUtensorMap mx, mWr;  // x (H,T) box(64,128); W_r (H,E) box(64,E)
+  CUtensorMap mx, mWr;  // x (H,T) box(64,128); W_r (H,E,A) box(64,E,1)
+  AdapterTable at;
   int* err;
   int32_t* ids;
   float* w;
   float* logits;  // [T,E] or nullptr
   int64_t T;
   int H, E, k;
-  __device__ int num_tiles() const { return (int)((T + 127) / 128); }
+  __device__ int num_tiles() const { return at.tok_tile[at.n]; }
   __device__ TileInfo tile(int t) const {
-    TileInfo ti;
-    ti.m0 = t * 128;
-    ti.mend = (int)(T < (int64_t)ti.m0 + 128 ? T : (int64_t)ti.m0 + 128);
-    ti.n0 = 0;
-    ti.g = 0;
-    ti.sub = 0;
+    TileInfo ti = adapter_token_tile(at, t);
     ti.nk = H / kBK;
-    ti.k0 = 0;
-    ti.mh = 1;
     return ti;
   }
   __device__ void prefetch() const {
@@ -57,15 +72,15 @@ struct ProbRouter {
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     mbar_arrive_expect_tx(bar, kAStage128 + E * 128);
     tma_load_2d(sa, &mx, bar, ks * kBK, ti.m0);
-    tma_load_2d(sb, &mWr, bar, ks * kBK, 0);
+    tma_load_3d(sb, &mWr, bar, ks * kBK, 0, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{E, 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int, int, uint32_t* stg) const {
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)ti.m0 + row;
     const int64_t t0 = t - lane;  // the warp's first token
-    const int nvalid = (int)(T - t0 < 32 ? T - t0 : 32);
-    const bool ok = t < T;
+    const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
+    const bool ok = t < ti.mend;
     // pass 1: row maximum (and the logits, if asked for)
     float mx = -INFINITY;
     for (int c = 0; c < E; c += 32) {
@@ -136,23 +151,18 @@ struct ProbRouterDx {
   static constexpr bool kAmn = false, kBmn = true;
   static constexpr int kEpiWarps = 8;  // load + store epilogue: two warps per lane quarter
   static constexpr bool kWide = false;
-  CUtensorMap mdl, mWr;  // dl (E,T) box(64,128); W_r (H,E) box(64,64)
+  CUtensorMap mdl, mWr;  // dl (E,T) box(64,128); W_r (H,E,A) box(64,64,1)
+  AdapterTable at;
   int* err;
   uint16_t* dx;
   int64_t T;
   int H, E;
   __device__ int ntn() const { return H / 256; }
-  __device__ int num_tiles() const { return (int)((T + 127) / 128) * ntn(); }
+  __device__ int num_tiles() const { return at.tok_tile[at.n] * ntn(); }
   __device__ TileInfo tile(int t) const {
-    TileInfo ti;
-    ti.m0 = t / ntn() * 128;
+    TileInfo ti = adapter_token_tile(at, t / ntn());
     ti.n0 = t % ntn() * 256;
-    ti.mend = (int)(T < (int64_t)ti.m0 + 128 ? T : (int64_t)ti.m0 + 128);
-    ti.g = 0;
-    ti.sub = 0;
     ti.nk = (E + kBK - 1) / kBK;
-    ti.k0 = 0;
-    ti.mh = 1;
     return ti;
   }
   __device__ void prefetch() const {
@@ -162,13 +172,13 @@ struct ProbRouterDx {
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     mbar_arrive_expect_tx(bar, kAStage128 + 4 * 8192);
     tma_load_2d(sa, &mdl, bar, ks * kBK, ti.m0);
-    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mWr, bar, ti.n0 + c * 64, ks * kBK);
+    for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mWr, bar, ti.n0 + c * 64, ks * kBK, ti.g);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int lane = threadIdx.x & 31;
     const int64_t t0 = (int64_t)ti.m0 + row - lane;  // the warp's first token
-    const int nvalid = (int)(T - t0 < 32 ? T - t0 : 32);
+    const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
     uint16_t* base = dx + t0 * H + ti.n0;
     for (int c = c0; c < 256; c += cs) {
       uint4 u[4];
@@ -190,8 +200,9 @@ struct ProbRouterDx {
 };
 
 // =====================================================================================
-// Router backward, weight part: dW_r = dl^T x  [E,H] fp32, K = tokens, split over
-// token slices (fp32 partials summed in slice order afterwards).
+// Router backward, weight part: dW_r[a] = dl^T x over adapter a's tokens  [E,H] fp32.
+// K = tokens; adapter a's token range is cut into split[a] slices of whole 64-token
+// steps (fp32 partials summed in slice order afterwards when split[a] > 1).
 // A: dl MN-major (experts contiguous); B: x MN-major.
 // =====================================================================================
 struct ProbRouterDW {
@@ -199,25 +210,30 @@ struct ProbRouterDW {
   static constexpr int kEpiWarps = 4;
   static constexpr bool kWide = false;
   CUtensorMap mdl, mx;  // dl (E,T) box(64,64); x (H,T) box(64,64)
+  AdapterTable at;
+  int split[kMaxAdapters];      // token slices of each adapter
+  int tbase[kMaxAdapters + 1];  // first tile of each adapter
   int* err;
-  float* out;  // dW_r, or the split partials
-  int64_t split_stride;
+  float* dWr;   // [A,E,H]
+  float* part;  // [A][kMaxSplit][E,H] partials
   int64_t T;
-  int H, E, split;
+  int H, E;
   __device__ int ntm() const { return (E + 127) / 128; }
   __device__ int ntn() const { return H / 256; }
-  __device__ int num_tiles() const { return split * ntm() * ntn(); }
+  __device__ int num_tiles() const { return tbase[at.n]; }
   __device__ TileInfo tile(int t) const {
-    const int per = ntm() * ntn();
-    const int sp = t / per, rem = t % per;
+    int a = 0;
+    while (a + 1 < at.n && t >= tbase[a + 1]) ++a;
+    const int per = ntm() * ntn(), u = t - tbase[a];
+    const int sp = u / per, rem = u % per;
     TileInfo ti;
     ti.m0 = rem / ntn() * 128;
     ti.n0 = rem % ntn() * 256;
     ti.mend = E;
-    ti.g = 0;
+    ti.g = a;
     ti.sub = sp;
-    const int nk = (int)((T + kBK - 1) / kBK), cs = (nk + split - 1) / split;
-    ti.k0 = sp * cs * kBK;
+    const int nk = (at.tok_off[a + 1] - at.tok_off[a] + kBK - 1) / kBK, cs = (nk + split[a] - 1) / split[a];
+    ti.k0 = at.tok_off[a] + sp * cs * kBK;
     ti.nk = max(0, min(cs, nk - sp * cs));
     ti.mh = 1;
     return ti;
@@ -234,26 +250,25 @@ struct ProbRouterDW {
     for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * 8192, &mx, bar, ti.n0 + c * 64, kt);
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ float* warp_rows(const TileInfo& ti, int row, int& nvalid) const {
-    const int m0 = ti.m0 + row - (threadIdx.x & 31);  // the warp's first expert row
-    nvalid = E - m0;
-    return out + ti.sub * split_stride + (int64_t)m0 * H + ti.n0;
+  // adapter a's output (split 1) or its slice's partial
+  __device__ float* out_of(const TileInfo& ti) const {
+    return split[ti.g] > 1 ? part + ((int64_t)ti.g * kMaxSplit + ti.sub) * E * H : dWr + (int64_t)ti.g * E * H;
   }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    int nvalid;
-    float* o0 = warp_rows(ti, row, nvalid);
+    const int m0 = ti.m0 + row - (threadIdx.x & 31);  // the warp's first expert row
+    float* o0 = out_of(ti) + (int64_t)m0 * H + ti.n0;
     for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      warp_store_rows_f32(o0 + c, H, nvalid, v, 1.0f, 32, stg);
+      warp_store_rows_f32(o0 + c, H, E - m0, v, 1.0f, 32, stg);
     }
   }
-  // a token slice with no K steps still owns its partial: zeros
+  // a token slice (or an adapter) with no K steps still owns its output: zeros
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     const int m = ti.m0 + row;
     if (m >= E) return;
     const float z[32] = {};
-    float* o = out + ti.sub * split_stride + (int64_t)m * H + ti.n0;
+    float* o = out_of(ti) + (int64_t)m * H + ti.n0;
     for (int c = c0; c < 256; c += cs) store_row_f32(o + c, z, 0.0f, 32);
   }
 };
@@ -310,15 +325,16 @@ __global__ void __launch_bounds__(256) router_dl_kernel(const int32_t* __restric
     if ((call) != cudaSuccess) return MOE_LORA_ERR_CUDA; \
   } while (0)
 
-int run_router_forward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, int32_t* ids, float* w,
-                       float* logits, void* scratch, int num_sms, cudaStream_t stream) {
+int run_router_forward(const moe_lora_dims* d, const AdapterTable& at, const uint16_t* x, const uint16_t* Wr,
+                       int32_t* ids, float* w, float* logits, void* scratch, int num_sms, cudaStream_t stream) {
   const RouterLayout L = router_layout(d);
   int* err = (int*)(static_cast<char*>(scratch) + L.err);
   LAUNCH(cudaMemsetAsync(err, 0, 16, stream));
   if (d->T == 0) return MOE_LORA_OK;
   ProbRouter p;
   MAP(tmap_2d(&p.mx, x, d->H, d->T, 64, 128));
-  MAP(tmap_2d(&p.mWr, Wr, d->H, d->E, 64, d->E));
+  MAP(tmap_3d(&p.mWr, Wr, d->H, d->E, d->A, 64, d->E));
+  p.at = at;
   p.err = err;
   p.ids = ids;
   p.w = w;
@@ -327,23 +343,30 @@ int run_router_forward(const moe_lora_dims* d, const uint16_t* x, const uint16_t
   p.H = d->H;
   p.E = d->E;
   p.k = d->k;
-  LAUNCH(launch_gemm(p, (int)((d->T + 127) / 128), num_sms, stream, K_ROUTER_FWD));
+  LAUNCH(launch_gemm(p, at.tok_tile[at.n], num_sms, stream, K_ROUTER_FWD));
   return MOE_LORA_OK;
 }
 
-int run_router_backward(const moe_lora_dims* d, const uint16_t* x, const uint16_t* Wr, const int32_t* ids,
-                        const float* w, const float* dw, float* dlogits, float* dWr, uint16_t* dx, void* scratch,
-                        int num_sms, cudaStream_t stream) {
+// Token slices of one adapter's dW_r reduction: at least 256 K steps (16,384 tokens)
+// each, at most kMaxSplit; a function of that adapter's token count alone.
+static int router_split(int64_t tokens) {
+  const int64_t nk = (tokens + 63) / 64;
+  return (int)std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, nk / 256));
+}
+
+int run_router_backward(const moe_lora_dims* d, const AdapterTable& at, const uint16_t* x, const uint16_t* Wr,
+                        const int32_t* ids, const float* w, const float* dw, float* dlogits, float* dWr, uint16_t* dx,
+                        void* scratch, int num_sms, cudaStream_t stream) {
   const RouterLayout L = router_layout(d);
   char* sc = static_cast<char*>(scratch);
   int* err = (int*)(sc + L.err);
   uint16_t* dl = (uint16_t*)(sc + L.dl);
   float* part = (float*)(sc + L.part);
   const int64_t T = d->T;
-  const int H = d->H, E = d->E;
+  const int H = d->H, E = d->E, A = d->A;
   LAUNCH(cudaMemsetAsync(err, 0, 16, stream));
   if (T == 0) {  // no tokens: dW_r = 0, nothing else to write
-    LAUNCH(cudaMemsetAsync(dWr, 0, sizeof(float) * (size_t)E * H, stream));
+    LAUNCH(cudaMemsetAsync(dWr, 0, sizeof(float) * (size_t)A * E * H, stream));
     return MOE_LORA_OK;
   }
   {
@@ -357,30 +380,38 @@ int run_router_backward(const moe_lora_dims* d, const uint16_t* x, const uint16_
   {
     ProbRouterDx p;
     MAP(tmap_2d(&p.mdl, dl, E, T, 64, 128));
-    MAP(tmap_2d(&p.mWr, Wr, H, E, 64, 64));
+    MAP(tmap_3d(&p.mWr, Wr, H, E, A, 64, 64));
+    p.at = at;
     p.err = err;
     p.dx = dx;
     p.T = T;
     p.H = H;
     p.E = E;
-    LAUNCH(launch_gemm(p, (int)((T + 127) / 128) * (H / 256), num_sms, stream, K_ROUTER_DX));
+    LAUNCH(launch_gemm(p, at.tok_tile[at.n] * (H / 256), num_sms, stream, K_ROUTER_DX));
   }
   {
-    // token slices of at least 256 K steps (16,384 tokens); fixed by the sizes alone
-    const int64_t nk = (T + 63) / 64;
-    const int split = (int)std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, nk / 256));
     ProbRouterDW p;
     MAP(tmap_2d(&p.mdl, dl, E, T, 64, 64));
     MAP(tmap_2d(&p.mx, x, H, T, 64, 64));
+    p.at = at;
+    const int per = ((E + 127) / 128) * (H / 256);
+    p.tbase[0] = 0;
+    for (int a = 0; a < A; ++a) {
+      p.split[a] = router_split(at.tok_off[a + 1] - at.tok_off[a]);
+      p.tbase[a + 1] = p.tbase[a] + p.split[a] * per;
+    }
     p.err = err;
-    p.split = split;
-    p.out = split > 1 ? part : dWr;
-    p.split_stride = (int64_t)E * H;
+    p.dWr = dWr;
+    p.part = part;
     p.T = T;
     p.H = H;
     p.E = E;
-    LAUNCH(launch_gemm(p, split * ((E + 127) / 128) * (H / 256), num_sms, stream, K_ROUTER_DW));
-    if (split > 1) LAUNCH(launch_reduce_splits(part, p.split_stride, split, p.split_stride, dWr, num_sms, stream));
+    LAUNCH(launch_gemm(p, p.tbase[A], num_sms, stream, K_ROUTER_DW));
+    const int64_t n = (int64_t)E * H;
+    for (int a = 0; a < A; ++a)
+      if (p.split[a] > 1)
+        LAUNCH(launch_reduce_splits(part + (int64_t)a * kMaxSplit * n, n, p.split[a], n, dWr + a * n, num_sms,
+                                    stream));
   }
   return MOE_LORA_OK;
 }

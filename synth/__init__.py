@@ -198,13 +198,14 @@ def make_inputs(shp: Shape, seed: int = 0, device: str = "cpu") -> Dict[str, tor
     return out
 
 
-def make_router_inputs(T: int, H: int, E: int, k: int, seed: int = 0, device: str = "cpu") -> Dict[str, torch.Tensor]:
-    """Inputs of the routing step: x [T,H] ~ N(0,1), W_r [E,H] ~ N(0, 1/H) (bf16 values);
-    the upstream routing-weight gradient dw [T,k] ~ N(0,1) fp32 and a grad-x the router
-    adds into, dx0 [T,H] ~ N(0,1) bf16."""
+def make_router_inputs(T: int, H: int, E: int, k: int, seed: int = 0, device: str = "cpu",
+                       A: int = 0) -> Dict[str, torch.Tensor]:
+    """Inputs of the routing step: x [T,H] ~ N(0,1), W_r [E,H] ~ N(0, 1/H) (bf16 values;
+    [A,E,H], one router per adapter, when A > 0); the upstream routing-weight gradient
+    dw [T,k] ~ N(0,1) fp32 and a grad-x the router adds into, dx0 [T,H] ~ N(0,1) bf16."""
     g = torch.Generator(device=device).manual_seed(seed)
     return {"x": _randn_bf16(g, (T, H), 1.0, device, 8192),
-            "Wr": _randn_bf16(g, (E, H), 1.0 / math.sqrt(H), device),
+            "Wr": _randn_bf16(g, (A, E, H) if A > 0 else (E, H), 1.0 / math.sqrt(H), device),
             "dw": _randn(g, (T, k), 1.0, device),
             "dx0": _randn_bf16(g, (T, H), 1.0, device, 8192)}
 

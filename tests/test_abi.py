@@ -118,25 +118,35 @@ def test_router_rejections(L):
     d = _dims()
     rb = m.moe_lora_workspace_bytes(d, m.MOE_LORA_WS_ROUTER_SCRATCH)
     assert rb >= 2 * 256 * 16
-    # the router needs one adapter and 16 <= E <= 256, E % 16 == 0
-    for bad in (dict(A=2), dict(E=8), dict(E=24), dict(E=272)):
+    # the router needs 16 <= E <= 256, E % 16 == 0
+    for bad in (dict(E=8), dict(E=24), dict(E=272)):
         db = _dims(**bad)
         assert m.moe_lora_workspace_bytes(db, m.MOE_LORA_WS_ROUTER_SCRATCH) == 0, bad
-        assert L.moe_lora_router_forward(ctypes.byref(db), FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None) == -5
+        assert L.moe_lora_router_forward(ctypes.byref(db), FAKE, FAKE, None, FAKE, FAKE, None, FAKE, 1 << 40,
+                                         None) == -5
     assert m.moe_lora_workspace_bytes(_dims(E=16, k=17), m.MOE_LORA_WS_ROUTER_SCRATCH) == 0
     dk = _dims(E=16, k=17)
-    assert L.moe_lora_router_forward(ctypes.byref(dk), FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None) == -2
+    assert L.moe_lora_router_forward(ctypes.byref(dk), FAKE, FAKE, None, FAKE, FAKE, None, FAKE, 1 << 40, None) == -2
     f = L.moe_lora_router_forward
-    assert f(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, None, FAKE, rb - 1, None) == -4
-    assert f(ctypes.byref(d), None, FAKE, FAKE, FAKE, None, FAKE, rb, None) == -1
-    assert f(ctypes.byref(d), FAKE, FAKE, FAKE + 4, FAKE, None, FAKE, rb, None) == -3
-    assert f(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE + 8, FAKE, rb, None) == -3
+    assert f(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, None, FAKE, rb - 1, None) == -4
+    assert f(ctypes.byref(d), None, FAKE, None, FAKE, FAKE, None, FAKE, rb, None) == -1
+    assert f(ctypes.byref(d), FAKE, FAKE, None, FAKE + 4, FAKE, None, FAKE, rb, None) == -3
+    assert f(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE + 8, FAKE, rb, None) == -3
     b = L.moe_lora_router_backward
-    assert b(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, rb - 1, None) == -4
-    assert b(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, rb, None) == -1
-    assert b(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE + 2, FAKE, rb, None) == -3
-    assert b(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, rb, None) == -1
+    assert b(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, rb - 1, None) == -4
+    assert b(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, rb, None) == -1
+    assert b(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, FAKE + 2, FAKE, rb, None) == -3
+    assert b(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, rb, None) == -1
     assert L.moe_lora_router_get_error(None, None) == -1
+    # several adapters (one router each): offsets required, with the plan's rules
+    da = _dims(A=2, T=300)
+    rba = m.moe_lora_workspace_bytes(da, m.MOE_LORA_WS_ROUTER_SCRATCH)
+    assert rba > rb
+    assert f(ctypes.byref(da), FAKE, FAKE, None, FAKE, FAKE, None, FAKE, rba, None) == -1
+    for offs in ([0, 100, 300], [0, 256, 200], [0, 128, 299], [1, 128, 300]):
+        o = (ctypes.c_int64 * 3)(*offs)
+        assert f(ctypes.byref(da), FAKE, FAKE, o, FAKE, FAKE, None, FAKE, rba, None) == -2, offs
+        assert b(ctypes.byref(da), FAKE, FAKE, o, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, rba, None) == -2, offs
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")

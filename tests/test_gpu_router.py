@@ -194,3 +194,64 @@ def test_router_deterministic():
         outs.append((ids.cpu(), w.cpu(), lg.cpu(), dWr.cpu(), dx.cpu()))
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+def _run_router(inp, T, H, E, k, A, offs, x, Wr, dw, dx0):
+    d = m.make_dims(T, H, 256, E, k, 16, A)
+    sc = m.router_scratch(d)
+    ids = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, k), float("nan"), device="cuda")
+    lg = torch.full((T, E), float("nan"), device="cuda")
+    m.moe_lora_router_forward(d, x, Wr, ids, w, lg, sc, adapter_offsets=offs)
+    dl = torch.full((T, E), float("nan"), device="cuda")
+    dWr = torch.full((A, E, H), float("nan"), device="cuda")
+    dx = dx0.clone()
+    m.moe_lora_router_backward(d, x, Wr, ids, w, dw, dl, dWr, dx, sc, adapter_offsets=offs)
+    torch.cuda.synchronize()
+    assert m.moe_lora_router_get_error(sc) == 0
+    return ids, w, lg, dl, dWr, dx
+
+
+@pytest.mark.parametrize("H,E,k,offs", [
+    (2048, 128, 8, [1024 * a for a in range(17)]),       # 16 adapters x 1,024 tokens (the multi-adapter pass)
+    (1024, 64, 4, [0, 256, 256, 896, 1000]),             # an empty adapter and a ragged last one
+    (1024, 64, 4, [0, 32768, 40000]),                    # adapter 0's dW_r is split over token slices
+])
+def test_router_multi_adapter_equals_standalone(H, E, k, offs):
+    """One router per adapter (OpenPipe/ART PR #1139, Behavior): the fused pass over
+    all adapters equals every adapter's standalone run bit for bit, and matches the
+    oracle's router with that adapter's W_r."""
+    A, T = len(offs) - 1, offs[-1]
+    inp = make_router_inputs(T, H, E, k, seed=31 + A, device="cuda", A=A)
+    ids, w, lg, dl, dWr, dx = _run_router(inp, T, H, E, k, A, offs, inp["x"], inp["Wr"], inp["dw"], inp["dx0"])
+    for a in range(A):
+        t0, t1 = offs[a], offs[a + 1]
+        if t1 == t0:
+            assert (dWr[a] == 0).all(), a
+            continue
+        s_ids, s_w, s_lg, s_dl, s_dWr, s_dx = _run_router(
+            inp, t1 - t0, H, E, k, 1, None, inp["x"][t0:t1].contiguous(), inp["Wr"][a].contiguous(),
+            inp["dw"][t0:t1].contiguous(), inp["dx0"][t0:t1].contiguous())
+        for name, fused, alone in (("ids", ids[t0:t1], s_ids), ("w", w[t0:t1], s_w), ("logits", lg[t0:t1], s_lg),
+                                   ("dlogits", dl[t0:t1], s_dl), ("dWr", dWr[a], s_dWr[0]),
+                                   ("dx", dx[t0:t1], s_dx)):
+            assert torch.equal(fused, alone), (a, name)
+    for a in (0, A - 1):  # the oracle, with each adapter's own router weights
+        t0, t1 = offs[a], min(offs[a + 1], offs[a] + 512)
+        if t1 == t0:
+            continue
+        xs = inp["x"][t0:t1].cpu()
+        l_ref, ids_ref, w_ref = oracle.router_forward(xs, inp["Wr"][a].cpu(), k, prec="f32")
+        assert rel_l2(lg[t0:t1], l_ref) <= 1e-5
+        _check_selection(ids[t0:t1], w[t0:t1], lg[t0:t1], l_ref, ids_ref, w_ref,
+                         1e-5 * float(l_ref.abs().max()) + 1e-6)
+        dl_ref, _, dx_ref = oracle.router_backward(xs, inp["Wr"][a].cpu(), ids[t0:t1].cpu(), inp["dw"][t0:t1].cpu(),
+                                                   prec="f32")
+        assert rel_l2(dl[t0:t1], dl_ref) <= 1e-4
+        assert_close("dx rows", dx[t0:t1], inp["dx0"][t0:t1].cpu().double() + dx_ref.double())
+    # dW_r[a] = dl^T x over adapter a's tokens, for the bf16 dlogits the kernels used
+    for a in range(A):
+        t0, t1 = offs[a], offs[a + 1]
+        if t1 > t0:
+            ref = dl[t0:t1].to(torch.bfloat16).double().t() @ inp["x"][t0:t1].double()
+            assert_close(f"dWr[{a}]", dWr[a], ref)

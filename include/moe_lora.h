@@ -279,6 +279,15 @@ MOE_LORA_API int moe_lora_gemm_selftest(int32_t M, int32_t N, int32_t K, const u
  * reporting as moe_lora_gemm_selftest. */
 MOE_LORA_API int moe_lora_gemm_pair_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
                                              const uint16_t* B, int32_t b_mn, float* C, void* stream);
+/* Error-path self-test of the bounded pipeline waits: the same plain GEMM (pair = 0:
+ * one-SM engine, 1: two-SM engine) with every operand copy withheld, as if a copy
+ * had been lost.  No wait in the engines is unbounded, so the kernel's waits give
+ * up (after about 2 s), set MOE_LORA_DEV_TIMEOUT in the self-test error word, and
+ * the kernel ends without writing C; the context stays usable.  Same argument
+ * rules as moe_lora_gemm_selftest; the check is the error word, not C. */
+MOE_LORA_API int moe_lora_gemm_starved_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
+                                                const uint16_t* B, int32_t b_mn, float* C, int32_t pair,
+                                                void* stream);
 /* Device error word of the self-test GEMMs (MOE_LORA_DEV_* bits); synchronises
  * the stream and clears the word. */
 MOE_LORA_API int moe_lora_gemm_selftest_error(void* stream);

@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_gemm_pair_selftest.restype = ctypes.c_int
         L.moe_lora_gemm_pair_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32,
                                                   P, ctypes.c_int32, P, P]
+        L.moe_lora_gemm_starved_selftest.restype = ctypes.c_int
+        L.moe_lora_gemm_starved_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P,
+                                                     ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_int32, P]
         L.moe_lora_profile_enable.restype = ctypes.c_int
         L.moe_lora_profile_enable.argtypes = [ctypes.c_int]
         L.moe_lora_profile_read.restype = ctypes.c_int
@@ -302,6 +305,18 @@ def moe_lora_gemm_pair_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor, b_
                                            _ptr(B, torch.bfloat16, "B"), int(b_mn), _ptr(C, torch.float32, "C"),
                                            _stream(stream))
     _check(rc, "moe_lora_gemm_pair_selftest")
+
+
+def moe_lora_gemm_starved_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor, b_mn: bool, C: torch.Tensor,
+                                   pair: bool, stream=None) -> None:
+    """The self-test GEMM with every operand copy withheld: its bounded waits must expire
+    and set MOE_LORA_DEV_TIMEOUT (read with moe_lora_gemm_selftest_error)."""
+    M, N = C.shape
+    K = A.shape[0] if a_mn else A.shape[1]
+    rc = lib().moe_lora_gemm_starved_selftest(M, N, K, _ptr(A, torch.bfloat16, "A"), int(a_mn),
+                                              _ptr(B, torch.bfloat16, "B"), int(b_mn), _ptr(C, torch.float32, "C"),
+                                              int(pair), _stream(stream))
+    _check(rc, "moe_lora_gemm_starved_selftest")
 
 
 def moe_lora_gemm_selftest_error(stream=None) -> int:

@@ -290,7 +290,7 @@ const char* moe_lora_strerror(int code) {
 static __device__ int g_selftest_err;
 
 static int selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn, const uint16_t* B,
-                    int32_t b_mn, float* C, int pair, void* stream) {
+                    int32_t b_mn, float* C, int pair, int starve, void* stream) {
   if (M <= 0 || M % 128 || K <= 0 || K % 64 || N <= 0) return MOE_LORA_ERR_DIMS;
   if (!(N % 256 == 0 || (N <= 256 && N % 16 == 0))) return MOE_LORA_ERR_DIMS;
   int rc;
@@ -299,17 +299,23 @@ static int selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t 
   if ((rc = device_sms(&sms))) return rc;
   int* err = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_selftest_err) != cudaSuccess) return MOE_LORA_ERR_CUDA;
-  return run_plain_gemm(M, N, K, A, a_mn, B, b_mn, C, err, sms, pair, static_cast<cudaStream_t>(stream));
+  return run_plain_gemm(M, N, K, A, a_mn, B, b_mn, C, err, sms, pair, starve, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_lora_gemm_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
                                       const uint16_t* B, int32_t b_mn, float* C, void* stream) {
-  return selftest(M, N, K, A, a_mn, B, b_mn, C, 0, stream);
+  return selftest(M, N, K, A, a_mn, B, b_mn, C, 0, 0, stream);
 }
 
 extern "C" int moe_lora_gemm_pair_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
                                            const uint16_t* B, int32_t b_mn, float* C, void* stream) {
-  return selftest(M, N, K, A, a_mn, B, b_mn, C, 1, stream);
+  return selftest(M, N, K, A, a_mn, B, b_mn, C, 1, 0, stream);
+}
+
+extern "C" int moe_lora_gemm_starved_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
+                                              const uint16_t* B, int32_t b_mn, float* C, int32_t pair,
+                                              void* stream) {
+  return selftest(M, N, K, A, a_mn, B, b_mn, C, pair ? 1 : 0, 1, stream);
 }
 
 extern "C" int moe_lora_gemm_selftest_error(void* stream) {

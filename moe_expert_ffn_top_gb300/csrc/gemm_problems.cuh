@@ -1117,6 +1117,7 @@ struct ProbPlain {
   int* err;
   float* C;
   int M, N, K;
+  int starve;  // 1: issue no operand copy (the bounded waits must expire; error-path self-test)
   __device__ int tn() const { return N < 256 ? N : 256; }
   __device__ int ntn() const { return (N + 255) / 256; }
   __device__ int num_tiles() const { return M / 128 * ntn(); }
@@ -1136,6 +1137,7 @@ struct ProbPlain {
     tma_prefetch_map(&mB);
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    if (starve) return;
     const int kt = ks * kBK;
     const int nbox = (tn() + 63) / 64;
     mbar_arrive_expect_tx(bar, kAStage128 + (BMN ? nbox * 8192 : tn() * 128));
@@ -1191,6 +1193,7 @@ struct ProbPlainPair : ProbPlain<AMN, BMN> {
     return (uint32_t)(ti.mh * kAStage128 + 2 * (BMN ? nbox() * 8192 : half_n() * 128));
   }
   __device__ void load_pair(const TileInfo& ti, int ks, int rank, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
+    if (this->starve) return;
     const int kt = ks * kBK, mrow = ti.m0 + rank * 128, nc = ti.n0 + rank * half_n();
     if (rank < ti.mh) {
       if (AMN) {

@@ -24,8 +24,9 @@ int run_router_backward(const moe_lora_dims* d, const AdapterTable& at, const ui
                         const int32_t* ids, const float* w, const float* dw, float* dlogits, float* dWr, uint16_t* dx,
                         void* scratch, int num_sms, cudaStream_t stream);
 
-// pair != 0: on the two-SM (cta_group::2) engine.
+// pair != 0: on the two-SM (cta_group::2) engine; starve != 0: no operand copy is
+// issued, so the pipeline's bounded waits expire (error-path self-test).
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,
-                   int* err, int num_sms, int pair, cudaStream_t stream);
+                   int* err, int num_sms, int pair, int starve, cudaStream_t stream);
 
 }  // namespace moelora

@@ -25,7 +25,7 @@ static int plain_maps(Prob& p, int M, int N, int K, const uint16_t* A, const uin
 
 template <bool AMN, bool BMN>
 static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, float* C, int* err, int num_sms,
-                 bool pair, cudaStream_t stream) {
+                 bool pair, int starve, cudaStream_t stream) {
   const uint32_t tn = N < 256 ? (uint32_t)N : 256u;
   const int ntn = (N + 255) / 256;
   int rc;
@@ -37,6 +37,7 @@ static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, floa
     p.M = M;
     p.N = N;
     p.K = K;
+    p.starve = starve;
     return launch_gemm_pair(p, (M + 255) / 256 * ntn, num_sms, stream, K_SELFTEST) == cudaSuccess
                ? MOE_LORA_OK
                : MOE_LORA_ERR_CUDA;
@@ -48,17 +49,18 @@ static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, floa
   p.M = M;
   p.N = N;
   p.K = K;
+  p.starve = starve;
   return launch_gemm(p, M / 128 * ntn, num_sms, stream, K_SELFTEST) == cudaSuccess ? MOE_LORA_OK
                                                                                   : MOE_LORA_ERR_CUDA;
 }
 
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,
-                   int* err, int num_sms, int pair, cudaStream_t stream) {
+                   int* err, int num_sms, int pair, int starve, cudaStream_t stream) {
   const bool pr = pair != 0;
-  if (a_mn && b_mn) return plain<true, true>(M, N, K, A, B, C, err, num_sms, pr, stream);
-  if (a_mn) return plain<true, false>(M, N, K, A, B, C, err, num_sms, pr, stream);
-  if (b_mn) return plain<false, true>(M, N, K, A, B, C, err, num_sms, pr, stream);
-  return plain<false, false>(M, N, K, A, B, C, err, num_sms, pr, stream);
+  if (a_mn && b_mn) return plain<true, true>(M, N, K, A, B, C, err, num_sms, pr, starve, stream);
+  if (a_mn) return plain<true, false>(M, N, K, A, B, C, err, num_sms, pr, starve, stream);
+  if (b_mn) return plain<false, true>(M, N, K, A, B, C, err, num_sms, pr, starve, stream);
+  return plain<false, false>(M, N, K, A, B, C, err, num_sms, pr, starve, stream);
 }
 
 }  // namespace moelora

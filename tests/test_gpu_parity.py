@@ -63,6 +63,29 @@ def test_engine_gemm_pair(a_mn, b_mn, M, N, K):
     assert rel_l2(C, ref) < 1e-5
 
 
+@pytest.mark.parametrize("pair", [False, True])
+def test_engine_wait_timeout_reports_and_recovers(pair):
+    """Failure detection without a GPU fault: with every operand copy withheld (as if
+    a copy were lost) the engine's bounded waits expire, the kernel ends with
+    MOE_LORA_DEV_TIMEOUT in the error word the host reads, and the context stays
+    usable for the next launch."""
+    M, N, K = (256, 256, 128) if pair else (128, 256, 128)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    A = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    assert m.moe_lora_gemm_selftest_error() == 0
+    m.moe_lora_gemm_starved_selftest(A, False, B, False, C, pair)
+    torch.cuda.synchronize()
+    assert m.moe_lora_gemm_selftest_error() & m.MOE_LORA_DEV_TIMEOUT
+    assert torch.isnan(C).all()  # the epilogue never ran
+    run = m.moe_lora_gemm_pair_selftest if pair else m.moe_lora_gemm_selftest
+    run(A, False, B, False, C)
+    torch.cuda.synchronize()
+    assert m.moe_lora_gemm_selftest_error() == 0
+    assert rel_l2(C, A.double() @ B.double().t()) < 1e-5
+
+
 # ----------------------------------------------------------------------------- plan
 def _plan_check(ids_cpu, E, shp, offs=None, BM=128):
     d = m.make_dims(shp.T, shp.H, shp.I, E, shp.k, shp.r, shp.A)

@@ -121,6 +121,21 @@ def traffic_for(kernel):
     return e.get("bytes_per_launch")
 
 
+# ------------------------------------------------------------------ multi-rank timing
+def max_over_ranks(dist, v, device):
+    """The slowest rank's value (every rank gets it); v itself on a single process."""
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_rank, ms):
+    """Whole-job throughput: the units every rank processed over the max-over-ranks time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -250,13 +265,6 @@ def run_ours(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     args_dev = (inp["x"], inp["topk_ids"], inp["topk_w"], inp["dy"])
     for _ in range(args.warmup):
         step(*args_dev)
@@ -278,9 +286,9 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     clk = clocks.stop()
     launches = m.moe_lora_launch_count(reset=True)
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, "cuda")
     flops = step_flops(T, R, H, I, r)
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(world, flops, ms)
 
     # ---- per-kernel event timing (a separate, identical pass)
     m.moe_lora_profile_enable(True)
@@ -411,8 +419,8 @@ def run_ours(args, rank, world, local_rank):
     s1.record(down)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = max_over_ranks(s0.elapsed_time(s1) / args.steps)
-    e2e = {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    ms_e2e = max_over_ranks(dist, s0.elapsed_time(s1) / args.steps, "cuda")
+    e2e = {"value": round(job_tflops(world, flops, ms_e2e), 2), "unit": "TFLOP/s",
            "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
            "copies": "pinned host memory, own streams, overlapped with neighbouring steps' compute"}
 

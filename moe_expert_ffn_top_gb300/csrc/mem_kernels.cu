@@ -167,18 +167,44 @@ __global__ void dw_kernel(PlanView pl, const float* __restrict__ part, int npart
 }
 
 __global__ void dy13w_kernel(PlanView pl, const float* __restrict__ dY13, uint16_t* __restrict__ dY13w, int r2) {
+  // one warp per token; lane l sums columns [8l, 8l+8) (+256 per pass; r2 % 16 == 0)
+  // with 16-byte loads, up to 8 routes' loads in flight before they are added in
+  // slot order
+  constexpr int kGroup = 8;
   const int lane = threadIdx.x & 31;
   const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int k = pl.k;
   for (int64_t t = w0; t < pl.T; t += nw) {
-    for (int q = lane; q < r2; q += 32) {
-      float acc = 0.0f;
-      for (int j = 0; j < pl.k; ++j) {
-        const int R = pl.row_of_route[t * pl.k + j];
-        if (R >= 0) acc += dY13[(int64_t)R * r2 + q];
+    const int R = lane < k ? pl.row_of_route[t * k + lane] : -1;
+    for (int c0 = 0; c0 < r2; c0 += 256) {  // warp-uniform loop: every lane takes part in the shuffles
+      const int c = c0 + lane * 8;
+      const bool on = c < r2;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j0 = 0; j0 < k; j0 += kGroup) {
+        float4 v[kGroup][2];
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {
+          const int Rj = __shfl_sync(0xffffffffu, R, (j0 + j) & 31);
+          const bool live = on && j0 + j < k && Rj >= 0;
+          const float4* p = reinterpret_cast<const float4*>(dY13 + (int64_t)(live ? Rj : 0) * r2 + c);
+          v[j][0] = live ? p[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[j][1] = live ? p[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {
+          if (j0 + j >= k || __shfl_sync(0xffffffffu, R, (j0 + j) & 31) < 0) continue;
+          acc[0] += v[j][0].x;
+          acc[1] += v[j][0].y;
+          acc[2] += v[j][0].z;
+          acc[3] += v[j][0].w;
+          acc[4] += v[j][1].x;
+          acc[5] += v[j][1].y;
+          acc[6] += v[j][1].z;
+          acc[7] += v[j][1].w;
+        }
       }
-      __nv_bfloat16 h = __float2bfloat16_rn(acc);
-      dY13w[t * r2 + q] = *reinterpret_cast<uint16_t*>(&h);
+      if (on) st_bf16x8(dY13w + t * r2 + c, acc);
     }
   }
 }

@@ -449,7 +449,7 @@ struct ProbW2 {
 // =====================================================================================
 struct ProbB2Expand {
   static constexpr bool kAmn = false, kBmn = false;
-  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiWarps = 8;  // store-bound epilogue: two warps per lane quarter keep more stores in flight
   static constexpr bool kWide = false;
   CUtensorMap mZ2w, mB2;  // Z2w (r,T) box(64,128); B2 (r,H,A) box(64,256,1)
   PlanView pl;
@@ -911,7 +911,7 @@ struct ProbDB13 {
 // =====================================================================================
 struct ProbA13Expand {
   static constexpr bool kAmn = false, kBmn = true;
-  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiWarps = 8;  // store-bound epilogue: two warps per lane quarter keep more stores in flight
   static constexpr bool kWide = false;
   CUtensorMap mdY13w, mA1, mA3;  // dY13w (2r,T) box(64,128); A1/A3 (H,r,A) box(64,64,1)
   PlanView pl;

@@ -412,6 +412,8 @@ def run_ours(args, rank, world, local_rank):
     run_e2e(2)
     torch.cuda.synchronize()
     barrier()
+    e2e_clocks = ClockSampler(local_rank)
+    e2e_clocks.start()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record(up)
     run_e2e(args.steps)
@@ -419,9 +421,11 @@ def run_ours(args, rank, world, local_rank):
     s1.record(down)
     torch.cuda.synchronize()
     barrier()
+    e2e_clk = e2e_clocks.stop()
     ms_e2e = max_over_ranks(dist, s0.elapsed_time(s1) / args.steps, "cuda")
     e2e = {"value": round(job_tflops(world, flops, ms_e2e), 2), "unit": "TFLOP/s",
            "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+           "clocks": e2e_clk,
            "copies": "pinned host memory, own streams, overlapped with neighbouring steps' compute"}
 
     # ---- CPU oracle baseline (rank 0, single GPU only)

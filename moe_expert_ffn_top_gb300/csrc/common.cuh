@@ -45,7 +45,7 @@ inline int64_t plan_chunks(const moe_lora_dims* d) {
 
 // ------------------------------------------------------------------ layouts
 struct PlanLayout {
-  size_t err, counts, offsets, row_of_route, route_of_row, tile_group, tok_off, tok_tile, wtile_off, wtile,
+  size_t err, counts, offsets, row_of_route, route_of_row, tile_group, tile_span, tok_off, tok_tile, wtile_off, wtile,
       chunk_base, total;
 };
 inline PlanLayout plan_layout(const moe_lora_dims* d) {
@@ -59,10 +59,11 @@ inline PlanLayout plan_layout(const moe_lora_dims* d) {
   L.row_of_route = take(sizeof(int32_t) * (TK > 0 ? TK : 1));
   L.route_of_row = take(sizeof(int32_t) * P);
   L.tile_group = take(sizeof(int32_t) * (P / kBlockM + 1));
+  L.tile_span = take(2 * sizeof(int32_t) * (P / kBlockM + 1));
   L.tok_off = take(sizeof(int32_t) * (kMaxAdapters + 1));
   L.tok_tile = take(sizeof(int32_t) * (kMaxAdapters + 1));
   L.wtile_off = take(sizeof(int32_t) * (G + 1));
-  L.wtile = take(2 * sizeof(int32_t) * (P / kBlockM + 1));
+  L.wtile = take(4 * sizeof(int32_t) * (P / kBlockM + 1));
   L.chunk_base = take(sizeof(int32_t) * G * (plan_chunks(d) > 0 ? plan_chunks(d) : 1));
   L.total = o;
   return L;
@@ -170,10 +171,12 @@ struct PlanView {
   const int* row_of_route;   // [T*k] padded row of route t*k+j, or -1
   const int* route_of_row;   // [P] route of a row, or -1 for padding
   const int* tile_group;     // [P/128] group of each 128-row tile
+  const int2* tile_span;     // [P/128] (first 128-row tile, number of 128-row tiles) of that tile's group
   const int* tok_off;        // [A+1] first token of each adapter
   const int* tok_tile;       // [A+1] first 128-token tile of each adapter
   const int* wtile_off;      // [G+1] first 256-row tile of each group
-  const int2* wtile;         // 256-row tiles: x = (first 128-row tile index << 1) | (halves - 1), y = group
+  const int4* wtile;         // 256-row tiles: x = (first 128-row tile << 1) | (halves - 1), y = group,
+                             // z = first 256-row tile of the group, w = the group's number of 256-row tiles
   int64_t T;
   int G, E, A, k;
 };
@@ -188,10 +191,11 @@ inline PlanView make_plan_view(const moe_lora_dims* d, const void* ws) {
   v.row_of_route = (const int*)(b + L.row_of_route);
   v.route_of_row = (const int*)(b + L.route_of_row);
   v.tile_group = (const int*)(b + L.tile_group);
+  v.tile_span = (const int2*)(b + L.tile_span);
   v.tok_off = (const int*)(b + L.tok_off);
   v.tok_tile = (const int*)(b + L.tok_tile);
   v.wtile_off = (const int*)(b + L.wtile_off);
-  v.wtile = (const int2*)(b + L.wtile);
+  v.wtile = (const int4*)(b + L.wtile);
   v.T = d->T;
   v.G = d->A * d->E;
   v.E = d->E;

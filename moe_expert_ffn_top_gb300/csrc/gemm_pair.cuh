@@ -26,11 +26,12 @@
 //   static constexpr bool kAmn, kBmn;  static constexpr int kEpiWarps;
 //   int* err;
 //   int      num_tiles() const;                    256-row tiles
-//   int2     tile_fetch(int t) const;              the tile's plan entry (global loads only)
-//   TileInfo tile_at(int t, int2 w) const;         decode (no memory access): m0 = first row of
-//                                                  the 256-row tile, mh = halves; nk, sub and n0
-//                                                  depend on t alone
+//   int4     tile_fetch(int t) const;              the tile's plan entry (global loads only)
+//   TileInfo tile_at(int t, int4 w) const;         decode (no memory access): m0 = first row of
+//                                                  the 256-row tile, mh = halves
 //   TileInfo tile(int t) const;                    tile_at(t, tile_fetch(t))
+//   static constexpr bool kIssuerNeedsTile;        false: nk and the MMA steps do not depend on
+//                                                  the entry, and the issuer decodes with zeros
 //   void     prefetch() const;
 //   uint32_t tx_bytes(const TileInfo&, int ks) const;   bytes BOTH CTAs load at step ks
 //   void     load_pair(const TileInfo&, int ks, int rank, uint8_t* sA, uint8_t* sB, uint32_t cbar) const;
@@ -92,12 +93,14 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(co
       uint32_t ph = 0;
       bool ok = true;
       uint32_t issued = 0, last_ph = 0;  // leader: stages armed, and the parity of their last use
-      // The next tile's plan entry is loaded a whole tile ahead, so no tile start
-      // waits on a global load.
-      int2 w = pair < ntiles ? p.tile_fetch(pair) : make_int2(0, 0);
+      // The next tile's plan entry is loaded at K step 2 of the current tile, when the
+      // stage ring is already full, so no tile start waits on a global load.
+      int4 w = pair < ntiles ? p.tile_fetch(pair) : make_int4(0, 0, 0, 0);
       for (int t = pair; t < ntiles && ok; t += npairs) {
         const TileInfo ti = p.tile_at(t, w);
-        if (t + npairs < ntiles) w = p.tile_fetch(t + npairs);
+        const bool more = t + npairs < ntiles;
+        const int fks = ti.nk > 2 ? 2 : ti.nk - 1;
+        if (ti.nk == 0 && more) w = p.tile_fetch(t + npairs);
         for (int ks = 0; ks < ti.nk; ++ks) {
           if (!mbar_wait(&empty[s], ph ^ 1u, err)) {
             ok = false;
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(co
           }
           uint8_t* sa = smem + s * kPairStage;
           p.load_pair(ti, ks, (int)rank, sa, sa + kPairAStage, mapa_shared(smem_u32(&full[s]), 0));
+          if (ks == fks && more) w = p.tile_fetch(t + npairs);
           if (++s == kPairStages) {
             s = 0;
             ph ^= 1u;
@@ -128,9 +132,15 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(co
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
+      int4 w = P::kIssuerNeedsTile && pair < ntiles ? p.tile_fetch(pair) : make_int4(0, 0, 0, 0);
       for (int t = pair; t < ntiles && ok; t += npairs) {
-        const TileInfo ti = p.tile_at(t, make_int2(0, 0));  // the issuer needs only nk and the steps
-        if (ti.nk == 0) continue;
+        const TileInfo ti = p.tile_at(t, w);
+        const bool more = P::kIssuerNeedsTile && t + npairs < ntiles;
+        const int fks = ti.nk > 2 ? 2 : ti.nk - 1;
+        if (ti.nk == 0) {
+          if (more) w = p.tile_fetch(t + npairs);
+          continue;
+        }
         if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, err)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
@@ -151,6 +161,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(co
             mma_bf16_pair(d + (uint32_t)st.col, ad, bd, idesc, (st.first && kk == 0) ? 0u : 1u);
           }
           mma_commit_pair_both(&empty[s]);
+          if (ks == fks && more) w = p.tile_fetch(t + npairs);
           if (++s == kPairStages) {
             s = 0;
             ph ^= 1u;

@@ -28,7 +28,7 @@ __device__ __forceinline__ int adapter_of_tile(const PlanView& pl, int t) {
 
 // 256-row tile of an M-grouped problem from its plan entry w: rows
 // [m0, m0 + 128*mh) of plan group w.y (mh = 2, or 1 for a group's odd last tile).
-__device__ __forceinline__ void wide_tile_from(int2 w, TileInfo& ti) {
+__device__ __forceinline__ void wide_tile_from(int4 w, TileInfo& ti) {
   const int mt = w.x >> 1;
   ti.mh = (w.x & 1) + 1;
   ti.m0 = mt * 128;
@@ -36,12 +36,8 @@ __device__ __forceinline__ void wide_tile_from(int2 w, TileInfo& ti) {
   ti.g = w.y;
   ti.k0 = 0;
 }
-// 256-row tile t of an M-grouped problem with ntn column tiles.
-__device__ __forceinline__ void wide_tile(const PlanView& pl, int t, int ntn, TileInfo& ti) {
-  wide_tile_from(pl.wtile[t / ntn], ti);
-}
 
-// 128-row tile t of an M-grouped problem with ntn column tiles.
+// 128-row tile t of an M-grouped problem with ntn column tiles (row-tile-major).
 __device__ __forceinline__ void narrow_tile(const PlanView& pl, int t, int ntn, TileInfo& ti) {
   const int mt = t / ntn;
   ti.mh = 1;
@@ -49,6 +45,44 @@ __device__ __forceinline__ void narrow_tile(const PlanView& pl, int t, int ntn, 
   ti.mend = ti.m0 + 128;
   ti.g = pl.tile_group[mt];
   ti.k0 = 0;
+}
+
+// Column-tile-major order inside each group: the base expert GEMMs walk all of a
+// group's row tiles for one column tile before the next column tile, so the CTAs
+// running at the same time share one block of expert weights (read once from DRAM)
+// rather than one block of routed rows.  A group's tiles are still the contiguous
+// range [first*ntn, (first+count)*ntn) of tile indices, so t / ntn names a row tile
+// of the right group.
+//
+// 128-row tiles: the plan entry of tile t (loads only: group, first row tile and
+// row-tile count of the group) ...
+__device__ __forceinline__ int4 nmajor_narrow_fetch(const PlanView& pl, int t, int ntn) {
+  const int l = t / ntn;
+  const int2 sp = pl.tile_span[l];
+  return make_int4(pl.tile_group[l], sp.x, sp.y, 0);
+}
+// ... and its decode (no memory access); returns the column tile.
+__device__ __forceinline__ int nmajor_narrow_decode(int4 e, int t, int ntn, TileInfo& ti) {
+  const int u = t - e.y * ntn;
+  ti.g = e.x;
+  ti.m0 = (e.y + u % e.z) * 128;
+  ti.mend = ti.m0 + 128;
+  ti.mh = 1;
+  ti.k0 = 0;
+  return u / e.z;
+}
+// 256-row tiles: the entry of tile t (two dependent loads: any 256-row tile of the
+// group gives the group's first tile and count, then the tile itself; z = column tile) ...
+__device__ __forceinline__ int4 nmajor_wide_fetch(const PlanView& pl, int t, int ntn) {
+  const int4 a = pl.wtile[t / ntn];
+  const int u = t - a.z * ntn;
+  const int4 w = pl.wtile[a.z + u % a.w];
+  return make_int4(w.x, w.y, u / a.w, 0);
+}
+// Decode of a 256-row tile entry (x, y as in the plan, z = column tile); returns the column tile.
+__device__ __forceinline__ int wide_entry_decode(int4 e, TileInfo& ti) {
+  wide_tile_from(e, ti);
+  return e.z;
 }
 
 // A-operand rows of a wide tile: one 128-row box per half present.
@@ -323,10 +357,9 @@ struct ProbW13 {
   __device__ int ntn() const { return I / 128; }
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
-  __device__ TileInfo tile(int t) const {
+  __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
-    narrow_tile(pl, t, ntn(), ti);
-    ti.n0 = t % ntn() * 128;
+    ti.n0 = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti) * 128;
     ti.sub = 0;
     ti.nk = H / kBK + 2 * nkr();
     return ti;
@@ -776,10 +809,9 @@ struct ProbW13Dgrad {
   float s;
   __device__ int ntn() const { return H / 256 + 1; }
   __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
-  __device__ TileInfo tile(int t) const {
-    const int nt = t % ntn();
+  __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
-    wide_tile(pl, t, ntn(), ti);
+    const int nt = wide_entry_decode(nmajor_wide_fetch(pl, t, ntn()), ti);
     ti.sub = nt == H / 256;
     ti.n0 = ti.sub ? 0 : nt * 256;
     ti.nk = 2 * (I / kBK);
@@ -1042,12 +1074,16 @@ struct ProbDA13 {
 struct ProbW2Pair : ProbW2 {
   CUtensorMap mW2h, mA2h;  // W2 (I,H,E) box(64,128,1); A2 (I,r,G) box(64,round32(r)/2,1),
                            // in place of the one-SM mW2/mA2
+  static constexpr bool kIssuerNeedsTile = true;  // the A2 tile has its own MMA N
   __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
-  __device__ int2 tile_fetch(int t) const { return pl.wtile[t / ntn()]; }
-  __device__ TileInfo tile_at(int t, int2 w) const {
-    const int nt = t % ntn();
+  // row-tile-major: the column-tile-major order measured no faster on the two-SM engine
+  __device__ int4 tile_fetch(int t) const {
+    const int4 w = pl.wtile[t / ntn()];
+    return make_int4(w.x, w.y, t % ntn(), 0);
+  }
+  __device__ TileInfo tile_at(int, int4 w) const {
     TileInfo ti;
-    wide_tile_from(w, ti);
+    const int nt = wide_entry_decode(w, ti);
     ti.sub = nt == H / 256;
     ti.n0 = ti.sub ? 0 : nt * 256;
     ti.nk = I / kBK;
@@ -1076,12 +1112,16 @@ struct ProbW2Pair : ProbW2 {
 
 // B3/B4: the 256 columns of I are two 64-wide MN-major boxes per CTA.
 struct ProbW2DgradPair : ProbW2Dgrad {
+  static constexpr bool kIssuerNeedsTile = false;  // every tile: N = 256, same K steps
   __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
-  __device__ int2 tile_fetch(int t) const { return pl.wtile[t / ntn()]; }
-  __device__ TileInfo tile_at(int t, int2 w) const {
-    const int nt = t % ntn();
+  // row-tile-major: the column-tile-major order measured no faster on the two-SM engine
+  __device__ int4 tile_fetch(int t) const {
+    const int4 w = pl.wtile[t / ntn()];
+    return make_int4(w.x, w.y, t % ntn(), 0);
+  }
+  __device__ TileInfo tile_at(int, int4 w) const {
     TileInfo ti;
-    wide_tile_from(w, ti);
+    const int nt = wide_entry_decode(w, ti);
     ti.n0 = nt * 256;
     ti.sub = nt;
     ti.nk = H / kBK + nkr();
@@ -1173,8 +1213,9 @@ struct ProbPlainPair : ProbPlain<AMN, BMN> {
   using Base = ProbPlain<AMN, BMN>;
   // B maps: K-major box(64, tn/2); MN-major box(64,64) as in the one-SM form.
   __device__ int num_tiles() const { return (this->M + 255) / 256 * this->ntn(); }
-  __device__ int2 tile_fetch(int) const { return make_int2(0, 0); }
-  __device__ TileInfo tile_at(int t, int2) const { return tile(t); }
+  static constexpr bool kIssuerNeedsTile = false;
+  __device__ int4 tile_fetch(int) const { return make_int4(0, 0, 0, 0); }
+  __device__ TileInfo tile_at(int t, int4) const { return tile(t); }
   __device__ TileInfo tile(int t) const {
     TileInfo ti;
     ti.m0 = t / this->ntn() * 256;

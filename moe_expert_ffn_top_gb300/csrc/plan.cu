@@ -132,12 +132,17 @@ __global__ void plan_scatter(const int* __restrict__ ids, int64_t TK, int k, int
 
 // padding rows -> -1; tile -> group; adapter tables into the workspace.
 __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __restrict__ offsets,
-                            int* __restrict__ route_of_row, int* __restrict__ tile_group, AdapterTable at,
-                            int* __restrict__ tok_off, int* __restrict__ tok_tile) {
+                            int* __restrict__ route_of_row, int* __restrict__ tile_group,
+                            int2* __restrict__ tile_span, AdapterTable at, int* __restrict__ tok_off,
+                            int* __restrict__ tok_tile) {
   for (int g = blockIdx.x; g < G; g += gridDim.x) {
     const int beg = offsets[g], end = offsets[g + 1], live = beg + counts[g];
     for (int p = live + threadIdx.x; p < end; p += blockDim.x) route_of_row[p] = -1;
-    for (int m = beg / kBlockM + threadIdx.x; m < end / kBlockM; m += blockDim.x) tile_group[m] = g;
+    const int2 span = make_int2(beg / kBlockM, (end - beg) / kBlockM);
+    for (int m = beg / kBlockM + threadIdx.x; m < end / kBlockM; m += blockDim.x) {
+      tile_group[m] = g;
+      tile_span[m] = span;
+    }
   }
   if (blockIdx.x == 0) {
     for (int a = threadIdx.x; a <= at.n; a += blockDim.x) {
@@ -148,7 +153,7 @@ __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __
 }
 
 __global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restrict__ wtile_off,
-                          int2* __restrict__ wtile) {
+                          int4* __restrict__ wtile) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     int carry = 0;
@@ -169,7 +174,8 @@ __global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restric
   __syncthreads();
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const int m = offsets[g] / kBlockM, n = (offsets[g + 1] - offsets[g]) / kBlockM, base = wtile_off[g];
-    for (int j = 0; 2 * j < n; ++j) wtile[base + j] = make_int2(((m + 2 * j) << 1) | (n - 2 * j >= 2 ? 1 : 0), g);
+    const int nw = (n + 1) / 2;
+    for (int j = 0; j < nw; ++j) wtile[base + j] = make_int4(((m + 2 * j) << 1) | (n - 2 * j >= 2 ? 1 : 0), g, base, nw);
   }
 }
 
@@ -183,10 +189,11 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
   int* row_of_route = (int*)(b + L.row_of_route);
   int* route_of_row = (int*)(b + L.route_of_row);
   int* tile_group = (int*)(b + L.tile_group);
+  int2* tile_span = (int2*)(b + L.tile_span);
   int* tok_off = (int*)(b + L.tok_off);
   int* tok_tile = (int*)(b + L.tok_tile);
   int* wtile_off = (int*)(b + L.wtile_off);
-  int2* wtile = (int2*)(b + L.wtile);
+  int4* wtile = (int4*)(b + L.wtile);
   int* chunk_base = (int*)(b + L.chunk_base);
   const int G = d->A * d->E;
   const int64_t TK = d->T * d->k;
@@ -218,8 +225,8 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
     prof_end(K_PLAN_SCATTER, stream);
   }
   prof_begin(K_PLAN_FINISH, stream);
-  plan_finish<<<G < 1024 ? G : 1024, 128, 0, stream>>>(G, counts, offsets, route_of_row, tile_group, at, tok_off,
-                                                       tok_tile);
+  plan_finish<<<G < 1024 ? G : 1024, 128, 0, stream>>>(G, counts, offsets, route_of_row, tile_group, tile_span,
+                                                  at, tok_off, tok_tile);
   prof_end(K_PLAN_FINISH, stream);
   prof_begin(K_PLAN_WIDE, stream);
   plan_wide<<<1, 1024, 0, stream>>>(G, offsets, wtile_off, wtile);

@@ -83,10 +83,11 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
   int* row_of_route = (int*)(b + L.row_of_route);
   int* route_of_row = (int*)(b + L.route_of_row);
   int* tile_group = (int*)(b + L.tile_group);
+  int2* tile_span = (int2*)(b + L.tile_span);
   int* tok_off = (int*)(b + L.tok_off);
   int* tok_tile = (int*)(b + L.tok_tile);
   int* wtile_off = (int*)(b + L.wtile_off);
-  int2* wtile = (int2*)(b + L.wtile);
+  int4* wtile = (int4*)(b + L.wtile);
   const int64_t TK = d->T * d->k;
   const int nch = (int)nchunks;
   if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_LORA_ERR_CUDA;
@@ -110,8 +111,8 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
   if (nch > 0)
     plan_scatter<<<nch, 32, hist_bytes, s>>>(topk_ids, TK, d->k, d->E, G, at, chunk_base, offsets, nch, row_of_route,
                                              route_of_row, err);
-  plan_finish<<<G < 1024 ? G : 1024, 128, 0, s>>>(G, counts, offsets, route_of_row, tile_group, at, tok_off,
-                                                  tok_tile);
+  plan_finish<<<G < 1024 ? G : 1024, 128, 0, s>>>(G, counts, offsets, route_of_row, tile_group, tile_span,
+                                                  at, tok_off, tok_tile);
   plan_wide<<<1, 1024, 0, s>>>(G, offsets, wtile_off, wtile);
   return cudaGetLastError() == cudaSuccess ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
 }

@@ -266,6 +266,13 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     args_dev = (inp["x"], inp["topk_ids"], inp["topk_w"], inp["dy"])
+    # pinned host buffers of the end-to-end leg, allocated before any other host-side
+    # work and filled without pageable intermediates (host memory churn makes the
+    # kernel compact memory, which stalls copies to and from pinned pages)
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in args_dev]
+    for hd, t in zip(h_in, args_dev):
+        hd.copy_(t)
+    h_out = [torch.zeros(t.shape, dtype=t.dtype, pin_memory=True) for t in [y, dx, dw] + [g[n] for n in ADAPTER_GRADS]]
     for _ in range(args.warmup):
         step(*args_dev)
     torch.cuda.synchronize()
@@ -370,12 +377,10 @@ def run_ours(args, rank, world, local_rank):
     # back device->host inside the timed region; copies run on their own streams
     # with double-buffered device inputs/outputs, so step i's read-back and step
     # i+1's upload overlap the compute of their neighbours.
-    h_in = [t.cpu().pin_memory() for t in args_dev]
     d_in = [[torch.empty_like(t) for t in args_dev] for _ in range(2)]
     outs_2 = [[y, dx, dw] + [g[n] for n in ADAPTER_GRADS]]
     y2, dx2, dw2, g2 = torch.empty_like(y), torch.empty_like(dx), torch.empty_like(dw), m.alloc_grads(d)
     outs_2.append([y2, dx2, dw2] + [g2[n] for n in ADAPTER_GRADS])
-    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs_2[0]]
     bi = sum(t.numel() * t.element_size() for t in h_in)
     bo = sum(t.numel() * t.element_size() for t in h_out)
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
@@ -385,13 +390,20 @@ def run_ours(args, rank, world, local_rank):
     for e_ in in_free + out_free:
         e_.record(stream)
 
-    def run_e2e(nsteps):
+    copy_ev = []  # per timed step: (upload start, upload end, read-back start, read-back end)
+
+    def run_e2e(nsteps, timed=False):
         for i in range(nsteps):
             b_ = i % 2
+            ce = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
             with torch.cuda.stream(up):
                 up.wait_event(in_free[b_])
+                if timed:
+                    ce[0].record(up)
                 for hd, dd in zip(h_in, d_in[b_]):
                     dd.copy_(hd, non_blocking=True)
+                if timed:
+                    ce[1].record(up)
                 in_ready[b_].record(up)
             stream.wait_event(in_ready[b_])
             stream.wait_event(out_free[b_])
@@ -405,27 +417,41 @@ def run_ours(args, rank, world, local_rank):
             out_ready[b_].record(stream)
             with torch.cuda.stream(down):
                 down.wait_event(out_ready[b_])
+                if timed:
+                    ce[2].record(down)
                 for o, ho in zip(outs_2[b_], h_out):
                     ho.copy_(o, non_blocking=True)
+                if timed:
+                    ce[3].record(down)
+                    copy_ev.append(ce)
                 out_free[b_].record(down)
 
-    run_e2e(2)
+    run_e2e(args.warmup)
     torch.cuda.synchronize()
     barrier()
     e2e_clocks = ClockSampler(local_rank)
     e2e_clocks.start()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record(up)
-    run_e2e(args.steps)
+    run_e2e(args.steps, timed=True)
     torch.cuda.current_stream(torch.device("cuda")).wait_stream(down)
     s1.record(down)
     torch.cuda.synchronize()
     barrier()
     e2e_clk = e2e_clocks.stop()
     ms_e2e = max_over_ranks(dist, s0.elapsed_time(s1) / args.steps, "cuda")
+    # per-step copy times: a host under memory compaction (seen right after a large
+    # test run) stalls single pinned copies for ~0.1 s; counted here, not removed
+    t_up = [e[0].elapsed_time(e[1]) for e in copy_ev]
+    t_dn = [e[2].elapsed_time(e[3]) for e in copy_ev]
+    med_up, med_dn = statistics.median(t_up), statistics.median(t_dn)
+    stalls = sum(1 for v in t_up if v > 3 * med_up) + sum(1 for v in t_dn if v > 3 * med_dn)
     e2e = {"value": round(job_tflops(world, flops, ms_e2e), 2), "unit": "TFLOP/s",
            "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
            "clocks": e2e_clk,
+           "copy_ms": {"upload_median": round(med_up, 2), "upload_max": round(max(t_up), 2),
+                       "readback_median": round(med_dn, 2), "readback_max": round(max(t_dn), 2),
+                       "stalled_copies": stalls},
            "copies": "pinned host memory, own streams, overlapped with neighbouring steps' compute"}
 
     # ---- CPU oracle baseline (rank 0, single GPU only)

@@ -9,7 +9,6 @@
 //   B5  W13^T dgrad + B1/B3 path;  dB1/dB3 (K-grouped per expert)
 //   B6a per-token sum of dY13;  B6 grad-x (A1/A3 path per token, then the source
 //       combine of the routed dXp rows);  dA1/dA3
-#include "gemm_pair.cuh"
 #include "gemm_problems.cuh"
 #include "launch.h"
 #include "passes.h"
@@ -101,9 +100,9 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   }
   // B2: routed dy rows and the scaled shared-expand gradients
   LAUNCH(launch_gather_bwd(pl, dy, dyB2, topk_w, Dp, D2p, dZ2p, d->H, d->r, d->scale, num_sms, stream));
-  // B3/B4: W2^T dgrad + A2 path + SwiGLU backward + router dots (two-SM tiles)
+  // B3/B4: W2^T dgrad + A2 path + SwiGLU backward + router dots
   {
-    ProbW2DgradPair p;
+    ProbW2Dgrad p;
     MAP(tmap_2d(&p.mDp, Dp, H, P, 64, 128));
     MAP(tmap_2d(&p.mD2p, D2p, r, P, 64, 128));
     MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 64));
@@ -122,7 +121,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.r = d->r;
     p.act = d->act;
     p.clamp = d->act_clamp;
-    LAUNCH(launch_gemm_pair(p, max_row_tiles * (d->I / 256), num_sms, stream, K_W2_DGRAD));
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream, K_W2_DGRAD));
   }
   LAUNCH(launch_dw(pl, part, d->I / 128, dw, num_sms, stream));
   // dA2 per (adapter, expert)

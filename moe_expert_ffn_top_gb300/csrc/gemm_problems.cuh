@@ -424,10 +424,9 @@ struct ProbW2 {
   int H, I, r;
   __device__ int ntn() const { return H / 256 + 1; }
   __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
-  __device__ TileInfo tile(int t) const {
-    const int nt = t % ntn();
+  __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
-    narrow_tile(pl, t, ntn(), ti);
+    const int nt = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
     ti.sub = nt == H / 256;
     ti.n0 = ti.sub ? 0 : nt * 256;
     ti.nk = I / kBK;
@@ -666,16 +665,12 @@ struct ProbW2Dgrad {
   __device__ int ntn() const { return I / 256; }
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
-  __device__ TileInfo tile(int t) const {
-    const int mt = t / ntn(), nt = t % ntn();
+  __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
-    ti.m0 = mt * 128;
-    ti.mend = ti.m0 + 128;
+    const int nt = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
     ti.n0 = nt * 256;
-    ti.g = pl.tile_group[mt];
     ti.sub = nt;
     ti.nk = H / kBK + nkr();
-    ti.k0 = 0;
     return ti;
   }
   __device__ void prefetch() const {
@@ -1061,7 +1056,7 @@ struct ProbDA13 {
 };
 
 // =====================================================================================
-// Two-SM (cta_group::2) forms of the four base expert GEMMs, for gemm_pair.cuh.
+// Two-SM (cta_group::2) form of the W2 expert GEMM, for gemm_pair.cuh.
 // A tile is 256 rows of one plan group: rank-0 CTA rows [m0, m0+128), rank-1 CTA
 // rows [m0+128, m0+256) (absent on a group's odd last tile).  The N columns of every
 // pair MMA are split in halves: rank v holds B columns [v*N/2, (v+1)*N/2).  Each
@@ -1107,39 +1102,6 @@ struct ProbW2Pair : ProbW2 {
   }
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     return MmaStep{ti.sub ? round32(r) : 256, 0, 0, ks == 0};
-  }
-};
-
-// B3/B4: the 256 columns of I are two 64-wide MN-major boxes per CTA.
-struct ProbW2DgradPair : ProbW2Dgrad {
-  static constexpr bool kIssuerNeedsTile = false;  // every tile: N = 256, same K steps
-  __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
-  // row-tile-major: the column-tile-major order measured no faster on the two-SM engine
-  __device__ int4 tile_fetch(int t) const {
-    const int4 w = pl.wtile[t / ntn()];
-    return make_int4(w.x, w.y, t % ntn(), 0);
-  }
-  __device__ TileInfo tile_at(int, int4 w) const {
-    TileInfo ti;
-    const int nt = wide_entry_decode(w, ti);
-    ti.n0 = nt * 256;
-    ti.sub = nt;
-    ti.nk = H / kBK + nkr();
-    return ti;
-  }
-  __device__ TileInfo tile(int t) const { return tile_at(t, tile_fetch(t)); }
-  __device__ uint32_t tx_bytes(const TileInfo& ti, int) const { return (uint32_t)(ti.mh * kAStage128 + 4 * 8192); }
-  __device__ void load_pair(const TileInfo& ti, int ks, int rank, uint8_t* sa, uint8_t* sb, uint32_t bar) const {
-    const int nb = H / kBK;
-    const int mrow = ti.m0 + rank * 128, nc = ti.n0 + rank * 128;
-    if (ks < nb) {
-      if (rank < ti.mh) tma_load_2d_pair(sa, &mDp, bar, ks * kBK, mrow);
-      for (int c = 0; c < 2; ++c) tma_load_3d_pair(sb + c * 8192, &mW2, bar, nc + c * 64, ks * kBK, ti.g % pl.E);
-    } else {
-      const int kb = ks - nb;
-      if (rank < ti.mh) tma_load_2d_pair(sa, &mD2p, bar, kb * kBK, mrow);
-      for (int c = 0; c < 2; ++c) tma_load_3d_pair(sb + c * 8192, &mA2, bar, nc + c * 64, kb * kBK, ti.g);
-    }
   }
 };
 

@@ -47,13 +47,26 @@ __device__ __forceinline__ void narrow_tile(const PlanView& pl, int t, int ntn, 
   ti.k0 = 0;
 }
 
-// Column-tile-major order inside each group: the base expert GEMMs walk all of a
-// group's row tiles for one column tile before the next column tile, so the CTAs
-// running at the same time share one block of expert weights (read once from DRAM)
-// rather than one block of routed rows.  A group's tiles are still the contiguous
-// range [first*ntn, (first+count)*ntn) of tile indices, so t / ntn names a row tile
-// of the right group.
-//
+// Column-tile-major order inside row chunks of each group: the base expert GEMMs walk
+// a chunk of up to kChunkRows of a group's rows for one block of weight columns, then
+// the next block, then the next chunk.  The CTAs running at the same time then share
+// a few weight blocks (read once from DRAM) and one chunk of routed rows (16 MB at
+// H = 4096, held in L2 across the column blocks); a group of up to kChunkRows rows --
+// the usual case -- is a single chunk.  A group's tiles are the contiguous range
+// [first*ntn, (first+count)*ntn) of tile indices, so t / ntn names a row tile of the
+// right group.
+constexpr int kChunkRows = 2048;
+
+// Row tile (offset from the group's first) and column tile of the group's tile u, for
+// a group of `count` row tiles cut into chunks of `chunk` row tiles.
+__device__ __forceinline__ void chunked_order(int u, int count, int chunk, int ntn, int& mt, int& nt) {
+  const int c = u / (chunk * ntn);
+  const int v = u - c * chunk * ntn;
+  const int cs = count - c * chunk < chunk ? count - c * chunk : chunk;
+  mt = c * chunk + v % cs;
+  nt = v / cs;
+}
+
 // 128-row tiles: the plan entry of tile t (loads only: group, first row tile and
 // row-tile count of the group) ...
 __device__ __forceinline__ int4 nmajor_narrow_fetch(const PlanView& pl, int t, int ntn) {
@@ -63,21 +76,23 @@ __device__ __forceinline__ int4 nmajor_narrow_fetch(const PlanView& pl, int t, i
 }
 // ... and its decode (no memory access); returns the column tile.
 __device__ __forceinline__ int nmajor_narrow_decode(int4 e, int t, int ntn, TileInfo& ti) {
-  const int u = t - e.y * ntn;
+  int mt, nt;
+  chunked_order(t - e.y * ntn, e.z, kChunkRows / 128, ntn, mt, nt);
   ti.g = e.x;
-  ti.m0 = (e.y + u % e.z) * 128;
+  ti.m0 = (e.y + mt) * 128;
   ti.mend = ti.m0 + 128;
   ti.mh = 1;
   ti.k0 = 0;
-  return u / e.z;
+  return nt;
 }
 // 256-row tiles: the entry of tile t (two dependent loads: any 256-row tile of the
-// group gives the group's first tile and count, then the tile itself; z = column tile) ...
+// group gives the group's first tile and count, then the tile itself; z = column tile).
 __device__ __forceinline__ int4 nmajor_wide_fetch(const PlanView& pl, int t, int ntn) {
   const int4 a = pl.wtile[t / ntn];
-  const int u = t - a.z * ntn;
-  const int4 w = pl.wtile[a.z + u % a.w];
-  return make_int4(w.x, w.y, u / a.w, 0);
+  int mt, nt;
+  chunked_order(t - a.z * ntn, a.w, kChunkRows / 256, ntn, mt, nt);
+  const int4 w = pl.wtile[a.z + mt];
+  return make_int4(w.x, w.y, nt, 0);
 }
 // Decode of a 256-row tile entry (x, y as in the plan, z = column tile); returns the column tile.
 __device__ __forceinline__ int wide_entry_decode(int4 e, TileInfo& ti) {

@@ -169,6 +169,24 @@ def test_rank128_wide():
         assert out[n][0, 0].abs().max().item() == 0 and out[n][0, 7].abs().max().item() == 0
 
 
+def test_large_groups_row_chunks():
+    """Groups far larger than one row chunk of the column-tile-major tile order (2,048
+    rows): 7,000 tokens, top-2 over 3 experts (~4,700 rows each: two full chunks and a
+    ragged one, 16 row tiles of 128 per chunk, 8 of 256 for the W13 dgrad), NaN-poisoned
+    workspaces, checked against the oracle on sampled tokens of every expert."""
+    shp = Shape(T=7000, H=1024, I=512, E=3, k=2, r=16)
+    inp = make_inputs(shp, seed=21, device="cuda")
+    sample = [0, 1, 2047, 2048, 2049, 3001, 4095, 4096, 5998, 6999]
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp, poison=True)
+    assert out["err"] == 0
+    counts = m.moe_lora_plan_readback(out["dims"], out["ws"].plan)["counts"]
+    assert int(counts.max()) > 2 * 2048
+    for n in ("y", "dx", "dw"):
+        assert torch.isfinite(out[n]).all(), n
+    _sampled_check(inp, shp, out, sample)
+
+
 def test_zero_scale_is_plain_moe_bitwise():
     """Zero adapter scale reproduces the layer without side adapters bit for bit
     (the pages' zero-scale preservation check)."""
@@ -238,7 +256,8 @@ def _sampled_check(inp, shp, out, sample):
         assert_close(n, out[n][:, ex].cpu(), g_ref[n])
         other = torch.ones(shp.E, dtype=torch.bool, device="cuda")
         other[ex] = False
-        assert out[n][:, other].abs().max().item() == 0, n
+        if other.any():
+            assert out[n][:, other].abs().max().item() == 0, n
 
 
 def _sparse_dy(inp, shp, sample):

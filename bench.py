@@ -247,7 +247,9 @@ def run_ours(args, rank, world, local_rank):
     inp = make_inputs(shp, seed=2 + rank, device="cuda")
     T, H, I, E, k, r = shp.T, shp.H, shp.I, shp.E, shp.k, shp.r
     R = int((inp["topk_ids"] >= 0).sum())
-    d = m.make_dims(T, H, I, E, k, r, 1, shp.scale, base_fmt=1 if shp.base_fmt == "mxfp4" else 0)
+    A = shp.A
+    d = m.make_dims(T, H, I, E, k, r, A, shp.scale, base_fmt=1 if shp.base_fmt == "mxfp4" else 0)
+    offs = inp["adapter_offsets"].tolist() if A > 1 else None  # token range of each adapter
     ws = m.Workspaces.allocate(d)
     y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     dx = torch.empty_like(y)
@@ -257,7 +259,7 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step(x, ids, tw, dy):
-        m.moe_lora_plan(d, ids, None, ws.plan)
+        m.moe_lora_plan(d, ids, offs, ws.plan)
         m.moe_lora_forward(d, ws.plan, x, tw, wts, y, ws.saved, ws.fwd)
         m.moe_lora_backward(d, ws.plan, ws.saved, x, tw, dy, wts, dx, dw, g, ws.bwd)
 
@@ -324,10 +326,49 @@ def run_ours(args, rank, world, local_rank):
     gemm_ms = sum(prof[n][0] for n in prof if n in fl) / args.steps
     gemm_flops = sum(fl[n] for n in prof if n in fl)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["bf16_sus"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sus"], 4), "traffic": traffic_for(dom),
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sus"], 4),
+                "traffic": traffic_for(dom) if args.workload == "prod" else None,
                 "peak_kind": f"bf16 dense, sustained ({pk['source']})",
                 "grouped_gemms_tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
                 "grouped_gemms_frac_of_burst_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 / pk["bf16"], 4)}
+
+    # ---- several adapters: the same work as one standalone pass per adapter (each
+    # its own plan, forward and backward over its token range), back to back
+    standalone = None
+    if A > 1:
+        d1 = m.make_dims(offs[1] - offs[0], H, I, E, k, r, 1, shp.scale)
+        ws1 = m.Workspaces.allocate(d1)
+        y1 = torch.empty(offs[1] - offs[0], H, dtype=torch.bfloat16, device="cuda")
+        dx1, dw1 = torch.empty_like(y1), torch.empty(offs[1] - offs[0], k, dtype=torch.float32, device="cuda")
+        g1 = m.alloc_grads(d1)
+        assert all(offs[a + 1] - offs[a] == offs[1] - offs[0] for a in range(A)), "equal token ranges"
+
+        def standalone_step():
+            for a in range(A):
+                sl = slice(offs[a], offs[a + 1])
+                wa = {n: (inp[n] if n in ("W1", "W3", "W2") else inp[n][a:a + 1]) for n in WEIGHTS}
+                x_, ids_, tw_, dy_ = (t[sl] for t in args_dev)
+                m.moe_lora_plan(d1, ids_, None, ws1.plan)
+                m.moe_lora_forward(d1, ws1.plan, x_, tw_, wa, y1, ws1.saved, ws1.fwd)
+                m.moe_lora_backward(d1, ws1.plan, ws1.saved, x_, tw_, dy_, wa, dx1, dw1, g1, ws1.bwd)
+
+        for _ in range(args.warmup):
+            standalone_step()
+        torch.cuda.synchronize()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(args.steps):
+            standalone_step()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        assert m.moe_lora_get_error(d1, ws1.plan) == 0, "device error word set"
+        ms_sa = max_over_ranks(dist, b0.elapsed_time(b1) / args.steps, "cuda")
+        standalone = {"ms_per_step": round(ms_sa, 3), "tflops": round(job_tflops(world, flops, ms_sa), 2),
+                      "fused_speedup": round(ms_sa / ms, 3),
+                      "note": f"{A} standalone single-adapter passes of {offs[1] - offs[0]} tokens back to back "
+                              f"(same total work); results equal the fused pass bit for bit (GPU tests)"}
+        del ws1, y1, dx1, dw1, g1
+        torch.cuda.empty_cache()
 
     # ---- the routing step ahead of the path (router forward / backward), timed on
     # its own: the headline step takes ids and weights as inputs, as the pages do.
@@ -410,7 +451,7 @@ def run_ours(args, rank, world, local_rank):
             yo, dxo, dwo = outs_2[b_][0], outs_2[b_][1], outs_2[b_][2]
             go = dict(zip(ADAPTER_GRADS, outs_2[b_][3:]))
             xi, idsi, twi, dyi = d_in[b_]
-            m.moe_lora_plan(d, idsi, None, ws.plan, stream)
+            m.moe_lora_plan(d, idsi, offs, ws.plan, stream)
             m.moe_lora_forward(d, ws.plan, xi, twi, wts, yo, ws.saved, ws.fwd, stream)
             m.moe_lora_backward(d, ws.plan, ws.saved, xi, twi, dyi, wts, dxo, dwo, go, ws.bwd, stream)
             in_free[b_].record(stream)
@@ -460,9 +501,18 @@ def run_ours(args, rank, world, local_rank):
         del ws
         torch.cuda.empty_cache()
         host = {n: v.cpu() for n, v in inp.items()}
-        v, info = oracle_sample(host, shp, args.cpu_seconds)
+        oshp = shp
+        if A > 1:  # the oracle takes one adapter: adapter 0's token range and factors
+            sl = slice(offs[0], offs[1])
+            host = {n: (host[n][sl] if n in ("x", "dy", "topk_ids", "topk_w") else
+                        host[n] if n in ("W1", "W3", "W2") else host[n][0:1].contiguous())
+                    for n in ("x", "dy", "topk_ids", "topk_w") + WEIGHTS}
+            host["adapter_offsets"] = torch.tensor([0, offs[1] - offs[0]], dtype=torch.int64)
+            oshp = Shape(T=offs[1] - offs[0], H=H, I=I, E=E, k=k, r=r, A=1, scale=shp.scale)
+        v, info = oracle_sample(host, oshp, args.cpu_seconds)
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
-               "sample": f"first {info['tokens']} tokens ({info['routes']} routes) of the same workload, "
+               "sample": f"first {info['tokens']} tokens ({info['routes']} routes) of the same workload"
+                         f"{' (adapter 0)' if A > 1 else ''}, "
                          f"forward+backward, {info['seconds']:.1f} s, plain C FP32 oracle with OpenMP"}
 
     if rank == 0:
@@ -476,9 +526,10 @@ def run_ours(args, rank, world, local_rank):
                        "tokens_per_gpu": T, "live_routes_per_gpu": R, "tflop_per_step_per_gpu": round(flops / 1e12, 3),
                        "pct_of_bf16_peak": round(100 * value / world / pk["bf16"], 2),
                        "parallelism": "replicas only (one independent batch per GPU, no collectives)",
-                       "l2": "inputs larger than L2 (12.9 GB frozen weights), no flush"},
+                       "adapters": A,
+                       "l2": f"inputs larger than L2 ({3 * E * H * I * 2 / 1e9:.1f} GB frozen weights), no flush"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "kernels": kernels, "router": router,
+            "clocks": clk, "kernels": kernels, "router": router, "standalone": standalone,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -528,7 +579,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="prod", choices=["prod", "prod_mxfp4", "prod_e16", "tiny", "edge"])
+    ap.add_argument("--workload", default="prod", choices=["prod", "prod_mxfp4", "prod_e16", "tiny", "edge", "multi"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

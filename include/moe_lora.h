@@ -137,7 +137,9 @@ typedef struct moe_lora_grads {
 MOE_LORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims* dims, int which);
 
 /* Routing plan (PR #9 leaves plan construction out of its timed scope).  A stable counting sort of the live routes by
- * (adapter, expert, token, slot); each group's rows are padded to a multiple of
+ * (expert, adapter, token, slot) -- the adapters routed to one expert sit side by
+ * side, so their tiles share that expert's base weights in L2 -- with group slot
+ * q = e*A + a (q = e for one adapter); each group's rows are padded to a multiple of
  * block_m and padding rows map to no route; every group starts at its own padded
  * offset, never rounded into a neighbouring expert (PR #9, Implementation).
  *   topk_ids         [T,k] int32, device.  -1 = masked route (not dispatched).
@@ -196,9 +198,10 @@ MOE_LORA_API int moe_lora_backward(const moe_lora_dims* dims, const void* plan_w
 MOE_LORA_API int moe_lora_get_error(const moe_lora_dims* dims, const void* plan_ws, void* stream);
 
 /* Copies a plan to HOST arrays for inspection (tests, debugging); synchronises
- * `stream`.  counts [A*E], offsets [A*E+1] (offsets[A*E] = P, the padded routed
- * row count), row_of_route [T*k] (-1 = not dispatched), route_of_row [P]
- * (t*k+j, or -1 on a padding row; pass cap >= P, or NULL/0 to skip). */
+ * `stream`.  counts [A*E] and offsets [A*E+1], both by group slot q = e*A + a
+ * (offsets[A*E] = P, the padded routed row count), row_of_route [T*k] (-1 = not
+ * dispatched), route_of_row [P] (t*k+j, or -1 on a padding row; pass cap >= P, or
+ * NULL/0 to skip). */
 MOE_LORA_API int moe_lora_plan_readback(const moe_lora_dims* dims, const void* plan_ws, int32_t* counts,
                                         int32_t* offsets, int32_t* row_of_route, int32_t* route_of_row,
                                         int64_t route_of_row_cap, void* stream);

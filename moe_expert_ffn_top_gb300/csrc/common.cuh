@@ -164,18 +164,24 @@ inline int check_router_dims(const moe_lora_dims* d) {
 }
 
 // ------------------------------------------------------------------ device plan view
+// Groups are laid out expert-major: plan slot q = e*A + a holds the rows of adapter a
+// routed to expert e, so the A groups sharing an expert's base weights are adjacent
+// in the padded rows (their tiles run back to back and find those weights in L2).
+// Per-group weights and gradients are indexed by g = a*E + e.
+__host__ __device__ inline int group_weight_index(int q, int A, int E) { return (q % A) * E + q / A; }
+
 struct PlanView {
   int* err;                  // sticky device error word
-  const int* counts;         // [G] live routes per (adapter, expert) group
-  const int* offsets;        // [G+1] padded row offsets; offsets[G] = P
+  const int* counts;         // [G] live routes per group, in plan-slot order (q = e*A + a)
+  const int* offsets;        // [G+1] padded row offsets by plan slot; offsets[G] = P
   const int* row_of_route;   // [T*k] padded row of route t*k+j, or -1
   const int* route_of_row;   // [P] route of a row, or -1 for padding
-  const int* tile_group;     // [P/128] group of each 128-row tile
+  const int* tile_group;     // [P/128] weight index g = a*E + e of each 128-row tile's group
   const int2* tile_span;     // [P/128] (first 128-row tile, number of 128-row tiles) of that tile's group
   const int* tok_off;        // [A+1] first token of each adapter
   const int* tok_tile;       // [A+1] first 128-token tile of each adapter
-  const int* wtile_off;      // [G+1] first 256-row tile of each group
-  const int4* wtile;         // 256-row tiles: x = (first 128-row tile << 1) | (halves - 1), y = group,
+  const int* wtile_off;      // [G+1] first 256-row tile of each group, by plan slot
+  const int4* wtile;         // 256-row tiles: x = (first 128-row tile << 1) | (halves - 1), y = weight index,
                              // z = first 256-row tile of the group, w = the group's number of 256-row tiles
   int64_t T;
   int G, E, A, k;

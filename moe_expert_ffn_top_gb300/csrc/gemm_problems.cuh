@@ -4,8 +4,8 @@
 //
 // Notation (row-major): x [T,H], Xp [P,H] routed rows (zero on padding rows),
 // W1/W3 [E,I,H], W2 [E,H,I], A1/A3 [A,r,H], B1/B3 [A*E,I,r], A2 [A*E,r,I], B2 [A,H,r].
-// A plan group g = a*E + e is (adapter a, expert e); its rows are
-// [offsets[g], offsets[g+1]), a multiple of 128 long.
+// A group (adapter a, expert e) has weight index g = a*E + e (TileInfo::g) and plan
+// slot q = e*A + a; its rows are [offsets[q], offsets[q+1]), a multiple of 128 long.
 //
 // The side-LoRA contract ("feat(mega): add fused shared side-LoRA kernels",
 // DeepGEMM PR #9, Summary): A1/A3 and B2 are shared, so the rank-r shrink
@@ -27,7 +27,8 @@ __device__ __forceinline__ int adapter_of_tile(const PlanView& pl, int t) {
 }
 
 // 256-row tile of an M-grouped problem from its plan entry w: rows
-// [m0, m0 + 128*mh) of plan group w.y (mh = 2, or 1 for a group's odd last tile).
+// [m0, m0 + 128*mh) of the group with weight index w.y (mh = 2, or 1 for a group's
+// odd last tile).
 __device__ __forceinline__ void wide_tile_from(int4 w, TileInfo& ti) {
   const int mt = w.x >> 1;
   ti.mh = (w.x & 1) + 1;
@@ -759,15 +760,15 @@ struct ProbDA2 {
   __device__ int ntn() const { return I / 256; }
   __device__ int num_tiles() const { return pl.G * ntn(); }
   __device__ TileInfo tile(int t) const {
-    const int g = t / ntn(), nt = t % ntn();
+    const int q = t / ntn(), nt = t % ntn();  // plan slot of the group
     TileInfo ti;
-    ti.g = g;
+    ti.g = group_weight_index(q, pl.A, pl.E);
     ti.m0 = 0;
     ti.mend = r;
     ti.n0 = nt * 256;
     ti.sub = 0;
-    ti.k0 = pl.offsets[g];
-    ti.nk = (pl.offsets[g + 1] - pl.offsets[g]) / kBK;
+    ti.k0 = pl.offsets[q];
+    ti.nk = (pl.offsets[q + 1] - pl.offsets[q]) / kBK;
     return ti;
   }
   __device__ void prefetch() const {
@@ -901,15 +902,15 @@ struct ProbDB13 {
   __device__ TileInfo tile(int t) const {
     const int which = t / (pl.G * ntm());
     const int rem = t % (pl.G * ntm());
-    const int g = rem / ntm(), mt = rem % ntm();
+    const int q = rem / ntm(), mt = rem % ntm();  // plan slot of the group
     TileInfo ti;
-    ti.g = g;
+    ti.g = group_weight_index(q, pl.A, pl.E);
     ti.m0 = mt * 128;
     ti.mend = I;
     ti.n0 = 0;
     ti.sub = which;
-    ti.k0 = pl.offsets[g];
-    ti.nk = (pl.offsets[g + 1] - pl.offsets[g]) / kBK;
+    ti.k0 = pl.offsets[q];
+    ti.nk = (pl.offsets[q + 1] - pl.offsets[q]) / kBK;
     return ti;
   }
   __device__ void prefetch() const {

@@ -1,6 +1,6 @@
 // Routing plan on the device: a stable counting sort of the live routes by
-// (adapter, expert, token, slot), each (adapter, expert) group padded to a
-// multiple of 128 rows.  Deterministic: the row of every route is a function of
+// (expert, adapter, token, slot), each (expert, adapter) group padded to a
+// multiple of 128 rows (plan slot q = e*A + a; one adapter: q = e).  Deterministic: the row of every route is a function of
 // the ids alone (the pages' atomic dispatch reordered rows between replays,
 // "feat(mega): add fused shared side-LoRA kernels", review thread on
 // repeatability; this plan does not).
@@ -31,7 +31,7 @@ __device__ __forceinline__ int group_of(const int* ids, int64_t rt, int k, int E
   const int64_t t = rt / k;
   int a = 0;
   while (a + 1 < at.n && t >= at.tok_off[a + 1]) ++a;
-  return a * E + e;
+  return e * at.n + a;
 }
 
 // one warp per chunk; smem histogram of G counters
@@ -112,7 +112,7 @@ __global__ void plan_scatter(const int* __restrict__ ids, int64_t TK, int k, int
         const int64_t t = rt / k;
         int a = 0;
         while (a + 1 < at.n && t >= at.tok_off[a + 1]) ++a;
-        g = a * E + e;
+        g = e * at.n + a;
       }
     }
     const unsigned peers = __match_any_sync(0xffffffffu, g);
@@ -131,7 +131,7 @@ __global__ void plan_scatter(const int* __restrict__ ids, int64_t TK, int k, int
 }
 
 // padding rows -> -1; tile -> group; adapter tables into the workspace.
-__global__ void plan_finish(int G, const int* __restrict__ counts, const int* __restrict__ offsets,
+__global__ void plan_finish(int G, int E, const int* __restrict__ counts, const int* __restrict__ offsets,
                             int* __restrict__ route_of_row, int* __restrict__ tile_group,
                             int2* __restrict__ tile_span, AdapterTable at, int* __restrict__ tok_off,
                             int* __restrict__ tok_tile) {
@@ -139,8 +139,9 @@ __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __
     const int beg = offsets[g], end = offsets[g + 1], live = beg + counts[g];
     for (int p = live + threadIdx.x; p < end; p += blockDim.x) route_of_row[p] = -1;
     const int2 span = make_int2(beg / kBlockM, (end - beg) / kBlockM);
+    const int wg = group_weight_index(g, at.n, E);
     for (int m = beg / kBlockM + threadIdx.x; m < end / kBlockM; m += blockDim.x) {
-      tile_group[m] = g;
+      tile_group[m] = wg;
       tile_span[m] = span;
     }
   }
@@ -152,7 +153,7 @@ __global__ void plan_finish(int G, const int* __restrict__ counts, const int* __
   }
 }
 
-__global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restrict__ wtile_off,
+__global__ void plan_wide(int G, int A, int E, const int* __restrict__ offsets, int* __restrict__ wtile_off,
                           int4* __restrict__ wtile) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
@@ -175,7 +176,9 @@ __global__ void plan_wide(int G, const int* __restrict__ offsets, int* __restric
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const int m = offsets[g] / kBlockM, n = (offsets[g + 1] - offsets[g]) / kBlockM, base = wtile_off[g];
     const int nw = (n + 1) / 2;
-    for (int j = 0; j < nw; ++j) wtile[base + j] = make_int4(((m + 2 * j) << 1) | (n - 2 * j >= 2 ? 1 : 0), g, base, nw);
+    const int wg = group_weight_index(g, A, E);
+    for (int j = 0; j < nw; ++j)
+      wtile[base + j] = make_int4(((m + 2 * j) << 1) | (n - 2 * j >= 2 ? 1 : 0), wg, base, nw);
   }
 }
 
@@ -225,11 +228,11 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
     prof_end(K_PLAN_SCATTER, stream);
   }
   prof_begin(K_PLAN_FINISH, stream);
-  plan_finish<<<G < 1024 ? G : 1024, 128, 0, stream>>>(G, counts, offsets, route_of_row, tile_group, tile_span,
+  plan_finish<<<G < 1024 ? G : 1024, 128, 0, stream>>>(G, d->E, counts, offsets, route_of_row, tile_group, tile_span,
                                                   at, tok_off, tok_tile);
   prof_end(K_PLAN_FINISH, stream);
   prof_begin(K_PLAN_WIDE, stream);
-  plan_wide<<<1, 1024, 0, stream>>>(G, offsets, wtile_off, wtile);
+  plan_wide<<<1, 1024, 0, stream>>>(G, d->A, d->E, offsets, wtile_off, wtile);
   prof_end(K_PLAN_WIDE, stream);
   return cudaGetLastError();
 }

@@ -111,8 +111,8 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
   if (nch > 0)
     plan_scatter<<<nch, 32, hist_bytes, s>>>(topk_ids, TK, d->k, d->E, G, at, chunk_base, offsets, nch, row_of_route,
                                              route_of_row, err);
-  plan_finish<<<G < 1024 ? G : 1024, 128, 0, s>>>(G, counts, offsets, route_of_row, tile_group, tile_span,
+  plan_finish<<<G < 1024 ? G : 1024, 128, 0, s>>>(G, d->E, counts, offsets, route_of_row, tile_group, tile_span,
                                                   at, tok_off, tok_tile);
-  plan_wide<<<1, 1024, 0, s>>>(G, offsets, wtile_off, wtile);
+  plan_wide<<<1, 1024, 0, s>>>(G, d->A, d->E, offsets, wtile_off, wtile);
   return cudaGetLastError() == cudaSuccess ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
 }

@@ -178,7 +178,8 @@ def backward(inp: dict, shp, tokens: Optional[Sequence[int]] = None, prec: str =
 
 
 def plan(ids: torch.Tensor, E: int, adapter_offsets: torch.Tensor, block_m: int = 128):
-    """Routing plan: counts [A*E], offsets [A*E+1], row_of_route [T*k], route_of_row [P]."""
+    """Routing plan: counts [A*E] and offsets [A*E+1] by group slot q = e*A + a,
+    row_of_route [T*k], route_of_row [P]."""
     L = lib("f32")
     ids = ids.to(torch.int32).contiguous().cpu()
     T, k = ids.shape

@@ -34,7 +34,8 @@
  * for the frozen base weights).  Adapter gradients are summed in (token, slot) order.
  *
  * The routing plan is a stable counting sort of the live routes by
- * (adapter, expert, token, slot), each group padded to a multiple of BLOCK_M rows
+ * (expert, adapter, token, slot) -- group slot q = e*A + a, so q = e for one
+ * adapter -- each group padded to a multiple of BLOCK_M rows
  * (pool padding of PR #9, Implementation: each expert's rows start at its own
  * padded offset, never rounded into a neighbour).
  *
@@ -186,8 +187,12 @@ static int adapter_of(const oinputs* in, int A, int64_t t) {
 
 /* ---------------- routing plan ---------------- */
 
-/* Stable counting sort of live routes by (adapter, expert, token, slot).
- * Returns the number of invalid ids (>= E or < -1), which are dropped. */
+/* Stable counting sort of live routes by (expert, adapter, token, slot); counts and
+ * offsets are indexed by the group slot q = e*A + a.  The pages fix no row order
+ * when several adapters share the layer (OpenPipe/ART PR #1139, Behavior: the
+ * dispatched rows only carry adapter ids); expert-major keeps the adapters routed to
+ * one expert side by side.  Returns the number of invalid ids (>= E or < -1), which
+ * are dropped. */
 int oracle_plan(int64_t T, int32_t k, int32_t E, int32_t A, int32_t BM, const int32_t* ids,
                 const int64_t* adapter_offsets, int32_t* counts, int32_t* offsets,
                 int32_t* row_of_route, int32_t* route_of_row, int64_t row_cap) {
@@ -200,7 +205,7 @@ int oracle_plan(int64_t T, int32_t k, int32_t E, int32_t A, int32_t BM, const in
     for (int j = 0; j < k; ++j) {
       int32_t e = ids[t * k + j];
       if (e >= E || e < -1) { ++bad; continue; }
-      if (e >= 0) counts[(int64_t)a * E + e]++;
+      if (e >= 0) counts[(int64_t)e * A + a]++;
     }
   }
   offsets[0] = 0;
@@ -216,7 +221,7 @@ int oracle_plan(int64_t T, int32_t k, int32_t E, int32_t A, int32_t BM, const in
       int32_t e = ids[t * k + j];
       int64_t rt = t * k + j;
       if (e < 0 || e >= E) { row_of_route[rt] = -1; continue; }
-      int32_t row = cursor[(int64_t)a * E + e]++;
+      int32_t row = cursor[(int64_t)e * A + a]++;
       row_of_route[rt] = row;
       if (row < row_cap) route_of_row[row] = (int32_t)rt;
     }

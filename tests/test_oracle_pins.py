@@ -227,7 +227,7 @@ def _plan_bruteforce(ids, E, offs, BM):
         for j in range(k):
             e = int(ids[t, j])
             if 0 <= e < E:
-                keys.append((adapter[t] * E + e, t, j))
+                keys.append((e * A + adapter[t], t, j))  # (expert, adapter, token, slot)
     keys.sort()
     counts = np.zeros(A * E, dtype=np.int64)
     for g, _, _ in keys:

@@ -110,10 +110,14 @@ __device__ __forceinline__ void load_a_wide(const TileInfo& ti, uint8_t* sa, con
 
 // Gated activations: ACT 0 = silu (SwiGLU), 1 = exact erf GELU (GeGLU); the
 // clamp c > 0 limits gate and up pre-activations to [-c, c] (0 = no clamp).
+// silu runs on the fast exponential and division (a few fp32 ulp, far below the
+// bf16 rounding of what is saved): the accurate forms put a dependent chain with a
+// slow-path branch on every element, which the epilogue warp (alone on its
+// scheduler) cannot hide.  For z -> -inf the denominator is +inf and the quotient 0.
 template <int ACT>
 __device__ __forceinline__ float act_fwd(float z) {
   if (ACT == 1) return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
-  return z / (1.0f + expf(-z));
+  return __fdividef(z, 1.0f + __expf(-z));
 }
 // f(z) and f'(z) together (one exponential and one division for silu).
 template <int ACT>
@@ -123,7 +127,7 @@ __device__ __forceinline__ void act_pair(float z, float& f, float& df) {
     f = z * cdf;
     df = cdf + z * 0.39894228040143268f * expf(-0.5f * z * z);
   } else {
-    const float sg = 1.0f / (1.0f + expf(-z));
+    const float sg = __fdividef(1.0f, 1.0f + __expf(-z));
     f = z * sg;
     df = sg * (1.0f + z * (1.0f - sg));
   }
@@ -358,10 +362,14 @@ struct ProbShrink {
 // N=256 MMA over W1|W3 rows), then ceil(r/64) steps per side for the expand
 // (N=128 into the gate half with Y1p/B1, then into the up half with Y3p/B3).
 // =====================================================================================
+// 256-row tiles: a third fewer operand bytes per FLOP than 128-row tiles, at the
+// price of an epilogue that no longer overlaps the next tile's main loop.  With the
+// fast silu that trade pays (same-box 9.33 -> 9.04 ms at 65,536 tokens, E256).
+constexpr bool kW13Wide = true;
 struct ProbW13 {
   static constexpr bool kAmn = false, kBmn = false;
-  static constexpr int kEpiWarps = 4;
-  static constexpr bool kWide = false;  // 256-row tiles measured slower: its epilogue is heavy
+  static constexpr bool kWide = kW13Wide;
+  static constexpr int kEpiWarps = kWide ? 8 : 4;
   CUtensorMap mXp, mY13p, mW1, mW3, mB1, mB3;  // Xp (H,P) box(64,128); Y13p (2r,P) box(64,128);
                                                // W1/W3 (H,I,E) box(64,128,1); B1/B3 (r,I,G) box(64,128,1)
   PlanView pl;
@@ -372,10 +380,15 @@ struct ProbW13 {
   float clamp;  // activation clamp (0 = none)
   __device__ int ntn() const { return I / 128; }
   __device__ int nkr() const { return (r + 63) / 64; }
-  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ int num_tiles() const {
+    return (kWide ? pl.wtile_off[pl.G] : pl.offsets[pl.G] / 128) * ntn();
+  }
   __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
-    ti.n0 = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti) * 128;
+    if (kWide)
+      ti.n0 = wide_entry_decode(nmajor_wide_fetch(pl, t, ntn()), ti) * 128;
+    else
+      ti.n0 = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti) * 128;
     ti.sub = 0;
     ti.nk = H / kBK + 2 * nkr();
     return ti;

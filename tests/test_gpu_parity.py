@@ -151,6 +151,21 @@ def test_tiny_forward_backward(T, mask):
     _full_check(inp, shp, out)
 
 
+def test_saturated_gates():
+    """x scaled by 64: gate pre-activations reach the hundreds, so silu sits at its
+    limits (exp(-z) overflows to inf for z < -88, giving 0; z for large z) in the
+    forward, the saved activation and the backward's sigmoid; all finite and within
+    tolerance of the oracle."""
+    shp = Shape(T=256, H=512, I=256, E=16, k=2, r=16)
+    inp = make_inputs(shp, seed=21)
+    inp["x"] = (inp["x"].float() * 64).to(torch.bfloat16)
+    out = run_gpu(inp, shp)
+    assert out["err"] == 0
+    g = inp["x"].float() @ inp["W1"][0].float().t()
+    assert (g < -88).float().mean() > 0.05  # the overflow branch is exercised
+    _full_check(inp, shp, out)
+
+
 def test_small_rank8_top8():
     shp = Shape(T=300, H=256, I=512, E=8, k=8, r=8, scale=0.5)
     inp = make_inputs(shp, seed=5)

@@ -123,7 +123,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.clamp = d->act_clamp;
     LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream, K_W2_DGRAD));
   }
-  LAUNCH(launch_dw(pl, part, d->I / 128, dw, num_sms, stream));
+  LAUNCH(launch_dw(pl, part, ProbW2Dgrad::kPartsPerTile * (d->I / 256), dw, num_sms, stream));
   // dA2 per (adapter, expert)
   {
     ProbDA2 p;

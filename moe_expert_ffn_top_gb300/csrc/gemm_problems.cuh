@@ -676,10 +676,16 @@ struct ProbDB2 {
 //   (router-gradient partial sums, reduced in a fixed order by the dw kernel)
 // Padding rows produce exact zeros.  A: Dp/D2p K-major; B: W2/A2 MN-major.
 // =====================================================================================
+// 128-row tiles: its epilogue loads the saved G, U and activation from DRAM, and on
+// 256-row tiles those loads no longer overlap the main loop (same-box 5.55 -> 6.77 ms
+// at 65,536 tokens, E256).
+constexpr bool kW2DgradWide = false;
 struct ProbW2Dgrad {
   static constexpr bool kAmn = false, kBmn = true;
-  static constexpr bool kWide = false;
+  static constexpr bool kWide = kW2DgradWide;
   static constexpr int kEpiWarps = 8;  // load-heavy epilogue: two warps per lane quarter
+  // router-gradient partial sums per row and column tile (one per epilogue column stripe)
+  static constexpr int kPartsPerTile = kWide ? 1 : kEpiWarps / 4;
   CUtensorMap mDp, mD2p, mW2, mA2;  // Dp (H,P) box(64,128); D2p (r,P) box(64,128);
                                     // W2 (I,H,E) box(64,64,1); A2 (I,r,G) box(64,64,1)
   PlanView pl;
@@ -693,10 +699,13 @@ struct ProbW2Dgrad {
   float clamp;  // activation clamp (0 = none)
   __device__ int ntn() const { return I / 256; }
   __device__ int nkr() const { return (r + 63) / 64; }
-  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ int num_tiles() const {
+    return (kWide ? pl.wtile_off[pl.G] : pl.offsets[pl.G] / 128) * ntn();
+  }
   __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
-    const int nt = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
+    const int nt = kWide ? wide_entry_decode(nmajor_wide_fetch(pl, t, ntn()), ti)
+                         : nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
     ti.n0 = nt * 256;
     ti.sub = nt;
     ti.nk = H / kBK + nkr();
@@ -710,13 +719,13 @@ struct ProbW2Dgrad {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int nb = H / kBK;
-    mbar_arrive_expect_tx(bar, kAStage128 + 4 * 8192);
+    mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 4 * 8192);
     if (ks < nb) {
-      tma_load_2d(sa, &mDp, bar, ks * kBK, ti.m0);
+      load_a_wide(ti, sa, &mDp, bar, ks * kBK);
       for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
     } else {
       const int kb = ks - nb;
-      tma_load_2d(sa, &mD2p, bar, kb * kBK, ti.m0);
+      load_a_wide(ti, sa, &mD2p, bar, kb * kBK);
       for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mA2, bar, ti.n0 + c * 64, kb * kBK, ti.g);
     }
   }
@@ -751,7 +760,7 @@ struct ProbW2Dgrad {
       warp_store_rows_bf16(dG + base0 + c, I, 32, og, 1.0f, stg);
       warp_store_rows_bf16(dU + base0 + c, I, 32, ou, 1.0f, stg);
     }
-    part[p * ((cs / 32) * ntn()) + (cs / 32) * ti.sub + c0 / 32] = live ? dot : 0.0f;
+    part[(p * ntn() + ti.sub) * kPartsPerTile + c0 / 32] = live ? dot : 0.0f;
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };

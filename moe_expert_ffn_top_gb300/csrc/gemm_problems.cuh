@@ -1104,14 +1104,18 @@ struct ProbDA13 {
 
 // F4/F5: base tiles split 256 W2 rows 128 / 128; the A2 tile (N = round32(r))
 // splits the A2 rows in halves of round32(r)/2 (rows past r read as zeros).
+// Row-tile-major on the two-SM engine.  Column-tile-major (2,048-row chunks) halves
+// its DRAM reads in a cold-cache capture (14.8 -> 8.0 GB per launch at 65,536 tokens)
+// but measured slower inside the step (4.50 vs 4.39 ms, same box, two alternations).
+constexpr bool kW2PairNmajor = false;
 struct ProbW2Pair : ProbW2 {
   CUtensorMap mW2h, mA2h;  // W2 (I,H,E) box(64,128,1); A2 (I,r,G) box(64,round32(r)/2,1),
                            // in place of the one-SM mW2/mA2
   static constexpr bool kIssuerNeedsTile = true;  // the A2 tile has its own MMA N
   __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
-  // row-tile-major: the column-tile-major order measured no faster on the two-SM engine
   __device__ int4 tile_fetch(int t) const {
-    const int4 w = pl.wtile[t / ntn()];
+    if (kW2PairNmajor) return nmajor_wide_fetch(pl, t, ntn());
+    const int4 w = pl.wtile[t / ntn()];  // row-tile-major
     return make_int4(w.x, w.y, t % ntn(), 0);
   }
   __device__ TileInfo tile_at(int, int4 w) const {

@@ -291,7 +291,10 @@ def test_edge_sweep_production_width(T):
     shp = shape("edge", T)
     inp = make_inputs(shp, seed=1000 + T, device="cuda")
     g = torch.Generator().manual_seed(T)
-    n = min(T, 12)
+    # 6 sampled tokens (<= 36 experts' weights copied to the host per case): the sweep
+    # churns far less host memory, which otherwise leaves the host compacting memory
+    # (and stalling pinned copies) for minutes after the suite
+    n = min(T, 6)
     sample = sorted(torch.randperm(T, generator=g)[:n].tolist())
     inp = _sparse_dy(inp, shp, sample)
     out = run_gpu(inp, shp)

@@ -417,7 +417,9 @@ def run_ours(args, rank, world, local_rank):
     # Every step copies its own inputs host->device and reads all of its results
     # back device->host inside the timed region; copies run on their own streams
     # with double-buffered device inputs/outputs, so step i's read-back and step
-    # i+1's upload overlap the compute of their neighbours.
+    # i+1's upload overlap the compute of their neighbours.  Each copy follows its
+    # data: dy goes up while the forward runs (only the backward reads it) and y
+    # comes back while the backward runs.
     d_in = [[torch.empty_like(t) for t in args_dev] for _ in range(2)]
     outs_2 = [[y, dx, dw] + [g[n] for n in ADAPTER_GRADS]]
     y2, dx2, dw2, g2 = torch.empty_like(y), torch.empty_like(dx), torch.empty_like(dw), m.alloc_grads(d)
@@ -426,46 +428,51 @@ def run_ours(args, rank, world, local_rank):
     bo = sum(t.numel() * t.element_size() for t in h_out)
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    in_ready, in_free = [ev(), ev()], [ev(), ev()]
-    out_ready, out_free = [ev(), ev()], [ev(), ev()]
+    fwd_in_ready, bwd_in_ready, in_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    fwd_done, bwd_done, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     for e_ in in_free + out_free:
         e_.record(stream)
 
-    copy_ev = []  # per timed step: (upload start, upload end, read-back start, read-back end)
+    copy_ev = []  # per timed step: start/end of the forward and backward uploads and read-backs
+
+    def copies(pairs, stream_, ce, j):
+        if ce is not None:
+            ce[j].record(stream_)
+        for src, dst in pairs:
+            dst.copy_(src, non_blocking=True)
+        if ce is not None:
+            ce[j + 1].record(stream_)
 
     def run_e2e(nsteps, timed=False):
         for i in range(nsteps):
             b_ = i % 2
-            ce = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
-            with torch.cuda.stream(up):
+            ce = [torch.cuda.Event(enable_timing=True) for _ in range(8)] if timed else None
+            xi, idsi, twi, dyi = d_in[b_]
+            with torch.cuda.stream(up):  # x, ids, weights, then dy
                 up.wait_event(in_free[b_])
-                if timed:
-                    ce[0].record(up)
-                for hd, dd in zip(h_in, d_in[b_]):
-                    dd.copy_(hd, non_blocking=True)
-                if timed:
-                    ce[1].record(up)
-                in_ready[b_].record(up)
-            stream.wait_event(in_ready[b_])
+                copies(zip(h_in[:3], d_in[b_][:3]), up, ce, 0)
+                fwd_in_ready[b_].record(up)
+                copies([(h_in[3], dyi)], up, ce, 2)
+                bwd_in_ready[b_].record(up)
+            stream.wait_event(fwd_in_ready[b_])
             stream.wait_event(out_free[b_])
             yo, dxo, dwo = outs_2[b_][0], outs_2[b_][1], outs_2[b_][2]
             go = dict(zip(ADAPTER_GRADS, outs_2[b_][3:]))
-            xi, idsi, twi, dyi = d_in[b_]
             m.moe_lora_plan(d, idsi, offs, ws.plan, stream)
             m.moe_lora_forward(d, ws.plan, xi, twi, wts, yo, ws.saved, ws.fwd, stream)
+            fwd_done[b_].record(stream)
+            stream.wait_event(bwd_in_ready[b_])
             m.moe_lora_backward(d, ws.plan, ws.saved, xi, twi, dyi, wts, dxo, dwo, go, ws.bwd, stream)
             in_free[b_].record(stream)
-            out_ready[b_].record(stream)
-            with torch.cuda.stream(down):
-                down.wait_event(out_ready[b_])
-                if timed:
-                    ce[2].record(down)
-                for o, ho in zip(outs_2[b_], h_out):
-                    ho.copy_(o, non_blocking=True)
-                if timed:
-                    ce[3].record(down)
-                    copy_ev.append(ce)
+            bwd_done[b_].record(stream)
+            with torch.cuda.stream(down):  # y, then the backward's results
+                down.wait_event(fwd_done[b_])
+                copies([(yo, h_out[0])], down, ce, 4)
+                down.wait_event(bwd_done[b_])
+                copies(zip(outs_2[b_][1:], h_out[1:]), down, ce, 6)
                 out_free[b_].record(down)
+            if timed:
+                copy_ev.append(ce)
 
     run_e2e(args.warmup)
     torch.cuda.synchronize()
@@ -483,8 +490,8 @@ def run_ours(args, rank, world, local_rank):
     ms_e2e = max_over_ranks(dist, s0.elapsed_time(s1) / args.steps, "cuda")
     # per-step copy times: a host under memory compaction (seen right after a large
     # test run) stalls single pinned copies for ~0.1 s; counted here, not removed
-    t_up = [e[0].elapsed_time(e[1]) for e in copy_ev]
-    t_dn = [e[2].elapsed_time(e[3]) for e in copy_ev]
+    t_up = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in copy_ev]
+    t_dn = [e[4].elapsed_time(e[5]) + e[6].elapsed_time(e[7]) for e in copy_ev]
     med_up, med_dn = statistics.median(t_up), statistics.median(t_dn)
     stalls = sum(1 for v in t_up if v > 3 * med_up) + sum(1 for v in t_dn if v > 3 * med_dn)
     e2e = {"value": round(job_tflops(world, flops, ms_e2e), 2), "unit": "TFLOP/s",
@@ -493,7 +500,8 @@ def run_ours(args, rank, world, local_rank):
            "copy_ms": {"upload_median": round(med_up, 2), "upload_max": round(max(t_up), 2),
                        "readback_median": round(med_dn, 2), "readback_max": round(max(t_dn), 2),
                        "stalled_copies": stalls},
-           "copies": "pinned host memory, own streams, overlapped with neighbouring steps' compute"}
+           "copies": "pinned host memory, own streams; dy uploaded during the forward and y read back "
+                     "during the backward; overlapped with neighbouring steps' compute"}
 
     # ---- CPU oracle baseline (rank 0, single GPU only)
     cpu = None

@@ -28,13 +28,13 @@ static void load_encode() {
 }
 
 static int encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                  const cuuint32_t* box) {
+                  const cuuint32_t* box, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   std::call_once(g_encode_once, load_encode);
   if (!g_encode) return -1;
   const cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
-                              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
@@ -44,6 +44,13 @@ int tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
   return encode(m, base, 2, dims, strides, box);
+}
+
+int tmap_2d_store32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  const cuuint64_t dims[2] = {inner, outer > 0 ? outer : 1};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {32, 32};
+  return encode(m, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {

@@ -148,6 +148,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.pl = pl;
     p.err = pl.err;
     p.dXp = dXp;
+    MAP(tmap_2d_store32(&p.mdXp, dXp, H, P));
     p.dY13 = dY13;
     p.H = d->H;
     p.I = d->I;
@@ -180,6 +181,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.pl = pl;
     p.err = pl.err;
     p.dXl = dXl;
+    MAP(tmap_2d_store32(&p.mdXl, dXl, H, T));
     p.H = d->H;
     p.r = d->r;
     LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_A13_EXPAND));

@@ -88,6 +88,9 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 128));
     MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 128));
     MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 128));
+    MAP(tmap_2d_store32(&p.mG, Gs, I, P));
+    MAP(tmap_2d_store32(&p.mU, Us, I, P));
+    MAP(tmap_2d_store32(&p.mAct, Act, I, P));
     p.pl = pl;
     p.err = pl.err;
     p.G = Gs;
@@ -109,6 +112,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.pl = pl;
     p.err = pl.err;
     p.O = O;
+    MAP(tmap_2d_store32(&p.mO, O, H, P));
     p.Z2 = Z2;
     p.H = d->H;
     p.I = d->I;
@@ -127,6 +131,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.pl = pl;
     p.err = pl.err;
     p.Yl = Yl;
+    MAP(tmap_2d_store32(&p.mYl, Yl, H, T));
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;

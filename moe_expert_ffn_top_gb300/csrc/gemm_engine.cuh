@@ -42,13 +42,15 @@ namespace moelora {
 constexpr int kBK = 64;
 constexpr int kBStageBytes = 256 * 128;  // 32 KB: up to 256 rows x 64 bf16
 constexpr int kAccCols = 256;
-// Per epilogue warp: a 32-row staging buffer used to turn row-per-thread
-// accumulator data into coalesced row segments (pitch 17 words for bf16 rows,
-// 33 for fp32 rows: conflict-free row writes either way).
+// Per epilogue warp: a 4 KB staging buffer (1024-byte aligned) used to turn
+// row-per-thread accumulator data into coalesced row segments: bf16 rows at a pitch
+// of 17 words, fp32 rows at 32 words with the column index XORed by the row (both
+// conflict-free), or two 2 KB tiles of 32 x 32 bf16 for TMA stores.
 constexpr int kStgPitch = 17;
-constexpr int kStgPitchF32 = 33;
-constexpr int kStgWordsPerWarp = 32 * kStgPitchF32;
-constexpr int kGemmSmemBytes = 192 * 1024 + 1024 + 256 + 8 * kStgWordsPerWarp * 4;
+constexpr int kStgWordsPerWarp = 1024;
+constexpr int kStgBytes = 8 * kStgWordsPerWarp * 4;
+// pipeline stages (at most 192 KB), staging, barriers, and slack to align the base
+constexpr int kGemmSmemBytes = 192 * 1024 + kStgBytes + 256 + 1024;
 
 // Per-problem pipeline shape.  Narrow problems: 128-row tiles, 4 stages of
 // (A 16 KB + B 32 KB), two TMEM accumulators (the epilogue of one tile overlaps the
@@ -91,12 +93,12 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
   static_assert(!P::kWide || (P::kEpiWarps == 8 && !P::kAmn), "wide tiles: 8 epilogue warps, K-major A");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStage + kStgBytes);
   uint64_t* empty = full + S::kStages;
   uint64_t* tfull = empty + S::kStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + S::kStages * S::kStage + 256);
+  uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + S::kStages * S::kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = p.err;
 
@@ -229,6 +231,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_kernel(const _
         aph ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group<0>();  // epilogue TMA stores complete before exit
   }
   __syncthreads();
   if (warp == 1) {

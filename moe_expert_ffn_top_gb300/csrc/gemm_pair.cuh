@@ -54,12 +54,12 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(co
   static_assert(P::kEpiWarps == 4 || P::kEpiWarps == 8, "4 or 8 epilogue warps");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStage + kStgBytes);
   uint64_t* empty = full + kPairStages;
   uint64_t* tfull = empty + kPairStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + kPairStages * kPairStage + 256);
+  uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + kPairStages * kPairStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(co
         aph ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group<0>();  // epilogue TMA stores complete before exit
   }
   __syncthreads();
   tc_fence_before();

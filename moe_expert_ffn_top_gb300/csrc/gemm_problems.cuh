@@ -257,18 +257,59 @@ __device__ __forceinline__ void warp_store_rows_bf16(uint16_t* dst0, int64_t ld,
 __device__ __forceinline__ void warp_store_rows_f32(float* dst0, int64_t ld, int nvalid, const float (&v)[32],
                                                     float mul, int n, uint32_t* stg) {
   const int lane = threadIdx.x & 31;
+  // row i, column j at word 32 i + (j ^ i): conflict-free row writes and reads
 #pragma unroll
-  for (int j = 0; j < 32; ++j) stg[lane * kStgPitchF32 + j] = __float_as_uint(v[j] * mul);
+  for (int j = 0; j < 32; ++j) stg[lane * 32 + (j ^ lane)] = __float_as_uint(v[j] * mul);
   __syncwarp();
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const int r = s * 4 + (lane >> 3), w = (lane & 7) * 4;
-    const uint32_t* src = stg + r * kStgPitchF32 + w;
-    const uint4 u = make_uint4(src[0], src[1], src[2], src[3]);
+    const uint32_t* src = stg + r * 32;
+    const uint4 u = make_uint4(src[w ^ r], src[(w + 1) ^ r], src[(w + 2) ^ r], src[(w + 3) ^ r]);
     if (r < nvalid && w < n) *reinterpret_cast<uint4*>(dst0 + (int64_t)r * ld + w) = u;
   }
   __syncwarp();
 }
+
+// Epilogue stores through TMA: the warp writes its 32 rows x 32 bf16 columns into
+// one of two 2 KB staging tiles (64-byte swizzle, conflict-free), one lane issues
+// the bulk tensor store, and the warp goes on while the copy engine writes the
+// rows out.  A tile is rewritten only after the store that last read it has
+// finished reading.  Constructed once per tile epilogue (waits for the warp's
+// earlier stores to finish reading the staging tiles).
+constexpr bool kEpiTmaStore = true;
+struct TmaStoreRing {
+  uint8_t* base;
+  int cur;
+  __device__ __forceinline__ explicit TmaStoreRing(uint32_t* stg) : base(reinterpret_cast<uint8_t*>(stg)), cur(0) {
+    if ((threadIdx.x & 31) == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+  }
+  // rows y0..y0+31 (one per lane), columns x0..x0+31 of the tensor of map m: v * mul
+  __device__ __forceinline__ void store_bf16(const CUtensorMap* m, int x0, int y0, const float (&v)[32],
+                                             float mul = 1.0f) {
+    const int lane = threadIdx.x & 31;
+    uint8_t* buf = base + cur * 2048;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 q;
+      q.x = pack_bf16x2(v[8 * j + 0] * mul, v[8 * j + 1] * mul);
+      q.y = pack_bf16x2(v[8 * j + 2] * mul, v[8 * j + 3] * mul);
+      q.z = pack_bf16x2(v[8 * j + 4] * mul, v[8 * j + 5] * mul);
+      q.w = pack_bf16x2(v[8 * j + 6] * mul, v[8 * j + 7] * mul);
+      *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = q;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(m, buf, x0, y0);
+      bulk_commit_group();
+    }
+    cur ^= 1;
+  }
+};
 
 // Issues the coalesced global loads of a warp's 32 rows x 32 bf16 columns.
 __device__ __forceinline__ void warp_load_rows_issue(const uint16_t* src0, int64_t ld, uint4 (&u)[4]) {
@@ -372,6 +413,7 @@ struct ProbW13 {
   static constexpr int kEpiWarps = kWide ? 8 : 4;
   CUtensorMap mXp, mY13p, mW1, mW3, mB1, mB3;  // Xp (H,P) box(64,128); Y13p (2r,P) box(64,128);
                                                // W1/W3 (H,I,E) box(64,128,1); B1/B3 (r,I,G) box(64,128,1)
+  CUtensorMap mG, mU, mAct;                    // outputs (I,P), 32 x 32 store boxes
   PlanView pl;
   int* err;
   uint16_t *G, *U, *Act;
@@ -423,15 +465,23 @@ struct ProbW13 {
     return MmaStep{128, half * 128, 0, 0};
   }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    const int64_t base = ((int64_t)ti.m0 + row - (threadIdx.x & 31)) * I + ti.n0;  // warp's first row
+    const int y0 = ti.m0 + row - (threadIdx.x & 31);  // warp's first row
+    TmaStoreRing out(stg);
+    const int64_t base = (int64_t)y0 * I + ti.n0;
     for (int c = c0; c < 128; c += cs) {
       float g[32], u[32], a[32];
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
       act_fwd_chunk(act, clamp, g, u, a);
-      warp_store_rows_bf16(G + base + c, I, 32, g, 1.0f, stg);
-      warp_store_rows_bf16(U + base + c, I, 32, u, 1.0f, stg);
-      warp_store_rows_bf16(Act + base + c, I, 32, a, 1.0f, stg);
+      if (kEpiTmaStore) {
+        out.store_bf16(&mG, ti.n0 + c, y0, g);
+        out.store_bf16(&mU, ti.n0 + c, y0, u);
+        out.store_bf16(&mAct, ti.n0 + c, y0, a);
+      } else {
+        warp_store_rows_bf16(G + base + c, I, 32, g, 1.0f, stg);
+        warp_store_rows_bf16(U + base + c, I, 32, u, 1.0f, stg);
+        warp_store_rows_bf16(Act + base + c, I, 32, a, 1.0f, stg);
+      }
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
@@ -447,6 +497,7 @@ struct ProbW2 {
   static constexpr int kEpiWarps = 4;
   static constexpr bool kWide = false;  // 256-row tiles measured slower: K = I is short
   CUtensorMap mAct, mW2, mA2;  // Act (I,P) box(64,128); W2 (I,H,E) box(64,256,1); A2 (I,r,G) box(64,r16,1)
+  CUtensorMap mO;              // output (H,P), 32 x 32 store boxes
   PlanView pl;
   int* err;
   uint16_t *O, *Z2;
@@ -482,12 +533,17 @@ struct ProbW2 {
   }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t p = (int64_t)ti.m0 + row;
+    TmaStoreRing out(stg);  // before any use of the staging buffer
     if (!ti.sub) {
-      uint16_t* o0 = O + (p - (threadIdx.x & 31)) * H + ti.n0;  // warp's first row
+      const int y0 = (int)(p - (threadIdx.x & 31));  // warp's first row
+      uint16_t* o0 = O + (int64_t)y0 * H + ti.n0;
       for (int c = c0; c < 256; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
-        warp_store_rows_bf16(o0 + c, H, 32, v, 1.0f, stg);
+        if (kEpiTmaStore)
+          out.store_bf16(&mO, ti.n0 + c, y0, v);
+        else
+          warp_store_rows_bf16(o0 + c, H, 32, v, 1.0f, stg);
       }
     } else {
       for (int c = c0; c < r; c += cs) {
@@ -513,6 +569,7 @@ struct ProbB2Expand {
   static constexpr int kEpiWarps = 8;  // store-bound epilogue: two warps per lane quarter keep more stores in flight
   static constexpr bool kWide = false;
   CUtensorMap mZ2w, mB2;  // Z2w (r,T) box(64,128); B2 (r,H,A) box(64,256,1)
+  CUtensorMap mYl;        // output (H,T), 32 x 32 store boxes
   PlanView pl;
   int* err;
   uint16_t* Yl;
@@ -546,10 +603,18 @@ struct ProbB2Expand {
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t t0 = (int64_t)ti.m0 + row - (threadIdx.x & 31);  // warp's first row
     const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
+    // A tile ends early only at the last token: adapters start on 128-token
+    // boundaries, so a whole-box store never reaches another adapter's rows, and
+    // the map clips rows past T.
+    TmaStoreRing out(stg);
     for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      warp_store_rows_bf16(Yl + t0 * H + ti.n0 + c, H, nvalid, v, s, stg);
+      if (nvalid <= 0) continue;
+      if (kEpiTmaStore)
+        out.store_bf16(&mYl, ti.n0 + c, (int)t0, v, s);
+      else
+        warp_store_rows_bf16(Yl + t0 * H + ti.n0 + c, H, nvalid, v, s, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
@@ -735,7 +800,8 @@ struct ProbW2Dgrad {
     const int rt = pl.route_of_row[p];
     const bool live = rt >= 0;
     const float w = live ? topk_w[rt] : 0.0f;
-    const int64_t base0 = (p - (threadIdx.x & 31)) * I + ti.n0;  // warp's first row
+    const int y0 = (int)(p - (threadIdx.x & 31));  // warp's first row
+    const int64_t base0 = (int64_t)y0 * I + ti.n0;
     float dot = 0.0f;
     for (int c = c0; c < 256; c += cs) {
       // the chunk's saved G, U and activation: coalesced loads, all in flight,
@@ -757,6 +823,7 @@ struct ProbW2Dgrad {
       warp_rows_to_lane(lu, stg, u);
       float og[32], ou[32];
       act_bwd_chunk(act, clamp, q, g, u, w, live, og, ou);
+      // staged warp stores: this epilogue's loads already use the staging buffer
       warp_store_rows_bf16(dG + base0 + c, I, 32, og, 1.0f, stg);
       warp_store_rows_bf16(dU + base0 + c, I, 32, ou, 1.0f, stg);
     }
@@ -832,6 +899,7 @@ struct ProbW13Dgrad {
   static constexpr bool kAmn = false, kBmn = true;
   static constexpr int kEpiWarps = 8;
   static constexpr bool kWide = true;
+  CUtensorMap mdXp;                          // output (H,P), 32 x 32 store boxes
   CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1);
                                              // B1/B3 (r,I,G) box(64,64,1)
   PlanView pl;
@@ -884,12 +952,17 @@ struct ProbW13Dgrad {
   }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t p = (int64_t)ti.m0 + row;
+    TmaStoreRing out(stg);  // before any use of the staging buffer
     if (!ti.sub) {
-      uint16_t* o0 = dXp + (p - (threadIdx.x & 31)) * H + ti.n0;  // warp's first row
+      const int y0 = (int)(p - (threadIdx.x & 31));  // warp's first row
+      uint16_t* o0 = dXp + (int64_t)y0 * H + ti.n0;
       for (int c = c0; c < 256; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
-        warp_store_rows_bf16(o0 + c, H, 32, v, 1.0f, stg);
+        if (kEpiTmaStore)
+          out.store_bf16(&mdXp, ti.n0 + c, y0, v);
+        else
+          warp_store_rows_bf16(o0 + c, H, 32, v, 1.0f, stg);
       }
     } else {
       float* o0 = dY13 + (p - (threadIdx.x & 31)) * (2 * r);  // warp's first row
@@ -979,6 +1052,7 @@ struct ProbA13Expand {
   static constexpr int kEpiWarps = 8;  // store-bound epilogue: two warps per lane quarter keep more stores in flight
   static constexpr bool kWide = false;
   CUtensorMap mdY13w, mA1, mA3;  // dY13w (2r,T) box(64,128); A1/A3 (H,r,A) box(64,64,1)
+  CUtensorMap mdXl;               // output (H,T), 32 x 32 store boxes
   PlanView pl;
   int* err;
   uint16_t* dXl;
@@ -1015,10 +1089,15 @@ struct ProbA13Expand {
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t t0 = (int64_t)ti.m0 + row - (threadIdx.x & 31);  // warp's first row
     const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
+    TmaStoreRing out(stg);  // whole-box stores: see ProbB2Expand
     for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      warp_store_rows_bf16(dXl + t0 * H + ti.n0 + c, H, nvalid, v, 1.0f, stg);
+      if (nvalid <= 0) continue;
+      if (kEpiTmaStore)
+        out.store_bf16(&mdXl, ti.n0 + c, (int)t0, v);
+      else
+        warp_store_rows_bf16(dXl + t0 * H + ti.n0 + c, H, nvalid, v, 1.0f, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}

@@ -10,6 +10,10 @@ namespace moelora {
 // 2D tensor [outer][inner]; box of box_inner x box_outer elements.  Returns 0 on success.
 int tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
             uint32_t box_outer);
+// 2D bf16 tensor [outer][inner] for epilogue TMA stores: 32 x 32 boxes (64-byte
+// rows) with the 64-byte swizzle of the staging tiles (16-byte chunk j of row i
+// sits at chunk j ^ ((i >> 1) & 3)).
+int tmap_2d_store32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer);
 // 3D tensor [d2][d1][d0]; box of b0 x b1 x 1.
 int tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1);
 

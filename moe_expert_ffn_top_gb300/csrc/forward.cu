@@ -103,8 +103,22 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.clamp = d->act_clamp;
     LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13));
   }
-  // F4/F5: W2 + expert-local A2 shrink (two-SM tiles)
-  {
+  // F4/F5: W2 + expert-local A2 shrink
+  if (kW2OneSmWide) {
+    ProbW2 p;
+    MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
+    MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 256));
+    MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, (uint32_t)((r + 15) / 16 * 16)));
+    MAP(tmap_2d_store32(&p.mO, O, H, P));
+    p.pl = pl;
+    p.err = pl.err;
+    p.O = O;
+    p.Z2 = Z2;
+    p.H = d->H;
+    p.I = d->I;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W2));
+  } else {
     ProbW2Pair p;
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
     MAP(tmap_3d(&p.mW2h, bW2, I, H, E, 64, 128));

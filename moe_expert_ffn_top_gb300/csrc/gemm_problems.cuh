@@ -492,10 +492,13 @@ struct ProbW13 {
 //   O = Act W2_e^T  [P,H] (unweighted),   Z2 = bf16(Act A2_ae^T) [P,r]
 // N tiles: H/256 base tiles over W2 rows, then one tile of round16(r) over A2 rows.
 // =====================================================================================
+// The forward W2 GEMM on the one-SM engine with 256-row tiles (true) or on the
+// two-SM engine (ProbW2Pair, false).
+constexpr bool kW2OneSmWide = true;
 struct ProbW2 {
   static constexpr bool kAmn = false, kBmn = false;
-  static constexpr int kEpiWarps = 4;
-  static constexpr bool kWide = false;  // 256-row tiles measured slower: K = I is short
+  static constexpr bool kWide = kW2OneSmWide;
+  static constexpr int kEpiWarps = kWide ? 8 : 4;
   CUtensorMap mAct, mW2, mA2;  // Act (I,P) box(64,128); W2 (I,H,E) box(64,256,1); A2 (I,r,G) box(64,r16,1)
   CUtensorMap mO;              // output (H,P), 32 x 32 store boxes
   PlanView pl;
@@ -503,10 +506,13 @@ struct ProbW2 {
   uint16_t *O, *Z2;
   int H, I, r;
   __device__ int ntn() const { return H / 256 + 1; }
-  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ int num_tiles() const {
+    return (kWide ? pl.wtile_off[pl.G] : pl.offsets[pl.G] / 128) * ntn();
+  }
   __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
-    const int nt = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
+    const int nt = kWide ? wide_entry_decode(nmajor_wide_fetch(pl, t, ntn()), ti)
+                         : nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
     ti.sub = nt == H / 256;
     ti.n0 = ti.sub ? 0 : nt * 256;
     ti.nk = I / kBK;

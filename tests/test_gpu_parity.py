@@ -248,6 +248,23 @@ def test_empty_batch():
         assert t.abs().max().item() == 0, n
 
 
+def test_all_routes_masked():
+    """Every route masked (ids all -1): no routed rows (P = 0, the grouped GEMMs have no
+    tiles) while the per-token kernels still run; y, dx, dw and all six adapter
+    gradients are exactly zero, and the oracle agrees."""
+    shp = Shape(T=200, H=512, I=256, E=16, k=2, r=16)
+    inp = make_inputs(shp, seed=31)
+    inp["topk_ids"] = torch.full_like(inp["topk_ids"], -1)
+    out = run_gpu(inp, shp, poison=True)
+    assert out["err"] == 0
+    got = m.moe_lora_plan_readback(out["dims"], out["ws"].plan)
+    assert int(got["offsets"][-1]) == 0 and int(got["counts"].sum()) == 0
+    for n in ("y", "dx", "dw") + ADAPTER_GRADS:
+        assert out[n].abs().max().item() == 0, n
+    y_ref = oracle.forward(inp, shp)
+    assert y_ref.abs().max().item() == 0
+
+
 # ----------------------------------------------------------------------------- production width
 def _sampled_check(inp, shp, out, sample):
     """Sparse-dy parity: dy is zero outside `sample`, so every gradient only has

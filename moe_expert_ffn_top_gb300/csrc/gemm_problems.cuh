@@ -277,6 +277,9 @@ __device__ __forceinline__ void warp_store_rows_f32(float* dst0, int64_t ld, int
 // rows out.  A tile is rewritten only after the store that last read it has
 // finished reading.  Constructed once per tile epilogue (waits for the warp's
 // earlier stores to finish reading the staging tiles).
+// TMA stores for the large bf16 epilogue outputs (false: the staged warp stores).
+// Same box, 65,536 tokens: step 31.9 -> 30.8 ms, W13 8.79 -> 8.31 ms, W13 dgrad
+// 8.70 -> 7.93 ms.
 constexpr bool kEpiTmaStore = true;
 struct TmaStoreRing {
   uint8_t* base;
@@ -493,7 +496,8 @@ struct ProbW13 {
 // N tiles: H/256 base tiles over W2 rows, then one tile of round16(r) over A2 rows.
 // =====================================================================================
 // The forward W2 GEMM on the one-SM engine with 256-row tiles (true) or on the
-// two-SM engine (ProbW2Pair, false).
+// two-SM engine (ProbW2Pair, false).  With the TMA-store epilogue: 4.22 vs 4.47 ms
+// (same box, 65,536 tokens, E256).
 constexpr bool kW2OneSmWide = true;
 struct ProbW2 {
   static constexpr bool kAmn = false, kBmn = false;

@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -99,11 +100,17 @@ GEMM_SOURCES = ("sm100_ptx.cuh", "common.cuh", "gemm_engine.cuh", "gemm_pair.cuh
 
 
 def src_hash():
+    """Hash of the GEMM sources' code: comments and blank lines removed, so an edit to
+    comments alone keeps the committed counters valid."""
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
-        with open(os.path.join(ROOT, "moe_expert_ffn_top_gb300", "csrc", f), "rb") as fh:
-            h.update(f.encode())
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "moe_expert_ffn_top_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(f.encode())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

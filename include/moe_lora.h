@@ -276,8 +276,9 @@ MOE_LORA_API const char* moe_lora_strerror(int code);
  * are reported through moe_lora_gemm_selftest_error(). */
 MOE_LORA_API int moe_lora_gemm_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn, const uint16_t* B,
                            int32_t b_mn, float* C, void* stream);
-/* The same plain GEMM on the two-SM engine the W2 expert GEMM uses: clusters of
- * two CTAs sharing each 256-row tile through tcgen05.mma.cta_group::2 (an odd last
+/* The same plain GEMM on the two-SM engine (the forward W2 expert GEMM's alternative
+ * form): clusters of two CTAs sharing each 256-row tile through
+ * tcgen05.mma.cta_group::2 (an odd last
  * 128-row tile runs on one CTA of the pair).  Same arguments, rules and error
  * reporting as moe_lora_gemm_selftest. */
 MOE_LORA_API int moe_lora_gemm_pair_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,

@@ -151,6 +151,17 @@ def test_tiny_forward_backward(T, mask):
     _full_check(inp, shp, out)
 
 
+@pytest.mark.parametrize("r", [24, 40, 64, 72, 120])
+def test_ranks_off_the_tile_boundaries(r):
+    """Ranks that are not multiples of 16, 32 or 64 (and 64 itself): partial MMA N
+    widths, zero-filled TMA boxes and partial store chunks on every side path."""
+    shp = Shape(T=150, H=512, I=256, E=8, k=2, r=r, mask_frac=0.1, scale=0.5)
+    inp = make_inputs(shp, seed=40 + r)
+    out = run_gpu(inp, shp, poison=True)
+    assert out["err"] == 0
+    _full_check(inp, shp, out)
+
+
 def test_saturated_gates():
     """x scaled by 64: gate pre-activations reach the hundreds, so silu sits at its
     limits (exp(-z) overflows to inf for z < -88, giving 0; z for large z) in the

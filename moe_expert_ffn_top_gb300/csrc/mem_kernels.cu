@@ -221,13 +221,18 @@ __global__ void combine_rows_kernel(PlanView pl, const uint16_t* __restrict__ ba
   const int k = pl.k;
   for (int64_t t = w0; t < pl.T; t += nw) {
     const int* rows = pl.row_of_route + t * k;
-    for (int c = lane * 8; c < H; c += 32 * 8) {
-      float acc[8];
+    // two 8-column groups per lane and pass (c and c + 256; H % 256 == 0), so up to
+    // 2 x 8 routed-row loads are in flight before they are added in slot order
+    for (int c = lane * 8; c < H; c += 2 * 32 * 8) {
+      const int c2 = c + 32 * 8;
+      const bool two = c2 < H;
+      float acc[8], acc2[8];
       ld_bf16x8(base + t * H + c, acc);
+      if (two) ld_bf16x8(base + t * H + c2, acc2);
       for (int j0 = 0; j0 < k; j0 += 8) {
         int R[8];
         float w[8];
-        uint4 u[8];
+        uint4 u[8], u2[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const bool in = j0 + j < k;
@@ -235,20 +240,27 @@ __global__ void combine_rows_kernel(PlanView pl, const uint16_t* __restrict__ ba
           w[j] = (in && topk_w) ? topk_w[t * k + j0 + j] : 1.0f;
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          u[j] = R[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)R[j] * H + c)) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 8; ++j) {
+          const uint4* rp = reinterpret_cast<const uint4*>(src + (R[j] >= 0 ? (int64_t)R[j] * H : 0));
+          u[j] = R[j] >= 0 ? __ldg(rp + c / 8) : make_uint4(0, 0, 0, 0);
+          u2[j] = (R[j] >= 0 && two) ? __ldg(rp + c2 / 8) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (R[j] < 0) continue;
           const uint32_t wd[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+          const uint32_t wd2[4] = {u2[j].x, u2[j].y, u2[j].z, u2[j].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             acc[2 * e] += w[j] * bf16_lo(wd[e]);
             acc[2 * e + 1] += w[j] * bf16_hi(wd[e]);
+            acc2[2 * e] += w[j] * bf16_lo(wd2[e]);
+            acc2[2 * e + 1] += w[j] * bf16_hi(wd2[e]);
           }
         }
       }
       st_bf16x8(out + t * H + c, acc);
+      if (two) st_bf16x8(out + t * H + c2, acc2);
     }
   }
 }

@@ -12,6 +12,9 @@ namespace moelora {
 namespace {
 
 constexpr int kThreads = 256;
+// 16-byte loads per lane in flight per pass of the routed-row scatters (4,096 bf16
+// columns: a whole production-width row)
+constexpr int kGatherVec = 16;
 
 __device__ __forceinline__ void copy_row_or_zero(uint16_t* dst, const uint16_t* src, int n, int lane) {
   // n bf16 (multiple of 8), 16 B per lane per step
@@ -46,10 +49,10 @@ __global__ void gather_fwd_kernel(PlanView pl, const uint16_t* __restrict__ x, c
   const int k = pl.k;
   for (int64_t t = w0; t < pl.T; t += nw) {
     const int* rows = pl.row_of_route + t * k;
-    for (int c0 = 0; c0 < H; c0 += 32 * 8 * 8) {  // 2048 columns per pass: 8 x 16 B per lane
-      uint4 v[8];
+    for (int c0 = 0; c0 < H; c0 += 32 * 8 * kGatherVec) {  // kGatherVec x 16 B per lane and pass
+      uint4 v[kGatherVec];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < kGatherVec; ++i) {
         const int c = c0 + (i * 32 + lane) * 8;
         v[i] = c < H ? __ldg(reinterpret_cast<const uint4*>(x + t * H + c)) : make_uint4(0, 0, 0, 0);
       }
@@ -57,7 +60,7 @@ __global__ void gather_fwd_kernel(PlanView pl, const uint16_t* __restrict__ x, c
         const int R = rows[j];
         if (R < 0) continue;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kGatherVec; ++i) {
           const int c = c0 + (i * 32 + lane) * 8;
           if (c < H) *reinterpret_cast<uint4*>(Xp + (int64_t)R * H + c) = v[i];
         }
@@ -114,10 +117,10 @@ __global__ void gather_bwd_kernel(PlanView pl, const uint16_t* __restrict__ dy, 
   const int k = pl.k;
   for (int64_t t = w0; t < pl.T; t += nw) {
     const int* rows = pl.row_of_route + t * k;
-    for (int c0 = 0; c0 < H; c0 += 32 * 8 * 8) {
-      uint4 v[8];
+    for (int c0 = 0; c0 < H; c0 += 32 * 8 * kGatherVec) {
+      uint4 v[kGatherVec];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < kGatherVec; ++i) {
         const int c = c0 + (i * 32 + lane) * 8;
         v[i] = c < H ? __ldg(reinterpret_cast<const uint4*>(dy + t * H + c)) : make_uint4(0, 0, 0, 0);
       }
@@ -125,7 +128,7 @@ __global__ void gather_bwd_kernel(PlanView pl, const uint16_t* __restrict__ dy, 
         const int R = rows[j];
         if (R < 0) continue;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kGatherVec; ++i) {
           const int c = c0 + (i * 32 + lane) * 8;
           if (c < H) *reinterpret_cast<uint4*>(Dp + (int64_t)R * H + c) = v[i];
         }

@@ -134,15 +134,19 @@ __global__ void gather_bwd_kernel(PlanView pl, const uint16_t* __restrict__ dy, 
         }
       }
     }
-    for (int q = lane; q < r; q += 32) {
-      const float v = __uint_as_float((uint32_t)dyB2[t * r + q] << 16);
-      __nv_bfloat16 a = __float2bfloat16_rn(s * v);
+    for (int q = lane * 8; q < r; q += 32 * 8) {  // 8 columns per lane (r % 8 == 0)
+      float v[8], a[8], b[8];
+      ld_bf16x8(dyB2 + t * r + q, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = s * v[i];
       for (int j = 0; j < k; ++j) {
         const int R = rows[j];
         if (R < 0) continue;
-        __nv_bfloat16 b = __float2bfloat16_rn(s * topk_w[t * k + j] * v);
-        D2p[(int64_t)R * r + q] = *reinterpret_cast<uint16_t*>(&a);
-        dZ2p[(int64_t)R * r + q] = *reinterpret_cast<uint16_t*>(&b);
+        const float sw = s * topk_w[t * k + j];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = sw * v[i];
+        st_bf16x8(D2p + (int64_t)R * r + q, a);
+        st_bf16x8(dZ2p + (int64_t)R * r + q, b);
       }
     }
   }

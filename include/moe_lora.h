@@ -206,6 +206,18 @@ MOE_LORA_API int moe_lora_plan_readback(const moe_lora_dims* dims, const void* p
                                         int32_t* offsets, int32_t* row_of_route, int32_t* route_of_row,
                                         int64_t route_of_row_cap, void* stream);
 
+/* Decodes an MXFP4 tensor (the frozen-base format of moe_lora_dims.base_fmt = 1) to
+ * bf16, exactly, on `stream`: elems E2M1 codes (two per byte, the lower index in the
+ * low nibble; bit 3 = sign, magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}) with one UE8M0
+ * scale byte per 32 consecutive elements (b -> 2^(b-127); b = 0 gives 2^-127, b = 255
+ * NaN).  Every decoded value is a bf16 value (no rounding), overflowing to +-inf at
+ * the largest scales.  The forward runs the same decode on W1, W3 and W2 (PR #9:
+ * "MXFP4-dequantized BF16" base).
+ *   packed [elems/2] uint8 and out [elems] bf16, device, 16-byte aligned; scales
+ *   [elems/32] uint8, device.  elems % 32 == 0 (MOE_LORA_ERR_DIMS otherwise). */
+MOE_LORA_API int moe_lora_mxfp4_decode(const uint8_t* packed, const uint8_t* scales, uint16_t* out, int64_t elems,
+                                       void* stream);
+
 /* Per-kernel timing of this library's own launches, for profiling and the
  * benchmark's roofline figures (off by default).  When on, every kernel launch is
  * bracketed by a CUDA event pair recorded on its launch stream. */

@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_gemm_starved_selftest.restype = ctypes.c_int
         L.moe_lora_gemm_starved_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P,
                                                      ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_int32, P]
+        L.moe_lora_mxfp4_decode.restype = ctypes.c_int
+        L.moe_lora_mxfp4_decode.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                             ctypes.c_void_p]
         L.moe_lora_profile_enable.restype = ctypes.c_int
         L.moe_lora_profile_enable.argtypes = [ctypes.c_int]
         L.moe_lora_profile_read.restype = ctypes.c_int
@@ -321,6 +324,16 @@ def moe_lora_gemm_starved_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor,
 
 def moe_lora_gemm_selftest_error(stream=None) -> int:
     return lib().moe_lora_gemm_selftest_error(_stream(stream))
+
+
+def moe_lora_mxfp4_decode(packed: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """MXFP4 (packed E2M1 pairs + one UE8M0 per 32) -> bf16 `out`, exactly, on the device."""
+    elems = out.numel()
+    if packed.numel() * 2 != elems or scales.numel() * 32 != elems:
+        raise ValueError("packed must hold elems/2 bytes and scales elems/32 bytes")
+    _check(lib().moe_lora_mxfp4_decode(_ptr(packed, torch.uint8, "packed"), _ptr(scales, torch.uint8, "scales"),
+                                       _ptr(out, torch.bfloat16, "out"), elems, _stream(stream)),
+           "moe_lora_mxfp4_decode")
 
 
 def moe_lora_profile_enable(on: bool) -> None:

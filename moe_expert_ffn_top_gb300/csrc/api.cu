@@ -309,6 +309,20 @@ static int selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t 
   return run_plain_gemm(M, N, K, A, a_mn, B, b_mn, C, err, sms, pair, starve, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int moe_lora_mxfp4_decode(const uint8_t* packed, const uint8_t* scales, uint16_t* out, int64_t elems,
+                                     void* stream) {
+  if (elems < 0 || elems % 32) return MOE_LORA_ERR_DIMS;
+  if (elems == 0) return MOE_LORA_OK;
+  int rc;
+  if ((rc = check_ptr(packed)) || (rc = check_ptr(out))) return rc;
+  if (!scales) return MOE_LORA_ERR_NULL;
+  int sms = 0;
+  if ((rc = device_sms(&sms))) return rc;
+  return launch_dequant_mxfp4(packed, scales, out, elems, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_LORA_OK
+             : MOE_LORA_ERR_CUDA;
+}
+
 extern "C" int moe_lora_gemm_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
                                       const uint16_t* B, int32_t b_mn, float* C, void* stream) {
   return selftest(M, N, K, A, a_mn, B, b_mn, C, 0, 0, stream);

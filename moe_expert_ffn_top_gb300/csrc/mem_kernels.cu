@@ -4,6 +4,8 @@
 // per-token reductions over the k
 // routes of a token (fixed slot order, fp32, one bf16 rounding).
 // All use 16-byte vector accesses, one warp per row, grid-stride over rows.
+#include <cuda_fp16.h>
+
 #include "launch.h"
 #include "prof.h"
 
@@ -272,31 +274,63 @@ __global__ void combine_rows_kernel(PlanView pl, const uint16_t* __restrict__ ba
   }
 }
 
-// MXFP4 -> bf16, exactly: one thread per 32-element scale group (16 packed bytes
-// and one UE8M0 byte in, 64 bytes of bf16 out).  E2M1 magnitudes are
+// MXFP4 -> bf16, exactly (32-element groups: 16 packed bytes and one UE8M0 byte in,
+// 64 bytes of bf16 out; see the kernel for the thread mapping).  E2M1 magnitudes are
 // {0, 0.5, 1, 1.5, 2, 3, 4, 6} (bit 3 = sign); the scale byte b means 2^(b-127)
 // (b = 0 is the fp32 subnormal 2^-127, b = 255 is NaN).  Every product is a bf16
 // value, so the conversion below rounds nothing.
+// Two E2M1 codes (one byte, the lower index in the low nibble) to two f16 values
+// (low half = low nibble) with the hardware conversion; every E2M1 value is exact in
+// f16.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(d) : "h"((uint16_t)byte));
+  return d;
+}
+constexpr bool kDequantCvt = true;  // false: decode the codes with a magnitude table
+
 __global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                                      uint16_t* __restrict__ out, int64_t groups) {
   const float kMag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-  for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
-       gi += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 pk = __ldg(reinterpret_cast<const uint4*>(packed) + gi);
-    const uint32_t b = scales[gi];
-    const float sc = __uint_as_float(b == 0 ? 0x00400000u : b == 255 ? 0x7FC00000u : b << 23);
-    const uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
-    uint16_t* dst = out + gi * 32;
+  // one thread per 8 elements (4 packed bytes in, 16 bytes of bf16 out), so a warp
+  // reads 128 and writes 512 contiguous bytes per step; 4 consecutive threads share
+  // one 32-element scale group
+  // Each thread takes kBatch such items a grid stride apart and issues all their
+  // loads before decoding any, so a warp keeps kBatch x 128 B of reads in flight.
+  constexpr int kBatch = 8;
+  const int64_t n8 = groups * 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n8; i0 += stride * kBatch) {
+    uint32_t w[kBatch], b[kBatch];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t i = i0 + u * stride;
+      w[u] = i < n8 ? __ldg(reinterpret_cast<const uint32_t*>(packed) + i) : 0u;
+      b[u] = i < n8 ? scales[i >> 2] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= n8) break;
+      const float sc = __uint_as_float(b[u] == 0 ? 0x00400000u : b[u] == 255 ? 0x7FC00000u : b[u] << 23);
       float v[8];
+      if (kDequantCvt) {
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const uint32_t code = (w[q] >> (4 * n)) & 15u;
-        const float mag = kMag[code & 7u] * sc;
-        v[n] = (code & 8u) ? -mag : mag;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t h2 = e2m1x2_to_f16x2((w[u] >> (8 * j)) & 0xFFu);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          v[2 * j] = f.x * sc;
+          v[2 * j + 1] = f.y * sc;
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const uint32_t code = (w[u] >> (4 * n)) & 15u;
+          const float mag = kMag[code & 7u] * sc;
+          v[n] = (code & 8u) ? -mag : mag;
+        }
       }
-      st_bf16x8(dst + 8 * q, v);
+      st_bf16x8(out + i * 8, v);
     }
   }
 }

@@ -424,6 +424,25 @@ def _decode_mxfp4_golden(packed, scales):
     return (table[codes] * sc).to(torch.bfloat16)
 
 
+def test_mxfp4_decode_every_code_and_scale():
+    """The decode kernel on all 256 packed bytes (every pair of E2M1 codes, -0 included)
+    under scale bytes from the subnormal 2^-127 to overflow, against the OCP table,
+    bit for bit; scale byte 255 decodes to NaN."""
+    scale_bytes = [0, 1, 2, 60, 120, 126, 127, 128, 129, 200, 253, 254]
+    packed = torch.arange(256, dtype=torch.uint8).repeat(len(scale_bytes))  # 16 groups per scale
+    scales = torch.tensor(scale_bytes, dtype=torch.uint8).repeat_interleave(16)
+    want = _decode_mxfp4_golden(packed.view(1, -1), scales.view(1, -1)).view(-1)
+    got = torch.empty(packed.numel() * 2, dtype=torch.bfloat16, device="cuda")
+    m.moe_lora_mxfp4_decode(packed.cuda(), scales.cuda(), got)
+    torch.cuda.synchronize()
+    assert torch.equal(got.cpu().view(torch.int16), want.view(torch.int16))
+    nan = torch.empty(64, dtype=torch.bfloat16, device="cuda")
+    m.moe_lora_mxfp4_decode(torch.arange(32, dtype=torch.uint8).cuda(), torch.full((2,), 255, dtype=torch.uint8).cuda(),
+                            nan)
+    torch.cuda.synchronize()
+    assert torch.isnan(nan.float()).all()
+
+
 def test_mxfp4_tiny_forward_backward():
     shp = Shape(T=200, H=512, I=256, E=16, k=2, r=16, mask_frac=0.1, base_fmt="mxfp4")
     inp = make_inputs(shp, seed=31)

@@ -150,10 +150,24 @@ def test_router_rejections(L):
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_mxfp4_decode_rejections(L):
+    """The decode entry point rejects bad sizes and pointers on the host; a zero-size
+    call is a no-op that succeeds without a device."""
+    assert L.moe_lora_mxfp4_decode(FAKE, FAKE, FAKE, 48, None) == -2        # not a multiple of 32
+    assert L.moe_lora_mxfp4_decode(FAKE, FAKE, FAKE, -32, None) == -2
+    assert L.moe_lora_mxfp4_decode(None, FAKE, FAKE, 64, None) == -1
+    assert L.moe_lora_mxfp4_decode(FAKE, None, FAKE, 64, None) == -1
+    assert L.moe_lora_mxfp4_decode(FAKE, FAKE, None, 64, None) == -1
+    assert L.moe_lora_mxfp4_decode(FAKE + 4, FAKE, FAKE, 64, None) == -3    # packed not 16-byte aligned
+    assert L.moe_lora_mxfp4_decode(FAKE, FAKE, FAKE + 2, 64, None) == -3    # out not 16-byte aligned
+    assert L.moe_lora_mxfp4_decode(None, None, None, 0, None) == 0
+
+
 def test_no_device_is_reported(L):
     d = _dims()
     nbytes = m.moe_lora_workspace_bytes(d, 0)
     assert L.moe_lora_plan(ctypes.byref(d), FAKE, None, FAKE, nbytes, None) == -7
+    assert L.moe_lora_mxfp4_decode(FAKE, FAKE, FAKE, 64, None) == -7
 
 
 def test_strerror(L):

@@ -576,7 +576,8 @@ struct ProbW2 {
 // =====================================================================================
 struct ProbB2Expand {
   static constexpr bool kAmn = false, kBmn = false;
-  static constexpr int kEpiWarps = 8;  // store-bound epilogue: two warps per lane quarter keep more stores in flight
+  // 8 epilogue warps (TMA-store epilogue; same box: 0.109 vs 0.143 ms with 4)
+  static constexpr int kEpiWarps = 8;
   static constexpr bool kWide = false;
   CUtensorMap mZ2w, mB2;  // Z2w (r,T) box(64,128); B2 (r,H,A) box(64,256,1)
   CUtensorMap mYl;        // output (H,T), 32 x 32 store boxes
@@ -1062,7 +1063,8 @@ struct ProbDB13 {
 // =====================================================================================
 struct ProbA13Expand {
   static constexpr bool kAmn = false, kBmn = true;
-  static constexpr int kEpiWarps = 8;  // store-bound epilogue: two warps per lane quarter keep more stores in flight
+  // 4 epilogue warps (TMA-store epilogue; same box: 0.147 vs 0.160 ms with 8)
+  static constexpr int kEpiWarps = 4;
   static constexpr bool kWide = false;
   CUtensorMap mdY13w, mA1, mA3;  // dY13w (2r,T) box(64,128); A1/A3 (H,r,A) box(64,64,1)
   CUtensorMap mdXl;               // output (H,T), 32 x 32 store boxes

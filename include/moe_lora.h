@@ -154,23 +154,27 @@ MOE_LORA_API int moe_lora_plan(const moe_lora_dims* dims, const int32_t* topk_id
                   void* plan_ws, size_t plan_bytes, void* stream);
 
 /* Routing plan for callers that cannot allocate device memory.  The pages have no
- * counterpart to this entry point; it exists for callers that may not call
- * cudaMalloc (or any allocator) when they route tokens -- code running while a
- * stream is being captured into a CUDA graph, memory-planned serving runtimes that
- * only hand out pre-reserved buffers, C hosts without an allocator binding.
- * It writes exactly the plan moe_lora_plan() writes, but the per-chunk expert
- * histograms it needs as temporary space live in a fixed 4 MiB array inside the
- * library (a file-scope __device__ array that every GPU loading the library holds
- * until the process exits), so the caller passes only the plan buffer itself:
+ * counterpart to this entry point.  It exists for callers that may not call
+ * cudaMalloc (or any allocator) when they route tokens: memory-planned serving
+ * runtimes that reserve all device memory up front and hand out only
+ * pre-reserved buffers, and C hosts that hold device pointers but have no
+ * allocator binding of their own.
+ * It writes exactly the plan moe_lora_plan() writes, with the same launch
+ * sequence, but the per-chunk expert histograms it needs as temporary space live
+ * in a fixed 4 MiB array inside the library (a file-scope __device__ array that
+ * every GPU loading the library holds until the process exits), so the caller
+ * passes only the plan buffer itself:
  *   plan_bytes >= moe_lora_workspace_bytes(dims, MOE_LORA_WS_PLAN)
- *                 - 256 * ceil(4 * A * E * ceil(T*k / 1024) / 256)
+ *                 - 256 * ceil(4 * A * E * max(1, ceil(T*k / 1024)) / 256)
  * (a full MOE_LORA_WS_PLAN buffer also works).  Sizes with
- * A * E * ceil(T*k / 1024) > 1,048,576 are rejected with MOE_LORA_ERR_SCRATCH_LIMIT
- * before any launch.  Nothing is allocated or freed.
- * The first call on each device looks up the array's device address (with that
- * device current); make that first call before any stream capture begins.
- * All calls share the one array: calls whose work overlaps on the GPU (other
- * streams, other host threads) race on it and must be serialised by the caller.
+ * A * E * max(1, ceil(T*k / 1024)) > 1,048,576 are rejected with
+ * MOE_LORA_ERR_SCRATCH_LIMIT before any launch.  Nothing is allocated or freed.
+ * The first call in each CUDA context (for runtime-API callers: on each device,
+ * in its primary context) looks up the array's device address with that context
+ * current and caches it; make that first call before any stream capture begins.
+ * All calls share the one array and every call overwrites it: calls whose work
+ * overlaps on the GPU (other streams, other host threads) race on it and must be
+ * serialised by the caller.
  * Other arguments, checks and errors are those of moe_lora_plan(). */
 MOE_LORA_API int moe_lora_plan_noalloc(const moe_lora_dims* dims, const int32_t* topk_ids,
                                        const int64_t* adapter_offsets, void* plan_ws, size_t plan_bytes,
@@ -222,6 +226,11 @@ MOE_LORA_API int moe_lora_mxfp4_decode(const uint8_t* packed, const uint8_t* sca
  * benchmark's roofline figures (off by default).  When on, every kernel launch is
  * bracketed by a CUDA event pair recorded on its launch stream. */
 MOE_LORA_API int moe_lora_profile_enable(int on);
+/* Restricts the timing to the launches of one kernel (by the name that
+ * moe_lora_profile_read reports), so that the event pairs around every other
+ * launch do not slow the step down; NULL times every kernel again.  Returns
+ * MOE_LORA_ERR_DIMS for an unknown name. */
+MOE_LORA_API int moe_lora_profile_select(const char* kernel);
 /* Reads and resets the per-kernel totals since the last read: for each kernel
  * that ran (at most cap), its static name, total milliseconds and launch count.
  * Waits for the recorded events.  Returns how many entries were written, or a

@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_void_p]
         L.moe_lora_profile_enable.restype = ctypes.c_int
         L.moe_lora_profile_enable.argtypes = [ctypes.c_int]
+        L.moe_lora_profile_select.restype = ctypes.c_int
+        L.moe_lora_profile_select.argtypes = [ctypes.c_char_p]
         L.moe_lora_profile_read.restype = ctypes.c_int
         L.moe_lora_profile_read.argtypes = [P, P, P, ctypes.c_int]
         L.moe_lora_launch_count.restype = ctypes.c_int64
@@ -338,6 +340,12 @@ def moe_lora_mxfp4_decode(packed: torch.Tensor, scales: torch.Tensor, out: torch
 
 def moe_lora_profile_enable(on: bool) -> None:
     lib().moe_lora_profile_enable(1 if on else 0)
+
+
+def moe_lora_profile_select(kernel: Optional[str]) -> None:
+    """Time only `kernel`'s launches (None: every kernel)."""
+    rc = lib().moe_lora_profile_select(kernel.encode() if kernel is not None else None)
+    _check(rc, "moe_lora_profile_select")
 
 
 def moe_lora_profile_read() -> Dict[str, tuple]:

@@ -134,8 +134,10 @@ int moe_lora_plan(const moe_lora_dims* d, const int32_t* topk_ids, const int64_t
   if ((rc = make_adapter_table(d, adapter_offsets, &at))) return rc;
   int sms;
   if ((rc = device_sms(&sms))) return rc;
-  return launch_plan(d, topk_ids, at, plan_ws, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_LORA_OK
-                                                                                                : MOE_LORA_ERR_CUDA;
+  int* chunk_base = reinterpret_cast<int*>(static_cast<char*>(plan_ws) + plan_layout(d).chunk_base);
+  return launch_plan(d, topk_ids, at, plan_ws, chunk_base, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_LORA_OK
+             : MOE_LORA_ERR_CUDA;
 }
 
 int moe_lora_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, const float* topk_w,

@@ -34,8 +34,12 @@ inline int make_adapter_table(const moe_lora_dims* d, const int64_t* adapter_off
   return MOE_LORA_OK;
 }
 
+// The plan kernels' launch sequence.  chunk_base: the per-chunk group histograms,
+// A*E*max(1, ceil(T*k/1024)) ints of device memory whose contents on entry do not
+// matter (moe_lora_plan passes the end of its workspace, moe_lora_plan_noalloc a
+// fixed array inside the library).
 cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const AdapterTable& at, void* ws,
-                        cudaStream_t stream);
+                        int* chunk_base, cudaStream_t stream);
 
 // out[i] = sum_s in[s*stride + i] for s = 0..split-1 in order (fp32, n % 4 == 0).
 cudaError_t launch_reduce_splits(const float* in, int64_t stride, int split, int64_t n, float* out, int num_sms,

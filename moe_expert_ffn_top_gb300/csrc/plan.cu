@@ -15,7 +15,6 @@
 
 #include "common.cuh"
 #include "launch.h"
-#include "plan_kernels.h"
 #include "prof.h"
 
 namespace moelora {
@@ -183,7 +182,7 @@ __global__ void plan_wide(int G, int A, int E, const int* __restrict__ offsets, 
 }
 
 cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const AdapterTable& at, void* ws,
-                        cudaStream_t stream) {
+                        int* chunk_base, cudaStream_t stream) {
   const PlanLayout L = plan_layout(d);
   char* b = static_cast<char*>(ws);
   int* err = (int*)(b + L.err);
@@ -197,7 +196,6 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
   int* tok_tile = (int*)(b + L.tok_tile);
   int* wtile_off = (int*)(b + L.wtile_off);
   int4* wtile = (int4*)(b + L.wtile);
-  int* chunk_base = (int*)(b + L.chunk_base);
   const int G = d->A * d->E;
   const int64_t TK = d->T * d->k;
   const int nchunks = (int)plan_chunks(d);
@@ -210,6 +208,10 @@ cudaError_t launch_plan(const moe_lora_dims* d, const int32_t* ids, const Adapte
     e = cudaFuncSetAttribute(plan_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
     if (e != cudaSuccess) return e;
   }
+  // plan_count rewrites every histogram entry that plan_scan and plan_scatter read,
+  // so chunk_base may hold anything on entry (the fixed array of the no-allocation
+  // entry point keeps the previous call's values); with no routes at all, the G
+  // entries plan_scan reads are cleared instead.
   if (nchunks > 0) {
     prof_begin(K_PLAN_COUNT, stream);
     plan_count<<<nchunks, 32, hist_bytes, stream>>>(ids, TK, d->k, d->E, G, at, chunk_base, nchunks, err);

@@ -1,25 +1,25 @@
 // Routing plan for callers that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc, or any allocator, at the point where they
-// route tokens: code that runs while a CUDA stream is being captured into a
-// graph (an allocation there breaks the capture), memory-planned serving
-// runtimes that hand out only pre-reserved buffers, and plain C hosts without an
-// allocator binding.  They still own the plan buffer itself (the output), but
-// cannot provide the extra temporary space that moe_lora_plan() keeps at the
-// end of its workspace for per-chunk expert histograms.
+// route tokens: memory-planned serving runtimes that reserve all device memory up
+// front and hand out only pre-reserved buffers (an allocation there fails or
+// fragments the reserved pool), and plain C hosts that hold device pointers but
+// have no allocator binding of their own.  They still own the plan buffer itself
+// (the output), but cannot provide the extra temporary space that moe_lora_plan()
+// keeps at the end of its workspace for per-chunk expert histograms.
 //
 // moe_lora_plan_noalloc() therefore takes that temporary space from a fixed
 // file-scope device array instead.  The array is part of the library image: every
 // GPU on which the library is loaded holds it (4 MiB) until the process exits.
-// Nothing here calls cudaMalloc, cudaFree or any allocating library routine.
+// Nothing here calls cudaMalloc, cudaFree or any allocating library routine; the
+// launch sequence is moe_lora_plan()'s own (launch_plan), given the array.
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
-#include "plan_kernels.h"
 
 namespace moelora {
 
@@ -28,23 +28,71 @@ constexpr int64_t kNoallocScratchInts = int64_t(1) << 20;  // 4 MiB
 static __device__ __align__(256) int g_plan_scratch[kNoallocScratchInts];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int* g_scratch_addr[kMaxDevices] = {};  // device address of g_plan_scratch, per device
-
 // In host code `g_plan_scratch` names a host-side stand-in, not device memory, so
-// the device address is looked up once per device (with that device current).
-int scratch_for_current_device(int** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_LORA_ERR_DEVICE;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || !p) return MOE_LORA_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<int*>(p);
+// its device address is looked up with cudaGetSymbolAddress.  A module is loaded
+// once per CUDA context (not per device: a driver-API host may create several
+// contexts on one device, and cudaDeviceReset replaces the primary context), so
+// the address is cached per context, keyed by the driver's unique context id.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  int* addr;
+};
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+ScratchEntry g_cache[kMaxContexts];
+int g_cached = 0;
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void load_ctx_entry_points() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
+// Device address of g_plan_scratch in the current context.
+int scratch_for_current_context(int** out) {
+  std::call_once(g_ctx_once, load_ctx_entry_points);
+  if (!g_ctx_current || !g_ctx_id) return MOE_LORA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return MOE_LORA_ERR_CUDA;
+  void* fresh = nullptr;
+  if (!ctx) {
+    // No context is current yet: the runtime's symbol lookup makes the current
+    // device's primary context current (as any runtime call would).
+    if (cudaGetSymbolAddress(&fresh, g_plan_scratch) != cudaSuccess || !fresh) return MOE_LORA_ERR_CUDA;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return MOE_LORA_ERR_CUDA;
   }
-  *out = g_scratch_addr[dev];
+  unsigned long long id = 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return MOE_LORA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < g_cached; ++i)
+    if (g_cache[i].ctx_id == id) {
+      *out = g_cache[i].addr;
+      return MOE_LORA_OK;
+    }
+  if (!fresh && (cudaGetSymbolAddress(&fresh, g_plan_scratch) != cudaSuccess || !fresh)) return MOE_LORA_ERR_CUDA;
+  // Context ids are never reused within a process; a full table keeps the oldest
+  // entries and looks the address up again on every call from a newer context.
+  if (g_cached < kMaxContexts) g_cache[g_cached++] = ScratchEntry{id, static_cast<int*>(fresh)};
+  *out = static_cast<int*>(fresh);
   return MOE_LORA_OK;
+}
+
+bool device_ok() {
+  int dev = 0, major = 0, minor = 0;
+  return cudaGetDevice(&dev) == cudaSuccess &&
+         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess && major == 10 &&
+         minor == 3;
 }
 }  // namespace
 
@@ -59,60 +107,17 @@ extern "C" int moe_lora_plan_noalloc(const moe_lora_dims* d, const int32_t* topk
   if (!plan_ws) return MOE_LORA_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(plan_ws) & 15u) return MOE_LORA_ERR_ALIGN;
   if (d->T > 0 && !topk_ids) return MOE_LORA_ERR_NULL;
-  const int G = d->A * d->E;
   const int64_t nchunks = plan_chunks(d);
-  if ((int64_t)G * (nchunks > 0 ? nchunks : 1) > kNoallocScratchInts) return MOE_LORA_ERR_SCRATCH_LIMIT;
-  const PlanLayout L = plan_layout(d);
-  if (plan_bytes < L.chunk_base) return MOE_LORA_ERR_WORKSPACE;  // the plan itself, without the histograms
+  if ((int64_t)d->A * d->E * (nchunks > 0 ? nchunks : 1) > kNoallocScratchInts) return MOE_LORA_ERR_SCRATCH_LIMIT;
+  if (plan_bytes < plan_layout(d).chunk_base) return MOE_LORA_ERR_WORKSPACE;  // the plan, without the histograms
   AdapterTable at;
   if ((rc = make_adapter_table(d, adapter_offsets, &at))) return rc;
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess || major != 10 ||
-      minor != 3)
-    return MOE_LORA_ERR_DEVICE;
+  if (!device_ok()) return MOE_LORA_ERR_DEVICE;
   int* chunk_base = nullptr;
-  if ((rc = scratch_for_current_device(&chunk_base))) return rc;
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* b = static_cast<char*>(plan_ws);
-  int* err = (int*)(b + L.err);
-  int* counts = (int*)(b + L.counts);
-  int* offsets = (int*)(b + L.offsets);
-  int* row_of_route = (int*)(b + L.row_of_route);
-  int* route_of_row = (int*)(b + L.route_of_row);
-  int* tile_group = (int*)(b + L.tile_group);
-  int2* tile_span = (int2*)(b + L.tile_span);
-  int* tok_off = (int*)(b + L.tok_off);
-  int* tok_tile = (int*)(b + L.tok_tile);
-  int* wtile_off = (int*)(b + L.wtile_off);
-  int4* wtile = (int4*)(b + L.wtile);
-  const int64_t TK = d->T * d->k;
-  const int nch = (int)nchunks;
-  if (cudaMemsetAsync(err, 0, 16, s) != cudaSuccess) return MOE_LORA_ERR_CUDA;
-  const size_t hist_bytes = sizeof(int) * (size_t)G;
-  if (hist_bytes > 48 * 1024) {
-    if (cudaFuncSetAttribute(plan_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(plan_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes) !=
-            cudaSuccess)
-      return MOE_LORA_ERR_CUDA;
-  }
-  // The shared array keeps the previous call's histograms.  plan_count rewrites
-  // every entry this call reads; with no routes at all, the G entries read by
-  // plan_scan are cleared here.
-  if (nch > 0) {
-    plan_count<<<nch, 32, hist_bytes, s>>>(topk_ids, TK, d->k, d->E, G, at, chunk_base, nch, err);
-  } else if (cudaMemsetAsync(chunk_base, 0, sizeof(int) * (size_t)G, s) != cudaSuccess) {
-    return MOE_LORA_ERR_CUDA;
-  }
-  plan_scan<<<1, 1024, 0, s>>>(chunk_base, nch > 0 ? nch : 1, G, counts, offsets);
-  if (nch > 0)
-    plan_scatter<<<nch, 32, hist_bytes, s>>>(topk_ids, TK, d->k, d->E, G, at, chunk_base, offsets, nch, row_of_route,
-                                             route_of_row, err);
-  plan_finish<<<G < 1024 ? G : 1024, 128, 0, s>>>(G, d->E, counts, offsets, route_of_row, tile_group, tile_span,
-                                                  at, tok_off, tok_tile);
-  plan_wide<<<1, 1024, 0, s>>>(G, d->A, d->E, offsets, wtile_off, wtile);
-  return cudaGetLastError() == cudaSuccess ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
+  if ((rc = scratch_for_current_context(&chunk_base))) return rc;
+  // The array keeps the previous call's histograms; launch_plan rewrites (or, with
+  // no routes, clears) every entry it reads before reading it.
+  return launch_plan(d, topk_ids, at, plan_ws, chunk_base, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_LORA_OK
+             : MOE_LORA_ERR_CUDA;
 }

@@ -2,6 +2,7 @@
 // grows on demand and is recycled after each read; nothing is allocated on the
 // device and nothing runs when timing is off except an atomic launch counter.
 #include <atomic>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -17,6 +18,7 @@ struct Rec {
 };
 std::mutex g_mu;
 std::atomic<bool> g_on{false};
+std::atomic<int> g_only{-1};        // >= 0: time only launches of this slot
 std::atomic<long long> g_launches{0};
 std::vector<Rec> g_pending;         // recorded, not yet read
 std::vector<cudaEvent_t> g_free;    // recycled events
@@ -48,6 +50,8 @@ const char* prof_name(int slot) {
 void prof_begin(int slot, cudaStream_t s) {
   t_slot = -1;
   if (!g_on.load(std::memory_order_relaxed)) return;
+  const int only = g_only.load(std::memory_order_relaxed);
+  if (only >= 0 && only != slot) return;
   std::lock_guard<std::mutex> lk(g_mu);
   t_start = take_event();
   if (!t_start) return;
@@ -76,6 +80,19 @@ extern "C" {
 int moe_lora_profile_enable(int on) {
   g_on.store(on != 0);
   return MOE_LORA_OK;
+}
+
+int moe_lora_profile_select(const char* kernel) {
+  if (!kernel) {
+    g_only.store(-1);
+    return MOE_LORA_OK;
+  }
+  for (int s = 0; s < K_NUM_SLOTS; ++s)
+    if (std::strcmp(prof_name(s), kernel) == 0) {
+      g_only.store(s);
+      return MOE_LORA_OK;
+    }
+  return MOE_LORA_ERR_DIMS;
 }
 
 int moe_lora_profile_read(const char** names, double* total_ms, int64_t* launches, int cap) {

@@ -1,5 +1,5 @@
 """Host-side logic of bench.py (no GPU): the FLOP model behind `value` and the
-roofline, the source hash that keys the committed DRAM-traffic counters, and the
+roofline, the per-kernel source hash that keys the committed DRAM-traffic counters, and the
 multi-rank helpers on one rank."""
 import importlib.util
 import json
@@ -33,36 +33,64 @@ def test_production_step_flops(bench):
     assert bench.step_flops(65536, 393216, 4096, 2048, 128) / 1e12 == pytest.approx(42.056, abs=1e-3)
 
 
+def _copy_tree(bench, tmp_path):
+    src = os.path.join(ROOT, "moe_expert_ffn_top_gb300")
+    shutil.copytree(src, tmp_path / "moe_expert_ffn_top_gb300",
+                    ignore=shutil.ignore_patterns("*.so", "*.o", "__pycache__", "_build*"))
+    return tmp_path / "moe_expert_ffn_top_gb300" / "csrc"
+
+
 def test_source_hash_ignores_comments_only(bench, tmp_path):
-    src = os.path.join(ROOT, "moe_expert_ffn_top_gb300", "csrc")
-    dst = tmp_path / "moe_expert_ffn_top_gb300" / "csrc"
-    dst.mkdir(parents=True)
-    for f in bench.GEMM_SOURCES:
-        shutil.copy(os.path.join(src, f), dst / f)
+    dst = _copy_tree(bench, tmp_path)
     root = bench.ROOT
     try:
         bench.ROOT = str(tmp_path)
-        h0 = bench.src_hash()
-        p = dst / bench.GEMM_SOURCES[-1]
+        h0 = bench.src_hash("w13_lora_swiglu")
+        p = dst / "gemm_engine.cuh"
         text = p.read_text()
         p.write_text("// a comment\n/* a block\n   comment */\n\n" + text.replace("\n", "  // note\n", 3))
-        assert bench.src_hash() == h0
+        assert bench.src_hash("w13_lora_swiglu") == h0
         p.write_text(text + "\nstatic const int kUnused = 1;\n")
-        assert bench.src_hash() != h0
+        assert bench.src_hash("w13_lora_swiglu") != h0
+    finally:
+        bench.ROOT = root
+
+
+def test_source_hash_is_per_problem(bench, tmp_path):
+    """A code change inside one problem type (or its host launch block) re-keys that
+    kernel's record only."""
+    dst = _copy_tree(bench, tmp_path)
+    root = bench.ROOT
+    try:
+        bench.ROOT = str(tmp_path)
+        names = list(bench.PROBLEM_OF)
+        h0 = {n: bench.src_hash(n) for n in names}
+        assert len(set(h0.values())) == len(names)
+        p = dst / "gemm_problems.cuh"
+        text = p.read_text()
+        marker = "struct ProbA13Expand {"
+        assert marker in text
+        p.write_text(text.replace(marker, marker + "\n  static constexpr int kProbe = 1;"))
+        h1 = {n: bench.src_hash(n) for n in names}
+        assert [n for n in names if h1[n] != h0[n]] == ["a13_expand"]
+        p.write_text(text)
+        f = dst / "forward.cu"
+        ftext = f.read_text()
+        f.write_text(ftext.replace("p.clamp = d->act_clamp;", "p.clamp = d->act_clamp + 0.0f;", 1))
+        h2 = {n: bench.src_hash(n) for n in names}
+        assert [n for n in names if h2[n] != h0[n]] == ["w13_lora_swiglu"]
     finally:
         bench.ROOT = root
 
 
 def test_traffic_follows_the_source_hash(bench, tmp_path):
-    rec = {"w13_lora_swiglu": {"bytes_per_launch": 123, "src_hash": bench.src_hash()}}
-    (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
-    src = os.path.join(ROOT, "moe_expert_ffn_top_gb300")
-    shutil.copytree(src, tmp_path / "moe_expert_ffn_top_gb300",
-                    ignore=shutil.ignore_patterns("*.so", "*.o", "__pycache__", "_build*"))
+    _copy_tree(bench, tmp_path)
     root = bench.ROOT
     try:
         bench.ROOT = str(tmp_path)
+        rec = {"w13_lora_swiglu": {"bytes_per_launch": 123, "src_hash": bench.src_hash("w13_lora_swiglu")}}
+        (tmp_path / "profiles").mkdir()
+        (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
         assert bench.traffic_for("w13_lora_swiglu") == 123
         assert bench.traffic_for("w2_a2") is None
         rec["w13_lora_swiglu"]["src_hash"] = "0" * 16

@@ -334,21 +334,128 @@ def test_edge_sweep_production_width(T):
     _sampled_check(inp, shp, out, sample)
 
 
+def _tile_sample(plan, k, per_kind=8, seed=0):
+    """Tokens chosen from the plan so that the sample's routed rows land in (a) the
+    second 128-row half of a 256-row tile (the wide GEMMs' second MMA and epilogue
+    half), (b) the last, partly padded 128-row tile of a group of two or more tiles,
+    (c) a group's first tile; `per_kind` tokens of each kind, each through an expert
+    no earlier pick used where possible.  Returns (sorted tokens, experts covered)."""
+    offs = plan["offsets"].long()
+    counts = plan["counts"].long()
+    ror = plan["row_of_route"].long()
+    live = (ror >= 0).nonzero().flatten()
+    rows = ror[live]
+    grp = torch.searchsorted(offs, rows, right=True) - 1
+    tile = (rows - offs[grp]) // 128
+    ntile = (counts[grp] + 127) // 128
+    kinds = [tile % 2 == 1, (tile == ntile - 1) & (counts[grp] % 128 != 0) & (ntile >= 2), tile == 0]
+    g = torch.Generator().manual_seed(seed)
+    chosen, experts = [], set()
+    for sel in kinds:
+        pos = sel.nonzero().flatten()
+        pos = pos[torch.randperm(pos.numel(), generator=g)]
+        picked = 0
+        for fresh_only in (True, False):
+            for i in pos.tolist():
+                if picked == per_kind:
+                    break
+                t, e = int(live[i]) // k, int(grp[i])
+                if t in chosen or (fresh_only and e in experts):
+                    continue
+                chosen.append(t)
+                experts.add(e)
+                picked += 1
+        assert picked == per_kind, "too few candidate rows of one kind"
+    return sorted(chosen), experts
+
+
+def _chunked_sampled_check(inp, shp, out, sample, chunk=4):
+    """_sampled_check for larger samples: the oracle runs on sub-problems of `chunk`
+    tokens (a few experts' weights on the host at a time).  dy is zero outside the
+    sample, and every gradient is linear in dy, so the adapter gradients of the
+    whole sample are the sums of the chunks' gradients; y, dx and dw are per token."""
+    E = shp.E
+    tot = {n: None for n in ("dA1", "dA3", "dB2")}
+    per_e = {n: {} for n in ("dB1", "dB3", "dA2")}
+    ys, dxs, dws = [], [], []
+    for c0 in range(0, len(sample), chunk):
+        sub, sshp, used, tok = sub_problem(inp, shp, sample[c0:c0 + chunk])
+        y_ref = oracle.forward(sub, sshp)
+        g_ref = oracle.backward(sub, sshp)
+        ys.append((tok, y_ref))
+        dxs.append((tok, g_ref["dx"]))
+        dws.append((tok, g_ref["dw"]))
+        for n in tot:
+            tot[n] = g_ref[n] if tot[n] is None else tot[n] + g_ref[n]
+        for n in per_e:
+            for i, e in enumerate(used):
+                v = g_ref[n][:, i]
+                per_e[n][e] = v if e not in per_e[n] else per_e[n][e] + v
+    for name, parts, got in (("y", ys, out["y"]), ("dx", dxs, out["dx"]), ("dw", dws, out["dw"])):
+        tk = torch.cat([t for t, _ in parts])
+        assert_close(name, got[tk.cuda()].cpu(), torch.cat([v for _, v in parts]))
+    mask = torch.ones(shp.T, dtype=torch.bool, device="cuda")
+    mask[torch.as_tensor(sample, device="cuda")] = False
+    assert out["dx"][mask].abs().max().item() == 0 and out["dw"][mask].abs().max().item() == 0
+    for n in tot:
+        assert_close(n, out[n].cpu(), tot[n])
+    ex = sorted(per_e["dB1"])
+    exd = torch.as_tensor(ex, device="cuda")
+    for n in per_e:
+        assert_close(n, out[n][:, exd].cpu(), torch.stack([per_e[n][e] for e in ex], dim=1))
+        other = torch.ones(E, dtype=torch.bool, device="cuda")
+        other[exd] = False
+        if other.any():
+            assert out[n][:, other].abs().max().item() == 0, n
+
+
 @pytest.mark.slow
 def test_production_shape_sampled():
     """65,536 tokens, H=4096, I=2048, E=256, top-6, rank 128: the benchmark's
-    workload and launch configuration, checked on sampled tokens (sparse dy)."""
+    workload and launch configuration.  The plan is read back first; 24 tokens are
+    chosen so that their routed rows land in second 128-row halves of 256-row
+    tiles, in groups' last (padded) tiles and in groups' first tiles, across many
+    experts, and the result is checked on them (sparse dy)."""
     shp = shape("prod")
     inp = make_inputs(shp, seed=2, device="cuda")
-    sample = [0, 1, 777, 4096, 33333, 65535]
-    inp = _sparse_dy(inp, shp, sample)
-    out = run_gpu(inp, shp)
-    assert out["err"] == 0
+    d = dims_of(shp)
+    ws = m.Workspaces.allocate(d)
+    m.moe_lora_plan(d, inp["topk_ids"], None, ws.plan)
+    got = m.moe_lora_plan_readback(d, ws.plan)
     want = oracle.plan(inp["topk_ids"].cpu(), shp.E, torch.tensor([0, shp.T]), 128)
-    got = m.moe_lora_plan_readback(out["dims"], out["ws"].plan)
     for k in ("counts", "offsets", "row_of_route", "route_of_row"):
         assert torch.equal(got[k], want[k]), k
-    _sampled_check(inp, shp, out, sample)
+    sample, experts = _tile_sample(got, shp.k, per_kind=8, seed=2)
+    assert len(sample) >= 24 and len(experts) >= 8
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp, ws=ws)
+    assert out["err"] == 0
+    _chunked_sampled_check(inp, shp, out, sample)
+
+
+@pytest.mark.parametrize("k,T", [(1, 65536), (2, 32768)])
+def test_topk_small_production_width(k, T):
+    """Top-k 1 and 2 (the pages' top-k 1/2/6 coverage) at production widths: H=4096,
+    I=2048, E=256, rank 128, a fifth of the routes masked, experts 0/127/255 empty;
+    ~200 rows per expert, so groups of two 128-row tiles (one full 256-row tile with a
+    padded second half).  Plan bit-exact; 24 plan-chosen tokens checked against the
+    oracle (sparse dy)."""
+    shp = Shape(T=T, H=4096, I=2048, E=256, k=k, r=128, mask_frac=0.2, empty_experts=(0, 127, 255))
+    inp = make_inputs(shp, seed=50 + k, device="cuda")
+    d = dims_of(shp)
+    ws = m.Workspaces.allocate(d)
+    m.moe_lora_plan(d, inp["topk_ids"], None, ws.plan)
+    got = m.moe_lora_plan_readback(d, ws.plan)
+    want = oracle.plan(inp["topk_ids"].cpu(), shp.E, torch.tensor([0, shp.T]), 128)
+    for n in ("counts", "offsets", "row_of_route", "route_of_row"):
+        assert torch.equal(got[n], want[n]), n
+    assert int(got["counts"][0]) == int(got["counts"][127]) == int(got["counts"][255]) == 0
+    sample, experts = _tile_sample(got, k, per_kind=8, seed=k)
+    assert len(sample) >= 24 and len(experts) >= 8
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp, ws=ws)
+    assert out["err"] == 0
+    _chunked_sampled_check(inp, shp, out, sample)
 
 
 # ----------------------------------------------------------------------------- several adapters

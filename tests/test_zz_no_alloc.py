@@ -1,11 +1,15 @@
 """moe_lora_plan_noalloc: the routing plan for callers that cannot allocate.
 
-Callers that may not call cudaMalloc while they route tokens (stream capture into
-a CUDA graph, memory-planned serving runtimes, C hosts without an allocator) use
-this entry point; its temporary histograms live in a fixed array inside the
-library instead of in caller-provided workspace.  These checks run it through the
-C ABI and compare it with moe_lora_plan() on the same inputs, on consecutive calls
-whose stale scratch contents differ, and check the size-limit rejection.
+Some callers may not call cudaMalloc (or any allocator) while they route tokens:
+memory-planned serving runtimes that reserve all device memory up front and hand
+out only pre-reserved buffers, and C hosts without an allocator binding of their
+own.  This entry point serves them: its temporary histograms live in a fixed
+array inside the library instead of in caller-provided workspace.  These checks
+run it through the C ABI and compare it with moe_lora_plan() on the same inputs,
+on consecutive calls whose stale scratch contents differ, drive a forward and
+backward from its plan twice in a row, and check the size-limit rejection.  The
+file is collected last, so a run that stops at the first failure has already run
+every other test.
 """
 import pytest
 import torch

@@ -69,7 +69,9 @@ extern "C" {
 #define MOE_LORA_WS_BWD_SCRATCH 3 /* backward temporaries */
 #define MOE_LORA_WS_ROUTER_SCRATCH 4 /* router error word and backward temporaries */
 
-/* Problem sizes.  H and I must be multiples of 256; r a multiple of 8 in [8,128];
+/* Problem sizes.  H and I must be multiples of 64 (the 64-element K step of every
+ * contraction; the 128- and 256-wide output tiles need not divide them: loads past
+ * a tensor's edge read zeros and nothing is stored there); r a multiple of 8 in [8,128];
  * 1 <= k <= 32; 1 <= E; A >= 1 adapters; block_m must be 128 (the plan pads
  * every (adapter, expert) group to a multiple of it).
  * Gated activation h = act(cl(gate)) * cl(up): act 0 = SwiGLU (silu), 1 = GeGLU

@@ -95,7 +95,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, p.split * d->A * (d->H / 128), num_sms, stream, K_DB2));
+    LAUNCH(launch_gemm(p, p.split * d->A * cdiv(d->H, 128), num_sms, stream, K_DB2));
     if (p.split > 1) LAUNCH(launch_reduce_splits(ksplit, p.split_stride, p.split, p.split_stride, gr->dB2, num_sms, stream));
   }
   // B2: routed dy rows and the scaled shared-expand gradients
@@ -121,9 +121,9 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.r = d->r;
     p.act = d->act;
     p.clamp = d->act_clamp;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 256), num_sms, stream, K_W2_DGRAD));
+    LAUNCH(launch_gemm(p, max_row_tiles * cdiv(d->I, 256), num_sms, stream, K_W2_DGRAD));
   }
-  LAUNCH(launch_dw(pl, part, ProbW2Dgrad::kPartsPerTile * (d->I / 256), dw, num_sms, stream));
+  LAUNCH(launch_dw(pl, part, ProbW2Dgrad::kPartsPerTile * cdiv(d->I, 256), dw, num_sms, stream));
   // dA2 per (adapter, expert)
   {
     ProbDA2 p;
@@ -134,7 +134,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.dA2 = gr->dA2;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, (int)G * (d->I / 256), num_sms, stream, K_DA2));
+    LAUNCH(launch_gemm(p, (int)G * cdiv(d->I, 256), num_sms, stream, K_DA2));
   }
   // B5: W13^T dgrad + B1/B3 path
   {
@@ -154,7 +154,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.I = d->I;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W13_DGRAD));
+    LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W13_DGRAD));
   }
   // dB1 / dB3 per (adapter, expert)
   {
@@ -168,7 +168,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.dB3 = gr->dB3;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, 2 * (int)G * (d->I / 128), num_sms, stream, K_DB13));
+    LAUNCH(launch_gemm(p, 2 * (int)G * cdiv(d->I, 128), num_sms, stream, K_DB13));
   }
   // B6a: per-token sum of the shared-shrink gradients
   LAUNCH(launch_dy13w(pl, dY13, dY13w, 2 * d->r, num_sms, stream));
@@ -184,7 +184,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     MAP(tmap_2d_store32(&p.mdXl, dXl, H, T));
     p.H = d->H;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_A13_EXPAND));
+    LAUNCH(launch_gemm(p, max_tok_tiles * cdiv(d->H, 256), num_sms, stream, K_A13_EXPAND));
   }
   LAUNCH(launch_combine_rows(pl, dXl, dXp, nullptr, dx, d->H, num_sms, stream, K_COMBINE_DX));
   // dA1 / dA3 per adapter
@@ -194,7 +194,7 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     MAP(tmap_2d(&p.mx, x, H, T, 64, 64));
     p.pl = pl;
     p.err = pl.err;
-    const int tiles = d->A * ((2 * d->r + 127) / 128) * (d->H / 256);
+    const int tiles = d->A * ((2 * d->r + 127) / 128) * cdiv(d->H, 256);
     p.split = pick_split();
     const int64_t n1 = (int64_t)A * r * H;
     p.out1 = p.split > 1 ? ksplit : gr->dA1;

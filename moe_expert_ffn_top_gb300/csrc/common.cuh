@@ -23,7 +23,7 @@ inline int check_dims(const moe_lora_dims* d) {
   if ((d->act != 0 && d->act != 1) || (d->base_fmt != 0 && d->base_fmt != 1)) return MOE_LORA_ERR_UNSUPPORTED;
   if (!(d->act_clamp >= 0.0f) || d->act_clamp > 3.0e38f) return MOE_LORA_ERR_DIMS;
   if (d->T < 0 || d->T > (int64_t)1 << 30) return MOE_LORA_ERR_DIMS;
-  if (d->H < 256 || d->H % 256 || d->I < 256 || d->I % 256) return MOE_LORA_ERR_DIMS;
+  if (d->H < 64 || d->H % 64 || d->I < 64 || d->I % 64) return MOE_LORA_ERR_DIMS;
   if (d->r < 8 || d->r > 128 || d->r % 8) return MOE_LORA_ERR_DIMS;
   if (d->k < 1 || d->k > 32 || d->E < 1 || d->A < 1 || d->A > kMaxAdapters) return MOE_LORA_ERR_DIMS;
   if ((int64_t)d->A * d->E > kMaxGroups) return MOE_LORA_ERR_DIMS;
@@ -110,7 +110,8 @@ inline FwdLayout fwd_layout(const moe_lora_dims* d) {
 
 struct BwdLayout {
   // dyB2 [T,r] bf16; Dp [P,H] bf16 (reused for dXp); D2p, dZ2p [P,r] bf16;
-  // dG, dU [P,I] bf16; part [P, I/128] f32; dY13 [P,2r] f32; dY13w [T,2r] bf16;
+  // dG, dU [P,I] bf16; part [P, 2*ceil(I/256)] f32 (router-gradient partial sums: at
+  // most two per row and 256-column tile); dY13 [P,2r] f32; dY13w [T,2r] bf16;
   // dXl [T,H] bf16 (grad-x through A1/A3); ksplit: fp32 partials of the
   // token-split dB2 and dA1/dA3 reductions [kMaxSplit][2][A][r][H]
   size_t dyB2, Dp, D2p, dZ2p, dG, dU, part, dY13, dY13w, dXl, ksplit, total;
@@ -126,7 +127,7 @@ inline BwdLayout bwd_layout(const moe_lora_dims* d) {
   L.dZ2p = take(2 * (size_t)P * d->r);
   L.dG = take(2 * (size_t)P * d->I);
   L.dU = take(2 * (size_t)P * d->I);
-  L.part = take(4 * (size_t)P * (d->I / 128));
+  L.part = take(4 * (size_t)P * 2 * ((d->I + 255) / 256));
   L.dY13 = take(4 * (size_t)P * 2 * d->r);
   L.dY13w = take(2 * (size_t)T * 2 * d->r);
   L.dXl = take(2 * (size_t)T * d->H);

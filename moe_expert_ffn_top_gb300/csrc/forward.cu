@@ -101,7 +101,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.r = d->r;
     p.act = d->act;
     p.clamp = d->act_clamp;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13));
+    LAUNCH(launch_gemm(p, max_row_tiles * cdiv(d->I, 128), num_sms, stream, K_W13));
   }
   // F4/F5: W2 + expert-local A2 shrink
   if (kW2OneSmWide) {
@@ -117,7 +117,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W2));
+    LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W2));
   } else {
     ProbW2Pair p;
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
@@ -131,7 +131,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm_pair(p, max_row_tiles * (d->H / 256 + 1), num_sms, stream, K_W2));
+    LAUNCH(launch_gemm_pair(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W2));
   }
   // F6a: per-token weighted sum of the A2 shrink
   LAUNCH(launch_z2w(pl, Z2, topk_w, Z2w, d->r, num_sms, stream));
@@ -149,7 +149,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.r = d->r;
     p.s = d->scale;
-    LAUNCH(launch_gemm(p, max_tok_tiles * (d->H / 256), num_sms, stream, K_B2_EXPAND));
+    LAUNCH(launch_gemm(p, max_tok_tiles * cdiv(d->H, 256), num_sms, stream, K_B2_EXPAND));
   }
   LAUNCH(launch_combine_rows(pl, Yl, O, topk_w, y, d->H, num_sms, stream, K_COMBINE_Y));
 #undef MAP

@@ -226,6 +226,10 @@ __device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], 
 }
 
 __device__ __forceinline__ int round16(int r) { return (r + 15) & ~15; }
+// Tiles of `b` covering `n` (H and I are multiples of 64, not of the tile widths:
+// TMA loads past the tensor edge read zeros, and epilogues skip the 32-column chunks
+// -- or rows -- that lie past it).
+__host__ __device__ __forceinline__ int cdiv(int n, int b) { return (n + b - 1) / b; }
 // N of a two-SM (M = 256) MMA: a multiple of 32, so each CTA holds a multiple of 16 columns.
 __device__ __forceinline__ int round32(int r) { return (r + 31) & ~31; }
 
@@ -423,7 +427,7 @@ struct ProbW13 {
   int H, I, r;
   int act;      // 0 = SwiGLU, 1 = GeGLU
   float clamp;  // activation clamp (0 = none)
-  __device__ int ntn() const { return I / 128; }
+  __device__ int ntn() const { return cdiv(I, 128); }
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const {
     return (kWide ? pl.wtile_off[pl.G] : pl.offsets[pl.G] / 128) * ntn();
@@ -471,7 +475,7 @@ struct ProbW13 {
     const int y0 = ti.m0 + row - (threadIdx.x & 31);  // warp's first row
     TmaStoreRing out(stg);
     const int64_t base = (int64_t)y0 * I + ti.n0;
-    for (int c = c0; c < 128; c += cs) {
+    for (int c = c0; c < 128 && ti.n0 + c < I; c += cs) {
       float g[32], u[32], a[32];
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
@@ -509,7 +513,7 @@ struct ProbW2 {
   int* err;
   uint16_t *O, *Z2;
   int H, I, r;
-  __device__ int ntn() const { return H / 256 + 1; }
+  __device__ int ntn() const { return cdiv(H, 256) + 1; }
   __device__ int num_tiles() const {
     return (kWide ? pl.wtile_off[pl.G] : pl.offsets[pl.G] / 128) * ntn();
   }
@@ -517,7 +521,7 @@ struct ProbW2 {
     TileInfo ti;
     const int nt = kWide ? wide_entry_decode(nmajor_wide_fetch(pl, t, ntn()), ti)
                          : nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
-    ti.sub = nt == H / 256;
+    ti.sub = nt == cdiv(H, 256);
     ti.n0 = ti.sub ? 0 : nt * 256;
     ti.nk = I / kBK;
     return ti;
@@ -547,7 +551,7 @@ struct ProbW2 {
     if (!ti.sub) {
       const int y0 = (int)(p - (threadIdx.x & 31));  // warp's first row
       uint16_t* o0 = O + (int64_t)y0 * H + ti.n0;
-      for (int c = c0; c < 256; c += cs) {
+      for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
         if (kEpiTmaStore)
@@ -586,7 +590,7 @@ struct ProbB2Expand {
   uint16_t* Yl;
   int H, r;
   float s;
-  __device__ int ntn() const { return H / 256; }
+  __device__ int ntn() const { return cdiv(H, 256); }
   __device__ int num_tiles() const { return pl.tok_tile[pl.A] * ntn(); }
   __device__ TileInfo tile(int t) const {
     const int mt = t / ntn(), nt = t % ntn();
@@ -618,7 +622,7 @@ struct ProbB2Expand {
     // boundaries, so a whole-box store never reaches another adapter's rows, and
     // the map clips rows past T.
     TmaStoreRing out(stg);
-    for (int c = c0; c < 256; c += cs) {
+    for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (nvalid <= 0) continue;
@@ -698,10 +702,10 @@ struct ProbDB2 {
   int64_t split_stride;
   int H, r, split;
   float s;
-  __device__ int num_tiles() const { return split * pl.A * (H / 128); }
+  __device__ int num_tiles() const { return split * pl.A * cdiv(H, 128); }
   __device__ TileInfo tile(int t) const {
-    const int per = pl.A * (H / 128);
-    const int sp = t / per, a = (t % per) / (H / 128), mt = t % (H / 128);
+    const int ntm = cdiv(H, 128), per = pl.A * ntm;
+    const int sp = t / per, a = (t % per) / ntm, mt = t % ntm;
     TileInfo ti;
     ti.g = a;
     ti.m0 = mt * 128;
@@ -730,7 +734,9 @@ struct ProbDB2 {
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    float* o0 = row_ptr(ti, (int64_t)ti.m0 + row - (threadIdx.x & 31));  // warp's first row
+    const int h0 = ti.m0 + row - (threadIdx.x & 31);  // warp's first row
+    if (h0 >= H) return;                                // rows past H (H % 128 == 64)
+    float* o0 = row_ptr(ti, h0);
     for (int c = c0; c < r; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
@@ -740,6 +746,7 @@ struct ProbDB2 {
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     const float z[32] = {};
     const int64_t h = (int64_t)ti.m0 + row;
+    if (h >= H) return;
     for (int c = c0; c < r; c += cs) store_row_f32(row_ptr(ti, h) + c, z, 0.f, r - c < 32 ? r - c : 32);
   }
 };
@@ -776,7 +783,7 @@ struct ProbW2Dgrad {
   int H, I, r;
   int act;      // 0 = SwiGLU, 1 = GeGLU
   float clamp;  // activation clamp (0 = none)
-  __device__ int ntn() const { return I / 256; }
+  __device__ int ntn() const { return cdiv(I, 256); }
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const {
     return (kWide ? pl.wtile_off[pl.G] : pl.offsets[pl.G] / 128) * ntn();
@@ -817,7 +824,7 @@ struct ProbW2Dgrad {
     const int y0 = (int)(p - (threadIdx.x & 31));  // warp's first row
     const int64_t base0 = (int64_t)y0 * I + ti.n0;
     float dot = 0.0f;
-    for (int c = c0; c < 256; c += cs) {
+    for (int c = c0; c < 256 && ti.n0 + c < I; c += cs) {
       // the chunk's saved G, U and activation: coalesced loads, all in flight,
       // then redistributed so each lane holds its own row
       uint4 lg[4], lu[4], la[4];
@@ -860,7 +867,7 @@ struct ProbDA2 {
   int* err;
   float* dA2;
   int I, r;
-  __device__ int ntn() const { return I / 256; }
+  __device__ int ntn() const { return cdiv(I, 256); }
   __device__ int num_tiles() const { return pl.G * ntn(); }
   __device__ TileInfo tile(int t) const {
     const int q = t / ntn(), nt = t % ntn();  // plan slot of the group
@@ -889,7 +896,7 @@ struct ProbDA2 {
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int rb = row - (threadIdx.x & 31);  // warp's first row
     float* o0 = dA2 + ((int64_t)ti.g * r + rb) * I + ti.n0;
-    for (int c = c0; c < 256; c += cs) {
+    for (int c = c0; c < 256 && ti.n0 + c < I; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       warp_store_rows_f32(o0 + c, I, r - rb, v, 1.0f, 32, stg);
@@ -898,7 +905,8 @@ struct ProbDA2 {
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     if (row >= r) return;
     const float z[32] = {};
-    for (int c = c0; c < 256; c += cs) store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, z, 0.f, 32);
+    for (int c = c0; c < 256 && ti.n0 + c < I; c += cs)
+      store_row_f32(dA2 + ((int64_t)ti.g * r + row) * I + ti.n0 + c, z, 0.f, 32);
   }
 };
 
@@ -922,12 +930,12 @@ struct ProbW13Dgrad {
   float* dY13;
   int H, I, r;
   float s;
-  __device__ int ntn() const { return H / 256 + 1; }
+  __device__ int ntn() const { return cdiv(H, 256) + 1; }
   __device__ int num_tiles() const { return pl.wtile_off[pl.G] * ntn(); }
   __device__ TileInfo tile(int t) const {  // column-tile-major inside each group
     TileInfo ti;
     const int nt = wide_entry_decode(nmajor_wide_fetch(pl, t, ntn()), ti);
-    ti.sub = nt == H / 256;
+    ti.sub = nt == cdiv(H, 256);
     ti.n0 = ti.sub ? 0 : nt * 256;
     ti.nk = 2 * (I / kBK);
     return ti;
@@ -970,7 +978,7 @@ struct ProbW13Dgrad {
     if (!ti.sub) {
       const int y0 = (int)(p - (threadIdx.x & 31));  // warp's first row
       uint16_t* o0 = dXp + (int64_t)y0 * H + ti.n0;
-      for (int c = c0; c < 256; c += cs) {
+      for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
         float v[32];
         tmem_ld32(taddr + c, v);
         if (kEpiTmaStore)
@@ -1006,7 +1014,7 @@ struct ProbDB13 {
   int* err;
   float *dB1, *dB3;
   int I, r;
-  __device__ int ntm() const { return I / 128; }
+  __device__ int ntm() const { return cdiv(I, 128); }
   __device__ int num_tiles() const { return 2 * pl.G * ntm(); }
   __device__ TileInfo tile(int t) const {
     const int which = t / (pl.G * ntm());
@@ -1039,6 +1047,7 @@ struct ProbDB13 {
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{round16(r), 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int64_t i0 = (int64_t)ti.m0 + row - (threadIdx.x & 31);  // warp's first row
+    if (i0 >= I) return;                                              // rows past I (I % 128 == 64)
     float* o0 = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i0) * r;
     for (int c = c0; c < r; c += cs) {
       float v[32];
@@ -1048,6 +1057,7 @@ struct ProbDB13 {
   }
   __device__ void epilogue_empty(const TileInfo& ti, int row, int c0, int cs) const {
     const int64_t i = (int64_t)ti.m0 + row;
+    if (i >= I) return;
     float* out = (ti.sub ? dB3 : dB1) + ((int64_t)ti.g * I + i) * r;
     const float z[32] = {};
     for (int c = c0; c < r; c += cs) store_row_f32(out + c, z, 0.f, r - c < 32 ? r - c : 32);
@@ -1072,7 +1082,7 @@ struct ProbA13Expand {
   int* err;
   uint16_t* dXl;
   int H, r;
-  __device__ int ntn() const { return H / 256; }
+  __device__ int ntn() const { return cdiv(H, 256); }
   __device__ int nkr() const { return (r + 63) / 64; }
   __device__ int num_tiles() const { return pl.tok_tile[pl.A] * ntn(); }
   __device__ TileInfo tile(int t) const {
@@ -1105,7 +1115,7 @@ struct ProbA13Expand {
     const int64_t t0 = (int64_t)ti.m0 + row - (threadIdx.x & 31);  // warp's first row
     const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
     TmaStoreRing out(stg);  // whole-box stores: see ProbB2Expand
-    for (int c = c0; c < 256; c += cs) {
+    for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (nvalid <= 0) continue;
@@ -1136,7 +1146,7 @@ struct ProbDA13 {
   int64_t split_stride;
   int H, r, split;
   __device__ int ntm() const { return (2 * r + 127) / 128; }
-  __device__ int ntn() const { return H / 256; }
+  __device__ int ntn() const { return cdiv(H, 256); }
   __device__ int num_tiles() const { return split * pl.A * ntm() * ntn(); }
   __device__ TileInfo tile(int t) const {
     const int per = ntm() * ntn();
@@ -1173,7 +1183,7 @@ struct ProbDA13 {
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int m = ti.m0 + row;
     const bool ok = m < 2 * r;
-    for (int c = c0; c < 256; c += cs) {
+    for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       if (ok) store_row_f32(out_row(ti, m) + c, v, 1.0f, 32);
@@ -1183,7 +1193,7 @@ struct ProbDA13 {
     const int m = ti.m0 + row;
     if (m >= 2 * r) return;
     const float z[32] = {};
-    for (int c = c0; c < 256; c += cs) store_row_f32(out_row(ti, m) + c, z, 0.f, 32);
+    for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) store_row_f32(out_row(ti, m) + c, z, 0.f, 32);
   }
 };
 
@@ -1215,7 +1225,7 @@ struct ProbW2Pair : ProbW2 {
   __device__ TileInfo tile_at(int, int4 w) const {
     TileInfo ti;
     const int nt = wide_entry_decode(w, ti);
-    ti.sub = nt == H / 256;
+    ti.sub = nt == cdiv(H, 256);
     ti.n0 = ti.sub ? 0 : nt * 256;
     ti.nk = I / kBK;
     return ti;

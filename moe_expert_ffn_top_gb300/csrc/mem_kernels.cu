@@ -230,7 +230,7 @@ __global__ void combine_rows_kernel(PlanView pl, const uint16_t* __restrict__ ba
   const int k = pl.k;
   for (int64_t t = w0; t < pl.T; t += nw) {
     const int* rows = pl.row_of_route + t * k;
-    // two 8-column groups per lane and pass (c and c + 256; H % 256 == 0), so up to
+    // two 8-column groups per lane and pass (c and c + 256, the second skipped past H), so up to
     // 2 x 8 routed-row loads are in flight before they are added in slot order
     for (int c = lane * 8; c < H; c += 2 * 32 * 8) {
       const int c2 = c + 32 * 8;

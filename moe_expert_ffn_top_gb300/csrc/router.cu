@@ -157,7 +157,7 @@ struct ProbRouterDx {
   uint16_t* dx;
   int64_t T;
   int H, E;
-  __device__ int ntn() const { return H / 256; }
+  __device__ int ntn() const { return cdiv(H, 256); }
   __device__ int num_tiles() const { return at.tok_tile[at.n] * ntn(); }
   __device__ TileInfo tile(int t) const {
     TileInfo ti = adapter_token_tile(at, t / ntn());
@@ -180,7 +180,7 @@ struct ProbRouterDx {
     const int64_t t0 = (int64_t)ti.m0 + row - lane;  // the warp's first token
     const int nvalid = (int)(ti.mend - t0 < 32 ? ti.mend - t0 : 32);
     uint16_t* base = dx + t0 * H + ti.n0;
-    for (int c = c0; c < 256; c += cs) {
+    for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
       uint4 u[4];
 #pragma unroll
       for (int s = 0; s < 4; ++s) {  // coalesced loads of the warp's rows, guarded at the tail
@@ -219,7 +219,7 @@ struct ProbRouterDW {
   int64_t T;
   int H, E;
   __device__ int ntm() const { return (E + 127) / 128; }
-  __device__ int ntn() const { return H / 256; }
+  __device__ int ntn() const { return cdiv(H, 256); }
   __device__ int num_tiles() const { return tbase[at.n]; }
   __device__ TileInfo tile(int t) const {
     int a = 0;
@@ -257,7 +257,7 @@ struct ProbRouterDW {
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     const int m0 = ti.m0 + row - (threadIdx.x & 31);  // the warp's first expert row
     float* o0 = out_of(ti) + (int64_t)m0 * H + ti.n0;
-    for (int c = c0; c < 256; c += cs) {
+    for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
       warp_store_rows_f32(o0 + c, H, E - m0, v, 1.0f, 32, stg);
@@ -269,7 +269,7 @@ struct ProbRouterDW {
     if (m >= E) return;
     const float z[32] = {};
     float* o = out_of(ti) + (int64_t)m * H + ti.n0;
-    for (int c = c0; c < 256; c += cs) store_row_f32(o + c, z, 0.0f, 32);
+    for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) store_row_f32(o + c, z, 0.0f, 32);
   }
 };
 
@@ -387,14 +387,14 @@ int run_router_backward(const moe_lora_dims* d, const AdapterTable& at, const ui
     p.T = T;
     p.H = H;
     p.E = E;
-    LAUNCH(launch_gemm(p, at.tok_tile[at.n] * (H / 256), num_sms, stream, K_ROUTER_DX));
+    LAUNCH(launch_gemm(p, at.tok_tile[at.n] * cdiv(H, 256), num_sms, stream, K_ROUTER_DX));
   }
   {
     ProbRouterDW p;
     MAP(tmap_2d(&p.mdl, dl, E, T, 64, 64));
     MAP(tmap_2d(&p.mx, x, H, T, 64, 64));
     p.at = at;
-    const int per = ((E + 127) / 128) * (H / 256);
+    const int per = ((E + 127) / 128) * cdiv(H, 256);
     p.tbase[0] = 0;
     for (int a = 0; a < A; ++a) {
       p.split[a] = router_split(at.tok_off[a + 1] - at.tok_off[a]);

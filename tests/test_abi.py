@@ -53,7 +53,7 @@ def test_workspace_sizes(L):
     p = m.make_dims(65536, 4096, 2048, 256, 6, 128)
     P = 65536 * 6 + 256 * 127
     assert m.moe_lora_workspace_bytes(p, m.MOE_LORA_WS_SAVED) >= 2 * P * (3 * 2048 + 256)
-    for bad in (dict(H=500), dict(I=128), dict(r=12), dict(r=136), dict(k=0), dict(k=33), dict(E=0), dict(A=0)):
+    for bad in (dict(H=500), dict(I=96), dict(H=32), dict(I=0), dict(r=12), dict(r=136), dict(k=0), dict(k=33), dict(E=0), dict(A=0)):
         assert m.moe_lora_workspace_bytes(_dims(**bad), 0) == 0, bad
 
 

@@ -162,6 +162,21 @@ def test_ranks_off_the_tile_boundaries(r):
     _full_check(inp, shp, out)
 
 
+@pytest.mark.parametrize("H,I", [(576, 320), (192, 64), (320, 448)])
+def test_widths_off_the_tile_boundaries(H, I):
+    """H and I multiples of 64 but not of the 128- and 256-wide tiles: a last W13
+    column tile with 64 of its 128 columns (I % 128 = 64), last W2 / W13-dgrad /
+    expand column tiles with 64 or 192 of 256 (H % 256), last dB2 row tiles with 64
+    of 128 rows (H % 128 = 64), last dB1/dB3 row tiles (I % 128 = 64), last W2-dgrad
+    and dA2 column tiles with 64 or 192 of 256 (I % 256); NaN-poisoned workspaces
+    and outputs, so nothing past an edge can leak."""
+    shp = Shape(T=300, H=H, I=I, E=8, k=2, r=24, mask_frac=0.1)
+    inp = make_inputs(shp, seed=60 + H + I)
+    out = run_gpu(inp, shp, poison=True)
+    assert out["err"] == 0
+    _full_check(inp, shp, out)
+
+
 def test_saturated_gates():
     """x scaled by 64: gate pre-activations reach the hundreds, so silu sits at its
     limits (exp(-z) overflows to inf for z < -88, giving 0; z for large z) in the

@@ -69,7 +69,7 @@ def _check_selection(ids_g, w_g, l_g, l_ref, ids_ref, w_ref, tie_tol):
 
 
 @pytest.mark.parametrize("T,H,E,k", [(300, 512, 16, 2), (1000, 1024, 128, 8), (517, 4096, 256, 6),
-                                     (4096, 4096, 256, 6), (129, 256, 32, 32)])
+                                     (4096, 4096, 256, 6), (129, 256, 32, 32), (200, 576, 64, 4)])
 def test_router_forward_matches_oracle(T, H, E, k):
     inp = make_router_inputs(T, H, E, k, seed=T + E, device="cuda")
     _, _, ids, w, lg = _gpu_forward(inp, T, H, E, k)
@@ -103,7 +103,8 @@ def test_router_ties_go_to_the_lower_id():
     _check_selection(ids, w, lg, l_ref, ids_ref, w_ref, 1e-5 * float(l_ref.abs().max()) + 1e-6)
 
 
-@pytest.mark.parametrize("T,H,E,k", [(300, 512, 16, 2), (1000, 1024, 128, 8), (4096, 4096, 256, 6)])
+@pytest.mark.parametrize("T,H,E,k", [(300, 512, 16, 2), (1000, 1024, 128, 8), (4096, 4096, 256, 6),
+                                     (200, 576, 64, 4), (150, 64, 16, 2)])
 def test_router_backward_matches_oracle(T, H, E, k):
     inp = make_router_inputs(T, H, E, k, seed=11 * T + E, device="cuda")
     d, sc, ids, w, _ = _gpu_forward(inp, T, H, E, k, logits=False)

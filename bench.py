@@ -99,10 +99,12 @@ def kernel_work(T, R, H, I, r, k, E=256):
 # that builds and launches it.  A change to another problem type leaves the record
 # valid; comments and blank lines do not count.
 ENGINE_SOURCES = ("sm100_ptx.cuh", "common.cuh", "gemm_engine.cuh", "gemm_pair.cuh")
-PROBLEM_OF = {"shrink_x_A13": "ProbShrink", "w13_lora_swiglu": "ProbW13", "w2_a2": "ProbW2",
-              "b2_expand": "ProbB2Expand", "dy_b2": "ProbDyB2", "dB2": "ProbDB2",
-              "w2_dgrad_swiglu_bwd": "ProbW2Dgrad", "dA2": "ProbDA2", "w13_dgrad_b13": "ProbW13Dgrad",
-              "dB13": "ProbDB13", "a13_expand": "ProbA13Expand", "dA13": "ProbDA13"}
+PROBLEM_OF = {"shrink_x_A13": ("ProbShrink", "K_SHRINK"), "w13_lora_swiglu": ("ProbW13T", "K_W13"),
+              "w2_a2": ("ProbW2T", "K_W2"), "b2_expand": ("ProbB2Expand", "K_B2_EXPAND"),
+              "dy_b2": ("ProbDyB2", "K_DYB2"), "dB2": ("ProbDB2", "K_DB2"),
+              "w2_dgrad_swiglu_bwd": ("ProbW2DgradT", "K_W2_DGRAD"), "dA2": ("ProbDA2", "K_DA2"),
+              "w13_dgrad_b13": ("ProbW13DgradT", "K_W13_DGRAD"), "dB13": ("ProbDB13", "K_DB13"),
+              "a13_expand": ("ProbA13Expand", "K_A13_EXPAND"), "dA13": ("ProbDA13", "K_DA13")}
 
 
 def _csrc(f):
@@ -117,22 +119,25 @@ def _code(text):
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
-def problem_source(prob):
+def problem_source(prob, slot):
     """The section of gemm_problems.cuh that defines `prob` (sections are delimited by
     '// ====' lines; the file's preamble, shared helpers included, comes with every
-    problem) and the host blocks of forward.cu / backward.cu that launch it."""
+    problem) and the host block of forward.cu / backward.cu that builds and launches
+    it: from the step's comment line above the first launch with profiler slot `slot`
+    to the last such launch."""
     text = _csrc("gemm_problems.cuh")
     parts = re.split(r"^// =+$", text, flags=re.M)
     mine = [p for p in parts if re.search(r"\bstruct\s+" + prob + r"\b(?!\w)", p)]
     host = []
     for f in ("forward.cu", "backward.cu"):
         lines = _csrc(f).splitlines()
-        for i, line in enumerate(lines):
-            if re.match(r"\s*" + prob + r"\s+p;", line):
-                j = i
-                while j < len(lines) and "launch_gemm" not in lines[j]:
-                    j += 1
-                host.append("\n".join(lines[i:j + 1]))
+        hits = [i for i, line in enumerate(lines) if re.search(r"\b" + slot + r"\b", line)]
+        if not hits:
+            continue
+        i = hits[0]
+        while i > 0 and not re.match(r"^  // \S", lines[i]):
+            i -= 1
+        host.append("\n".join(lines[i:hits[-1] + 1]))
     return parts[0] + "".join(mine) + "".join(host)
 
 
@@ -142,9 +147,9 @@ def src_hash(kernel):
     for f in ENGINE_SOURCES:
         h.update(f.encode())
         h.update(_code(_csrc(f)).encode())
-    prob = PROBLEM_OF.get(kernel, kernel)
+    prob, slot = PROBLEM_OF[kernel]
     h.update(prob.encode())
-    h.update(_code(problem_source(prob)).encode())
+    h.update(_code(problem_source(prob, slot)).encode())
     return h.hexdigest()[:16]
 
 
@@ -274,16 +279,18 @@ def per_kernel_pass(m, fn, steps, only=None):
     return prof
 
 
-def measure_workload(m, name, seed, args, local_rank, dist, world):
+def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False):
     """A compact record of one more workload (the same step: plan + forward +
     backward), measured after the headline: step time with its own clock record,
     the per-kernel times, the workspace sizes and, for several adapters, the same
-    work as standalone single-adapter passes back to back."""
+    work as standalone single-adapter passes back to back.  mx_once: an MXFP4 base
+    decoded once per pass (base_fmt 2) instead of inside the GEMMs (1)."""
     shp = shape(name)
     inp = make_inputs(shp, seed=seed, device="cuda")
     T, H, I, E, k, r, A = shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A
     R = int((inp["topk_ids"] >= 0).sum())
-    d = m.make_dims(T, H, I, E, k, r, A, shp.scale, base_fmt=1 if shp.base_fmt == "mxfp4" else 0)
+    d = m.make_dims(T, H, I, E, k, r, A, shp.scale,
+                    base_fmt=(2 if mx_once else 1) if shp.base_fmt == "mxfp4" else 0)
     offs = inp["adapter_offsets"].tolist() if A > 1 else None
     ws = m.Workspaces.allocate(d)
     y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
@@ -309,7 +316,9 @@ def measure_workload(m, name, seed, args, local_rank, dist, world):
     pk = peaks()
     prof = per_kernel_pass(m, step, args.steps)
     value = job_tflops(world, flops, ms)
-    rec = {"workload": f"{name}: T={T} H={H} I={I} E={E} top{k} r={r} A={A} s={shp.scale} base={shp.base_fmt}",
+    base = shp.base_fmt + ((" decoded once per pass" if mx_once else " decoded in the GEMMs")
+                           if shp.base_fmt == "mxfp4" else "")
+    rec = {"workload": f"{name}: T={T} H={H} I={I} E={E} top{k} r={r} A={A} s={shp.scale} base={base}",
            "ms_per_step": round(ms, 3), "value": round(value, 2), "unit": "TFLOP/s",
            "pct_of_bf16_peak": round(100 * value / world / pk["bf16"], 2), "live_routes": R,
            "tflop_per_step": round(flops / 1e12, 4), "launches_per_step": launches, "clocks": clk,
@@ -677,6 +686,7 @@ def run_ours(args, rank, world, local_rank):
     subs = {}
     if args.workload == "prod" and world == 1 and not args.no_sub_records:
         subs["mxfp4"] = measure_workload(m, "prod_mxfp4", 3, args, local_rank, dist, world)
+        subs["mxfp4_once"] = measure_workload(m, "prod_mxfp4", 3, args, local_rank, dist, world, mx_once=True)
         subs["multi"] = measure_workload(m, "multi", 4, args, local_rank, dist, world)
 
     if rank == 0:
@@ -745,7 +755,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="prod", choices=["prod", "prod_mxfp4", "prod_e16", "tiny", "edge", "multi"])
+    ap.add_argument("--workload", default="prod", choices=["prod", "prod_mxfp4", "prod_e16", "prod_e16_mxfp4", "tiny", "edge", "multi"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-records", action="store_true",

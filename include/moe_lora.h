@@ -80,7 +80,13 @@ extern "C" {
  * thread SwiGLU/GeGLU and an activation clamp through every kernel (PR #9,
  * Summary); which pre-activations the clamp applies to is not stated there, and
  * this library clamps both gate and up.
- * base_fmt 0 (bf16 base weights) or 1 (MXFP4 base weights, see moe_lora_weights).
+ * base_fmt 0: bf16 base weights.  base_fmt 1 or 2: MXFP4 base weights (see
+ * moe_lora_weights), decoded exactly to bf16 and fed to the same BF16 tensor-core
+ * contractions -- 1: inside the expert GEMMs, tile by tile in shared memory, so
+ * the base occupies only its packed bytes and scales (no bf16 copy anywhere);
+ * 2: once per forward into the saved workspace (3 * E*I*H bf16 more), which the
+ * backward reuses -- faster on GB300 today, since the in-GEMM decode is repeated
+ * by every row tile of an expert.
  * T may be 0 (every call is a no-op). */
 typedef struct moe_lora_dims {
   int64_t T;        /* tokens */
@@ -93,19 +99,19 @@ typedef struct moe_lora_dims {
   int32_t block_m;  /* plan padding unit, 128 */
   float scale;      /* side-LoRA scale s */
   int32_t act;      /* 0 = SwiGLU, 1 = GeGLU */
-  int32_t base_fmt; /* 0 = bf16, 1 = MXFP4 */
+  int32_t base_fmt; /* 0 = bf16, 1 = MXFP4 decoded in the GEMMs, 2 = MXFP4 decoded once */
   float act_clamp;  /* activation clamp (0 = none) */
 } moe_lora_dims;
 
 /* Frozen base and adapter weights (device).
- *   W1, W3 [E,I,H]; W2 [E,H,I]: bf16 bits when base_fmt = 0.  When base_fmt = 1
+ *   W1, W3 [E,I,H]; W2 [E,H,I]: bf16 bits when base_fmt = 0.  When base_fmt = 1 or 2
  *     (MXFP4) they hold E2M1 element codes, two per byte (low nibble = lower index
  *     along the last axis), and S1, S3 [E,I,H/32], S2 [E,H,I/32] hold one UE8M0
  *     scale byte (value 2^(b-127); 255 decodes to NaN) per 32 consecutive elements
  *     of that axis: the OCP MX encoding, read from the pages' "E2M1 values with a
- *     UE8M0 scale per 32 elements".  The base is decoded exactly to bf16 (in the
- *     saved workspace) and the BF16 tensor-core path runs on it; the adapters
- *     stay bf16.  S1/S3/S2 are ignored (may be NULL) when base_fmt = 0.
+ *     UE8M0 scale per 32 elements" (base_fmt 1 or 2).  The base is decoded exactly
+ *     to bf16 and the BF16 tensor-core path runs on it; the adapters stay bf16.
+ *     S1/S3/S2 are ignored (may be NULL) when base_fmt = 0.
  *   A1, A3 [A,r,H] (shared by experts); B1, B3 [A,E,I,r] (expert-local);
  *   A2 [A,E,r,I] (expert-local); B2 [A,H,r] (shared), bf16 bits. */
 typedef struct moe_lora_weights {
@@ -212,7 +218,7 @@ MOE_LORA_API int moe_lora_plan_readback(const moe_lora_dims* dims, const void* p
                                         int32_t* offsets, int32_t* row_of_route, int32_t* route_of_row,
                                         int64_t route_of_row_cap, void* stream);
 
-/* Decodes an MXFP4 tensor (the frozen-base format of moe_lora_dims.base_fmt = 1) to
+/* Decodes an MXFP4 tensor (the frozen-base format of moe_lora_dims.base_fmt = 1 and 2) to
  * bf16, exactly, on `stream`: elems E2M1 codes (two per byte, the lower index in the
  * low nibble; bit 3 = sign, magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}) with one UE8M0
  * scale byte per 32 consecutive elements (b -> 2^(b-127); b = 0 gives 2^-127, b = 255

@@ -95,7 +95,7 @@ static int check_weights(const moe_lora_dims* d, const moe_lora_weights* w) {
     const int rc = check_ptr(p);
     if (rc) return rc;
   }
-  if (d->base_fmt == 1) {
+  if (d->base_fmt == 1 || d->base_fmt == 2) {
     const void* sc[] = {w->S1, w->S3, w->S2};
     for (const void* p : sc) {
       const int rc = check_ptr(p);

@@ -57,10 +57,13 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   const int max_tok_tiles = (int)((T + 127) / 128) + d->A;
   const int max_row_tiles = (int)(P / 128);
   cudaError_t ce;
-  // Base weights: as given (bf16), or the copy the forward decoded from MXFP4.
-  const void* bW1 = d->base_fmt == 1 ? (const void*)(sv + SL.W1) : w->W1;
-  const void* bW3 = d->base_fmt == 1 ? (const void*)(sv + SL.W3) : w->W3;
-  const void* bW2 = d->base_fmt == 1 ? (const void*)(sv + SL.W2) : w->W2;
+  // An MXFP4 base: decoded inside the two dgrad GEMMs, stage by stage (base_fmt 1,
+  // the ...T<true> problem types), or the bf16 copy the forward decoded into `saved`
+  // (base_fmt 2).
+  const bool mx = d->base_fmt == 1;
+  const void* bW1 = d->base_fmt == 2 ? (const void*)(sv + SL.W1) : w->W1;
+  const void* bW3 = d->base_fmt == 2 ? (const void*)(sv + SL.W3) : w->W3;
+  const void* bW2 = d->base_fmt == 2 ? (const void*)(sv + SL.W2) : w->W2;
 #define MAP(call)                                 \
   do {                                            \
     if ((call) != 0) return MOE_LORA_ERR_CUDA;    \
@@ -101,11 +104,12 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   // B2: routed dy rows and the scaled shared-expand gradients
   LAUNCH(launch_gather_bwd(pl, dy, dyB2, topk_w, Dp, D2p, dZ2p, d->H, d->r, d->scale, num_sms, stream));
   // B3/B4: W2^T dgrad + A2 path + SwiGLU backward + router dots
-  {
-    ProbW2Dgrad p;
+  auto w2d = [&](auto p) -> int {
     MAP(tmap_2d(&p.mDp, Dp, H, P, 64, 128));
     MAP(tmap_2d(&p.mD2p, D2p, r, P, 64, 128));
-    MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 64));
+    if (!mx) MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 64));
+    p.W2q = (const uint8_t*)w->W2;
+    p.S2q = w->S2;
     MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, 64));
     p.pl = pl;
     p.err = pl.err;
@@ -122,8 +126,11 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.act = d->act;
     p.clamp = d->act_clamp;
     LAUNCH(launch_gemm(p, max_row_tiles * cdiv(d->I, 256), num_sms, stream, K_W2_DGRAD));
-  }
-  LAUNCH(launch_dw(pl, part, ProbW2Dgrad::kPartsPerTile * cdiv(d->I, 256), dw, num_sms, stream));
+    return 0;
+  };
+  if (int rc = mx ? w2d(ProbW2DgradT<true>{}) : w2d(ProbW2DgradT<false>{})) return rc;
+  const int parts = mx ? ProbW2DgradT<true>::kPartsPerTile : ProbW2DgradT<false>::kPartsPerTile;
+  LAUNCH(launch_dw(pl, part, parts * cdiv(d->I, 256), dw, num_sms, stream));
   // dA2 per (adapter, expert)
   {
     ProbDA2 p;
@@ -137,12 +144,17 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     LAUNCH(launch_gemm(p, (int)G * cdiv(d->I, 256), num_sms, stream, K_DA2));
   }
   // B5: W13^T dgrad + B1/B3 path
-  {
-    ProbW13Dgrad p;
+  auto w13d = [&](auto p) -> int {
     MAP(tmap_2d(&p.mdG, dG, I, P, 64, 128));
     MAP(tmap_2d(&p.mdU, dU, I, P, 64, 128));
-    MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 64));
-    MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 64));
+    if (!mx) {
+      MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 64));
+      MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 64));
+    }
+    p.W1q = (const uint8_t*)w->W1;
+    p.W3q = (const uint8_t*)w->W3;
+    p.S1q = w->S1;
+    p.S3q = w->S3;
     MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 64));
     MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 64));
     p.pl = pl;
@@ -155,7 +167,9 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.r = d->r;
     p.s = d->scale;
     LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W13_DGRAD));
-  }
+    return 0;
+  };
+  if (int rc = mx ? w13d(ProbW13DgradT<true>{}) : w13d(ProbW13DgradT<false>{})) return rc;
   // dB1 / dB3 per (adapter, expert)
   {
     ProbDB13 p;

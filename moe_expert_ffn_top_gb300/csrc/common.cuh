@@ -2,6 +2,7 @@
 // layouts (host), and the device view of a routing plan.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -20,7 +21,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Returns MOE_LORA_OK when the sizes are supported.
 inline int check_dims(const moe_lora_dims* d) {
   if (!d) return MOE_LORA_ERR_NULL;
-  if ((d->act != 0 && d->act != 1) || (d->base_fmt != 0 && d->base_fmt != 1)) return MOE_LORA_ERR_UNSUPPORTED;
+  if ((d->act != 0 && d->act != 1) || d->base_fmt < 0 || d->base_fmt > 2) return MOE_LORA_ERR_UNSUPPORTED;
   if (!(d->act_clamp >= 0.0f) || d->act_clamp > 3.0e38f) return MOE_LORA_ERR_DIMS;
   if (d->T < 0 || d->T > (int64_t)1 << 30) return MOE_LORA_ERR_DIMS;
   if (d->H < 64 || d->H % 64 || d->I < 64 || d->I % 64) return MOE_LORA_ERR_DIMS;
@@ -69,8 +70,9 @@ inline PlanLayout plan_layout(const moe_lora_dims* d) {
   return L;
 }
 
-// What the forward keeps for the backward (bf16 unless noted).  With an MXFP4
-// base it also holds the decoded bf16 base W1, W3 [E,I,H] and W2 [E,H,I].
+// What the forward keeps for the backward (bf16).  An MXFP4 base decoded inside the
+// GEMMs (base_fmt 1) is never stored in bf16; decoded once per pass (base_fmt 2) it
+// adds the bf16 W1, W3 [E,I,H] and W2 [E,H,I], which the backward reuses.
 struct SavedLayout {
   size_t Y13p, G, U, Act, Z2w, W1, W3, W2, total;   // [P,2r], [P,I], [P,I], [P,I], [T,r]
 };
@@ -84,7 +86,7 @@ inline SavedLayout saved_layout(const moe_lora_dims* d) {
   L.U = take(2 * (size_t)P * d->I);
   L.Act = take(2 * (size_t)P * d->I);
   L.Z2w = take(2 * (size_t)T * d->r);
-  const size_t wbytes = d->base_fmt == 1 ? 2 * (size_t)d->E * d->I * d->H : 0;
+  const size_t wbytes = d->base_fmt == 2 ? 2 * (size_t)d->E * d->I * d->H : 0;
   L.W1 = take(wbytes);
   L.W3 = take(wbytes);
   L.W2 = take(wbytes);
@@ -237,6 +239,70 @@ __device__ __forceinline__ void ld_bf16x8(const uint16_t* src, float* v) {
 }
 __device__ __forceinline__ void st_f32x4(float* dst, const float* v) {
   *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// ------------------------------------------------------------------ MXFP4 (E2M1 + UE8M0)
+// Two E2M1 codes (one byte, the lower index in the low nibble) to two f16 values
+// (low half = low nibble) with the hardware conversion; every E2M1 value is exact in
+// f16.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(d) : "h"((uint16_t)byte));
+  return d;
+}
+// UE8M0 scale byte b -> 2^(b-127) (b = 0: the fp32 subnormal 2^-127; b = 255: NaN).
+__device__ __forceinline__ float ue8m0_to_float(uint32_t b) {
+  return __uint_as_float(b == 0 ? 0x00400000u : b == 255 ? 0x7FC00000u : b << 23);
+}
+// Eight E2M1 codes (one 32-bit word, element 0 in the lowest nibble) times the scale
+// `sc`, as eight bf16 values in one 16-byte vector.  Every product of an E2M1 value
+// and a power of two is a bf16 value (or overflows to inf), so nothing is rounded.
+__device__ __forceinline__ uint4 mx_decode8(uint32_t w, float sc) {
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t h2 = e2m1x2_to_f16x2((w >> (8 * j)) & 0xFFu);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    o[j] = pack_bf16x2(f.x * sc, f.y * sc);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The same decode without conversion instructions, for scale bytes b in [2, 252]
+// (where every product is a normal bf16 value): the bf16 bit patterns of the E2M1
+// magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} are looked up with byte permutes (high
+// bytes 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80 C0), each code's sign
+// bit is moved to bit 15 of its half with the permute's sign-replicating mode, and
+// one bf16x2 multiply by 2^(b-127) (bf16 bits b << 7 in both halves) scales them --
+// exactly, as the product of a value of at most two significant bits and a power of
+// two is representable.  scale2 = (b << 7) * 0x10001.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint4 mx_decode8_fast(uint32_t w, uint32_t scale2) {
+  const uint32_t s03 = w & 0x7777u, s47 = (w >> 16) & 0x7777u;  // magnitude codes, 4 per selector
+  const uint32_t hA = prmt(0x3F3F3F00u, 0x40404040u, s03), lA = prmt(0xC0800000u, 0xC0804000u, s03);
+  const uint32_t hB = prmt(0x3F3F3F00u, 0x40404040u, s47), lB = prmt(0xC0800000u, 0xC0804000u, s47);
+  const uint32_t w4 = w << 4;  // byte k's top bit = sign of element 2k (w's own: of element 2k + 1)
+  uint32_t o[4] = {prmt(lA, hA, 0x5140u), prmt(lA, hA, 0x7362u), prmt(lB, hB, 0x5140u), prmt(lB, hB, 0x7362u)};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t sg = prmt(w4, w, ((8u | (4u + k)) << 12) | ((8u | k) << 4));  // 0xFF bytes where negative
+    o[k] = mul_bf16x2(o[k] | (sg & 0x80008000u), scale2);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+// Either decode, by the scale byte.
+__device__ __forceinline__ uint4 mx_decode8_any(uint32_t w, uint32_t b) {
+  if (b >= 2u && b <= 252u) return mx_decode8_fast(w, (b << 7) * 0x10001u);
+  return mx_decode8(w, ue8m0_to_float(b));
 }
 
 }  // namespace moelora

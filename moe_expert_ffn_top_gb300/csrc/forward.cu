@@ -36,12 +36,15 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   const int max_row_tiles = (int)(P / 128);
   int rc = 0;
   cudaError_t ce;
-  // Base weights for the BF16 path: as given, or decoded from MXFP4 into `saved`
-  // (the backward reuses the decoded copy).
+  // An MXFP4 base: base_fmt 1 decodes it inside the expert GEMMs, stage by stage,
+  // into the same bf16 operand tiles (ProbW13T<true>, ProbW2T<true>), so no decoded
+  // copy exists anywhere; base_fmt 2 decodes it once per pass into `saved` (which the
+  // backward reuses) and runs the bf16 GEMMs on that copy.
+  const bool mx = d->base_fmt == 1;
   const void* bW1 = w->W1;
   const void* bW3 = w->W3;
   const void* bW2 = w->W2;
-  if (d->base_fmt == 1) {
+  if (d->base_fmt == 2) {
     uint16_t* q1 = (uint16_t*)(sv + SL.W1);
     uint16_t* q3 = (uint16_t*)(sv + SL.W3);
     uint16_t* q2 = (uint16_t*)(sv + SL.W2);
@@ -80,12 +83,17 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   // F2: routed rows
   LAUNCH(launch_gather_fwd(pl, x, Y13, Xp, Y13p, d->H, 2 * d->r, num_sms, stream));
   // F3: W13 + expert-local expand + SwiGLU
-  {
-    ProbW13 p;
+  auto w13 = [&](auto p) -> int {
     MAP(tmap_2d(&p.mXp, Xp, H, P, 64, 128));
     MAP(tmap_2d(&p.mY13p, Y13p, 2 * r, P, 64, 128));
-    MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 128));
-    MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 128));
+    if (!mx) {
+      MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 128));
+      MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 128));
+    }
+    p.W1q = (const uint8_t*)w->W1;
+    p.W3q = (const uint8_t*)w->W3;
+    p.S1q = w->S1;
+    p.S3q = w->S3;
     MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 128));
     MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 128));
     MAP(tmap_2d_store32(&p.mG, Gs, I, P));
@@ -102,12 +110,15 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.act = d->act;
     p.clamp = d->act_clamp;
     LAUNCH(launch_gemm(p, max_row_tiles * cdiv(d->I, 128), num_sms, stream, K_W13));
-  }
+    return 0;
+  };
+  if ((rc = mx ? w13(ProbW13T<true>{}) : w13(ProbW13T<false>{}))) return rc;
   // F4/F5: W2 + expert-local A2 shrink
-  if (kW2OneSmWide) {
-    ProbW2 p;
+  auto w2 = [&](auto p) -> int {
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
-    MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 256));
+    if (!mx) MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 256));
+    p.W2q = (const uint8_t*)w->W2;
+    p.S2q = w->S2;
     MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, (uint32_t)((r + 15) / 16 * 16)));
     MAP(tmap_2d_store32(&p.mO, O, H, P));
     p.pl = pl;
@@ -118,6 +129,10 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.I = d->I;
     p.r = d->r;
     LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W2));
+    return 0;
+  };
+  if (kW2OneSmWide || mx) {
+    if ((rc = mx ? w2(ProbW2T<true>{}) : w2(ProbW2T<false>{}))) return rc;
   } else {
     ProbW2Pair p;
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));

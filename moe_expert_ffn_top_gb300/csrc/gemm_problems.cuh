@@ -414,10 +414,14 @@ struct ProbShrink {
 // price of an epilogue that no longer overlaps the next tile's main loop.  With the
 // fast silu that trade pays (same-box 9.33 -> 9.04 ms at 65,536 tokens, E256).
 constexpr bool kW13Wide = true;
-struct ProbW13 {
+// MX: W1/W3 are MXFP4, decoded into the stage by the epilogue warps (no TMA for them).
+template <bool MX>
+struct ProbW13T {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr bool kWide = kW13Wide;
+  static constexpr bool kDecode = MX;
   static constexpr int kEpiWarps = kWide ? 8 : 4;
+  const uint8_t *W1q, *W3q, *S1q, *S3q;  // MX: packed [E,I,H/2], scales [E,I,H/32]
   CUtensorMap mXp, mY13p, mW1, mW3, mB1, mB3;  // Xp (H,P) box(64,128); Y13p (2r,P) box(64,128);
                                                // W1/W3 (H,I,E) box(64,128,1); B1/B3 (r,I,G) box(64,128,1)
   CUtensorMap mG, mU, mAct;                    // outputs (I,P), 32 x 32 store boxes
@@ -454,16 +458,26 @@ struct ProbW13 {
     const int nb = H / kBK;
     const int e = ti.g % pl.E;
     if (ks < nb) {
-      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 2 * 128 * 128);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 0 : 2 * 128 * 128));
       load_a_wide(ti, sa, &mXp, bar, ks * kBK);
-      tma_load_3d(sb, &mW1, bar, ks * kBK, ti.n0, e);
-      tma_load_3d(sb + 128 * 128, &mW3, bar, ks * kBK, ti.n0, e);
+      if (!MX) {
+        tma_load_3d(sb, &mW1, bar, ks * kBK, ti.n0, e);
+        tma_load_3d(sb + 128 * 128, &mW3, bar, ks * kBK, ti.n0, e);
+      }
     } else {
       const int j = ks - nb, half = j / nkr(), kb = j % nkr();
       mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 128 * 128);
       load_a_wide(ti, sa, &mY13p, bar, half * r + kb * kBK);
       tma_load_3d(sb, half ? &mB3 : &mB1, bar, kb * kBK, ti.n0, ti.g);
     }
+  }
+  // MX, base K steps: rows 0..127 of the B tile are W1 rows n0.., 128..255 W3 rows
+  __device__ bool decodes(const TileInfo&, int ks) const { return MX && ks < H / kBK; }
+  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
+    const int64_t row = (int64_t)(ti.g % pl.E) * I + ti.n0;
+    const int64_t po = row * (H / 2) + ks * (kBK / 2), so = row * (H / 32) + ks * (kBK / 32);
+    const int lim = I - ti.n0 < 128 ? I - ti.n0 : 128;
+    return MxSrc{{W1q + po, W3q + po}, {S1q + so, S3q + so}, H / 2, H / 32, {lim, lim}, false};
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const {
     const int nb = H / kBK;
@@ -493,6 +507,7 @@ struct ProbW13 {
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
+using ProbW13 = ProbW13T<false>;
 
 // =====================================================================================
 // Forward F4/F5 -- W2 expert GEMM with the expert-local A2 shrink:
@@ -503,10 +518,14 @@ struct ProbW13 {
 // two-SM engine (ProbW2Pair, false).  With the TMA-store epilogue: 4.22 vs 4.47 ms
 // (same box, 65,536 tokens, E256).
 constexpr bool kW2OneSmWide = true;
-struct ProbW2 {
+// MX: W2 is MXFP4, decoded into the stage by the epilogue warps (no TMA for it).
+template <bool MX>
+struct ProbW2T {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr bool kWide = kW2OneSmWide;
+  static constexpr bool kDecode = MX;
   static constexpr int kEpiWarps = kWide ? 8 : 4;
+  const uint8_t *W2q, *S2q;  // MX: packed [E,H,I/2], scales [E,H,I/32]
   CUtensorMap mAct, mW2, mA2;  // Act (I,P) box(64,128); W2 (I,H,E) box(64,256,1); A2 (I,r,G) box(64,r16,1)
   CUtensorMap mO;              // output (H,P), 32 x 32 store boxes
   PlanView pl;
@@ -533,14 +552,24 @@ struct ProbW2 {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     if (!ti.sub) {
-      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 256 * 128);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 0 : 256 * 128));
       load_a_wide(ti, sa, &mAct, bar, ks * kBK);
-      tma_load_3d(sb, &mW2, bar, ks * kBK, ti.n0, ti.g % pl.E);
+      if (!MX) tma_load_3d(sb, &mW2, bar, ks * kBK, ti.n0, ti.g % pl.E);
     } else {
       mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + round16(r) * 128);
       load_a_wide(ti, sa, &mAct, bar, ks * kBK);
       tma_load_3d(sb, &mA2, bar, ks * kBK, 0, ti.g);
     }
+  }
+  // MX, base tiles: B rows are W2 rows h = n0 + rho
+  __device__ bool decodes(const TileInfo& ti, int) const { return MX && !ti.sub; }
+  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
+    const int64_t row = (int64_t)(ti.g % pl.E) * H + ti.n0;
+    const int64_t po = row * (I / 2) + ks * (kBK / 2), so = row * (I / 32) + ks * (kBK / 32);
+    const int64_t po2 = po + 128 * (int64_t)(I / 2), so2 = so + 128 * (int64_t)(I / 32);
+    const int left = H - ti.n0;
+    return MxSrc{{W2q + po, W2q + po2}, {S2q + so, S2q + so2}, I / 2, I / 32,
+                 {left < 128 ? left : 128, left - 128 < 0 ? 0 : (left - 128 < 128 ? left - 128 : 128)}, false};
   }
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     return MmaStep{ti.sub ? round16(r) : 256, 0, 0, ks == 0};
@@ -569,6 +598,7 @@ struct ProbW2 {
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
+using ProbW2 = ProbW2T<false>;
 
 // =====================================================================================
 // Forward F6 (first half) -- shared B2 expand, once per token:
@@ -763,13 +793,19 @@ struct ProbDB2 {
 // 256-row tiles those loads no longer overlap the main loop (same-box 5.55 -> 6.77 ms
 // at 65,536 tokens, E256).
 constexpr bool kW2DgradWide = false;
-struct ProbW2Dgrad {
+// MX: W2 is MXFP4, decoded into the stage (MN-major boxes) by the epilogue warps; on
+// 256-row tiles (the decoding warps are the epilogue warps, idle during the main loop
+// only there, and each decoded weight tile then serves 256 rows instead of 128).
+template <bool MX>
+struct ProbW2DgradT {
   static constexpr bool kAmn = false, kBmn = true;
-  static constexpr bool kWide = kW2DgradWide;
+  static constexpr bool kWide = MX || kW2DgradWide;
+  static constexpr bool kDecode = MX;
+  const uint8_t *W2q, *S2q;  // MX: packed [E,H,I/2], scales [E,H,I/32]
   // 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
   // loads in flight leave the operand copies more of the memory system (same box:
-  // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256)
-  static constexpr int kEpiWarps = 4;
+  // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256); 256-row tiles need 8
+  static constexpr int kEpiWarps = kWide ? 8 : 4;
   // router-gradient partial sums per row and column tile (one per epilogue column stripe)
   static constexpr int kPartsPerTile = kWide ? 1 : kEpiWarps / 4;
   CUtensorMap mDp, mD2p, mW2, mA2;  // Dp (H,P) box(64,128); D2p (r,P) box(64,128);
@@ -805,15 +841,24 @@ struct ProbW2Dgrad {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int nb = H / kBK;
-    mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 4 * 8192);
+    mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX && ks < nb ? 0 : 4 * 8192));
     if (ks < nb) {
       load_a_wide(ti, sa, &mDp, bar, ks * kBK);
-      for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
+      if (!MX)
+        for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
     } else {
       const int kb = ks - nb;
       load_a_wide(ti, sa, &mD2p, bar, kb * kBK);
       for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mA2, bar, ti.n0 + c * 64, kb * kBK, ti.g);
     }
+  }
+  // MX, base K steps: box b holds W2[e][h][i] for i = n0 + 64 b.., h = 64 ks + (rho % 64)
+  __device__ bool decodes(const TileInfo&, int ks) const { return MX && ks < H / kBK; }
+  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
+    const int64_t row = (int64_t)(ti.g % pl.E) * H + ks * kBK;
+    const int64_t po = row * (I / 2) + ti.n0 / 2, so = row * (I / 32) + ti.n0 / 32;
+    const int boxes = (I - ti.n0) / 64;
+    return MxSrc{{W2q + po, W2q + po}, {S2q + so, S2q + so}, I / 2, I / 32, {boxes < 4 ? boxes : 4, 0}, true};
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
@@ -852,6 +897,7 @@ struct ProbW2Dgrad {
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
+using ProbW2Dgrad = ProbW2DgradT<false>;
 
 // =====================================================================================
 // Backward -- expert-local A2 gradient, K-grouped over each group's rows:
@@ -917,10 +963,15 @@ struct ProbDA2 {
 // A: dG/dU K-major; B: W1/W3/B1/B3 MN-major.  In the extra tile dY1 accumulates
 // in TMEM columns [0,r) and dY3 in [128,128+r).
 // =====================================================================================
-struct ProbW13Dgrad {
+// MX: W1/W3 are MXFP4, decoded into the stage (MN-major boxes) by the epilogue warps.
+template <bool MX>
+struct ProbW13DgradT {
   static constexpr bool kAmn = false, kBmn = true;
   static constexpr int kEpiWarps = 8;
   static constexpr bool kWide = true;
+  static constexpr bool kDecode = MX;
+  static constexpr bool kNoinlineEpilogue = MX;  // see epilogue_call
+  const uint8_t *W1q, *W3q, *S1q, *S3q;  // MX: packed [E,I,H/2], scales [E,I,H/32]
   CUtensorMap mdXp;                          // output (H,P), 32 x 32 store boxes
   CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1);
                                              // B1/B3 (r,I,G) box(64,64,1)
@@ -953,11 +1004,12 @@ struct ProbW13Dgrad {
     const bool second = ks >= nb;
     const int kk = (second ? ks - nb : ks) * kBK;
     if (!ti.sub) {
-      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + 4 * 8192);
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 0 : 4 * 8192));
       load_a_wide(ti, sa, second ? &mdU : &mdG, bar, kk);
       const CUtensorMap* mw = second ? &mW3 : &mW1;
       const int e = ti.g % pl.E;
-      for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, mw, bar, ti.n0 + c * 64, kk, e);
+      if (!MX)
+        for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, mw, bar, ti.n0 + c * 64, kk, e);
     } else {
       const int nbox = (round16(r) + 63) / 64;
       mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + nbox * 8192);
@@ -965,6 +1017,19 @@ struct ProbW13Dgrad {
       const CUtensorMap* mb = second ? &mB3 : &mB1;
       for (int c = 0; c < nbox; ++c) tma_load_3d(sb + c * 8192, mb, bar, c * 64, kk, ti.g);
     }
+  }
+  // MX, base tiles: box b holds W1[e][i][h] (W3 in the second half of K) for
+  // h = n0 + 64 b.., i = 64 ks' + (rho % 64)
+  __device__ bool decodes(const TileInfo& ti, int) const { return MX && !ti.sub; }
+  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
+    const int nb = I / kBK;
+    const bool second = ks >= nb;
+    const int64_t row = (int64_t)(ti.g % pl.E) * I + (second ? ks - nb : ks) * kBK;
+    const int64_t po = row * (H / 2) + ti.n0 / 2, so = row * (H / 32) + ti.n0 / 32;
+    const uint8_t* pq = (second ? W3q : W1q) + po;
+    const uint8_t* sq = (second ? S3q : S1q) + so;
+    const int boxes = (H - ti.n0) / 64;
+    return MxSrc{{pq, pq}, {sq, sq}, H / 2, H / 32, {boxes < 4 ? boxes : 4, 0}, true};
   }
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     const int nb = I / kBK;
@@ -999,6 +1064,7 @@ struct ProbW13Dgrad {
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
+using ProbW13Dgrad = ProbW13DgradT<false>;
 
 // =====================================================================================
 // Backward -- expert-local B1/B3 gradients, K-grouped over each group's rows:

@@ -279,14 +279,6 @@ __global__ void combine_rows_kernel(PlanView pl, const uint16_t* __restrict__ ba
 // {0, 0.5, 1, 1.5, 2, 3, 4, 6} (bit 3 = sign); the scale byte b means 2^(b-127)
 // (b = 0 is the fp32 subnormal 2^-127, b = 255 is NaN).  Every product is a bf16
 // value, so the conversion below rounds nothing.
-// Two E2M1 codes (one byte, the lower index in the low nibble) to two f16 values
-// (low half = low nibble) with the hardware conversion; every E2M1 value is exact in
-// f16.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t d;
-  asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(d) : "h"((uint16_t)byte));
-  return d;
-}
 constexpr bool kDequantCvt = true;  // false: decode the codes with a magnitude table
 
 __global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
@@ -312,7 +304,7 @@ __global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ packed, const u
     for (int u = 0; u < kBatch; ++u) {
       const int64_t i = i0 + u * stride;
       if (i >= n8) break;
-      const float sc = __uint_as_float(b[u] == 0 ? 0x00400000u : b[u] == 255 ? 0x7FC00000u : b[u] << 23);
+      const float sc = ue8m0_to_float(b[u]);
       float v[8];
       if (kDequantCvt) {
 #pragma unroll

@@ -60,6 +60,9 @@ def shape(name: str, T: Optional[int] = None) -> Shape:
         # production widths with 16 experts and 4,096 tokens: the same ~1,536 rows
         # per expert as "prod" in a few GB of device memory (profiler captures)
         return Shape(T=T or 4096, H=4096, I=2048, E=16, k=6, r=128, router="normal")
+    if name == "prod_e16_mxfp4":
+        # "prod_e16" with an MXFP4 base (profiler captures of the MXFP4-decoding GEMMs)
+        return Shape(T=T or 4096, H=4096, I=2048, E=16, k=6, r=128, router="normal", base_fmt="mxfp4")
     if name == "prod_mxfp4":
         return Shape(T=T or 65536, H=4096, I=2048, E=256, k=6, r=128, router="normal",
                      base_fmt="mxfp4")

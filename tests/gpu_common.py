@@ -39,16 +39,18 @@ def assert_close(name: str, got: torch.Tensor, ref: torch.Tensor) -> None:
     assert rl <= REL_L2_MAX and cs >= COSINE_MIN, f"{name}: relL2={rl:.3e} cosine={cs:.7f}"
 
 
-def dims_of(shp: Shape, scale: Optional[float] = None) -> m.Dims:
+def dims_of(shp: Shape, scale: Optional[float] = None, mx_once: bool = False) -> m.Dims:
+    """mx_once: an MXFP4 base decoded once per pass (base_fmt 2) instead of inside the GEMMs (1)."""
+    mx = 2 if mx_once else 1
     return m.make_dims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, shp.scale if scale is None else scale,
-                       base_fmt=1 if shp.base_fmt == "mxfp4" else 0, act=1 if shp.act == "geglu" else 0,
+                       base_fmt=mx if shp.base_fmt == "mxfp4" else 0, act=1 if shp.act == "geglu" else 0,
                        act_clamp=shp.clamp)
 
 
 def run_gpu(inp: Dict[str, torch.Tensor], shp: Shape, scale: Optional[float] = None, poison: bool = False,
-            backward: bool = True, ws: Optional[m.Workspaces] = None) -> Dict[str, torch.Tensor]:
+            backward: bool = True, ws: Optional[m.Workspaces] = None, mx_once: bool = False) -> Dict[str, torch.Tensor]:
     """Plan + forward (+ backward) on cuda:0 through the C ABI; results on the device."""
-    d = dims_of(shp, scale)
+    d = dims_of(shp, scale, mx_once)
     if ws is None:
         ws = m.Workspaces.allocate(d)
     if poison:  # 0xFF bytes are bf16/fp32 NaNs: padding or stale rows must never leak

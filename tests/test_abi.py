@@ -74,7 +74,7 @@ def test_forward_rejections(L):
     assert _call_forward(L, _dims(H=500)) == -2
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 2, 0)) == -5   # unknown activation
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 0, -1.0)) == -2  # negative clamp
-    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 2)) == -5   # unknown base format
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 3)) == -5   # unknown base format
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 1)) == -1   # MXFP4 without scales
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 64, 1.0, 0, 0)) == -2    # block_m != 128
     assert _call_forward(L, d, plan=None) == -1

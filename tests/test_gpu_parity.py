@@ -573,12 +573,14 @@ def test_mxfp4_tiny_forward_backward():
     _full_check(inp, shp, out)
 
 
-def test_mxfp4_equals_decoded_bf16_base_bitwise():
+@pytest.mark.parametrize("mx_once", [False, True])
+def test_mxfp4_equals_decoded_bf16_base_bitwise(mx_once):
     """An MXFP4 base gives bit for bit what the same layer gives with the decoded
-    values as a bf16 base (the decode is exact)."""
+    values as a bf16 base (the decode is exact), decoded inside the GEMMs or once per
+    pass."""
     shp = Shape(T=256, H=512, I=256, E=16, k=2, r=16, base_fmt="mxfp4")
     inp = make_inputs(shp, seed=32)
-    q = run_gpu(inp, shp)
+    q = run_gpu(inp, shp, mx_once=mx_once)
     deq = {n: v for n, v in inp.items() if n not in ("S1", "S3", "S2")}
     for n in ("W1", "W3", "W2"):
         deq[n] = _decode_mxfp4_golden(inp[n], inp["S" + n[1]])
@@ -587,14 +589,56 @@ def test_mxfp4_equals_decoded_bf16_base_bitwise():
         assert torch.equal(q[n], b[n]), n
 
 
-def test_mxfp4_production_width_sampled():
+@pytest.mark.parametrize("H,I", [(576, 320), (192, 64)])
+def test_mxfp4_in_gemm_decode_off_tile_boundaries_bitwise(H, I):
+    """The in-GEMM decode on partial column tiles and K rows: H, I multiples of 64 but
+    not of the tile widths; equal bit for bit to the decoded bf16 base."""
+    shp = Shape(T=200, H=H, I=I, E=8, k=2, r=24, mask_frac=0.1, base_fmt="mxfp4")
+    inp = make_inputs(shp, seed=35 + H)
+    q = run_gpu(inp, shp, poison=True)
+    deq = {n: v for n, v in inp.items() if n not in ("S1", "S3", "S2")}
+    for n in ("W1", "W3", "W2"):
+        deq[n] = _decode_mxfp4_golden(inp[n], inp["S" + n[1]])
+    b = run_gpu(deq, Shape(T=200, H=H, I=I, E=8, k=2, r=24, mask_frac=0.1), poison=True)
+    for n in ("y", "dx", "dw") + ADAPTER_GRADS:
+        assert torch.equal(q[n], b[n]), n
+
+
+def test_mxfp4_in_gemm_decode_extreme_scales_bitwise():
+    """The in-GEMM decode takes a permute-and-multiply route for scale bytes 2..252 and
+    the exact fp32 route for the rest (subnormal and overflowing products): with scale
+    bytes 0, 1, 253 and 254 mixed into every weight tensor, the layer still gives, bit
+    for bit, what it gives with the decoded values (OCP table) as a bf16 base."""
+    shp = Shape(T=256, H=512, I=256, E=16, k=2, r=16, base_fmt="mxfp4")
+    inp = make_inputs(shp, seed=34)
+    g = torch.Generator().manual_seed(34)
+    for n in ("S1", "S3", "S2"):
+        sc = inp[n].clone()
+        pick = torch.rand(sc.shape, generator=g) < 0.05
+        sc[pick] = torch.tensor([0, 1, 253, 254], dtype=torch.uint8)[torch.randint(0, 4, (int(pick.sum()),),
+                                                                                   generator=g)]
+        inp[n] = sc
+    q = run_gpu(inp, shp)
+    deq = {n: v for n, v in inp.items() if n not in ("S1", "S3", "S2")}
+    for n in ("W1", "W3", "W2"):
+        deq[n] = _decode_mxfp4_golden(inp[n], inp["S" + n[1]])
+    b = run_gpu(deq, Shape(T=256, H=512, I=256, E=16, k=2, r=16))
+    for n in ("y", "dx"):
+        assert torch.equal(q[n].view(torch.int16), b[n].view(torch.int16)), n
+    for n in ("dw",) + ADAPTER_GRADS:
+        assert torch.equal(q[n].view(torch.int32), b[n].view(torch.int32)), n
+
+
+@pytest.mark.parametrize("mx_once", [False, True])
+def test_mxfp4_production_width_sampled(mx_once):
     """MXFP4 base at production widths (H=4096, I=2048, E=256, top-6, rank 128),
-    2,048 tokens, sampled sparse-dy parity against the oracle."""
+    2,048 tokens, sampled sparse-dy parity against the oracle; decoded inside the
+    GEMMs or once per pass."""
     shp = shape("prod_mxfp4", 2048)
     inp = make_inputs(shp, seed=33, device="cuda")
     sample = [0, 5, 333, 1024, 2047]
     inp = _sparse_dy(inp, shp, sample)
-    out = run_gpu(inp, shp)
+    out = run_gpu(inp, shp, mx_once=mx_once)
     assert out["err"] == 0
     _sampled_check(inp, shp, out, sample)
 

@@ -116,9 +116,10 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     p.topk_w = topk_w;
     p.G = Gs;
     p.U = Us;
-    p.Act = Act;
     p.dG = dG;
     p.dU = dU;
+    MAP(tmap_2d_store32(&p.mdG, dG, I, P));
+    MAP(tmap_2d_store32(&p.mdU, dU, I, P));
     p.part = part;
     p.H = d->H;
     p.I = d->I;

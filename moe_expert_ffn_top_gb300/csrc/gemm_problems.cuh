@@ -162,29 +162,35 @@ __device__ __forceinline__ void act_fwd_chunk(int act, float c, float (&g)[32], 
 //   dG = dAct * cl(U) * act'(cl(G)) * [G in clamp],  dU = dAct * act(cl(G)) * [U in clamp]
 // (dead rows give zeros).  G/U are the saved values, whose clamp test matches the
 // forward's fp32 decision.
+// Also returns sum_i q_i * act(cl(g_i)) * cl(u_i): the chunk's share of the router
+// dot <Q, Act>, with the activation recomputed from the saved G and U (so the saved
+// activation is not read again; it differs from the saved bf16 value by the
+// rounding of G and U, far inside the tolerance).
 template <int ACT, bool CL>
-__device__ __forceinline__ void act_bwd_chunk(const float (&q)[32], const float (&g)[32], const float (&u)[32],
-                                              float w, bool live, float c, float (&og)[32], float (&ou)[32]) {
+__device__ __forceinline__ float act_bwd_chunk(const float (&q)[32], const float (&g)[32], const float (&u)[32],
+                                               float w, bool live, float c, float (&og)[32], float (&ou)[32]) {
+  float dot = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const float da = w * q[i];
     float f, df;
     act_pair<ACT>(CL ? clamp_act(g[i], c) : g[i], f, df);
     const float uc = CL ? clamp_act(u[i], c) : u[i];
+    dot += q[i] * (f * uc);
     og[i] = live ? da * uc * df * (CL ? clamp_pass(g[i], c) : 1.0f) : 0.0f;
     ou[i] = live ? da * f * (CL ? clamp_pass(u[i], c) : 1.0f) : 0.0f;
   }
+  return dot;
 }
-__device__ __forceinline__ void act_bwd_chunk(int act, float c, const float (&q)[32], const float (&g)[32],
-                                              const float (&u)[32], float w, bool live, float (&og)[32],
-                                              float (&ou)[32]) {
+__device__ __forceinline__ float act_bwd_chunk(int act, float c, const float (&q)[32], const float (&g)[32],
+                                               const float (&u)[32], float w, bool live, float (&og)[32],
+                                               float (&ou)[32]) {
   if (act == 1) {
-    if (c > 0.0f) act_bwd_chunk<1, true>(q, g, u, w, live, c, og, ou);
-    else act_bwd_chunk<1, false>(q, g, u, w, live, c, og, ou);
-  } else {
-    if (c > 0.0f) act_bwd_chunk<0, true>(q, g, u, w, live, c, og, ou);
-    else act_bwd_chunk<0, false>(q, g, u, w, live, c, og, ou);
+    if (c > 0.0f) return act_bwd_chunk<1, true>(q, g, u, w, live, c, og, ou);
+    return act_bwd_chunk<1, false>(q, g, u, w, live, c, og, ou);
   }
+  if (c > 0.0f) return act_bwd_chunk<0, true>(q, g, u, w, live, c, og, ou);
+  return act_bwd_chunk<0, false>(q, g, u, w, live, c, og, ou);
 }
 // Value saved (as bf16) for a gate/up pre-activation v so that the backward sees
 // the forward's fp32 clamp decision: a clamped element (|v| > c) is saved as the
@@ -810,10 +816,11 @@ struct ProbW2DgradT {
   static constexpr int kPartsPerTile = kWide ? 1 : kEpiWarps / 4;
   CUtensorMap mDp, mD2p, mW2, mA2;  // Dp (H,P) box(64,128); D2p (r,P) box(64,128);
                                     // W2 (I,H,E) box(64,64,1); A2 (I,r,G) box(64,64,1)
+  CUtensorMap mdG, mdU;             // outputs (I,P), 32 x 32 store boxes (4 epilogue warps)
   PlanView pl;
   int* err;
   const float* topk_w;
-  const uint16_t *G, *U, *Act;
+  const uint16_t *G, *U;
   uint16_t *dG, *dU;
   float* part;
   int H, I, r;
@@ -868,30 +875,31 @@ struct ProbW2DgradT {
     const float w = live ? topk_w[rt] : 0.0f;
     const int y0 = (int)(p - (threadIdx.x & 31));  // warp's first row
     const int64_t base0 = (int64_t)y0 * I + ti.n0;
+    // With 4 epilogue warps the staging slots of warps 4..7 are free: each warp keeps
+    // its load-transposition buffer and gets a TMA-store ring in the slot 4 further on.
+    constexpr bool kTmaOut = kEpiTmaStore && kEpiWarps == 4;
+    TmaStoreRing out(stg + (kTmaOut ? 4 * kStgWordsPerWarp : 0));
     float dot = 0.0f;
     for (int c = c0; c < 256 && ti.n0 + c < I; c += cs) {
-      // the chunk's saved G, U and activation: coalesced loads, all in flight,
-      // then redistributed so each lane holds its own row
-      uint4 lg[4], lu[4], la[4];
+      // the chunk's saved G and U: coalesced loads, all in flight, then redistributed
+      // so each lane holds its own row
+      uint4 lg[4], lu[4];
       warp_load_rows_issue(G + base0 + c, I, lg);
       warp_load_rows_issue(U + base0 + c, I, lu);
-      warp_load_rows_issue(Act + base0 + c, I, la);
       float q[32];
       tmem_ld32(taddr + c, q);
       float g[32], u[32];
-      {
-        float a[32];
-        warp_rows_to_lane(la, stg, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dot += q[i] * a[i];
-      }
       warp_rows_to_lane(lg, stg, g);
       warp_rows_to_lane(lu, stg, u);
       float og[32], ou[32];
-      act_bwd_chunk(act, clamp, q, g, u, w, live, og, ou);
-      // staged warp stores: this epilogue's loads already use the staging buffer
-      warp_store_rows_bf16(dG + base0 + c, I, 32, og, 1.0f, stg);
-      warp_store_rows_bf16(dU + base0 + c, I, 32, ou, 1.0f, stg);
+      dot += act_bwd_chunk(act, clamp, q, g, u, w, live, og, ou);
+      if (kTmaOut) {
+        out.store_bf16(&mdG, ti.n0 + c, y0, og);
+        out.store_bf16(&mdU, ti.n0 + c, y0, ou);
+      } else {  // staged warp stores: the loads use the staging buffer
+        warp_store_rows_bf16(dG + base0 + c, I, 32, og, 1.0f, stg);
+        warp_store_rows_bf16(dU + base0 + c, I, 32, ou, 1.0f, stg);
+      }
     }
     part[(p * ntn() + ti.sub) * kPartsPerTile + c0 / 32] = live ? dot : 0.0f;
   }

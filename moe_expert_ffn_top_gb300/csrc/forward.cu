@@ -90,8 +90,10 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
       MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 128));
       MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 128));
     }
-    p.W1q = (const uint8_t*)w->W1;
-    p.W3q = (const uint8_t*)w->W3;
+    if (mx) {
+      MAP(tmap_3d_u8(&p.mW1q, w->W1, H / 2, I, E, 32, 128));
+      MAP(tmap_3d_u8(&p.mW3q, w->W3, H / 2, I, E, 32, 128));
+    }
     p.S1q = w->S1;
     p.S3q = w->S3;
     MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 128));
@@ -117,7 +119,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   auto w2 = [&](auto p) -> int {
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
     if (!mx) MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 256));
-    p.W2q = (const uint8_t*)w->W2;
+    if (mx) MAP(tmap_3d_u8(&p.mW2q, w->W2, I / 2, H, E, 32, 256));
     p.S2q = w->S2;
     MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, (uint32_t)((r + 15) / 16 * 16)));
     MAP(tmap_2d_store32(&p.mO, O, H, P));

@@ -27,18 +27,22 @@
 //   static constexpr bool kWide;           256-row tiles (see EngineShape)
 //   static constexpr bool kDecode;         B operand decoded from MXFP4 (wide problems only);
 //   (kDecode only:)
+//   static constexpr bool kMxMN;           layout of the packed rows (below)
 //   bool  decodes(const TileInfo&, int ks) const;   false: the producer loads B with TMA
-//   MxSrc mx_src(const TileInfo&, int ks) const;    where the stage's B rows are (below)
+//   MxScales mx_scales(const TileInfo&, int ks) const;   where the stage's scale bytes are
+//   and load() copies the stage's packed E2M1 rows with TMA into the last 12 KB of the
+//   B buffer (kMxRaw), counted on the stage's full barrier
 // An epilogue warp handles the 32-column chunks c = c0, c0 + cs, ... of its row.
 //
 // With kDecode the epilogue warps are also the decoders.  On 256-row tiles they are
-// idle while the main loop runs (one accumulator, no overlap), so for every K step of
-// a tile they wait until the stage is free, write its B tile (bf16, in the swizzled
-// layout TMA would write) and arrive on the stage's full barrier -- which therefore
-// counts the producer's TMA bytes plus one arrival per epilogue warp -- and after the
-// tile's last K step they run its epilogue.  Their global loads run one K step ahead,
-// so the next step's packed bytes are in flight while a step is decoded and while an
-// epilogue runs.
+// idle while the main loop runs (one accumulator, no overlap): for every K step of a
+// tile they wait for the stage's full barrier (its A tile and its packed weight rows
+// have landed), decode the packed rows into the stage's bf16 B tile (in the swizzled
+// layout TMA would write) and arrive on the stage's decoded barrier, which the MMA
+// waits on instead; after a tile's last K step they run its epilogue.  The packed
+// rows travel by TMA with the rest of the stage, so the ring's depth hides their
+// latency; the scale bytes (rows too narrow for TMA in general) are loaded by the
+// decoding threads one K step ahead.
 //
 // Operand tiles in shared memory use the 128-byte swizzle written by TMA:
 //   A K-major : 128 rows x 128 B                         (one 16 KB box)
@@ -105,70 +109,99 @@ struct MmaStep {
 // The B tile of a stage is 256 rows of 64 bf16 in the 128-byte swizzle -- row rho at
 // rho * 128, its 16-byte chunk c (elements 8c..8c+7) at chunk position c ^ (rho & 7)
 // -- which is the layout TMA writes for a K-major tile of 256 rows and for four
-// MN-major boxes of 64 x 64 (rho = 64 * box + K row) alike.  Decoder thread dt (of
-// NT) takes the 32-element halves dt + NT j of the tile (row = half / 2), so
-// neighbouring lanes read the two halves of a row (32 contiguous bytes).
-//
-// Every B row of a stage is 64 consecutive elements of one weight row: 32 packed bytes
-// (64 E2M1 codes) and the UE8M0 bytes of its two 32-element groups.  MxSrc locates
-// them.  K-major tiles (mn = false): rows 0..127 are rows 0..lim[0]-1 of a block
-// starting at p[0] / s[0], rows 128..255 rows 0..lim[1]-1 of a block at p[1] / s[1],
-// consecutive rows prs / srs bytes apart; rows past lim are zeros.  MN-major tiles
-// (mn = true): box b = rho / 64 (b < lim[0], else zeros) holds, for K row kk = rho % 64,
-// the 64 elements at p[0] + kk * prs + 32 b (scales s[0] + kk * srs + 2 b).
-struct MxSrc {
-  const uint8_t* p[2];
-  const uint8_t* s[2];
-  int64_t prs, srs;
-  int lim[2];
-  bool mn;
-};
-template <int NT>
-struct MxStage {
-  static constexpr int kItems = 512 / NT;
-  uint4 pk[kItems];
-  uint32_t sc[kItems];
-};
-// Read-only global loads issued exactly where written: as volatile asm they keep their
-// place before the stage wait that follows them, so a K step's packed bytes are in
-// flight while the previous step decodes (plain loads may be sunk to their first use).
-__device__ __forceinline__ uint4 ldg_issue_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// MN-major boxes of 64 x 64 (rho = 64 * box + K row) alike.  The producer copies the
+// stage's packed rows (64 E2M1 codes = 32 bytes per B row, 8 KB) into the last 12 KB
+// of the same buffer (kMxRaw):
+//   K-major (kMxMN false): B row rho's 32 bytes at rho * 32;
+//   MN-major (kMxMN true):  one box of 64 K rows x 128 bytes, B row rho = 64 b + kk's
+//                           32 bytes at kk * 128 + 32 b.
+// Each decoding thread (dt of NT = 256) takes two 32-element halves (items): it reads
+// their packed bytes, all decoding warps meet at a named barrier (decoded rows 160..255
+// overwrite the packed bytes), and it writes 2 x 64 bytes of bf16.  The item mapping
+// puts the 32 lanes of a warp on distinct banks for the reads and the writes.
+constexpr int kMxRaw = 20480;  // offset of the packed rows in the 32 KB B buffer
+template <bool MN>
+__device__ __forceinline__ void mx_item(int dt, int j, int& rho, int& half) {
+  half = dt & 1;
+  rho = MN ? ((dt >> 1) & 3) * 64 + (dt >> 3) + 32 * j : (dt >> 1) + 128 * j;
 }
+// Where a stage's UE8M0 bytes are: B row rho's two bytes (one per 32-element half).
+//   K-major: rows 0..127 at s[0] + rho * rs, rows 128..255 at s[1] + (rho - 128) * rs,
+//            valid below lim[0] / lim[1] rows;
+//   MN-major: row 64 b + kk at s[0] + kk * rs + 2 b, valid for b < lim[0].
+// Rows past the tensor's edge (zeros from the zero-filled TMA copy) take scale 1.
+struct MxScales {
+  const uint8_t* s[2];
+  int64_t rs;
+  int lim[2];
+};
+// Read-only byte loads issued exactly where written (volatile asm keeps them ahead of
+// the stage wait that follows, so they overlap the current step's decode).
 __device__ __forceinline__ uint32_t ldg_issue_u8(const void* p) {
   uint32_t v;
   asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
-template <int NT>
-__device__ __forceinline__ void mx_load(const MxSrc& src, int dt, MxStage<NT>& st) {
-  const int half = dt & 1;
+template <bool MN>
+__device__ __forceinline__ void mx_load_scales(const MxScales& sc, int dt, uint32_t (&out)[2]) {
 #pragma unroll
-  for (int j = 0; j < MxStage<NT>::kItems; ++j) {
-    const int rho = (dt >> 1) + (NT / 2) * j;
-    const int h = src.mn ? 0 : rho >> 7;
-    const int r = src.mn ? (rho & 63) : (rho & 127);
-    const int b = src.mn ? (rho >> 6) : 0;
-    const bool ok = src.mn ? b < src.lim[0] : r < (h ? src.lim[1] : src.lim[0]);  // selects, not indexing:
-    const uint8_t* pp = (h ? src.p[1] : src.p[0]) + r * src.prs + 32 * b;           // the arrays stay in
-    const uint8_t* sp = (h ? src.s[1] : src.s[0]) + r * src.srs + 2 * b;            // registers
-    st.pk[j] = ok ? ldg_issue_v4(pp + 16 * half) : make_uint4(0, 0, 0, 0);
-    st.sc[j] = ok ? ldg_issue_u8(sp + half) : 127u;
+  for (int j = 0; j < 2; ++j) {
+    int rho, half;
+    mx_item<MN>(dt, j, rho, half);
+    const int h = MN ? 0 : rho >> 7;
+    const int r = MN ? (rho & 63) : (rho & 127);
+    const int b = MN ? rho >> 6 : 0;
+    const bool ok = MN ? b < sc.lim[0] : r < (h ? sc.lim[1] : sc.lim[0]);
+    const uint8_t* sp = (h ? sc.s[1] : sc.s[0]) + r * sc.rs + 2 * b + half;
+    out[j] = ok ? ldg_issue_u8(sp) : 127u;
   }
 }
-template <int NT>
-__device__ __forceinline__ void mx_store(uint8_t* sb, int dt, const MxStage<NT>& st) {
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+template <int NT, bool MN>
+__device__ __forceinline__ void mx_decode_stage(uint8_t* sb, int dt, const uint32_t (&scale)[2]) {
+  static_assert(NT == 256, "two items per decoding thread");
+  const uint8_t* raw = sb + kMxRaw;
+  uint4 pk[2];
 #pragma unroll
-  for (int j = 0; j < MxStage<NT>::kItems; ++j) {
-    const int item = dt + NT * j, rho = item >> 1, half = item & 1;
-    const uint32_t wd[4] = {st.pk[j].x, st.pk[j].y, st.pk[j].z, st.pk[j].w};
+  for (int j = 0; j < 2; ++j) {
+    int rho, half;
+    mx_item<MN>(dt, j, rho, half);
+    const int off = MN ? (rho & 63) * 128 + (rho >> 6) * 32 + half * 16 : rho * 32 + half * 16;
+    pk[j] = *reinterpret_cast<const uint4*>(raw + off);
+  }
+  named_barrier_sync(1, NT);  // every packed byte read before decoded rows overwrite them
+  // One choice per warp and stage between the permute route (scale bytes 2..252: all
+  // but the extremes) and the exact fp32 route, so that the common case is one
+  // straight-line block whose eight independent word decodes the compiler interleaves.
+  const bool fast = scale[0] - 2u <= 250u && scale[1] - 2u <= 250u;
+  uint4 o[2][4];
+  if (__all_sync(0xffffffffu, fast)) {
+    const uint32_t s2[2] = {(scale[0] << 7) * 0x10001u, (scale[1] << 7) * 0x10001u};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      o[j][0] = mx_decode8_fast(pk[j].x, s2[j]);
+      o[j][1] = mx_decode8_fast(pk[j].y, s2[j]);
+      o[j][2] = mx_decode8_fast(pk[j].z, s2[j]);
+      o[j][3] = mx_decode8_fast(pk[j].w, s2[j]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      o[j][0] = mx_decode8_any(pk[j].x, scale[j]);
+      o[j][1] = mx_decode8_any(pk[j].y, scale[j]);
+      o[j][2] = mx_decode8_any(pk[j].z, scale[j]);
+      o[j][3] = mx_decode8_any(pk[j].w, scale[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    int rho, half;
+    mx_item<MN>(dt, j, rho, half);
 #pragma unroll
     for (int w = 0; w < 4; ++w)
-      *reinterpret_cast<uint4*>(sb + rho * 128 + (((half * 4 + w) ^ (rho & 7)) << 4)) = mx_decode8_any(wd[w], st.sc[j]);
+      *reinterpret_cast<uint4*>(sb + rho * 128 + (((half * 4 + w) ^ (rho & 7)) << 4)) = o[j][w];
   }
 }
 
@@ -213,15 +246,17 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
   uint64_t* empty = full + S::kStages;
   uint64_t* tfull = empty + S::kStages;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* dec = tempty + 2;  // kDecode: the stage's B tile has been decoded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dec + S::kStages);
   uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + S::kStages * S::kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = p.err;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(&full[s], 1 + (DecodeOf<P>::value ? P::kEpiWarps : 0));
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&dec[s], P::kEpiWarps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -282,7 +317,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(S::kWide ? 0 : acc * kAccCols);
         for (int ks = 0; ks < ti.nk; ++ks) {
-          if (!mbar_wait(&full[s], ph, err)) {
+          if (!mbar_wait(DecodeOf<P>::value ? &dec[s] : &full[s], ph, err)) {
             ok = false;
             break;
           }
@@ -375,36 +410,27 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
       };
       int s = 0;
       uint32_t ph = 0;
-      MxStage<NT> b0, b1;  // register buffers: the current step's and the next step's loads
-      bool nb = false;     // buffer of the current step
-      auto load_next = [&]() {  // the step (ti, ks) into the other buffer
-        if (nb) mx_load<NT>(p.mx_src(ti, ks), dt, b0);
-        else mx_load<NT>(p.mx_src(ti, ks), dt, b1);
-      };
+      uint32_t sc[2] = {127u, 127u};  // the current step's scale bytes (two items)
       bool have = next();
       bool cdec = have && p.decodes(ti, ks);
-      if (cdec) mx_load<NT>(p.mx_src(ti, ks), dt, b0);
+      if (cdec) mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, sc);
       while (have) {
-        // Within a tile the next step's loads are issued before this step is decoded.
-        // After a tile's last step the iterator moves on only once the epilogue has
-        // run, so neither decode buffers nor a second tile's state are live across it
-        // (the epilogue needs the registers).
+        // The next step's scale bytes are loaded before this step is decoded; after a
+        // tile's last step the iterator moves on only once the epilogue has run (the
+        // epilogue needs the registers).
         const bool last = ks == ti.nk - 1;
+        uint32_t nsc[2] = {127u, 127u};
         bool ndec = false;
         if (!last) {
           next();  // ks + 1 of the same tile
           ndec = p.decodes(ti, ks);
-          if (ndec) load_next();
+          if (ndec) mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, nsc);
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1u, err))) break;
-        if (cdec) {
-          uint8_t* sb = smem + s * S::kStage + S::kAStage;
-          if (nb) mx_store<NT>(sb, dt, b1);
-          else mx_store<NT>(sb, dt, b0);
-        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, err))) break;
+        if (cdec) mx_decode_stage<NT, P::kMxMN>(smem + s * S::kStage + S::kAStage, dt, sc);
         fence_proxy_async_smem();  // generic-proxy stores before the MMA's reads
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (lane == 0) mbar_arrive(&dec[s]);
         if (++s == S::kStages) {
           s = 0;
           ph ^= 1u;
@@ -413,9 +439,10 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           if (!run_epilogue(ti)) break;
           have = next();
           ndec = have && p.decodes(ti, ks);
-          if (ndec) load_next();
+          if (ndec) mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, nsc);
         }
-        nb = !nb;
+        sc[0] = nsc[0];
+        sc[1] = nsc[1];
         cdec = ndec;
       }
     } else {

@@ -426,8 +426,10 @@ struct ProbW13T {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr bool kWide = kW13Wide;
   static constexpr bool kDecode = MX;
+  static constexpr bool kMxMN = false;
   static constexpr int kEpiWarps = kWide ? 8 : 4;
-  const uint8_t *W1q, *W3q, *S1q, *S3q;  // MX: packed [E,I,H/2], scales [E,I,H/32]
+  const uint8_t *S1q, *S3q;  // MX: scales [E,I,H/32]
+  CUtensorMap mW1q, mW3q;    // MX: packed [E,I,H/2] bytes, box (32, 128, 1)
   CUtensorMap mXp, mY13p, mW1, mW3, mB1, mB3;  // Xp (H,P) box(64,128); Y13p (2r,P) box(64,128);
                                                // W1/W3 (H,I,E) box(64,128,1); B1/B3 (r,I,G) box(64,128,1)
   CUtensorMap mG, mU, mAct;                    // outputs (I,P), 32 x 32 store boxes
@@ -464,9 +466,12 @@ struct ProbW13T {
     const int nb = H / kBK;
     const int e = ti.g % pl.E;
     if (ks < nb) {
-      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 0 : 2 * 128 * 128));
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 2 * 128 * 32 : 2 * 128 * 128));
       load_a_wide(ti, sa, &mXp, bar, ks * kBK);
-      if (!MX) {
+      if (MX) {  // packed rows: W1's into rows 0..127, W3's into rows 128..255
+        tma_load_3d(sb + kMxRaw, &mW1q, bar, ks * (kBK / 2), ti.n0, e);
+        tma_load_3d(sb + kMxRaw + 128 * 32, &mW3q, bar, ks * (kBK / 2), ti.n0, e);
+      } else {
         tma_load_3d(sb, &mW1, bar, ks * kBK, ti.n0, e);
         tma_load_3d(sb + 128 * 128, &mW3, bar, ks * kBK, ti.n0, e);
       }
@@ -479,11 +484,10 @@ struct ProbW13T {
   }
   // MX, base K steps: rows 0..127 of the B tile are W1 rows n0.., 128..255 W3 rows
   __device__ bool decodes(const TileInfo&, int ks) const { return MX && ks < H / kBK; }
-  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
-    const int64_t row = (int64_t)(ti.g % pl.E) * I + ti.n0;
-    const int64_t po = row * (H / 2) + ks * (kBK / 2), so = row * (H / 32) + ks * (kBK / 32);
+  __device__ MxScales mx_scales(const TileInfo& ti, int ks) const {
+    const int64_t so = ((int64_t)(ti.g % pl.E) * I + ti.n0) * (H / 32) + ks * (kBK / 32);
     const int lim = I - ti.n0 < 128 ? I - ti.n0 : 128;
-    return MxSrc{{W1q + po, W3q + po}, {S1q + so, S3q + so}, H / 2, H / 32, {lim, lim}, false};
+    return MxScales{{S1q + so, S3q + so}, H / 32, {lim, lim}};
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const {
     const int nb = H / kBK;
@@ -530,8 +534,10 @@ struct ProbW2T {
   static constexpr bool kAmn = false, kBmn = false;
   static constexpr bool kWide = kW2OneSmWide;
   static constexpr bool kDecode = MX;
+  static constexpr bool kMxMN = false;
   static constexpr int kEpiWarps = kWide ? 8 : 4;
-  const uint8_t *W2q, *S2q;  // MX: packed [E,H,I/2], scales [E,H,I/32]
+  const uint8_t* S2q;  // MX: scales [E,H,I/32]
+  CUtensorMap mW2q;    // MX: packed [E,H,I/2] bytes, box (32, 256, 1)
   CUtensorMap mAct, mW2, mA2;  // Act (I,P) box(64,128); W2 (I,H,E) box(64,256,1); A2 (I,r,G) box(64,r16,1)
   CUtensorMap mO;              // output (H,P), 32 x 32 store boxes
   PlanView pl;
@@ -558,9 +564,12 @@ struct ProbW2T {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     if (!ti.sub) {
-      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 0 : 256 * 128));
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 256 * 32 : 256 * 128));
       load_a_wide(ti, sa, &mAct, bar, ks * kBK);
-      if (!MX) tma_load_3d(sb, &mW2, bar, ks * kBK, ti.n0, ti.g % pl.E);
+      if (MX)
+        tma_load_3d(sb + kMxRaw, &mW2q, bar, ks * (kBK / 2), ti.n0, ti.g % pl.E);
+      else
+        tma_load_3d(sb, &mW2, bar, ks * kBK, ti.n0, ti.g % pl.E);
     } else {
       mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + round16(r) * 128);
       load_a_wide(ti, sa, &mAct, bar, ks * kBK);
@@ -569,13 +578,11 @@ struct ProbW2T {
   }
   // MX, base tiles: B rows are W2 rows h = n0 + rho
   __device__ bool decodes(const TileInfo& ti, int) const { return MX && !ti.sub; }
-  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
-    const int64_t row = (int64_t)(ti.g % pl.E) * H + ti.n0;
-    const int64_t po = row * (I / 2) + ks * (kBK / 2), so = row * (I / 32) + ks * (kBK / 32);
-    const int64_t po2 = po + 128 * (int64_t)(I / 2), so2 = so + 128 * (int64_t)(I / 32);
+  __device__ MxScales mx_scales(const TileInfo& ti, int ks) const {
+    const int64_t so = ((int64_t)(ti.g % pl.E) * H + ti.n0) * (I / 32) + ks * (kBK / 32);
     const int left = H - ti.n0;
-    return MxSrc{{W2q + po, W2q + po2}, {S2q + so, S2q + so2}, I / 2, I / 32,
-                 {left < 128 ? left : 128, left - 128 < 0 ? 0 : (left - 128 < 128 ? left - 128 : 128)}, false};
+    return MxScales{{S2q + so, S2q + so + 128 * (int64_t)(I / 32)}, I / 32,
+                    {left < 128 ? left : 128, left - 128 < 0 ? 0 : (left - 128 < 128 ? left - 128 : 128)}};
   }
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     return MmaStep{ti.sub ? round16(r) : 256, 0, 0, ks == 0};
@@ -807,7 +814,9 @@ struct ProbW2DgradT {
   static constexpr bool kAmn = false, kBmn = true;
   static constexpr bool kWide = MX || kW2DgradWide;
   static constexpr bool kDecode = MX;
-  const uint8_t *W2q, *S2q;  // MX: packed [E,H,I/2], scales [E,H,I/32]
+  static constexpr bool kMxMN = true;
+  const uint8_t* S2q;  // MX: scales [E,H,I/32]
+  CUtensorMap mW2q;    // MX: packed [E,H,I/2] bytes, box (128, 64, 1)
   // 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
   // loads in flight leave the operand copies more of the memory system (same box:
   // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256); 256-row tiles need 8
@@ -848,10 +857,12 @@ struct ProbW2DgradT {
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
     const int nb = H / kBK;
-    mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX && ks < nb ? 0 : 4 * 8192));
+    mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX && ks < nb ? 64 * 128 : 4 * 8192));
     if (ks < nb) {
       load_a_wide(ti, sa, &mDp, bar, ks * kBK);
-      if (!MX)
+      if (MX)  // 64 rows of W2 (h) x 256 packed columns (i)
+        tma_load_3d(sb + kMxRaw, &mW2q, bar, ti.n0 / 2, ks * kBK, ti.g % pl.E);
+      else
         for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
     } else {
       const int kb = ks - nb;
@@ -861,11 +872,10 @@ struct ProbW2DgradT {
   }
   // MX, base K steps: box b holds W2[e][h][i] for i = n0 + 64 b.., h = 64 ks + (rho % 64)
   __device__ bool decodes(const TileInfo&, int ks) const { return MX && ks < H / kBK; }
-  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
-    const int64_t row = (int64_t)(ti.g % pl.E) * H + ks * kBK;
-    const int64_t po = row * (I / 2) + ti.n0 / 2, so = row * (I / 32) + ti.n0 / 32;
+  __device__ MxScales mx_scales(const TileInfo& ti, int ks) const {
+    const int64_t so = ((int64_t)(ti.g % pl.E) * H + ks * kBK) * (I / 32) + ti.n0 / 32;
     const int boxes = (I - ti.n0) / 64;
-    return MxSrc{{W2q + po, W2q + po}, {S2q + so, S2q + so}, I / 2, I / 32, {boxes < 4 ? boxes : 4, 0}, true};
+    return MxScales{{S2q + so, S2q + so}, I / 32, {boxes < 4 ? boxes : 4, 0}};
   }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
@@ -978,8 +988,10 @@ struct ProbW13DgradT {
   static constexpr int kEpiWarps = 8;
   static constexpr bool kWide = true;
   static constexpr bool kDecode = MX;
+  static constexpr bool kMxMN = true;
   static constexpr bool kNoinlineEpilogue = MX;  // see epilogue_call
-  const uint8_t *W1q, *W3q, *S1q, *S3q;  // MX: packed [E,I,H/2], scales [E,I,H/32]
+  const uint8_t *S1q, *S3q;  // MX: scales [E,I,H/32]
+  CUtensorMap mW1q, mW3q;    // MX: packed [E,I,H/2] bytes, box (128, 64, 1)
   CUtensorMap mdXp;                          // output (H,P), 32 x 32 store boxes
   CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1);
                                              // B1/B3 (r,I,G) box(64,64,1)
@@ -1012,12 +1024,13 @@ struct ProbW13DgradT {
     const bool second = ks >= nb;
     const int kk = (second ? ks - nb : ks) * kBK;
     if (!ti.sub) {
-      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 0 : 4 * 8192));
+      mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + (MX ? 64 * 128 : 4 * 8192));
       load_a_wide(ti, sa, second ? &mdU : &mdG, bar, kk);
-      const CUtensorMap* mw = second ? &mW3 : &mW1;
       const int e = ti.g % pl.E;
-      if (!MX)
-        for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, mw, bar, ti.n0 + c * 64, kk, e);
+      if (MX)  // 64 rows of W1 / W3 (i) x 256 packed columns (h)
+        tma_load_3d(sb + kMxRaw, second ? &mW3q : &mW1q, bar, ti.n0 / 2, kk, e);
+      else
+        for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, second ? &mW3 : &mW1, bar, ti.n0 + c * 64, kk, e);
     } else {
       const int nbox = (round16(r) + 63) / 64;
       mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + nbox * 8192);
@@ -1029,15 +1042,13 @@ struct ProbW13DgradT {
   // MX, base tiles: box b holds W1[e][i][h] (W3 in the second half of K) for
   // h = n0 + 64 b.., i = 64 ks' + (rho % 64)
   __device__ bool decodes(const TileInfo& ti, int) const { return MX && !ti.sub; }
-  __device__ MxSrc mx_src(const TileInfo& ti, int ks) const {
+  __device__ MxScales mx_scales(const TileInfo& ti, int ks) const {
     const int nb = I / kBK;
     const bool second = ks >= nb;
     const int64_t row = (int64_t)(ti.g % pl.E) * I + (second ? ks - nb : ks) * kBK;
-    const int64_t po = row * (H / 2) + ti.n0 / 2, so = row * (H / 32) + ti.n0 / 32;
-    const uint8_t* pq = (second ? W3q : W1q) + po;
-    const uint8_t* sq = (second ? S3q : S1q) + so;
+    const uint8_t* sq = (second ? S3q : S1q) + row * (H / 32) + ti.n0 / 32;
     const int boxes = (H - ti.n0) / 64;
-    return MxSrc{{pq, pq}, {sq, sq}, H / 2, H / 32, {boxes < 4 ? boxes : 4, 0}, true};
+    return MxScales{{sq, sq}, H / 32, {boxes < 4 ? boxes : 4, 0}};
   }
   __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
     const int nb = I / kBK;

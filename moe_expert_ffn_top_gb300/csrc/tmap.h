@@ -16,5 +16,8 @@ int tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
 int tmap_2d_store32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer);
 // 3D tensor [d2][d1][d0]; box of b0 x b1 x 1.
 int tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1);
+// 3D byte tensor [d2][d1][d0] (MXFP4 packed codes or scales), no swizzle: a box lands
+// in shared memory as b1 rows of b0 bytes.  d0 a multiple of 16, b0 of 16.
+int tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1);
 
 }  // namespace moelora

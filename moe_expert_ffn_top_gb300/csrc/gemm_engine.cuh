@@ -226,8 +226,8 @@ constexpr int gemm_threads() {
 // epilogue warps also decode: the decode loop and the epilogue then get their own
 // register allocations; the call saves the loop's live registers once per tile.
 // Measured per problem (MXFP4 base, 65,536 tokens, E256): the W13 dgrad 45.8 -> 29.5
-// ms with the call; W13 (37.0 -> 56.5 ms) and the W2 dgrad (11.3 -> 19.7) keep the
-// epilogue inline.
+// ms with the call (global-load decoders); W13 (37.0 -> 56.5 ms then, 20.3 -> 22.0 ms
+// with the TMA-fed decoders) and the W2 dgrad (11.3 -> 19.7) keep the epilogue inline.
 template <class P>
 __device__ __noinline__ void epilogue_call(const P& p, const TileInfo& ti, int row, uint32_t taddr, int c0, int cs,
                                            uint32_t* stg) {

@@ -140,6 +140,34 @@ def test_finite_differences(act, clamp):
             assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (n, fd, an)
 
 
+@pytest.mark.parametrize("A,mask,act,clamp", [(1, 0.0, "swiglu", 0.0), (2, 0.25, "geglu", 0.3)])
+def test_adjoint_in_the_linear_factors(A, mask, act, clamp):
+    """The output is linear in the routing weights w, in A2 and in B2 (each enters once,
+    after the activation), so for any direction v the change y(theta + v) - y(theta)
+    is exactly the Jacobian applied to v, and <dy, y(theta + v) - y(theta)> must equal
+    <grad theta, v> -- an adjoint test with no finite-difference step (FP64 oracle,
+    rounding off: agreement to ~1e-12 relative).  A sign, index or transposition
+    mistake in dw, dA2 or dB2 breaks it."""
+    shp, inp = _tiny(T=6, H=16, I=8, E=3, k=2, r=3, A=A, mask=mask, act=act, clamp=clamp, seed=7)
+    if A > 1:
+        inp["adapter_offsets"] = torch.tensor([0, 3, 6], dtype=torch.int64)
+    y0 = oracle.forward(inp, shp, prec="f64", round_bf16=False)
+    grads = oracle.backward(inp, shp, prec="f64", round_bf16=False)
+    dy = inp["dy"].double()
+    g = torch.Generator().manual_seed(11)
+    for name, grad_name in (("topk_w", "dw"), ("A2", "dA2"), ("B2", "dB2")):
+        v = torch.randn(inp[name].shape, generator=g, dtype=torch.float64)
+        moved = dict(inp)
+        moved[name] = inp[name].double() + v
+        y1 = oracle.forward(moved, shp, prec="f64", round_bf16=False)
+        lhs = (dy * (y1 - y0)).sum().item()
+        gv = grads[grad_name]
+        if name == "topk_w":  # masked slots carry no gradient and move nothing
+            v = torch.where(inp["topk_ids"] >= 0, v, torch.zeros_like(v))
+        rhs = (gv * v).sum().item()
+        assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(lhs)), (name, lhs, rhs)
+
+
 def test_zero_scale_is_plain_moe_bitwise():
     """s = 0 with random adapters gives bit-for-bit the output of the same layer
     with the side path removed (adapters zero), in the rounded FP32 oracle."""

@@ -589,6 +589,24 @@ def test_mxfp4_equals_decoded_bf16_base_bitwise(mx_once):
         assert torch.equal(q[n], b[n]), n
 
 
+@pytest.mark.parametrize("A,act,clamp,T", [(2, "swiglu", 0.0, 256), (1, "geglu", 0.25, 200), (4, "geglu", 0.0, 512),
+                                          (1, "swiglu", 0.0, 77)])
+def test_mxfp4_in_gemm_decode_variants_bitwise(A, act, clamp, T):
+    """The in-GEMM decode under several adapters (group index = adapter * E + expert),
+    GeGLU with and without a binding clamp, and a ragged token count: bit for bit the
+    layer with the decoded values as a bf16 base."""
+    shp = Shape(T=T, H=512, I=256, E=8, k=2, r=16, A=A, mask_frac=0.1, base_fmt="mxfp4", act=act, clamp=clamp)
+    inp = make_inputs(shp, seed=36 + A + T)
+    q = run_gpu(inp, shp)
+    deq = {n: v for n, v in inp.items() if n not in ("S1", "S3", "S2")}
+    for n in ("W1", "W3", "W2"):
+        deq[n] = _decode_mxfp4_golden(inp[n], inp["S" + n[1]])
+    b = run_gpu(deq, Shape(T=T, H=512, I=256, E=8, k=2, r=16, A=A, mask_frac=0.1, act=act, clamp=clamp))
+    assert q["err"] == 0 and b["err"] == 0
+    for n in ("y", "dx", "dw") + ADAPTER_GRADS:
+        assert torch.equal(q[n], b[n]), n
+
+
 @pytest.mark.parametrize("H,I", [(576, 320), (192, 64)])
 def test_mxfp4_in_gemm_decode_off_tile_boundaries_bitwise(H, I):
     """The in-GEMM decode on partial column tiles and K rows: H, I multiples of 64 but

@@ -58,7 +58,7 @@ class _ODims(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("r", ctypes.c_int32),
                 ("A", ctypes.c_int32), ("block_m", ctypes.c_int32), ("scale", ctypes.c_double),
                 ("round_bf16", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("pad_", ctypes.c_int32), ("clamp", ctypes.c_double)]
+                ("act_quant", ctypes.c_int32), ("clamp", ctypes.c_double)]
 
 
 _TENSOR_FIELDS = ("w", "x", "dy", "W1", "W3", "W2", "A1", "A3", "B1", "B3", "A2", "B2")
@@ -78,6 +78,10 @@ def lib(prec: str = "f32") -> ctypes.CDLL:
             L.oracle_forward.restype = ctypes.c_int
             L.oracle_backward.restype = ctypes.c_int
             L.oracle_e2m1_value.restype = ctypes.c_double
+            L.oracle_e4m3_value.restype = ctypes.c_double
+            L.oracle_e4m3_round.restype = ctypes.c_double
+            L.oracle_e4m3_round.argtypes = [ctypes.c_double]
+            L.oracle_mxfp8_quantize.restype = ctypes.c_int
             L.oracle_ue8m0_value.restype = ctypes.c_double
             L.oracle_round_bf16.restype = ctypes.c_double
             L.oracle_round_bf16.argtypes = [ctypes.c_double]
@@ -119,7 +123,8 @@ def _otensor(t: Optional[torch.Tensor], prec: str, keep: _Keep, scales=None) -> 
 def _pack(inp: dict, shp, prec: str, scale: float, round_bf16: bool, nthreads: int):
     keep = _Keep()
     d = _ODims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, 128, float(scale),
-               1 if round_bf16 else 0, nthreads, 1 if shp.act == "geglu" else 0, 0, float(shp.clamp))
+               1 if round_bf16 else 0, nthreads, 1 if shp.act == "geglu" else 0,
+               1 if shp.base_fmt == "mxfp4_native" else 0, float(shp.clamp))
     ids = keep(inp["topk_ids"].to(torch.int32).contiguous().cpu())
     offs = keep(inp["adapter_offsets"].to(torch.int64).contiguous().cpu())
     fields = {}
@@ -202,6 +207,29 @@ def plan(ids: torch.Tensor, E: int, adapter_offsets: torch.Tensor, block_m: int 
 
 def e2m1_value(code: int) -> float:
     return lib("f32").oracle_e2m1_value(ctypes.c_int(code))
+
+
+def e4m3_value(code: int) -> float:
+    return lib("f32").oracle_e4m3_value(ctypes.c_int(code))
+
+
+def e4m3_round(v: float) -> float:
+    return lib("f32").oracle_e4m3_round(v)
+
+
+def mxfp8_quantize(v: torch.Tensor):
+    """MXFP8 (E4M3 elements, one UE8M0 scale per 32 from the start) of a 1-D tensor:
+    (codes uint8 [n], scale bytes uint8 [ceil(n/32)], dequantised float64 [n])."""
+    v = v.detach().double().contiguous().cpu().flatten()
+    n = v.numel()
+    codes = torch.zeros(n, dtype=torch.uint8)
+    scales = torch.zeros((n + 31) // 32, dtype=torch.uint8)
+    deq = torch.zeros(n, dtype=torch.float64)
+    bad = lib("f32").oracle_mxfp8_quantize(ctypes.c_void_p(v.data_ptr()), ctypes.c_int64(n),
+                                           ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()),
+                                           ctypes.c_void_p(deq.data_ptr()))
+    assert bad == 0
+    return codes, scales, deq
 
 
 def ue8m0_value(b: int) -> float:

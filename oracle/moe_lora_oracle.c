@@ -43,6 +43,17 @@
  * 1 mantissa bit) with one UE8M0 scale 2^(b-127) per 32 contiguous elements along
  * the contraction axis; low nibble = lower index.  Decoded here from the bit fields.
  *
+ * Native FP4 forward (act_quant = 1): the gate/up base products take x_t as MXFP8,
+ * i.e. q8(x_t), so that both operands of those products are block-scaled
+ * low-precision values ("FP8/FP4/FP8 forwards" in the PR's Fresh validation;
+ * block-scaled FP4 against dequantise-to-BF16 in its Performance notes):
+ *   g = W1_e q8(x_t) + s B1 y1,   u = W3_e q8(x_t) + s B3 y3
+ * with everything else unchanged (y1/y3 still use x_t).  q8 is the OCP MX FP8
+ * format with E4M3 elements: per 32 contiguous values one shared scale 2^X,
+ * X = floor(log2 max|v|) - 8 (8 = the exponent of E4M3's largest power of two),
+ * and each element v / 2^X rounded to nearest even on the E4M3 grid, saturating at
+ * +-448.  The backward treats q8 as the identity, like rb.
+ *
  * Build: real = float (default) or double (-DORACLE_DOUBLE).  Compile with
  * -ffp-contract=off so x86 and Arm hosts give identical results.
  */
@@ -84,7 +95,7 @@ typedef struct {
   int32_t round_bf16;     /* 1: bf16 rounding points on; 0: off */
   int32_t nthreads;       /* OpenMP threads (0 = runtime default) */
   int32_t act;            /* 0: SwiGLU, 1: GeGLU */
-  int32_t pad_;
+  int32_t act_quant;      /* 1: q8(x) in the gate/up base products (native FP4 forward) */
   double clamp;           /* activation clamp c (0 = none) */
 } odims;
 
@@ -127,6 +138,67 @@ static double e2m1_value(int code) {
 }
 
 static double ue8m0_value(uint8_t b) { return b == 255 ? NAN : ldexp(1.0, (int)b - 127); }
+
+/* E4M3 code -> value, from the bit fields: 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN
+ * (no infinities, so S.1111.110 = 448 is the largest finite magnitude). */
+static double e4m3_value(int code) {
+  int sign = (code >> 7) & 1, ebits = (code >> 3) & 15, m = code & 7;
+  if (ebits == 15 && m == 7) return NAN;
+  double mag = ebits == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, ebits - 7);
+  return sign ? -mag : mag;
+}
+
+/* v rounded to the nearest E4M3 value (ties to even), saturating at +-448.  On
+ * [2^e, 2^(e+1)) the grid spacing is 2^(e-3); below 2^-6 it is the subnormal 2^-9. */
+static double e4m3_round(double v) {
+  double a = fabs(v);
+  if (a == 0) return v;
+  int ex;
+  frexp(a, &ex); /* a in [2^(ex-1), 2^ex) */
+  int e = ex - 1 < -6 ? -6 : ex - 1;
+  double q = ldexp(1.0, e - 3);
+  double r = nearbyint(a / q) * q;
+  if (r > 448) r = 448;
+  return signbit(v) ? -r : r;
+}
+
+/* E4M3 code of a value already on the grid (the sign taken from v, also for 0). */
+static int e4m3_code(double v) {
+  int sign = signbit(v) ? 0x80 : 0;
+  double a = fabs(v);
+  for (int c = 0; c < 127; ++c)
+    if (e4m3_value(c) == a) return sign | c;
+  return -1;
+}
+
+/* One MXFP8 block of n <= 32 values: the scale byte (X + 127; X = 0 for an all-zero
+ * block, clamped to the byte range otherwise) and each value's q8 in deq[].  The
+ * division by 2^X is exact. */
+static uint8_t mxfp8_block(const real* v, int n, double* deq) {
+  double amax = 0;
+  for (int i = 0; i < n; ++i) amax = fabs((double)v[i]) > amax ? fabs((double)v[i]) : amax;
+  int X = 0;
+  if (amax > 0) {
+    int ex;
+    frexp(amax, &ex); /* floor(log2 amax) = ex - 1 */
+    X = ex - 1 - 8;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+  }
+  for (int i = 0; i < n; ++i) deq[i] = ldexp(e4m3_round(ldexp((double)v[i], -X)), X);
+  return (uint8_t)(X + 127);
+}
+
+/* q8 of a row of n values in blocks of 32 from its start */
+static void mxfp8_row(const real* v, int64_t n, real* out) {
+  double deq[32];
+  for (int64_t b = 0; b < n; b += 32) {
+    int m = n - b < 32 ? (int)(n - b) : 32;
+    mxfp8_block(v + b, m, deq);
+    for (int i = 0; i < m; ++i) out[b + i] = (real)deq[i];
+  }
+}
 
 static real ld(const otensor* t, int64_t i) {
   switch (t->dtype) {
@@ -233,14 +305,15 @@ int oracle_plan(int64_t T, int32_t k, int32_t E, int32_t A, int32_t BM, const in
 /* ---------------- per-route forward ---------------- */
 
 typedef struct {
-  real *xt, *y1, *y3, *g, *u, *h, *z2, *o, *rowbuf;
+  real *xt, *xq, *y1, *y3, *g, *u, *h, *z2, *o, *rowbuf;
 } fwd_scratch;
 
 static void fwd_alloc(const odims* d, fwd_scratch* s) {
   int64_t H = d->H, I = d->I, r = d->r;
-  int64_t n = H + 2 * r + 3 * I + r + H + (H > I ? H : I);
+  int64_t n = 2 * H + 2 * r + 3 * I + r + H + (H > I ? H : I);
   real* p = (real*)malloc(sizeof(real) * n);
   s->xt = p; p += H;
+  s->xq = p; p += H;
   s->y1 = p; p += r;
   s->y3 = p; p += r;
   s->g = p; p += I;
@@ -253,11 +326,18 @@ static void fwd_alloc(const odims* d, fwd_scratch* s) {
 
 static void fwd_free(fwd_scratch* s) { free(s->xt); }
 
+/* x_t into s->xt, and q8(x_t) into s->xq for the native FP4 forward */
+static void load_token(const odims* d, const oinputs* in, int64_t t, fwd_scratch* s) {
+  ld_row(&in->x, t * d->H, d->H, s->xt);
+  if (d->act_quant) mxfp8_row(s->xt, d->H, s->xq);
+}
+
 /* forward of one live route (t, slot with expert e, adapter a); s->xt holds x_t */
 static void route_forward(const odims* d, const oinputs* in, int a, int e, fwd_scratch* s) {
   const int64_t H = d->H, I = d->I, r = d->r, E = d->E;
   const real sc = (real)d->scale;
   real* row = s->rowbuf;
+  const real* xb = d->act_quant ? s->xq : s->xt; /* x as the gate/up base products see it */
   for (int64_t q = 0; q < r; ++q) {
     real acc1 = 0, acc3 = 0;
     ld_row(&in->A1, ((int64_t)a * r + q) * H, H, row);
@@ -270,9 +350,9 @@ static void route_forward(const odims* d, const oinputs* in, int a, int e, fwd_s
   for (int64_t i = 0; i < I; ++i) {
     real gb = 0, ub = 0, gl = 0, ul = 0;
     ld_row(&in->W1, ((int64_t)e * I + i) * H, H, row);
-    for (int64_t c = 0; c < H; ++c) gb += row[c] * s->xt[c];
+    for (int64_t c = 0; c < H; ++c) gb += row[c] * xb[c];
     ld_row(&in->W3, ((int64_t)e * I + i) * H, H, row);
-    for (int64_t c = 0; c < H; ++c) ub += row[c] * s->xt[c];
+    for (int64_t c = 0; c < H; ++c) ub += row[c] * xb[c];
     int64_t bbase = (((int64_t)a * E + e) * I + i) * r;
     for (int64_t q = 0; q < r; ++q) gl += ld(&in->B1, bbase + q) * s->y1[q];
     for (int64_t q = 0; q < r; ++q) ul += ld(&in->B3, bbase + q) * s->y3[q];
@@ -309,7 +389,7 @@ int oracle_forward(const odims* d, const oinputs* in, const int64_t* tokens, int
       int64_t t = tokens ? tokens[n] : n;
       int a = adapter_of(in, d->A, t);
       for (int64_t c = 0; c < H; ++c) acc[c] = 0;
-      ld_row(&in->x, t * H, H, s.xt);
+      load_token(d, in, t, &s);
       for (int64_t j = 0; j < k; ++j) {
         int32_t e = in->ids[t * k + j];
         if (e < 0 || e >= d->E) continue;
@@ -365,7 +445,7 @@ int oracle_backward(const odims* d, const oinputs* in, const int64_t* tokens, in
     for (int64_t n = 0; n < ntok; ++n) {
       int64_t t = tokens ? tokens[n] : n;
       int a = adapter_of(in, d->A, t);
-      ld_row(&in->x, t * H, H, s.xt);
+      load_token(d, in, t, &s);
       ld_row(&in->dy, t * H, H, dyt);
       for (int64_t c = 0; c < H; ++c) dxa[c] = 0;
       for (int64_t j = 0; j < k; ++j) {
@@ -651,6 +731,30 @@ int oracle_router_backward(int64_t T, int32_t H, int32_t E, int32_t k, int32_t n
 
 /* decoders exposed for the format pins */
 double oracle_e2m1_value(int code) { return e2m1_value(code); }
+double oracle_e4m3_value(int code) { return e4m3_value(code); }
+double oracle_e4m3_round(double v) { return e4m3_round(v); }
+
+/* MXFP8 of n values (blocks of 32 from the start): E4M3 codes[n], scale bytes
+ * [ceil(n/32)], and the dequantised values deq[n].  Returns the number of values
+ * whose q8 is not an E4M3 value times the block scale (0 when consistent). */
+int oracle_mxfp8_quantize(const double* v, int64_t n, uint8_t* codes, uint8_t* scales, double* deq) {
+  real blk[32];
+  double dq[32];
+  int bad = 0;
+  for (int64_t b = 0; b < n; b += 32) {
+    int m = n - b < 32 ? (int)(n - b) : 32;
+    for (int i = 0; i < m; ++i) blk[i] = (real)v[b + i];
+    uint8_t sb = mxfp8_block(blk, m, dq);
+    scales[b / 32] = sb;
+    for (int i = 0; i < m; ++i) {
+      deq[b + i] = dq[i];
+      int c = e4m3_code(ldexp(dq[i], 127 - (int)sb));
+      if (c < 0) ++bad;
+      codes[b + i] = (uint8_t)(c < 0 ? 0x7F : c);
+    }
+  }
+  return bad;
+}
 double oracle_ue8m0_value(int b) { return ue8m0_value((uint8_t)b); }
 double oracle_round_bf16(double v) { return (double)round_bf16((real)v); }
 int oracle_real_bytes(void) { return (int)sizeof(real); }

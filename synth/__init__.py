@@ -15,6 +15,9 @@ Workload shapes follow the pages' fixtures:
   * "prod": the matched production shape of the same PR, Matched production-shape
     performance: 65,536 tokens, H=4096, I=2048, E=256, top-6, rank 128.
   * "prod_mxfp4": the same with an MXFP4 (E2M1 + UE8M0 per 32) frozen base.
+  * "prod_native": "prod_mxfp4" with the gate/up products on block-scaled FP4
+    tensor cores (MXFP8 activations), the "native MXFP4" base the same PR times
+    beside the dequantised one (Performance).
   * "multi": several adapters sharing one MoE layer, after OpenPipe/ART PR #1139,
     Behavior (dispatched expert rows carry adapter ids).
 """
@@ -43,7 +46,7 @@ class Shape:
     mask_frac: float = 0.0  # fraction of (token, slot) routes masked out
     empty_experts: tuple = ()  # experts that receive no token
     router: str = "linear"  # "linear": logits = x W_r^T ; "normal": logits ~ N(0,1)
-    base_fmt: str = "bf16"  # "bf16" or "mxfp4"
+    base_fmt: str = "bf16"  # "bf16", "mxfp4", or "mxfp4_native" (MXFP4 base, MXFP8 gate/up activations)
     act: str = "swiglu"     # "swiglu" or "geglu"
     clamp: float = 0.0      # activation clamp c on the gate/up pre-activations (0 = none)
 
@@ -66,6 +69,11 @@ def shape(name: str, T: Optional[int] = None) -> Shape:
     if name == "prod_mxfp4":
         return Shape(T=T or 65536, H=4096, I=2048, E=256, k=6, r=128, router="normal",
                      base_fmt="mxfp4")
+    if name == "prod_e16_native":
+        return Shape(T=T or 4096, H=4096, I=2048, E=16, k=6, r=128, router="normal", base_fmt="mxfp4_native")
+    if name == "prod_native":
+        return Shape(T=T or 65536, H=4096, I=2048, E=256, k=6, r=128, router="normal",
+                     base_fmt="mxfp4_native")
     if name == "multi":
         return Shape(T=T or 16384, H=2048, I=768, E=128, k=8, r=8, A=16)
     raise KeyError(name)
@@ -185,7 +193,7 @@ def make_inputs(shp: Shape, seed: int = 0, device: str = "cpu") -> Dict[str, tor
     out["W1"] = _randn_bf16(g, (E, I, H), sH, device, 8)
     out["W3"] = _randn_bf16(g, (E, I, H), sH, device, 8)
     out["W2"] = _randn_bf16(g, (E, H, I), sI, device, 8)
-    if shp.base_fmt == "mxfp4":
+    if shp.base_fmt in ("mxfp4", "mxfp4_native"):
         for n in ("W1", "W3", "W2"):
             p, s = mxfp4_quantize(out[n])
             out[n] = p

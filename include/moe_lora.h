@@ -321,6 +321,30 @@ MOE_LORA_API int moe_lora_gemm_pair_selftest(int32_t M, int32_t N, int32_t K, co
 MOE_LORA_API int moe_lora_gemm_starved_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
                                                 const uint16_t* B, int32_t b_mn, float* C, int32_t pair,
                                                 void* stream);
+/* Self-test of the block-scaled FP4 tensor-core path (kind::mxf8f6f4) that the
+ * native FP4 forward (base_fmt 3) runs its gate/up base products on:
+ *   C[M,N] (fp32) = sum_k (Aq[m,k] 2^(As[m,k/32]-127)) (Bq[n,k] 2^(Bs[n,k/32]-127))
+ * Aq [M,K]: E4M3 codes, one per byte.  Bq [N,K/2]: E2M1 codes, two per byte, the low
+ * nibble holding the lower k; 32-byte aligned.  As [M,K/32], Bs [N,K/32]: UE8M0
+ * scale bytes.  M % 128 == 0, N % 256 == 0, K % 128 == 0.  layout selects how the
+ * scale words are placed in tensor memory (0: the layout the MoE path uses; 1: one
+ * row per lane, a comparison case that gives a wrong C).  Bad sizes:
+ * MOE_LORA_ERR_DIMS; layout out of range: MOE_LORA_ERR_UNSUPPORTED; Bq not 32-byte
+ * aligned: MOE_LORA_ERR_ALIGN.  Device-side wait timeouts are reported through
+ * moe_lora_gemm_selftest_error().  Not part of the MoE method. */
+MOE_LORA_API int moe_lora_native_selftest(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, const uint8_t* As,
+                                          const uint8_t* Bq, const uint8_t* Bs, float* C, int32_t layout,
+                                          void* stream);
+/* The MXFP8 quantiser of the native FP4 forward, standalone: for x [rows, n] bf16
+ * (device, n % 32 == 0), codes [rows, n] E4M3 and scales [rows, n/32] UE8M0 bytes,
+ * per 32 consecutive elements of a row -- the OCP MX format: shared scale 2^X with
+ * X = floor(log2 max|v|) - 8 (8 = the exponent of E4M3's largest power of two; X = 0
+ * for an all-zero block; X clamped to [-127, 127]), each element v / 2^X rounded to
+ * nearest even on the E4M3 grid and saturated at +-448.  The pages name the native
+ * forward's formats only ("FP8/FP4/FP8 forwards", PR #9, Fresh validation); this is
+ * the plainest reading.  Returns MOE_LORA_ERR_DIMS for bad sizes; rows = 0 is a no-op. */
+MOE_LORA_API int moe_lora_mxfp8_quantize(const uint16_t* x, int64_t rows, int32_t n, uint8_t* codes,
+                                         uint8_t* scales, void* stream);
 /* Device error word of the self-test GEMMs (MOE_LORA_DEV_* bits); synchronises
  * the stream and clears the word. */
 MOE_LORA_API int moe_lora_gemm_selftest_error(void* stream);

@@ -90,6 +90,11 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_gemm_starved_selftest.restype = ctypes.c_int
         L.moe_lora_gemm_starved_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P,
                                                      ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_int32, P]
+        L.moe_lora_native_selftest.restype = ctypes.c_int
+        L.moe_lora_native_selftest.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P,
+                                               ctypes.c_int32, P]
+        L.moe_lora_mxfp8_quantize.restype = ctypes.c_int
+        L.moe_lora_mxfp8_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
         L.moe_lora_mxfp4_decode.restype = ctypes.c_int
         L.moe_lora_mxfp4_decode.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                              ctypes.c_void_p]
@@ -117,7 +122,9 @@ def lib() -> ctypes.CDLL:
 def make_dims(T: int, H: int, I: int, E: int, k: int, r: int, A: int = 1, scale: float = 1.0,
               base_fmt: int = 0, act: int = 0, act_clamp: float = 0.0) -> Dims:
     """base_fmt: 0 = bf16 base weights; MXFP4 (packed E2M1 codes + UE8M0 scales S1/S3/S2) decoded
-    inside the GEMMs (1) or once per pass into the saved workspace (2);
+    inside the GEMMs (1) or once per pass into the saved workspace (2); 3 = the native FP4
+    forward (gate/up base products on block-scaled FP4 tensor cores from MXFP8 activations,
+    the rest as 1; H and I multiples of 128);
     act: 0 = SwiGLU, 1 = GeGLU; act_clamp: clamp of the gate/up pre-activations (0 = none)."""
     return Dims(T, H, I, E, k, r, A, 128, float(scale), int(act), int(base_fmt), float(act_clamp))
 
@@ -198,7 +205,7 @@ def moe_lora_plan_readback(dims: Dims, plan_ws: torch.Tensor, stream=None) -> Di
 
 
 def _weights(w: Dict[str, torch.Tensor], dims: Dims) -> Weights:
-    mx = dims.base_fmt in (1, 2)
+    mx = dims.base_fmt in (1, 2, 3)
     base = [_ptr(w[n], torch.uint8 if mx else torch.bfloat16, n) for n in ("W1", "W3", "W2")]
     side = [_ptr(w[n], torch.bfloat16, n) for n in ("A1", "A3", "B1", "B3", "A2", "B2")]
     scales = [_ptr(w[n], torch.uint8, n) if mx else None for n in ("S1", "S3", "S2")]
@@ -323,6 +330,27 @@ def moe_lora_gemm_starved_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor,
                                               _ptr(B, torch.bfloat16, "B"), int(b_mn), _ptr(C, torch.float32, "C"),
                                               int(pair), _stream(stream))
     _check(rc, "moe_lora_gemm_starved_selftest")
+
+
+def moe_lora_native_selftest(Aq: torch.Tensor, As: torch.Tensor, Bq: torch.Tensor, Bs: torch.Tensor,
+                             C: torch.Tensor, layout: int = 0, stream=None) -> None:
+    """Block-scaled FP4 self-test GEMM: C [M,N] fp32 from E4M3 codes Aq [M,K], packed
+    E2M1 codes Bq [N,K/2] and UE8M0 scale bytes As [M,K/32], Bs [N,K/32] (all uint8)."""
+    M, K = Aq.shape
+    N = Bq.shape[0]
+    rc = lib().moe_lora_native_selftest(M, N, K, _ptr(Aq, torch.uint8, "Aq"), _ptr(As, torch.uint8, "As"),
+                                        _ptr(Bq, torch.uint8, "Bq"), _ptr(Bs, torch.uint8, "Bs"),
+                                        _ptr(C, torch.float32, "C"), int(layout), _stream(stream))
+    _check(rc, "moe_lora_native_selftest")
+
+
+def moe_lora_mxfp8_quantize(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """MXFP8 (E4M3 codes, one UE8M0 scale byte per 32 along a row) of a bf16 matrix
+    x [rows, n] into codes [rows, n] and scales [rows, n/32] (uint8, device)."""
+    rows, n = x.shape
+    rc = lib().moe_lora_mxfp8_quantize(_ptr(x, torch.bfloat16, "x"), rows, n, _ptr(codes, torch.uint8, "codes"),
+                                       _ptr(scales, torch.uint8, "scales"), _stream(stream))
+    _check(rc, "moe_lora_mxfp8_quantize")
 
 
 def moe_lora_gemm_selftest_error(stream=None) -> int:

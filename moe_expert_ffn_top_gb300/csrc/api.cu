@@ -68,6 +68,20 @@ int tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
   return encode(m, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
+int tmap_2d_b8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer > 0 ? outer : 1};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {128, box_outer};
+  return encode(m, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+int tmap_fp4_unpacked(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 / 2, d0 / 2 * d1};
+  const cuuint32_t box[3] = {128, b1, 1};
+  return encode(m, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B);
+}
+
 // ------------------------------------------------------------------ device
 // Requires the current device to be an sm_103 GPU; returns its SM count (or the
 // MOELORA_NUM_SMS override, for running beside other work).
@@ -103,13 +117,16 @@ static int check_weights(const moe_lora_dims* d, const moe_lora_weights* w) {
     const int rc = check_ptr(p);
     if (rc) return rc;
   }
-  if (d->base_fmt == 1 || d->base_fmt == 2) {
+  if (d->base_fmt >= 1) {
     const void* sc[] = {w->S1, w->S3, w->S2};
     for (const void* p : sc) {
       const int rc = check_ptr(p);
       if (rc) return rc;
     }
   }
+  // the native forward's FP4 tensor maps read W1/W3 with 32-byte alignment
+  if (d->base_fmt == 3 && ((reinterpret_cast<uintptr_t>(w->W1) | reinterpret_cast<uintptr_t>(w->W3)) & 31u))
+    return MOE_LORA_ERR_ALIGN;
   return MOE_LORA_OK;
 }
 
@@ -347,6 +364,37 @@ extern "C" int moe_lora_gemm_starved_selftest(int32_t M, int32_t N, int32_t K, c
                                               const uint16_t* B, int32_t b_mn, float* C, int32_t pair,
                                               void* stream) {
   return selftest(M, N, K, A, a_mn, B, b_mn, C, pair ? 1 : 0, 1, stream);
+}
+
+extern "C" int moe_lora_native_selftest(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, const uint8_t* As,
+                                        const uint8_t* Bq, const uint8_t* Bs, float* C, int32_t layout,
+                                        void* stream) {
+  if (M <= 0 || M % 128 || N <= 0 || N % 256 || K <= 0 || K % 128) return MOE_LORA_ERR_DIMS;
+  if (layout != 0 && layout != 1) return MOE_LORA_ERR_UNSUPPORTED;
+  int rc;
+  if ((rc = check_ptr(Aq)) || (rc = check_ptr(As)) || (rc = check_ptr(Bq)) || (rc = check_ptr(Bs)) ||
+      (rc = check_ptr(C)))
+    return rc;
+  if (reinterpret_cast<uintptr_t>(Bq) % 32) return MOE_LORA_ERR_ALIGN;
+  int sms;
+  if ((rc = device_sms(&sms))) return rc;
+  int* err = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_selftest_err) != cudaSuccess) return MOE_LORA_ERR_CUDA;
+  return run_plain_native(M, N, K, Aq, As, Bq, Bs, C, layout, err, sms, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_lora_mxfp8_quantize(const uint16_t* x, int64_t rows, int32_t n, uint8_t* codes, uint8_t* scales,
+                                       void* stream) {
+  if (rows < 0 || n <= 0 || n % 32) return MOE_LORA_ERR_DIMS;
+  if (rows == 0) return MOE_LORA_OK;
+  int rc;
+  if ((rc = check_ptr(x)) || (rc = check_ptr(codes))) return rc;
+  if (!scales) return MOE_LORA_ERR_NULL;
+  int sms = 0;
+  if ((rc = device_sms(&sms))) return rc;
+  return launch_quant_mxfp8(x, rows, n, codes, scales, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_LORA_OK
+             : MOE_LORA_ERR_CUDA;
 }
 
 extern "C" int moe_lora_gemm_selftest_error(void* stream) {

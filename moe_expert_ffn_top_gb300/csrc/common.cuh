@@ -21,10 +21,12 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Returns MOE_LORA_OK when the sizes are supported.
 inline int check_dims(const moe_lora_dims* d) {
   if (!d) return MOE_LORA_ERR_NULL;
-  if ((d->act != 0 && d->act != 1) || d->base_fmt < 0 || d->base_fmt > 2) return MOE_LORA_ERR_UNSUPPORTED;
+  if ((d->act != 0 && d->act != 1) || d->base_fmt < 0 || d->base_fmt > 3) return MOE_LORA_ERR_UNSUPPORTED;
   if (!(d->act_clamp >= 0.0f) || d->act_clamp > 3.0e38f) return MOE_LORA_ERR_DIMS;
   if (d->T < 0 || d->T > (int64_t)1 << 30) return MOE_LORA_ERR_DIMS;
   if (d->H < 64 || d->H % 64 || d->I < 64 || d->I % 64) return MOE_LORA_ERR_DIMS;
+  // native FP4 forward: whole 128-wide K steps and 128-column tiles
+  if (d->base_fmt == 3 && (d->H % 128 || d->I % 128)) return MOE_LORA_ERR_DIMS;
   if (d->r < 8 || d->r > 128 || d->r % 8) return MOE_LORA_ERR_DIMS;
   if (d->k < 1 || d->k > 32 || d->E < 1 || d->A < 1 || d->A > kMaxAdapters) return MOE_LORA_ERR_DIMS;
   if ((int64_t)d->A * d->E > kMaxGroups) return MOE_LORA_ERR_DIMS;

@@ -39,8 +39,11 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   // An MXFP4 base: base_fmt 1 decodes it inside the expert GEMMs, stage by stage,
   // into the same bf16 operand tiles (ProbW13T<true>, ProbW2T<true>), so no decoded
   // copy exists anywhere; base_fmt 2 decodes it once per pass into `saved` (which the
-  // backward reuses) and runs the bf16 GEMMs on that copy.
-  const bool mx = d->base_fmt == 1;
+  // backward reuses) and runs the bf16 GEMMs on that copy.  base_fmt 3 (native FP4
+  // forward) runs the gate/up base products on block-scaled FP4 tensor cores from
+  // MXFP8 routed rows (ProbW13Nv) and the rest as base_fmt 1.
+  const bool nat = d->base_fmt == 3;
+  const bool mx = d->base_fmt == 1 || nat;
   const void* bW1 = w->W1;
   const void* bW3 = w->W3;
   const void* bW2 = w->W2;
@@ -80,8 +83,13 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.s = d->scale;
     LAUNCH(launch_gemm(p, max_tok_tiles, num_sms, stream, K_SHRINK));
   }
-  // F2: routed rows
-  LAUNCH(launch_gather_fwd(pl, x, Y13, Xp, Y13p, d->H, 2 * d->r, num_sms, stream));
+  // F2: routed rows (native: as MXFP8 codes Xq [P,H] and scale words, in the Xp buffer)
+  uint8_t* Xq = reinterpret_cast<uint8_t*>(Xp);
+  uint8_t* Xs = Xq + P * H;
+  if (nat)
+    LAUNCH(launch_gather_fwd_mxfp8(pl, x, Y13, Xq, Xs, Y13p, d->H, 2 * d->r, num_sms, stream));
+  else
+    LAUNCH(launch_gather_fwd(pl, x, Y13, Xp, Y13p, d->H, 2 * d->r, num_sms, stream));
   // F3: W13 + expert-local expand + SwiGLU
   auto w13 = [&](auto p) -> int {
     MAP(tmap_2d(&p.mXp, Xp, H, P, 64, 128));
@@ -114,7 +122,31 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     LAUNCH(launch_gemm(p, max_row_tiles * cdiv(d->I, 128), num_sms, stream, K_W13));
     return 0;
   };
-  if ((rc = mx ? w13(ProbW13T<true>{}) : w13(ProbW13T<false>{}))) return rc;
+  if (nat) {
+    ProbW13Nv p;
+    MAP(tmap_2d_b8(&p.mXq, Xq, H, P, 128));
+    MAP(tmap_fp4_unpacked(&p.mW1f, w->W1, H, I, E, 128));
+    MAP(tmap_fp4_unpacked(&p.mW3f, w->W3, H, I, E, 128));
+    MAP(tmap_2d(&p.mY13p, Y13p, 2 * r, P, 64, 128));
+    MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 128));
+    MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 128));
+    MAP(tmap_2d_store32(&p.mG, Gs, I, P));
+    MAP(tmap_2d_store32(&p.mU, Us, I, P));
+    MAP(tmap_2d_store32(&p.mAct, Act, I, P));
+    p.Xs = Xs;
+    p.S1q = w->S1;
+    p.S3q = w->S3;
+    p.pl = pl;
+    p.err = pl.err;
+    p.H = d->H;
+    p.I = d->I;
+    p.r = d->r;
+    p.act = d->act;
+    p.clamp = d->act_clamp;
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13));
+  } else if ((rc = mx ? w13(ProbW13T<true>{}) : w13(ProbW13T<false>{}))) {
+    return rc;
+  }
   // F4/F5: W2 + expert-local A2 shrink
   auto w2 = [&](auto p) -> int {
     MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));

@@ -44,6 +44,22 @@
 // latency; the scale bytes (rows too narrow for TMA in general) are loaded by the
 // decoding threads one K step ahead.
 //
+// Block-scaled FP4 problems (P::kNative): 128-row tiles with one 128 x 256
+// accumulator (columns 0..255); tensor-memory columns 256.. hold each stage's scale
+// words (kNvSfCols per stage).  On a native K step (K = 128) the A tile holds 128 rows
+// of 128 E4M3 codes and the B tile 256 rows of 128 E2M1 codes, each code in its own
+// byte position as TMA's 16U4_ALIGN16B type writes them (16 codes in 8 bytes, then 8
+// bytes of gap); every row carries one UE8M0 scale per 32 K elements.  Such a copy
+// counts its PACKED bytes on the stage barrier (64 per row of 128 codes), not the
+// bytes it writes to shared memory (measured: expecting the latter never completes).  The epilogue
+// warps walk the K steps like decoders: for a native step they write the stage's scale
+// words into tensor memory and arrive on the stage's decoded barrier, which the MMA
+// waits on; it then issues four kind::mxf8f6f4 MMAs of K = 32 (scale byte kk of each
+// word for step kk).  Other K steps of such a problem are ordinary BF16 steps.
+//   static constexpr bool kNative;
+//   bool     native_step(const TileInfo&, int ks) const;
+//   NvScales nv_scales(const TileInfo&, int ks) const;   where the step's scale words are
+//
 // Operand tiles in shared memory use the 128-byte swizzle written by TMA:
 //   A K-major : 128 rows x 128 B                         (one 16 KB box)
 //   A MN-major: two boxes of 64 K-rows x 64 M, 8 KB apart
@@ -71,6 +87,12 @@ constexpr int kStgBytes = 8 * kStgWordsPerWarp * 4;
 // pipeline stages (at most 192 KB), staging, barriers, and slack to align the base
 constexpr int kGemmSmemBytes = 192 * 1024 + kStgBytes + 256 + 1024;
 
+// P::kNative when the problem declares it, else false.
+template <class P, class = void>
+struct NativeOf : std::false_type {};
+template <class P>
+struct NativeOf<P, std::void_t<decltype(P::kNative)>> : std::integral_constant<bool, P::kNative> {};
+
 // Per-problem pipeline shape.  Narrow problems: 128-row tiles, 4 stages of
 // (A 16 KB + B 32 KB), two TMEM accumulators (the epilogue of one tile overlaps the
 // main loop of the next).  Wide problems (P::kWide): 256-row tiles as two M=128
@@ -83,7 +105,7 @@ struct EngineShape {
   static constexpr int kAStage = kWide ? 2 * 128 * 128 : 128 * 128;
   static constexpr int kStage = kAStage + kBStageBytes;
   static constexpr int kStages = kWide ? 3 : 4;
-  static constexpr int kAccBufs = kWide ? 1 : 2;
+  static constexpr int kAccBufs = kWide || NativeOf<P>::value ? 1 : 2;
   static_assert(kStages * kStage <= 192 * 1024, "pipeline exceeds shared memory budget");
 };
 
@@ -227,6 +249,71 @@ __device__ __forceinline__ bool mx_decode_stage(uint8_t* sb, int dt, const uint3
   return true;
 }
 
+// ------------------------------------------------------------------ block-scaled FP4
+// Scale words of a native K step: 4 UE8M0 bytes (the step's four 32-element blocks,
+// byte j for K elements 32j..32j+31) per operand row, row i of the A tile at
+// a + i * as, row i of the B tile at b[i >> 7] + (i & 127) * bs (4-byte aligned).
+struct NvScales {
+  const uint8_t* a;
+  const uint8_t* b[2];
+  int64_t as, bs;
+};
+constexpr int kNvSfCols = 12;  // per stage: A 4 columns, then B 8 columns
+// Layout of the scale words in tensor memory.  kNvLayoutGroups (the one the MMAs use):
+// the words of operand row i sit in column i / 32 of that operand's block at lane i % 32
+// of every lane quarter (each quarter holds all rows).  kNvLayoutRows (self-test
+// comparison only): row i at lane i % 128 of column i / 128.
+constexpr int kNvLayoutGroups = 0, kNvLayoutRows = 1;
+__device__ __forceinline__ uint32_t ldg_issue_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+// The six words this thread (lane of a quarter; half 0 / 1 = the first / second warp
+// of that quarter) stores for one step.  kNvLayoutGroups: half 0 takes A columns 0..3
+// and B columns 0..1, half 1 B columns 2..7 (A/B row 32c + lane for column c).
+template <int L>
+__device__ __forceinline__ void nv_load_scales(const NvScales& sc, int q, int half, int lane, uint32_t (&w)[6]) {
+  if (L == kNvLayoutGroups) {
+    if (half == 0) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) w[c] = ldg_issue_u32(sc.a + (32 * c + lane) * sc.as);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) w[4 + c] = ldg_issue_u32(sc.b[0] + (32 * c + lane) * sc.bs);
+    } else {
+#pragma unroll
+      for (int c = 2; c < 8; ++c) {
+        const int row = 32 * c + lane;
+        w[c - 2] = ldg_issue_u32(sc.b[row >> 7] + (row & 127) * sc.bs);
+      }
+    }
+  } else {
+    const int row = 32 * q + lane;
+    w[0] = ldg_issue_u32(sc.a + row * sc.as);
+    w[1] = ldg_issue_u32(sc.b[0] + row * sc.bs);
+    w[2] = ldg_issue_u32(sc.b[1] + row * sc.bs);
+    w[3] = w[4] = w[5] = 0;
+  }
+}
+// Stores them at the stage's scale columns (sf: tensor-memory address of column 0 of
+// the stage's block, lane 0) in this warp's lane quarter.
+template <int L>
+__device__ __forceinline__ void nv_store_scales(uint32_t sf, int q, int half, const uint32_t (&w)[6]) {
+  const uint32_t qa = sf + ((uint32_t)(32 * q) << 16);
+  if (L == kNvLayoutGroups) {
+    if (half == 0) {
+      tmem_st4(qa, w[0], w[1], w[2], w[3]);
+      tmem_st2(qa + 4, w[4], w[5]);
+    } else {
+      tmem_st2(qa + 6, w[0], w[1]);
+      tmem_st4(qa + 8, w[2], w[3], w[4], w[5]);
+    }
+  } else if (half == 0) {
+    tmem_st4(qa, w[0], w[0], w[0], w[0]);
+    tmem_st2(qa + 4, w[1], w[2]);
+  }
+}
+
 // P::kNoinlineEpilogue when the problem declares it, else false (see epilogue_call).
 template <class P, class = void>
 struct NoinlineEpilogueOf : std::false_type {};
@@ -239,6 +326,11 @@ template <class P, class = void>
 struct DecodeOf : std::false_type {};
 template <class P>
 struct DecodeOf<P, std::void_t<decltype(P::kDecode)>> : std::integral_constant<bool, P::kDecode> {};
+// P::kNvLayout (self-test problems) or the layout the MMAs use.
+template <class P, class = void>
+struct NvLayoutOf : std::integral_constant<int, kNvLayoutGroups> {};
+template <class P>
+struct NvLayoutOf<P, std::void_t<decltype(P::kNvLayout)>> : std::integral_constant<int, P::kNvLayout> {};
 template <class P>
 constexpr int gemm_threads() {
   return 64 + 32 * P::kEpiWarps;
@@ -262,6 +354,12 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
   static_assert(P::kEpiWarps == 4 || P::kEpiWarps == 8, "4 or 8 epilogue warps");
   static_assert(!P::kWide || (P::kEpiWarps == 8 && !P::kAmn), "wide tiles: 8 epilogue warps, K-major A");
   static_assert(!DecodeOf<P>::value || P::kWide, "decoding epilogue warps need 256-row tiles");
+  static_assert(!NativeOf<P>::value || (!P::kWide && P::kEpiWarps == 8 && !P::kAmn && !P::kBmn && !DecodeOf<P>::value),
+                "block-scaled problems: 128-row tiles, 8 epilogue warps, K-major operands");
+  static_assert(!NativeOf<P>::value || kAccCols + S::kStages * kNvSfCols <= 2 * kAccCols, "scale words exceed TMEM");
+  // The epilogue warps walk the K steps (and the MMA waits for them) in decoding and
+  // block-scaled problems.
+  constexpr bool kWalk = DecodeOf<P>::value || NativeOf<P>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStage + kStgBytes);
@@ -339,15 +437,33 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(S::kWide ? 0 : acc * kAccCols);
         for (int ks = 0; ks < ti.nk; ++ks) {
-          if (!mbar_wait(DecodeOf<P>::value ? &dec[s] : &full[s], ph, err)) {
+          if (!mbar_wait(kWalk ? &dec[s] : &full[s], ph, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const MmaStep st = p.mma_step(ti, ks);
-          const uint32_t idesc = idesc_bf16_f32(128, st.n, P::kAmn, P::kBmn);
           const uint32_t sa = smem_u32(smem + s * S::kStage);
           const uint32_t sb = sa + S::kAStage + (uint32_t)st.b_off;
+          if constexpr (NativeOf<P>::value) {
+            if (p.native_step(ti, ks)) {
+              // 128 K elements of one-byte codes: four K = 32 steps, 32 bytes apart,
+              // step kk using byte kk of every scale word
+              const uint32_t sfa = tmem_base + (uint32_t)(kAccCols + s * kNvSfCols);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_mx(d + (uint32_t)st.col, sw128_desc(sa + kk * 32, 16, 1024), sw128_desc(sb + kk * 32, 16, 1024),
+                       idesc_mx_f32(128, st.n, kMxTypeE4M3, kMxTypeE2M1, kk, kk), sfa, sfa + 4,
+                       (st.first && kk == 0) ? 0u : 1u);
+              mma_commit(&empty[s]);
+              if (++s == S::kStages) {
+                s = 0;
+                ph ^= 1u;
+              }
+              continue;
+            }
+          }
+          const uint32_t idesc = idesc_bf16_f32(128, st.n, P::kAmn, P::kBmn);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = P::kAmn ? sw128_desc(sa + kk * 2048, 8192, 1024) : sw128_desc(sa + kk * 32, 16, 1024);
@@ -404,10 +520,14 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
       }
       return true;
     };
-    if constexpr (DecodeOf<P>::value) {
-      // Decode every K step of this CTA's tiles (in the producer's order), then run each
-      // tile's epilogue after its last step.  Tiles without K steps have nothing to
-      // decode and no accumulator; they get epilogue_empty.
+    if constexpr (kWalk) {
+      // Decode every K step of this CTA's tiles (in the producer's order), or write
+      // its scale words, then run each tile's epilogue after its last step.  Tiles
+      // without K steps have nothing to decode and no accumulator; they get
+      // epilogue_empty.
+      constexpr bool kNat = NativeOf<P>::value;
+      constexpr int kNvL = NvLayoutOf<P>::value;
+      constexpr int kPre = kNat ? 6 : 2;  // words loaded one step ahead per thread
       constexpr int NT = 32 * P::kEpiWarps;
       const int dt = threadIdx.x - 64;  // decoder thread 0..NT-1
       int t = blockIdx.x, ks = 0;
@@ -430,33 +550,58 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         ti.nk = 0;  // exhausted: every later call returns false too
         return false;
       };
+      // whether step (ti, ks) needs the walkers' work, and its words loaded ahead
+      auto step_work = [&]() -> bool {
+        if constexpr (kNat)
+          return p.native_step(ti, ks);
+        else
+          return p.decodes(ti, ks);
+      };
+      auto load_pre = [&](uint32_t (&w)[kPre]) {
+        if constexpr (kNat)
+          nv_load_scales<kNvL>(p.nv_scales(ti, ks), q, half, lane, w);
+        else
+          mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, w);
+      };
       int s = 0;
       uint32_t ph = 0;
-      uint32_t sc[2] = {127u, 127u};  // the current step's scale bytes (two items)
+      uint32_t sc[kPre];  // the current step's scale bytes (two items) or words
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) sc[i] = 127u;
       bool have = next();
-      bool cdec = have && p.decodes(ti, ks);
-      if (cdec) mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, sc);
+      bool cdec = have && step_work();
+      if (cdec) load_pre(sc);
       while (have) {
         // The next step's scale bytes are loaded before this step is decoded; after a
         // tile's last step the iterator moves on only once the epilogue has run (the
         // epilogue needs the registers).
         const bool last = ks == ti.nk - 1;
-        uint32_t nsc[2] = {127u, 127u};
+        uint32_t nsc[kPre];
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) nsc[i] = 127u;
         bool ndec = false;
         if (!last) {
           next();  // ks + 1 of the same tile
-          ndec = p.decodes(ti, ks);
-          if (ndec) mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, nsc);
+          ndec = step_work();
+          if (ndec) load_pre(nsc);
         }
-        // Steps that decode agree inside mx_decode_stage; the others here.  Either way
-        // all decoding warps pass the same barriers and leave the loop together.
         const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], ph, err));
-        if (cdec) {
-          if (!mx_decode_stage<NT, P::kMxMN>(smem + s * S::kStage + S::kAStage, dt, sc, got)) break;
-        } else if (!decoders_agree<NT>(got)) {
-          break;
+        if constexpr (kNat) {
+          // Each warp writes its own lane quarter: no barrier between the warps, and a
+          // warp whose wait gave up simply leaves (the MMA's wait then gives up too).
+          if (!got) break;
+          if (cdec) nv_store_scales<kNvL>(tmem_base + (uint32_t)(kAccCols + s * kNvSfCols), q, half, sc);
+          tc_fence_before();
+        } else {
+          // Steps that decode agree inside mx_decode_stage; the others here.  Either
+          // way all decoding warps pass the same barriers and leave the loop together.
+          if (cdec) {
+            if (!mx_decode_stage<NT, P::kMxMN>(smem + s * S::kStage + S::kAStage, dt, sc, got)) break;
+          } else if (!decoders_agree<NT>(got)) {
+            break;
+          }
+          fence_proxy_async_smem();  // generic-proxy stores before the MMA's reads
         }
-        fence_proxy_async_smem();  // generic-proxy stores before the MMA's reads
         __syncwarp();
         if (lane == 0) mbar_arrive(&dec[s]);
         if (++s == S::kStages) {
@@ -464,13 +609,17 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           ph ^= 1u;
         }
         if (last) {
-          if (!decoders_agree<NT>(run_epilogue(ti))) break;
+          if constexpr (kNat) {
+            if (!run_epilogue(ti)) break;
+          } else {
+            if (!decoders_agree<NT>(run_epilogue(ti))) break;
+          }
           have = next();
-          ndec = have && p.decodes(ti, ks);
-          if (ndec) mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, nsc);
+          ndec = have && step_work();
+          if (ndec) load_pre(nsc);
         }
-        sc[0] = nsc[0];
-        sc[1] = nsc[1];
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) sc[i] = nsc[i];
         cdec = ndec;
       }
     } else {

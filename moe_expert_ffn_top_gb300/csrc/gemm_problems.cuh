@@ -519,6 +519,86 @@ struct ProbW13T {
 };
 using ProbW13 = ProbW13T<false>;
 
+// Native FP4 forward F3: the gate/up base products on block-scaled FP4 tensor cores,
+//   G = q8(Xp) W1_e^T + s (Y1p B1_e^T),   U = q8(Xp) W3_e^T + s (Y3p B3_e^T)
+// with q8(Xp) the routed rows as MXFP8 (E4M3 codes Xq + scale words Xs, from
+// launch_gather_fwd_mxfp8) and W1/W3 in MXFP4 as stored -- no decoded copy.  128-row
+// tiles x (128 W1 rows + 128 W3 rows): H/128 native K steps, then the BF16 side-LoRA
+// steps of ProbW13 into the same accumulator; the same epilogue.  H, I multiples of 128.
+struct ProbW13Nv {
+  static constexpr bool kAmn = false, kBmn = false, kWide = false, kNative = true;
+  static constexpr int kEpiWarps = 8;
+  const uint8_t* Xs;          // [P/128][H/128][128][4] scale bytes of Xq
+  const uint8_t *S1q, *S3q;   // [E,I,H/32] scale bytes of W1/W3
+  CUtensorMap mXq;            // Xq (H,P) bytes, box (128,128)
+  CUtensorMap mW1f, mW3f;     // W1/W3 E2M1 (H,I,E), box (128 codes, 128, 1)
+  CUtensorMap mY13p, mB1, mB3;  // as ProbW13
+  CUtensorMap mG, mU, mAct;
+  PlanView pl;
+  int* err;
+  int H, I, r;
+  int act;
+  float clamp;
+  __device__ int ntn() const { return I / 128; }
+  __device__ int nkr() const { return (r + 63) / 64; }
+  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    TileInfo ti;
+    ti.n0 = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti) * 128;
+    ti.sub = 0;
+    ti.nk = H / 128 + 2 * nkr();
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mXq);
+    tma_prefetch_map(&mW1f);
+    tma_prefetch_map(&mW3f);
+    tma_prefetch_map(&mY13p);
+    tma_prefetch_map(&mB1);
+    tma_prefetch_map(&mB3);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    const int nb = H / 128;
+    if (ks < nb) {
+      const int e = ti.g % pl.E;
+      mbar_arrive_expect_tx(bar, 128 * 128 + 2 * 128 * 64);  // E2M1 boxes count packed bytes
+      tma_load_2d(sa, &mXq, bar, ks * 128, ti.m0);
+      tma_load_3d(sb, &mW1f, bar, ks * 128, ti.n0, e);
+      tma_load_3d(sb + 128 * 128, &mW3f, bar, ks * 128, ti.n0, e);
+    } else {
+      const int j = ks - nb, half = j / nkr(), kb = j % nkr();
+      mbar_arrive_expect_tx(bar, kAStage128 + 128 * 128);
+      tma_load_2d(sa, &mY13p, bar, half * r + kb * kBK, ti.m0);
+      tma_load_3d(sb, half ? &mB3 : &mB1, bar, kb * kBK, ti.n0, ti.g);
+    }
+  }
+  __device__ bool native_step(const TileInfo&, int ks) const { return ks < H / 128; }
+  __device__ NvScales nv_scales(const TileInfo& ti, int ks) const {
+    const int64_t rs = H / 32;
+    const int64_t wo = ((int64_t)(ti.g % pl.E) * I + ti.n0) * rs + ks * 4;
+    return NvScales{Xs + ((int64_t)(ti.m0 >> 7) * (H / 128) + ks) * 512, {S1q + wo, S3q + wo}, 4, rs};
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const {
+    const int nb = H / 128;
+    if (ks < nb) return MmaStep{256, 0, 0, ks == 0};
+    return MmaStep{128, ((ks - nb) / nkr()) * 128, 0, 0};
+  }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
+    const int y0 = ti.m0 + row - (threadIdx.x & 31);  // warp's first row
+    TmaStoreRing out(stg);
+    for (int c = c0; c < 128; c += cs) {
+      float g[32], u[32], a[32];
+      tmem_ld32(taddr + c, g);
+      tmem_ld32(taddr + 128 + c, u);
+      act_fwd_chunk(act, clamp, g, u, a);
+      out.store_bf16(&mG, ti.n0 + c, y0, g);
+      out.store_bf16(&mU, ti.n0 + c, y0, u);
+      out.store_bf16(&mAct, ti.n0 + c, y0, a);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
+};
+
 // =====================================================================================
 // Forward F4/F5 -- W2 expert GEMM with the expert-local A2 shrink:
 //   O = Act W2_e^T  [P,H] (unweighted),   Z2 = bf16(Act A2_ae^T) [P,r]
@@ -1393,6 +1473,62 @@ struct ProbPlain {
       float v[32];
       tmem_ld32(taddr + c, v);
       warp_store_rows_f32(o0 + c, N, 32, v, 1.0f, tn() - c < 32 ? tn() - c : 32, stg);
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
+};
+
+// Block-scaled plain GEMM (self-test of the native FP4 path):
+//   C[M,N] = (Aq x 2^(As-127)) (Bq x 2^(Bs-127))^T   in fp32
+// with Aq [M,K] E4M3 codes, As [M,K/32] and Bs [N,K/32] UE8M0 bytes (one per 32 K
+// elements), Bq [N,K/2] packed E2M1 codes (low nibble = lower K).  M % 128 == 0,
+// N % 256 == 0, K % 128 == 0.  L: layout of the scale words in tensor memory.
+template <int L>
+struct ProbPlainNv {
+  static constexpr bool kAmn = false, kBmn = false, kWide = false, kNative = true;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kNvLayout = L;
+  CUtensorMap mA, mB;  // Aq (K,M) bytes, box (128,128); Bq (K,N) E2M1, box (128,256)
+  const uint8_t *As, *Bs;
+  int* err;
+  float* C;
+  int M, N, K;
+  __device__ int ntn() const { return N / 256; }
+  __device__ int num_tiles() const { return M / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    TileInfo ti;
+    ti.m0 = t / ntn() * 128;
+    ti.n0 = t % ntn() * 256;
+    ti.mend = ti.m0 + 128;
+    ti.g = 0;
+    ti.sub = 0;
+    ti.nk = K / 128;
+    ti.k0 = 0;
+    ti.mh = 1;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mA);
+    tma_prefetch_map(&mB);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+    mbar_arrive_expect_tx(bar, 128 * 128 + 256 * 64);  // E2M1 boxes count packed bytes
+    tma_load_2d(sa, &mA, bar, ks * 128, ti.m0);
+    tma_load_3d(sb, &mB, bar, ks * 128, ti.n0, 0);
+  }
+  __device__ bool native_step(const TileInfo&, int) const { return true; }
+  __device__ NvScales nv_scales(const TileInfo& ti, int ks) const {
+    const int64_t rs = K / 32;
+    const uint8_t* b = Bs + ti.n0 * rs + ks * 4;
+    return NvScales{As + ti.m0 * rs + ks * 4, {b, b + 128 * rs}, rs, rs};
+  }
+  __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
+    float* o0 = C + ((int64_t)ti.m0 + row - (threadIdx.x & 31)) * N + ti.n0;  // warp's first row
+    for (int c = c0; c < 256; c += cs) {
+      float v[32];
+      tmem_ld32(taddr + c, v);
+      warp_store_rows_f32(o0 + c, N, 32, v, 1.0f, 32, stg);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}

@@ -52,6 +52,13 @@ cudaError_t launch_dequant_mxfp4(const uint8_t* packed, const uint8_t* scales, u
 // Xp[p] = x[token(p)], Y13p[p] = Y13[token(p)]; zero rows for padding.
 cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint16_t* Xp,
                               uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream);
+// Native FP4 forward: routed rows of x as MXFP8 -- E4M3 codes Xq [P,H] and scale
+// bytes Xs in the tile-major layout [P/128][H/128][128][4] (H % 128 == 0) -- and Y13p.
+cudaError_t launch_gather_fwd_mxfp8(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint8_t* Xq,
+                                    uint8_t* Xs, uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream);
+// Standalone MXFP8 quantiser (row-major scale bytes [rows, n/32]); n % 32 == 0.
+cudaError_t launch_quant_mxfp8(const uint16_t* x, int64_t rows, int n, uint8_t* codes, uint8_t* scales,
+                               int num_sms, cudaStream_t stream);
 
 // Z2w[t] = bf16(sum_j w_tj Z2[row(t,j)])  [T,r]
 cudaError_t launch_z2w(const PlanView& pl, const uint16_t* Z2, const float* topk_w, uint16_t* Z2w, int r,

@@ -79,6 +79,135 @@ __global__ void gather_fwd_kernel(PlanView pl, const uint16_t* __restrict__ x, c
   zero_padding_rows(pl, Xp, H, Y13p, r2);
 }
 
+// ---------------------------------------------------------------- MXFP8 routed rows
+// E4M3 code of v (already divided by the block scale): round to nearest even,
+// saturating at +-448 -- the conversion instruction's own rounding.  Two values per
+// instruction; `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 2^e as a float for e in [-127, 127] (2^-127 is subnormal)
+__device__ __forceinline__ float exp2i(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << 22);
+}
+// One MXFP8 block of 32 bf16 (OCP MX: shared scale 2^X, X = floor(log2 max|v|) - 8,
+// X = 0 for an all-zero block, clamped to [-127, 127]): the 32 E4M3 codes and the
+// scale byte X + 127.
+__device__ __forceinline__ uint32_t mxfp8_block(const uint4 (&v)[4], uint4 (&codes)[2]) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      f[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  int X = 0;
+  if (amax > 0.f) {
+    const uint32_t b = __float_as_uint(amax);
+    const int e = (int)(b >> 23);
+    const int fl = e ? e - 127 : (31 - __clz((int)b)) - 149;  // floor(log2 amax), subnormals too
+    X = min(max(fl - 8, -127), 127);
+  }
+  const float inv = exp2i(-X);  // exact scaling by a power of two
+  uint32_t q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    q[i] = e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) | (e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+  codes[0] = make_uint4(q[0], q[1], q[2], q[3]);
+  codes[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  return (uint32_t)(X + 127);
+}
+
+// Forward routed rows for the native FP4 forward, by scatter like gather_fwd_kernel:
+// one warp per token quantises its x row once to MXFP8 (lane = one 32-element block)
+// and writes the codes to each routed row of Xq [P,H], the scale bytes to Xs in the
+// tile-major layout [P/128][H/128][128 rows][4 blocks] (one 4-byte word per row and
+// 128-wide K step), and the token's Y13 row to Y13p.  Padding rows get zero codes and
+// scale bytes 127.
+__global__ void gather_fwd_mxfp8_kernel(PlanView pl, const uint16_t* __restrict__ x,
+                                        const uint16_t* __restrict__ Y13, uint8_t* __restrict__ Xq,
+                                        uint8_t* __restrict__ Xs, uint16_t* __restrict__ Y13p, int H, int r2) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int k = pl.k, ks_per_row = H / 128;
+  for (int64_t t = w0; t < pl.T; t += nw) {
+    const int* rows = pl.row_of_route + t * k;
+    for (int b0 = 0; b0 < H / 32; b0 += 32) {  // 32 blocks of 32 per pass
+      const int blk = b0 + lane;
+      const bool on = blk < H / 32;
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[i] = on ? __ldg(reinterpret_cast<const uint4*>(x + t * H + blk * 32 + 8 * i)) : make_uint4(0, 0, 0, 0);
+      uint4 codes[2];
+      const uint32_t sb = mxfp8_block(v, codes);
+      // the 4 scale bytes of one K step (blocks 4j..4j+3) as one word, on lane 4j
+      const uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8) |
+                            (__shfl_down_sync(0xffffffffu, sb, 2) << 16) | (__shfl_down_sync(0xffffffffu, sb, 3) << 24);
+      for (int j = 0; j < k; ++j) {
+        const int R = rows[j];
+        if (R < 0 || !on) continue;
+        uint4* dst = reinterpret_cast<uint4*>(Xq + (int64_t)R * H + blk * 32);
+        dst[0] = codes[0];
+        dst[1] = codes[1];
+        if ((lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(Xs + ((int64_t)(R >> 7) * ks_per_row + (blk >> 2)) * 512 + (R & 127) * 4) =
+              word;
+      }
+    }
+    for (int c = lane * 8; c < r2; c += 32 * 8) {
+      const uint4 y = __ldg(reinterpret_cast<const uint4*>(Y13 + t * r2 + c));
+      for (int j = 0; j < k; ++j) {
+        const int R = rows[j];
+        if (R >= 0) *reinterpret_cast<uint4*>(Y13p + (int64_t)R * r2 + c) = y;
+      }
+    }
+  }
+  // padding rows: zero codes (H bytes = H/2 bf16 of zeros) and neutral scale words
+  const int wib = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  for (int g = blockIdx.x; g < pl.G; g += gridDim.x) {
+    const int beg = pl.offsets[g] + pl.counts[g], end = pl.offsets[g + 1];
+    for (int64_t p = beg + wib; p < end; p += wpb) {
+      copy_row_or_zero(reinterpret_cast<uint16_t*>(Xq + p * H), nullptr, H / 2, lane);
+      copy_row_or_zero(Y13p + p * r2, nullptr, r2, lane);
+      for (int j = lane; j < ks_per_row; j += 32)
+        *reinterpret_cast<uint32_t*>(Xs + ((p >> 7) * ks_per_row + j) * 512 + (p & 127) * 4) = 0x7F7F7F7Fu;
+    }
+  }
+}
+
+// The same MXFP8 quantisation on its own: one warp per row of x [rows, n], one
+// 32-element block per lane, codes [rows, n] and scale bytes [rows, n/32] row-major.
+__global__ void quant_mxfp8_kernel(const uint16_t* __restrict__ x, int64_t rows, int n, uint8_t* __restrict__ codes,
+                                   uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nb = n / 32;
+  for (int64_t t = w0; t < rows; t += nw) {
+    for (int blk = lane; blk < nb; blk += 32) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(x + t * n + blk * 32 + 8 * i));
+      uint4 c[2];
+      const uint32_t sb = mxfp8_block(v, c);
+      uint4* dst = reinterpret_cast<uint4*>(codes + t * n + blk * 32);
+      dst[0] = c[0];
+      dst[1] = c[1];
+      scales[t * nb + blk] = (uint8_t)sb;
+    }
+  }
+}
+
 // one warp per token; lane covers r/32.. columns (r <= 128 -> up to 4 per lane)
 __global__ void z2w_kernel(PlanView pl, const uint16_t* __restrict__ Z2, const float* __restrict__ topk_w,
                            uint16_t* __restrict__ Z2w, int r) {
@@ -376,6 +505,20 @@ cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint1
   prof_begin(K_GATHER_FWD, stream);
   gather_fwd_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, x, Y13, Xp, Y13p, H, r2);
   prof_end(K_GATHER_FWD, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_fwd_mxfp8(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint8_t* Xq,
+                                    uint8_t* Xs, uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream) {
+  prof_begin(K_GATHER_FWD, stream);
+  gather_fwd_mxfp8_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, x, Y13, Xq, Xs, Y13p, H, r2);
+  prof_end(K_GATHER_FWD, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mxfp8(const uint16_t* x, int64_t rows, int n, uint8_t* codes, uint8_t* scales,
+                               int num_sms, cudaStream_t stream) {
+  quant_mxfp8_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(x, rows, n, codes, scales);
   return cudaGetLastError();
 }
 

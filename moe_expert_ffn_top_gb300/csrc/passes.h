@@ -28,5 +28,8 @@ int run_router_backward(const moe_lora_dims* d, const AdapterTable& at, const ui
 // issued, so the pipeline's bounded waits expire (error-path self-test).
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,
                    int* err, int num_sms, int pair, int starve, cudaStream_t stream);
+// Block-scaled plain GEMM through the native FP4 engine path (see ProbPlainNv).
+int run_plain_native(int M, int N, int K, const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                     float* C, int layout, int* err, int num_sms, cudaStream_t stream);
 
 }  // namespace moelora

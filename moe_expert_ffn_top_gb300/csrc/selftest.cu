@@ -63,5 +63,29 @@ int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint1
   return plain<false, false>(M, N, K, A, B, C, err, num_sms, pr, starve, stream);
 }
 
+template <int L>
+static int plain_native(int M, int N, int K, const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq,
+                        const uint8_t* Bs, float* C, int* err, int num_sms, cudaStream_t stream) {
+  ProbPlainNv<L> p;
+  if (tmap_2d_b8(&p.mA, Aq, (uint64_t)K, (uint64_t)M, 128) ||
+      tmap_fp4_unpacked(&p.mB, Bq, (uint64_t)K, (uint64_t)N, 1, 256))
+    return MOE_LORA_ERR_CUDA;
+  p.As = As;
+  p.Bs = Bs;
+  p.err = err;
+  p.C = C;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  return launch_gemm(p, M / 128 * (N / 256), num_sms, stream, K_SELFTEST) == cudaSuccess ? MOE_LORA_OK
+                                                                                       : MOE_LORA_ERR_CUDA;
+}
+
+int run_plain_native(int M, int N, int K, const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                     float* C, int layout, int* err, int num_sms, cudaStream_t stream) {
+  if (layout == kNvLayoutRows) return plain_native<kNvLayoutRows>(M, N, K, Aq, As, Bq, Bs, C, err, num_sms, stream);
+  return plain_native<kNvLayoutGroups>(M, N, K, Aq, As, Bq, Bs, C, err, num_sms, stream);
+}
+
 }  // namespace moelora
 

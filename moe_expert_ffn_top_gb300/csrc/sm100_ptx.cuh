@@ -160,6 +160,53 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Block-scaled MMA (kind::mxf8f6f4, scale_vec::1X): per 32 K elements each row of A
+// and of B carries one UE8M0 scale 2^(b-127), read from tensor memory.  Element
+// type codes of the instruction descriptor for this kind: E4M3 = 0, E2M1 = 5.
+constexpr int kMxTypeE4M3 = 0;
+constexpr int kMxTypeE2M1 = 5;
+
+// Instruction descriptor of a block-scaled MMA, both operands K-major, fp32
+// accumulation implied.  Fields: [4,6) which byte of B's 32-bit scale words this
+// step uses, [7,10) A type, [10,13) B type, [17,23) N >> 3, 23 scale type (1 =
+// UE8M0), [24,29) M >> 4, [29,31) which byte of A's scale words.  The N and M fields
+// sit where they do in the kind::f16 descriptor above.
+__host__ __device__ constexpr uint32_t idesc_mx_f32(int M, int N, int atype, int btype, int sf_a, int sf_b) {
+  return ((uint32_t)sf_b << 4) | ((uint32_t)atype << 7) | ((uint32_t)btype << 10) | ((uint32_t)(N >> 3) << 17) |
+         (1u << 23) | ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_a << 29);
+}
+
+// D[tmem] (+)= (A x scales)[smem] * (B x scales)[smem]^T, one 128 x N x 32 step,
+// issued by one thread; sfa / sfb: tensor-memory addresses of the scale words.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Stores 2 / 4 consecutive 32-bit tensor-memory columns of this warp's lane quarter
+// (one value per column from each thread, thread i -> lane i of the quarter), then
+// waits for the stores to complete.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(a), "r"(b)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(a), "r"(b), "r"(c), "r"(d)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

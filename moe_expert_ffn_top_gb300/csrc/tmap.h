@@ -20,4 +20,14 @@ int tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t
 // in shared memory as b1 rows of b0 bytes.  d0 a multiple of 16, b0 of 16.
 int tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1);
 
+// 2D byte tensor [outer][inner] (E4M3 codes) with the 128-byte swizzle: a box of
+// 128 x box_outer lands as box_outer rows of 128 bytes.
+int tmap_2d_b8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer);
+// E2M1 codes packed two per byte (low nibble first), [d2][d1][d0 codes] (d2 = 1 for
+// a 2D tensor), copied to shared memory one code per byte position as the
+// 16U4_ALIGN16B type does (each 16 codes = 8 bytes, then 8 bytes of gap) with the
+// 128-byte swizzle; box 128 codes x b1 rows.  d0 a multiple of 128, base 32-byte
+// aligned.
+int tmap_fp4_unpacked(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1);
+
 }  // namespace moelora

@@ -7,6 +7,7 @@ from typing import Dict, Iterable, Optional
 import torch
 
 import moe_expert_ffn_top_gb300 as m
+import oracle
 from synth import Shape
 
 ADAPTER_GRADS = ("dA1", "dA3", "dB1", "dB3", "dA2", "dB2")
@@ -40,10 +41,12 @@ def assert_close(name: str, got: torch.Tensor, ref: torch.Tensor) -> None:
 
 
 def dims_of(shp: Shape, scale: Optional[float] = None, mx_once: bool = False) -> m.Dims:
-    """mx_once: an MXFP4 base decoded once per pass (base_fmt 2) instead of inside the GEMMs (1)."""
+    """mx_once: an MXFP4 base decoded once per pass (base_fmt 2) instead of inside the GEMMs (1);
+    base_fmt "mxfp4_native" is the native FP4 forward (3)."""
     mx = 2 if mx_once else 1
+    fmt = {"mxfp4": mx, "mxfp4_native": 3}.get(shp.base_fmt, 0)
     return m.make_dims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, shp.scale if scale is None else scale,
-                       base_fmt=mx if shp.base_fmt == "mxfp4" else 0, act=1 if shp.act == "geglu" else 0,
+                       base_fmt=fmt, act=1 if shp.act == "geglu" else 0,
                        act_clamp=shp.clamp)
 
 
@@ -113,3 +116,50 @@ def sub_problem(inp: Dict[str, torch.Tensor], shp: Shape, tokens: Iterable[int])
     sshp = Shape(T=len(tok), H=shp.H, I=shp.I, E=len(used), k=shp.k, r=shp.r, A=1, scale=shp.scale,
                  base_fmt=shp.base_fmt, act=shp.act, clamp=shp.clamp)
     return sub, sshp, used, tok
+
+
+def _full_check(inp, shp, out, tokens=None):
+    """Compare everything the GPU returned with the oracle (all tokens if None)."""
+    y_ref = oracle.forward(inp, shp, tokens=tokens)
+    g_ref = oracle.backward(inp, shp, tokens=tokens)
+    sel = slice(None) if tokens is None else torch.as_tensor(tokens)
+    assert_close("y", out["y"].cpu()[sel], y_ref)
+    assert_close("dx", out["dx"].cpu()[sel], g_ref["dx"])
+    assert_close("dw", out["dw"].cpu()[sel], g_ref["dw"])
+    for n in ADAPTER_GRADS:
+        assert_close(n, out[n].cpu(), g_ref[n])
+
+
+def _sampled_check(inp, shp, out, sample):
+    """Sparse-dy parity: dy is zero outside `sample`, so every gradient only has
+    contributions from the sampled tokens and the oracle can compute it exactly
+    on that sub-problem; outside the sample dx and dw must be exactly zero."""
+    sub, sshp, used, tok = sub_problem(inp, shp, sample)
+    y_ref = oracle.forward(sub, sshp)
+    g_ref = oracle.backward(sub, sshp)
+    tk = tok.cuda()
+    assert_close("y", out["y"][tk].cpu(), y_ref)
+    assert_close("dx", out["dx"][tk].cpu(), g_ref["dx"])
+    assert_close("dw", out["dw"][tk].cpu(), g_ref["dw"])
+    mask = torch.ones(shp.T, dtype=torch.bool, device="cuda")
+    mask[tk] = False
+    assert out["dx"][mask].abs().max().item() == 0 if mask.any() else True
+    assert out["dw"][mask].abs().max().item() == 0 if mask.any() else True
+    ex = torch.as_tensor(used, device="cuda")
+    for n in ("dA1", "dA3", "dB2"):
+        assert_close(n, out[n].cpu(), g_ref[n])
+    for n in ("dB1", "dB3", "dA2"):
+        assert_close(n, out[n][:, ex].cpu(), g_ref[n])
+        other = torch.ones(shp.E, dtype=torch.bool, device="cuda")
+        other[ex] = False
+        if other.any():
+            assert out[n][:, other].abs().max().item() == 0, n
+
+
+def _sparse_dy(inp, shp, sample):
+    dy = torch.zeros_like(inp["dy"])
+    idx = torch.as_tensor(sample, device=dy.device)
+    dy[idx] = inp["dy"][idx]
+    out = dict(inp)
+    out["dy"] = dy
+    return out

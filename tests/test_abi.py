@@ -64,7 +64,7 @@ def _call_forward(L, d, **over):
     args = dict(plan=FAKE, x=FAKE, w=FAKE, y=FAKE, saved=FAKE, saved_bytes=1 << 40, scratch=FAKE,
                 scratch_bytes=1 << 40)
     args.update(over)
-    W = m.Weights(*([over.get("weight", FAKE)] * 9))
+    W = m.Weights(*([over.get("weight", FAKE)] * 9 + [over.get("scales")] * 3))
     return L.moe_lora_forward(ctypes.byref(d), args["plan"], args["x"], args["w"], ctypes.byref(W), args["y"],
                               args["saved"], args["saved_bytes"], args["scratch"], args["scratch_bytes"], None)
 
@@ -74,7 +74,11 @@ def test_forward_rejections(L):
     assert _call_forward(L, _dims(H=500)) == -2
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 2, 0)) == -5   # unknown activation
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 0, -1.0)) == -2  # negative clamp
-    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 3)) == -5   # unknown base format
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 4)) == -5   # unknown base format
+    assert _call_forward(L, m.Dims(256, 576, 256, 16, 2, 16, 1, 128, 1.0, 0, 3)) == -2   # native: H % 128
+    assert _call_forward(L, m.Dims(256, 512, 320, 16, 2, 16, 1, 128, 1.0, 0, 3)) == -2   # native: I % 128
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 3), weight=FAKE + 16,
+                         scales=FAKE) == -3                                            # native: W1/W3 32 B
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 1)) == -1   # MXFP4 without scales
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 64, 1.0, 0, 0)) == -2    # block_m != 128
     assert _call_forward(L, d, plan=None) == -1
@@ -161,6 +165,26 @@ def test_mxfp4_decode_rejections(L):
     assert L.moe_lora_mxfp4_decode(FAKE + 4, FAKE, FAKE, 64, None) == -3    # packed not 16-byte aligned
     assert L.moe_lora_mxfp4_decode(FAKE, FAKE, FAKE + 2, 64, None) == -3    # out not 16-byte aligned
     assert L.moe_lora_mxfp4_decode(None, None, None, 0, None) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_native_entry_rejections(L):
+    """The MXFP8 quantiser and the block-scaled self-test GEMM reject bad sizes,
+    pointers and layouts on the host."""
+    assert L.moe_lora_mxfp8_quantize(FAKE, 4, 48, FAKE, FAKE, None) == -2      # n not a multiple of 32
+    assert L.moe_lora_mxfp8_quantize(FAKE, -1, 64, FAKE, FAKE, None) == -2
+    assert L.moe_lora_mxfp8_quantize(None, 4, 64, FAKE, FAKE, None) == -1
+    assert L.moe_lora_mxfp8_quantize(FAKE, 4, 64, FAKE, None, None) == -1
+    assert L.moe_lora_mxfp8_quantize(FAKE, 4, 64, FAKE + 8, FAKE, None) == -3
+    assert L.moe_lora_mxfp8_quantize(None, 0, 64, None, None, None) == 0       # no rows: no-op
+    assert L.moe_lora_mxfp8_quantize(FAKE, 4, 64, FAKE, FAKE, None) == -7      # no device
+    ok = (256, 512, 256, FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert L.moe_lora_native_selftest(100, 512, 256, *ok[3:], 0, None) == -2   # M % 128
+    assert L.moe_lora_native_selftest(256, 384, 256, *ok[3:], 0, None) == -2   # N % 256
+    assert L.moe_lora_native_selftest(256, 512, 192, *ok[3:], 0, None) == -2   # K % 128
+    assert L.moe_lora_native_selftest(*ok, 2, None) == -5                     # unknown layout
+    assert L.moe_lora_native_selftest(256, 512, 256, FAKE, FAKE, FAKE + 16, FAKE, FAKE, 0, None) == -3  # Bq 32 B
+    assert L.moe_lora_native_selftest(*ok, 0, None) == -7
 
 
 def test_no_device_is_reported(L):

@@ -15,7 +15,8 @@ import moe_expert_ffn_top_gb300 as m
 import oracle
 from synth import EDGE_TOKEN_COUNTS, Shape, make_inputs, shape
 
-from gpu_common import ADAPTER_GRADS, assert_close, dims_of, rel_l2, run_gpu, sub_problem
+from gpu_common import (ADAPTER_GRADS, _full_check, _sampled_check, _sparse_dy, assert_close, dims_of, rel_l2,
+                        run_gpu, sub_problem)
 
 pytestmark = pytest.mark.gpu
 
@@ -130,18 +131,6 @@ def test_plan_bad_ids_flagged_and_dropped():
 
 
 # ----------------------------------------------------------------------------- full path
-def _full_check(inp, shp, out, tokens=None):
-    """Compare everything the GPU returned with the oracle (all tokens if None)."""
-    y_ref = oracle.forward(inp, shp, tokens=tokens)
-    g_ref = oracle.backward(inp, shp, tokens=tokens)
-    sel = slice(None) if tokens is None else torch.as_tensor(tokens)
-    assert_close("y", out["y"].cpu()[sel], y_ref)
-    assert_close("dx", out["dx"].cpu()[sel], g_ref["dx"])
-    assert_close("dw", out["dw"].cpu()[sel], g_ref["dw"])
-    for n in ADAPTER_GRADS:
-        assert_close(n, out[n].cpu(), g_ref[n])
-
-
 @pytest.mark.parametrize("T,mask", [(256, 0.0), (200, 0.15), (17, 0.0)])
 def test_tiny_forward_backward(T, mask):
     shp = Shape(T=T, H=512, I=256, E=16, k=2, r=16, mask_frac=mask)
@@ -292,41 +281,6 @@ def test_all_routes_masked():
 
 
 # ----------------------------------------------------------------------------- production width
-def _sampled_check(inp, shp, out, sample):
-    """Sparse-dy parity: dy is zero outside `sample`, so every gradient only has
-    contributions from the sampled tokens and the oracle can compute it exactly
-    on that sub-problem; outside the sample dx and dw must be exactly zero."""
-    sub, sshp, used, tok = sub_problem(inp, shp, sample)
-    y_ref = oracle.forward(sub, sshp)
-    g_ref = oracle.backward(sub, sshp)
-    tk = tok.cuda()
-    assert_close("y", out["y"][tk].cpu(), y_ref)
-    assert_close("dx", out["dx"][tk].cpu(), g_ref["dx"])
-    assert_close("dw", out["dw"][tk].cpu(), g_ref["dw"])
-    mask = torch.ones(shp.T, dtype=torch.bool, device="cuda")
-    mask[tk] = False
-    assert out["dx"][mask].abs().max().item() == 0 if mask.any() else True
-    assert out["dw"][mask].abs().max().item() == 0 if mask.any() else True
-    ex = torch.as_tensor(used, device="cuda")
-    for n in ("dA1", "dA3", "dB2"):
-        assert_close(n, out[n].cpu(), g_ref[n])
-    for n in ("dB1", "dB3", "dA2"):
-        assert_close(n, out[n][:, ex].cpu(), g_ref[n])
-        other = torch.ones(shp.E, dtype=torch.bool, device="cuda")
-        other[ex] = False
-        if other.any():
-            assert out[n][:, other].abs().max().item() == 0, n
-
-
-def _sparse_dy(inp, shp, sample):
-    dy = torch.zeros_like(inp["dy"])
-    idx = torch.as_tensor(sample, device=dy.device)
-    dy[idx] = inp["dy"][idx]
-    out = dict(inp)
-    out["dy"] = dy
-    return out
-
-
 @pytest.mark.parametrize("T", EDGE_TOKEN_COUNTS)
 def test_edge_sweep_production_width(T):
     """H=4096, I=2048, E=256, top-6, rank 128, a fifth of the routes masked, experts 0/127/255

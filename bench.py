@@ -279,6 +279,14 @@ def per_kernel_pass(m, fn, steps, only=None):
     return prof
 
 
+def base_fmt_of(shp, mx_once=False):
+    """The library's base_fmt for a synthetic shape: bf16 0, MXFP4 decoded in the
+    GEMMs 1 (or once per pass 2), the native FP4 forward 3."""
+    if shp.base_fmt == "mxfp4":
+        return 2 if mx_once else 1
+    return 3 if shp.base_fmt == "mxfp4_native" else 0
+
+
 def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False):
     """A compact record of one more workload (the same step: plan + forward +
     backward), measured after the headline: step time with its own clock record,
@@ -289,8 +297,7 @@ def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False
     inp = make_inputs(shp, seed=seed, device="cuda")
     T, H, I, E, k, r, A = shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A
     R = int((inp["topk_ids"] >= 0).sum())
-    d = m.make_dims(T, H, I, E, k, r, A, shp.scale,
-                    base_fmt=(2 if mx_once else 1) if shp.base_fmt == "mxfp4" else 0)
+    d = m.make_dims(T, H, I, E, k, r, A, shp.scale, base_fmt=base_fmt_of(shp, mx_once))
     offs = inp["adapter_offsets"].tolist() if A > 1 else None
     ws = m.Workspaces.allocate(d)
     y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
@@ -318,6 +325,9 @@ def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False
     value = job_tflops(world, flops, ms)
     base = shp.base_fmt + ((" decoded once per pass" if mx_once else " decoded in the GEMMs")
                            if shp.base_fmt == "mxfp4" else "")
+    if shp.base_fmt == "mxfp4_native":
+        base = ("mxfp4, gate/up products native (MXFP8 x MXFP4 on block-scaled FP4 tensor cores), "
+                "the rest decoded in the GEMMs")
     rec = {"workload": f"{name}: T={T} H={H} I={I} E={E} top{k} r={r} A={A} s={shp.scale} base={base}",
            "ms_per_step": round(ms, 3), "value": round(value, 2), "unit": "TFLOP/s",
            "pct_of_bf16_peak": round(100 * value / world / pk["bf16"], 2), "live_routes": R,
@@ -325,6 +335,16 @@ def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False
            "kernels_ms": {n: round(t / c, 4) for n, (t, c) in prof.items()},
            "workspace_gb": {w_: round(m.moe_lora_workspace_bytes(d, i_) / 1e9, 3)
                             for w_, i_ in (("plan", 0), ("saved", 1), ("fwd_scratch", 2), ("bwd_scratch", 3))}}
+    if shp.base_fmt == "mxfp4_native" and "w13_lora_swiglu" in prof:
+        t, c = prof["w13_lora_swiglu"]
+        kms = t / c
+        f13 = 4.0 * R * H * I + 4.0 * R * I * r   # gate/up base products + the B1/B3 expand
+        fp8 = 2.0 * pk["bf16"]                    # dense FP8 peak: measured BF16 x the nominal 4.5 / 2.25
+        rec["w13_native"] = {"ms": round(kms, 4), "tflops": round(f13 / kms / 1e9, 1),
+                             "peak_fp8_tflops": round(fp8, 1), "frac_of_fp8_peak": round(f13 / kms / 1e9 / fp8, 4),
+                             "frac_of_bf16_peak": round(f13 / kms / 1e9 / pk["bf16"], 4),
+                             "note": "kind::mxf8f6f4 runs E4M3 x E2M1 at the FP8 rate; the FP8 peak is the "
+                                     "measured BF16 burst x 2 (nominal dense ratio), not measured"}
     if A > 1:
         ms_sa, clk_sa = standalone_time(m, inp, shp, offs, args, stream, local_rank, dist)
         rec["standalone"] = {"ms_per_step": round(ms_sa, 3), "value": round(job_tflops(world, flops, ms_sa), 2),
@@ -421,7 +441,7 @@ def run_ours(args, rank, world, local_rank):
     T, H, I, E, k, r = shp.T, shp.H, shp.I, shp.E, shp.k, shp.r
     R = int((inp["topk_ids"] >= 0).sum())
     A = shp.A
-    d = m.make_dims(T, H, I, E, k, r, A, shp.scale, base_fmt=1 if shp.base_fmt == "mxfp4" else 0)
+    d = m.make_dims(T, H, I, E, k, r, A, shp.scale, base_fmt=base_fmt_of(shp))
     offs = inp["adapter_offsets"].tolist() if A > 1 else None  # token range of each adapter
     ws = m.Workspaces.allocate(d)
     y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
@@ -693,6 +713,7 @@ def run_ours(args, rank, world, local_rank):
     if args.workload == "prod" and world == 1 and not args.no_sub_records:
         subs["mxfp4"] = measure_workload(m, "prod_mxfp4", 3, args, local_rank, dist, world)
         subs["mxfp4_once"] = measure_workload(m, "prod_mxfp4", 3, args, local_rank, dist, world, mx_once=True)
+        subs["native"] = measure_workload(m, "prod_native", 3, args, local_rank, dist, world)
         subs["multi"] = measure_workload(m, "multi", 4, args, local_rank, dist, world)
 
     if rank == 0:
@@ -761,7 +782,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="prod", choices=["prod", "prod_mxfp4", "prod_e16", "prod_e16_mxfp4", "tiny", "edge", "multi"])
+    ap.add_argument("--workload", default="prod", choices=["prod", "prod_mxfp4", "prod_e16", "prod_e16_mxfp4", "prod_native",
+                                                            "prod_e16_native", "tiny", "edge", "multi"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-records", action="store_true",

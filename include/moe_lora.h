@@ -325,8 +325,11 @@ MOE_LORA_API int moe_lora_gemm_starved_selftest(int32_t M, int32_t N, int32_t K,
  * native FP4 forward (base_fmt 3) runs its gate/up base products on:
  *   C[M,N] (fp32) = sum_k (Aq[m,k] 2^(As[m,k/32]-127)) (Bq[n,k] 2^(Bs[n,k/32]-127))
  * Aq [M,K]: E4M3 codes, one per byte.  Bq [N,K/2]: E2M1 codes, two per byte, the low
- * nibble holding the lower k; 32-byte aligned.  As [M,K/32], Bs [N,K/32]: UE8M0
- * scale bytes.  M % 128 == 0, N % 256 == 0, K % 128 == 0.  layout selects how the
+ * nibble holding the lower k; 32-byte aligned.  As, Bs: the UE8M0 scale bytes of A
+ * and B (one per 32 consecutive k of a row) in the tile-major layout
+ * [rows/128][K/128][128][4]: byte j of the word for (row, 128-wide k step) scales
+ * that row's k elements 32j..32j+31 of the step.  M % 128 == 0, N % 256 == 0,
+ * K % 128 == 0.  layout selects how the
  * scale words are placed in tensor memory (0: the layout the MoE path uses; 1: one
  * row per lane, a comparison case that gives a wrong C).  Bad sizes:
  * MOE_LORA_ERR_DIMS; layout out of range: MOE_LORA_ERR_UNSUPPORTED; Bq not 32-byte

@@ -335,7 +335,8 @@ def moe_lora_gemm_starved_selftest(A: torch.Tensor, a_mn: bool, B: torch.Tensor,
 def moe_lora_native_selftest(Aq: torch.Tensor, As: torch.Tensor, Bq: torch.Tensor, Bs: torch.Tensor,
                              C: torch.Tensor, layout: int = 0, stream=None) -> None:
     """Block-scaled FP4 self-test GEMM: C [M,N] fp32 from E4M3 codes Aq [M,K], packed
-    E2M1 codes Bq [N,K/2] and UE8M0 scale bytes As [M,K/32], Bs [N,K/32] (all uint8)."""
+    E2M1 codes Bq [N,K/2] and UE8M0 scale bytes As, Bs in the tile-major layout
+    [rows/128][K/128][128][4] (all uint8)."""
     M, K = Aq.shape
     N = Bq.shape[0]
     rc = lib().moe_lora_native_selftest(M, N, K, _ptr(Aq, torch.uint8, "Aq"), _ptr(As, torch.uint8, "As"),

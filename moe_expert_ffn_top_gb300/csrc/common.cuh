@@ -98,6 +98,7 @@ inline SavedLayout saved_layout(const moe_lora_dims* d) {
 
 struct FwdLayout {
   size_t Y13, Xp, O, Z2, total;   // [T,2r], [P,H], [P,H], [P,r]  (bf16)
+  size_t S13t;                    // native FP4 forward: W1/W3 scale bytes, tile-major (2 x E*I*H/32)
 };
 inline FwdLayout fwd_layout(const moe_lora_dims* d) {
   FwdLayout L;
@@ -108,6 +109,7 @@ inline FwdLayout fwd_layout(const moe_lora_dims* d) {
   L.Xp = take(2 * (size_t)P * d->H);
   L.O = take(2 * (size_t)P * d->H);
   L.Z2 = take(2 * (size_t)P * d->r);
+  L.S13t = take(d->base_fmt == 3 ? 2 * (size_t)d->E * d->I * (d->H / 32) : 0);
   L.total = o;
   return L;
 }

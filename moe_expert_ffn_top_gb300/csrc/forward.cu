@@ -123,6 +123,11 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     return 0;
   };
   if (nat) {
+    // the W1/W3 scale bytes in the tile-major layout the native stages copy (per pass)
+    uint8_t* S1t = reinterpret_cast<uint8_t*>(sc + FL.S13t);
+    uint8_t* S3t = S1t + E * I * (H / 32);
+    LAUNCH(launch_scales_to_tiles(w->S1, (int64_t)(E * I), d->H, S1t, num_sms, stream));
+    LAUNCH(launch_scales_to_tiles(w->S3, (int64_t)(E * I), d->H, S3t, num_sms, stream));
     ProbW13Nv p;
     MAP(tmap_2d_b8(&p.mXq, Xq, H, P, 128));
     MAP(tmap_fp4_unpacked(&p.mW1f, w->W1, H, I, E, 128));
@@ -134,8 +139,8 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     MAP(tmap_2d_store32(&p.mU, Us, I, P));
     MAP(tmap_2d_store32(&p.mAct, Act, I, P));
     p.Xs = Xs;
-    p.S1q = w->S1;
-    p.S3q = w->S3;
+    p.S1t = S1t;
+    p.S3t = S3t;
     p.pl = pl;
     p.err = pl.err;
     p.H = d->H;

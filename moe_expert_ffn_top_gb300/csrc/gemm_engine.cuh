@@ -52,13 +52,16 @@
 // bytes of gap); every row carries one UE8M0 scale per 32 K elements.  Such a copy
 // counts its PACKED bytes on the stage barrier (64 per row of 128 codes), not the
 // bytes it writes to shared memory (measured: expecting the latter never completes).  The epilogue
-// warps walk the K steps like decoders: for a native step they write the stage's scale
-// words into tensor memory and arrive on the stage's decoded barrier, which the MMA
-// waits on; it then issues four kind::mxf8f6f4 MMAs of K = 32 (scale byte kk of each
-// word for step kk).  Other K steps of such a problem are ordinary BF16 steps.
+// warps walk the K steps like decoders: for a native step they copy the stage's scale
+// words (which the producer brought into the stage's last kNvSfBytes with the
+// operands) into tensor memory and arrive on the stage's decoded barrier, which the
+// MMA waits on; it then issues four kind::mxf8f6f4 MMAs of K = 32 (scale byte kk of
+// each word for step kk).  Other K steps of such a problem are ordinary BF16 steps.
+// Three stages of 50 KB (A 16 KB, B 32 KB, scale words 1.5 KB).
 //   static constexpr bool kNative;
 //   bool     native_step(const TileInfo&, int ks) const;
-//   NvScales nv_scales(const TileInfo&, int ks) const;   where the step's scale words are
+//   and load() copies the step's scale words to sA + kNvSfOff: 128 words of A rows
+//   0..127, then 256 words of B rows 0..255 (one word = the step's 4 scale bytes)
 //
 // Operand tiles in shared memory use the 128-byte swizzle written by TMA:
 //   A K-major : 128 rows x 128 B                         (one 16 KB box)
@@ -99,12 +102,15 @@ struct NativeOf<P, std::void_t<decltype(P::kNative)>> : std::integral_constant<b
 // MMAs sharing each B tile, 3 stages of (A 32 KB + B 32 KB), one accumulator pair
 // using all 512 TMEM columns -- a third fewer operand bytes per FLOP streamed into
 // the SM, at the price of an epilogue that no longer overlaps the main loop.
+constexpr int kNvSfOff = 128 * 128 + kBStageBytes;  // scale words of a native stage
+constexpr int kNvSfBytes = 384 * 4;
 template <class P>
 struct EngineShape {
   static constexpr bool kWide = P::kWide;
+  static constexpr bool kNat = NativeOf<P>::value;
   static constexpr int kAStage = kWide ? 2 * 128 * 128 : 128 * 128;
-  static constexpr int kStage = kAStage + kBStageBytes;
-  static constexpr int kStages = kWide ? 3 : 4;
+  static constexpr int kStage = kNat ? 50 * 1024 : kAStage + kBStageBytes;
+  static constexpr int kStages = kWide || kNat ? 3 : 4;
   static constexpr int kAccBufs = kWide || NativeOf<P>::value ? 1 : 2;
   static_assert(kStages * kStage <= 192 * 1024, "pipeline exceeds shared memory budget");
 };
@@ -251,47 +257,37 @@ __device__ __forceinline__ bool mx_decode_stage(uint8_t* sb, int dt, const uint3
 
 // ------------------------------------------------------------------ block-scaled FP4
 // Scale words of a native K step: 4 UE8M0 bytes (the step's four 32-element blocks,
-// byte j for K elements 32j..32j+31) per operand row, row i of the A tile at
-// a + i * as, row i of the B tile at b[i >> 7] + (i & 127) * bs (4-byte aligned).
-struct NvScales {
-  const uint8_t* a;
-  const uint8_t* b[2];
-  int64_t as, bs;
-};
+// byte j for K elements 32j..32j+31) per operand row; in shared memory word i is A
+// row i (i < 128), word 128 + i is B row i.
 constexpr int kNvSfCols = 12;  // per stage: A 4 columns, then B 8 columns
 // Layout of the scale words in tensor memory.  kNvLayoutGroups (the one the MMAs use):
 // the words of operand row i sit in column i / 32 of that operand's block at lane i % 32
 // of every lane quarter (each quarter holds all rows).  kNvLayoutRows (self-test
 // comparison only): row i at lane i % 128 of column i / 128.
 constexpr int kNvLayoutGroups = 0, kNvLayoutRows = 1;
-__device__ __forceinline__ uint32_t ldg_issue_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
 // The six words this thread (lane of a quarter; half 0 / 1 = the first / second warp
-// of that quarter) stores for one step.  kNvLayoutGroups: half 0 takes A columns 0..3
-// and B columns 0..1, half 1 B columns 2..7 (A/B row 32c + lane for column c).
+// of that quarter) stores for one step, from the stage's words sw.  kNvLayoutGroups:
+// half 0 takes A columns 0..3 and B columns 0..1, half 1 B columns 2..7 (A/B row
+// 32c + lane for column c); consecutive lanes read consecutive words.
 template <int L>
-__device__ __forceinline__ void nv_load_scales(const NvScales& sc, int q, int half, int lane, uint32_t (&w)[6]) {
+__device__ __forceinline__ void nv_load_scales(const uint32_t* sw, int q, int half, int lane, uint32_t (&w)[6]) {
+  const uint32_t* sa = sw;
+  const uint32_t* sb = sw + 128;
   if (L == kNvLayoutGroups) {
     if (half == 0) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = ldg_issue_u32(sc.a + (32 * c + lane) * sc.as);
+      for (int c = 0; c < 4; ++c) w[c] = sa[32 * c + lane];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) w[4 + c] = ldg_issue_u32(sc.b[0] + (32 * c + lane) * sc.bs);
+      for (int c = 0; c < 2; ++c) w[4 + c] = sb[32 * c + lane];
     } else {
 #pragma unroll
-      for (int c = 2; c < 8; ++c) {
-        const int row = 32 * c + lane;
-        w[c - 2] = ldg_issue_u32(sc.b[row >> 7] + (row & 127) * sc.bs);
-      }
+      for (int c = 2; c < 8; ++c) w[c - 2] = sb[32 * c + lane];
     }
   } else {
     const int row = 32 * q + lane;
-    w[0] = ldg_issue_u32(sc.a + row * sc.as);
-    w[1] = ldg_issue_u32(sc.b[0] + row * sc.bs);
-    w[2] = ldg_issue_u32(sc.b[1] + row * sc.bs);
+    w[0] = sa[row];
+    w[1] = sb[row];
+    w[2] = sb[128 + row];
     w[3] = w[4] = w[5] = 0;
   }
 }
@@ -527,7 +523,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
       // epilogue_empty.
       constexpr bool kNat = NativeOf<P>::value;
       constexpr int kNvL = NvLayoutOf<P>::value;
-      constexpr int kPre = kNat ? 6 : 2;  // words loaded one step ahead per thread
+      constexpr int kPre = 2;  // decoders: scale bytes loaded one step ahead per thread
       constexpr int NT = 32 * P::kEpiWarps;
       const int dt = threadIdx.x - 64;  // decoder thread 0..NT-1
       int t = blockIdx.x, ks = 0;
@@ -558,10 +554,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           return p.decodes(ti, ks);
       };
       auto load_pre = [&](uint32_t (&w)[kPre]) {
-        if constexpr (kNat)
-          nv_load_scales<kNvL>(p.nv_scales(ti, ks), q, half, lane, w);
-        else
-          mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, w);
+        if constexpr (!kNat) mx_load_scales<P::kMxMN>(p.mx_scales(ti, ks), dt, w);
       };
       int s = 0;
       uint32_t ph = 0;
@@ -590,7 +583,11 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           // Each warp writes its own lane quarter: no barrier between the warps, and a
           // warp whose wait gave up simply leaves (the MMA's wait then gives up too).
           if (!got) break;
-          if (cdec) nv_store_scales<kNvL>(tmem_base + (uint32_t)(kAccCols + s * kNvSfCols), q, half, sc);
+          if (cdec) {
+            uint32_t w[6];
+            nv_load_scales<kNvL>(reinterpret_cast<const uint32_t*>(smem + s * S::kStage + kNvSfOff), q, half, lane, w);
+            nv_store_scales<kNvL>(tmem_base + (uint32_t)(kAccCols + s * kNvSfCols), q, half, w);
+          }
           tc_fence_before();
         } else {
           // Steps that decode agree inside mx_decode_stage; the others here.  Either

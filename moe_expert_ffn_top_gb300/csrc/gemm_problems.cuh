@@ -529,7 +529,7 @@ struct ProbW13Nv {
   static constexpr bool kAmn = false, kBmn = false, kWide = false, kNative = true;
   static constexpr int kEpiWarps = 8;
   const uint8_t* Xs;          // [P/128][H/128][128][4] scale bytes of Xq
-  const uint8_t *S1q, *S3q;   // [E,I,H/32] scale bytes of W1/W3
+  const uint8_t *S1t, *S3t;   // [E*I/128][H/128][128][4] scale bytes of W1/W3 (launch_scales_to_tiles)
   CUtensorMap mXq;            // Xq (H,P) bytes, box (128,128)
   CUtensorMap mW1f, mW3f;     // W1/W3 E2M1 (H,I,E), box (128 codes, 128, 1)
   CUtensorMap mY13p, mB1, mB3;  // as ProbW13
@@ -561,10 +561,15 @@ struct ProbW13Nv {
     const int nb = H / 128;
     if (ks < nb) {
       const int e = ti.g % pl.E;
-      mbar_arrive_expect_tx(bar, 128 * 128 + 2 * 128 * 64);  // E2M1 boxes count packed bytes
+      const int64_t kt = H / 128;
+      const int64_t wt = ((int64_t)e * (I / 128) + (ti.n0 >> 7)) * kt + ks;  // weight row tile, K step
+      mbar_arrive_expect_tx(bar, 128 * 128 + 2 * 128 * 64 + kNvSfBytes);  // E2M1 boxes count packed bytes
       tma_load_2d(sa, &mXq, bar, ks * 128, ti.m0);
       tma_load_3d(sb, &mW1f, bar, ks * 128, ti.n0, e);
       tma_load_3d(sb + 128 * 128, &mW3f, bar, ks * 128, ti.n0, e);
+      bulk_load(sa + kNvSfOff, Xs + ((int64_t)(ti.m0 >> 7) * kt + ks) * 512, 512, bar);
+      bulk_load(sa + kNvSfOff + 512, S1t + wt * 512, 512, bar);
+      bulk_load(sa + kNvSfOff + 1024, S3t + wt * 512, 512, bar);
     } else {
       const int j = ks - nb, half = j / nkr(), kb = j % nkr();
       mbar_arrive_expect_tx(bar, kAStage128 + 128 * 128);
@@ -573,11 +578,6 @@ struct ProbW13Nv {
     }
   }
   __device__ bool native_step(const TileInfo&, int ks) const { return ks < H / 128; }
-  __device__ NvScales nv_scales(const TileInfo& ti, int ks) const {
-    const int64_t rs = H / 32;
-    const int64_t wo = ((int64_t)(ti.g % pl.E) * I + ti.n0) * rs + ks * 4;
-    return NvScales{Xs + ((int64_t)(ti.m0 >> 7) * (H / 128) + ks) * 512, {S1q + wo, S3q + wo}, 4, rs};
-  }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const {
     const int nb = H / 128;
     if (ks < nb) return MmaStep{256, 0, 0, ks == 0};
@@ -1480,9 +1480,10 @@ struct ProbPlain {
 
 // Block-scaled plain GEMM (self-test of the native FP4 path):
 //   C[M,N] = (Aq x 2^(As-127)) (Bq x 2^(Bs-127))^T   in fp32
-// with Aq [M,K] E4M3 codes, As [M,K/32] and Bs [N,K/32] UE8M0 bytes (one per 32 K
-// elements), Bq [N,K/2] packed E2M1 codes (low nibble = lower K).  M % 128 == 0,
-// N % 256 == 0, K % 128 == 0.  L: layout of the scale words in tensor memory.
+// with Aq [M,K] E4M3 codes, Bq [N,K/2] packed E2M1 codes (low nibble = lower K), and
+// As, Bs the UE8M0 bytes (one per 32 K elements) in the tile-major layout
+// [rows/128][K/128][128 rows][4].  M % 128 == 0, N % 256 == 0, K % 128 == 0.
+// L: layout of the scale words in tensor memory.
 template <int L>
 struct ProbPlainNv {
   static constexpr bool kAmn = false, kBmn = false, kWide = false, kNative = true;
@@ -1512,16 +1513,15 @@ struct ProbPlainNv {
     tma_prefetch_map(&mB);
   }
   __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
-    mbar_arrive_expect_tx(bar, 128 * 128 + 256 * 64);  // E2M1 boxes count packed bytes
+    mbar_arrive_expect_tx(bar, 128 * 128 + 256 * 64 + kNvSfBytes);  // E2M1 boxes count packed bytes
     tma_load_2d(sa, &mA, bar, ks * 128, ti.m0);
     tma_load_3d(sb, &mB, bar, ks * 128, ti.n0, 0);
+    const int64_t kt = K / 128;
+    bulk_load(sa + kNvSfOff, As + ((int64_t)(ti.m0 >> 7) * kt + ks) * 512, 512, bar);
+    bulk_load(sa + kNvSfOff + 512, Bs + ((int64_t)(ti.n0 >> 7) * kt + ks) * 512, 512, bar);
+    bulk_load(sa + kNvSfOff + 1024, Bs + ((int64_t)((ti.n0 >> 7) + 1) * kt + ks) * 512, 512, bar);
   }
   __device__ bool native_step(const TileInfo&, int) const { return true; }
-  __device__ NvScales nv_scales(const TileInfo& ti, int ks) const {
-    const int64_t rs = K / 32;
-    const uint8_t* b = Bs + ti.n0 * rs + ks * 4;
-    return NvScales{As + ti.m0 * rs + ks * 4, {b, b + 128 * rs}, rs, rs};
-  }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
     float* o0 = C + ((int64_t)ti.m0 + row - (threadIdx.x & 31)) * N + ti.n0;  // warp's first row

@@ -185,6 +185,20 @@ __global__ void gather_fwd_mxfp8_kernel(PlanView pl, const uint16_t* __restrict_
   }
 }
 
+// Scale bytes [rows, K/32] (row-major, one per 32 K elements) to the tile-major layout
+// [rows/128][K/128][128][4]: the 4 bytes of one 128-wide K step of a row become one
+// word, and the 128 words of a row tile for one K step 512 contiguous bytes (what a
+// native GEMM stage copies).  rows % 128 == 0, K % 128 == 0.
+__global__ void scales_to_tiles_kernel(const uint8_t* __restrict__ S, int64_t rows, int kt,
+                                       uint8_t* __restrict__ St) {
+  const int64_t n = rows * kt;  // words
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < n; w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = w & 127, j = (w >> 7) % kt, rt = (w >> 7) / kt;  // row in tile, K step, row tile
+    const int64_t row = rt * 128 + i;
+    *reinterpret_cast<uint32_t*>(St + w * 4) = __ldg(reinterpret_cast<const uint32_t*>(S + row * kt * 4 + j * 4));
+  }
+}
+
 // The same MXFP8 quantisation on its own: one warp per row of x [rows, n], one
 // 32-element block per lane, codes [rows, n] and scale bytes [rows, n/32] row-major.
 __global__ void quant_mxfp8_kernel(const uint16_t* __restrict__ x, int64_t rows, int n, uint8_t* __restrict__ codes,
@@ -513,6 +527,12 @@ cudaError_t launch_gather_fwd_mxfp8(const PlanView& pl, const uint16_t* x, const
   prof_begin(K_GATHER_FWD, stream);
   gather_fwd_mxfp8_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, x, Y13, Xq, Xs, Y13p, H, r2);
   prof_end(K_GATHER_FWD, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scales_to_tiles(const uint8_t* S, int64_t rows, int K, uint8_t* St, int num_sms,
+                                   cudaStream_t stream) {
+  scales_to_tiles_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(S, rows, K / 128, St);
   return cudaGetLastError();
 }
 

@@ -38,6 +38,12 @@ def _tables():
     return e4, e2
 
 
+def _tiles(sc):
+    """Scale bytes [rows, K/32] -> the tile-major layout [rows/128][K/128][128][4]."""
+    rows, nb = sc.shape
+    return sc.view(rows // 128, 128, nb // 4, 4).permute(0, 2, 1, 3).contiguous()
+
+
 def _native_operands(M, N, K, seed, lo=118, hi=136):
     g = torch.Generator().manual_seed(seed)
     aq = (torch.randint(0, 127, (M, K), generator=g) | (torch.randint(0, 2, (M, K), generator=g) << 7)).to(torch.uint8)
@@ -57,7 +63,7 @@ def test_native_engine_gemm(M, N, K):
     sides, scale words in tensor memory) against float64."""
     aq, asc, bq, bsc, ref = _native_operands(M, N, K, seed=M + N + K)
     C = torch.full((M, N), float("nan"), device="cuda")
-    m.moe_lora_native_selftest(aq.cuda(), asc.cuda(), bq.cuda(), bsc.cuda(), C)
+    m.moe_lora_native_selftest(aq.cuda(), _tiles(asc).cuda(), bq.cuda(), _tiles(bsc).cuda(), C)
     torch.cuda.synchronize()
     assert m.moe_lora_gemm_selftest_error() == 0
     assert rel_l2(C, ref) < 1e-6
@@ -68,7 +74,7 @@ def test_native_engine_scale_placement_matters():
     placement gives a different, wrong product on the same operands."""
     aq, asc, bq, bsc, ref = _native_operands(256, 512, 256, seed=5)
     C = torch.full((256, 512), float("nan"), device="cuda")
-    m.moe_lora_native_selftest(aq.cuda(), asc.cuda(), bq.cuda(), bsc.cuda(), C, layout=1)
+    m.moe_lora_native_selftest(aq.cuda(), _tiles(asc).cuda(), bq.cuda(), _tiles(bsc).cuda(), C, layout=1)
     torch.cuda.synchronize()
     assert m.moe_lora_gemm_selftest_error() == 0
     assert rel_l2(C, ref) > 1e-2

@@ -281,10 +281,12 @@ def per_kernel_pass(m, fn, steps, only=None):
 
 def base_fmt_of(shp, mx_once=False):
     """The library's base_fmt for a synthetic shape: bf16 0, MXFP4 decoded in the
-    GEMMs 1 (or once per pass 2), the native FP4 forward 3."""
+    GEMMs 1 (or once per pass 2), the native FP4 forward with the rest as 1 (3) or as 2 (4)."""
     if shp.base_fmt == "mxfp4":
         return 2 if mx_once else 1
-    return 3 if shp.base_fmt == "mxfp4_native" else 0
+    if shp.base_fmt == "mxfp4_native":
+        return 4 if mx_once else 3
+    return 0
 
 
 def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False):
@@ -327,7 +329,7 @@ def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False
                            if shp.base_fmt == "mxfp4" else "")
     if shp.base_fmt == "mxfp4_native":
         base = ("mxfp4, gate/up products native (MXFP8 x MXFP4 on block-scaled FP4 tensor cores), "
-                "the rest decoded in the GEMMs")
+                "the rest decoded " + ("once per pass" if mx_once else "in the GEMMs"))
     rec = {"workload": f"{name}: T={T} H={H} I={I} E={E} top{k} r={r} A={A} s={shp.scale} base={base}",
            "ms_per_step": round(ms, 3), "value": round(value, 2), "unit": "TFLOP/s",
            "pct_of_bf16_peak": round(100 * value / world / pk["bf16"], 2), "live_routes": R,
@@ -714,6 +716,7 @@ def run_ours(args, rank, world, local_rank):
         subs["mxfp4"] = measure_workload(m, "prod_mxfp4", 3, args, local_rank, dist, world)
         subs["mxfp4_once"] = measure_workload(m, "prod_mxfp4", 3, args, local_rank, dist, world, mx_once=True)
         subs["native"] = measure_workload(m, "prod_native", 3, args, local_rank, dist, world)
+        subs["native_once"] = measure_workload(m, "prod_native", 3, args, local_rank, dist, world, mx_once=True)
         subs["multi"] = measure_workload(m, "multi", 4, args, local_rank, dist, world)
 
     if rank == 0:

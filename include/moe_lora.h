@@ -86,7 +86,14 @@ extern "C" {
  * the base occupies only its packed bytes and scales (no bf16 copy anywhere);
  * 2: once per forward into the saved workspace (3 * E*I*H bf16 more), which the
  * backward reuses -- faster on GB300 today, since the in-GEMM decode is repeated
- * by every row tile of an expert.
+ * by every row tile of an expert.  base_fmt 3 or 4: the native FP4 forward -- the
+ * gate/up base products run on block-scaled FP4 tensor cores (tcgen05 kind::mxf8f6f4)
+ * with the routed rows of x quantised to MXFP8 (E4M3 codes, one UE8M0 scale per 32
+ * along H; the rule of moe_lora_mxfp8_quantize) and the MXFP4 W1/W3 as stored, so
+ * their results carry that quantisation ("FP8/FP4/FP8 forwards", PR #9, Fresh
+ * validation); the side paths, the W2 forward and the backward (straight through
+ * the quantisation) run as base_fmt 1 (3) or 2 (4).  H and I must be multiples of
+ * 128 and W1/W3 32-byte aligned.
  * T may be 0 (every call is a no-op). */
 typedef struct moe_lora_dims {
   int64_t T;        /* tokens */
@@ -99,18 +106,20 @@ typedef struct moe_lora_dims {
   int32_t block_m;  /* plan padding unit, 128 */
   float scale;      /* side-LoRA scale s */
   int32_t act;      /* 0 = SwiGLU, 1 = GeGLU */
-  int32_t base_fmt; /* 0 = bf16, 1 = MXFP4 decoded in the GEMMs, 2 = MXFP4 decoded once */
+  int32_t base_fmt; /* 0 = bf16, 1 = MXFP4 decoded in the GEMMs, 2 = MXFP4 decoded once,
+                       3 / 4 = native FP4 forward, the rest as 1 / 2 */
   float act_clamp;  /* activation clamp (0 = none) */
 } moe_lora_dims;
 
 /* Frozen base and adapter weights (device).
- *   W1, W3 [E,I,H]; W2 [E,H,I]: bf16 bits when base_fmt = 0.  When base_fmt = 1 or 2
+ *   W1, W3 [E,I,H]; W2 [E,H,I]: bf16 bits when base_fmt = 0.  When base_fmt = 1..4
  *     (MXFP4) they hold E2M1 element codes, two per byte (low nibble = lower index
  *     along the last axis), and S1, S3 [E,I,H/32], S2 [E,H,I/32] hold one UE8M0
  *     scale byte (value 2^(b-127); 255 decodes to NaN) per 32 consecutive elements
  *     of that axis: the OCP MX encoding, read from the pages' "E2M1 values with a
- *     UE8M0 scale per 32 elements" (base_fmt 1 or 2).  The base is decoded exactly
- *     to bf16 and the BF16 tensor-core path runs on it; the adapters stay bf16.
+ *     UE8M0 scale per 32 elements".  The base is decoded exactly to bf16 and the
+ *     BF16 tensor-core path runs on it (except the native gate/up products of
+ *     base_fmt 3 and 4, which read it as stored); the adapters stay bf16.
  *     S1/S3/S2 are ignored (may be NULL) when base_fmt = 0.
  *   A1, A3 [A,r,H] (shared by experts); B1, B3 [A,E,I,r] (expert-local);
  *   A2 [A,E,r,I] (expert-local); B2 [A,H,r] (shared), bf16 bits. */
@@ -327,11 +336,13 @@ MOE_LORA_API int moe_lora_gemm_starved_selftest(int32_t M, int32_t N, int32_t K,
  * Aq [M,K]: E4M3 codes, one per byte.  Bq [N,K/2]: E2M1 codes, two per byte, the low
  * nibble holding the lower k; 32-byte aligned.  As, Bs: the UE8M0 scale bytes of A
  * and B (one per 32 consecutive k of a row) in the tile-major layout
- * [rows/128][K/128][128][4]: byte j of the word for (row, 128-wide k step) scales
- * that row's k elements 32j..32j+31 of the step.  M % 128 == 0, N % 256 == 0,
- * K % 128 == 0.  layout selects how the
- * scale words are placed in tensor memory (0: the layout the MoE path uses; 1: one
- * row per lane, a comparison case that gives a wrong C).  Bad sizes:
+ * [rows/128][K/128][32][4][4]: one 4-byte word per (row, 128-wide k step), byte j
+ * scaling that row's k elements 32j..32j+31 of the step, and the 128 words of a row
+ * block for one k step 512 bytes with row i's word at position 4 (i % 32) + i / 32.
+ * M % 128 == 0, N % 256 == 0, K % 128 == 0.  layout selects how the scale words
+ * reach tensor memory: 0, written by the epilogue warps (tcgen05.st) in the layout
+ * the MMA reads; 2, the same layout copied by the MMA-issuing thread (tcgen05.cp);
+ * 1, one row per lane, a comparison case that gives a wrong C.  Bad sizes:
  * MOE_LORA_ERR_DIMS; layout out of range: MOE_LORA_ERR_UNSUPPORTED; Bq not 32-byte
  * aligned: MOE_LORA_ERR_ALIGN.  Device-side wait timeouts are reported through
  * moe_lora_gemm_selftest_error().  Not part of the MoE method. */

@@ -122,9 +122,9 @@ def lib() -> ctypes.CDLL:
 def make_dims(T: int, H: int, I: int, E: int, k: int, r: int, A: int = 1, scale: float = 1.0,
               base_fmt: int = 0, act: int = 0, act_clamp: float = 0.0) -> Dims:
     """base_fmt: 0 = bf16 base weights; MXFP4 (packed E2M1 codes + UE8M0 scales S1/S3/S2) decoded
-    inside the GEMMs (1) or once per pass into the saved workspace (2); 3 = the native FP4
+    inside the GEMMs (1) or once per pass into the saved workspace (2); 3 / 4 = the native FP4
     forward (gate/up base products on block-scaled FP4 tensor cores from MXFP8 activations,
-    the rest as 1; H and I multiples of 128);
+    the rest as 1 / as 2; H and I multiples of 128);
     act: 0 = SwiGLU, 1 = GeGLU; act_clamp: clamp of the gate/up pre-activations (0 = none)."""
     return Dims(T, H, I, E, k, r, A, 128, float(scale), int(act), int(base_fmt), float(act_clamp))
 
@@ -205,7 +205,7 @@ def moe_lora_plan_readback(dims: Dims, plan_ws: torch.Tensor, stream=None) -> Di
 
 
 def _weights(w: Dict[str, torch.Tensor], dims: Dims) -> Weights:
-    mx = dims.base_fmt in (1, 2, 3)
+    mx = dims.base_fmt in (1, 2, 3, 4)
     base = [_ptr(w[n], torch.uint8 if mx else torch.bfloat16, n) for n in ("W1", "W3", "W2")]
     side = [_ptr(w[n], torch.bfloat16, n) for n in ("A1", "A3", "B1", "B3", "A2", "B2")]
     scales = [_ptr(w[n], torch.uint8, n) if mx else None for n in ("S1", "S3", "S2")]

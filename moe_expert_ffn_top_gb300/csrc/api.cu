@@ -117,7 +117,7 @@ static int check_weights(const moe_lora_dims* d, const moe_lora_weights* w) {
     const int rc = check_ptr(p);
     if (rc) return rc;
   }
-  if (d->base_fmt >= 1) {
+  if (fmt_mx(d)) {
     const void* sc[] = {w->S1, w->S3, w->S2};
     for (const void* p : sc) {
       const int rc = check_ptr(p);
@@ -125,7 +125,7 @@ static int check_weights(const moe_lora_dims* d, const moe_lora_weights* w) {
     }
   }
   // the native forward's FP4 tensor maps read W1/W3 with 32-byte alignment
-  if (d->base_fmt == 3 && ((reinterpret_cast<uintptr_t>(w->W1) | reinterpret_cast<uintptr_t>(w->W3)) & 31u))
+  if (fmt_native(d) && ((reinterpret_cast<uintptr_t>(w->W1) | reinterpret_cast<uintptr_t>(w->W3)) & 31u))
     return MOE_LORA_ERR_ALIGN;
   return MOE_LORA_OK;
 }
@@ -370,7 +370,7 @@ extern "C" int moe_lora_native_selftest(int32_t M, int32_t N, int32_t K, const u
                                         const uint8_t* Bq, const uint8_t* Bs, float* C, int32_t layout,
                                         void* stream) {
   if (M <= 0 || M % 128 || N <= 0 || N % 256 || K <= 0 || K % 128) return MOE_LORA_ERR_DIMS;
-  if (layout != 0 && layout != 1) return MOE_LORA_ERR_UNSUPPORTED;
+  if (layout < 0 || layout > 2) return MOE_LORA_ERR_UNSUPPORTED;
   int rc;
   if ((rc = check_ptr(Aq)) || (rc = check_ptr(As)) || (rc = check_ptr(Bq)) || (rc = check_ptr(Bs)) ||
       (rc = check_ptr(C)))

@@ -60,10 +60,10 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   // An MXFP4 base: decoded inside the two dgrad GEMMs, stage by stage (base_fmt 1,
   // the ...T<true> problem types), or the bf16 copy the forward decoded into `saved`
   // (base_fmt 2).
-  const bool mx = d->base_fmt == 1 || d->base_fmt == 3;
-  const void* bW1 = d->base_fmt == 2 ? (const void*)(sv + SL.W1) : w->W1;
-  const void* bW3 = d->base_fmt == 2 ? (const void*)(sv + SL.W3) : w->W3;
-  const void* bW2 = d->base_fmt == 2 ? (const void*)(sv + SL.W2) : w->W2;
+  const bool mx = fmt_in_gemm(d);
+  const void* bW1 = fmt_once(d) ? (const void*)(sv + SL.W1) : w->W1;
+  const void* bW3 = fmt_once(d) ? (const void*)(sv + SL.W3) : w->W3;
+  const void* bW2 = fmt_once(d) ? (const void*)(sv + SL.W2) : w->W2;
 #define MAP(call)                                 \
   do {                                            \
     if ((call) != 0) return MOE_LORA_ERR_CUDA;    \

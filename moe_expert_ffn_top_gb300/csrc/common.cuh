@@ -18,15 +18,22 @@ constexpr int kMaxSplit = 8;       // token-range slices of the long-K reduction
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Base formats: 0 bf16; MXFP4 decoded inside the expert GEMMs (1) or once per pass
+// into the saved workspace (2); the native FP4 forward with the rest as 1 (3) or as 2 (4).
+inline bool fmt_mx(const moe_lora_dims* d) { return d->base_fmt >= 1; }
+inline bool fmt_in_gemm(const moe_lora_dims* d) { return d->base_fmt == 1 || d->base_fmt == 3; }
+inline bool fmt_once(const moe_lora_dims* d) { return d->base_fmt == 2 || d->base_fmt == 4; }
+inline bool fmt_native(const moe_lora_dims* d) { return d->base_fmt >= 3; }
+
 // Returns MOE_LORA_OK when the sizes are supported.
 inline int check_dims(const moe_lora_dims* d) {
   if (!d) return MOE_LORA_ERR_NULL;
-  if ((d->act != 0 && d->act != 1) || d->base_fmt < 0 || d->base_fmt > 3) return MOE_LORA_ERR_UNSUPPORTED;
+  if ((d->act != 0 && d->act != 1) || d->base_fmt < 0 || d->base_fmt > 4) return MOE_LORA_ERR_UNSUPPORTED;
   if (!(d->act_clamp >= 0.0f) || d->act_clamp > 3.0e38f) return MOE_LORA_ERR_DIMS;
   if (d->T < 0 || d->T > (int64_t)1 << 30) return MOE_LORA_ERR_DIMS;
   if (d->H < 64 || d->H % 64 || d->I < 64 || d->I % 64) return MOE_LORA_ERR_DIMS;
   // native FP4 forward: whole 128-wide K steps and 128-column tiles
-  if (d->base_fmt == 3 && (d->H % 128 || d->I % 128)) return MOE_LORA_ERR_DIMS;
+  if (fmt_native(d) && (d->H % 128 || d->I % 128)) return MOE_LORA_ERR_DIMS;
   if (d->r < 8 || d->r > 128 || d->r % 8) return MOE_LORA_ERR_DIMS;
   if (d->k < 1 || d->k > 32 || d->E < 1 || d->A < 1 || d->A > kMaxAdapters) return MOE_LORA_ERR_DIMS;
   if ((int64_t)d->A * d->E > kMaxGroups) return MOE_LORA_ERR_DIMS;
@@ -88,7 +95,7 @@ inline SavedLayout saved_layout(const moe_lora_dims* d) {
   L.U = take(2 * (size_t)P * d->I);
   L.Act = take(2 * (size_t)P * d->I);
   L.Z2w = take(2 * (size_t)T * d->r);
-  const size_t wbytes = d->base_fmt == 2 ? 2 * (size_t)d->E * d->I * d->H : 0;
+  const size_t wbytes = fmt_once(d) ? 2 * (size_t)d->E * d->I * d->H : 0;
   L.W1 = take(wbytes);
   L.W3 = take(wbytes);
   L.W2 = take(wbytes);
@@ -109,7 +116,7 @@ inline FwdLayout fwd_layout(const moe_lora_dims* d) {
   L.Xp = take(2 * (size_t)P * d->H);
   L.O = take(2 * (size_t)P * d->H);
   L.Z2 = take(2 * (size_t)P * d->r);
-  L.S13t = take(d->base_fmt == 3 ? 2 * (size_t)d->E * d->I * (d->H / 32) : 0);
+  L.S13t = take(fmt_native(d) ? 2 * (size_t)d->E * d->I * (d->H / 32) : 0);
   L.total = o;
   return L;
 }

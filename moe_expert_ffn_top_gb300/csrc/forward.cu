@@ -41,13 +41,14 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   // copy exists anywhere; base_fmt 2 decodes it once per pass into `saved` (which the
   // backward reuses) and runs the bf16 GEMMs on that copy.  base_fmt 3 (native FP4
   // forward) runs the gate/up base products on block-scaled FP4 tensor cores from
-  // MXFP8 routed rows (ProbW13Nv) and the rest as base_fmt 1.
-  const bool nat = d->base_fmt == 3;
-  const bool mx = d->base_fmt == 1 || nat;
+  // MXFP8 routed rows (ProbW13Nv) and the rest as base_fmt 1; base_fmt 4 the same
+  // with the rest as base_fmt 2.
+  const bool nat = fmt_native(d);
+  const bool mx = fmt_in_gemm(d);
   const void* bW1 = w->W1;
   const void* bW3 = w->W3;
   const void* bW2 = w->W2;
-  if (d->base_fmt == 2) {
+  if (fmt_once(d)) {
     uint16_t* q1 = (uint16_t*)(sv + SL.W1);
     uint16_t* q3 = (uint16_t*)(sv + SL.W3);
     uint16_t* q2 = (uint16_t*)(sv + SL.W2);
@@ -135,9 +136,9 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     MAP(tmap_2d(&p.mY13p, Y13p, 2 * r, P, 64, 128));
     MAP(tmap_3d(&p.mB1, w->B1, r, I, G, 64, 128));
     MAP(tmap_3d(&p.mB3, w->B3, r, I, G, 64, 128));
-    MAP(tmap_2d_store32(&p.mG, Gs, I, P));
-    MAP(tmap_2d_store32(&p.mU, Us, I, P));
-    MAP(tmap_2d_store32(&p.mAct, Act, I, P));
+    p.G = Gs;
+    p.U = Us;
+    p.Act = Act;
     p.Xs = Xs;
     p.S1t = S1t;
     p.S3t = S3t;

@@ -51,17 +51,20 @@
 // byte position as TMA's 16U4_ALIGN16B type writes them (16 codes in 8 bytes, then 8
 // bytes of gap); every row carries one UE8M0 scale per 32 K elements.  Such a copy
 // counts its PACKED bytes on the stage barrier (64 per row of 128 codes), not the
-// bytes it writes to shared memory (measured: expecting the latter never completes).  The epilogue
-// warps walk the K steps like decoders: for a native step they copy the stage's scale
-// words (which the producer brought into the stage's last kNvSfBytes with the
-// operands) into tensor memory and arrive on the stage's decoded barrier, which the
-// MMA waits on; it then issues four kind::mxf8f6f4 MMAs of K = 32 (scale byte kk of
-// each word for step kk).  Other K steps of such a problem are ordinary BF16 steps.
-// Three stages of 50 KB (A 16 KB, B 32 KB, scale words 1.5 KB).
+// bytes it writes to shared memory (measured: expecting the latter never completes).
+// The epilogue warps walk the K steps like decoders: for a native step they copy the
+// stage's scale words (which the producer brought with the operands) into tensor
+// memory and arrive on the stage's decoded barrier, which the MMA waits on; it then
+// issues four kind::mxf8f6f4 MMAs of K = 32 (scale byte kk of each word for step kk).
+// Other K steps of such a problem are ordinary BF16 steps.  Four stages of 48 KB
+// (A 16 KB, B 32 KB) and four 1.5 KB blocks of scale words after them; no epilogue
+// staging buffers (the epilogue stores rows from registers), which is what makes room
+// for the fourth stage.
 //   static constexpr bool kNative;
 //   bool     native_step(const TileInfo&, int ks) const;
-//   and load() copies the step's scale words to sA + kNvSfOff: 128 words of A rows
-//   0..127, then 256 words of B rows 0..255 (one word = the step's 4 scale bytes)
+//   void     load(const TileInfo&, int ks, uint8_t* sA, uint8_t* sB, uint8_t* sSf, uint64_t* bar) const;
+//            copies the step's scale words to sSf: 128 words of A rows 0..127, then 256
+//            words of B rows 0..255 (one word = the step's 4 scale bytes)
 //
 // Operand tiles in shared memory use the 128-byte swizzle written by TMA:
 //   A K-major : 128 rows x 128 B                         (one 16 KB box)
@@ -102,17 +105,21 @@ struct NativeOf<P, std::void_t<decltype(P::kNative)>> : std::integral_constant<b
 // MMAs sharing each B tile, 3 stages of (A 32 KB + B 32 KB), one accumulator pair
 // using all 512 TMEM columns -- a third fewer operand bytes per FLOP streamed into
 // the SM, at the price of an epilogue that no longer overlaps the main loop.
-constexpr int kNvSfOff = 128 * 128 + kBStageBytes;  // scale words of a native stage
-constexpr int kNvSfBytes = 384 * 4;
+constexpr int kNvSfBytes = 384 * 4;  // scale words of one native stage
 template <class P>
 struct EngineShape {
   static constexpr bool kWide = P::kWide;
   static constexpr bool kNat = NativeOf<P>::value;
   static constexpr int kAStage = kWide ? 2 * 128 * 128 : 128 * 128;
-  static constexpr int kStage = kNat ? 50 * 1024 : kAStage + kBStageBytes;
-  static constexpr int kStages = kWide || kNat ? 3 : 4;
-  static constexpr int kAccBufs = kWide || NativeOf<P>::value ? 1 : 2;
+  static constexpr int kStage = kAStage + kBStageBytes;
+  static constexpr int kStages = kWide ? 3 : 4;
+  static constexpr int kAccBufs = kWide || kNat ? 1 : 2;
+  static constexpr int kSfArea = kNat ? kStages * kNvSfBytes : 0;  // after the ring
+  static constexpr int kStg = kNat ? 0 : kStgBytes;                // epilogue staging, after that
+  static constexpr int kBarOff = kStages * kStage + kSfArea + kStg;
+  static constexpr int kSmem = kBarOff + 256 + 1024;  // barriers and TMEM slot, alignment slack
   static_assert(kStages * kStage <= 192 * 1024, "pipeline exceeds shared memory budget");
+  static_assert(kSmem <= kGemmSmemBytes, "shared memory exceeds the launch size");
 };
 
 struct TileInfo {
@@ -257,14 +264,19 @@ __device__ __forceinline__ bool mx_decode_stage(uint8_t* sb, int dt, const uint3
 
 // ------------------------------------------------------------------ block-scaled FP4
 // Scale words of a native K step: 4 UE8M0 bytes (the step's four 32-element blocks,
-// byte j for K elements 32j..32j+31) per operand row; in shared memory word i is A
-// row i (i < 128), word 128 + i is B row i.
+// byte j for K elements 32j..32j+31) per operand row, in blocks of 128 rows (A rows
+// 0..127, then B rows 0..127 and 128..255).  Inside a block the word of row i sits at
+// position nv_word(i) = 4 (i % 32) + i / 32: 16-byte row j holds the words of rows j,
+// 32 + j, 64 + j, 96 + j, which is what the tensor-memory layout below wants per lane.
 constexpr int kNvSfCols = 12;  // per stage: A 4 columns, then B 8 columns
+__host__ __device__ constexpr int nv_word(int i) { return 4 * (i & 31) + (i >> 5); }
 // Layout of the scale words in tensor memory.  kNvLayoutGroups (the one the MMAs use):
 // the words of operand row i sit in column i / 32 of that operand's block at lane i % 32
-// of every lane quarter (each quarter holds all rows).  kNvLayoutRows (self-test
+// of every lane quarter (each quarter holds all rows), written by the epilogue warps
+// with tcgen05.st.  kNvLayoutCopy: the same layout, copied by the MMA thread itself with
+// tcgen05.cp (no epilogue-warp work in the main loop).  kNvLayoutRows (self-test
 // comparison only): row i at lane i % 128 of column i / 128.
-constexpr int kNvLayoutGroups = 0, kNvLayoutRows = 1;
+constexpr int kNvLayoutGroups = 0, kNvLayoutRows = 1, kNvLayoutCopy = 2;
 // The six words this thread (lane of a quarter; half 0 / 1 = the first / second warp
 // of that quarter) stores for one step, from the stage's words sw.  kNvLayoutGroups:
 // half 0 takes A columns 0..3 and B columns 0..1, half 1 B columns 2..7 (A/B row
@@ -276,18 +288,18 @@ __device__ __forceinline__ void nv_load_scales(const uint32_t* sw, int q, int ha
   if (L == kNvLayoutGroups) {
     if (half == 0) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = sa[32 * c + lane];
+      for (int c = 0; c < 4; ++c) w[c] = sa[nv_word(32 * c + lane)];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) w[4 + c] = sb[32 * c + lane];
+      for (int c = 0; c < 2; ++c) w[4 + c] = sb[nv_word(32 * c + lane)];
     } else {
 #pragma unroll
-      for (int c = 2; c < 8; ++c) w[c - 2] = sb[32 * c + lane];
+      for (int c = 2; c < 8; ++c) w[c - 2] = sb[128 * (c >> 2) + nv_word(32 * (c & 3) + lane)];
     }
   } else {
     const int row = 32 * q + lane;
-    w[0] = sa[row];
-    w[1] = sb[row];
-    w[2] = sb[128 + row];
+    w[0] = sa[nv_word(row)];
+    w[1] = sb[nv_word(row)];
+    w[2] = sb[128 + nv_word(row)];
     w[3] = w[4] = w[5] = 0;
   }
 }
@@ -308,6 +320,7 @@ __device__ __forceinline__ void nv_store_scales(uint32_t sf, int q, int half, co
     tmem_st4(qa, w[0], w[0], w[0], w[0]);
     tmem_st2(qa + 4, w[1], w[2]);
   }
+  tmem_wait_st();
 }
 
 // P::kNoinlineEpilogue when the problem declares it, else false (see epilogue_call).
@@ -350,21 +363,23 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
   static_assert(P::kEpiWarps == 4 || P::kEpiWarps == 8, "4 or 8 epilogue warps");
   static_assert(!P::kWide || (P::kEpiWarps == 8 && !P::kAmn), "wide tiles: 8 epilogue warps, K-major A");
   static_assert(!DecodeOf<P>::value || P::kWide, "decoding epilogue warps need 256-row tiles");
-  static_assert(!NativeOf<P>::value || (!P::kWide && P::kEpiWarps == 8 && !P::kAmn && !P::kBmn && !DecodeOf<P>::value),
-                "block-scaled problems: 128-row tiles, 8 epilogue warps, K-major operands");
+  static_assert(!NativeOf<P>::value || (!P::kWide && !P::kAmn && !P::kBmn && !DecodeOf<P>::value && P::kEpiWarps == 8),
+                "block-scaled problems: 128-row tiles, K-major operands, 8 epilogue warps");
   static_assert(!NativeOf<P>::value || kAccCols + S::kStages * kNvSfCols <= 2 * kAccCols, "scale words exceed TMEM");
   // The epilogue warps walk the K steps (and the MMA waits for them) in decoding and
-  // block-scaled problems.
-  constexpr bool kWalk = DecodeOf<P>::value || NativeOf<P>::value;
+  // block-scaled problems -- unless the MMA thread copies the scale words itself.
+  constexpr bool kNvCopy = NativeOf<P>::value && NvLayoutOf<P>::value == kNvLayoutCopy;
+  constexpr bool kWalk = DecodeOf<P>::value || (NativeOf<P>::value && !kNvCopy);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStage + kStgBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   uint64_t* empty = full + S::kStages;
   uint64_t* tfull = empty + S::kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* dec = tempty + 2;  // kDecode: the stage's B tile has been decoded
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dec + S::kStages);
-  uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + S::kStages * S::kStage);
+  uint32_t* stg_base = reinterpret_cast<uint32_t*>(smem + S::kStages * S::kStage + S::kSfArea);
+  uint8_t* sf_base = smem + S::kStages * S::kStage;  // native: scale words of stage s at + s * kNvSfBytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = p.err;
 
@@ -406,7 +421,10 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             break;
           }
           uint8_t* sa = smem + s * S::kStage;
-          p.load(ti, ks, sa, sa + S::kAStage, &full[s]);
+          if constexpr (NativeOf<P>::value)
+            p.load(ti, ks, sa, sa + S::kAStage, sf_base + s * kNvSfBytes, &full[s]);
+          else
+            p.load(ti, ks, sa, sa + S::kAStage, &full[s]);
           issued |= 1u << s;
           last_ph = (last_ph & ~(1u << s)) | (ph << s);
           if (++s == S::kStages) {
@@ -446,6 +464,13 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
               // 128 K elements of one-byte codes: four K = 32 steps, 32 bytes apart,
               // step kk using byte kk of every scale word
               const uint32_t sfa = tmem_base + (uint32_t)(kAccCols + s * kNvSfCols);
+              if constexpr (kNvCopy) {
+                // the stage's three 512-byte blocks of words (A, B rows 0..127, B rows
+                // 128..255) into columns 0..3, 4..7, 8..11 of the stage's scale block
+                const uint32_t sw = smem_u32(sf_base + s * kNvSfBytes);
+#pragma unroll
+                for (int b = 0; b < 3; ++b) tmem_cp_32x128b_x4(sfa + 4 * b, plain_desc(sw + 512 * b, 128, 128));
+              }
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 mma_mx(d + (uint32_t)st.col, sw128_desc(sa + kk * 32, 16, 1024), sw128_desc(sb + kk * 32, 16, 1024),
@@ -585,7 +610,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           if (!got) break;
           if (cdec) {
             uint32_t w[6];
-            nv_load_scales<kNvL>(reinterpret_cast<const uint32_t*>(smem + s * S::kStage + kNvSfOff), q, half, lane, w);
+            nv_load_scales<kNvL>(reinterpret_cast<const uint32_t*>(sf_base + s * kNvSfBytes), q, half, lane, w);
             nv_store_scales<kNvL>(tmem_base + (uint32_t)(kAccCols + s * kNvSfCols), q, half, w);
           }
           tc_fence_before();
@@ -644,14 +669,15 @@ template <class P>
 cudaError_t launch_gemm(const P& p, int max_tiles, int num_sms, cudaStream_t stream, int slot) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, EngineShape<P>::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (max_tiles <= 0) return cudaSuccess;
   const int grid = max_tiles < num_sms ? max_tiles : num_sms;
   prof_begin(slot, stream);
-  gemm_kernel<P><<<grid, gemm_threads<P>(), kGemmSmemBytes, stream>>>(p);
+  gemm_kernel<P><<<grid, gemm_threads<P>(), EngineShape<P>::kSmem, stream>>>(p);
   prof_end(slot, stream);
   return cudaGetLastError();
 }

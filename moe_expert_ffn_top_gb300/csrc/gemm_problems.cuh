@@ -519,23 +519,46 @@ struct ProbW13T {
 };
 using ProbW13 = ProbW13T<false>;
 
+// 32 consecutive values of one row as bf16 (64 bytes, 16-byte aligned) from registers.
+__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 q;
+    q.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+    q.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+    q.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+    q.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+    *reinterpret_cast<uint4*>(dst + 8 * j) = q;
+  }
+}
+
 // Native FP4 forward F3: the gate/up base products on block-scaled FP4 tensor cores,
 //   G = q8(Xp) W1_e^T + s (Y1p B1_e^T),   U = q8(Xp) W3_e^T + s (Y3p B3_e^T)
 // with q8(Xp) the routed rows as MXFP8 (E4M3 codes Xq + scale words Xs, from
 // launch_gather_fwd_mxfp8) and W1/W3 in MXFP4 as stored -- no decoded copy.  128-row
 // tiles x (128 W1 rows + 128 W3 rows): H/128 native K steps, then the BF16 side-LoRA
 // steps of ProbW13 into the same accumulator; the same epilogue.  H, I multiples of 128.
+// Epilogue of the native W13, measured (65,536 tokens, E256): 16-byte row stores from
+// registers with four stages 6.68 ms; TMA bulk stores out of staging tiles with three
+// stages 6.81 ms; 16 epilogue warps releasing the accumulator as soon as it is read
+// (the next tile's MMAs overlapping the activation and the stores) 6.90 ms; the
+// activation computed and stored 8 columns at a time (fewer live registers) 7.29 ms;
+// gate and up read with one tensor-memory wait or one each: no difference.  In-kernel cycle
+// counters put the MMA issuer at ~98% of the FP8 rate while it has operands, waiting
+// for them 31% of the kernel with the producer's ring full: operand delivery (each
+// stage's A and weight tiles landing from L2/HBM) is what holds it, not the epilogue.
 struct ProbW13Nv {
   static constexpr bool kAmn = false, kBmn = false, kWide = false, kNative = true;
   static constexpr int kEpiWarps = 8;
+  static constexpr int kNvLayout = kNvLayoutCopy;  // scale words copied by the MMA thread
   const uint8_t* Xs;          // [P/128][H/128][128][4] scale bytes of Xq
   const uint8_t *S1t, *S3t;   // [E*I/128][H/128][128][4] scale bytes of W1/W3 (launch_scales_to_tiles)
   CUtensorMap mXq;            // Xq (H,P) bytes, box (128,128)
   CUtensorMap mW1f, mW3f;     // W1/W3 E2M1 (H,I,E), box (128 codes, 128, 1)
   CUtensorMap mY13p, mB1, mB3;  // as ProbW13
-  CUtensorMap mG, mU, mAct;
   PlanView pl;
   int* err;
+  uint16_t *G, *U, *Act;  // [P,I] outputs
   int H, I, r;
   int act;
   float clamp;
@@ -557,7 +580,7 @@ struct ProbW13Nv {
     tma_prefetch_map(&mB1);
     tma_prefetch_map(&mB3);
   }
-  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint8_t* sf, uint64_t* bar) const {
     const int nb = H / 128;
     if (ks < nb) {
       const int e = ti.g % pl.E;
@@ -567,9 +590,9 @@ struct ProbW13Nv {
       tma_load_2d(sa, &mXq, bar, ks * 128, ti.m0);
       tma_load_3d(sb, &mW1f, bar, ks * 128, ti.n0, e);
       tma_load_3d(sb + 128 * 128, &mW3f, bar, ks * 128, ti.n0, e);
-      bulk_load(sa + kNvSfOff, Xs + ((int64_t)(ti.m0 >> 7) * kt + ks) * 512, 512, bar);
-      bulk_load(sa + kNvSfOff + 512, S1t + wt * 512, 512, bar);
-      bulk_load(sa + kNvSfOff + 1024, S3t + wt * 512, 512, bar);
+      bulk_load(sf, Xs + ((int64_t)(ti.m0 >> 7) * kt + ks) * 512, 512, bar);
+      bulk_load(sf + 512, S1t + wt * 512, 512, bar);
+      bulk_load(sf + 1024, S3t + wt * 512, 512, bar);
     } else {
       const int j = ks - nb, half = j / nkr(), kb = j % nkr();
       mbar_arrive_expect_tx(bar, kAStage128 + 128 * 128);
@@ -583,17 +606,16 @@ struct ProbW13Nv {
     if (ks < nb) return MmaStep{256, 0, 0, ks == 0};
     return MmaStep{128, ((ks - nb) / nkr()) * 128, 0, 0};
   }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    const int y0 = ti.m0 + row - (threadIdx.x & 31);  // warp's first row
-    TmaStoreRing out(stg);
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t*) const {
+    const int64_t o = ((int64_t)ti.m0 + row) * I + ti.n0;  // this thread's row: 64-byte row segments
     for (int c = c0; c < 128; c += cs) {
       float g[32], u[32], a[32];
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
       act_fwd_chunk(act, clamp, g, u, a);
-      out.store_bf16(&mG, ti.n0 + c, y0, g);
-      out.store_bf16(&mU, ti.n0 + c, y0, u);
-      out.store_bf16(&mAct, ti.n0 + c, y0, a);
+      store_row_bf16(G + o + c, g);
+      store_row_bf16(U + o + c, u);
+      store_row_bf16(Act + o + c, a);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
@@ -1512,23 +1534,25 @@ struct ProbPlainNv {
     tma_prefetch_map(&mA);
     tma_prefetch_map(&mB);
   }
-  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint64_t* bar) const {
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint8_t* sf, uint64_t* bar) const {
     mbar_arrive_expect_tx(bar, 128 * 128 + 256 * 64 + kNvSfBytes);  // E2M1 boxes count packed bytes
     tma_load_2d(sa, &mA, bar, ks * 128, ti.m0);
     tma_load_3d(sb, &mB, bar, ks * 128, ti.n0, 0);
     const int64_t kt = K / 128;
-    bulk_load(sa + kNvSfOff, As + ((int64_t)(ti.m0 >> 7) * kt + ks) * 512, 512, bar);
-    bulk_load(sa + kNvSfOff + 512, Bs + ((int64_t)(ti.n0 >> 7) * kt + ks) * 512, 512, bar);
-    bulk_load(sa + kNvSfOff + 1024, Bs + ((int64_t)((ti.n0 >> 7) + 1) * kt + ks) * 512, 512, bar);
+    bulk_load(sf, As + ((int64_t)(ti.m0 >> 7) * kt + ks) * 512, 512, bar);
+    bulk_load(sf + 512, Bs + ((int64_t)(ti.n0 >> 7) * kt + ks) * 512, 512, bar);
+    bulk_load(sf + 1024, Bs + ((int64_t)((ti.n0 >> 7) + 1) * kt + ks) * 512, 512, bar);
   }
   __device__ bool native_step(const TileInfo&, int) const { return true; }
   __device__ MmaStep mma_step(const TileInfo&, int ks) const { return MmaStep{256, 0, 0, ks == 0}; }
-  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t* stg) const {
-    float* o0 = C + ((int64_t)ti.m0 + row - (threadIdx.x & 31)) * N + ti.n0;  // warp's first row
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t*) const {
+    float* o = C + ((int64_t)ti.m0 + row) * N + ti.n0;  // this thread's row (no staging: native shape)
     for (int c = c0; c < 256; c += cs) {
       float v[32];
       tmem_ld32(taddr + c, v);
-      warp_store_rows_f32(o0 + c, N, 32, v, 1.0f, 32, stg);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(o + c + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}

@@ -150,7 +150,8 @@ __global__ void gather_fwd_mxfp8_kernel(PlanView pl, const uint16_t* __restrict_
         v[i] = on ? __ldg(reinterpret_cast<const uint4*>(x + t * H + blk * 32 + 8 * i)) : make_uint4(0, 0, 0, 0);
       uint4 codes[2];
       const uint32_t sb = mxfp8_block(v, codes);
-      // the 4 scale bytes of one K step (blocks 4j..4j+3) as one word, on lane 4j
+      // the 4 scale bytes of one K step (blocks 4j..4j+3) as one word, on lane 4j; in
+      // its 512-byte block the word of row i sits at 4 (i % 32) + i / 32
       const uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8) |
                             (__shfl_down_sync(0xffffffffu, sb, 2) << 16) | (__shfl_down_sync(0xffffffffu, sb, 3) << 24);
       for (int j = 0; j < k; ++j) {
@@ -160,8 +161,8 @@ __global__ void gather_fwd_mxfp8_kernel(PlanView pl, const uint16_t* __restrict_
         dst[0] = codes[0];
         dst[1] = codes[1];
         if ((lane & 3) == 0)
-          *reinterpret_cast<uint32_t*>(Xs + ((int64_t)(R >> 7) * ks_per_row + (blk >> 2)) * 512 + (R & 127) * 4) =
-              word;
+          *reinterpret_cast<uint32_t*>(Xs + ((int64_t)(R >> 7) * ks_per_row + (blk >> 2)) * 512 +
+                                       (4 * (R & 31) + ((R >> 5) & 3)) * 4) = word;
       }
     }
     for (int c = lane * 8; c < r2; c += 32 * 8) {
@@ -180,22 +181,25 @@ __global__ void gather_fwd_mxfp8_kernel(PlanView pl, const uint16_t* __restrict_
       copy_row_or_zero(reinterpret_cast<uint16_t*>(Xq + p * H), nullptr, H / 2, lane);
       copy_row_or_zero(Y13p + p * r2, nullptr, r2, lane);
       for (int j = lane; j < ks_per_row; j += 32)
-        *reinterpret_cast<uint32_t*>(Xs + ((p >> 7) * ks_per_row + j) * 512 + (p & 127) * 4) = 0x7F7F7F7Fu;
+        *reinterpret_cast<uint32_t*>(Xs + ((p >> 7) * ks_per_row + j) * 512 + (4 * (p & 31) + ((p >> 5) & 3)) * 4) =
+            0x7F7F7F7Fu;
     }
   }
 }
 
 // Scale bytes [rows, K/32] (row-major, one per 32 K elements) to the tile-major layout
-// [rows/128][K/128][128][4]: the 4 bytes of one 128-wide K step of a row become one
-// word, and the 128 words of a row tile for one K step 512 contiguous bytes (what a
-// native GEMM stage copies).  rows % 128 == 0, K % 128 == 0.
+// [rows/128][K/128][32][4][4]: the 4 bytes of one 128-wide K step of a row become one
+// word, the 128 words of a row tile for one K step 512 contiguous bytes (what a
+// native GEMM stage copies), row i's word at position 4 (i % 32) + i / 32 of them.
+// rows % 128 == 0, K % 128 == 0.
 __global__ void scales_to_tiles_kernel(const uint8_t* __restrict__ S, int64_t rows, int kt,
                                        uint8_t* __restrict__ St) {
   const int64_t n = rows * kt;  // words
   for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < n; w += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = w & 127, j = (w >> 7) % kt, rt = (w >> 7) / kt;  // row in tile, K step, row tile
     const int64_t row = rt * 128 + i;
-    *reinterpret_cast<uint32_t*>(St + w * 4) = __ldg(reinterpret_cast<const uint32_t*>(S + row * kt * 4 + j * 4));
+    *reinterpret_cast<uint32_t*>(St + (w & ~(int64_t)127) * 4 + (4 * (i & 31) + (i >> 5)) * 4) =
+        __ldg(reinterpret_cast<const uint32_t*>(S + row * kt * 4 + j * 4));
   }
 }
 

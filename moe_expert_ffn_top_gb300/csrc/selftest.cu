@@ -84,6 +84,7 @@ static int plain_native(int M, int N, int K, const uint8_t* Aq, const uint8_t* A
 int run_plain_native(int M, int N, int K, const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
                      float* C, int layout, int* err, int num_sms, cudaStream_t stream) {
   if (layout == kNvLayoutRows) return plain_native<kNvLayoutRows>(M, N, K, Aq, As, Bq, Bs, C, err, num_sms, stream);
+  if (layout == kNvLayoutCopy) return plain_native<kNvLayoutCopy>(M, N, K, Aq, As, Bq, Bs, C, err, num_sms, stream);
   return plain_native<kNvLayoutGroups>(M, N, K, Aq, As, Bq, Bs, C, err, num_sms, stream);
 }
 

@@ -199,21 +199,35 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // Stores 2 / 4 consecutive 32-bit tensor-memory columns of this warp's lane quarter
-// (one value per column from each thread, thread i -> lane i of the quarter), then
-// waits for the stores to complete.
+// (one value per column from each thread, thread i -> lane i of the quarter); the
+// stores complete at the next tmem_wait_st.
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(a), "r"(b)
-      : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
 }
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(a), "r"(b), "r"(c), "r"(d)
-      : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor without swizzle (fields as sw128_desc, layout 0):
+// 8-row x 16-byte core matrices, `lbo` / `sbo` bytes apart along the two directions.
+__device__ __forceinline__ uint64_t plain_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Copies 32 rows x 16 bytes of shared memory (descriptor sdesc) into 4 consecutive
+// tensor-memory columns at lanes 0..31 of every lane quarter (row i -> lane i, its
+// four 32-bit words -> the four columns).  Asynchronous; ordered with the tcgen05.mma
+// issued after it by the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread completed.

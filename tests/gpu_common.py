@@ -42,9 +42,10 @@ def assert_close(name: str, got: torch.Tensor, ref: torch.Tensor) -> None:
 
 def dims_of(shp: Shape, scale: Optional[float] = None, mx_once: bool = False) -> m.Dims:
     """mx_once: an MXFP4 base decoded once per pass (base_fmt 2) instead of inside the GEMMs (1);
-    base_fmt "mxfp4_native" is the native FP4 forward (3)."""
+    base_fmt "mxfp4_native" is the native FP4 forward with the rest decoded in the GEMMs (3)
+    or once per pass (4)."""
     mx = 2 if mx_once else 1
-    fmt = {"mxfp4": mx, "mxfp4_native": 3}.get(shp.base_fmt, 0)
+    fmt = {"mxfp4": mx, "mxfp4_native": mx + 2}.get(shp.base_fmt, 0)
     return m.make_dims(shp.T, shp.H, shp.I, shp.E, shp.k, shp.r, shp.A, shp.scale if scale is None else scale,
                        base_fmt=fmt, act=1 if shp.act == "geglu" else 0,
                        act_clamp=shp.clamp)

@@ -74,7 +74,8 @@ def test_forward_rejections(L):
     assert _call_forward(L, _dims(H=500)) == -2
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 2, 0)) == -5   # unknown activation
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 0, -1.0)) == -2  # negative clamp
-    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 4)) == -5   # unknown base format
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 5)) == -5   # unknown base format
+    assert _call_forward(L, m.Dims(256, 576, 256, 16, 2, 16, 1, 128, 1.0, 0, 4)) == -2   # native + once: H % 128
     assert _call_forward(L, m.Dims(256, 576, 256, 16, 2, 16, 1, 128, 1.0, 0, 3)) == -2   # native: H % 128
     assert _call_forward(L, m.Dims(256, 512, 320, 16, 2, 16, 1, 128, 1.0, 0, 3)) == -2   # native: I % 128
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 3), weight=FAKE + 16,
@@ -182,7 +183,7 @@ def test_native_entry_rejections(L):
     assert L.moe_lora_native_selftest(100, 512, 256, *ok[3:], 0, None) == -2   # M % 128
     assert L.moe_lora_native_selftest(256, 384, 256, *ok[3:], 0, None) == -2   # N % 256
     assert L.moe_lora_native_selftest(256, 512, 192, *ok[3:], 0, None) == -2   # K % 128
-    assert L.moe_lora_native_selftest(*ok, 2, None) == -5                     # unknown layout
+    assert L.moe_lora_native_selftest(*ok, 3, None) == -5                     # unknown layout
     assert L.moe_lora_native_selftest(256, 512, 256, FAKE, FAKE, FAKE + 16, FAKE, FAKE, 0, None) == -3  # Bq 32 B
     assert L.moe_lora_native_selftest(*ok, 0, None) == -7
 

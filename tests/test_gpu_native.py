@@ -39,9 +39,10 @@ def _tables():
 
 
 def _tiles(sc):
-    """Scale bytes [rows, K/32] -> the tile-major layout [rows/128][K/128][128][4]."""
+    """Scale bytes [rows, K/32] -> the tile-major layout [rows/128][K/128][32][4][4]:
+    per 128-row block and 128-wide K step, row 32b + a's 4 bytes at word 4a + b."""
     rows, nb = sc.shape
-    return sc.view(rows // 128, 128, nb // 4, 4).permute(0, 2, 1, 3).contiguous()
+    return sc.view(rows // 128, 4, 32, nb // 4, 4).permute(0, 3, 2, 1, 4).contiguous()
 
 
 def _native_operands(M, N, K, seed, lo=118, hi=136):
@@ -57,13 +58,15 @@ def _native_operands(M, N, K, seed, lo=118, hi=136):
     return aq, asc, bq, bsc, A @ B.T
 
 
+@pytest.mark.parametrize("layout", [0, 2])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 512, 512), (640, 768, 1024)])
-def test_native_engine_gemm(M, N, K):
+def test_native_engine_gemm(M, N, K, layout):
     """The block-scaled MMA path of the engine (E4M3 x E2M1, UE8M0 per 32 on both
-    sides, scale words in tensor memory) against float64."""
+    sides, scale words in tensor memory, written by the epilogue warps (0) or copied
+    by the MMA thread (2)) against float64."""
     aq, asc, bq, bsc, ref = _native_operands(M, N, K, seed=M + N + K)
     C = torch.full((M, N), float("nan"), device="cuda")
-    m.moe_lora_native_selftest(aq.cuda(), _tiles(asc).cuda(), bq.cuda(), _tiles(bsc).cuda(), C)
+    m.moe_lora_native_selftest(aq.cuda(), _tiles(asc).cuda(), bq.cuda(), _tiles(bsc).cuda(), C, layout=layout)
     torch.cuda.synchronize()
     assert m.moe_lora_gemm_selftest_error() == 0
     assert rel_l2(C, ref) < 1e-6
@@ -113,12 +116,25 @@ def test_mxfp8_quantizer_bitwise():
         assert ((codes[i][~nz] & 0x7F) == 0).all(), i
 
 
-def test_native_tiny_forward_backward():
+@pytest.mark.parametrize("once", [False, True])
+def test_native_tiny_forward_backward(once):
+    """base_fmt 3 (the rest decoded in the GEMMs) and 4 (decoded once per pass)."""
     shp = Shape(T=200, H=512, I=256, E=16, k=2, r=16, mask_frac=0.1, base_fmt="mxfp4_native")
     inp = make_inputs(shp, seed=61)
-    out = run_gpu(inp, shp, poison=True)
+    out = run_gpu(inp, shp, poison=True, mx_once=once)
     assert out["err"] == 0
     _full_check(inp, shp, out)
+
+
+def test_native_modes_agree_bitwise():
+    """base_fmt 3 and 4 differ only in where the MXFP4 weights are decoded (exactly)
+    outside the native products: every output and gradient equal bit for bit."""
+    shp = Shape(T=256, H=512, I=256, E=16, k=2, r=16, base_fmt="mxfp4_native")
+    inp = make_inputs(shp, seed=65)
+    a = run_gpu(inp, shp)
+    b = run_gpu(inp, shp, mx_once=True)
+    for n in ("y", "dx", "dw", "dA1", "dA3", "dB1", "dB3", "dA2", "dB2"):
+        assert torch.equal(a[n], b[n]), n
 
 
 @pytest.mark.parametrize("A,act,clamp,T,H,I", [(2, "swiglu", 0.0, 256, 512, 256), (1, "geglu", 0.25, 77, 640, 384),
@@ -145,13 +161,14 @@ def test_native_looser_gate_against_bf16_activations():
     assert 1e-4 < d <= 5e-2, d
 
 
-def test_native_production_width_sampled():
+@pytest.mark.parametrize("once", [False, True])
+def test_native_production_width_sampled(once):
     """Production widths (H=4096, I=2048, E=256, top-6, rank 128), 2,048 tokens,
-    sampled sparse-dy parity against the oracle's native mode."""
+    sampled sparse-dy parity against the oracle's native mode (base_fmt 3 and 4)."""
     shp = shape("prod_native", 2048)
     inp = make_inputs(shp, seed=64, device="cuda")
     sample = [0, 7, 700, 1500, 2047]
     inp = _sparse_dy(inp, shp, sample)
-    out = run_gpu(inp, shp)
+    out = run_gpu(inp, shp, mx_once=once)
     assert out["err"] == 0
     _sampled_check(inp, shp, out, sample)

@@ -32,7 +32,7 @@ static int encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* 
                   CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   std::call_once(g_encode_once, load_encode);
   if (!g_encode) return -1;
-  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};  // rank <= 5
   const CUresult r = g_encode(m, type, rank, const_cast<void*>(base), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -66,6 +66,13 @@ int tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
   const cuuint64_t strides[2] = {d0, d0 * d1};
   const cuuint32_t box[3] = {b0, b1, 1};
   return encode(m, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+int tmap_mn4(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t d2) {
+  const cuuint64_t dims[4] = {64, rows, cols / 64, d2};
+  const cuuint64_t strides[3] = {cols * 2, 128, rows * cols * 2};
+  const cuuint32_t box[4] = {64, 64, 4, 1};
+  return encode(m, base, 4, dims, strides, box);
 }
 
 int tmap_2d_b8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {

@@ -107,10 +107,10 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   auto w2d = [&](auto p) -> int {
     MAP(tmap_2d(&p.mDp, Dp, H, P, 64, 128));
     MAP(tmap_2d(&p.mD2p, D2p, r, P, 64, 128));
-    if (!mx) MAP(tmap_3d(&p.mW2, bW2, I, H, E, 64, 64));
+    if (!mx) MAP(kMnChunkCopy ? tmap_mn4(&p.mW2, bW2, I, H, E) : tmap_3d(&p.mW2, bW2, I, H, E, 64, 64));
     if (mx) MAP(tmap_3d_u8(&p.mW2q, w->W2, I / 2, H, E, 128, 64));
     p.S2q = w->S2;
-    MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, 64));
+    MAP(kMnChunkCopy ? tmap_mn4(&p.mA2, w->A2, I, r, G) : tmap_3d(&p.mA2, w->A2, I, r, G, 64, 64));
     p.pl = pl;
     p.err = pl.err;
     p.topk_w = topk_w;
@@ -149,8 +149,8 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
     MAP(tmap_2d(&p.mdG, dG, I, P, 64, 128));
     MAP(tmap_2d(&p.mdU, dU, I, P, 64, 128));
     if (!mx) {
-      MAP(tmap_3d(&p.mW1, bW1, H, I, E, 64, 64));
-      MAP(tmap_3d(&p.mW3, bW3, H, I, E, 64, 64));
+      MAP(kMnChunkCopy ? tmap_mn4(&p.mW1, bW1, H, I, E) : tmap_3d(&p.mW1, bW1, H, I, E, 64, 64));
+      MAP(kMnChunkCopy ? tmap_mn4(&p.mW3, bW3, H, I, E) : tmap_3d(&p.mW3, bW3, H, I, E, 64, 64));
     }
     if (mx) {
       MAP(tmap_3d_u8(&p.mW1q, w->W1, H / 2, I, E, 128, 64));

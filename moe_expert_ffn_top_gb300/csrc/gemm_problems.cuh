@@ -20,6 +20,12 @@ namespace moelora {
 
 constexpr int kAStage128 = 128 * 128;  // bytes of one 128-row x 64 bf16 operand tile
 
+// MN-major weight tiles of the dgrads (256 columns = four 64 x 64 boxes, 8 KB apart):
+// one 4D copy over the weight seen as 64-column chunks (tmap_mn4) instead of four 3D
+// copies -- the producer's TMA issue is what held the W2 dgrad (in-kernel counters:
+// 69% of the kernel issuing copies, the MMA waiting for operands 32%).
+constexpr bool kMnChunkCopy = true;
+
 __device__ __forceinline__ int adapter_of_tile(const PlanView& pl, int t) {
   int a = 0;
   while (a + 1 < pl.A && t >= pl.tok_tile[a + 1]) ++a;
@@ -926,7 +932,8 @@ struct ProbW2DgradT {
   // router-gradient partial sums per row and column tile (one per epilogue column stripe)
   static constexpr int kPartsPerTile = kWide ? 1 : kEpiWarps / 4;
   CUtensorMap mDp, mD2p, mW2, mA2;  // Dp (H,P) box(64,128); D2p (r,P) box(64,128);
-                                    // W2 (I,H,E) box(64,64,1); A2 (I,r,G) box(64,64,1)
+                                    // W2 (I,H,E), A2 (I,r,G): box(64,64,1), or 64-column
+                                    // chunks box(64,64,4,1) with kMnChunkCopy
   CUtensorMap mdG, mdU;             // outputs (I,P), 32 x 32 store boxes (4 epilogue warps)
   PlanView pl;
   int* err;
@@ -965,11 +972,17 @@ struct ProbW2DgradT {
       if (MX)  // 64 rows of W2 (h) x 256 packed columns (i)
         tma_load_3d(sb + kMxRaw, &mW2q, bar, ti.n0 / 2, ks * kBK, ti.g % pl.E);
       else
-        for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
+        if (kMnChunkCopy)
+          tma_load_4d(sb, &mW2, bar, 0, ks * kBK, ti.n0 / 64, ti.g % pl.E);
+        else
+          for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mW2, bar, ti.n0 + c * 64, ks * kBK, ti.g % pl.E);
     } else {
       const int kb = ks - nb;
       load_a_wide(ti, sa, &mD2p, bar, kb * kBK);
-      for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mA2, bar, ti.n0 + c * 64, kb * kBK, ti.g);
+      if (kMnChunkCopy)
+        tma_load_4d(sb, &mA2, bar, 0, kb * kBK, ti.n0 / 64, ti.g);
+      else
+        for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, &mA2, bar, ti.n0 + c * 64, kb * kBK, ti.g);
     }
   }
   // MX, base K steps: box b holds W2[e][h][i] for i = n0 + 64 b.., h = 64 ks + (rho % 64)
@@ -1095,7 +1108,8 @@ struct ProbW13DgradT {
   const uint8_t *S1q, *S3q;  // MX: scales [E,I,H/32]
   CUtensorMap mW1q, mW3q;    // MX: packed [E,I,H/2] bytes, box (128, 64, 1)
   CUtensorMap mdXp;                          // output (H,P), 32 x 32 store boxes
-  CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1);
+  CUtensorMap mdG, mdU, mW1, mW3, mB1, mB3;  // dG/dU (I,P) box(64,128); W1/W3 (H,I,E) box(64,64,1)
+                                             // or chunks box(64,64,4,1) (kMnChunkCopy);
                                              // B1/B3 (r,I,G) box(64,64,1)
   PlanView pl;
   int* err;
@@ -1132,7 +1146,10 @@ struct ProbW13DgradT {
       if (MX)  // 64 rows of W1 / W3 (i) x 256 packed columns (h)
         tma_load_3d(sb + kMxRaw, second ? &mW3q : &mW1q, bar, ti.n0 / 2, kk, e);
       else
-        for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, second ? &mW3 : &mW1, bar, ti.n0 + c * 64, kk, e);
+        if (kMnChunkCopy)
+          tma_load_4d(sb, second ? &mW3 : &mW1, bar, 0, kk, ti.n0 / 64, e);
+        else
+          for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * 8192, second ? &mW3 : &mW1, bar, ti.n0 + c * 64, kk, e);
     } else {
       const int nbox = (round16(r) + 63) / 64;
       mbar_arrive_expect_tx(bar, ti.mh * kAStage128 + nbox * 8192);

@@ -20,6 +20,11 @@ int tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t
 // in shared memory as b1 rows of b0 bytes.  d0 a multiple of 16, b0 of 16.
 int tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1);
 
+// bf16 tensor [d2][rows][cols] (cols % 64 == 0) seen as 64-column chunks -- dims
+// {64, rows, cols/64, d2}, strides {cols*2, 128, rows*cols*2} bytes -- with a box of
+// {64, 64, 4, 1}: one copy lands four MN-major 64 x 64 tiles of columns c0 .. c0+255,
+// 8 KB apart, exactly as four 2D boxes would (chunks past the last column read zeros).
+int tmap_mn4(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t d2);
 // 2D byte tensor [outer][inner] (E4M3 codes) with the 128-byte swizzle: a box of
 // 128 x box_outer lands as box_outer rows of 128 bytes.
 int tmap_2d_b8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer);

@@ -217,15 +217,16 @@ def e4m3_round(v: float) -> float:
     return lib("f32").oracle_e4m3_round(v)
 
 
-def mxfp8_quantize(v: torch.Tensor):
+def mxfp8_quantize(v: torch.Tensor, prec: str = "f32"):
     """MXFP8 (E4M3 elements, one UE8M0 scale per 32 from the start) of a 1-D tensor:
-    (codes uint8 [n], scale bytes uint8 [ceil(n/32)], dequantised float64 [n])."""
+    (codes uint8 [n], scale bytes uint8 [ceil(n/32)], dequantised float64 [n]).  prec:
+    the oracle build whose arithmetic quantises (f32 reads the values as fp32)."""
     v = v.detach().double().contiguous().cpu().flatten()
     n = v.numel()
     codes = torch.zeros(n, dtype=torch.uint8)
     scales = torch.zeros((n + 31) // 32, dtype=torch.uint8)
     deq = torch.zeros(n, dtype=torch.float64)
-    bad = lib("f32").oracle_mxfp8_quantize(ctypes.c_void_p(v.data_ptr()), ctypes.c_int64(n),
+    bad = lib(prec).oracle_mxfp8_quantize(ctypes.c_void_p(v.data_ptr()), ctypes.c_int64(n),
                                            ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()),
                                            ctypes.c_void_p(deq.data_ptr()))
     assert bad == 0

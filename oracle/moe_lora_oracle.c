@@ -43,16 +43,17 @@
  * 1 mantissa bit) with one UE8M0 scale 2^(b-127) per 32 contiguous elements along
  * the contraction axis; low nibble = lower index.  Decoded here from the bit fields.
  *
- * Native FP4 forward (act_quant = 1): the gate/up base products take x_t as MXFP8,
- * i.e. q8(x_t), so that both operands of those products are block-scaled
- * low-precision values ("FP8/FP4/FP8 forwards" in the PR's Fresh validation;
- * block-scaled FP4 against dequantise-to-BF16 in its Performance notes):
- *   g = W1_e q8(x_t) + s B1 y1,   u = W3_e q8(x_t) + s B3 y3
- * with everything else unchanged (y1/y3 still use x_t).  q8 is the OCP MX FP8
+ * Native FP4 forward (act_quant = 1): both base products of the forward take their
+ * activations as MXFP8, so that both operands are block-scaled low-precision values
+ * ("FP8/FP4/FP8 forwards" in the PR's Fresh validation; block-scaled FP4 against
+ * dequantise-to-BF16 in its Performance notes):
+ *   g = W1_e q8(x_t) + s B1 y1,   u = W3_e q8(x_t) + s B3 y3,   o = W2_e q8(h) + s B2 z2
+ * with everything else unchanged (y1/y3 use x_t, z2 = rb(A2 h) uses h).  q8 is the OCP MX FP8
  * format with E4M3 elements: per 32 contiguous values one shared scale 2^X,
  * X = floor(log2 max|v|) - 8 (8 = the exponent of E4M3's largest power of two),
  * and each element v / 2^X rounded to nearest even on the E4M3 grid, saturating at
- * +-448.  The backward treats q8 as the identity, like rb.
+ * +-448; q8(h) takes the blocks along I.  The backward treats q8 as the identity, like
+ * rb; the router-weight gradient stays <dy_t, o_j> with this o.
  *
  * Build: real = float (default) or double (-DORACLE_DOUBLE).  Compile with
  * -ffp-contract=off so x86 and Arm hosts give identical results.
@@ -95,7 +96,7 @@ typedef struct {
   int32_t round_bf16;     /* 1: bf16 rounding points on; 0: off */
   int32_t nthreads;       /* OpenMP threads (0 = runtime default) */
   int32_t act;            /* 0: SwiGLU, 1: GeGLU */
-  int32_t act_quant;      /* 1: q8(x) in the gate/up base products (native FP4 forward) */
+  int32_t act_quant;      /* 1: q8(x) and q8(h) in the base products (native FP4 forward) */
   double clamp;           /* activation clamp c (0 = none) */
 } odims;
 
@@ -305,12 +306,12 @@ int oracle_plan(int64_t T, int32_t k, int32_t E, int32_t A, int32_t BM, const in
 /* ---------------- per-route forward ---------------- */
 
 typedef struct {
-  real *xt, *xq, *y1, *y3, *g, *u, *h, *z2, *o, *rowbuf;
+  real *xt, *xq, *y1, *y3, *g, *u, *h, *hq, *z2, *o, *rowbuf;
 } fwd_scratch;
 
 static void fwd_alloc(const odims* d, fwd_scratch* s) {
   int64_t H = d->H, I = d->I, r = d->r;
-  int64_t n = 2 * H + 2 * r + 3 * I + r + H + (H > I ? H : I);
+  int64_t n = 2 * H + 2 * r + 4 * I + r + H + (H > I ? H : I);
   real* p = (real*)malloc(sizeof(real) * n);
   s->xt = p; p += H;
   s->xq = p; p += H;
@@ -319,6 +320,7 @@ static void fwd_alloc(const odims* d, fwd_scratch* s) {
   s->g = p; p += I;
   s->u = p; p += I;
   s->h = p; p += I;
+  s->hq = p; p += I;
   s->z2 = p; p += r;
   s->o = p; p += H;
   s->rowbuf = p;
@@ -366,10 +368,12 @@ static void route_forward(const odims* d, const oinputs* in, int a, int e, fwd_s
     for (int64_t i = 0; i < I; ++i) acc += row[i] * s->h[i];
     s->z2[q] = rb(d, acc);
   }
+  if (d->act_quant) mxfp8_row(s->h, I, s->hq);
+  const real* hb = d->act_quant ? s->hq : s->h; /* h as the down base product sees it */
   for (int64_t c = 0; c < H; ++c) {
     real ob = 0, ol = 0;
     ld_row(&in->W2, ((int64_t)e * H + c) * I, I, row);
-    for (int64_t i = 0; i < I; ++i) ob += row[i] * s->h[i];
+    for (int64_t i = 0; i < I; ++i) ob += row[i] * hb[i];
     int64_t b2 = ((int64_t)a * H + c) * r;
     for (int64_t q = 0; q < r; ++q) ol += ld(&in->B2, b2 + q) * s->z2[q];
     s->o[c] = ob + sc * ol;

@@ -8,9 +8,10 @@ validation).  Each test ties the oracle to something it does not compute itself:
   * rounding to E4M3 against brute force over the whole grid (nearest value, ties
     to the even code, saturation at 448);
   * the shared-scale rule: every block's max|v| / 2^X falls in [256, 512);
-  * the identity on inputs that are already MXFP8 values: native == plain bitwise;
-  * the dense special case in torch float64: gate/up base products on q8(x) with
-    a straight-through gradient, side paths on x, for the forward and every
+  * the identity on inputs that are already MXFP8 values, with a zero down-projection
+    base (so q8 of the activation has nothing to act on): native == plain bitwise;
+  * the dense special case in torch float64: base products on q8(x) and q8(h) with
+    straight-through gradients, side paths on x and h, for the forward and every
     gradient the oracle returns.
 """
 import math
@@ -113,10 +114,12 @@ def _native(shp):
 
 def test_native_identity_on_mxfp8_values():
     """x already in MXFP8 (each block's max in [256, 448] x 2^X, all values on the
-    grid x 2^X): q8(x) = x, so the native forward and backward equal the plain ones
-    bitwise (FP32 oracle, rounding on)."""
+    grid x 2^X): q8(x) = x; with W2 = 0 the down base product vanishes in both modes,
+    so the native forward and backward equal the plain ones bitwise (FP32 oracle,
+    rounding on)."""
     shp = Shape(T=6, H=64, I=32, E=3, k=2, r=8, base_fmt="mxfp4")
     inp = make_inputs(shp, seed=9)
+    inp["W2"] = torch.zeros_like(inp["W2"])            # E2M1 code 0 under any scale
     grid = torch.tensor(_grid(), dtype=torch.float64)
     g = torch.Generator().manual_seed(10)
     x = torch.zeros(shp.T, shp.H, dtype=torch.float64)
@@ -139,9 +142,9 @@ def test_native_identity_on_mxfp8_values():
 
 
 def _dense_native_reference(inp, shp, scale):
-    """One expert, one slot, weight w: torch float64 with the gate/up base products
-    on q8(x) (straight-through: the gradient passes q8 unchanged) and the side
-    shrinks A1 x, A3 x on x itself."""
+    """One expert, one slot, weight w: torch float64 with the base products on q8(x)
+    and q8(h) (straight-through: the gradient passes q8 unchanged) and the side
+    shrinks A1 x, A3 x and A2 h on x and h themselves."""
     leaves = {n: inp[n].clone().double().requires_grad_(True)
               for n in ("x", "topk_w", "A1", "A3", "B1", "B3", "A2", "B2")}
     W1, W3, W2 = inp["W1"].double()[0], inp["W3"].double()[0], inp["W2"].double()[0]
@@ -153,8 +156,10 @@ def _dense_native_reference(inp, shp, scale):
     g = xq @ W1.T + scale * y1 @ leaves["B1"][0, 0].T
     u = xq @ W3.T + scale * y3 @ leaves["B3"][0, 0].T
     h = torch.nn.functional.silu(g) * u
+    hq8 = torch.stack([oracle.mxfp8_quantize(h[t].detach(), prec="f64")[2] for t in range(shp.T)])
+    hq = h + (hq8 - h).detach()
     z2 = h @ leaves["A2"][0, 0].T
-    o = h @ W2.T + scale * z2 @ leaves["B2"][0].T
+    o = hq @ W2.T + scale * z2 @ leaves["B2"][0].T
     y = leaves["topk_w"][:, :1] * o
     (y * inp["dy"].double()).sum().backward()
     return y.detach(), {n: v.grad for n, v in leaves.items()}, q

@@ -131,7 +131,11 @@ int run_backward(const moe_lora_dims* d, const void* plan_ws, const void* saved,
   };
   if (int rc = mx ? w2d(ProbW2DgradT<true>{}) : w2d(ProbW2DgradT<false>{})) return rc;
   const int parts = mx ? ProbW2DgradT<true>::kPartsPerTile : ProbW2DgradT<false>::kPartsPerTile;
-  LAUNCH(launch_dw(pl, part, parts * cdiv(d->I, 256), dw, num_sms, stream));
+  if (fmt_native(d))  // the down product ran on q8(Act): dw from the forward's O and Z2 rows
+    LAUNCH(launch_dw_from_o(pl, dy, dyB2, (const uint16_t*)(sv + SL.O), (const uint16_t*)(sv + SL.Z2), d->H, d->r,
+                            d->scale, dw, num_sms, stream));
+  else
+    LAUNCH(launch_dw(pl, part, parts * cdiv(d->I, 256), dw, num_sms, stream));
   // dA2 per (adapter, expert)
   {
     ProbDA2 p;

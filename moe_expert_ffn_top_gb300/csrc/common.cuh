@@ -83,7 +83,7 @@ inline PlanLayout plan_layout(const moe_lora_dims* d) {
 // GEMMs (base_fmt 1) is never stored in bf16; decoded once per pass (base_fmt 2) it
 // adds the bf16 W1, W3 [E,I,H] and W2 [E,H,I], which the backward reuses.
 struct SavedLayout {
-  size_t Y13p, G, U, Act, Z2w, W1, W3, W2, total;   // [P,2r], [P,I], [P,I], [P,I], [T,r]
+  size_t Y13p, G, U, Act, Z2w, O, Z2, W1, W3, W2, total;   // [P,2r], [P,I], [P,I], [P,I], [T,r]
 };
 inline SavedLayout saved_layout(const moe_lora_dims* d) {
   SavedLayout L;
@@ -95,6 +95,10 @@ inline SavedLayout saved_layout(const moe_lora_dims* d) {
   L.U = take(2 * (size_t)P * d->I);
   L.Act = take(2 * (size_t)P * d->I);
   L.Z2w = take(2 * (size_t)T * d->r);
+  // native FP4 forward: the forward's routed down rows O [P,H] and the A2 shrink Z2
+  // [P,r] (bf16), from which the backward takes the router-weight gradient
+  L.O = take(fmt_native(d) ? 2 * (size_t)P * d->H : 0);
+  L.Z2 = take(fmt_native(d) ? 2 * (size_t)P * d->r : 0);
   const size_t wbytes = fmt_once(d) ? 2 * (size_t)d->E * d->I * d->H : 0;
   L.W1 = take(wbytes);
   L.W3 = take(wbytes);
@@ -106,6 +110,8 @@ inline SavedLayout saved_layout(const moe_lora_dims* d) {
 struct FwdLayout {
   size_t Y13, Xp, O, Z2, total;   // [T,2r], [P,H], [P,H], [P,r]  (bf16)
   size_t S13t;                    // native FP4 forward: W1/W3 scale bytes, tile-major (2 x E*I*H/32)
+  size_t S2t;                     //   W2's, tile-major (E*H*I/32)
+  size_t Actq, Acts;              //   the activation as MXFP8: codes [P,I], tile-major scale words
 };
 inline FwdLayout fwd_layout(const moe_lora_dims* d) {
   FwdLayout L;
@@ -117,6 +123,9 @@ inline FwdLayout fwd_layout(const moe_lora_dims* d) {
   L.O = take(2 * (size_t)P * d->H);
   L.Z2 = take(2 * (size_t)P * d->r);
   L.S13t = take(fmt_native(d) ? 2 * (size_t)d->E * d->I * (d->H / 32) : 0);
+  L.S2t = take(fmt_native(d) ? (size_t)d->E * d->H * (d->I / 32) : 0);
+  L.Actq = take(fmt_native(d) ? (size_t)P * d->I : 0);
+  L.Acts = take(fmt_native(d) ? (size_t)P * (d->I / 32) : 0);
   L.total = o;
   return L;
 }
@@ -229,6 +238,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+// ---------------------------------------------------------------- MXFP8 (native FP4 forward)
+// E4M3 code of v (already divided by the block scale): round to nearest even,
+// saturating at +-448 -- the conversion instruction's own rounding.  Two values per
+// instruction; `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 2^e as a float for e in [-127, 127] (2^-127 is subnormal)
+__device__ __forceinline__ float exp2i(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << 22);
+}
+// One MXFP8 block of 32 values (OCP MX: shared scale 2^X, X = floor(log2 max|v|) - 8,
+// X = 0 for an all-zero block, clamped to [-127, 127]): the 32 E4M3 codes and the
+// scale byte X + 127.
+__device__ __forceinline__ uint32_t mxfp8_block_f32(const float (&f)[32], uint4 (&codes)[2]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  int X = 0;
+  if (amax > 0.f) {
+    const uint32_t b = __float_as_uint(amax);
+    const int e = (int)(b >> 23);
+    const int fl = e ? e - 127 : (31 - __clz((int)b)) - 149;  // floor(log2 amax), subnormals too
+    X = min(max(fl - 8, -127), 127);
+  }
+  const float inv = exp2i(-X);  // exact scaling by a power of two
+  uint32_t q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    q[i] = e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) | (e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+  codes[0] = make_uint4(q[0], q[1], q[2], q[3]);
+  codes[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  return (uint32_t)(X + 127);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 

@@ -26,8 +26,10 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
   uint16_t* Z2w = (uint16_t*)(sv + SL.Z2w);
   uint16_t* Y13 = (uint16_t*)(sc + FL.Y13);
   uint16_t* Xp = (uint16_t*)(sc + FL.Xp);
-  uint16_t* O = (uint16_t*)(sc + FL.O);
-  uint16_t* Z2 = (uint16_t*)(sc + FL.Z2);
+  // native FP4 forward: O and Z2 are kept in `saved` (the backward's router-weight
+  // gradient reads them)
+  uint16_t* O = (uint16_t*)(fmt_native(d) ? sv + SL.O : sc + FL.O);
+  uint16_t* Z2 = (uint16_t*)(fmt_native(d) ? sv + SL.Z2 : sc + FL.Z2);
 
   const uint64_t T = (uint64_t)d->T, H = d->H, I = d->I, E = d->E, A = d->A, r = d->r;
   const uint64_t P = (uint64_t)rows_cap(d), G = A * E;
@@ -139,6 +141,8 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.G = Gs;
     p.U = Us;
     p.Act = Act;
+    p.Actq = reinterpret_cast<uint8_t*>(sc + FL.Actq);
+    p.Acts = reinterpret_cast<uint8_t*>(sc + FL.Acts);
     p.Xs = Xs;
     p.S1t = S1t;
     p.S3t = S3t;
@@ -171,7 +175,26 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W2));
     return 0;
   };
-  if (kW2OneSmWide || mx) {
+  if (nat) {
+    // W2's scale bytes in the tile-major layout, then the native down product
+    uint8_t* S2t = reinterpret_cast<uint8_t*>(sc + FL.S2t);
+    LAUNCH(launch_scales_to_tiles(w->S2, (int64_t)(E * H), d->I, S2t, num_sms, stream));
+    ProbW2Nv p;
+    MAP(tmap_2d_b8(&p.mActq, sc + FL.Actq, I, P, 128));
+    MAP(tmap_fp4_unpacked(&p.mW2f, w->W2, I, H, E, 256));
+    MAP(tmap_2d(&p.mAct, Act, I, P, 64, 128));
+    MAP(tmap_3d(&p.mA2, w->A2, I, r, G, 64, (uint32_t)((r + 15) / 16 * 16)));
+    p.Acts = reinterpret_cast<const uint8_t*>(sc + FL.Acts);
+    p.S2t = S2t;
+    p.pl = pl;
+    p.err = pl.err;
+    p.O = O;
+    p.Z2 = Z2;
+    p.H = d->H;
+    p.I = d->I;
+    p.r = d->r;
+    LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W2));
+  } else if (kW2OneSmWide || mx) {
     if ((rc = mx ? w2(ProbW2T<true>{}) : w2(ProbW2T<false>{}))) return rc;
   } else {
     ProbW2Pair p;

@@ -565,6 +565,8 @@ struct ProbW13Nv {
   PlanView pl;
   int* err;
   uint16_t *G, *U, *Act;  // [P,I] outputs
+  uint8_t *Actq, *Acts;   // the activation as MXFP8 for the native W2: codes [P,I], scale
+                          // words [P/128][I/128][32][4][4] (as launch_scales_to_tiles lays them)
   int H, I, r;
   int act;
   float clamp;
@@ -614,6 +616,8 @@ struct ProbW13Nv {
   }
   __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t*) const {
     const int64_t o = ((int64_t)ti.m0 + row) * I + ti.n0;  // this thread's row: 64-byte row segments
+    const int64_t p = (int64_t)ti.m0 + row;
+    uint8_t* sw = Acts + ((p >> 7) * (I / 128) + (ti.n0 >> 7)) * 512 + nv_word((int)(p & 127)) * 4;
     for (int c = c0; c < 128; c += cs) {
       float g[32], u[32], a[32];
       tmem_ld32(taddr + c, g);
@@ -622,6 +626,15 @@ struct ProbW13Nv {
       store_row_bf16(G + o + c, g);
       store_row_bf16(U + o + c, u);
       store_row_bf16(Act + o + c, a);
+      // q8 of the stored (bf16-rounded) activation: this thread's 32 columns are one
+      // MXFP8 block, byte c / 32 of the row's scale word for this 128-wide K step
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = __bfloat162float(__float2bfloat16_rn(a[i]));
+      uint4 q[2];
+      sw[c >> 5] = (uint8_t)mxfp8_block_f32(a, q);
+      uint4* dq = reinterpret_cast<uint4*>(Actq + o + c);
+      dq[0] = q[0];
+      dq[1] = q[1];
     }
   }
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
@@ -720,6 +733,82 @@ struct ProbW2T {
   __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
 };
 using ProbW2 = ProbW2T<false>;
+
+// Native FP4 forward F4/F5: the down base product on block-scaled FP4 tensor cores,
+//   O = q8(Act) W2_e^T   [P,H] (unweighted),   Z2 = bf16(Act A2_ae^T) [P,r]
+// with q8(Act) the activation as MXFP8 (written by ProbW13Nv's epilogue) and W2 in
+// MXFP4 as stored.  128-row tiles: H/256 native tiles over W2 rows (I/128 steps), then
+// one BF16 tile over A2 rows on the bf16 activation (the side shrink stays BF16).  H, I
+// multiples of 128; a last native tile with 128 valid rows reads zero codes past H.
+struct ProbW2Nv {
+  static constexpr bool kAmn = false, kBmn = false, kWide = false, kNative = true;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kNvLayout = kNvLayoutCopy;
+  const uint8_t* Acts;       // [P/128][I/128][512] scale words of Actq
+  const uint8_t* S2t;        // [E*H/128][I/128][512] scale words of W2 (launch_scales_to_tiles)
+  CUtensorMap mActq;         // Actq (I,P) bytes, box (128,128)
+  CUtensorMap mW2f;          // W2 E2M1 (I,H,E), box (128 codes, 256, 1)
+  CUtensorMap mAct, mA2;     // Act (I,P) box(64,128); A2 (I,r,G) box(64,r16,1)
+  PlanView pl;
+  int* err;
+  uint16_t *O, *Z2;
+  int H, I, r;
+  __device__ int ntn() const { return cdiv(H, 256) + 1; }
+  __device__ int num_tiles() const { return pl.offsets[pl.G] / 128 * ntn(); }
+  __device__ TileInfo tile(int t) const {
+    TileInfo ti;
+    const int nt = nmajor_narrow_decode(nmajor_narrow_fetch(pl, t, ntn()), t, ntn(), ti);
+    ti.sub = nt == cdiv(H, 256);
+    ti.n0 = ti.sub ? 0 : nt * 256;
+    ti.nk = ti.sub ? I / kBK : I / 128;
+    return ti;
+  }
+  __device__ void prefetch() const {
+    tma_prefetch_map(&mActq);
+    tma_prefetch_map(&mW2f);
+    tma_prefetch_map(&mAct);
+    tma_prefetch_map(&mA2);
+  }
+  __device__ void load(const TileInfo& ti, int ks, uint8_t* sa, uint8_t* sb, uint8_t* sf, uint64_t* bar) const {
+    if (!ti.sub) {
+      const int e = ti.g % pl.E;
+      const int64_t kt = I / 128, hb = H / 128;
+      const int64_t b0 = (int64_t)e * hb + (ti.n0 >> 7);
+      const int64_t b1 = (ti.n0 >> 7) + 1 < hb ? b0 + 1 : b0;  // past H: any valid block (codes there are 0)
+      mbar_arrive_expect_tx(bar, 128 * 128 + 256 * 64 + kNvSfBytes);  // E2M1 boxes count packed bytes
+      tma_load_2d(sa, &mActq, bar, ks * 128, ti.m0);
+      tma_load_3d(sb, &mW2f, bar, ks * 128, ti.n0, e);
+      bulk_load(sf, Acts + ((int64_t)(ti.m0 >> 7) * kt + ks) * 512, 512, bar);
+      bulk_load(sf + 512, S2t + (b0 * kt + ks) * 512, 512, bar);
+      bulk_load(sf + 1024, S2t + (b1 * kt + ks) * 512, 512, bar);
+    } else {
+      mbar_arrive_expect_tx(bar, kAStage128 + round16(r) * 128);
+      tma_load_2d(sa, &mAct, bar, ks * kBK, ti.m0);
+      tma_load_3d(sb, &mA2, bar, ks * kBK, 0, ti.g);
+    }
+  }
+  __device__ bool native_step(const TileInfo& ti, int) const { return !ti.sub; }
+  __device__ MmaStep mma_step(const TileInfo& ti, int ks) const {
+    return MmaStep{ti.sub ? round16(r) : 256, 0, 0, ks == 0};
+  }
+  __device__ void epilogue(const TileInfo& ti, int row, uint32_t taddr, int c0, int cs, uint32_t*) const {
+    const int64_t p = (int64_t)ti.m0 + row;
+    if (!ti.sub) {
+      for (int c = c0; c < 256 && ti.n0 + c < H; c += cs) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+        store_row_bf16(O + p * H + ti.n0 + c, v);
+      }
+    } else {
+      for (int c = c0; c < r; c += cs) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+        store_row_bf16(Z2 + p * r + c, v, 1.0f, r - c < 32 ? r - c : 32);
+      }
+    }
+  }
+  __device__ void epilogue_empty(const TileInfo&, int, int, int) const {}
+};
 
 // =====================================================================================
 // Forward F6 (first half) -- shared B2 expand, once per token:

@@ -57,6 +57,10 @@ cudaError_t launch_gather_fwd(const PlanView& pl, const uint16_t* x, const uint1
 cudaError_t launch_gather_fwd_mxfp8(const PlanView& pl, const uint16_t* x, const uint16_t* Y13, uint8_t* Xq,
                                     uint8_t* Xs, uint16_t* Y13p, int H, int r2, int num_sms, cudaStream_t stream);
 // Standalone MXFP8 quantiser (row-major scale bytes [rows, n/32]); n % 32 == 0.
+// Native FP4 forward's router-weight gradient from the saved O and Z2 rows:
+// dw[t,j] = <dy_t, O[row]> + s <dyB2_t, Z2[row]>  (0 for masked slots).
+cudaError_t launch_dw_from_o(const PlanView& pl, const uint16_t* dy, const uint16_t* dyB2, const uint16_t* O,
+                             const uint16_t* Z2, int H, int r, float s, float* dw, int num_sms, cudaStream_t stream);
 // Scale bytes [rows, K/32] -> tile-major [rows/128][K/128][128][4] (rows, K % 128 == 0).
 cudaError_t launch_scales_to_tiles(const uint8_t* S, int64_t rows, int K, uint8_t* St, int num_sms,
                                    cudaStream_t stream);

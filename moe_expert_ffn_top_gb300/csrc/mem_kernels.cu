@@ -80,21 +80,7 @@ __global__ void gather_fwd_kernel(PlanView pl, const uint16_t* __restrict__ x, c
 }
 
 // ---------------------------------------------------------------- MXFP8 routed rows
-// E4M3 code of v (already divided by the block scale): round to nearest even,
-// saturating at +-448 -- the conversion instruction's own rounding.  Two values per
-// instruction; `lo` lands in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-// 2^e as a float for e in [-127, 127] (2^-127 is subnormal)
-__device__ __forceinline__ float exp2i(int e) {
-  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << 22);
-}
-// One MXFP8 block of 32 bf16 (OCP MX: shared scale 2^X, X = floor(log2 max|v|) - 8,
-// X = 0 for an all-zero block, clamped to [-127, 127]): the 32 E4M3 codes and the
-// scale byte X + 127.
+// One MXFP8 block of 32 bf16 (four 16-byte words): mxfp8_block_f32 on their values.
 __device__ __forceinline__ uint32_t mxfp8_block(const uint4 (&v)[4], uint4 (&codes)[2]) {
   float f[32];
 #pragma unroll
@@ -106,24 +92,7 @@ __device__ __forceinline__ uint32_t mxfp8_block(const uint4 (&v)[4], uint4 (&cod
       f[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     }
   }
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  int X = 0;
-  if (amax > 0.f) {
-    const uint32_t b = __float_as_uint(amax);
-    const int e = (int)(b >> 23);
-    const int fl = e ? e - 127 : (31 - __clz((int)b)) - 149;  // floor(log2 amax), subnormals too
-    X = min(max(fl - 8, -127), 127);
-  }
-  const float inv = exp2i(-X);  // exact scaling by a power of two
-  uint32_t q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    q[i] = e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) | (e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
-  codes[0] = make_uint4(q[0], q[1], q[2], q[3]);
-  codes[1] = make_uint4(q[4], q[5], q[6], q[7]);
-  return (uint32_t)(X + 127);
+  return mxfp8_block_f32(f, codes);
 }
 
 // Forward routed rows for the native FP4 forward, by scatter like gather_fwd_kernel:
@@ -183,6 +152,43 @@ __global__ void gather_fwd_mxfp8_kernel(PlanView pl, const uint16_t* __restrict_
       for (int j = lane; j < ks_per_row; j += 32)
         *reinterpret_cast<uint32_t*>(Xs + ((p >> 7) * ks_per_row + j) * 512 + (4 * (p & 31) + ((p >> 5) & 3)) * 4) =
             0x7F7F7F7Fu;
+    }
+  }
+}
+
+// Router-weight gradient of the native FP4 forward, whose down base product ran on
+// q8(Act), so that <Q, a> no longer equals <dy, o>: from the forward's saved rows,
+//   dw[t,j] = <dy_t, O[row]> + s <dyB2_t, Z2[row]>   (fp32; 0 for a masked slot)
+// with row = row_of_route[t*k + j] (o = O + s B2 Z2, and dyB2 = dy B2).  One warp per
+// token; H % 256 == 0 is not needed (8 columns per lane and step, H % 8 == 0).
+__global__ void dw_from_o_kernel(PlanView pl, const uint16_t* __restrict__ dy, const uint16_t* __restrict__ dyB2,
+                                 const uint16_t* __restrict__ O, const uint16_t* __restrict__ Z2, int H, int r,
+                                 float s, float* __restrict__ dw) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int k = pl.k;
+  for (int64_t t = w0; t < pl.T; t += nw) {
+    for (int j = 0; j < k; ++j) {
+      const int R = pl.row_of_route[t * k + j];
+      float acc = 0.f;
+      if (R >= 0) {
+        for (int c = lane * 8; c < H; c += 256) {
+          const uint4 a = __ldg(reinterpret_cast<const uint4*>(dy + t * H + c));
+          const uint4 b = __ldg(reinterpret_cast<const uint4*>(O + (int64_t)R * H + c));
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            acc += bf16_lo(aw[q]) * bf16_lo(bw[q]) + bf16_hi(aw[q]) * bf16_hi(bw[q]);
+        }
+        float side = 0.f;
+        for (int q = lane; q < r; q += 32)
+          side += __uint_as_float((uint32_t)dyB2[t * r + q] << 16) * __uint_as_float((uint32_t)Z2[(int64_t)R * r + q] << 16);
+        acc += s * side;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) dw[t * k + j] = acc;
     }
   }
 }
@@ -531,6 +537,14 @@ cudaError_t launch_gather_fwd_mxfp8(const PlanView& pl, const uint16_t* x, const
   prof_begin(K_GATHER_FWD, stream);
   gather_fwd_mxfp8_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, x, Y13, Xq, Xs, Y13p, H, r2);
   prof_end(K_GATHER_FWD, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_from_o(const PlanView& pl, const uint16_t* dy, const uint16_t* dyB2, const uint16_t* O,
+                             const uint16_t* Z2, int H, int r, float s, float* dw, int num_sms, cudaStream_t stream) {
+  prof_begin(K_DW, stream);
+  dw_from_o_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, dy, dyB2, O, Z2, H, r, s, dw);
+  prof_end(K_DW, stream);
   return cudaGetLastError();
 }
 

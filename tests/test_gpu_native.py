@@ -9,8 +9,10 @@ Bars:
   * the block-scaled GEMM engine: float64 within fp32 accumulation (relL2 1e-6);
   * the layer against the oracle's native mode (the same MXFP8 activations, a
     straight-through backward): relL2 5e-3 and cosine 0.9999 as everywhere;
-  * the stated, looser gate against the BF16-activation layer: relL2 5e-2 on y
-    (E4M3 keeps 3 mantissa bits: a relative rounding error up to 2^-4 per element).
+  * the stated, looser gate against the BF16-activation layer: relL2 1e-1 on y.
+    Both forward base products take E4M3 inputs (3 mantissa bits: a relative rounding
+    error up to 2^-4 per element, ~0.03 RMS); two independent roundings give ~0.04,
+    which the gate's derivative can amplify by up to ~1.5.
 """
 import pytest
 import torch
@@ -151,14 +153,15 @@ def test_native_variants(A, act, clamp, T, H, I):
 
 def test_native_looser_gate_against_bf16_activations():
     """The stated gate of the native forward against the same layer with BF16
-    activations (the MXFP4 base decoded inside the GEMMs): relL2 <= 5e-2 on y, and the
-    two differ (the activations really are quantised)."""
+    activations (the MXFP4 base decoded inside the GEMMs): relL2 <= 1e-1 on y (two
+    E4M3 roundings, see the module docstring), and the two differ (the activations
+    really are quantised)."""
     shp = Shape(T=256, H=512, I=256, E=16, k=2, r=16, base_fmt="mxfp4_native")
     inp = make_inputs(shp, seed=63)
     nat = run_gpu(inp, shp, backward=False)
     ref = run_gpu(inp, Shape(**{**shp.__dict__, "base_fmt": "mxfp4"}), backward=False)
     d = rel_l2(nat["y"], ref["y"])
-    assert 1e-4 < d <= 5e-2, d
+    assert 1e-4 < d <= 1e-1, d
 
 
 @pytest.mark.parametrize("once", [False, True])

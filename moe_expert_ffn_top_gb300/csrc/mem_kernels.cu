@@ -161,6 +161,9 @@ __global__ void gather_fwd_mxfp8_kernel(PlanView pl, const uint16_t* __restrict_
 //   dw[t,j] = <dy_t, O[row]> + s <dyB2_t, Z2[row]>   (fp32; 0 for a masked slot)
 // with row = row_of_route[t*k + j] (o = O + s B2 Z2, and dyB2 = dy B2).  One warp per
 // token; H % 256 == 0 is not needed (8 columns per lane and step, H % 8 == 0).
+// Measured: 0.80 ms at 65,536 tokens (O and dy read at the copy rate); fusing it into
+// the dy gather, which holds each dy row in registers, took that kernel from 0.64 to
+// 3.31 ms (246 registers: one block per SM, the per-route reductions serialised).
 __global__ void dw_from_o_kernel(PlanView pl, const uint16_t* __restrict__ dy, const uint16_t* __restrict__ dyB2,
                                  const uint16_t* __restrict__ O, const uint16_t* __restrict__ Z2, int H, int r,
                                  float s, float* __restrict__ dw) {

@@ -68,7 +68,9 @@ def kernel_work(T, R, H, I, r, k, E=256):
     fl = {
         "shrink_x_A13": 2.0 * T * H * 2 * r,
         "w13_lora_swiglu": 4.0 * R * H * I + 4.0 * R * I * r,
+        "w13_native": 4.0 * R * H * I + 4.0 * R * I * r,
         "w2_a2": 2.0 * R * I * H + 2.0 * R * I * r,
+        "w2_native": 2.0 * R * I * H + 2.0 * R * I * r,
         "b2_expand": 2.0 * T * r * H,
         "dy_b2": 2.0 * T * H * r,
         "dB2": 2.0 * T * H * r,
@@ -84,6 +86,7 @@ def kernel_work(T, R, H, I, r, k, E=256):
         "z2_combine": 2.0 * (R * r + T * r),
         "gather_bwd": 2.0 * (T * H + R * H + 3 * R * r),
         "dw_reduce": 4.0 * (R * (I // 128) + T * k),
+        "dw_native": 2.0 * (R * H + R * H + R * r) + 4.0 * T * k,
         "dy13_combine": 4.0 * R * 2 * r + 2.0 * T * 2 * r,
         "dequant_mxfp4": (2.0 + 0.5 + 1.0 / 32) * E_I_H,
         "combine_y": 2.0 * (R * H + 2 * T * H),
@@ -337,8 +340,8 @@ def measure_workload(m, name, seed, args, local_rank, dist, world, mx_once=False
            "kernels_ms": {n: round(t / c, 4) for n, (t, c) in prof.items()},
            "workspace_gb": {w_: round(m.moe_lora_workspace_bytes(d, i_) / 1e9, 3)
                             for w_, i_ in (("plan", 0), ("saved", 1), ("fwd_scratch", 2), ("bwd_scratch", 3))}}
-    if shp.base_fmt == "mxfp4_native" and "w13_lora_swiglu" in prof:
-        t, c = prof["w13_lora_swiglu"]
+    if shp.base_fmt == "mxfp4_native" and "w13_native" in prof:
+        t, c = prof["w13_native"]
         kms = t / c
         f13 = 4.0 * R * H * I + 4.0 * R * I * r   # gate/up base products + the B1/B3 expand
         fp8 = 2.0 * pk["bf16"]                    # dense FP8 peak: measured BF16 x the nominal 4.5 / 2.25

@@ -153,7 +153,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.r = d->r;
     p.act = d->act;
     p.clamp = d->act_clamp;
-    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13));
+    LAUNCH(launch_gemm(p, max_row_tiles * (d->I / 128), num_sms, stream, K_W13_NV));
   } else if ((rc = mx ? w13(ProbW13T<true>{}) : w13(ProbW13T<false>{}))) {
     return rc;
   }
@@ -193,7 +193,7 @@ int run_forward(const moe_lora_dims* d, const void* plan_ws, const uint16_t* x, 
     p.H = d->H;
     p.I = d->I;
     p.r = d->r;
-    LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W2));
+    LAUNCH(launch_gemm(p, max_row_tiles * (cdiv(d->H, 256) + 1), num_sms, stream, K_W2_NV));
   } else if (kW2OneSmWide || mx) {
     if ((rc = mx ? w2(ProbW2T<true>{}) : w2(ProbW2T<false>{}))) return rc;
   } else {

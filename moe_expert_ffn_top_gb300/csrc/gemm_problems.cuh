@@ -525,6 +525,9 @@ struct ProbW13T {
 };
 using ProbW13 = ProbW13T<false>;
 
+// =====================================================================================
+// Native FP4 forward F3 (block-scaled MMAs; see ProbW13Nv below)
+// =====================================================================================
 // 32 consecutive values of one row as bf16 (64 bytes, 16-byte aligned) from registers.
 __device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float (&v)[32]) {
 #pragma unroll
@@ -734,6 +737,9 @@ struct ProbW2T {
 };
 using ProbW2 = ProbW2T<false>;
 
+// =====================================================================================
+// Native FP4 forward F4/F5
+// =====================================================================================
 // Native FP4 forward F4/F5: the down base product on block-scaled FP4 tensor cores,
 //   O = q8(Act) W2_e^T   [P,H] (unweighted),   Z2 = bf16(Act A2_ae^T) [P,r]
 // with q8(Act) the activation as MXFP8 (written by ProbW13Nv's epilogue) and W2 in

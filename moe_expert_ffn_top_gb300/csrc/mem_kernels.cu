@@ -545,9 +545,9 @@ cudaError_t launch_gather_fwd_mxfp8(const PlanView& pl, const uint16_t* x, const
 
 cudaError_t launch_dw_from_o(const PlanView& pl, const uint16_t* dy, const uint16_t* dyB2, const uint16_t* O,
                              const uint16_t* Z2, int H, int r, float s, float* dw, int num_sms, cudaStream_t stream) {
-  prof_begin(K_DW, stream);
+  prof_begin(K_DW_NV, stream);
   dw_from_o_kernel<<<grid_for(num_sms), kThreads, 0, stream>>>(pl, dy, dyB2, O, Z2, H, r, s, dw);
-  prof_end(K_DW, stream);
+  prof_end(K_DW_NV, stream);
   return cudaGetLastError();
 }
 

@@ -43,7 +43,7 @@ const char* prof_name(int slot) {
       "shrink_x_A13", "gather_fwd", "w13_lora_swiglu", "w2_a2", "z2_combine", "b2_expand", "combine_y",
       "dy_b2", "dB2", "gather_bwd", "w2_dgrad_swiglu_bwd", "dw_reduce", "dA2", "w13_dgrad_b13", "dB13",
       "dy13_combine", "a13_expand", "combine_dx", "dA13", "dequant_mxfp4", "split_reduce", "selftest_gemm",
-      "router_topk", "router_dlogits", "router_dx", "router_dWr"};
+      "router_topk", "router_dlogits", "router_dx", "router_dWr", "w13_native", "w2_native", "dw_native"};
   return (slot >= 0 && slot < K_NUM_SLOTS) ? names[slot] : "?";
 }
 

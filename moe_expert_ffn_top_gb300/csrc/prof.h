@@ -12,6 +12,7 @@ enum ProfSlot {
   K_DYB2, K_DB2, K_GATHER_BWD, K_W2_DGRAD, K_DW, K_DA2, K_W13_DGRAD, K_DB13, K_DY13W, K_A13_EXPAND, K_COMBINE_DX, K_DA13,
   K_DEQUANT, K_SPLIT_REDUCE, K_SELFTEST,
   K_ROUTER_FWD, K_ROUTER_DL, K_ROUTER_DX, K_ROUTER_DW,
+  K_W13_NV, K_W2_NV, K_DW_NV,  // native FP4 forward
   K_NUM_SLOTS
 };
 

@@ -175,3 +175,19 @@ def test_native_production_width_sampled(once):
     out = run_gpu(inp, shp, mx_once=once)
     assert out["err"] == 0
     _sampled_check(inp, shp, out, sample)
+
+
+@pytest.mark.parametrize("once", [False, True])
+def test_native_edge_production_width_sampled(once):
+    """The native forward on the pages' boundary sweep shape: production widths, a
+    fifth of the routes masked, experts 0/127/255 empty, an odd token count (1,029),
+    GeGLU with the production clamp 10; sampled sparse-dy parity against the oracle's
+    native mode, and the routed rows' padding never reaching an output."""
+    shp = Shape(T=1029, H=4096, I=2048, E=256, k=6, r=128, mask_frac=0.2, empty_experts=(0, 127, 255),
+                base_fmt="mxfp4_native", act="geglu", clamp=10.0)
+    inp = make_inputs(shp, seed=66, device="cuda")
+    sample = [0, 1, 514, 1028]
+    inp = _sparse_dy(inp, shp, sample)
+    out = run_gpu(inp, shp, poison=True, mx_once=once)
+    assert out["err"] == 0
+    _sampled_check(inp, shp, out, sample)

@@ -246,37 +246,6 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ timed regions
-def _compaction_counters():
-    """Sum of the host kernel's memory-compaction scan/migration counters, or None."""
-    try:
-        with open("/proc/vmstat") as f:
-            vals = dict(line.split() for line in f if line.startswith("compact_"))
-        keys = ("compact_migrate_scanned", "compact_free_scanned", "compact_isolated", "compact_stall")
-        return sum(int(vals.get(k, 0)) for k in keys)
-    except (OSError, ValueError):
-        return None
-
-
-def host_settle(max_s=60.0, quiet_s=1.0, poll_s=0.5):
-    """Wait (bounded) until the host's memory compaction has been idle for quiet_s:
-    right after a process that allocated and freed many GB of host memory (the test
-    suite's oracle sub-problems), single pinned copies stall for ~0.1 s while the
-    host compacts.  Returns {waited_s, settled} for the record."""
-    t0 = time.time()
-    last = _compaction_counters()
-    if last is None:
-        return {"waited_s": 0.0, "settled": None}
-    quiet_since = time.time()
-    while time.time() - t0 < max_s:
-        time.sleep(poll_s)
-        cur = _compaction_counters()
-        if cur != last:
-            last, quiet_since = cur, time.time()
-        elif time.time() - quiet_since >= quiet_s:
-            return {"waited_s": round(time.time() - t0, 2), "settled": True}
-    return {"waited_s": round(time.time() - t0, 2), "settled": False}
-
-
 def timed_region(fn, steps, stream, local_rank, dist, sample_clocks=True):
     """Runs fn() `steps` times between CUDA events on `stream` (barrier and
     synchronize on both sides), sampling the SM clocks meanwhile.  Returns
@@ -694,7 +663,6 @@ def run_ours(args, rank, world, local_rank):
             if timed:
                 copy_ev.append(ce)
 
-    settle = host_settle()  # before the leg: a host still compacting memory stalls pinned copies
     run_e2e(args.warmup)
     torch.cuda.synchronize()
     barrier()
@@ -721,7 +689,6 @@ def run_ours(args, rank, world, local_rank):
            "copy_ms": {"upload_median": round(med_up, 2), "upload_max": round(max(t_up), 2),
                        "readback_median": round(med_dn, 2), "readback_max": round(max(t_dn), 2),
                        "stalled_copies": stalls},
-           "host_settle": settle,
            "copies": "pinned host memory, own streams; dy uploaded during the forward and y read back "
                      "during the backward; overlapped with neighbouring steps' compute"}
 

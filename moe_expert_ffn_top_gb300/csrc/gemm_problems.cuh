@@ -427,11 +427,10 @@ struct ProbShrink {
 // fast silu that trade pays (same-box 9.33 -> 9.04 ms at 65,536 tokens, E256).
 constexpr bool kW13Wide = true;
 // MX: W1/W3 are MXFP4, decoded into the stage by the epilogue warps (no TMA for them).
-// W13's epilogue stores: 64-byte row segments straight from registers (true) or the
-// TMA-store ring (false).  Same box, two alternations, 65,536 tokens: W13 9.7-9.9 ms
-// with row stores against 8.7-8.9 ms with the ring (the native W13, without staging
+// W13's epilogue stores through the TMA-store ring.  Measured against 64-byte row
+// segments straight from registers (same box, two alternations, 65,536 tokens): W13
+// 8.7-8.9 ms with the ring, 9.7-9.9 ms with row stores (the native W13, without staging
 // buffers and with a fourth stage, prefers row stores).
-constexpr bool kW13RowStore = false;
 template <bool MX>
 struct ProbW13T {
   static constexpr bool kAmn = false, kBmn = false;
@@ -515,12 +514,7 @@ struct ProbW13T {
       tmem_ld32(taddr + c, g);
       tmem_ld32(taddr + 128 + c, u);
       act_fwd_chunk(act, clamp, g, u, a);
-      if (kW13RowStore) {
-        const int64_t o = ((int64_t)ti.m0 + row) * I + ti.n0 + c;  // this thread's row
-        store_row_bf16(G + o, g, 1.0f, 32);
-        store_row_bf16(U + o, u, 1.0f, 32);
-        store_row_bf16(Act + o, a, 1.0f, 32);
-      } else if (kEpiTmaStore) {
+      if (kEpiTmaStore) {
         out.store_bf16(&mG, ti.n0 + c, y0, g);
         out.store_bf16(&mU, ti.n0 + c, y0, u);
         out.store_bf16(&mAct, ti.n0 + c, y0, a);

@@ -86,14 +86,17 @@ extern "C" {
  * the base occupies only its packed bytes and scales (no bf16 copy anywhere);
  * 2: once per forward into the saved workspace (3 * E*I*H bf16 more), which the
  * backward reuses -- faster on GB300 today, since the in-GEMM decode is repeated
- * by every row tile of an expert.  base_fmt 3 or 4: the native FP4 forward -- the
- * gate/up base products run on block-scaled FP4 tensor cores (tcgen05 kind::mxf8f6f4)
- * with the routed rows of x quantised to MXFP8 (E4M3 codes, one UE8M0 scale per 32
- * along H; the rule of moe_lora_mxfp8_quantize) and the MXFP4 W1/W3 as stored, so
- * their results carry that quantisation ("FP8/FP4/FP8 forwards", PR #9, Fresh
- * validation); the side paths, the W2 forward and the backward (straight through
- * the quantisation) run as base_fmt 1 (3) or 2 (4).  H and I must be multiples of
- * 128 and W1/W3 32-byte aligned.
+ * by every row tile of an expert.  base_fmt 3 or 4: the native FP4 forward -- both
+ * base products of the forward run on block-scaled FP4 tensor cores (tcgen05
+ * kind::mxf8f6f4) with their activations quantised to MXFP8 (E4M3 codes, one UE8M0
+ * scale per 32 consecutive values; the rule of moe_lora_mxfp8_quantize): the routed
+ * rows of x against the MXFP4 W1/W3 as stored, the bf16 activation against the MXFP4
+ * W2, so their results carry that quantisation ("FP8/FP4/FP8 forwards", PR #9, Fresh
+ * validation).  The side paths stay bf16; the backward (straight through the
+ * quantisation) runs as base_fmt 1 (3) or 2 (4), and the router-weight gradient is
+ * taken from the forward's routed down rows, which these modes keep in `saved`
+ * (3.5 GB more at 65,536 tokens, H4096).  H and I must be multiples of 128 and
+ * W1/W3/W2 32-byte aligned.
  * T may be 0 (every call is a no-op). */
 typedef struct moe_lora_dims {
   int64_t T;        /* tokens */

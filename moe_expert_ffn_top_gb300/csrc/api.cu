@@ -131,8 +131,9 @@ static int check_weights(const moe_lora_dims* d, const moe_lora_weights* w) {
       if (rc) return rc;
     }
   }
-  // the native forward's FP4 tensor maps read W1/W3 with 32-byte alignment
-  if (fmt_native(d) && ((reinterpret_cast<uintptr_t>(w->W1) | reinterpret_cast<uintptr_t>(w->W3)) & 31u))
+  // the native forward's FP4 tensor maps read W1/W3/W2 with 32-byte alignment
+  if (fmt_native(d) && ((reinterpret_cast<uintptr_t>(w->W1) | reinterpret_cast<uintptr_t>(w->W3) |
+                         reinterpret_cast<uintptr_t>(w->W2)) & 31u))
     return MOE_LORA_ERR_ALIGN;
   return MOE_LORA_OK;
 }

@@ -65,6 +65,8 @@ def _call_forward(L, d, **over):
                 scratch_bytes=1 << 40)
     args.update(over)
     W = m.Weights(*([over.get("weight", FAKE)] * 9 + [over.get("scales")] * 3))
+    if "w2" in over:
+        W.W2 = over["w2"]
     return L.moe_lora_forward(ctypes.byref(d), args["plan"], args["x"], args["w"], ctypes.byref(W), args["y"],
                               args["saved"], args["saved_bytes"], args["scratch"], args["scratch_bytes"], None)
 
@@ -80,6 +82,8 @@ def test_forward_rejections(L):
     assert _call_forward(L, m.Dims(256, 512, 320, 16, 2, 16, 1, 128, 1.0, 0, 3)) == -2   # native: I % 128
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 3), weight=FAKE + 16,
                          scales=FAKE) == -3                                            # native: W1/W3 32 B
+    assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 4), scales=FAKE,
+                         w2=FAKE + 16) == -3                                           # native: W2 32 B
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 128, 1.0, 0, 1)) == -1   # MXFP4 without scales
     assert _call_forward(L, m.Dims(256, 512, 256, 16, 2, 16, 1, 64, 1.0, 0, 0)) == -2    # block_m != 128
     assert _call_forward(L, d, plan=None) == -1

@@ -120,8 +120,9 @@ inline FwdLayout fwd_layout(const moe_lora_dims* d) {
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.Y13 = take(2 * (size_t)T * 2 * d->r);
   L.Xp = take(2 * (size_t)P * d->H);
-  L.O = take(2 * (size_t)P * d->H);
-  L.Z2 = take(2 * (size_t)P * d->r);
+  // (native FP4 forward: O and Z2 live in `saved` instead)
+  L.O = take(fmt_native(d) ? 0 : 2 * (size_t)P * d->H);
+  L.Z2 = take(fmt_native(d) ? 0 : 2 * (size_t)P * d->r);
   L.S13t = take(fmt_native(d) ? 2 * (size_t)d->E * d->I * (d->H / 32) : 0);
   L.S2t = take(fmt_native(d) ? (size_t)d->E * d->H * (d->I / 32) : 0);
   L.Actq = take(fmt_native(d) ? (size_t)P * d->I : 0);

@@ -430,7 +430,10 @@ constexpr bool kW13Wide = true;
 // W13's epilogue stores through the TMA-store ring.  Measured against 64-byte row
 // segments straight from registers (same box, two alternations, 65,536 tokens): W13
 // 8.7-8.9 ms with the ring, 9.7-9.9 ms with row stores (the native W13, without staging
-// buffers and with a fourth stage, prefers row stores).
+// buffers and with a fourth stage, prefers row stores).  Handing the accumulator back
+// to the MMA right after the last tensor-memory read of a tile (before the last chunk's
+// activation and stores) was measured too: 8.58-8.59 ms against 8.55-8.57 ms, no gain,
+// since the next tile's loads and MMAs already overlap the epilogue of the other buffer.
 template <bool MX>
 struct ProbW13T {
   static constexpr bool kAmn = false, kBmn = false;
@@ -1024,7 +1027,11 @@ struct ProbW2DgradT {
   static constexpr bool kMxMN = true;
   const uint8_t* S2q;  // MX: scales [E,H,I/32]
   CUtensorMap mW2q;    // MX: packed [E,H,I/2] bytes, box (128, 64, 1)
-  // 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
+  // On the two-SM engine (each CTA copying its 128 rows of dY and its 128 of the tile's
+// 256 I columns with one 4D copy: 32 KB per SM per 64-wide K step instead of 48 KB)
+// this GEMM measured 5.23-5.25 ms against 4.86-4.88 ms here (65,536 tokens, E256, same
+// box, two alternations), so the one-SM form stays.
+// 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
   // loads in flight leave the operand copies more of the memory system (same box:
   // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256); 256-row tiles need 8
   static constexpr int kEpiWarps = kWide ? 8 : 4;

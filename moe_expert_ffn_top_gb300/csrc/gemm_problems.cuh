@@ -1028,10 +1028,10 @@ struct ProbW2DgradT {
   const uint8_t* S2q;  // MX: scales [E,H,I/32]
   CUtensorMap mW2q;    // MX: packed [E,H,I/2] bytes, box (128, 64, 1)
   // On the two-SM engine (each CTA copying its 128 rows of dY and its 128 of the tile's
-// 256 I columns with one 4D copy: 32 KB per SM per 64-wide K step instead of 48 KB)
-// this GEMM measured 5.23-5.25 ms against 4.86-4.88 ms here (65,536 tokens, E256, same
-// box, two alternations), so the one-SM form stays.
-// 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
+  // 256 I columns with one 4D copy: 32 KB per SM per 64-wide K step instead of 48 KB)
+  // this GEMM measured 5.23-5.25 ms against 4.86-4.88 ms here (65,536 tokens, E256,
+  // same box, two alternations), so the one-SM form stays.
+  // 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
   // loads in flight leave the operand copies more of the memory system (same box:
   // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256); 256-row tiles need 8
   static constexpr int kEpiWarps = kWide ? 8 : 4;

@@ -1032,8 +1032,9 @@ struct ProbW2DgradT {
   // this GEMM measured 5.23-5.25 ms against 4.86-4.88 ms here (65,536 tokens, E256,
   // same box, two alternations), and 5.58-5.64 against 5.02 with 8 epilogue warps per
   // CTA, so the one-SM form stays.  The same two-SM engine runs a plain 8192^3 GEMM
-  // faster than the one-SM 128-row form (1,733-1,758 vs 1,513-1,523 TFLOP/s), so what
-  // costs here is this problem's epilogue traffic, not the engine.
+  // faster than the one-SM 128-row form (1,733-1,758 vs 1,513-1,523 TFLOP/s): the loss
+  // comes with this problem (its epilogue's DRAM loads and stores, its grouped tiles),
+  // not with the engine; which of them was not isolated.
   // 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
   // loads in flight leave the operand copies more of the memory system (same box:
   // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256); 256-row tiles need 8

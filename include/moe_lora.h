@@ -319,9 +319,10 @@ MOE_LORA_API int moe_lora_gemm_selftest(int32_t M, int32_t N, int32_t K, const u
                            int32_t b_mn, float* C, void* stream);
 /* The same plain GEMM on the two-SM engine (the forward W2 expert GEMM's alternative
  * form): clusters of two CTAs sharing each 256-row tile through
- * tcgen05.mma.cta_group::2 (an odd last
- * 128-row tile runs on one CTA of the pair).  Same arguments, rules and error
- * reporting as moe_lora_gemm_selftest. */
+ * tcgen05.mma.cta_group::2 (an odd last 128-row tile runs on one CTA of the pair).
+ * An MN-major B with N a multiple of 256 is copied as 8-row groups of each CTA's two
+ * 64-column chunks; other shapes as whole 64-column chunks.  Same arguments, rules and
+ * error reporting as moe_lora_gemm_selftest. */
 MOE_LORA_API int moe_lora_gemm_pair_selftest(int32_t M, int32_t N, int32_t K, const uint16_t* A, int32_t a_mn,
                                              const uint16_t* B, int32_t b_mn, float* C, void* stream);
 /* Error-path self-test of the bounded pipeline waits: the same plain GEMM (pair = 0:

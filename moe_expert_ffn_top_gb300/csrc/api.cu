@@ -75,6 +75,13 @@ int tmap_mn4(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
   return encode(m, base, 4, dims, strides, box);
 }
 
+int tmap_mn_k8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t d2, uint32_t chunks) {
+  const cuuint64_t dims[5] = {64, 8, cols / 64, rows / 8, d2};
+  const cuuint64_t strides[4] = {cols * 2, 128, cols * 16, rows * cols * 2};
+  const cuuint32_t box[5] = {64, 8, chunks, 8, 1};
+  return encode(m, base, 5, dims, strides, box);
+}
+
 int tmap_2d_b8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   const cuuint64_t dims[2] = {inner, outer > 0 ? outer : 1};
   const cuuint64_t strides[1] = {inner};

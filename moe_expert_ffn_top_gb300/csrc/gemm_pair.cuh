@@ -49,6 +49,15 @@ constexpr int kPairStage = kPairAStage + kPairBStage;
 constexpr int kPairStages = 6;
 static_assert(kPairStages * kPairStage <= 192 * 1024, "pair pipeline exceeds shared memory budget");
 
+// P::kBmnCompact: an MN-major B half sits as 8-K-row groups of its two 64-column chunks
+// (chunk stride 1 KB, group stride 2 KB) instead of whole chunks 8 KB apart.  With whole
+// chunks the pair MMA reads MN-major B slowly (plain 8192^3 GEMM: 1,197-1,529 against
+// 1,644-1,706 TFLOP/s K-major); with the groups at the K-major rate (1,627-1,678).
+template <class P, class = void>
+struct BmnCompactOf : std::false_type {};
+template <class P>
+struct BmnCompactOf<P, std::void_t<decltype(P::kBmnCompact)>> : std::integral_constant<bool, P::kBmnCompact> {};
+
 template <class P>
 __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(const __grid_constant__ P p) {
   static_assert(P::kEpiWarps == 4 || P::kEpiWarps == 8, "4 or 8 epilogue warps");
@@ -157,7 +166,9 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1) gemm_pair_kernel(co
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = P::kAmn ? sw128_desc(sa + kk * 2048, 8192, 1024) : sw128_desc(sa + kk * 32, 16, 1024);
-            const uint64_t bd = P::kBmn ? sw128_desc(sb + kk * 2048, 8192, 1024) : sw128_desc(sb + kk * 32, 16, 1024);
+            const uint64_t bd = BmnCompactOf<P>::value ? sw128_desc(sb + kk * 4096, 1024, 2048)
+                                : P::kBmn              ? sw128_desc(sb + kk * 2048, 8192, 1024)
+                                                       : sw128_desc(sb + kk * 32, 16, 1024);
             mma_bf16_pair(d + (uint32_t)st.col, ad, bd, idesc, (st.first && kk == 0) ? 0u : 1u);
           }
           mma_commit_pair_both(&empty[s]);

@@ -1031,10 +1031,12 @@ struct ProbW2DgradT {
   // 256 I columns with one 4D copy: 32 KB per SM per 64-wide K step instead of 48 KB)
   // this GEMM measured 5.23-5.25 ms against 4.86-4.88 ms here (65,536 tokens, E256,
   // same box, two alternations), and 5.58-5.64 against 5.02 with 8 epilogue warps per
-  // CTA, so the one-SM form stays.  The same two-SM engine runs a plain 8192^3 GEMM
-  // faster than the one-SM 128-row form (1,733-1,758 vs 1,513-1,523 TFLOP/s): the loss
-  // comes with this problem (its epilogue's DRAM loads and stores, its grouped tiles),
-  // not with the engine; which of them was not isolated.
+  // CTA, and 5.23-5.26 against 4.84-4.85 with W2 copied as 8-row groups of chunk pairs
+  // (the layout that brings the two-SM engine's plain GEMM with MN-major B from
+  // 1,197-1,529 to 1,627-1,678 TFLOP/s), so the one-SM form stays.  That engine runs a
+  // plain 8192^3 GEMM faster than the one-SM 128-row form (1,627-1,715 vs 1,430-1,517
+  // TFLOP/s): the loss comes with this problem (its epilogue's DRAM loads and stores, its
+  // grouped tiles), not with the engine; which of them was not isolated.
   // 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
   // loads in flight leave the operand copies more of the memory system (same box:
   // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256); 256-row tiles need 8
@@ -1688,9 +1690,13 @@ struct ProbPlainNv {
 // Plain GEMM on the two-SM engine (self-test): 256-row tiles, the MMA N (tn rounded
 // up to 32) split in halves.  M % 128 == 0 (an odd last 128-row tile runs on the
 // rank-0 CTA alone).
-template <bool AMN, bool BMN>
+// CB (MN-major B, N % 256 == 0): each CTA's B half copied as 8-K-row groups of its two
+// 64-column chunks (tmap_mn_k8), the layout the two-SM MMA reads at full rate.
+template <bool AMN, bool BMN, bool CB = false>
 struct ProbPlainPair : ProbPlain<AMN, BMN> {
   using Base = ProbPlain<AMN, BMN>;
+  static constexpr bool kBmnCompact = BMN && CB;
+  CUtensorMap mB5;  // kBmnCompact: B [K,N] (tmap_mn_k8, two chunks)
   // B maps: K-major box(64, tn/2); MN-major box(64,64) as in the one-SM form.
   __device__ int num_tiles() const { return (this->M + 255) / 256 * this->ntn(); }
   static constexpr bool kIssuerNeedsTile = false;
@@ -1724,7 +1730,9 @@ struct ProbPlainPair : ProbPlain<AMN, BMN> {
         tma_load_2d_pair(sa, &this->mA, bar, kt, mrow);
       }
     }
-    if (BMN) {
+    if (kBmnCompact) {
+      tma_load_5d_pair(sb, &mB5, bar, 0, 0, nc / 64, kt / 8, 0);
+    } else if (BMN) {
       for (int c = 0; c < nbox(); ++c) tma_load_2d_pair(sb + c * 8192, &this->mB, bar, nc + c * 64, kt);
     } else {
       tma_load_2d_pair(sb, &this->mB, bar, kt, nc);

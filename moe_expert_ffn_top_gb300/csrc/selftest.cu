@@ -23,26 +23,35 @@ static int plain_maps(Prob& p, int M, int N, int K, const uint16_t* A, const uin
   return MOE_LORA_OK;
 }
 
+template <bool AMN, bool BMN, bool CB>
+static int plain_pair(int M, int N, int K, const uint16_t* A, const uint16_t* B, float* C, int* err, int num_sms,
+                      int starve, cudaStream_t stream) {
+  using Prob = ProbPlainPair<AMN, BMN, CB>;
+  const uint32_t tn = N < 256 ? (uint32_t)N : 256u;
+  Prob p;
+  int rc;
+  if ((rc = plain_maps<Prob, AMN, BMN>(p, M, N, K, A, B, ((tn + 31) & ~31u) / 2))) return rc;
+  if (Prob::kBmnCompact && tmap_mn_k8(&p.mB5, B, (uint64_t)N, (uint64_t)K, 1, 2)) return MOE_LORA_ERR_CUDA;
+  p.err = err;
+  p.C = C;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.starve = starve;
+  return launch_gemm_pair(p, (M + 255) / 256 * ((N + 255) / 256), num_sms, stream, K_SELFTEST) == cudaSuccess
+             ? MOE_LORA_OK
+             : MOE_LORA_ERR_CUDA;
+}
+
 template <bool AMN, bool BMN>
 static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, float* C, int* err, int num_sms,
                  bool pair, int starve, cudaStream_t stream) {
+  if (pair)  // MN-major B in whole 256-column tiles: the chunk-pair layout
+    return BMN && N % 256 == 0 ? plain_pair<AMN, BMN, true>(M, N, K, A, B, C, err, num_sms, starve, stream)
+                               : plain_pair<AMN, BMN, false>(M, N, K, A, B, C, err, num_sms, starve, stream);
   const uint32_t tn = N < 256 ? (uint32_t)N : 256u;
-  const int ntn = (N + 255) / 256;
-  int rc;
-  if (pair) {
-    ProbPlainPair<AMN, BMN> p;
-    if ((rc = plain_maps<ProbPlainPair<AMN, BMN>, AMN, BMN>(p, M, N, K, A, B, ((tn + 31) & ~31u) / 2))) return rc;
-    p.err = err;
-    p.C = C;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.starve = starve;
-    return launch_gemm_pair(p, (M + 255) / 256 * ntn, num_sms, stream, K_SELFTEST) == cudaSuccess
-               ? MOE_LORA_OK
-               : MOE_LORA_ERR_CUDA;
-  }
   ProbPlain<AMN, BMN> p;
+  int rc;
   if ((rc = plain_maps<ProbPlain<AMN, BMN>, AMN, BMN>(p, M, N, K, A, B, tn))) return rc;
   p.err = err;
   p.C = C;
@@ -50,8 +59,9 @@ static int plain(int M, int N, int K, const uint16_t* A, const uint16_t* B, floa
   p.N = N;
   p.K = K;
   p.starve = starve;
-  return launch_gemm(p, M / 128 * ntn, num_sms, stream, K_SELFTEST) == cudaSuccess ? MOE_LORA_OK
-                                                                                  : MOE_LORA_ERR_CUDA;
+  return launch_gemm(p, M / 128 * ((N + 255) / 256), num_sms, stream, K_SELFTEST) == cudaSuccess
+             ? MOE_LORA_OK
+             : MOE_LORA_ERR_CUDA;
 }
 
 int run_plain_gemm(int M, int N, int K, const uint16_t* A, int a_mn, const uint16_t* B, int b_mn, float* C,

@@ -25,6 +25,11 @@ int tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
 // {64, 64, 4, 1}: one copy lands four MN-major 64 x 64 tiles of columns c0 .. c0+255,
 // 8 KB apart, exactly as four 2D boxes would (chunks past the last column read zeros).
 int tmap_mn4(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t d2);
+// bf16 tensor [d2][rows][cols] (cols % 64 == 0, rows % 8 == 0) seen as {64 columns,
+// 8 rows, cols/64 chunks, rows/8 groups, d2}; a box of {64, 8, chunks, 8, 1} lands 64
+// rows x 64 chunks columns MN-major as 8-row groups (2 KB for two chunks) of 1 KB
+// chunk atoms.
+int tmap_mn_k8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t d2, uint32_t chunks);
 // 2D byte tensor [outer][inner] (E4M3 codes) with the 128-byte swizzle: a box of
 // 128 x box_outer lands as box_outer rows of 128 bytes.
 int tmap_2d_b8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer);

@@ -1036,7 +1036,10 @@ struct ProbW2DgradT {
   // 1,197-1,529 to 1,627-1,678 TFLOP/s), so the one-SM form stays.  That engine runs a
   // plain 8192^3 GEMM faster than the one-SM 128-row form (1,627-1,715 vs 1,430-1,517
   // TFLOP/s): the loss comes with this problem (its epilogue's DRAM loads and stores, its
-  // grouped tiles), not with the engine; which of them was not isolated.
+  // grouped tiles), not with the engine; which of them was not isolated.  Clusters of
+  // two CTAs on neighbouring row tiles, each copying half of the shared W2 tile and
+  // multicasting it to both (a third fewer L2 reads), measured 5.08-5.10 against
+  // 4.95-4.97 ms: the shared L2 reads are not what holds it.
   // 4 epilogue warps: with the fast silu they keep up with the main loop, and fewer
   // loads in flight leave the operand copies more of the memory system (same box:
   // 5.22 vs 5.36 ms with 8 warps, 65,536 tokens, E256); 256-row tiles need 8

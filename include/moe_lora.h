@@ -335,7 +335,7 @@ MOE_LORA_API int moe_lora_gemm_starved_selftest(int32_t M, int32_t N, int32_t K,
                                                 const uint16_t* B, int32_t b_mn, float* C, int32_t pair,
                                                 void* stream);
 /* Self-test of the block-scaled FP4 tensor-core path (kind::mxf8f6f4) that the
- * native FP4 forward (base_fmt 3) runs its gate/up base products on:
+ * native FP4 forward (base_fmt 3 and 4) runs its gate/up and down base products on:
  *   C[M,N] (fp32) = sum_k (Aq[m,k] 2^(As[m,k/32]-127)) (Bq[n,k] 2^(Bs[n,k/32]-127))
  * Aq [M,K]: E4M3 codes, one per byte.  Bq [N,K/2]: E2M1 codes, two per byte, the low
  * nibble holding the lower k; 32-byte aligned.  As, Bs: the UE8M0 scale bytes of A

@@ -32,6 +32,15 @@ def test_kernel_flops_sum_to_the_step(bench, T, R, H, I, r, k, E):
     assert step == pytest.approx(bench.step_flops(T, R, H, I, r), rel=1e-12)
 
 
+def test_dominant_kernel_is_one_the_configuration_launches(bench):
+    """The roofline's kernel is W13 (tied with the W13 dgrad, the forward first): the
+    BF16/MXFP4 W13 GEMM, or the native one when the forward's base products run on FP4
+    tensor cores (that configuration never launches w13_lora_swiglu)."""
+    fl, _ = bench.kernel_work(65536, 393216, 4096, 2048, 128, 6, 256)
+    assert bench.dominant_kernel(fl, native=False) == "w13_lora_swiglu"
+    assert bench.dominant_kernel(fl, native=True) == "w13_native"
+
+
 def test_production_step_flops(bench):
     """42.06 TFLOP at 65,536 tokens, H4096 I2048, top-6, rank 128 (every route live)."""
     assert bench.step_flops(65536, 393216, 4096, 2048, 128) / 1e12 == pytest.approx(42.056, abs=1e-3)
